@@ -1,0 +1,263 @@
+"""CPU oracle for the Q4 dequant-in-GEMV family (f64, plain C behind ctypes).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  The CUDA
+library never calls it and shares no code with it.
+
+Every function here takes the weights in their *host* storage format (the
+bytes before any device repack) and computes in IEEE double precision:
+
+* ``q4_0``:  blocks ``uint8[n, k/32, 18]`` -- fp16 scale ``d`` (little
+  endian) then 16 nibble bytes; element ``i`` of a block is the low nibble of
+  byte ``i`` and element ``i+16`` its high nibble; ``w = d*(q-8)``
+  (crate inferencelayer, Functions: q4_0_to_q8_0n, gemv_q1_k_lcpp_src).
+* ``affine``: nibbles ``uint8[n, k/2]`` (element ``2i`` low nibble of byte
+  ``i``, ``2i+1`` high nibble), ``s`` and ``m`` as bf16 bits
+  ``uint16[n, k/32]``; ``w = s*q + m`` (Module gpu, Structs Q and HalfSet).
+
+The composed calls below mirror the library's C entry points one for one;
+each is the plain definition written out (decode, sequential dot, then the
+fused neighbour), with the passage it follows named in its docstring.
+
+Parity note: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, exhaustive decodes, exact rationals, invariants, brute force).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q4_oracle.c")
+_LIB = os.path.join(_HERE, "libq4oracle.so")
+
+FMT_Q4_0 = 0
+FMT_AFFINE = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler (no fused multiply-add)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+             "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The compiled oracle.  ``Q4_ORACLE_LIB`` may name another build of the
+    same source (the mutant tests use it to plant mistakes on the CPU)."""
+    global _lib
+    if _lib is None:
+        path = os.environ.get("Q4_ORACLE_LIB")
+        if not path:
+            path = build()
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        L.q4o_half.restype = ctypes.c_double
+        L.q4o_half.argtypes = [ctypes.c_uint16]
+        L.q4o_bf16.restype = ctypes.c_double
+        L.q4o_bf16.argtypes = [ctypes.c_uint16]
+        L.q4o_q4_0_row.argtypes = [P, I64, I64, P]
+        L.q4o_affine_row.argtypes = [P, P, P, I64, I64, P]
+        L.q4o_gemv.argtypes = [ctypes.c_int, P, P, P, I64, I64, P, I64, P, P, P]
+        L.q4o_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double, P]
+        L.q4o_silu.restype = ctypes.c_double
+        L.q4o_silu.argtypes = [ctypes.c_double]
+        L.q4o_swiglu.argtypes = [P, P, I64, P]
+        L.q4o_add.argtypes = [P, P, I64, P]
+        L.q4o_argmax.restype = I64
+        L.q4o_argmax.argtypes = [P, I64]
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+@dataclass
+class HostWeight:
+    """A quantised weight matrix in its host storage format (see module doc)."""
+    fmt: int
+    n: int
+    k: int
+    a: np.ndarray                   # q4_0: blocks; affine: nibbles
+    s: np.ndarray | None = None     # affine: bf16 scale bits
+    m: np.ndarray | None = None     # affine: bf16 min bits
+
+    def __post_init__(self):
+        assert self.k % 32 == 0 and self.n >= 1
+        self.a = np.ascontiguousarray(self.a, dtype=np.uint8)
+        if self.fmt == FMT_Q4_0:
+            assert self.a.size == self.n * (self.k // 32) * 18
+        else:
+            assert self.a.size == self.n * self.k // 2
+            self.s = np.ascontiguousarray(self.s, dtype=np.uint16)
+            self.m = np.ascontiguousarray(self.m, dtype=np.uint16)
+            assert self.s.size == self.m.size == self.n * self.k // 32
+
+    @staticmethod
+    def q4_0(blocks: np.ndarray, n: int, k: int) -> "HostWeight":
+        return HostWeight(FMT_Q4_0, n, k, blocks)
+
+    @staticmethod
+    def affine(nib: np.ndarray, s: np.ndarray, m: np.ndarray, n: int, k: int) -> "HostWeight":
+        return HostWeight(FMT_AFFINE, n, k, nib, s, m)
+
+
+# ---------------------------------------------------------------- primitives
+
+def half_to_f64(bits: int) -> float:
+    """IEEE binary16 bits -> value."""
+    return lib().q4o_half(int(bits) & 0xFFFF)
+
+
+def bf16_to_f64(bits: int) -> float:
+    """bfloat16 bits -> value."""
+    return lib().q4o_bf16(int(bits) & 0xFFFF)
+
+
+def dequant_row(W: HostWeight, row: int) -> np.ndarray:
+    """Row ``row`` of W as f64 weights (the format's value formula)."""
+    out = np.empty(W.k, dtype=np.float64)
+    if W.fmt == FMT_Q4_0:
+        lib().q4o_q4_0_row(_p(W.a), W.k, row, _p(out))
+    else:
+        lib().q4o_affine_row(_p(W.a), _p(W.s), _p(W.m), W.k, row, _p(out))
+    return out
+
+
+def dequant(W: HostWeight) -> np.ndarray:
+    """All of W as f64 ``[n, k]`` (small matrices only)."""
+    return np.stack([dequant_row(W, i) for i in range(W.n)])
+
+
+def gemv(W: HostWeight, x) -> tuple[np.ndarray, np.ndarray]:
+    """``y[r, i] = sum_k w[i, k] x[r, k]`` and the tolerance scale
+    ``S[r, i] = sum_k |w[i, k]| |x[r, k]|``, both f64 ``[nb, n]``.
+
+    x is ``[nb, k]`` (any float dtype; fp32 inputs convert exactly)."""
+    x = _f64(x)
+    if x.ndim == 1:
+        x = x[None, :]
+    nb, k = x.shape
+    assert k == W.k
+    y = np.empty((nb, W.n), dtype=np.float64)
+    S = np.empty((nb, W.n), dtype=np.float64)
+    wrow = np.empty(W.k, dtype=np.float64)
+    b = W.s if W.s is not None else W.a
+    c = W.m if W.m is not None else W.a
+    lib().q4o_gemv(W.fmt, _p(W.a), _p(b), _p(c), W.n, W.k, _p(x), nb, _p(y), _p(S), _p(wrow))
+    return y, S
+
+
+def rmsnorm(x, gamma, eps: float) -> np.ndarray:
+    """``xhat = x / sqrt(mean(x^2) + eps) * gamma`` per row (honeycrisp/mod.rs,
+    Op::RmsNorm: eps and width d = len(gamma) are its parameters)."""
+    x = _f64(x)
+    if x.ndim == 1:
+        x = x[None, :]
+    g = _f64(gamma)
+    nb, k = x.shape
+    assert g.shape == (k,)
+    out = np.empty_like(x)
+    lib().q4o_rmsnorm(_p(x), _p(g), nb, k, float(eps), _p(out))
+    return out
+
+
+def silu(t: float) -> float:
+    return lib().q4o_silu(float(t))
+
+
+def swiglu(g, u) -> np.ndarray:
+    """``h = silu(g) * u`` elementwise (honeycrisp/mod.rs, fused_ffn_residual step 4)."""
+    g = _f64(g)
+    u = _f64(u)
+    assert g.shape == u.shape
+    h = np.empty_like(g)
+    lib().q4o_swiglu(_p(g), _p(u), g.size, _p(h))
+    return h
+
+
+def add(a, b) -> np.ndarray:
+    a = _f64(a)
+    b = _f64(b)
+    assert a.shape == b.shape
+    out = np.empty_like(a)
+    lib().q4o_add(_p(a), _p(b), a.size, _p(out))
+    return out
+
+
+def argmax(v) -> int:
+    """Index of the maximum of a 1-D vector, lowest index on ties."""
+    v = _f64(v).ravel()
+    return int(lib().q4o_argmax(_p(v), v.size))
+
+
+# ------------------------------------------------------------ composed calls
+# One per library entry point; the fused steps are applied in the order the
+# pages' fused kernels apply them.
+
+def q4_gemv(W: HostWeight, x):
+    """Plain dequant-in-GEMV: returns (y, S)."""
+    return gemv(W, x)
+
+
+def q4_nrm_gemv(W: HostWeight, x, gamma, eps):
+    """RMSNorm prologue then GEMV (honeycrisp/mod.rs, forward_decode_fused_layers
+    step "1+2 Q matmul with inline input_norm").  Returns (y, S) with S taken
+    over the normed activations."""
+    return gemv(W, rmsnorm(x, gamma, eps))
+
+
+def q4_dual_gemv(Wa: HostWeight, Wb: HostWeight, x, gamma=None, eps=0.0):
+    """Two weight streams over one (optionally normed) activation batch
+    (forward_decode_fused_layers step 3, K+V with inline input_norm).
+    Returns (ya, Sa, yb, Sb)."""
+    xh = rmsnorm(x, gamma, eps) if gamma is not None else _f64(x)
+    ya, Sa = gemv(Wa, xh)
+    yb, Sb = gemv(Wb, xh)
+    return ya, Sa, yb, Sb
+
+
+def q4_gus_nrm(Wg: HostWeight, Wu: HostWeight, x, gamma, eps):
+    """RMSNorm, gate and up GEMVs, then ``h = silu(g) * u`` (honeycrisp/mod.rs,
+    post_norm + gate + up + silu fused).  Returns (h, g, Sg, u, Su)."""
+    xh = rmsnorm(x, gamma, eps)
+    g, Sg = gemv(Wg, xh)
+    u, Su = gemv(Wu, xh)
+    return swiglu(g, u), g, Sg, u, Su
+
+
+def q4_res_gemv(W: HostWeight, x, r):
+    """``y = W x + r`` (honeycrisp/mod.rs, fused matmul + residual).
+    Returns (y, S)."""
+    y, S = gemv(W, x)
+    r = _f64(r)
+    if r.ndim == 1:
+        r = r[None, :]
+    return add(y, r), S
+
+
+def q4_argmax(W: HostWeight, x, gamma=None, eps=0.0):
+    """Logits projection (optionally behind an RMSNorm) and greedy argmax per
+    activation row (Module gpu, module sampling).  Returns (idx, logits, S)."""
+    xh = rmsnorm(x, gamma, eps) if gamma is not None else _f64(x)
+    logits, S = gemv(W, xh)
+    idx = np.array([argmax(logits[r]) for r in range(logits.shape[0])], dtype=np.int64)
+    return idx, logits, S

@@ -1,0 +1,179 @@
+/*
+ * q4_oracle.c -- plain, slow, obviously correct CPU oracle for the weight-only
+ * 4-bit dequant-in-GEMV family (Q4_0 blocks and affine-Q4 groups) and its fused
+ * neighbours (RMSNorm, SwiGLU, residual add, greedy argmax).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this code.  The CUDA library never
+ * includes, links or calls it, and it shares no source with the CUDA path.
+ *
+ * Everything is computed in IEEE double precision, one output at a time:
+ * dequantise a weight row to f64 from its stored bytes, then a sequential dot
+ * product in ascending k.  No blocking, no reordering, no group-sum rewrite.
+ * Build with -ffp-contract=off so that no multiply-add is fused on any host.
+ *
+ * Sources (the pages this code follows):
+ *  - Q4_0 block (32 weights in 18 bytes: fp16 scale d, then 16 nibble bytes;
+ *    weight = d * (q - 8)): crate inferencelayer, Functions, entries
+ *    q4_0_to_q8_0n (the lossless upcast keeps d and maps q to nib - 8) and
+ *    gemv_q1_k_lcpp_src (Q4_0's 18-byte 32-weight block).  Nibble order inside
+ *    the 16 bytes is not stated on the pages; the reading taken is the GGUF
+ *    order the pages read as-is (gemv_q8_0n_k_lcpp_src): byte i holds element i
+ *    in its low nibble and element i+16 in its high nibble.
+ *  - Affine-Q4 group (32 weights, bf16 scale s and bf16 min m, weight =
+ *    s*q + m): Module gpu (qwen4_exp), Structs Q (affine-Q4 projection with
+ *    byte offsets into a bf16 weight buffer) and HalfSet (even/odd streams plus
+ *    per-32 group sums).  Reading: nibbles are planar [n][k/2] with byte i of a
+ *    row holding element 2i (low nibble) and 2i+1 (high nibble); s and m are
+ *    planar [n][k/32].
+ *  - RMSNorm with eps and width d = len(gamma): honeycrisp/mod.rs, Op::RmsNorm
+ *    and forward_decode_fused_layers step "1+2 Q matmul with inline
+ *    input_norm".  Reading: xhat = x / sqrt(mean(x^2) + eps) * gamma.
+ *  - SwiGLU mid = silu(gate) * up: honeycrisp/mod.rs, fused_ffn_residual step 4.
+ *  - Residual y = matmul(x, w) + residual: honeycrisp/mod.rs, fused
+ *    matmul + residual dispatch in forward_decode_fused_layers.
+ *  - Greedy argmax over logits: Module gpu, module sampling.  Reading: ties go
+ *    to the lowest index.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+/* IEEE 754 binary16 -> double, from the bit fields. */
+double q4o_half(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);                 /* subnormal: f * 2^-24 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f | 0x400), e - 25);    /* 1.f * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 (the upper half of an IEEE binary32) -> double, from the bit fields. */
+double q4o_bf16(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);                /* subnormal: f * 2^-133 */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f | 0x80), e - 134);    /* 1.f * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* One row of Q4_0 weights, dequantised to f64.
+ * blocks: [n][k/32][18] bytes; w: [k]. */
+void q4o_q4_0_row(const uint8_t *blocks, int64_t k, int64_t row, double *w)
+{
+    int64_t nblk = k / 32;
+    const uint8_t *r = blocks + row * nblk * 18;
+    for (int64_t b = 0; b < nblk; ++b) {
+        const uint8_t *blk = r + b * 18;
+        double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));
+        const uint8_t *qs = blk + 2;
+        for (int j = 0; j < 32; ++j) {
+            int q = (j < 16) ? (qs[j] & 0x0f) : (qs[j - 16] >> 4);
+            w[b * 32 + j] = d * (double)(q - 8);
+        }
+    }
+}
+
+/* One row of affine-Q4 weights, dequantised to f64.
+ * nib: [n][k/2] bytes; s, m: [n][k/32] bf16 bits; w: [k]. */
+void q4o_affine_row(const uint8_t *nib, const uint16_t *s, const uint16_t *m,
+                    int64_t k, int64_t row, double *w)
+{
+    const uint8_t *r = nib + row * (k / 2);
+    const uint16_t *sr = s + row * (k / 32);
+    const uint16_t *mr = m + row * (k / 32);
+    for (int64_t e = 0; e < k; ++e) {
+        int byte = r[e / 2];
+        int q = (e & 1) ? (byte >> 4) : (byte & 0x0f);
+        double sg = q4o_bf16(sr[e / 32]);
+        double mg = q4o_bf16(mr[e / 32]);
+        w[e] = sg * (double)q + mg;
+    }
+}
+
+/* y[r][i] = sum_k w[i][k] * x[r][k], summed sequentially in ascending k, and
+ * bound[r][i] = sum_k |w[i][k]| * |x[r][k]| (the scale of the parity tolerance).
+ * fmt 0: a = Q4_0 blocks.  fmt 1: a = nibbles, b = s, c = m.
+ * x: [nb][k] f64; y, bound: [nb][n]; wrow: scratch of k doubles. */
+void q4o_gemv(int fmt, const void *a, const void *b, const void *c,
+              int64_t n, int64_t k, const double *x, int64_t nb,
+              double *y, double *bound, double *wrow)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        if (fmt == 0)
+            q4o_q4_0_row((const uint8_t *)a, k, i, wrow);
+        else
+            q4o_affine_row((const uint8_t *)a, (const uint16_t *)b,
+                           (const uint16_t *)c, k, i, wrow);
+        for (int64_t r = 0; r < nb; ++r) {
+            const double *xr = x + r * k;
+            double acc = 0.0, mag = 0.0;
+            for (int64_t e = 0; e < k; ++e) {
+                acc += wrow[e] * xr[e];
+                mag += fabs(wrow[e]) * fabs(xr[e]);
+            }
+            y[r * n + i] = acc;
+            if (bound)
+                bound[r * n + i] = mag;
+        }
+    }
+}
+
+/* xhat[r][e] = x[r][e] / sqrt(mean_e' x[r][e']^2 + eps) * gamma[e]. */
+void q4o_rmsnorm(const double *x, const double *gamma, int64_t nb, int64_t k,
+                 double eps, double *xhat)
+{
+    for (int64_t r = 0; r < nb; ++r) {
+        const double *xr = x + r * k;
+        double ss = 0.0;
+        for (int64_t e = 0; e < k; ++e)
+            ss += xr[e] * xr[e];
+        double rms = sqrt(ss / (double)k + eps);
+        for (int64_t e = 0; e < k; ++e)
+            xhat[r * k + e] = xr[e] / rms * gamma[e];
+    }
+}
+
+/* silu(t) = t / (1 + exp(-t)) */
+double q4o_silu(double t)
+{
+    return t / (1.0 + exp(-t));
+}
+
+/* h = silu(g) * u, elementwise. */
+void q4o_swiglu(const double *g, const double *u, int64_t count, double *h)
+{
+    for (int64_t i = 0; i < count; ++i)
+        h[i] = q4o_silu(g[i]) * u[i];
+}
+
+/* out = a + b, elementwise. */
+void q4o_add(const double *a, const double *b, int64_t count, double *out)
+{
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = a[i] + b[i];
+}
+
+/* Index of the largest value; the lowest index wins a tie. */
+int64_t q4o_argmax(const double *v, int64_t n)
+{
+    int64_t best = 0;
+    for (int64_t i = 1; i < n; ++i)
+        if (v[i] > v[best])
+            best = i;
+    return best;
+}

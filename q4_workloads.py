@@ -1,0 +1,252 @@
+"""Seeded synthetic inputs for the Q4 dequant-in-GEMV workloads.
+
+Shared by the tests, the smoke check and the benchmark.  This module holds
+none of the method's arithmetic: only random draws (numpy PCG64,
+``default_rng(seed)``) and their *storage encodings* (fp16 / bf16 rounding of
+the drawn scales, nibble packing into the host byte layouts).  Both the
+oracle and the CUDA library consume exactly the bytes produced here.
+
+Host storage formats (the readings of the pages, stated once):
+
+* Q4_0: ``uint8[n, k/32, 18]``; bytes 0-1 = fp16 scale ``d`` little endian;
+  bytes 2..17 = 16 nibble bytes, byte ``i`` holding element ``i`` in its low
+  nibble and element ``i + 16`` in its high nibble (GGUF order).
+* affine-Q4: nibbles ``uint8[n, k/2]`` with byte ``i`` holding element ``2i``
+  (low nibble) and ``2i + 1`` (high nibble); ``s`` and ``m`` as bf16 bit
+  patterns ``uint16[n, k/32]``.
+
+Draw order for every weight matrix: nibbles ``q`` (``integers(0, 16,
+(n, k))``), then scales, then (affine) mins.  Activations are drawn after the
+weights of the same configuration, in the order documented per builder.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+D_RANGE = (0.005, 0.02)       # fp16 scale d ~ U[0.005, 0.02]
+S_RANGE = (0.005, 0.02)       # bf16 scale s ~ U[0.005, 0.02]
+M_RANGE = (-0.1, 0.0)         # bf16 min m ~ U[-0.1, 0]
+EPS = 1e-6
+
+
+def f32_to_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (round to nearest, ties to even); return the bits."""
+    u = np.ascontiguousarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def pack_q4_0(q: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
+    """Pack nibbles ``q[n, k]`` (0..15) and fp16 scale bits ``d_bits[n, k/32]``
+    into Q4_0 host blocks ``uint8[n, k/32, 18]``."""
+    n, k = q.shape
+    nb = k // 32
+    qb = q.reshape(n, nb, 32).astype(np.uint8)
+    out = np.empty((n, nb, 18), dtype=np.uint8)
+    d = np.ascontiguousarray(d_bits, dtype=np.uint16).reshape(n, nb)
+    out[:, :, 0] = (d & 0xFF).astype(np.uint8)
+    out[:, :, 1] = (d >> 8).astype(np.uint8)
+    out[:, :, 2:] = qb[:, :, :16] | (qb[:, :, 16:] << 4)
+    return out
+
+
+def pack_affine_nibbles(q: np.ndarray) -> np.ndarray:
+    """Pack nibbles ``q[n, k]`` into ``uint8[n, k/2]`` (even element low)."""
+    q = q.astype(np.uint8)
+    return np.ascontiguousarray(q[:, 0::2] | (q[:, 1::2] << 4))
+
+
+@dataclass
+class Q4_0Host:
+    n: int
+    k: int
+    blocks: np.ndarray          # uint8[n, k/32, 18]
+
+
+@dataclass
+class AffineHost:
+    n: int
+    k: int
+    nib: np.ndarray             # uint8[n, k/2]
+    s: np.ndarray               # uint16[n, k/32] bf16 bits
+    m: np.ndarray               # uint16[n, k/32] bf16 bits
+
+
+def draw_q4_0(rng: np.random.Generator, n: int, k: int, d_range=D_RANGE) -> Q4_0Host:
+    """q ~ U{0..15}, d ~ U[d_range] rounded to fp16."""
+    assert k % 32 == 0
+    q = rng.integers(0, 16, size=(n, k), dtype=np.uint8)
+    d = rng.uniform(d_range[0], d_range[1], size=(n, k // 32)).astype(np.float16)
+    return Q4_0Host(n, k, pack_q4_0(q, d.view(np.uint16)))
+
+
+def draw_affine(rng: np.random.Generator, n: int, k: int,
+                s_range=S_RANGE, m_range=M_RANGE) -> AffineHost:
+    """q ~ U{0..15}, s ~ U[s_range], m ~ U[m_range], both rounded to bf16."""
+    assert k % 32 == 0
+    q = rng.integers(0, 16, size=(n, k), dtype=np.uint8)
+    s = rng.uniform(s_range[0], s_range[1], size=(n, k // 32)).astype(np.float32)
+    m = rng.uniform(m_range[0], m_range[1], size=(n, k // 32)).astype(np.float32)
+    return AffineHost(n, k, pack_affine_nibbles(q), f32_to_bf16_bits(s), f32_to_bf16_bits(m))
+
+
+def draw_x(rng: np.random.Generator, nb: int, k: int) -> np.ndarray:
+    """Activations ~ N(0, 1), fp32 ``[nb, k]``."""
+    return rng.standard_normal((nb, k)).astype(np.float32)
+
+
+def draw_gamma(rng: np.random.Generator, k: int) -> np.ndarray:
+    """RMSNorm weight gamma = 1 + 0.1 * N(0, 1), fp32 ``[k]``."""
+    return (1.0 + 0.1 * rng.standard_normal(k)).astype(np.float32)
+
+
+# ------------------------------------------------------------ configurations
+
+@dataclass
+class Cfg0:
+    """Q4_0 GEMV, nb = 1, N = K = 1024; seed 0.  Draws: W, x."""
+    W: Q4_0Host
+    x: np.ndarray
+
+
+def cfg0(seed: int = 0, n: int = 1024, k: int = 1024) -> Cfg0:
+    rng = np.random.default_rng(seed)
+    W = draw_q4_0(rng, n, k)
+    return Cfg0(W, draw_x(rng, 1, k))
+
+
+@dataclass
+class Cfg1:
+    """Fused RMSNorm + Q4_0 q-projection (2048 x 2048) and the dual K/V pair
+    (2 x 512 x 2048) over one normed x; nb = 1; seed 1.
+    Draws: x, gamma, Wq, Wk, Wv."""
+    x: np.ndarray
+    gamma: np.ndarray
+    Wq: Q4_0Host
+    Wk: Q4_0Host
+    Wv: Q4_0Host
+    eps: float = EPS
+
+
+def cfg1(seed: int = 1, hidden: int = 2048, kv: int = 512, nb: int = 1) -> Cfg1:
+    rng = np.random.default_rng(seed)
+    x = draw_x(rng, nb, hidden)
+    gamma = draw_gamma(rng, hidden)
+    Wq = draw_q4_0(rng, hidden, hidden)
+    Wk = draw_q4_0(rng, kv, hidden)
+    Wv = draw_q4_0(rng, kv, hidden)
+    return Cfg1(x, gamma, Wq, Wk, Wv)
+
+
+@dataclass
+class Cfg2:
+    """MLP block, nb = 1, hidden 2048, intermediate 8192, all Q4_0; seed 2.
+    Draws: x, gamma, Wg, Wu, Wd, residual r."""
+    x: np.ndarray
+    gamma: np.ndarray
+    Wg: Q4_0Host
+    Wu: Q4_0Host
+    Wd: Q4_0Host
+    r: np.ndarray
+    eps: float = EPS
+
+
+def cfg2(seed: int = 2, hidden: int = 2048, inter: int = 8192, nb: int = 1) -> Cfg2:
+    rng = np.random.default_rng(seed)
+    x = draw_x(rng, nb, hidden)
+    gamma = draw_gamma(rng, hidden)
+    Wg = draw_q4_0(rng, inter, hidden)
+    Wu = draw_q4_0(rng, inter, hidden)
+    Wd = draw_q4_0(rng, hidden, inter)
+    r = draw_x(rng, nb, hidden)
+    return Cfg2(x, gamma, Wg, Wu, Wd, r)
+
+
+@dataclass
+class Cfg3:
+    """Affine-Q4 multi-row matvec, K = 4096, N = 14336, nb in {1,2,4,8,16};
+    seed 3.  Draws: W, then x for nb = 16 (smaller nb take the first rows)."""
+    W: AffineHost
+    x: np.ndarray
+
+
+def cfg3(seed: int = 3, n: int = 14336, k: int = 4096, nb_max: int = 16) -> Cfg3:
+    rng = np.random.default_rng(seed)
+    W = draw_affine(rng, n, k)
+    return Cfg3(W, draw_x(rng, nb_max, k))
+
+
+@dataclass
+class Layer:
+    gamma_in: np.ndarray
+    Wq: Q4_0Host
+    Wk: Q4_0Host
+    Wv: Q4_0Host
+    Wo: Q4_0Host
+    attn: np.ndarray            # N(0,1) stand-in for the attention output
+    gamma_post: np.ndarray
+    Wg: Q4_0Host
+    Wu: Q4_0Host
+    Wd: Q4_0Host
+
+
+@dataclass
+class Cfg4:
+    """Synthetic decode step: ``layers`` decoder blocks, nb = 1, hidden 2048,
+    then a final RMSNorm, a Q4_0 logits projection and argmax.
+
+    Seeds: the step input x and the final gamma / logits weight come from
+    ``default_rng(seed)``; layer ``l`` draws from ``default_rng(seed*1000+l)``
+    in the order gamma_in, Wq, Wk, Wv, Wo, attn, gamma_post, Wg, Wu, Wd."""
+    x: np.ndarray
+    layers: list = field(default_factory=list)
+    gamma_final: np.ndarray | None = None
+    Wlogits: Q4_0Host | None = None
+    eps: float = EPS
+
+
+def cfg4_layer(seed: int, layer: int, hidden: int = 2048, kv: int = 512,
+               inter: int = 8192, nb: int = 1) -> Layer:
+    rng = np.random.default_rng(seed * 1000 + layer)
+    gamma_in = draw_gamma(rng, hidden)
+    Wq = draw_q4_0(rng, hidden, hidden)
+    Wk = draw_q4_0(rng, kv, hidden)
+    Wv = draw_q4_0(rng, kv, hidden)
+    Wo = draw_q4_0(rng, hidden, hidden)
+    attn = draw_x(rng, nb, hidden)
+    gamma_post = draw_gamma(rng, hidden)
+    Wg = draw_q4_0(rng, inter, hidden)
+    Wu = draw_q4_0(rng, inter, hidden)
+    Wd = draw_q4_0(rng, hidden, inter)
+    return Layer(gamma_in, Wq, Wk, Wv, Wo, attn, gamma_post, Wg, Wu, Wd)
+
+
+def cfg4(seed: int = 4, layers: int = 16, hidden: int = 2048, kv: int = 512,
+         inter: int = 8192, vocab: int = 65536, nb: int = 1) -> Cfg4:
+    rng = np.random.default_rng(seed)
+    x = draw_x(rng, nb, hidden)
+    gamma_final = draw_gamma(rng, hidden)
+    Wlogits = draw_q4_0(rng, vocab, hidden)
+    c = Cfg4(x, [], gamma_final, Wlogits)
+    for l in range(layers):
+        c.layers.append(cfg4_layer(seed, l, hidden, kv, inter, nb))
+    return c
+
+
+def q4_0_weight_bytes(n: int, k: int) -> int:
+    """Algorithmic Q4_0 bytes: 18 per 32 weights."""
+    return n * (k // 32) * 18
+
+
+def affine_weight_bytes(n: int, k: int) -> int:
+    """Algorithmic affine-Q4 bytes: 16 nibble bytes + 2 + 2 per 32 weights."""
+    return n * (k // 32) * 20
+
+
+def decode_step_weight_bytes(layers: int = 16, hidden: int = 2048, kv: int = 512,
+                             inter: int = 8192, vocab: int = 65536) -> int:
+    per_layer = (q4_0_weight_bytes(hidden, hidden) * 2 + q4_0_weight_bytes(kv, hidden) * 2
+                 + q4_0_weight_bytes(inter, hidden) * 2 + q4_0_weight_bytes(hidden, inter))
+    return layers * per_layer + q4_0_weight_bytes(vocab, hidden)

@@ -1,0 +1,53 @@
+"""The oracle pins have teeth: plant a plausible mistake in a copy of the
+oracle's C source (on the CPU), rebuild it, and check that the pin suite now
+fails.  Each mutant is one slip a reader of the pages could make."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "q4_oracle.c")
+
+MUTANTS = [
+    ("q4_0 nibble order interleaved",
+     "int q = (j < 16) ? (qs[j] & 0x0f) : (qs[j - 16] >> 4);",
+     "int q = (qs[j / 2] >> (4 * (j & 1))) & 0x0f;"),
+    ("q4_0 offset dropped", "w[b * 32 + j] = d * (double)(q - 8);", "w[b * 32 + j] = d * (double)q;"),
+    ("q4_0 offset sign", "w[b * 32 + j] = d * (double)(q - 8);", "w[b * 32 + j] = d * (double)(8 - q);"),
+    ("fp16 scale byte order", "double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));",
+     "double d = q4o_half((uint16_t)(blk[1] | (blk[0] << 8)));"),
+    ("fp16 exponent bias", "v = ldexp((double)(f | 0x400), e - 25);", "v = ldexp((double)(f | 0x400), e - 24);"),
+    ("fp16 subnormal scale", "v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    ("bf16 exponent bias", "v = ldexp((double)(f | 0x80), e - 134);", "v = ldexp((double)(f | 0x80), e - 133);"),
+    ("affine nibble order", "int q = (e & 1) ? (byte >> 4) : (byte & 0x0f);",
+     "int q = (e & 1) ? (byte & 0x0f) : (byte >> 4);"),
+    ("affine min sign", "w[e] = sg * (double)q + mg;", "w[e] = sg * (double)q - mg;"),
+    ("affine min dropped", "w[e] = sg * (double)q + mg;", "w[e] = sg * (double)q;"),
+    ("activation row ignored", "acc += wrow[e] * xr[e];", "acc += wrow[e] * x[e];"),
+    ("rmsnorm sum not mean", "double rms = sqrt(ss / (double)k + eps);", "double rms = sqrt(ss + eps);"),
+    ("rmsnorm eps outside sqrt", "double rms = sqrt(ss / (double)k + eps);",
+     "double rms = sqrt(ss / (double)k) + eps;"),
+    ("rmsnorm gamma dropped", "xhat[r * k + e] = xr[e] / rms * gamma[e];", "xhat[r * k + e] = xr[e] / rms;"),
+    ("silu sign", "return t / (1.0 + exp(-t));", "return t / (1.0 + exp(t));"),
+    ("swiglu factors swapped", "h[i] = q4o_silu(g[i]) * u[i];", "h[i] = q4o_silu(u[i]) * g[i];"),
+    ("residual subtracted", "out[i] = a[i] + b[i];", "out[i] = a[i] - b[i];"),
+    ("argmax tie to last", "if (v[i] > v[best])", "if (v[i] >= v[best])"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-shared", "-fPIC",
+                           "-o", str(so), str(mut), "-lm"])
+    env = dict(os.environ, Q4_ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, "pins did not catch mutant: " + name

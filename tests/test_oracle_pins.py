@@ -1,0 +1,409 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test is chosen so that a plausible slip in the oracle (a wrong nibble
+order, a dropped ``-8``, a swapped operand, a transposed index, ``sum``
+instead of ``mean`` in RMSNorm, ``eps`` outside the square root, ``silu`` on
+the wrong factor, a tie going to the wrong index) fails at least one of them:
+
+* exhaustive decodes of every fp16 and bf16 bit pattern against numpy's own
+  conversions (a library routine);
+* the golden layout fixtures in ``tests/golden/`` and their closed forms;
+* exact rational arithmetic (``fractions.Fraction``) on tiny products;
+* a brute-force numpy decode with correctly rounded sums (``math.fsum``);
+* one-hot activations, all-zero weights, power-of-two scalings;
+* closed forms for RMSNorm of a constant vector and for the affine group-sum
+  identity, and scipy's logistic function for SiLU.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import q4_workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_fixture(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, val = line.split(":", 1)
+            out[key.strip()] = val.split()
+    return out
+
+
+def _q4_0_weight(blocks, n, k):
+    return oracle.HostWeight.q4_0(blocks, n, k)
+
+
+def _aff_weight(a):
+    return oracle.HostWeight.affine(a.nib, a.s, a.m, a.n, a.k)
+
+
+# ------------------------------------------------------------------ decoders
+
+def test_half_decode_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_f64(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert math.copysign(1.0, oracle.half_to_f64(0x8000)) == -1.0
+
+
+def test_bf16_decode_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32)
+    ref = (bits << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    got = np.array([oracle.bf16_to_f64(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# ------------------------------------------------------------- layout pins
+
+def test_q4_0_block_fixture_closed_form():
+    fx = _read_fixture("q4_0_block.txt")
+    blk = np.array([int(b, 16) for b in fx["bytes"]], dtype=np.uint8)
+    assert blk.size == 18                       # 18 bytes per 32 weights
+    w = oracle.dequant_row(_q4_0_weight(blk, 1, 32), 0)
+    expect = [2.0 * (i - 8) for i in range(16)] + [2.0 * (7 - i) for i in range(16)]
+    assert w.tolist() == expect
+
+
+def test_affine_group_fixture_closed_form():
+    fx = _read_fixture("affine_group.txt")
+    nib = np.array([int(b, 16) for b in fx["nibbles"]], dtype=np.uint8)
+    s = np.array([int(fx["s"][0], 16)], dtype=np.uint16)
+    m = np.array([int(fx["m"][0], 16)], dtype=np.uint16)
+    w = oracle.dequant_row(oracle.HostWeight.affine(nib, s, m, 1, 32), 0)
+    expect = []
+    for i in range(16):
+        expect += [i - 0.5, 14.5 - i]
+    assert w.tolist() == expect
+
+
+def test_generator_layout_matches_fixture_reading():
+    # The generator's packing puts element i and i+16 in byte i (Q4_0) and
+    # elements 2i, 2i+1 in byte i (affine): decode of a known q gives it back.
+    rng = np.random.default_rng(11)
+    q = rng.integers(0, 16, size=(3, 64), dtype=np.uint8)
+    d = np.full((3, 2), 0x3C00, dtype=np.uint16)           # d = 1.0
+    W = _q4_0_weight(wl.pack_q4_0(q, d), 3, 64)
+    assert np.array_equal(oracle.dequant(W), q.astype(np.float64) - 8.0)
+    s = np.full((3, 2), 0x3F80, dtype=np.uint16)           # s = 1.0
+    m = np.zeros((3, 2), dtype=np.uint16)                  # m = 0
+    Wa = oracle.HostWeight.affine(wl.pack_affine_nibbles(q), s, m, 3, 64)
+    assert np.array_equal(oracle.dequant(Wa), q.astype(np.float64))
+
+
+# ------------------------------------------------------------ dot products
+
+def _frac_half(bits):
+    return Fraction(float(np.uint16(bits).view(np.float16)))
+
+
+def _frac_bf16(bits):
+    return Fraction(float(np.uint32(int(bits) << 16).view(np.float32)))
+
+
+@pytest.mark.parametrize("n,k", [(1, 32), (2, 64), (3, 96)])
+def test_q4_0_exact_rationals(n, k):
+    rng = np.random.default_rng(100 + n)
+    W = wl.draw_q4_0(rng, n, k)
+    x = wl.draw_x(rng, 2, k)
+    y, S = oracle.q4_gemv(_q4_0_weight(W.blocks, n, k), x)
+    for r in range(2):
+        for i in range(n):
+            exact = Fraction(0)
+            for b in range(k // 32):
+                blk = W.blocks[i, b]
+                d = _frac_half(int(blk[0]) | (int(blk[1]) << 8))
+                for j in range(32):
+                    q = (blk[2 + j] & 15) if j < 16 else (blk[2 + j - 16] >> 4)
+                    exact += d * (int(q) - 8) * Fraction(float(x[r, b * 32 + j]))
+            err = abs(Fraction(y[r, i]) - exact)
+            assert err <= Fraction(k) * Fraction(2) ** -52 * Fraction(S[r, i])
+
+
+@pytest.mark.parametrize("n,k", [(1, 32), (2, 64), (3, 96)])
+def test_affine_exact_rationals(n, k):
+    rng = np.random.default_rng(200 + n)
+    A = wl.draw_affine(rng, n, k)
+    x = wl.draw_x(rng, 2, k)
+    y, S = oracle.q4_gemv(_aff_weight(A), x)
+    for r in range(2):
+        for i in range(n):
+            exact = Fraction(0)
+            for e in range(k):
+                byte = int(A.nib[i, e // 2])
+                q = (byte >> 4) if (e & 1) else (byte & 15)
+                w = _frac_bf16(A.s[i, e // 32]) * q + _frac_bf16(A.m[i, e // 32])
+                exact += w * Fraction(float(x[r, e]))
+            err = abs(Fraction(y[r, i]) - exact)
+            assert err <= Fraction(k) * Fraction(2) ** -52 * Fraction(S[r, i])
+
+
+def _numpy_decode_q4_0(blocks):
+    n, nbk, _ = blocks.shape
+    d = blocks[:, :, 0].astype(np.uint16) | (blocks[:, :, 1].astype(np.uint16) << 8)
+    dv = d.view(np.float16).astype(np.float64)
+    lo = (blocks[:, :, 2:] & 0x0F).astype(np.int64)
+    hi = (blocks[:, :, 2:] >> 4).astype(np.int64)
+    q = np.concatenate([lo, hi], axis=2) - 8
+    return (q * dv[:, :, None]).reshape(n, nbk * 32)
+
+
+def _numpy_decode_affine(A):
+    q = np.empty((A.n, A.k), dtype=np.int64)
+    q[:, 0::2] = A.nib & 0x0F
+    q[:, 1::2] = A.nib >> 4
+    s = (A.s.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    m = (A.m.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return q * np.repeat(s, 32, axis=1) + np.repeat(m, 32, axis=1)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("n,k", [(16, 256), (7, 96), (5, 32)])
+def test_brute_force_numpy_fsum(fmt, n, k):
+    rng = np.random.default_rng(7 * n + k)
+    if fmt == "q4_0":
+        H = wl.draw_q4_0(rng, n, k)
+        W = _q4_0_weight(H.blocks, n, k)
+        wd = _numpy_decode_q4_0(H.blocks)
+    else:
+        H = wl.draw_affine(rng, n, k)
+        W = _aff_weight(H)
+        wd = _numpy_decode_affine(H)
+    # every nibble value is present somewhere
+    assert len(np.unique(np.rint(wd * 1e6))) > 16
+    x = wl.draw_x(rng, 3, k)
+    y, S = oracle.q4_gemv(W, x)
+    for r in range(3):
+        for i in range(n):
+            ref = math.fsum(wd[i] * x[r].astype(np.float64))
+            assert abs(y[r, i] - ref) <= k * 2.0 ** -53 * S[r, i]
+            assert S[r, i] == pytest.approx(math.fsum(np.abs(wd[i] * x[r])), rel=1e-12)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+def test_one_hot_picks_the_column(fmt):
+    # N != K and nb rows with different one-hots catch transposed operands
+    # and a wrong row order.
+    n, k = 48, 96
+    rng = np.random.default_rng(5)
+    W = (_q4_0_weight(wl.draw_q4_0(rng, n, k).blocks, n, k) if fmt == "q4_0"
+         else _aff_weight(wl.draw_affine(rng, n, k)))
+    dense = oracle.dequant(W)
+    cols = [0, 17, 31, 32, 95]
+    x = np.zeros((len(cols), k), dtype=np.float32)
+    for r, c in enumerate(cols):
+        x[r, c] = 1.0
+    y, _ = oracle.q4_gemv(W, x)
+    for r, c in enumerate(cols):
+        assert np.array_equal(y[r], dense[:, c])
+
+
+def test_q4_0_all_eight_is_exact_zero():
+    rng = np.random.default_rng(6)
+    n, k = 9, 128
+    q = np.full((n, k), 8, dtype=np.uint8)
+    d = rng.uniform(0.005, 0.02, size=(n, k // 32)).astype(np.float16).view(np.uint16)
+    W = _q4_0_weight(wl.pack_q4_0(q, d), n, k)
+    y, S = oracle.q4_gemv(W, wl.draw_x(rng, 2, k))
+    assert np.all(y == 0.0) and np.all(S == 0.0)
+
+
+def test_q4_0_power_of_two_scalings_are_exact():
+    rng = np.random.default_rng(8)
+    n, k = 11, 160
+    H = wl.draw_q4_0(rng, n, k)
+    x = wl.draw_x(rng, 2, k)
+    y, _ = oracle.q4_gemv(_q4_0_weight(H.blocks, n, k), x)
+    b2 = H.blocks.copy()
+    d = (b2[:, :, 0].astype(np.uint16) | (b2[:, :, 1].astype(np.uint16) << 8)) + 0x0400  # exponent + 1
+    b2[:, :, 0] = (d & 0xFF).astype(np.uint8)
+    b2[:, :, 1] = (d >> 8).astype(np.uint8)
+    y2, _ = oracle.q4_gemv(_q4_0_weight(b2, n, k), x)
+    assert np.array_equal(y2, 2.0 * y)
+    y4, _ = oracle.q4_gemv(_q4_0_weight(H.blocks, n, k), 4.0 * x)
+    assert np.array_equal(y4, 4.0 * y)
+
+
+def test_q4_0_additive_in_x():
+    rng = np.random.default_rng(9)
+    n, k = 6, 64
+    W = _q4_0_weight(wl.draw_q4_0(rng, n, k).blocks, n, k)
+    x1, x2 = wl.draw_x(rng, 1, k), wl.draw_x(rng, 1, k)
+    y1, S1 = oracle.q4_gemv(W, x1)
+    y2, S2 = oracle.q4_gemv(W, x2)
+    y12, _ = oracle.q4_gemv(W, x1.astype(np.float64) + x2.astype(np.float64))
+    assert np.allclose(y12, y1 + y2, rtol=0, atol=1e-12 * (S1 + S2).max())
+
+
+def test_affine_group_sum_identities():
+    # w = s*q + m  =>  y = sum_g s_g * sum_j q_j x_j + m_g * gsum_g.
+    rng = np.random.default_rng(10)
+    n, k, G = 4, 128, 4
+    x = wl.draw_x(rng, 2, k).astype(np.float64)
+    gs = np.array([[math.fsum(x[r, 32 * g:32 * g + 32]) for g in range(G)] for r in range(2)])
+    s = wl.f32_to_bf16_bits(rng.uniform(0.005, 0.02, (n, G)).astype(np.float32))
+    m = wl.f32_to_bf16_bits(rng.uniform(-0.1, 0.0, (n, G)).astype(np.float32))
+    sv = (s.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    mv = (m.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    # all q = 0 -> sum_g m_g gsum_g
+    W0 = oracle.HostWeight.affine(np.zeros((n, k // 2), np.uint8), s, m, n, k)
+    y0, _ = oracle.q4_gemv(W0, x)
+    ref0 = gs @ mv.T
+    assert np.allclose(y0, ref0, rtol=1e-13, atol=1e-14)
+    # s = 0 gives the same whatever q is
+    Ws = oracle.HostWeight.affine(rng.integers(0, 256, (n, k // 2), dtype=np.uint8),
+                                  np.zeros_like(s), m, n, k)
+    ys, _ = oracle.q4_gemv(Ws, x)
+    assert np.allclose(ys, ref0, rtol=1e-13, atol=1e-14)
+    # q = c in every group: sum_g (s_g c + m_g) gsum_g
+    for c in (1, 7, 15):
+        byte = np.uint8(c | (c << 4))
+        Wc = oracle.HostWeight.affine(np.full((n, k // 2), byte, np.uint8), s, m, n, k)
+        yc, _ = oracle.q4_gemv(Wc, x)
+        refc = gs @ (sv * c + mv).T
+        assert np.allclose(yc, refc, rtol=1e-12, atol=1e-13)
+    # m = 0: pure scale, y = sum_g s_g * sum_j q_j x_j
+    nib = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+    Wm = oracle.HostWeight.affine(nib, s, np.zeros_like(m), n, k)
+    ym, _ = oracle.q4_gemv(Wm, x)
+    q = np.empty((n, k)); q[:, 0::2] = nib & 15; q[:, 1::2] = nib >> 4
+    refm = np.array([[sum(sv[i, g] * math.fsum(q[i, 32 * g:32 * g + 32] * x[r, 32 * g:32 * g + 32])
+                          for g in range(G)) for i in range(n)] for r in range(2)])
+    assert np.allclose(ym, refm, rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------------ RMSNorm
+
+@pytest.mark.parametrize("eps", [1e-6, 0.5])
+@pytest.mark.parametrize("k", [32, 2048])
+def test_rmsnorm_constant_vector(eps, k):
+    rng = np.random.default_rng(12)
+    gamma = wl.draw_gamma(rng, k).astype(np.float64)
+    for c in (3.0, -0.25, 1e-3):
+        xh = oracle.rmsnorm(np.full((1, k), c), gamma, eps)
+        ref = gamma * (c / math.sqrt(c * c + eps))
+        assert np.allclose(xh[0], ref, rtol=1e-14, atol=0)
+
+
+def test_rmsnorm_two_elements_and_scale_invariance():
+    g = np.array([1.5, -2.0])
+    xh = oracle.rmsnorm(np.array([[3.0, 4.0]]), g, 0.0)
+    rms = math.sqrt((9.0 + 16.0) / 2.0)
+    assert np.allclose(xh[0], [3.0 / rms * 1.5, 4.0 / rms * -2.0], rtol=1e-15)
+    rng = np.random.default_rng(13)
+    x = wl.draw_x(rng, 2, 256)
+    gamma = wl.draw_gamma(rng, 256)
+    a = oracle.rmsnorm(x, gamma, 1e-12)
+    b = oracle.rmsnorm(1000.0 * x.astype(np.float64), gamma, 1e-12)
+    assert np.allclose(a, b, rtol=1e-12, atol=0)
+
+
+def test_nrm_gemv_constant_vector_closed_form():
+    rng = np.random.default_rng(14)
+    n, k, c, eps = 8, 64, 0.75, 1e-6
+    W = _q4_0_weight(wl.draw_q4_0(rng, n, k).blocks, n, k)
+    gamma = wl.draw_gamma(rng, k).astype(np.float64)
+    y, _ = oracle.q4_nrm_gemv(W, np.full((1, k), c), gamma, eps)
+    y2, _ = oracle.q4_gemv(W, gamma * (c / math.sqrt(c * c + eps)))
+    assert np.allclose(y, y2, rtol=1e-13, atol=1e-15)
+
+
+# ----------------------------------------------------------- SiLU, residual
+
+def test_silu_against_logistic():
+    scipy_special = pytest.importorskip("scipy.special")
+    t = np.concatenate([np.linspace(-30, 30, 601), [0.0, 1e-8, -1e-8, 50.0, -50.0]])
+    got = np.array([oracle.silu(v) for v in t])
+    ref = t * scipy_special.expit(t)
+    assert np.allclose(got, ref, rtol=1e-14, atol=1e-300)
+    assert oracle.silu(0.0) == 0.0
+
+
+def test_swiglu_factor_order():
+    g = np.array([2.0, -1.0, 0.0])
+    u = np.array([-3.0, 5.0, 7.0])
+    h = oracle.swiglu(g, u)
+    ref = [2.0 / (1.0 + math.exp(-2.0)) * -3.0, -1.0 / (1.0 + math.exp(1.0)) * 5.0, 0.0]
+    assert np.allclose(h, ref, rtol=1e-15)
+
+
+def test_gus_zero_gate_or_up_gives_zero():
+    rng = np.random.default_rng(15)
+    n, k = 16, 64
+    zeros = _q4_0_weight(wl.pack_q4_0(np.full((n, k), 8, np.uint8),
+                                      np.full((n, k // 32), 0x3C00, np.uint16)), n, k)
+    W = _q4_0_weight(wl.draw_q4_0(rng, n, k).blocks, n, k)
+    x = wl.draw_x(rng, 1, k)
+    gamma = wl.draw_gamma(rng, k)
+    h, *_ = oracle.q4_gus_nrm(zeros, W, x, gamma, 1e-6)
+    assert np.all(h == 0.0)
+    h, *_ = oracle.q4_gus_nrm(W, zeros, x, gamma, 1e-6)
+    assert np.all(h == 0.0)
+
+
+def test_residual_cases():
+    rng = np.random.default_rng(16)
+    n, k = 12, 96
+    H = wl.draw_q4_0(rng, n, k)
+    W = _q4_0_weight(H.blocks, n, k)
+    x = wl.draw_x(rng, 2, k)
+    y0, _ = oracle.q4_gemv(W, x)
+    y, _ = oracle.q4_res_gemv(W, x, np.zeros((2, n)))
+    assert np.array_equal(y, y0)
+    r = wl.draw_x(rng, 2, n)
+    zero = _q4_0_weight(wl.pack_q4_0(np.full((n, k), 8, np.uint8),
+                                     np.full((n, k // 32), 0x3C00, np.uint16)), n, k)
+    yz, _ = oracle.q4_res_gemv(zero, x, r)
+    assert np.array_equal(yz, r.astype(np.float64))
+
+
+def test_dual_is_two_gemvs():
+    rng = np.random.default_rng(17)
+    k = 64
+    Wa = _q4_0_weight(wl.draw_q4_0(rng, 16, k).blocks, 16, k)
+    Wb = _q4_0_weight(wl.draw_q4_0(rng, 8, k).blocks, 8, k)
+    x = wl.draw_x(rng, 1, k)
+    gamma = wl.draw_gamma(rng, k)
+    ya, _, yb, _ = oracle.q4_dual_gemv(Wa, Wb, x, gamma, 1e-6)
+    ra, _ = oracle.q4_nrm_gemv(Wa, x, gamma, 1e-6)
+    rb, _ = oracle.q4_nrm_gemv(Wb, x, gamma, 1e-6)
+    assert np.array_equal(ya, ra) and np.array_equal(yb, rb)
+
+
+# ------------------------------------------------------------------- argmax
+
+def test_argmax_matches_numpy_first_max():
+    rng = np.random.default_rng(18)
+    cases = [rng.standard_normal(1000),
+             np.array([1.0, 3.0, 3.0, 2.0]),
+             np.full(17, -4.0),
+             np.array([-np.inf, -1e300, -1e300]),
+             np.concatenate([np.zeros(50), [5.0], np.zeros(50), [5.0]])]
+    for v in cases:
+        assert oracle.argmax(v) == int(np.argmax(v))
+
+
+def test_argmax_planted_unique_max():
+    rng = np.random.default_rng(19)
+    n, k = 64, 32
+    q = rng.integers(0, 16, (n, k), dtype=np.uint8)
+    q[41, :] = 15                         # row 41 dominates for a positive x
+    d = np.full((n, 1), 0x3C00, np.uint16)
+    W = _q4_0_weight(wl.pack_q4_0(q, d), n, k)
+    idx, logits, _ = oracle.q4_argmax(W, np.ones((1, k), np.float32))
+    assert idx[0] == 41 == int(np.argmax(logits[0]))
