@@ -1,0 +1,311 @@
+"""Python binding of libq4gemv (weight-only 4-bit dequant-in-GEMV for sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libq4gemv.so``; this module checks tensor dtypes and devices,
+passes raw pointers and the current CUDA stream, and raises on a non-OK
+status.  PyTorch provides device memory and streams, nothing else.  There is
+no CPU fallback: if the library is missing the calls raise.
+
+Entry points (same names as the C ABI in ``include/q4gemv.h``):
+``q4_gemv``, ``q4_nrm_gemv``, ``q4_dual_gemv``, ``q4_gus_nrm``,
+``q4_res_gemv``, ``q4_argmax``, ``q4_group_sums``; plus ``Q4Weight`` for
+repacking host weights into the device layout.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+LIB_PATH = os.path.join(_HERE, "libq4gemv.so")
+HEADER_PATH = os.path.join(_ROOT, "include", "q4gemv.h")
+
+Q4_FMT_Q4_0 = 0
+Q4_FMT_AFFINE = 1
+MAX_NB = 16
+
+STATUS = {0: "Q4_OK", 1: "Q4_ERR_NULL", 2: "Q4_ERR_SHAPE", 3: "Q4_ERR_ALIGN",
+          4: "Q4_ERR_UNSUPPORTED", 5: "Q4_ERR_WORKSPACE", 6: "Q4_ERR_CUDA"}
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s" % (what, STATUS.get(status, status)))
+
+
+class _CWeight(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("n", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("dev", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libq4gemv.so in-tree (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libq4gemv.so is not built (run __graft_entry__.build() or "
+                               "bit_weight_quantized_q4_gb300.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+        W = ctypes.POINTER(_CWeight)
+        sig = {
+            "q4_packed_bytes": (SZ, [I32, I32, I32]),
+            "q4_weight_bytes": (SZ, [I32, I32, I32]),
+            "q4_repack_q4_0": (I32, [P, I32, I32, P, SZ]),
+            "q4_repack_affine": (I32, [P, P, P, I32, I32, P, SZ]),
+            "q4_unpack_q4_0": (I32, [P, SZ, I32, I32, P]),
+            "q4_unpack_affine": (I32, [P, SZ, I32, I32, P, P, P]),
+            "q4_group_sums": (I32, [P, I32, I32, P, P]),
+            "q4_gemv": (I32, [W, P, P, I32, P, P]),
+            "q4_nrm_gemv": (I32, [W, P, P, F, I32, P, P]),
+            "q4_dual_gemv": (I32, [W, W, P, P, F, I32, P, P, P]),
+            "q4_gus_nrm": (I32, [W, W, P, P, F, I32, P, P]),
+            "q4_res_gemv": (I32, [W, P, P, I32, P, P]),
+            "q4_argmax_workspace_bytes": (SZ, [I32, I32]),
+            "q4_argmax": (I32, [W, P, P, F, I32, P, P, P, P, SZ, P]),
+            "q4_plan": (I32, [I32, I32, I32, I32, I32, I32, ctypes.POINTER(ctypes.c_int32)]),
+            "q4_status_str": (ctypes.c_char_p, [I32]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions ``include/q4gemv.h`` declares."""
+    src = open(HEADER_PATH).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(q4_[a-z0-9_]+)\s*\(", src)))
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise Q4Error(status, what)
+
+
+# ------------------------------------------------------------------ host side
+
+def packed_bytes(fmt: int, n: int, k: int) -> int:
+    return int(lib().q4_packed_bytes(fmt, n, k))
+
+
+def weight_bytes(fmt: int, n: int, k: int) -> int:
+    return int(lib().q4_weight_bytes(fmt, n, k))
+
+
+def repack_q4_0(blocks: np.ndarray, n: int, k: int) -> np.ndarray:
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    if blocks.size != n * (k // 32) * 18:
+        raise ValueError("Q4_0 blocks must be uint8[n, k/32, 18]")
+    nbytes = packed_bytes(Q4_FMT_Q4_0, n, k)
+    if nbytes == 0:
+        raise ValueError("bad shape n=%d k=%d" % (n, k))
+    out = np.empty(nbytes, dtype=np.uint8)
+    _check(lib().q4_repack_q4_0(blocks.ctypes.data, n, k, out.ctypes.data, nbytes), "q4_repack_q4_0")
+    return out
+
+
+def repack_affine(nib: np.ndarray, s: np.ndarray, m: np.ndarray, n: int, k: int) -> np.ndarray:
+    nib = np.ascontiguousarray(nib, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint16)
+    m = np.ascontiguousarray(m, dtype=np.uint16)
+    if nib.size != n * k // 2 or s.size != n * k // 32 or m.size != n * k // 32:
+        raise ValueError("affine weights must be nib uint8[n, k/2], s/m uint16[n, k/32]")
+    nbytes = packed_bytes(Q4_FMT_AFFINE, n, k)
+    if nbytes == 0:
+        raise ValueError("bad shape n=%d k=%d" % (n, k))
+    out = np.empty(nbytes, dtype=np.uint8)
+    _check(lib().q4_repack_affine(nib.ctypes.data, s.ctypes.data, m.ctypes.data, n, k,
+                                  out.ctypes.data, nbytes), "q4_repack_affine")
+    return out
+
+
+def unpack_q4_0(packed: np.ndarray, n: int, k: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    out = np.zeros((n, k // 32, 18), dtype=np.uint8)
+    _check(lib().q4_unpack_q4_0(packed.ctypes.data, packed.size, n, k, out.ctypes.data), "q4_unpack_q4_0")
+    return out
+
+
+def unpack_affine(packed: np.ndarray, n: int, k: int):
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    nib = np.zeros((n, k // 2), dtype=np.uint8)
+    s = np.zeros((n, k // 32), dtype=np.uint16)
+    m = np.zeros((n, k // 32), dtype=np.uint16)
+    _check(lib().q4_unpack_affine(packed.ctypes.data, packed.size, n, k, nib.ctypes.data,
+                                  s.ctypes.data, m.ctypes.data), "q4_unpack_affine")
+    return nib, s, m
+
+
+def plan(fmt: int, tiles: int, chunks: int, nb: int, pairs: bool, num_sms: int) -> dict:
+    out = (ctypes.c_int32 * 6)()
+    _check(lib().q4_plan(fmt, tiles, chunks, nb, int(pairs), num_sms, out), "q4_plan")
+    return dict(zip(("TG", "S", "Cs", "groups", "ctas", "smem"), list(out)))
+
+
+# ---------------------------------------------------------------- device side
+
+def _torch():
+    import torch
+    return torch
+
+
+class Q4Weight:
+    """A repacked weight matrix resident in device memory (owns its tensor)."""
+
+    def __init__(self, fmt: int, n: int, k: int, packed: np.ndarray, device="cuda"):
+        torch = _torch()
+        self.fmt, self.n, self.k = int(fmt), int(n), int(k)
+        self.tensor = torch.from_numpy(packed).to(device)
+        self.nbytes = int(packed.size)
+        self._c = _CWeight(self.fmt, self.n, self.k, self.tensor.data_ptr(), self.nbytes)
+
+    @classmethod
+    def from_q4_0(cls, blocks: np.ndarray, n: int, k: int, device="cuda") -> "Q4Weight":
+        return cls(Q4_FMT_Q4_0, n, k, repack_q4_0(blocks, n, k), device)
+
+    @classmethod
+    def from_affine(cls, nib, s, m, n: int, k: int, device="cuda") -> "Q4Weight":
+        return cls(Q4_FMT_AFFINE, n, k, repack_affine(nib, s, m, n, k), device)
+
+    @property
+    def weight_bytes(self) -> int:
+        """Algorithmic bytes: 18 (Q4_0) or 20 (affine) per 32 weights."""
+        return weight_bytes(self.fmt, self.n, self.k)
+
+    def cref(self):
+        return ctypes.byref(self._c)
+
+
+def _stream():
+    return _torch().cuda.current_stream().cuda_stream
+
+
+def _dev_f32(t, name, shape=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
+        raise TypeError("%s must be a CUDA float32 tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    return t
+
+
+def _rows(x, k):
+    x = _dev_f32(x, "x")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    if x.dim() != 2 or x.shape[1] != k:
+        raise ValueError("x must be [nb, %d]" % k)
+    return x, x.shape[0]
+
+
+def _out(out, shape, like):
+    torch = _torch()
+    if out is None:
+        return torch.empty(shape, dtype=torch.float32, device=like.device)
+    return _dev_f32(out, "out", shape)
+
+
+def q4_group_sums(x, out=None):
+    torch = _torch()
+    x = _dev_f32(x, "x")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    nb, k = x.shape
+    out = _out(out, (nb, k // 32), x)
+    _check(lib().q4_group_sums(x.data_ptr(), nb, k, out.data_ptr(), _stream()), "q4_group_sums")
+    return out
+
+
+def q4_gemv(W: Q4Weight, x, gsum=None, out=None):
+    x, nb = _rows(x, W.k)
+    out = _out(out, (nb, W.n), x)
+    gp = None
+    if gsum is not None:
+        gp = _dev_f32(gsum, "gsum", (nb, W.k // 32)).data_ptr()
+    _check(lib().q4_gemv(W.cref(), x.data_ptr(), gp, nb, out.data_ptr(), _stream()), "q4_gemv")
+    return out
+
+
+def q4_nrm_gemv(W: Q4Weight, x, gamma, eps: float, out=None):
+    x, nb = _rows(x, W.k)
+    gamma = _dev_f32(gamma, "gamma", (W.k,))
+    out = _out(out, (nb, W.n), x)
+    _check(lib().q4_nrm_gemv(W.cref(), x.data_ptr(), gamma.data_ptr(), float(eps), nb, out.data_ptr(),
+                             _stream()), "q4_nrm_gemv")
+    return out
+
+
+def q4_dual_gemv(Wa: Q4Weight, Wb: Q4Weight, x, gamma=None, eps: float = 0.0, out_a=None, out_b=None):
+    x, nb = _rows(x, Wa.k)
+    gp = None if gamma is None else _dev_f32(gamma, "gamma", (Wa.k,)).data_ptr()
+    out_a = _out(out_a, (nb, Wa.n), x)
+    out_b = _out(out_b, (nb, Wb.n), x)
+    _check(lib().q4_dual_gemv(Wa.cref(), Wb.cref(), x.data_ptr(), gp, float(eps), nb, out_a.data_ptr(),
+                              out_b.data_ptr(), _stream()), "q4_dual_gemv")
+    return out_a, out_b
+
+
+def q4_gus_nrm(Wg: Q4Weight, Wu: Q4Weight, x, gamma, eps: float, out=None):
+    x, nb = _rows(x, Wg.k)
+    gamma = _dev_f32(gamma, "gamma", (Wg.k,))
+    out = _out(out, (nb, Wg.n), x)
+    _check(lib().q4_gus_nrm(Wg.cref(), Wu.cref(), x.data_ptr(), gamma.data_ptr(), float(eps), nb,
+                            out.data_ptr(), _stream()), "q4_gus_nrm")
+    return out
+
+
+def q4_res_gemv(W: Q4Weight, x, r, out=None):
+    """``out = W x + r``; pass ``out=r`` for the in-place residual stream."""
+    x, nb = _rows(x, W.k)
+    r = _dev_f32(r, "r", (nb, W.n)) if _torch().is_tensor(r) and r.dim() == 2 else _dev_f32(r, "r").view(nb, W.n)
+    out = _out(out, (nb, W.n), x)
+    _check(lib().q4_res_gemv(W.cref(), x.data_ptr(), r.data_ptr(), nb, out.data_ptr(), _stream()),
+           "q4_res_gemv")
+    return out
+
+
+def q4_argmax_workspace_bytes(n: int, nb: int) -> int:
+    return int(lib().q4_argmax_workspace_bytes(n, nb))
+
+
+def q4_argmax(W: Q4Weight, x, gamma=None, eps: float = 0.0, want_val=False, want_logits=False,
+              workspace=None, idx=None, val=None, logits=None):
+    """Greedy argmax of the logits ``W xhat`` per activation row.  Returns
+    ``(idx int32[nb], val or None, logits or None)``."""
+    torch = _torch()
+    x, nb = _rows(x, W.k)
+    gp = None if gamma is None else _dev_f32(gamma, "gamma", (W.k,)).data_ptr()
+    ws_bytes = q4_argmax_workspace_bytes(W.n, nb)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    if idx is None:
+        idx = torch.empty(nb, dtype=torch.int32, device=x.device)
+    if want_val and val is None:
+        val = torch.empty(nb, dtype=torch.float32, device=x.device)
+    if want_logits and logits is None:
+        logits = torch.empty((nb, W.n), dtype=torch.float32, device=x.device)
+    _check(lib().q4_argmax(W.cref(), x.data_ptr(), gp, float(eps), nb, idx.data_ptr(),
+                           None if val is None else val.data_ptr(),
+                           None if logits is None else logits.data_ptr(),
+                           workspace.data_ptr(), workspace.numel(), _stream()), "q4_argmax")
+    return idx, val, logits

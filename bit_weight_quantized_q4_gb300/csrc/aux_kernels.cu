@@ -1,0 +1,101 @@
+// aux_kernels.cu -- the argmax fold (pass 2) and the activation group sums.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "q4_internal.h"
+
+namespace q4 {
+namespace dev {
+
+// Pass 2 of the greedy argmax (Module gpu, module sampling): one CTA per
+// activation row folds the per-group (max, index) pairs of pass 1.  Larger
+// value wins, ties go to the lower index; pass 1 already ranked NaN lowest.
+__global__ void __launch_bounds__(256) argmax_fold_kernel(const float *am_val, const int *am_idx,
+                                                          int groups, int32_t *idx, float *val) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ float sv[8];
+    __shared__ int si[8];
+    const int r = blockIdx.x, tid = threadIdx.x;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = tid; i < groups; i += 256) {
+        float v = am_val[(size_t)r * groups + i];
+        int j = am_idx[(size_t)r * groups + i];
+        if (v > bv || (v == bv && j < bi)) {
+            bv = v;
+            bi = j;
+        }
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
+        }
+    }
+    if ((tid & 31) == 0) {
+        sv[tid >> 5] = bv;
+        si[tid >> 5] = bi;
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (tid == 0) {
+        bv = sv[0];
+        bi = si[0];
+        for (int w = 1; w < 8; ++w)
+            if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) {
+                bv = sv[w];
+                bi = si[w];
+            }
+        idx[r] = bi;
+        if (val) val[r] = bv;
+    }
+}
+
+// gsum[r][g] = sum of x[r][32g .. 32g+31], added in ascending order
+// (Module gpu, Struct HalfSet: per-32 group sums of a row batch).
+__global__ void __launch_bounds__(256) group_sums_kernel(const float *x, int nb, int k, float *gsum) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int G = k / 32;
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    if (i < nb * G) {
+        const int r = i / G, gi = i - r * G;
+        const float *xr = x + (size_t)r * k + 32 * gi;
+        float s = 0.f;
+        for (int e = 0; e < 32; ++e) s += xr[e];
+        gsum[i] = s;
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace dev
+
+static int launch_pdl(const void *func, dim3 grid, dim3 block, void **args, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, func, args) == cudaSuccess ? 0 : -1;
+}
+
+int launch_argmax_fold(const float *am_val, const int *am_idx, int groups, int nb, int32_t *idx,
+                       float *val, void *stream) {
+    void *args[] = {(void *)&am_val, (void *)&am_idx, (void *)&groups, (void *)&idx, (void *)&val};
+    return launch_pdl((const void *)dev::argmax_fold_kernel, dim3(nb), dim3(256), args,
+                      (cudaStream_t)stream);
+}
+
+int launch_group_sums(const float *x, int nb, int k, float *gsum, void *stream) {
+    void *args[] = {(void *)&x, (void *)&nb, (void *)&k, (void *)&gsum};
+    const int total = nb * (k / 32);
+    return launch_pdl((const void *)dev::group_sums_kernel, dim3((total + 255) / 256), dim3(256), args,
+                      (cudaStream_t)stream);
+}
+
+}  // namespace q4

@@ -1,0 +1,254 @@
+// capi.cu -- the C entry points of libq4gemv: argument validation, the launch
+// plan, and the kernel launches.  Every check happens before anything is
+// enqueued; on any error nothing is launched.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/q4gemv.h"
+#include "q4_internal.h"
+
+namespace q4 {
+int launch_argmax_fold(const float *am_val, const int *am_idx, int groups, int nb, int32_t *idx,
+                       float *val, void *stream);
+int launch_group_sums(const float *x, int nb, int k, float *gsum, void *stream);
+}  // namespace q4
+
+namespace {
+
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool shape_ok(int32_t n, int32_t k) {
+    return n >= 1 && k >= 32 && k % 32 == 0 && k <= 65536 && n <= (1 << 24);
+}
+
+q4_status check_weight(const q4_weight *W) {
+    if (!W || !W->dev) return Q4_ERR_NULL;
+    if (W->fmt != Q4_FMT_Q4_0 && W->fmt != Q4_FMT_AFFINE) return Q4_ERR_UNSUPPORTED;
+    if (!shape_ok(W->n, W->k)) return Q4_ERR_SHAPE;
+    if (W->bytes < q4_packed_bytes(W->fmt, W->n, W->k)) return Q4_ERR_SHAPE;
+    if (!aligned16(W->dev)) return Q4_ERR_ALIGN;
+    return Q4_OK;
+}
+
+q4_status check_act(const void *p) {
+    if (!p) return Q4_ERR_NULL;
+    if (!aligned16(p)) return Q4_ERR_ALIGN;
+    return Q4_OK;
+}
+
+int num_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return sms;
+}
+
+#define Q4_TRY(expr)                      \
+    do {                                  \
+        q4_status _s = (expr);            \
+        if (_s != Q4_OK) return _s;       \
+    } while (0)
+
+q4::GemvParams base_params(const q4_weight *W0, const q4_weight *W1, int mode, const float *x,
+                           const float *gamma, float eps, int nb) {
+    q4::GemvParams p;
+    memset(&p, 0, sizeof(p));
+    p.w[0] = (const uint8_t *)W0->dev;
+    p.n[0] = W0->n;
+    p.tiles[0] = (int)q4::tiles_of(W0->n);
+    if (W1) {
+        p.w[1] = (const uint8_t *)W1->dev;
+        p.n[1] = W1->n;
+        p.tiles[1] = (int)q4::tiles_of(W1->n);
+    }
+    p.mode = mode;
+    p.T = mode == q4::MODE_SINGLE ? p.tiles[0]
+          : mode == q4::MODE_CONCAT ? p.tiles[0] + p.tiles[1]
+                                    : 2 * p.tiles[0];
+    p.K = W0->k;
+    p.C = (int)q4::chunks_of(W0->k);
+    p.nb = nb;
+    p.x = x;
+    p.gamma = gamma;
+    p.eps = eps;
+    return p;
+}
+
+q4_status run(const q4::GemvParams &p, int fmt, cudaStream_t stream, q4::Plan *plan_out = nullptr) {
+    const int sms = num_sms();
+    if (sms <= 0) return Q4_ERR_CUDA;
+    q4::Plan plan = q4::make_plan(fmt, p.T, p.C, p.nb, p.mode == q4::MODE_PAIRS, sms);
+    q4::GemvParams pp = p;
+    pp.TG = plan.TG;
+    pp.S = plan.S;
+    pp.Cs = plan.Cs;
+    pp.groups = plan.groups;
+    if (plan_out) *plan_out = plan;
+    cudaGetLastError();  // clear a stale error so the check below is ours
+    int rc = fmt == Q4_FMT_Q4_0 ? q4::launch_gemv_q4_0(pp, plan, stream)
+                                : q4::launch_gemv_affine(pp, plan, stream);
+    if (rc != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
+    return Q4_OK;
+}
+
+inline bool nb_ok(int32_t nb) { return nb >= 1 && nb <= q4::kMaxNb; }
+
+}  // namespace
+
+extern "C" {
+
+const char *q4_status_str(q4_status s) {
+    switch (s) {
+        case Q4_OK: return "Q4_OK";
+        case Q4_ERR_NULL: return "Q4_ERR_NULL: a required pointer is NULL";
+        case Q4_ERR_SHAPE: return "Q4_ERR_SHAPE: shape or byte count out of range";
+        case Q4_ERR_ALIGN: return "Q4_ERR_ALIGN: device pointer not 16-byte aligned";
+        case Q4_ERR_UNSUPPORTED: return "Q4_ERR_UNSUPPORTED: nb, format or combination not supported";
+        case Q4_ERR_WORKSPACE: return "Q4_ERR_WORKSPACE: workspace missing or too small";
+        case Q4_ERR_CUDA: return "Q4_ERR_CUDA: a CUDA runtime call failed";
+    }
+    return "unknown q4_status";
+}
+
+q4_status q4_plan(int32_t fmt, int32_t tiles, int32_t chunks, int32_t nb, int32_t pairs, int32_t sms,
+                  int32_t out[6]) {
+    if (!out) return Q4_ERR_NULL;
+    if (fmt != Q4_FMT_Q4_0 && fmt != Q4_FMT_AFFINE) return Q4_ERR_UNSUPPORTED;
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    if (tiles < 1 || chunks < 1 || sms < 1 || (pairs && (tiles & 1))) return Q4_ERR_SHAPE;
+    q4::Plan p = q4::make_plan(fmt, tiles, chunks, nb, pairs != 0, sms);
+    out[0] = p.TG;
+    out[1] = p.S;
+    out[2] = p.Cs;
+    out[3] = p.groups;
+    out[4] = p.ctas;
+    out[5] = (int32_t)p.smem;
+    return Q4_OK;
+}
+
+q4_status q4_group_sums(const float *x, int32_t nb, int32_t k, float *gsum, cudaStream_t stream) {
+    Q4_TRY(check_act(x));
+    Q4_TRY(check_act(gsum));
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    if (!shape_ok(1, k)) return Q4_ERR_SHAPE;
+    cudaGetLastError();
+    if (q4::launch_group_sums(x, nb, k, gsum, stream) != 0 || cudaGetLastError() != cudaSuccess)
+        return Q4_ERR_CUDA;
+    return Q4_OK;
+}
+
+q4_status q4_gemv(const q4_weight *W, const float *x, const float *gsum, int32_t nb, float *y,
+                  cudaStream_t stream) {
+    Q4_TRY(check_weight(W));
+    Q4_TRY(check_act(x));
+    Q4_TRY(check_act(y));
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    if (gsum && !aligned16(gsum)) return Q4_ERR_ALIGN;
+    q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, x, nullptr, 0.f, nb);
+    p.gsum = W->fmt == Q4_FMT_AFFINE ? gsum : nullptr;
+    p.epi = q4::EPI_STORE;
+    p.out[0] = y;
+    return run(p, W->fmt, stream);
+}
+
+q4_status q4_nrm_gemv(const q4_weight *W, const float *x, const float *gamma, float eps, int32_t nb,
+                      float *y, cudaStream_t stream) {
+    Q4_TRY(check_weight(W));
+    Q4_TRY(check_act(x));
+    Q4_TRY(check_act(gamma));
+    Q4_TRY(check_act(y));
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, x, gamma, eps, nb);
+    p.epi = q4::EPI_STORE;
+    p.out[0] = y;
+    return run(p, W->fmt, stream);
+}
+
+q4_status q4_dual_gemv(const q4_weight *Wa, const q4_weight *Wb, const float *x, const float *gamma,
+                       float eps, int32_t nb, float *ya, float *yb, cudaStream_t stream) {
+    Q4_TRY(check_weight(Wa));
+    Q4_TRY(check_weight(Wb));
+    Q4_TRY(check_act(x));
+    Q4_TRY(check_act(ya));
+    Q4_TRY(check_act(yb));
+    if (gamma && !aligned16(gamma)) return Q4_ERR_ALIGN;
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    if (Wa->fmt != Wb->fmt) return Q4_ERR_UNSUPPORTED;
+    if (Wa->k != Wb->k) return Q4_ERR_SHAPE;
+    q4::GemvParams p = base_params(Wa, Wb, q4::MODE_CONCAT, x, gamma, eps, nb);
+    p.epi = q4::EPI_STORE;
+    p.out[0] = ya;
+    p.out[1] = yb;
+    return run(p, Wa->fmt, stream);
+}
+
+q4_status q4_gus_nrm(const q4_weight *Wg, const q4_weight *Wu, const float *x, const float *gamma,
+                     float eps, int32_t nb, float *h, cudaStream_t stream) {
+    Q4_TRY(check_weight(Wg));
+    Q4_TRY(check_weight(Wu));
+    Q4_TRY(check_act(x));
+    Q4_TRY(check_act(gamma));
+    Q4_TRY(check_act(h));
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    if (Wg->fmt != Wu->fmt) return Q4_ERR_UNSUPPORTED;
+    if (Wg->k != Wu->k || Wg->n != Wu->n) return Q4_ERR_SHAPE;
+    q4::GemvParams p = base_params(Wg, Wu, q4::MODE_PAIRS, x, gamma, eps, nb);
+    p.epi = q4::EPI_SWIGLU;
+    p.out[0] = h;
+    return run(p, Wg->fmt, stream);
+}
+
+q4_status q4_res_gemv(const q4_weight *W, const float *x, const float *r_in, int32_t nb, float *y,
+                      cudaStream_t stream) {
+    Q4_TRY(check_weight(W));
+    Q4_TRY(check_act(x));
+    Q4_TRY(check_act(r_in));
+    Q4_TRY(check_act(y));
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, x, nullptr, 0.f, nb);
+    p.epi = q4::EPI_RESIDUAL;
+    p.out[0] = y;
+    p.res = r_in;
+    return run(p, W->fmt, stream);
+}
+
+size_t q4_argmax_workspace_bytes(int32_t n, int32_t nb) {
+    if (n < 1 || !nb_ok(nb)) return 0;
+    // one (value, index) pair per group and activation row; a group has at
+    // least one tile, so the tile count bounds the groups of any plan
+    const size_t groups = (size_t)q4::tiles_of(n);
+    return groups * (size_t)nb * 8u + 16u;
+}
+
+q4_status q4_argmax(const q4_weight *W, const float *x, const float *gamma, float eps, int32_t nb,
+                    int32_t *idx, float *val, float *logits, void *workspace, size_t ws_bytes,
+                    cudaStream_t stream) {
+    Q4_TRY(check_weight(W));
+    Q4_TRY(check_act(x));
+    if (!idx) return Q4_ERR_NULL;
+    if (!aligned16(idx) || (val && !aligned16(val)) || (logits && !aligned16(logits)) ||
+        (gamma && !aligned16(gamma)))
+        return Q4_ERR_ALIGN;
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    if (!workspace) return Q4_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return Q4_ERR_ALIGN;
+    if (ws_bytes < q4_argmax_workspace_bytes(W->n, nb)) return Q4_ERR_WORKSPACE;
+    q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, x, gamma, eps, nb);
+    p.epi = q4::EPI_ARGMAX;
+    p.out[0] = logits;
+    const size_t groups_max = (size_t)q4::tiles_of(W->n);
+    p.am_val = (float *)workspace;
+    p.am_idx = (int *)((uint8_t *)workspace + ((groups_max * nb * 4 + 15) & ~(size_t)15));
+    q4::Plan plan;
+    Q4_TRY(run(p, W->fmt, stream, &plan));
+    // the groups of this plan: pass 2 folds exactly those
+    // (run() recomputed p.groups into its own copy; the plan carries it)
+    cudaGetLastError();
+    if (q4::launch_argmax_fold(p.am_val, p.am_idx, plan.groups, nb, idx, val, stream) != 0 ||
+        cudaGetLastError() != cudaSuccess)
+        return Q4_ERR_CUDA;
+    return Q4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// gemv_launch.cuh -- host launcher for the dequant-in-GEMV kernel: picks the
+// n-tile count from nb, raises the dynamic shared-memory limit once per
+// device, and launches with programmatic dependent launch (and a cluster
+// when K is split).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "gemv_kernel.cuh"
+
+namespace q4 {
+
+template <int FMT, int NT>
+static int launch_nt(const GemvParams &p, const Plan &plan, cudaStream_t stream) {
+    auto kern = dev::gemv_kernel<FMT, NT>;
+    int devid = 0;
+    if (cudaGetDevice(&devid) != cudaSuccess) return -1;
+    static size_t smem_set[64] = {0};
+    if (devid < 64 && plan.smem > smem_set[devid]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem) !=
+            cudaSuccess)
+            return -1;
+        smem_set[devid] = plan.smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.ctas, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (plan.S > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)plan.S;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? 0 : -1;
+}
+
+template <int FMT>
+static int launch_gemv_fmt(const GemvParams &p, const Plan &plan, cudaStream_t stream) {
+    const int nt = (2 * p.nb + 7) / 8;  // 8-column n-tiles of (hi, lo) pairs
+    if (nt <= 1) return launch_nt<FMT, 1>(p, plan, stream);
+    if (nt <= 2) return launch_nt<FMT, 2>(p, plan, stream);
+    return launch_nt<FMT, 4>(p, plan, stream);
+}
+
+}  // namespace q4

@@ -1,0 +1,183 @@
+// repack.cpp -- host-side lossless re-layout of Q4_0 / affine-Q4 weights into
+// the coalesced device layout described in q4_internal.h, and its inverse.
+//
+// The pages re-lay block formats once at load time so that the GEMV reads
+// aligned vectors (honeycrisp/mod.rs: transpose_q8_blocks; crate
+// inferencelayer: q1_rp4_repack_src, the ROWPACK4 layout).  Here each 16-row x
+// 128-column tile chunk becomes one contiguous record whose 16-byte lanes are
+// exactly the tensor-core operand fragments of the kernel's warps.
+#include <string.h>
+
+#include "../../include/q4gemv.h"
+#include "q4_internal.h"
+
+namespace {
+
+inline uint32_t load_u32(const uint8_t *p) {
+    uint32_t v;
+    memcpy(&v, p, 4);
+    return v;
+}
+inline void store_u32(uint8_t *p, uint32_t v) { memcpy(p, &v, 4); }
+
+bool shape_ok(int32_t n, int32_t k) {
+    return n >= 1 && k >= 32 && k % 32 == 0 && k <= 65536 && n <= (1 << 24);
+}
+
+// Nibble q of element e (0..31) of block `blk` of a Q4_0 row (GGUF order).
+inline int q4_0_nib(const uint8_t *blk, int e) {
+    const uint8_t *qs = blk + 2;
+    return e < 16 ? (qs[e] & 15) : (qs[e - 16] >> 4);
+}
+
+// Nibble of element e of an affine row (even element in the low nibble).
+inline int affine_nib(const uint8_t *row, int64_t e) {
+    int b = row[e >> 1];
+    return (e & 1) ? (b >> 4) : (b & 15);
+}
+
+}  // namespace
+
+extern "C" size_t q4_packed_bytes(int32_t fmt, int32_t n, int32_t k) {
+    if ((fmt != Q4_FMT_Q4_0 && fmt != Q4_FMT_AFFINE) || !shape_ok(n, k)) return 0;
+    return (size_t)q4::tiles_of(n) * (size_t)q4::chunks_of(k) * (size_t)q4::rec_bytes(fmt);
+}
+
+extern "C" size_t q4_weight_bytes(int32_t fmt, int32_t n, int32_t k) {
+    if ((fmt != Q4_FMT_Q4_0 && fmt != Q4_FMT_AFFINE) || !shape_ok(n, k)) return 0;
+    return (size_t)n * (size_t)(k / 32) * (fmt == Q4_FMT_Q4_0 ? 18u : 20u);
+}
+
+// Generic packer: `get_q(row, blk, e)` gives the nibble of element e of a
+// block, `get_s` / `get_m` the 16-bit scale / min of a block.
+template <class GetQ, class GetS, class GetM>
+static void pack(int fmt, int32_t n, int32_t k, uint8_t *out, GetQ get_q, GetS get_s, GetM get_m) {
+    const int64_t T = q4::tiles_of(n), C = q4::chunks_of(k), B = k / 32;
+    const int rec = q4::rec_bytes(fmt);
+    const uint32_t pad_word = fmt == Q4_FMT_Q4_0 ? 0x88888888u : 0u;  // zero weights
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t c = 0; c < C; ++c) {
+            uint8_t *r = out + (t * C + c) * rec;
+            for (int h = 0; h < 2; ++h)
+                for (int g = 0; g < 8; ++g)
+                    for (int tp = 0; tp < 4; ++tp)
+                        for (int j = 0; j < 4; ++j) {
+                            int64_t row = t * 16 + h * 8 + g, blk = c * 4 + j;
+                            uint32_t word = pad_word;
+                            if (row < n && blk < B) {
+                                word = 0;
+                                for (int i = 0; i < 8; ++i)
+                                    word |= (uint32_t)get_q(row, blk, q4::nib_elem(tp, i)) << (4 * i);
+                            }
+                            store_u32(r + h * 512 + (4 * g + tp) * 16 + j * 4, word);
+                        }
+            for (int g = 0; g < 8; ++g)
+                for (int j = 0; j < 4; ++j) {
+                    int64_t blk = c * 4 + j, r0 = t * 16 + g, r1 = r0 + 8;
+                    uint32_t s0 = (r0 < n && blk < B) ? get_s(r0, blk) : 0;
+                    uint32_t s1 = (r1 < n && blk < B) ? get_s(r1, blk) : 0;
+                    store_u32(r + 1024 + g * 16 + j * 4, s0 | (s1 << 16));
+                    if (fmt == Q4_FMT_AFFINE) {
+                        uint32_t m0 = (r0 < n && blk < B) ? get_m(r0, blk) : 0;
+                        uint32_t m1 = (r1 < n && blk < B) ? get_m(r1, blk) : 0;
+                        store_u32(r + 1152 + g * 16 + j * 4, m0 | (m1 << 16));
+                    }
+                }
+        }
+    }
+}
+
+extern "C" q4_status q4_repack_q4_0(const void *host_blocks, int32_t n, int32_t k, void *host_out,
+                                    size_t out_bytes) {
+    if (!host_blocks || !host_out) return Q4_ERR_NULL;
+    if (!shape_ok(n, k)) return Q4_ERR_SHAPE;
+    if (out_bytes < q4_packed_bytes(Q4_FMT_Q4_0, n, k)) return Q4_ERR_SHAPE;
+    const uint8_t *src = (const uint8_t *)host_blocks;
+    const int64_t B = k / 32;
+    auto blk_ptr = [&](int64_t row, int64_t blk) { return src + (row * B + blk) * 18; };
+    pack(Q4_FMT_Q4_0, n, k, (uint8_t *)host_out,
+         [&](int64_t row, int64_t blk, int e) { return q4_0_nib(blk_ptr(row, blk), e); },
+         [&](int64_t row, int64_t blk) {
+             const uint8_t *b = blk_ptr(row, blk);
+             return (uint32_t)b[0] | ((uint32_t)b[1] << 8);
+         },
+         [&](int64_t, int64_t) { return 0u; });
+    return Q4_OK;
+}
+
+extern "C" q4_status q4_repack_affine(const uint8_t *nib, const uint16_t *s, const uint16_t *m,
+                                      int32_t n, int32_t k, void *host_out, size_t out_bytes) {
+    if (!nib || !s || !m || !host_out) return Q4_ERR_NULL;
+    if (!shape_ok(n, k)) return Q4_ERR_SHAPE;
+    if (out_bytes < q4_packed_bytes(Q4_FMT_AFFINE, n, k)) return Q4_ERR_SHAPE;
+    const int64_t B = k / 32;
+    pack(Q4_FMT_AFFINE, n, k, (uint8_t *)host_out,
+         [&](int64_t row, int64_t blk, int e) { return affine_nib(nib + row * (k / 2), blk * 32 + e); },
+         [&](int64_t row, int64_t blk) { return (uint32_t)s[row * B + blk]; },
+         [&](int64_t row, int64_t blk) { return (uint32_t)m[row * B + blk]; });
+    return Q4_OK;
+}
+
+// Walk every real (row, block) of a packed buffer and hand its 32 nibbles and
+// 16-bit scale / min to `put`.
+template <class Put>
+static void unpack(int fmt, int32_t n, int32_t k, const uint8_t *in, Put put) {
+    const int64_t T = q4::tiles_of(n), C = q4::chunks_of(k), B = k / 32;
+    const int rec = q4::rec_bytes(fmt);
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < C; ++c) {
+            const uint8_t *r = in + (t * C + c) * rec;
+            for (int h = 0; h < 2; ++h)
+                for (int g = 0; g < 8; ++g)
+                    for (int j = 0; j < 4; ++j) {
+                        int64_t row = t * 16 + h * 8 + g, blk = c * 4 + j;
+                        if (row >= n || blk >= B) continue;
+                        int q[32];
+                        for (int tp = 0; tp < 4; ++tp) {
+                            uint32_t word = load_u32(r + h * 512 + (4 * g + tp) * 16 + j * 4);
+                            for (int i = 0; i < 8; ++i) q[q4::nib_elem(tp, i)] = (word >> (4 * i)) & 15;
+                        }
+                        uint32_t sw = load_u32(r + 1024 + g * 16 + j * 4);
+                        uint16_t sv = (uint16_t)(h ? (sw >> 16) : (sw & 0xFFFF));
+                        uint16_t mv = 0;
+                        if (fmt == Q4_FMT_AFFINE) {
+                            uint32_t mw = load_u32(r + 1152 + g * 16 + j * 4);
+                            mv = (uint16_t)(h ? (mw >> 16) : (mw & 0xFFFF));
+                        }
+                        put(row, blk, q, sv, mv);
+                    }
+        }
+}
+
+extern "C" q4_status q4_unpack_q4_0(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,
+                                    void *host_blocks) {
+    if (!host_packed || !host_blocks) return Q4_ERR_NULL;
+    if (!shape_ok(n, k)) return Q4_ERR_SHAPE;
+    if (packed_bytes < q4_packed_bytes(Q4_FMT_Q4_0, n, k)) return Q4_ERR_SHAPE;
+    uint8_t *dst = (uint8_t *)host_blocks;
+    const int64_t B = k / 32;
+    unpack(Q4_FMT_Q4_0, n, k, (const uint8_t *)host_packed,
+           [&](int64_t row, int64_t blk, const int *q, uint16_t s, uint16_t) {
+               uint8_t *b = dst + (row * B + blk) * 18;
+               b[0] = (uint8_t)(s & 0xFF);
+               b[1] = (uint8_t)(s >> 8);
+               for (int i = 0; i < 16; ++i) b[2 + i] = (uint8_t)(q[i] | (q[i + 16] << 4));
+           });
+    return Q4_OK;
+}
+
+extern "C" q4_status q4_unpack_affine(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,
+                                      uint8_t *nib, uint16_t *s, uint16_t *m) {
+    if (!host_packed || !nib || !s || !m) return Q4_ERR_NULL;
+    if (!shape_ok(n, k)) return Q4_ERR_SHAPE;
+    if (packed_bytes < q4_packed_bytes(Q4_FMT_AFFINE, n, k)) return Q4_ERR_SHAPE;
+    const int64_t B = k / 32;
+    unpack(Q4_FMT_AFFINE, n, k, (const uint8_t *)host_packed,
+           [&](int64_t row, int64_t blk, const int *q, uint16_t sv, uint16_t mv) {
+               uint8_t *r = nib + row * (k / 2) + blk * 16;
+               for (int i = 0; i < 16; ++i) r[i] = (uint8_t)(q[2 * i] | (q[2 * i + 1] << 4));
+               s[row * B + blk] = sv;
+               m[row * B + blk] = mv;
+           });
+    return Q4_OK;
+}

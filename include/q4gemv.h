@@ -1,0 +1,183 @@
+/*
+ * q4gemv.h -- C ABI of libq4gemv: weight-only 4-bit dequant-in-GEMV over a
+ * small batch of activation rows, fused with its decode-step neighbours.
+ *
+ * Sources for the operations (page title, then the item on it):
+ *  - crate inferencelayer (docs.rs), Functions: gemv_q4_k_lcpp_src (Q4 GEMV,
+ *    1-16 activation columns, fp32 accumulation), q4_0_to_q8_0n (Q4_0 weight
+ *    = d * (nib - 8)), gemv_q1_k_lcpp_src (a Q4_0 block is 18 bytes per 32
+ *    weights), gemm_q4_splitk_reduce_src (split-K partials folded in a fixed
+ *    slice order).
+ *  - Module gpu (qwen4_exp, docs.cherenkov.io): Struct Q (affine-Q4
+ *    projection), Struct HalfSet (per-32 activation group sums feed the
+ *    multi-row Q4 matvecs), Constant MAX_NB (rows per step), module
+ *    sampling (logits projection and greedy argmax).
+ *  - honeycrisp/mod.rs (cyber.page): forward_decode_fused_layers (Q matmul
+ *    with inline input_norm; K+V dual with inline input_norm; matmul +
+ *    residual; post_norm + gate + up + silu), fused_ffn_residual, Op::RmsNorm.
+ *
+ * Conventions for every call below:
+ *  - Memory: weights, activations, outputs and workspaces are DEVICE
+ *    pointers owned by the caller; the library allocates nothing, keeps no
+ *    pointer after a call returns and has no host-visible state.  Host
+ *    pointers appear only in the repack/unpack calls and are marked "host".
+ *  - Layout: activations are row-major [nb][k] fp32, outputs [nb][n] fp32
+ *    (row r of a batch is one decode position).  1 <= nb <= 16, k % 32 == 0,
+ *    1 <= n, k <= 65536 (one packed weight must stay below 2^31 bytes).
+ *  - Alignment: every device pointer must be 16-byte aligned.
+ *  - Errors: arguments are validated on the host before anything is
+ *    launched; on any error nothing is launched and a status other than
+ *    Q4_OK is returned.  A launch failure returns Q4_ERR_CUDA (from
+ *    cudaGetLastError).  Kernels never trap and never spin on a flag.
+ *  - Asynchrony: calls enqueue work on `stream` and return; they never
+ *    synchronise the host.  Kernels are launched with programmatic
+ *    dependent launch: each waits for the preceding kernel in the stream
+ *    before it reads activations or writes outputs, and only reads weights
+ *    (which must not be written concurrently) before that point.
+ *  - Aliasing: outputs must not overlap inputs, except y == r in
+ *    q4_res_gemv.
+ *  - Numerics: fp32 accumulation of exact dequantised weights against the
+ *    activations carried to about 22 significant bits; per output
+ *    |y - y_exact| <= 1e-3 * sum_k |w_k| |x_k| + 1e-6 for finite inputs.
+ */
+#ifndef Q4GEMV_H
+#define Q4GEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    Q4_OK = 0,
+    Q4_ERR_NULL = 1,          /* a required pointer is NULL */
+    Q4_ERR_SHAPE = 2,         /* n, k or a byte count is out of range / inconsistent */
+    Q4_ERR_ALIGN = 3,         /* a device pointer is not 16-byte aligned */
+    Q4_ERR_UNSUPPORTED = 4,   /* nb outside 1..16, unknown format, mixed formats */
+    Q4_ERR_WORKSPACE = 5,     /* workspace missing or smaller than required */
+    Q4_ERR_CUDA = 6           /* a CUDA runtime call failed */
+} q4_status;
+
+typedef enum {
+    Q4_FMT_Q4_0 = 0,    /* 32 weights: fp16 scale d + 16 nibble bytes; w = d*(q-8) */
+    Q4_FMT_AFFINE = 1   /* 32 weights: bf16 scale s, bf16 min m, 16 nibble bytes; w = s*q + m */
+} q4_format;
+
+/* A non-owning view of one repacked weight matrix in device memory.
+ * `dev` points to q4_packed_bytes(fmt, n, k) bytes written by a repack call
+ * (copied to the device by the caller); `bytes` is that size. */
+typedef struct {
+    int32_t fmt;        /* q4_format */
+    int32_t n;          /* output rows */
+    int32_t k;          /* input length, multiple of 32 */
+    const void *dev;    /* device pointer, 16-byte aligned */
+    size_t bytes;       /* size of the packed buffer */
+} q4_weight;
+
+/* Size in bytes of the device layout of an n x k weight (0 on bad shape).
+ * The layout is 16-row tiles x 128-column chunks; rows are padded to a
+ * multiple of 16 and columns to a multiple of 128 with zero-valued weights,
+ * so the size may exceed the algorithmic 18 (Q4_0) or 20 (affine) bytes per
+ * 32 weights when n % 16 or k % 128 is not zero. */
+size_t q4_packed_bytes(int32_t fmt, int32_t n, int32_t k);
+
+/* Algorithmic weight bytes of an n x k matrix: 18 (Q4_0) or 20 (affine) per
+ * 32 weights; 0 on bad shape. */
+size_t q4_weight_bytes(int32_t fmt, int32_t n, int32_t k);
+
+/* Host -> host, lossless, deterministic repack of Q4_0 blocks into the
+ * device layout.  host_blocks: [n][k/32] blocks of 18 bytes (fp16 d little
+ * endian, then 16 bytes; byte i holds element i in its low nibble and
+ * element i+16 in its high nibble).  host_out: q4_packed_bytes(...) bytes. */
+q4_status q4_repack_q4_0(const void *host_blocks, int32_t n, int32_t k,
+                         void *host_out, size_t out_bytes);
+
+/* Host -> host repack of affine-Q4 weights.  nib: [n][k/2] bytes, byte i
+ * holding element 2i (low nibble) and 2i+1 (high nibble); s, m: [n][k/32]
+ * bf16 bit patterns; host_out: q4_packed_bytes(...) bytes. */
+q4_status q4_repack_affine(const uint8_t *nib, const uint16_t *s, const uint16_t *m,
+                           int32_t n, int32_t k, void *host_out, size_t out_bytes);
+
+/* Inverse of q4_repack_q4_0 (host -> host); used to check the round trip. */
+q4_status q4_unpack_q4_0(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,
+                         void *host_blocks);
+
+/* Inverse of q4_repack_affine (host -> host). */
+q4_status q4_unpack_affine(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,
+                           uint8_t *nib, uint16_t *s, uint16_t *m);
+
+/* Per-32 group sums of a row batch (Module gpu, Struct HalfSet):
+ * gsum[r][g] = fp32 sum of x[r][32g .. 32g+31], added in ascending order.
+ * x: [nb][k] device fp32; gsum: [nb][k/32] device fp32. */
+q4_status q4_group_sums(const float *x, int32_t nb, int32_t k, float *gsum, cudaStream_t stream);
+
+/* y[r][i] = sum_k w[i][k] * x[r][k]   (dequant-in-GEMV).
+ * x: [nb][k]; y: [nb][n].  gsum: affine weights only, [nb][k/32] group sums
+ * of x as q4_group_sums writes them, or NULL to have the kernel compute them
+ * (ignored for Q4_0). */
+q4_status q4_gemv(const q4_weight *W, const float *x, const float *gsum, int32_t nb,
+                  float *y, cudaStream_t stream);
+
+/* RMSNorm prologue then GEMV (honeycrisp/mod.rs, forward_decode_fused_layers,
+ * "Q matmul with inline input_norm"):
+ *   xhat[r][k] = x[r][k] / sqrt(mean_k x[r][k]^2 + eps) * gamma[k];
+ *   y[r][i] = sum_k w[i][k] * xhat[r][k].
+ * gamma: [k] device fp32. */
+q4_status q4_nrm_gemv(const q4_weight *W, const float *x, const float *gamma, float eps,
+                      int32_t nb, float *y, cudaStream_t stream);
+
+/* Two weight streams over one (optionally RMS-normed) activation batch in
+ * one launch (forward_decode_fused_layers, K+V dual with inline input_norm):
+ *   ya = Wa * xhat, yb = Wb * xhat, xhat = x when gamma is NULL.
+ * Wa and Wb must have the same format and k.  ya: [nb][Wa.n], yb: [nb][Wb.n]. */
+q4_status q4_dual_gemv(const q4_weight *Wa, const q4_weight *Wb, const float *x,
+                       const float *gamma, float eps, int32_t nb, float *ya, float *yb,
+                       cudaStream_t stream);
+
+/* RMSNorm, gate and up projections and the SwiGLU epilogue in one launch
+ * (forward_decode_fused_layers, post_norm + gate + up + silu; fused_ffn_residual
+ * step 4):  h[r][i] = silu(g) * u,  g = (Wg xhat)[r][i], u = (Wu xhat)[r][i],
+ * silu(t) = t / (1 + exp(-t)).  Wg and Wu: same format, n and k.  h: [nb][n]. */
+q4_status q4_gus_nrm(const q4_weight *Wg, const q4_weight *Wu, const float *x,
+                     const float *gamma, float eps, int32_t nb, float *h, cudaStream_t stream);
+
+/* GEMV with a residual-add epilogue (forward_decode_fused_layers, fused
+ * matmul + residual):  y[r][i] = sum_k w[i][k] x[r][k] + r_in[r][i].
+ * r_in, y: [nb][n]; y may equal r_in (in-place residual stream). */
+q4_status q4_res_gemv(const q4_weight *W, const float *x, const float *r_in, int32_t nb,
+                      float *y, cudaStream_t stream);
+
+/* Workspace bytes q4_argmax needs for an n-row logits projection and nb rows. */
+size_t q4_argmax_workspace_bytes(int32_t n, int32_t nb);
+
+/* Logits projection (optionally behind an RMSNorm when gamma is not NULL)
+ * and greedy argmax per activation row (Module gpu, module sampling), in two
+ * passes: pass 1 computes the logits tile by tile and writes one (max, index)
+ * pair per thread-block group to `workspace`; pass 2 folds those pairs in
+ * group order.  Ties go to the lowest index; a NaN logit ranks below every
+ * number.  idx: [nb] int32 (required); val: [nb] the maximum logit, or NULL;
+ * logits: [nb][n] all logits, or NULL.  workspace: device memory of at least
+ * q4_argmax_workspace_bytes(n, nb) bytes, no initialisation needed. */
+q4_status q4_argmax(const q4_weight *W, const float *x, const float *gamma, float eps,
+                    int32_t nb, int32_t *idx, float *val, float *logits,
+                    void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Launch plan the library uses for a GEMV-shaped call (host-only; exposed
+ * for tests and tuning).  tiles: 16-row tiles of the launch, chunks: 128-k
+ * chunks per row, pairs: 1 when tiles come in gate/up pairs, num_sms:
+ * multiprocessors of the device.  out[0..5] = tiles per group, K-split
+ * (cluster size), chunks per K-slice, groups, CTAs, dynamic shared bytes. */
+q4_status q4_plan(int32_t fmt, int32_t tiles, int32_t chunks, int32_t nb, int32_t pairs,
+                  int32_t num_sms, int32_t out[6]);
+
+/* Human-readable name of a status. */
+const char *q4_status_str(q4_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4GEMV_H */

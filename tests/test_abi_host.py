@@ -1,0 +1,174 @@
+"""Host-side tests of libq4gemv that need no GPU: the library loads and
+exports every function its header declares, the repack is lossless, the
+launch planner keeps its invariants, and invalid arguments are rejected
+before anything is launched."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import bit_weight_quantized_q4_gb300 as q4
+import q4_workloads as wl
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    q4.build()
+
+
+def test_exports_every_declared_symbol():
+    L = q4.lib()
+    names = q4.header_functions()
+    assert len(names) >= 16
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings():
+    L = q4.lib()
+    for s in range(7):
+        assert L.q4_status_str(s).decode().startswith(q4.STATUS[s])
+
+
+@pytest.mark.parametrize("n,k", [(1, 32), (16, 128), (17, 96), (33, 160), (100, 544), (64, 1024)])
+def test_repack_roundtrip_random(n, k):
+    rng = np.random.default_rng(n * 1000 + k)
+    H = wl.draw_q4_0(rng, n, k)
+    P = q4.repack_q4_0(H.blocks, n, k)
+    assert P.size == q4.packed_bytes(0, n, k)
+    assert np.array_equal(q4.unpack_q4_0(P, n, k), H.blocks)
+    A = wl.draw_affine(rng, n, k)
+    P = q4.repack_affine(A.nib, A.s, A.m, n, k)
+    nib, s, m = q4.unpack_affine(P, n, k)
+    assert np.array_equal(nib, A.nib) and np.array_equal(s, A.s) and np.array_equal(m, A.m)
+
+
+def test_repack_roundtrip_edge_values():
+    # scales: +-0, smallest subnormal, largest finite, inf; every nibble value
+    n, k = 5, 64
+    q = np.tile(np.arange(16, dtype=np.uint8), (n, k // 16))
+    d = np.array([[0x0000, 0x8000], [0x0001, 0x7BFF], [0xFBFF, 0x7C00], [0x3C00, 0xBC00], [0x0400, 0x03FF]],
+                 dtype=np.uint16)
+    blocks = wl.pack_q4_0(q, d)
+    P = q4.repack_q4_0(blocks, n, k)
+    assert np.array_equal(q4.unpack_q4_0(P, n, k), blocks)
+
+
+def test_packed_sizes_and_padding():
+    # full tiles and chunks: the packed size is the algorithmic size plus
+    # nothing for Q4_0 payload+scales (1152 B per 16x128 = 18 B per 32 weights)
+    assert q4.packed_bytes(0, 14336, 4096) == q4.weight_bytes(0, 14336, 4096) == 33030144
+    assert q4.packed_bytes(1, 14336, 4096) == q4.weight_bytes(1, 14336, 4096) == 36700160
+    assert q4.weight_bytes(0, 1, 32) == 18 and q4.weight_bytes(1, 1, 32) == 20
+    assert q4.packed_bytes(0, 1, 32) == 1152       # one padded tile chunk
+    assert q4.packed_bytes(0, 0, 32) == 0 and q4.packed_bytes(0, 4, 33) == 0
+    assert q4.packed_bytes(2, 4, 32) == 0
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("tiles,chunks,pairs", [(896, 32, False), (1024, 16, True), (128, 16, False),
+                                                (64, 16, False), (4096, 16, False), (1, 1, False),
+                                                (2, 1, True), (7, 3, False), (128, 64, False)])
+@pytest.mark.parametrize("nb", [1, 3, 8, 16])
+def test_plan_invariants(fmt, tiles, chunks, pairs, nb):
+    p = q4.plan(fmt, tiles, chunks, nb, pairs, 152)
+    assert 1 <= p["S"] <= 8 and (p["S"] & (p["S"] - 1)) == 0
+    assert p["S"] * p["Cs"] >= chunks and p["Cs"] >= 1
+    assert p["groups"] * p["TG"] >= tiles and (p["groups"] - 1) * p["TG"] < tiles
+    assert p["ctas"] == p["groups"] * p["S"]
+    assert p["smem"] <= 227 * 1024
+    assert p["TG"] * nb <= max(64, 2 * nb)
+    if pairs:
+        assert p["TG"] % 2 == 0
+    # the activation slice fits the staging budget
+    assert 4 * nb * p["Cs"] * 128 <= 64 * 1024 or p["S"] == 8
+
+
+def test_plan_rejects_bad_arguments():
+    with pytest.raises(q4.Q4Error):
+        q4.plan(0, 0, 1, 1, False, 152)
+    with pytest.raises(q4.Q4Error):
+        q4.plan(0, 3, 1, 1, True, 152)    # pairs need an even tile count
+    with pytest.raises(q4.Q4Error):
+        q4.plan(0, 8, 1, 17, False, 152)
+    with pytest.raises(q4.Q4Error):
+        q4.plan(5, 8, 1, 1, False, 152)
+
+
+def _cw(fmt=0, n=16, k=64, dev=0x1000, nbytes=None):
+    if nbytes is None:
+        nbytes = q4.packed_bytes(fmt, n, k)
+    return q4._CWeight(fmt, n, k, dev, nbytes)
+
+
+A = 0x10000    # a 16-byte aligned fake device address: never dereferenced, since
+               # every case below fails validation before any CUDA call
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("null_weight", 1), ("null_x", 1), ("null_y", 1), ("bad_fmt", 4), ("bad_k", 2), ("bad_n", 2),
+    ("small_bytes", 2), ("misaligned_w", 3), ("misaligned_x", 3), ("nb0", 4), ("nb17", 4),
+])
+def test_gemv_validation(case, expect):
+    L = q4.lib()
+    W = _cw()
+    x, y, nb = A, A + 4096, 1
+    if case == "null_weight":
+        W.dev = None
+    elif case == "null_x":
+        x = None
+    elif case == "null_y":
+        y = None
+    elif case == "bad_fmt":
+        W.fmt = 7
+    elif case == "bad_k":
+        W.k = 48
+    elif case == "bad_n":
+        W.n = 0
+    elif case == "small_bytes":
+        W.bytes = 100
+    elif case == "misaligned_w":
+        W.dev = A + 8
+    elif case == "misaligned_x":
+        x = A + 4
+    elif case == "nb0":
+        nb = 0
+    elif case == "nb17":
+        nb = 17
+    assert L.q4_gemv(ctypes.byref(W), x, None, nb, y, None) == expect
+
+
+def test_fused_validation():
+    L = q4.lib()
+    Wa, Wb = _cw(0, 16, 64), _cw(1, 16, 64)
+    # mixed formats
+    assert L.q4_dual_gemv(ctypes.byref(Wa), ctypes.byref(Wb), A, None, 0.0, 1, A, A, None) == 4
+    assert L.q4_gus_nrm(ctypes.byref(Wa), ctypes.byref(Wb), A, A, 1e-6, 1, A, None) == 4
+    # mismatched k / n
+    Wc = _cw(0, 16, 96)
+    assert L.q4_dual_gemv(ctypes.byref(Wa), ctypes.byref(Wc), A, None, 0.0, 1, A, A, None) == 2
+    Wd = _cw(0, 32, 64)
+    assert L.q4_gus_nrm(ctypes.byref(Wa), ctypes.byref(Wd), A, A, 1e-6, 1, A, None) == 2
+    # gamma is required by nrm and gus
+    assert L.q4_nrm_gemv(ctypes.byref(Wa), A, None, 1e-6, 1, A, None) == 1
+    assert L.q4_gus_nrm(ctypes.byref(Wa), ctypes.byref(Wa), A, None, 1e-6, 1, A, None) == 1
+    # residual pointer required
+    assert L.q4_res_gemv(ctypes.byref(Wa), A, None, 1, A, None) == 1
+    # argmax: workspace missing / too small / misaligned, idx missing
+    ws = q4.q4_argmax_workspace_bytes(16, 1)
+    assert ws > 0
+    assert L.q4_argmax(ctypes.byref(Wa), A, None, 0.0, 1, A, None, None, None, ws, None) == 5
+    assert L.q4_argmax(ctypes.byref(Wa), A, None, 0.0, 1, A, None, None, A, ws - 1, None) == 5
+    assert L.q4_argmax(ctypes.byref(Wa), A, None, 0.0, 1, A, None, None, A + 4, ws, None) == 3
+    assert L.q4_argmax(ctypes.byref(Wa), A, None, 0.0, 1, None, None, None, A, ws, None) == 1
+    # group sums
+    assert L.q4_group_sums(A, 1, 48, A, None) == 2
+    assert L.q4_group_sums(None, 1, 64, A, None) == 1
+
+
+def test_repack_validation():
+    L = q4.lib()
+    buf = np.zeros(4096, np.uint8)
+    assert L.q4_repack_q4_0(None, 1, 32, buf.ctypes.data, buf.size) == 1
+    assert L.q4_repack_q4_0(buf.ctypes.data, 1, 33, buf.ctypes.data, buf.size) == 2
+    assert L.q4_repack_q4_0(buf.ctypes.data, 1, 32, buf.ctypes.data, 10) == 2
