@@ -1,0 +1,543 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q4 dequant-in-GEMV hot path on the synthetic decode step.
+
+One step = one pass of the whole fused path over one batch: 16 layers of
+(RMSNorm+q, dual RMSNorm+k/v, o+residual, RMSNorm+gate/up+SwiGLU,
+down+residual) then RMSNorm + a 65536 x 2048 logits projection + argmax,
+all Q4_0, hidden 2048, kv 512, intermediate 8192, nb = 1, replayed as one
+CUDA graph of 82 kernels.  622,854,144 weight bytes stream from HBM per step
+(more than L2 holds), so every step reads cold weights.
+
+Prints ONE JSON line (rank 0).  ``value`` is weight GB/s of the whole job
+(all ranks), ``ms_per_step`` the step time; ``e2e`` repeats the measure with
+the step's inputs copied from pinned host memory and its result read back
+inside the timed region; ``roofline`` is the SwiGLU MLP kernel (the largest
+share of the step) against the measured HBM peak; ``cpu_baseline`` is the f64
+C oracle on the host.  ``--impl reference`` times the oracle itself as the
+reference arm.  Multi-GPU (torchrun) runs independent replicas (weak
+scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q4 GEMV weight GB/s (fraction of GB300 HBM peak) and µs per fused decode-step"
+WORKLOAD = ("synthetic 16-layer Q4_0 decode step, nb=1, hidden 2048, kv 512, intermediate 8192, "
+            "logits 65536 x 2048 + argmax, one CUDA graph")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=16)
+    ap.add_argument("--no-kernels", action="store_true", help="skip the per-shape kernel table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, world: int, device="cpu") -> float:
+    """Maximum of a per-rank float over all ranks (the job's wall time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def job_rate(bytes_per_step: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job weight GB/s: every rank streams its own replica's weights."""
+    return bytes_per_step * steps * world / max_seconds / 1e9
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, power, reasons, n = [], [], [], set(), 0
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        top = max(power) if power else 0.0
+        loaded = [s for s, p in zip(sm, power) if p >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": n, "power_w_max": top}
+
+
+# ----------------------------------------------------------------- peaks
+
+def measured_peaks() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: a profile summary taken on other sources is stale."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_weight_quantized_q4_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag: str) -> float | None:
+    """DRAM bytes per launch from profiles/traffic.txt (lines of
+    ``tag source_hash=<h> dram_bytes_per_launch=<n>``), if it was taken on the
+    current kernel sources, else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(p) as f:
+            for ln in f:
+                parts = ln.split()
+                if not parts or parts[0] != kernel_tag:
+                    continue
+                kv = dict(x.split("=", 1) for x in parts[1:] if "=" in x)
+                if kv.get("source_hash") != kernel_source_hash():
+                    return None
+                return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+    return None
+
+
+# ------------------------------------------------------------ our arm
+
+def time_replays(graph, steps: int, stream) -> float:
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+class _GraphEvent:
+    """A timing event that becomes an event-record node when recorded during
+    stream capture (cudaEventRecordExternal), via torch when it supports it,
+    else through the CUDA runtime directly."""
+    _rt = None
+
+    def __init__(self):
+        import torch
+        try:
+            self.ev = torch.cuda.Event(enable_timing=True, external=True)
+            self.raw = None
+        except TypeError:
+            self.ev = None
+            rt = _GraphEvent.runtime()
+            h = ctypes.c_void_p()
+            if rt.cudaEventCreate(ctypes.byref(h)) != 0:
+                raise RuntimeError("cudaEventCreate failed")
+            self.raw = h
+
+    @classmethod
+    def runtime(cls):
+        if cls._rt is None:
+            import glob
+            import torch
+            names = ["libcudart.so.13", "libcudart.so"]
+            base = os.path.dirname(torch.__file__)
+            names += glob.glob(os.path.join(base, "..", "nvidia", "cu13", "lib", "libcudart.so*"))
+            names += glob.glob("/usr/local/cuda/lib64/libcudart.so*")
+            for n in names:
+                try:
+                    cls._rt = ctypes.CDLL(n)
+                    break
+                except OSError:
+                    continue
+            if cls._rt is None:
+                raise RuntimeError("libcudart not found")
+        return cls._rt
+
+    def record(self):
+        import torch
+        if self.ev is not None:
+            self.ev.record()
+            return
+        st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        if self.runtime().cudaEventRecordWithFlags(self.raw, st, 1) != 0:
+            raise RuntimeError("cudaEventRecordWithFlags failed")
+
+    def elapsed_ms(self, other) -> float:
+        if self.ev is not None:
+            return self.ev.elapsed_time(other.ev)
+        ms = ctypes.c_float()
+        if self.runtime().cudaEventElapsedTime(ctypes.byref(ms), self.raw, other.raw) != 0:
+            raise RuntimeError("cudaEventElapsedTime failed")
+        return ms.value
+
+
+def dominant_kernel_timing(step, steps: int):
+    """Average duration of the SwiGLU MLP kernel (gate+up, 2 x 8192 x 2048
+    Q4_0) inside the step, from timing events captured around each of its
+    launches in a graph of the step, replayed `steps` times."""
+    import torch
+    evs = {}
+
+    def around(name, l, fn):
+        if name != "gus":
+            return fn()
+        a, b = _GraphEvent(), _GraphEvent()
+        a.record()
+        fn()
+        b.record()
+        evs[l] = (a, b)
+
+    g = step.capture(around=around)
+    durs = []
+    for _ in range(steps):
+        g.replay()
+        torch.cuda.synchronize()
+        durs += [a.elapsed_ms(b) * 1e3 for a, b in evs.values()]
+    return statistics.mean(durs), len(durs)
+
+
+def e2e_timing(step, graph, steps: int, warmup: int):
+    """Step inputs (x and the attention stand-ins) copied in from pinned host
+    memory and the argmax read back, inside the timed region."""
+    import torch
+    srcs = [step.x_in] + [L.attn for L in step.layers]
+    host = [t.cpu().pin_memory() for t in srcs]
+    idx_h = torch.empty(step.idx.shape, dtype=step.idx.dtype).pin_memory()
+    val_h = torch.empty(step.val.shape, dtype=step.val.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for d, h in zip(srcs, host):
+            d.copy_(h, non_blocking=True)
+        graph.replay()
+        idx_h.copy_(step.idx, non_blocking=True)
+        val_h.copy_(step.val, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = idx_h.numel() * idx_h.element_size() + val_h.numel() * val_h.element_size()
+    return e0.elapsed_time(e1) / 1e3, h2d, d2h
+
+
+def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
+    """Per-shape cold timings of single calls: a graph of `reps` back-to-back
+    calls over rotating weight copies whose total exceeds 3x L2."""
+    import numpy as np
+    import torch
+
+    import bit_weight_quantized_q4_gb300 as q4
+    import q4_workloads as wl
+    out = {}
+    rng = np.random.default_rng(3)
+    n, k = 14336, 4096
+
+    def bench_calls(weights, fn):
+        g = torch.cuda.CUDAGraph()
+        fn(weights[0])
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                fn(weights[i % len(weights)])
+        g.replay()
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(3):
+            t = time_replays(g, 1, torch.cuda.current_stream())
+            best = t if best is None else min(best, t)
+        return best / reps
+
+    for fmt in ("affine", "q4_0"):
+        H = wl.draw_affine(rng, n, k) if fmt == "affine" else wl.draw_q4_0(rng, n, k)
+        W0 = (q4.Q4Weight.from_affine(H.nib, H.s, H.m, n, k, device) if fmt == "affine"
+              else q4.Q4Weight.from_q4_0(H.blocks, n, k, device))
+        copies = max(2, -(-3 * l2_bytes // W0.nbytes))
+        host = W0.tensor.cpu().numpy()
+        Ws = [W0] + [q4.Q4Weight(W0.fmt, n, k, host, device) for _ in range(copies - 1)]
+        for nb in ((1, 2, 4, 8, 16) if fmt == "affine" else (1,)):
+            x = torch.from_numpy(wl.draw_x(rng, nb, k)).to(device)
+            y = torch.empty((nb, n), dtype=torch.float32, device=device)
+            t = bench_calls(Ws, lambda W: q4.q4_gemv(W, x, out=y))
+            gbs = W0.weight_bytes / t / 1e9
+            out["%s_n%d_k%d_nb%d" % (fmt, n, k, nb)] = {"us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1),
+                                                      "frac_of_hbm": round(gbs / peak, 4)}
+        del Ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import bit_weight_quantized_q4_gb300 as q4
+    import q4_workloads as wl
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    q4.build()
+    q4.lib()
+
+    cfg = wl.cfg4(layers=args.layers)
+    step = DecodeStep(cfg, device)
+    wbytes = step.weight_bytes
+    graph = step.capture()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(device)
+    uuid = str(getattr(props, "uuid", "") or "")
+    uuid = (uuid if uuid.startswith("GPU-") else "GPU-" + uuid) if uuid else None
+    clocks = ClockSampler(uuid).start()
+    barrier(world)
+    secs = time_replays(graph, args.steps, stream)
+    barrier(world)
+    clk = clocks.stop()
+    max_secs = reduce_max(secs, world, device)
+    value = job_rate(wbytes, args.steps, world, max_secs)
+    ms_per_step = max_secs * 1e3 / args.steps
+
+    peak, peak_src = measured_peaks()
+    gus_us, gus_n = dominant_kernel_timing(step, max(3, min(args.steps, 10)))
+    L0 = step.layers[0]
+    gus_bytes = L0.Wg.weight_bytes + L0.Wu.weight_bytes
+    achieved = gus_bytes / (gus_us * 1e-6) / 1e9
+
+    e2e_secs, h2d, d2h = e2e_timing(step, graph, args.steps, max(1, args.warmup))
+    e2e_max = reduce_max(e2e_secs, world, device)
+
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0)
+    kernels = None
+    if rank == 0 and world == 1 and not args.no_kernels:
+        kernels = kernel_table(device, l2 or 128 << 20, peak)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline_sample(cfg, wbytes, budget_s=12.0)
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "frac_of_hbm_peak": round(value / world / peak, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "precision": "Q4_0 weights dequantised exactly to f16; activations as f16 hi+lo pairs; fp32 accumulate",
+        "data": "synthetic (seeded PCG64; q~U{0..15}, d~U[0.005,0.02] fp16, x~N(0,1), gamma=1+0.1N(0,1))",
+        "config": {"workload": WORKLOAD, "layers": args.layers, "nb": 1, "kernels_per_step": step.n_kernels,
+                   "weight_bytes_per_step": wbytes,
+                   "l2": "inputs larger than L2: %d weight bytes per step vs %d B L2" % (wbytes, l2),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "gpu_launches": step.n_kernels * args.steps,
+        "clocks": clk,
+        "e2e": {"value": round(job_rate(wbytes, args.steps, world, e2e_max), 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_max * 1e3 / args.steps, 5),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "roofline": {"kernel": "q4_gus_nrm (RMSNorm + gate/up 2 x 8192 x 2048 Q4_0 + SwiGLU)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src + " (MEASURED_PEAKS hbm_gbs)",
+                     "algorithmic_bytes_per_launch": gus_bytes, "launch_us": round(gus_us, 3),
+                     "launches_timed": gus_n, "traffic": profiled_traffic("gus_nrm_8192x2048")},
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if kernels is not None:
+        line["kernels"] = kernels
+    return line
+
+
+# ---------------------------------------------------------- oracle arms
+
+def cpu_baseline_sample(cfg, wbytes: int, budget_s: float = 12.0) -> dict:
+    """The f64 C oracle (single thread) on whole decode steps of the same
+    workload, repeated until about `budget_s` seconds have passed."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.decode_step(cfg)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 10:
+            break
+    return {"value": round(wbytes * n / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d full decode step(s) (%d weight bytes each) in the f64 C oracle, 1 thread, %.1f s"
+                      % (n, wbytes, el)}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the f64 C oracle on the host, one full decode step of
+    the same workload per timed step (rank 0 only)."""
+    if rank != 0:
+        return None
+    import oracle
+    import q4_workloads as wl
+    oracle.build()
+    cfg = wl.cfg4(layers=args.layers)
+    wbytes = wl.decode_step_weight_bytes(layers=args.layers)
+    for _ in range(args.warmup):
+        oracle.decode_step(cfg)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode_step(cfg)
+    el = time.perf_counter() - t0
+    value = wbytes * args.steps / el / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded PCG64, same workload as the GPU arm)",
+        "config": {"workload": WORKLOAD, "layers": args.layers, "nb": 1, "weight_bytes_per_step": wbytes},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "one full decode step per timed step in the f64 C oracle, 1 thread"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

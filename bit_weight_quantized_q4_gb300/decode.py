@@ -1,0 +1,119 @@
+"""The synthetic Q4 decode step: per layer RMSNorm + q projection, dual K/V,
+o projection + residual (its input an attention stand-in), RMSNorm + gate/up
++ SwiGLU, down + residual; then a final RMSNorm, the logits projection and
+the greedy argmax.  All launches are libq4gemv calls on one stream and the
+whole step is captured once as a CUDA graph and replayed.
+
+The step order is the fused decode path of honeycrisp/mod.rs
+(forward_decode_fused_layers: one command buffer per step) with the final
+logits projection and greedy argmax of Module gpu (module sampling).  The
+attention output is replaced by a fixed seeded vector per layer, so the q, k
+and v projections are computed and stored but not consumed.
+
+Kernels per step: 5 per layer + 2 for the argmax (82 for 16 layers).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import Q4Weight, q4_argmax, q4_argmax_workspace_bytes, q4_dual_gemv, q4_gus_nrm, q4_nrm_gemv, \
+    q4_res_gemv
+
+
+@dataclass
+class DeviceLayer:
+    gamma_in: torch.Tensor
+    Wq: Q4Weight
+    Wk: Q4Weight
+    Wv: Q4Weight
+    Wo: Q4Weight
+    attn: torch.Tensor
+    gamma_post: torch.Tensor
+    Wg: Q4Weight
+    Wu: Q4Weight
+    Wd: Q4Weight
+
+
+KERNELS_PER_LAYER = 5
+KERNELS_FINAL = 2
+
+
+class DecodeStep:
+    """Device-resident weights and activation buffers of one decode step.
+
+    ``cfg`` is a ``q4_workloads.Cfg4`` (host weights).  ``x_in`` holds the
+    step input; after ``run()`` (or a graph replay) ``idx`` / ``val`` hold
+    the argmax and ``hid`` the final hidden state."""
+
+    def __init__(self, cfg, device="cuda"):
+        T = lambda a: torch.from_numpy(a.copy()).to(device)
+        W = lambda H: Q4Weight.from_q4_0(H.blocks, H.n, H.k, device)
+        self.eps = float(cfg.eps)
+        self.layers = [DeviceLayer(T(L.gamma_in), W(L.Wq), W(L.Wk), W(L.Wv), W(L.Wo), T(L.attn),
+                                   T(L.gamma_post), W(L.Wg), W(L.Wu), W(L.Wd)) for L in cfg.layers]
+        self.gamma_final = T(cfg.gamma_final)
+        self.Wlogits = W(cfg.Wlogits)
+        nb, hidden = cfg.x.shape
+        L0 = self.layers[0]
+        f32 = dict(dtype=torch.float32, device=device)
+        self.nb, self.hidden = nb, hidden
+        self.x_in = T(cfg.x)
+        self.hid = torch.empty((nb, hidden), **f32)
+        self.q = torch.empty((nb, L0.Wq.n), **f32)
+        self.k = torch.empty((nb, L0.Wk.n), **f32)
+        self.v = torch.empty((nb, L0.Wv.n), **f32)
+        self.h = torch.empty((nb, L0.Wg.n), **f32)
+        self.idx = torch.empty(nb, dtype=torch.int32, device=device)
+        self.val = torch.empty(nb, **f32)
+        self.ws = torch.empty(q4_argmax_workspace_bytes(self.Wlogits.n, nb), dtype=torch.uint8, device=device)
+
+    @property
+    def n_kernels(self) -> int:
+        return KERNELS_PER_LAYER * len(self.layers) + KERNELS_FINAL
+
+    @property
+    def weight_bytes(self) -> int:
+        b = self.Wlogits.weight_bytes
+        for L in self.layers:
+            b += sum(w.weight_bytes for w in (L.Wq, L.Wk, L.Wv, L.Wo, L.Wg, L.Wu, L.Wd))
+        return b
+
+    def run(self, hook=None, around=None):
+        """Enqueue one step.  ``hook(name, layer)`` runs after each call
+        (tests use it to snapshot intermediates); ``around(name, layer, fn)``
+        may wrap a call (the benchmark brackets one kernel with events)."""
+        call = around or (lambda name, l, fn: fn())
+        src = self.x_in
+        eps = self.eps
+        for l, L in enumerate(self.layers):
+            call("q", l, lambda: q4_nrm_gemv(L.Wq, src, L.gamma_in, eps, out=self.q))
+            hook and hook("q", l)
+            call("kv", l, lambda: q4_dual_gemv(L.Wk, L.Wv, src, L.gamma_in, eps, out_a=self.k, out_b=self.v))
+            hook and hook("kv", l)
+            call("o", l, lambda: q4_res_gemv(L.Wo, L.attn, src, out=self.hid))
+            hook and hook("o", l)
+            call("gus", l, lambda: q4_gus_nrm(L.Wg, L.Wu, self.hid, L.gamma_post, eps, out=self.h))
+            hook and hook("gus", l)
+            call("down", l, lambda: q4_res_gemv(L.Wd, self.h, self.hid, out=self.hid))
+            hook and hook("down", l)
+            src = self.hid
+        call("argmax", len(self.layers),
+             lambda: q4_argmax(self.Wlogits, self.hid, self.gamma_final, eps, workspace=self.ws,
+                               idx=self.idx, val=self.val))
+        hook and hook("argmax", len(self.layers))
+
+    def capture(self, around=None) -> torch.cuda.CUDAGraph:
+        """Capture one step as a CUDA graph (after one eager warm-up run)."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(around=around)
+        torch.cuda.synchronize()
+        return g

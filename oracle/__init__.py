@@ -261,3 +261,37 @@ def q4_argmax(W: HostWeight, x, gamma=None, eps=0.0):
     logits, S = gemv(W, xh)
     idx = np.array([argmax(logits[r]) for r in range(logits.shape[0])], dtype=np.int64)
     return idx, logits, S
+
+
+# ---------------------------------------------------------------- decode step
+# The synthetic decode step of honeycrisp/mod.rs, forward_decode_fused_layers
+# (per layer: Q with inline input_norm, K+V dual with inline input_norm,
+# o projection + residual, post_norm + gate + up + silu, down + residual),
+# followed by the final norm, logits projection and greedy argmax of Module
+# gpu, module sampling.  The attention output is the layer's given stand-in.
+
+def _hw(H) -> HostWeight:
+    return HostWeight.q4_0(H.blocks, H.n, H.k)
+
+
+def decode_layer(L, src, eps: float) -> dict:
+    """One layer on f64 activations ``src [nb, hidden]``; returns every
+    intermediate (and its tolerance scale) as f64 arrays."""
+    src = _f64(src)
+    q, Sq = q4_nrm_gemv(_hw(L.Wq), src, L.gamma_in, eps)
+    k, Sk, v, Sv = q4_dual_gemv(_hw(L.Wk), _hw(L.Wv), src, L.gamma_in, eps)
+    hid_o, So = q4_res_gemv(_hw(L.Wo), L.attn, src)
+    h, g, Sg, u, Su = q4_gus_nrm(_hw(L.Wg), _hw(L.Wu), hid_o, L.gamma_post, eps)
+    hid, Sd = q4_res_gemv(_hw(L.Wd), h, hid_o)
+    return dict(q=q, Sq=Sq, k=k, Sk=Sk, v=v, Sv=Sv, hid_o=hid_o, So=So, h=h, g=g, Sg=Sg, u=u, Su=Su,
+                hid=hid, Sd=Sd)
+
+
+def decode_step(cfg, layers=None):
+    """The whole step in f64 from ``cfg.x``; returns (idx, logits, hidden)."""
+    hid = _f64(cfg.x)
+    Ls = cfg.layers if layers is None else cfg.layers[:layers]
+    for L in Ls:
+        hid = decode_layer(L, hid, cfg.eps)["hid"]
+    idx, logits, _ = q4_argmax(_hw(cfg.Wlogits), hid, cfg.gamma_final, cfg.eps)
+    return idx, logits, hid

@@ -1,0 +1,124 @@
+"""Parity at the full workload sizes: the Q4_0 GEMV (1024 x 1024), the fused
+RMSNorm q projection and dual K/V (2048 x 2048, 2 x 512 x 2048), the MLP
+block (gate/up 8192 x 2048 + SwiGLU, down 2048 x 8192 + residual), the affine
+14336 x 4096 matvec at nb = 1, 2, 4, 8, 16, and the whole 16-layer decode step
+in the launch configuration the benchmark times (teacher-forced: each call is
+checked against the oracle run on that call's own GPU inputs)."""
+import numpy as np
+import pytest
+
+import oracle
+import q4_workloads as wl
+from parity import check, check_argmax, check_residual, check_swiglu, dev_weight, host_weight, to_np
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def q4():
+    import bit_weight_quantized_q4_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+def T(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def test_q4_0_gemv_1024(q4):
+    c = wl.cfg0()
+    y = q4.q4_gemv(dev_weight(c.W), T(c.x))
+    ref, S = oracle.q4_gemv(host_weight(c.W), c.x)
+    check(to_np(y), ref, S, what="1024x1024")
+
+
+def test_nrm_q_and_dual_kv_2048(q4):
+    c = wl.cfg1()
+    y = q4.q4_nrm_gemv(dev_weight(c.Wq), T(c.x), T(c.gamma), c.eps)
+    ref, S = oracle.q4_nrm_gemv(host_weight(c.Wq), c.x, c.gamma, c.eps)
+    check(to_np(y), ref, S, what="nrm q")
+    yk, yv = q4.q4_dual_gemv(dev_weight(c.Wk), dev_weight(c.Wv), T(c.x), T(c.gamma), c.eps)
+    ra, Sa, rb, Sb = oracle.q4_dual_gemv(host_weight(c.Wk), host_weight(c.Wv), c.x, c.gamma, c.eps)
+    check(to_np(yk), ra, Sa, what="dual k")
+    check(to_np(yv), rb, Sb, what="dual v")
+
+
+def test_mlp_block_2048_8192(q4):
+    c = wl.cfg2()
+    h = q4.q4_gus_nrm(dev_weight(c.Wg), dev_weight(c.Wu), T(c.x), T(c.gamma), c.eps)
+    _, g, Sg, u, Su = oracle.q4_gus_nrm(host_weight(c.Wg), host_weight(c.Wu), c.x, c.gamma, c.eps)
+    check_swiglu(to_np(h), g, Sg, u, Su, what="gus")
+    r = T(c.r)
+    y = q4.q4_res_gemv(dev_weight(c.Wd), h, r)
+    ref, S = oracle.q4_res_gemv(host_weight(c.Wd), h.cpu().numpy(), c.r)   # teacher-forced on the GPU h
+    check_residual(to_np(y), ref, S, what="down+res")
+
+
+@pytest.fixture(scope="module")
+def cfg3():
+    return wl.cfg3()
+
+
+@pytest.mark.parametrize("nb", [1, 2, 4, 8, 16])
+def test_affine_14336x4096(q4, cfg3, nb):
+    x = cfg3.x[:nb]
+    W = dev_weight(cfg3.W)
+    y = q4.q4_gemv(W, T(x))
+    ref, S = oracle.q4_gemv(host_weight(cfg3.W), x)
+    check(to_np(y), ref, S, what="affine nb=%d" % nb)
+    gs = q4.q4_group_sums(T(x))
+    assert torch.equal(q4.q4_gemv(W, T(x), gsum=gs), y)
+
+
+def test_decode_step_teacher_forced(q4):
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+    cfg = wl.cfg4()
+    step = DecodeStep(cfg)
+    snaps = []
+
+    def hook(name, l):
+        if name == "q":
+            snaps.append({"src": (step.x_in if l == 0 else step.hid).clone(), "q": step.q.clone()})
+        elif name == "kv":
+            snaps[-1].update(k=step.k.clone(), v=step.v.clone())
+        elif name == "o":
+            snaps[-1]["hid_o"] = step.hid.clone()
+        elif name == "gus":
+            snaps[-1]["h"] = step.h.clone()
+        elif name == "down":
+            snaps[-1]["hid"] = step.hid.clone()
+        elif name == "argmax":
+            snaps.append({"idx": step.idx.clone(), "val": step.val.clone(), "final": step.hid.clone()})
+
+    step.run(hook=hook)
+    torch.cuda.synchronize()
+    for l, L in enumerate(cfg.layers):
+        s = snaps[l]
+        src = s["src"].cpu().numpy()
+        q, Sq = oracle.q4_nrm_gemv(oracle._hw(L.Wq), src, L.gamma_in, cfg.eps)
+        check(to_np(s["q"]), q, Sq, what="layer %d q" % l)
+        ka, Ska, kb, Skb = oracle.q4_dual_gemv(oracle._hw(L.Wk), oracle._hw(L.Wv), src, L.gamma_in, cfg.eps)
+        check(to_np(s["k"]), ka, Ska, what="layer %d k" % l)
+        check(to_np(s["v"]), kb, Skb, what="layer %d v" % l)
+        ho, So = oracle.q4_res_gemv(oracle._hw(L.Wo), L.attn, src)
+        check_residual(to_np(s["hid_o"]), ho, So, what="layer %d o" % l)
+        _, g, Sg, u, Su = oracle.q4_gus_nrm(oracle._hw(L.Wg), oracle._hw(L.Wu), s["hid_o"].cpu().numpy(),
+                                            L.gamma_post, cfg.eps)
+        check_swiglu(to_np(s["h"]), g, Sg, u, Su, what="layer %d gus" % l)
+        hd, Sd = oracle.q4_res_gemv(oracle._hw(L.Wd), s["h"].cpu().numpy(), s["hid_o"].cpu().numpy())
+        check_residual(to_np(s["hid"]), hd, Sd, what="layer %d down" % l)
+    fin = snaps[-1]
+    _, lref, Sl = oracle.q4_argmax(oracle._hw(cfg.Wlogits), fin["final"].cpu().numpy(), cfg.gamma_final, cfg.eps)
+    check_argmax(fin["idx"].cpu().numpy(), lref, what="decode argmax")
+    assert abs(float(fin["val"][0]) - lref[0].max()) <= 1e-3 * Sl[0].max() + 1e-6
+
+    # the captured graph the benchmark replays gives the same bits as the
+    # eager run checked above
+    g = step.capture()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(step.idx, fin["idx"]) and torch.equal(step.val, fin["val"])
+    assert torch.equal(step.hid, fin["final"])
