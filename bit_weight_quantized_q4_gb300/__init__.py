@@ -77,6 +77,7 @@ def lib() -> ctypes.CDLL:
             "q4_res_gemv": (I32, [W, P, P, I32, P, P]),
             "q4_argmax_workspace_bytes": (SZ, [I32, I32]),
             "q4_argmax": (I32, [W, P, P, F, I32, P, P, P, P, SZ, P]),
+            "q4_argmax_noalloc": (I32, [W, P, P, F, I32, P, P, P, P]),
             "q4_plan": (I32, [I32, I32, I32, I32, I32, I32, ctypes.POINTER(ctypes.c_int32)]),
             "q4_status_str": (ctypes.c_char_p, [I32]),
         }
@@ -308,4 +309,26 @@ def q4_argmax(W: Q4Weight, x, gamma=None, eps: float = 0.0, want_val=False, want
                            None if val is None else val.data_ptr(),
                            None if logits is None else logits.data_ptr(),
                            workspace.data_ptr(), workspace.numel(), _stream()), "q4_argmax")
+    return idx, val, logits
+
+
+def q4_argmax_noalloc(W: Q4Weight, x, gamma=None, eps: float = 0.0, want_val=False, want_logits=False,
+                      idx=None, val=None, logits=None):
+    """Like ``q4_argmax`` but without a workspace: the pass-1 pairs live in a
+    fixed array inside the library (for callers that cannot allocate device
+    memory; see ``q4_argmax_noalloc`` in the C header for the size limit and
+    the sharing rules).  Returns ``(idx, val or None, logits or None)``."""
+    torch = _torch()
+    x, nb = _rows(x, W.k)
+    gp = None if gamma is None else _dev_f32(gamma, "gamma", (W.k,)).data_ptr()
+    if idx is None:
+        idx = torch.empty(nb, dtype=torch.int32, device=x.device)
+    if want_val and val is None:
+        val = torch.empty(nb, dtype=torch.float32, device=x.device)
+    if want_logits and logits is None:
+        logits = torch.empty((nb, W.n), dtype=torch.float32, device=x.device)
+    _check(lib().q4_argmax_noalloc(W.cref(), x.data_ptr(), gp, float(eps), nb, idx.data_ptr(),
+                                   None if val is None else val.data_ptr(),
+                                   None if logits is None else logits.data_ptr(), _stream()),
+           "q4_argmax_noalloc")
     return idx, val, logits

@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/q4gemv.h"
 #include "q4_internal.h"
 
@@ -252,3 +254,81 @@ q4_status q4_argmax(const q4_weight *W, const float *x, const float *gamma, floa
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free greedy argmax.
+//
+// q4_argmax needs a caller-provided workspace for its pass-1 (max, index)
+// pairs.  Some callers cannot provide one: a plug-in whose host application
+// owns all device memory and hands out no allocator, or a decode loop that
+// must not touch the allocator once it is running (a cudaMalloc there can
+// synchronise the device and stall a latency-critical step).  For them
+// q4_argmax_noalloc keeps those pairs in the fixed array below, which is
+// compiled into the library: every GPU that loads the library holds these
+// 128 KiB until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 128u * 1024u;
+constexpr int kNoAllocMaxDevices = 64;
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char q4_noalloc_argmax_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The array's
+// name in host code is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+q4_status noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return Q4_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, q4_noalloc_argmax_scratch) != cudaSuccess || p == nullptr)
+            return Q4_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return Q4_OK;
+}
+
+}  // namespace
+
+extern "C" q4_status q4_argmax_noalloc(const q4_weight *W, const float *x, const float *gamma, float eps,
+                                       int32_t nb, int32_t *idx, float *val, float *logits,
+                                       cudaStream_t stream) {
+    Q4_TRY(check_weight(W));
+    Q4_TRY(check_act(x));
+    if (!idx) return Q4_ERR_NULL;
+    if (!aligned16(idx) || (val && !aligned16(val)) || (logits && !aligned16(logits)) ||
+        (gamma && !aligned16(gamma)))
+        return Q4_ERR_ALIGN;
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    const int sms = num_sms();
+    if (sms <= 0) return Q4_ERR_CUDA;
+    // The pairs this call needs: one per (thread-block group, activation row).
+    const q4::Plan plan = q4::make_plan(W->fmt, (int)q4::tiles_of(W->n), (int)q4::chunks_of(W->k), nb,
+                                        false, sms);
+    const size_t val_bytes = ((size_t)plan.groups * nb * 4 + 15) & ~(size_t)15;
+    if (val_bytes + (size_t)plan.groups * nb * 4 > kNoAllocScratchBytes) return Q4_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    Q4_TRY(noalloc_scratch(&scratch));
+    q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, x, gamma, eps, nb);
+    p.epi = q4::EPI_ARGMAX;
+    p.out[0] = logits;
+    p.am_val = (float *)scratch;
+    p.am_idx = (int *)((unsigned char *)scratch + val_bytes);
+    q4::Plan used;
+    Q4_TRY(run(p, W->fmt, stream, &used));
+    cudaGetLastError();
+    if (q4::launch_argmax_fold(p.am_val, p.am_idx, used.groups, nb, idx, val, stream) != 0 ||
+        cudaGetLastError() != cudaSuccess)
+        return Q4_ERR_CUDA;
+    return Q4_OK;
+}

@@ -165,6 +165,28 @@ q4_status q4_argmax(const q4_weight *W, const float *x, const float *gamma, floa
                     int32_t nb, int32_t *idx, float *val, float *logits,
                     void *workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* Allocation-free variant of q4_argmax.  The pages have no counterpart: this
+ * exists for callers that cannot allocate device memory where they need the
+ * argmax, such as a plug-in whose host application owns all device memory and
+ * gives it no allocator, or a decode loop that must not call cudaMalloc once
+ * running (a cudaMalloc can synchronise the device and stall the step).
+ * Same arguments and results as q4_argmax without the workspace: the pass-1
+ * (max, index) pairs live in a 128 KiB array compiled into the library, which
+ * every GPU that loads the library holds until the process exits.
+ * - Limit: the call needs (groups of its launch plan) x nb pairs of 8 bytes;
+ *   ceil(n/16) * nb <= 16382 always fits (the 65536-row logits projection
+ *   fits at every nb).  A larger need returns Q4_ERR_WORKSPACE and launches
+ *   nothing.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture.
+ * - Every call shares the one array.  Nothing in it needs to start at zero
+ *   (pass 1 writes every pair pass 2 reads), but calls whose kernels overlap
+ *   on the GPU (other streams, other threads) race on it: serialise them.
+ * - It calls no cudaMalloc, cudaFree or other allocating routine. */
+q4_status q4_argmax_noalloc(const q4_weight *W, const float *x, const float *gamma, float eps,
+                            int32_t nb, int32_t *idx, float *val, float *logits, cudaStream_t stream);
+
 /* Launch plan the library uses for a GEMV-shaped call (host-only; exposed
  * for tests and tuning).  tiles: 16-row tiles of the launch, chunks: 128-k
  * chunks per row, pairs: 1 when tiles come in gate/up pairs, num_sms:
