@@ -81,6 +81,7 @@ q4_status run(const q4::GemvParams &p, int fmt, cudaStream_t stream, q4::Plan *p
     const int sms = num_sms();
     if (sms <= 0) return Q4_ERR_CUDA;
     q4::Plan plan = q4::make_plan(fmt, p.T, p.C, p.nb, p.mode == q4::MODE_PAIRS, sms);
+    if (plan.smem > (size_t)227 * 1024) return Q4_ERR_UNSUPPORTED;  // nb * k too large to stage
     q4::GemvParams pp = p;
     pp.TG = plan.TG;
     pp.S = plan.S;

@@ -9,9 +9,9 @@
 
 namespace q4 {
 
-template <int FMT, int NT>
+template <int FMT, int NT, bool NB1>
 static int launch_nt(const GemvParams &p, const Plan &plan, cudaStream_t stream) {
-    auto kern = dev::gemv_kernel<FMT, NT>;
+    auto kern = dev::gemv_kernel<FMT, NT, NB1>;
     int devid = 0;
     if (cudaGetDevice(&devid) != cudaSuccess) return -1;
     static size_t smem_set[64] = {0};
@@ -45,10 +45,9 @@ static int launch_nt(const GemvParams &p, const Plan &plan, cudaStream_t stream)
 
 template <int FMT>
 static int launch_gemv_fmt(const GemvParams &p, const Plan &plan, cudaStream_t stream) {
-    const int nt = (2 * p.nb + 7) / 8;  // 8-column n-tiles of (hi, lo) pairs
-    if (nt <= 1) return launch_nt<FMT, 1>(p, plan, stream);
-    if (nt <= 2) return launch_nt<FMT, 2>(p, plan, stream);
-    return launch_nt<FMT, 4>(p, plan, stream);
+    if (p.nb == 1) return launch_nt<FMT, 1, true>(p, plan, stream);
+    if (p.nb <= 8) return launch_nt<FMT, 1, false>(p, plan, stream);
+    return launch_nt<FMT, 2, false>(p, plan, stream);
 }
 
 }  // namespace q4

@@ -51,6 +51,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxNb = 16;
 constexpr int kMaxCluster = 8;
+constexpr size_t kXsCap = 64 * 1024;          // activation slice staged per CTA
+constexpr int kRingDepth = 8;                 // weight records per warp in the cp.async ring
 
 struct GemvParams {
     const uint8_t *w[2];   // packed weights of (up to) two matrices
@@ -61,9 +63,10 @@ struct GemvParams {
     int K;                 // input length
     int C;                 // 128-column chunks per row
     int nb;                // activation rows
-    int TG;                // tiles per group (one group = one cluster)
+    int TG;                // most tiles one group holds (sizes shared memory)
     int S;                 // K-split: CTAs per cluster
     int Cs;                // chunks per K-slice
+    int groups;            // tile groups; group g holds tile units [g*P/groups, (g+1)*P/groups)
     const float *x;        // [nb][K]
     const float *gamma;    // [K] or nullptr (no RMSNorm)
     float eps;
@@ -73,17 +76,19 @@ struct GemvParams {
     const float *res;      // residual [nb][n0]
     float *am_val;         // argmax partials [nb][groups]
     int *am_idx;
-    int groups;
 };
+
+inline int ntiles_for(int nb) { return nb <= 8 ? 1 : 2; }
 
 // Dynamic shared memory of one CTA.
 inline size_t smem_bytes(int fmt, int TG, int Cs, int nb) {
-    size_t xs = (size_t)4 * nb * Cs * kChunkK;                     // hi/lo f16 activations
-    size_t gs = fmt == 1 ? (size_t)4 * nb * Cs * kBlocksPerChunk : 0;  // affine group sums
-    size_t slots = (size_t)4 * kWarps * TG * kTileRows * nb;       // per-warp partials
-    size_t red = (size_t)4 * TG * kTileRows * nb;                  // CTA partials
-    size_t misc = (size_t)4 * 4 * kWarps * kMaxNb + 4 * 8 * kMaxNb;  // reductions
-    return xs + gs + slots + red + misc;
+    size_t xs = (size_t)4 * nb * Cs * kChunkK;                                   // hi/lo f16 activations
+    size_t gs = fmt == 1 ? (size_t)4 * Cs * kBlocksPerChunk * 8 * ntiles_for(nb) : 0;  // group sums
+    size_t red = (size_t)4 * TG * kTileRows * nb;                                // CTA partials
+    size_t bslot = (size_t)4 * kWarps * 2 * kTileRows * nb;                      // warp boundary tiles
+    size_t misc = (size_t)4 * 4 * kWarps * kMaxNb + 4 * 8 * kMaxNb;             // reductions
+    size_t ring = (size_t)kWarps * kRingDepth * rec_bytes(fmt);                  // weight records
+    return xs + gs + red + bslot + misc + ring;
 }
 
 struct Plan {
@@ -91,34 +96,44 @@ struct Plan {
     size_t smem;
 };
 
-// Tiles per group and K-split for a launch of T tiles x C chunks.
+// Launch plan for T tiles x C chunks.  One group of tiles per cluster of S
+// CTAs (S splits K); at most one CTA per SM where the work allows, so that
+// the next kernel in the stream can be resident beside it.  Chooses the
+// split whose busiest CTA has the least work; ties go to the smaller split.
 inline Plan make_plan(int fmt, int T, int C, int nb, bool pairs, int num_sms) {
-    Plan p{};
-    const size_t xs_cap = 64 * 1024;
-    int S = 1;
-    // the activation slice must fit in shared memory
-    while (S < kMaxCluster && (size_t)4 * nb * ((C + S - 1) / S) * kChunkK > xs_cap) S *= 2;
-    // split K further when there are too few tiles to cover every SM
-    while (S < kMaxCluster && (int64_t)T * S < num_sms && (C + 2 * S - 1) / (2 * S) >= 2) S *= 2;
-    if (S > C) S = 1 << (31 - __builtin_clz((unsigned)C));   // at least one chunk per slice
-    int Cs = (C + S - 1) / S;
-    const int target = 2 * num_sms;        // two 256-thread CTAs per SM
-    int TG = (int)(((int64_t)T * S + target - 1) / target);
-    if (TG < 1) TG = 1;
-    int tg_cap = 64 / nb;
-    if (tg_cap < 1) tg_cap = 1;
-    if (TG > tg_cap) TG = tg_cap;
-    if (pairs) {
-        if (TG < 2) TG = 2;
-        TG += TG & 1;
+    const int pw = pairs ? 2 : 1;
+    const int P = T / pw;                       // allocation units (tiles or gate/up pairs)
+    Plan best{};
+    long long best_cost = -1;
+    for (int S = 1; S <= kMaxCluster; S *= 2) {
+        if (S > 1 && S > C) break;
+        const int Cs = (C + S - 1) / S;
+        if ((size_t)4 * nb * Cs * kChunkK > kXsCap && S < kMaxCluster) continue;
+        int G = num_sms / S;
+        if (G < 1) G = 1;
+        if (G > P) G = P;
+        int per = (P + G - 1) / G;                      // units of the busiest group
+        const int cap = 128 / (nb * pw) > 0 ? 128 / (nb * pw) : 1;  // partials fit shared memory
+        if (per > cap) {
+            per = cap;
+            G = (P + per - 1) / per;
+        }
+        const int ctas = G * S;
+        const int waves = (ctas + num_sms - 1) / num_sms;
+        // records on the busiest SM, plus about a microsecond of one SM's
+        // share of HBM (~40 records) for each cluster-wide exchange
+        const long long cost = (long long)per * pw * Cs * waves + (S > 1 ? 40 : 0);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best.TG = per * pw;
+            best.S = S;
+            best.Cs = Cs;
+            best.groups = G;
+            best.ctas = ctas;
+        }
     }
-    p.TG = TG;
-    p.S = S;
-    p.Cs = Cs;
-    p.groups = (T + TG - 1) / TG;
-    p.ctas = p.groups * S;
-    p.smem = smem_bytes(fmt, TG, Cs, nb);
-    return p;
+    best.smem = smem_bytes(fmt, best.TG, best.Cs, nb);
+    return best;
 }
 
 // Launchers, one per kernel instantiation family (defined in the .cu files).

@@ -71,15 +71,23 @@ def test_packed_sizes_and_padding():
                                                 (2, 1, True), (7, 3, False), (128, 64, False)])
 @pytest.mark.parametrize("nb", [1, 3, 8, 16])
 def test_plan_invariants(fmt, tiles, chunks, pairs, nb):
-    p = q4.plan(fmt, tiles, chunks, nb, pairs, 152)
+    sms = 152
+    p = q4.plan(fmt, tiles, chunks, nb, pairs, sms)
+    pw = 2 if pairs else 1
+    units = tiles // pw
     assert 1 <= p["S"] <= 8 and (p["S"] & (p["S"] - 1)) == 0
     assert p["S"] * p["Cs"] >= chunks and p["Cs"] >= 1
-    assert p["groups"] * p["TG"] >= tiles and (p["groups"] - 1) * p["TG"] < tiles
+    assert 1 <= p["groups"] <= units
+    # balanced contiguous ranges: the busiest group holds TG tiles and all fit
+    assert p["TG"] == -(-units // p["groups"]) * pw or p["TG"] == max(1, 128 // (nb * pw)) * pw
+    assert p["groups"] * p["TG"] >= tiles
     assert p["ctas"] == p["groups"] * p["S"]
     assert p["smem"] <= 227 * 1024
-    assert p["TG"] * nb <= max(64, 2 * nb)
+    assert p["TG"] * nb <= max(128, nb * pw)       # partial sums fit shared memory
     if pairs:
         assert p["TG"] % 2 == 0
+    if p["TG"] * nb < 128 // pw:                    # not capped: at most one CTA per SM
+        assert p["ctas"] <= sms
     # the activation slice fits the staging budget
     assert 4 * nb * p["Cs"] * 128 <= 64 * 1024 or p["S"] == 8
 
