@@ -2,18 +2,20 @@
 """Benchmark of the Q4 dequant-in-GEMV hot path on the synthetic decode step.
 
 One step = one pass of the whole fused path over one batch: 16 layers of
-(RMSNorm+q, dual RMSNorm+k/v, o+residual, RMSNorm+gate/up+SwiGLU,
-down+residual) then RMSNorm + a 65536 x 2048 logits projection + argmax,
-all Q4_0, hidden 2048, kv 512, intermediate 8192, nb = 1, replayed as one
-CUDA graph of 82 kernels.  622,854,144 weight bytes stream from HBM per step
-(more than L2 holds), so every step reads cold weights.
+(RMSNorm+q/k/v, o+residual, RMSNorm+gate/up+SwiGLU, down+residual) then
+RMSNorm + a 65536 x 2048 logits projection + argmax, all Q4_0, hidden 2048,
+kv 512, intermediate 8192, nb = 1, run by ``q4_decode_step`` as one
+persistent kernel and replayed from a CUDA graph.  622,854,144 weight bytes
+stream from HBM per step (more than L2 holds), so every step reads cold
+weights.
 
 Prints ONE JSON line (rank 0).  ``value`` is weight GB/s of the whole job
 (all ranks), ``ms_per_step`` the step time; ``e2e`` repeats the measure with
 the step's inputs copied from pinned host memory and its result read back
-inside the timed region; ``roofline`` is the SwiGLU MLP kernel (the largest
-share of the step) against the measured HBM peak; ``cpu_baseline`` is the f64
-C oracle on the host.  ``--impl reference`` times the oracle itself as the
+inside the timed region; ``roofline`` is the decode-step kernel against the
+measured HBM peak; ``graph_of_calls`` times the same step as 82 separate
+library calls in one graph; ``cpu_baseline`` is the f64 C oracle on the
+host.  ``--impl reference`` times the oracle itself as the
 reference arm.  Multi-GPU (torchrun) runs independent replicas (weak
 scaling, no collective on the data path).
 """
@@ -35,7 +37,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Q4 GEMV weight GB/s (fraction of GB300 HBM peak) and µs per fused decode-step"
 WORKLOAD = ("synthetic 16-layer Q4_0 decode step, nb=1, hidden 2048, kv 512, intermediate 8192, "
-            "logits 65536 x 2048 + argmax, one CUDA graph")
+            "logits 65536 x 2048 + argmax, one persistent kernel replayed from a CUDA graph")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -270,28 +272,42 @@ class _GraphEvent:
         return ms.value
 
 
-def dominant_kernel_timing(step, steps: int):
-    """Average duration of the SwiGLU MLP kernel (gate+up, 2 x 8192 x 2048
-    Q4_0) inside the step, from timing events captured around each of its
-    launches in a graph of the step, replayed `steps` times."""
+def kernel_timing(step, steps: int, fused: bool, name: str = "gus"):
+    """Average duration of one kernel inside the step, from timing events
+    captured around each of its launches in a graph of the step, replayed
+    `steps` times: the persistent step kernel (fused) or every launch of the
+    call named `name` (call-by-call step)."""
     import torch
-    evs = {}
-
-    def around(name, l, fn):
-        if name != "gus":
-            return fn()
+    evs = []
+    if fused:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step.run_fused()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
         a, b = _GraphEvent(), _GraphEvent()
-        a.record()
-        fn()
-        b.record()
-        evs[l] = (a, b)
-
-    g = step.capture(around=around)
+        with torch.cuda.graph(g):
+            a.record()
+            step.run_fused()   # includes the 16-byte clear of the barrier counter
+            b.record()
+        evs.append((a, b))
+    else:
+        def around(nm, l, fn):
+            if nm != name:
+                return fn()
+            a, b = _GraphEvent(), _GraphEvent()
+            a.record()
+            fn()
+            b.record()
+            evs.append((a, b))
+        g = step.capture(around=around)
     durs = []
     for _ in range(steps):
         g.replay()
         torch.cuda.synchronize()
-        durs += [a.elapsed_ms(b) * 1e3 for a, b in evs.values()]
+        durs += [a.elapsed_ms(b) * 1e3 for a, b in evs]
     return statistics.mean(durs), len(durs)
 
 
@@ -390,11 +406,13 @@ def run_ours(args, rank, world, local):
     cfg = wl.cfg4(layers=args.layers)
     step = DecodeStep(cfg, device)
     wbytes = step.weight_bytes
-    graph = step.capture()
+    graph = step.capture(fused=True)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
+    step.run_fused()
+    q4.q4_decode_check(step.step_ws)  # every grid barrier completed
 
     props = torch.cuda.get_device_properties(device)
     uuid = str(getattr(props, "uuid", "") or "")
@@ -409,13 +427,19 @@ def run_ours(args, rank, world, local):
     ms_per_step = max_secs * 1e3 / args.steps
 
     peak, peak_src = measured_peaks()
-    gus_us, gus_n = dominant_kernel_timing(step, max(3, min(args.steps, 10)))
-    L0 = step.layers[0]
-    gus_bytes = L0.Wg.weight_bytes + L0.Wu.weight_bytes
-    achieved = gus_bytes / (gus_us * 1e-6) / 1e9
+    k_us, k_n = kernel_timing(step, max(3, min(args.steps, 10)), fused=True)
+    achieved = wbytes / (k_us * 1e-6) / 1e9
 
     e2e_secs, h2d, d2h = e2e_timing(step, graph, args.steps, max(1, args.warmup))
     e2e_max = reduce_max(e2e_secs, world, device)
+
+    # the same step as 82 separate library calls in one graph
+    calls_graph = step.capture()
+    for _ in range(max(1, args.warmup)):
+        calls_graph.replay()
+    calls_secs = time_replays(calls_graph, args.steps, stream)
+    gus_us, _ = kernel_timing(step, 3, fused=False, name="gus")
+    del calls_graph
 
     l2 = int(getattr(props, "L2_cache_size", 0) or 0)
     kernels = None
@@ -444,20 +468,24 @@ def run_ours(args, rank, world, local):
         "dtype": "f32",
         "precision": "Q4_0 weights dequantised exactly to f16; activations as f16 hi+lo pairs; fp32 accumulate",
         "data": "synthetic (seeded PCG64; q~U{0..15}, d~U[0.005,0.02] fp16, x~N(0,1), gamma=1+0.1N(0,1))",
-        "config": {"workload": WORKLOAD, "layers": args.layers, "nb": 1, "kernels_per_step": step.n_kernels,
+        "config": {"workload": WORKLOAD, "layers": args.layers, "nb": 1, "kernels_per_step": 1,
                    "weight_bytes_per_step": wbytes,
                    "l2": "inputs larger than L2: %d weight bytes per step vs %d B L2" % (wbytes, l2),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "gpu_launches": step.n_kernels * args.steps,
+        "gpu_launches": 1 * args.steps,
         "clocks": clk,
         "e2e": {"value": round(job_rate(wbytes, args.steps, world, e2e_max), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_max * 1e3 / args.steps, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "roofline": {"kernel": "q4_gus_nrm (RMSNorm + gate/up 2 x 8192 x 2048 Q4_0 + SwiGLU)",
+        "roofline": {"kernel": "decode_kernel (q4_decode_step: the whole step, one persistent kernel)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src + " (MEASURED_PEAKS hbm_gbs)",
-                     "algorithmic_bytes_per_launch": gus_bytes, "launch_us": round(gus_us, 3),
-                     "launches_timed": gus_n, "traffic": profiled_traffic("gus_nrm_8192x2048")},
+                     "algorithmic_bytes_per_launch": wbytes, "launch_us": round(k_us, 3),
+                     "launches_timed": k_n, "traffic": profiled_traffic("decode_step_16layer")},
+        "graph_of_calls": {"kernels_per_step": step.n_kernels,
+                           "us_per_step": round(calls_secs * 1e6 / args.steps, 2),
+                           "weight_gbs": round(wbytes * args.steps / calls_secs / 1e9, 2),
+                           "gus_launch_us": round(gus_us, 3)},
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu

@@ -43,6 +43,12 @@ class _CWeight(ctypes.Structure):
                 ("dev", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
 
 
+class _CDecodeLayer(ctypes.Structure):
+    _fields_ = [("Wq", _CWeight), ("Wk", _CWeight), ("Wv", _CWeight), ("Wo", _CWeight), ("Wg", _CWeight),
+                ("Wu", _CWeight), ("Wd", _CWeight), ("gamma_in", ctypes.c_void_p),
+                ("gamma_post", ctypes.c_void_p), ("attn", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -78,6 +84,9 @@ def lib() -> ctypes.CDLL:
             "q4_argmax_workspace_bytes": (SZ, [I32, I32]),
             "q4_argmax": (I32, [W, P, P, F, I32, P, P, P, P, SZ, P]),
             "q4_argmax_noalloc": (I32, [W, P, P, F, I32, P, P, P, P]),
+            "q4_decode_workspace_bytes": (SZ, [I32]),
+            "q4_decode_step": (I32, [P, I32, W, P, F, I32, P, P, P, P, P, P, P, P, P, SZ, P]),
+            "q4_decode_check": (I32, [P, P]),
             "q4_plan": (I32, [I32, I32, I32, I32, I32, I32, ctypes.POINTER(ctypes.c_int32)]),
             "q4_status_str": (ctypes.c_char_p, [I32]),
         }
@@ -332,3 +341,43 @@ def q4_argmax_noalloc(W: Q4Weight, x, gamma=None, eps: float = 0.0, want_val=Fal
                                    None if logits is None else logits.data_ptr(), _stream()),
            "q4_argmax_noalloc")
     return idx, val, logits
+
+
+def q4_decode_workspace_bytes(nb: int) -> int:
+    return int(lib().q4_decode_workspace_bytes(nb))
+
+
+class DecodeLayers:
+    """Host array of q4_decode_layer descriptors (keeps the tensors alive)."""
+
+    def __init__(self, layers):
+        self.layers = list(layers)
+        arr = (_CDecodeLayer * len(self.layers))()
+        for i, L in enumerate(self.layers):
+            arr[i] = _CDecodeLayer(L.Wq._c, L.Wk._c, L.Wv._c, L.Wo._c, L.Wg._c, L.Wu._c, L.Wd._c,
+                                   _dev_f32(L.gamma_in, "gamma_in").data_ptr(),
+                                   _dev_f32(L.gamma_post, "gamma_post").data_ptr(),
+                                   _dev_f32(L.attn, "attn").data_ptr())
+        self.arr = arr
+
+    def __len__(self):
+        return len(self.layers)
+
+
+def q4_decode_step(layers: DecodeLayers, Wlogits: Q4Weight, gamma_final, eps: float, x_in, hid, q, k, v, h,
+                   idx, val, workspace, n_layers: int | None = None):
+    """One decode step as a single persistent kernel (see ``q4_decode_step``
+    in the C header).  All buffers are caller-owned CUDA tensors."""
+    n = len(layers) if n_layers is None else int(n_layers)
+    nb = x_in.shape[0]
+    _check(lib().q4_decode_step(ctypes.cast(layers.arr, ctypes.c_void_p), n, Wlogits.cref(),
+                                _dev_f32(gamma_final, "gamma_final").data_ptr(), float(eps), nb,
+                                _dev_f32(x_in, "x_in").data_ptr(), _dev_f32(hid, "hid").data_ptr(),
+                                _dev_f32(q, "q").data_ptr(), _dev_f32(k, "k").data_ptr(),
+                                _dev_f32(v, "v").data_ptr(), _dev_f32(h, "h").data_ptr(), idx.data_ptr(),
+                                None if val is None else val.data_ptr(), workspace.data_ptr(),
+                                workspace.numel(), _stream()), "q4_decode_step")
+
+
+def q4_decode_check(workspace):
+    _check(lib().q4_decode_check(workspace.data_ptr(), _stream()), "q4_decode_check")

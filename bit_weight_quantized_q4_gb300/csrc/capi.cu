@@ -59,10 +59,12 @@ q4::GemvParams base_params(const q4_weight *W0, const q4_weight *W1, int mode, c
     p.w[0] = (const uint8_t *)W0->dev;
     p.n[0] = W0->n;
     p.tiles[0] = (int)q4::tiles_of(W0->n);
+    p.nmat = 1;
     if (W1) {
         p.w[1] = (const uint8_t *)W1->dev;
         p.n[1] = W1->n;
         p.tiles[1] = (int)q4::tiles_of(W1->n);
+        p.nmat = 2;
     }
     p.mode = mode;
     p.T = mode == q4::MODE_SINGLE ? p.tiles[0]
@@ -332,4 +334,191 @@ extern "C" q4_status q4_argmax_noalloc(const q4_weight *W, const float *x, const
         cudaGetLastError() != cudaSuccess)
         return Q4_ERR_CUDA;
     return Q4_OK;
+}
+
+// ---------------------------------------------------------------------------
+// The whole synthetic decode step as one persistent kernel.
+namespace {
+
+constexpr int kStepMaxGroups = 1024;  // bound on the CTAs of a step (argmax pairs)
+
+q4_status check_layer_shapes(const q4_decode_layer &L, int fmt, int hidden, int inter) {
+    const q4_weight *ws[7] = {&L.Wq, &L.Wk, &L.Wv, &L.Wo, &L.Wg, &L.Wu, &L.Wd};
+    for (const q4_weight *w : ws) {
+        Q4_TRY(check_weight(w));
+        if (w->fmt != fmt) return Q4_ERR_UNSUPPORTED;
+    }
+    if (L.Wq.k != hidden || L.Wk.k != hidden || L.Wv.k != hidden || L.Wg.k != hidden || L.Wu.k != hidden)
+        return Q4_ERR_SHAPE;
+    if (L.Wo.n != hidden || L.Wd.n != hidden || L.Wg.n != inter || L.Wu.n != inter || L.Wd.k != inter)
+        return Q4_ERR_SHAPE;
+    if (!L.gamma_in || !L.gamma_post || !L.attn) return Q4_ERR_NULL;
+    if (!aligned16(L.gamma_in) || !aligned16(L.gamma_post) || !aligned16(L.attn)) return Q4_ERR_ALIGN;
+    return Q4_OK;
+}
+
+q4::GemvParams step_job(int G, int nb) {
+    q4::GemvParams p;
+    memset(&p, 0, sizeof(p));
+    p.nb = nb;
+    p.S = 1;
+    p.groups = G;
+    return p;
+}
+
+void add_mat(q4::GemvParams &p, const q4_weight &W, float *out) {
+    const int i = p.nmat++;
+    p.w[i] = (const uint8_t *)W.dev;
+    p.n[i] = W.n;
+    p.tiles[i] = (int)q4::tiles_of(W.n);
+    p.out[i] = out;
+    p.K = W.k;
+    p.C = (int)q4::chunks_of(W.k);
+    p.Cs = p.C;
+}
+
+void finish_job(q4::GemvParams &p, int &TGmax, int &Kmax) {
+    int T = 0;
+    for (int i = 0; i < p.nmat; ++i) T += p.tiles[i];
+    if (p.mode == q4::MODE_PAIRS) T = 2 * p.tiles[0];
+    p.T = T;
+    const int pw = p.mode == q4::MODE_PAIRS ? 2 : 1;
+    const int P = T / pw;
+    if (p.groups > P) p.groups = P;  // never more groups than tile units
+    p.TG = (P + p.groups - 1) / p.groups * pw;
+    if (p.TG > TGmax) TGmax = p.TG;
+    if (p.K > Kmax) Kmax = p.K;
+}
+
+}  // namespace
+
+extern "C" size_t q4_decode_workspace_bytes(int32_t nb) {
+    if (!nb_ok(nb)) return 0;
+    return 16 + (size_t)8 * nb * kStepMaxGroups;
+}
+
+extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_layers, const q4_weight *Wlogits,
+                                    const float *gamma_final, float eps, int32_t nb, const float *x_in,
+                                    float *hid, float *q, float *k, float *v, float *h, int32_t *idx,
+                                    float *val, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (!layers || !Wlogits) return Q4_ERR_NULL;
+    if (n_layers < 1 || 4 * n_layers + 1 > q4::kMaxStepJobs) return Q4_ERR_UNSUPPORTED;
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    Q4_TRY(check_weight(Wlogits));
+    const int fmt = Wlogits->fmt;
+    const int hidden = layers[0].Wo.n, inter = layers[0].Wg.n;
+    for (int l = 0; l < n_layers; ++l) {
+        Q4_TRY(check_layer_shapes(layers[l], fmt, hidden, inter));
+        if (layers[l].Wq.n != layers[0].Wq.n || layers[l].Wk.n != layers[0].Wk.n ||
+            layers[l].Wv.n != layers[0].Wv.n || layers[l].Wo.k != layers[0].Wo.k)
+            return Q4_ERR_SHAPE;
+    }
+    if (layers[0].Wo.k != hidden) return Q4_ERR_SHAPE;  // the attention output has width hidden
+    if (Wlogits->k != hidden) return Q4_ERR_SHAPE;
+    Q4_TRY(check_act(gamma_final));
+    Q4_TRY(check_act(x_in));
+    Q4_TRY(check_act(hid));
+    Q4_TRY(check_act(q));
+    Q4_TRY(check_act(k));
+    Q4_TRY(check_act(v));
+    Q4_TRY(check_act(h));
+    if (!idx) return Q4_ERR_NULL;
+    if (!aligned16(idx) || (val && !aligned16(val))) return Q4_ERR_ALIGN;
+    if (!workspace) return Q4_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return Q4_ERR_ALIGN;
+    if (ws_bytes < q4_decode_workspace_bytes(nb)) return Q4_ERR_WORKSPACE;
+
+    const int sms = num_sms();
+    if (sms <= 0) return Q4_ERR_CUDA;
+    const int G = sms < kStepMaxGroups ? sms : kStepMaxGroups;  // one CTA per SM
+
+    // the step's jobs; the StepParams block travels as the kernel argument
+    static thread_local q4::StepParams sp;
+    memset(&sp, 0, sizeof(sp));
+    unsigned char *wsb = (unsigned char *)workspace;
+    sp.counter = (unsigned *)wsb;
+    sp.err = (int *)(wsb + 4);
+    sp.release = (unsigned *)(wsb + 8);
+    sp.idx = idx;
+    sp.val = val;
+    sp.nb = nb;
+    int TGmax = 1, Kmax = 0;
+    int nj = 0;
+    for (int l = 0; l < n_layers; ++l) {
+        const q4_decode_layer &L = layers[l];
+        const float *src = l == 0 ? x_in : hid;
+        q4::GemvParams a = step_job(G, nb);  // RMSNorm + q, k, v (one input, three weights)
+        a.mode = q4::MODE_CONCAT;
+        add_mat(a, L.Wq, q);
+        add_mat(a, L.Wk, k);
+        add_mat(a, L.Wv, v);
+        a.x = src;
+        a.gamma = L.gamma_in;
+        a.eps = eps;
+        a.epi = q4::EPI_STORE;
+        finish_job(a, TGmax, Kmax);
+        sp.jobs[nj++] = a;
+        q4::GemvParams o = step_job(G, nb);  // o projection of the attention output + residual
+        o.mode = q4::MODE_SINGLE;
+        add_mat(o, L.Wo, hid);
+        o.x = L.attn;
+        o.res = src;
+        o.epi = q4::EPI_RESIDUAL;
+        finish_job(o, TGmax, Kmax);
+        sp.jobs[nj++] = o;
+        q4::GemvParams gu = step_job(G, nb);  // RMSNorm + gate/up + SwiGLU
+        gu.mode = q4::MODE_PAIRS;
+        add_mat(gu, L.Wg, h);
+        add_mat(gu, L.Wu, nullptr);
+        gu.x = hid;
+        gu.gamma = L.gamma_post;
+        gu.eps = eps;
+        gu.epi = q4::EPI_SWIGLU;
+        finish_job(gu, TGmax, Kmax);
+        sp.jobs[nj++] = gu;
+        q4::GemvParams d = step_job(G, nb);  // down projection + residual, in place
+        d.mode = q4::MODE_SINGLE;
+        add_mat(d, L.Wd, hid);
+        d.x = h;
+        d.res = hid;
+        d.epi = q4::EPI_RESIDUAL;
+        finish_job(d, TGmax, Kmax);
+        sp.jobs[nj++] = d;
+    }
+    q4::GemvParams lg = step_job(G, nb);  // final RMSNorm + logits + per-group argmax
+    lg.mode = q4::MODE_SINGLE;
+    add_mat(lg, *Wlogits, nullptr);
+    lg.x = hid;
+    lg.gamma = gamma_final;
+    lg.eps = eps;
+    lg.epi = q4::EPI_ARGMAX;
+    lg.am_val = (float *)(wsb + 16);
+    lg.am_idx = (int *)(wsb + 16 + (size_t)4 * nb * kStepMaxGroups);
+    finish_job(lg, TGmax, Kmax);
+    sp.jobs[nj++] = lg;
+    sp.njobs = nj;
+    sp.Kmax = Kmax;
+    sp.TGmax = TGmax;
+    // every job runs on all G CTAs; a job's groups may be fewer (clipped to
+    // its tile units), and the CTAs beyond them skip that job's work
+
+    const size_t smem = q4::step_smem_bytes(fmt, TGmax, Kmax, nb);
+    if (smem > (size_t)227 * 1024) return Q4_ERR_UNSUPPORTED;
+    const int occ = fmt == Q4_FMT_Q4_0 ? q4::step_occupancy_q4_0(nb, smem) : q4::step_occupancy_affine(nb, smem);
+    if (occ < 1) return Q4_ERR_UNSUPPORTED;
+    cudaGetLastError();
+    if (cudaMemsetAsync(workspace, 0, 16, stream) != cudaSuccess) return Q4_ERR_CUDA;
+    const int rc = fmt == Q4_FMT_Q4_0 ? q4::launch_step_q4_0(sp, G, smem, stream)
+                                      : q4::launch_step_affine(sp, G, smem, stream);
+    if (rc != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
+    return Q4_OK;
+}
+
+extern "C" q4_status q4_decode_check(const void *workspace, cudaStream_t stream) {
+    if (!workspace) return Q4_ERR_NULL;
+    int err = 0;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return Q4_ERR_CUDA;
+    if (cudaMemcpy(&err, (const unsigned char *)workspace + 4, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return Q4_ERR_CUDA;
+    return err ? Q4_ERR_CUDA : Q4_OK;
 }

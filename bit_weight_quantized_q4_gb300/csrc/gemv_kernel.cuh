@@ -139,15 +139,16 @@ __device__ __forceinline__ float2 scale_pair(uint32_t w) {
 }
 
 __device__ __forceinline__ void map_tile(const GemvParams &p, int t, int &m, int &tm) {
-    if (p.mode == MODE_SINGLE) {
-        m = 0;
-        tm = t;
-    } else if (p.mode == MODE_CONCAT) {
-        m = t < p.tiles[0] ? 0 : 1;
-        tm = m ? t - p.tiles[0] : t;
-    } else {
+    if (p.mode == MODE_PAIRS) {
         m = t & 1;
         tm = t >> 1;
+        return;
+    }
+    m = 0;
+    tm = t;
+    while (m + 1 < p.nmat && tm >= p.tiles[m]) {
+        tm -= p.tiles[m];
+        ++m;
     }
 }
 
@@ -173,108 +174,181 @@ __device__ __forceinline__ void am_warp(float &bv, int &bi) {
     }
 }
 
-template <int FMT, int NT, bool NB1>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
-    constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
-    constexpr int DEPTH = kRingDepth;  // weight records per warp: 1 in use, the rest in flight
-    constexpr int GSW = 8 * NT;     // group-sum row width (activation rows, padded)
+// ---------------------------------------------------------------------------
+// The engine shared by the per-call kernel and the persistent decode-step
+// kernel.  A "job" (GemvParams) is one GEMV-shaped launch: up to three
+// matrices over one activation batch with one prologue and one epilogue.
+// Within a job, group g of `groups` owns a contiguous range of 16-row tiles
+// (gate/up pairs for SwiGLU) and cluster rank r its K-slice; the CTA's
+// (tile, chunk) records are split into contiguous ranges, one per warp.
 
-    extern __shared__ __align__(16) uint8_t smem[];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, tq = lane & 3;
-    const int nb = NB1 ? 1 : p.nb;
-    const int S = p.S;
-    const int group = blockIdx.x / S;
-    const int rank = blockIdx.x - group * S;
+struct Geo {
+    int t0, tiles_here;              // this group's tiles [t0, t0 + tiles_here)
+    int c0, cs_here, Ks, kb, ke;     // K-slice: chunks [c0, c0 + cs_here), columns [kb, ke)
+    int U, ub, ue, n_my, first_tl;   // records of the CTA; this warp's [ub, ue)
+};
+
+template <int NW>
+__device__ __forceinline__ Geo make_geo(const GemvParams &p, int group, int rank, int warp) {
+    Geo q;
     const int pw = p.mode == MODE_PAIRS ? 2 : 1;
     const int P = p.T / pw;
-    const int t0 = (int)(((long long)group * P) / p.groups) * pw;
-    const int t1 = (int)(((long long)(group + 1) * P) / p.groups) * pw;
-    const int tiles_here = t1 - t0;
-    const int c0 = rank * p.Cs;
-    const int cs_here = max(0, min(p.Cs, p.C - c0));
-    const int Ks = p.Cs * kChunkK;
-    const int kb = c0 * kChunkK;
-    const int ke = min(p.K, kb + Ks);  // real activations of this slice: [kb, ke)
-    const int xbs = 128 * nb;          // bytes of one block's activations in shared memory
+    if (group < p.groups) {
+        q.t0 = (int)(((long long)group * P) / p.groups) * pw;
+        const int t1 = (int)(((long long)(group + 1) * P) / p.groups) * pw;
+        q.tiles_here = t1 - q.t0;
+    } else {  // a job with fewer tile units than CTAs: this CTA has none
+        q.t0 = 0;
+        q.tiles_here = 0;
+    }
+    q.c0 = rank * p.Cs;
+    q.cs_here = max(0, min(p.Cs, p.C - q.c0));
+    q.Ks = p.Cs * kChunkK;
+    q.kb = q.c0 * kChunkK;
+    q.ke = min(p.K, q.kb + q.Ks);
+    q.U = q.tiles_here * q.cs_here;
+    q.ub = (warp * q.U) / NW;
+    q.ue = ((warp + 1) * q.U) / NW;
+    q.n_my = q.ue - q.ub;
+    q.first_tl = q.cs_here > 0 ? q.ub / q.cs_here : 0;
+    return q;
+}
 
-    // shared memory carve-up (sizes match smem_bytes())
-    uint8_t *xs = smem;                                                  // [Cs*4][nt][2][lanes][16 B]
-    float *gs = reinterpret_cast<float *>(smem + (size_t)4 * nb * Ks);  // [Cs*4][GSW]
-    float *red = gs + (FMT == 1 ? p.Cs * kBlocksPerChunk * GSW : 0);    // [TG][16][nb]
-    float *bslot = red + p.TG * kTileRows * nb;                         // [warp][2][16][nb]
-    float *rbuf = bslot + kWarps * 2 * kTileRows * nb;                  // [4][warp][kMaxNb]
-    float *nx = rbuf + 4 * kWarps * kMaxNb;                             // [8][kMaxNb] row stats
-    uint8_t *ring = reinterpret_cast<uint8_t *>(nx + 8 * kMaxNb) + (size_t)warp * DEPTH * REC;  // this warp's
+template <int REC>
+__device__ __forceinline__ const uint8_t *tile_ptr(const GemvParams &p, int t0, int c0, int tl) {
+    int m, tm;
+    map_tile(p, t0 + tl, m, tm);
+    return p.w[m] + ((size_t)tm * p.C + (size_t)c0) * REC;
+}
 
-    auto tile_ptr = [&](int tl) -> const uint8_t * {
-        int m, tm;
-        map_tile(p, t0 + tl, m, tm);
-        return p.w[m] + ((size_t)tm * p.C + (size_t)c0) * REC;
-    };
+// The weight records a warp streams, in order, across the jobs of a launch:
+// each job's [ub, ue) range of this warp, job after job.  The load side runs
+// up to DEPTH-1 records ahead of the compute side, across job boundaries.
+template <int REC, int NW>
+struct WeightStream {
+    const GemvParams *jobs;
+    int njobs, group, rank, warp;
+    int job, t0, c0, cs, tl, c, left, tiles;
+    const uint8_t *ptr;
 
-    // the next kernel may launch now; it waits for this one before it reads
-    // what this one writes
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-    const int U = tiles_here * cs_here;
-    const int ub = (warp * U) / kWarps, ue = ((warp + 1) * U) / kWarps;
-    const int n_my = ue - ub;
-    const int first_tl = cs_here > 0 ? ub / cs_here : 0;
-    int ltl = first_tl, lc = ub - first_tl * cs_here;
-    const uint8_t *lptr = n_my > 0 ? tile_ptr(ltl) + (size_t)lc * REC : nullptr;
-    // copy the next record of this warp's range into the ring stage at shared
-    // address `dst`: each lane its two 16-byte nibble pieces, lanes 0..7
-    // (0..15 affine) the scale (and min) words; then advance the cursor
-    const uint32_t ring_a = smem_u32(ring);
-    auto load_next = [&](uint32_t dst) {
-        const uint8_t *src = lptr + lane * 16;
+    __device__ __forceinline__ void next_job() {
+        while (left == 0 && job + 1 < njobs) {
+            ++job;
+            const Geo q = make_geo<NW>(jobs[job], group, rank, warp);
+            if (q.n_my > 0) {
+                t0 = q.t0;
+                c0 = q.c0;
+                cs = q.cs_here;
+                tiles = q.tiles_here;
+                tl = q.first_tl;
+                c = q.ub - tl * cs;
+                left = q.n_my;
+                ptr = tile_ptr<REC>(jobs[job], t0, c0, tl) + (size_t)c * REC;
+            }
+        }
+    }
+    __device__ __forceinline__ void init(const GemvParams *j, int n, int grp, int rk, int w) {
+        jobs = j;
+        njobs = n;
+        group = grp;
+        rank = rk;
+        warp = w;
+        job = -1;
+        left = 0;
+        ptr = nullptr;
+        next_job();
+    }
+    // copy the next record into the ring stage at shared address `dst`:
+    // each lane its two 16-byte nibble pieces, lanes 0..7 (0..15 affine) the
+    // scale (and min) words
+    __device__ __forceinline__ void issue(uint32_t dst, int lane) {
+        const uint8_t *src = ptr + lane * 16;
         const uint32_t d = dst + lane * 16;
         cp_async16_at<0>(d, src);
         cp_async16_at<512>(d, src);
         if (lane < (REC - 1024) / 16) cp_async16_at<1024>(d, src);
-        lptr += REC;
-        if (++lc == cs_here) {
-            lc = 0;
-            if (++ltl < tiles_here) lptr = tile_ptr(ltl);
+        ptr += REC;
+        --left;
+        if (++c == cs) {
+            c = 0;
+            if (++tl < tiles && left > 0) ptr = tile_ptr<REC>(jobs[job], t0, c0, tl);
         }
-    };
-    for (int s = 0; s < DEPTH - 1; ++s) {
-        if (s < n_my) load_next(ring_a + s * REC);
-        cp_async_commit();
+        if (left == 0) next_job();
     }
+};
 
+// Shared-memory regions of one CTA (sizes: engine_smem()).
+struct Smem {
+    uint8_t *xs;     // activation slice, hi/lo f16 in mma B-fragment order
+    float *gs;       // affine: group sums [blocks][GSW]
+    float *red;      // CTA results [TG][16][nb]
+    float *slots;    // per-warp tile partials [warp][TG][16][nb]
+    float *rbuf;     // reductions [4][warp][kMaxNb]
+    float *nx;       // row stats [8][kMaxNb]: 2 inv_rms, 3 scale, 5 inv_scale
+    uint8_t *ring;   // weight records [warp][DEPTH][REC]
+};
+
+template <int NW>
+__device__ __forceinline__ Smem carve(uint8_t *smem, int fmt, int nb, int Cs, int GSW, int TG) {
+    Smem m;
+    m.xs = smem;
+    m.gs = reinterpret_cast<float *>(smem + (size_t)4 * nb * Cs * kChunkK);
+    m.red = m.gs + (fmt == 1 ? Cs * kBlocksPerChunk * GSW : 0);
+    m.slots = m.red + TG * kTileRows * nb;
+    m.rbuf = m.slots + NW * TG * kTileRows * nb;
+    m.nx = m.rbuf + 4 * NW * kMaxNb;
+    m.ring = reinterpret_cast<uint8_t *>(m.nx + 8 * kMaxNb);
+    return m;
+}
+
+// The activation scale of a row: 2^e with bound * 2^e in [2^14, 2^15), from
+// the exponent field of `bound` (e clamped to [-100, 100]; 1 for 0 or
+// non-finite bounds; subnormal bounds take the clamp).
+__device__ __forceinline__ void row_scale(float bound, float &scale, float &inv_scale) {
+    scale = 1.f;
+    inv_scale = 1.f;
+    if (bound > 0.f && bound <= 3.0e38f) {
+        const int be = (int)((__float_as_uint(bound) >> 23) & 0xFF);  // bound in [2^(be-127), 2^(be-126))
+        int e = 14 - (be - 127);
+        e = max(-100, min(100, e));
+        scale = __uint_as_float((uint32_t)(127 + e) << 23);
+        inv_scale = __uint_as_float((uint32_t)(127 - e) << 23);
+    }
+}
+
+// Stage this CTA's activation slice of job p: per row, scale by a power of
+// two chosen from its largest magnitude (after RMSNorm when gamma is given)
+// and split into f16 hi + lo, stored in B-fragment order:
+//   per 32-column block: [n-tile][k16 step][lane g*4+t][hi(k=2t,2t+1), hi(2t+8,2t+9), lo(..), lo(..)]
+// Activation loads bypass L1 (.cg): in the persistent kernel another SM may
+// have rewritten them since this SM last read them.
+template <int FMT, int NT, bool NB1, int NW>
+__device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S, int tid, int warp, int lane) {
+    constexpr int GSW = 8 * NT;
+    constexpr int NTH = NW * 32;
+    const int nb = NB1 ? 1 : p.nb;
+    const int Ks = q.Ks, kb = q.kb, ke = q.ke;
+    const int xbs = 128 * nb;
     const bool norm = p.gamma != nullptr;
-    // nb == 1 and a slice of at most 2 * kThreads * RP columns: the whole
-    // activation slice passes through registers in a single global read
-    constexpr int RP = 16;
-    const bool fast = NB1 && Ks <= 2 * kThreads * RP;
-    float2 xv[RP], gv[RP];
-    if (NB1 && fast && norm) {
-        // gamma is a weight: load it before waiting for the previous kernel
-#pragma unroll
-        for (int q = 0; q < RP; ++q) {
-            const int k = kb + 2 * (tid + q * kThreads);
-            gv[q] = k < ke ? *reinterpret_cast<const float2 *>(p.gamma + k) : make_float2(0.f, 0.f);
-        }
-    }
-
-    // ---- activations are the previous kernel's output: wait for it.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    if (NB1 && fast) {
+    constexpr int RP = 8192 / (2 * NTH);  // nb == 1: a slice up to 8192 columns passes through registers
+    if (NB1 && Ks <= 2 * NTH * RP) {
+        const int npass = (Ks / 2 + NTH - 1) / NTH;  // pairs per thread actually used
+        float2 xv[RP], gv[RP];
         float ss = 0.f, mx = 0.f;
 #pragma unroll
-        for (int q = 0; q < RP; ++q) {
-            const int k = kb + 2 * (tid + q * kThreads);
-            float2 v = make_float2(0.f, 0.f);
-            if (k < ke) v = *reinterpret_cast<const float2 *>(p.x + k);
-            xv[q] = v;
+        for (int qq = 0; qq < RP; ++qq) {
+            if (qq >= npass) break;
+            float2 v = make_float2(0.f, 0.f), gm = make_float2(1.f, 1.f);
+            const int k = kb + 2 * (tid + qq * NTH);
+            if (k < ke) {
+                v = __ldcg(reinterpret_cast<const float2 *>(p.x + k));
+                if (norm) gm = *reinterpret_cast<const float2 *>(p.gamma + k);
+            }
+            xv[qq] = v;
+            gv[qq] = gm;
             ss = fmaf(v.x, v.x, ss);
             ss = fmaf(v.y, v.y, ss);
-            const float ax = norm ? fabsf(v.x * gv[q].x) : fabsf(v.x);
-            const float ay = norm ? fabsf(v.y * gv[q].y) : fabsf(v.y);
-            mx = fmaxf(mx, fmaxf(ax, ay));
+            mx = fmaxf(mx, fmaxf(fabsf(norm ? v.x * gm.x : v.x), fabsf(norm ? v.y * gm.y : v.y)));
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -282,47 +356,41 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         }
         if (lane == 0) {
-            rbuf[warp] = ss;
-            rbuf[kWarps + warp] = mx;
+            m.rbuf[warp] = ss;
+            m.rbuf[NW + warp] = mx;
         }
         __syncthreads();
         float tss = 0.f, tmx = 0.f;  // every thread adds the warps in the same order
-        for (int w = 0; w < kWarps; ++w) {
-            tss += rbuf[w];
-            tmx = fmaxf(tmx, rbuf[kWarps + w]);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            tss += m.rbuf[w];
+            tmx = fmaxf(tmx, m.rbuf[NW + w]);
         }
         if (norm && S > 1) {
             // the RMS needs the whole row: add the slices' sums in rank order
             cg::cluster_group cluster = cg::this_cluster();
-            if (tid == 0) nx[0] = tss;
+            if (tid == 0) m.nx[0] = tss;
             cluster.sync();
             tss = 0.f;
-            for (int q = 0; q < S; ++q) tss += cluster.map_shared_rank(nx, q)[0];
+            for (int r = 0; r < S; ++r) tss += cluster.map_shared_rank(m.nx, r)[0];
         }
         const float inv_rms = norm ? 1.0f / sqrtf(tss / (float)p.K + p.eps) : 1.f;
-        const float bound = tmx * inv_rms;
-        float scale = 1.f, inv_scale = 1.f;
-        if (bound > 0.f && bound <= 3.0e38f) {
-            int ex;
-            frexpf(bound, &ex);  // bound in [2^(ex-1), 2^ex)
-            int e = 15 - ex;     // bound * 2^e in [2^14, 2^15)
-            e = max(-100, min(100, e));
-            scale = ldexpf(1.f, e);
-            inv_scale = ldexpf(1.f, -e);
-        }
+        float scale, inv_scale;
+        row_scale(tmx * inv_rms, scale, inv_scale);
         if (tid == 0) {
-            nx[2 * kMaxNb] = inv_rms;
-            nx[3 * kMaxNb] = scale;
-            nx[5 * kMaxNb] = inv_scale;
+            m.nx[2 * kMaxNb] = inv_rms;
+            m.nx[3 * kMaxNb] = scale;
+            m.nx[5 * kMaxNb] = inv_scale;
         }
 #pragma unroll
-        for (int q = 0; q < RP; ++q) {
-            const int kl = 2 * (tid + q * kThreads);
+        for (int qq = 0; qq < RP; ++qq) {
+            if (qq >= npass) break;
+            const int kl = 2 * (tid + qq * NTH);
             if (kl < Ks) {
-                float v0 = xv[q].x, v1 = xv[q].y;
+                float v0 = xv[qq].x, v1 = xv[qq].y;
                 if (norm) {
-                    v0 = v0 * inv_rms * gv[q].x;
-                    v1 = v1 * inv_rms * gv[q].y;
+                    v0 = v0 * inv_rms * gv[qq].x;
+                    v1 = v1 * inv_rms * gv[qq].y;
                 }
                 v0 *= scale;
                 v1 *= scale;
@@ -331,165 +399,171 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
                 __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
                 const int kk = kl & 31, k16 = kk & 15;
                 const int off = (kl >> 5) * 128 + (kk >> 4) * 64 + ((k16 & 7) >> 1) * 16 + (k16 >> 3) * 4;
-                *reinterpret_cast<__half2 *>(xs + off) = hi;
-                *reinterpret_cast<__half2 *>(xs + off + 8) = lo;
+                *reinterpret_cast<__half2 *>(m.xs + off) = hi;
+                *reinterpret_cast<__half2 *>(m.xs + off + 8) = lo;
             }
         }
         if (FMT == 1) {
-            __syncthreads();  // row stats visible to the group-sum loop
             const int nblk = p.Cs * kBlocksPerChunk;
-            for (int i = tid; i < GSW * nblk; i += kThreads) {
+            for (int i = tid; i < GSW * nblk; i += NTH) {
                 const int r = i / nblk, bl = i - r * nblk;
                 const int kblk = kb + 32 * bl;
                 float sacc = 0.f;
                 if (r == 0 && kblk < ke) {
                     if (p.gsum != nullptr && !norm) {
-                        sacc = p.gsum[kblk / 32];
+                        sacc = __ldcg(p.gsum + kblk / 32);
                     } else {
+                        float vv[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) vv[e] = __ldcg(p.x + kblk + e);
+#pragma unroll
                         for (int e = 0; e < 32; ++e) {
-                            float v = p.x[kblk + e];
+                            float v = vv[e];
                             if (norm) v = v * inv_rms * p.gamma[kblk + e];
                             sacc += v;
                         }
                     }
                     sacc *= scale;
                 }
-                gs[bl * GSW + r] = sacc;
-            }
-        }
-    } else {
-        // pass 1: per activation row, sum of squares and max |x*gamma| (or |x|)
-        for (int r = 0; r < nb; ++r) {
-            float ss = 0.f, mx = 0.f;
-            const float *xr = p.x + (size_t)r * p.K;
-            for (int k = kb + 2 * tid; k < ke; k += 2 * kThreads) {
-                float2 v = *reinterpret_cast<const float2 *>(xr + k);
-                ss = fmaf(v.x, v.x, ss);
-                ss = fmaf(v.y, v.y, ss);
-                if (norm) {
-                    float2 gm = *reinterpret_cast<const float2 *>(p.gamma + k);
-                    mx = fmaxf(mx, fmaxf(fabsf(v.x * gm.x), fabsf(v.y * gm.y)));
-                } else {
-                    mx = fmaxf(mx, fmaxf(fabsf(v.x), fabsf(v.y)));
-                }
-            }
-    #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            }
-            if (lane == 0) {
-                rbuf[warp * kMaxNb + r] = ss;
-                rbuf[kWarps * kMaxNb + warp * kMaxNb + r] = mx;
+                m.gs[bl * GSW + r] = sacc;
             }
         }
         __syncthreads();
-        if (tid < nb) {
-            float ss = 0.f, mx = 0.f;
-            for (int w = 0; w < kWarps; ++w) {
-                ss += rbuf[w * kMaxNb + tid];
-                mx = fmaxf(mx, rbuf[kWarps * kMaxNb + w * kMaxNb + tid]);
+        return;
+    }
+    // general nb: two passes over the slice
+    for (int r = 0; r < nb; ++r) {
+        float ss = 0.f, mx = 0.f;
+        const float *xr = p.x + (size_t)r * p.K;
+        for (int k = kb + 2 * tid; k < ke; k += 2 * NTH) {
+            float2 v = __ldcg(reinterpret_cast<const float2 *>(xr + k));
+            ss = fmaf(v.x, v.x, ss);
+            ss = fmaf(v.y, v.y, ss);
+            if (norm) {
+                float2 gm = *reinterpret_cast<const float2 *>(p.gamma + k);
+                mx = fmaxf(mx, fmaxf(fabsf(v.x * gm.x), fabsf(v.y * gm.y)));
+            } else {
+                mx = fmaxf(mx, fmaxf(fabsf(v.x), fabsf(v.y)));
             }
-            nx[0 * kMaxNb + tid] = ss;  // this slice's sum of squares
-            nx[1 * kMaxNb + tid] = mx;
         }
-        if (norm && S > 1) {
-            // the RMS needs the whole row: add the slices' sums in rank order
-            cg::cluster_group cluster = cg::this_cluster();
-            cluster.sync();
-            if (tid < nb) {
-                float tot = 0.f;
-                for (int q = 0; q < S; ++q) tot += cluster.map_shared_rank(nx, q)[tid];
-                nx[4 * kMaxNb + tid] = tot;
-            }
-        } else if (tid < nb) {
-            nx[4 * kMaxNb + tid] = nx[tid];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         }
-        __syncthreads();
-        if (tid < nb) {
-            float inv_rms = 1.f;
-            if (norm) inv_rms = 1.0f / sqrtf(nx[4 * kMaxNb + tid] / (float)p.K + p.eps);
-            float bound = nx[1 * kMaxNb + tid] * inv_rms;
-            float scale = 1.f, inv_scale = 1.f;
-            if (bound > 0.f && bound <= 3.0e38f) {
-                int ex;
-                frexpf(bound, &ex);  // bound in [2^(ex-1), 2^ex)
-                int e = 15 - ex;     // bound * 2^e in [2^14, 2^15)
-                e = max(-100, min(100, e));
-                scale = ldexpf(1.f, e);
-                inv_scale = ldexpf(1.f, -e);
-            }
-            nx[2 * kMaxNb + tid] = inv_rms;
-            nx[3 * kMaxNb + tid] = scale;
-            nx[5 * kMaxNb + tid] = inv_scale;
-        }
-        __syncthreads();
-
-        // pass 2: scaled (and normed) activations as hi + lo f16 pairs, stored
-        // per block in the order the lanes load their mma B fragments:
-        //   [n-tile][k16 step][lane g*4+t][hi(k=2t,2t+1), hi(2t+8,2t+9), lo(..), lo(..)]
-        {
-            const int half_ks = Ks >> 1;
-            for (int i = tid; i < nb * half_ks; i += kThreads) {
-                const int r = i / half_ks, kp = i - r * half_ks;
-                const int kl = 2 * kp, k = kb + kl;
-                float v0 = 0.f, v1 = 0.f;
-                if (k < ke) {
-                    float2 v = *reinterpret_cast<const float2 *>(p.x + (size_t)r * p.K + k);
-                    v0 = v.x;
-                    v1 = v.y;
-                    if (norm) {
-                        const float ir = nx[2 * kMaxNb + r];
-                        float2 gm = *reinterpret_cast<const float2 *>(p.gamma + k);
-                        v0 = v0 * ir * gm.x;
-                        v1 = v1 * ir * gm.y;
-                    }
-                }
-                const float sc = nx[3 * kMaxNb + r];
-                v0 *= sc;
-                v1 *= sc;
-                __half2 hi = __floats2half2_rn(v0, v1);
-                float2 hf = __half22float2(hi);
-                __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
-                const int bl = kl >> 5, kk = kl & 31, st = kk >> 4, k16 = kk & 15;
-                const int nt = r >> 3, cols = min(8, nb - 8 * nt);
-                const int off = bl * xbs + nt * 1024 + st * 64 * cols + (4 * (r & 7) + ((k16 & 7) >> 1)) * 16 +
-                                (k16 >> 3) * 4;
-                *reinterpret_cast<__half2 *>(xs + off) = hi;
-                *reinterpret_cast<__half2 *>(xs + off + 8) = lo;
-            }
-            if (FMT == 1) {
-                // per-32 group sums of the (normed) activations, ascending order
-                const int nblk = p.Cs * kBlocksPerChunk;
-                for (int i = tid; i < GSW * nblk; i += kThreads) {
-                    const int r = i / nblk, bl = i - r * nblk;
-                    const int kblk = kb + 32 * bl;
-                    float s = 0.f;
-                    if (r < nb && kblk < ke) {
-                        if (p.gsum != nullptr && !norm) {
-                            s = p.gsum[(size_t)r * (p.K / 32) + kblk / 32];
-                        } else {
-                            const float *xr = p.x + (size_t)r * p.K + kblk;
-                            const float ir = nx[2 * kMaxNb + r];
-                            for (int e = 0; e < 32; ++e) {
-                                float v = xr[e];
-                                if (norm) v = v * ir * p.gamma[kblk + e];
-                                s += v;
-                            }
-                        }
-                        s *= nx[3 * kMaxNb + r];
-                    }
-                    gs[bl * GSW + r] = s;
-                }
-            }
+        if (lane == 0) {
+            m.rbuf[warp * kMaxNb + r] = ss;
+            m.rbuf[NW * kMaxNb + warp * kMaxNb + r] = mx;
         }
     }
     __syncthreads();
+    if (tid < nb) {
+        float ss = 0.f, mx = 0.f;
+        for (int w = 0; w < NW; ++w) {
+            ss += m.rbuf[w * kMaxNb + tid];
+            mx = fmaxf(mx, m.rbuf[NW * kMaxNb + w * kMaxNb + tid]);
+        }
+        m.nx[0 * kMaxNb + tid] = ss;  // this slice's sum of squares
+        m.nx[1 * kMaxNb + tid] = mx;
+    }
+    if (norm && S > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        if (tid < nb) {
+            float tot = 0.f;
+            for (int r = 0; r < S; ++r) tot += cluster.map_shared_rank(m.nx, r)[tid];
+            m.nx[4 * kMaxNb + tid] = tot;
+        }
+    } else if (tid < nb) {
+        m.nx[4 * kMaxNb + tid] = m.nx[tid];
+    }
+    __syncthreads();
+    if (tid < nb) {
+        float inv_rms = 1.f;
+        if (norm) inv_rms = 1.0f / sqrtf(m.nx[4 * kMaxNb + tid] / (float)p.K + p.eps);
+        float scale, inv_scale;
+        row_scale(m.nx[1 * kMaxNb + tid] * inv_rms, scale, inv_scale);
+        m.nx[2 * kMaxNb + tid] = inv_rms;
+        m.nx[3 * kMaxNb + tid] = scale;
+        m.nx[5 * kMaxNb + tid] = inv_scale;
+    }
+    __syncthreads();
+    const int half_ks = Ks >> 1;
+    for (int i = tid; i < nb * half_ks; i += NTH) {
+        const int r = i / half_ks, kp = i - r * half_ks;
+        const int kl = 2 * kp, k = kb + kl;
+        float v0 = 0.f, v1 = 0.f;
+        if (k < ke) {
+            float2 v = __ldcg(reinterpret_cast<const float2 *>(p.x + (size_t)r * p.K + k));
+            v0 = v.x;
+            v1 = v.y;
+            if (norm) {
+                const float ir = m.nx[2 * kMaxNb + r];
+                float2 gm = *reinterpret_cast<const float2 *>(p.gamma + k);
+                v0 = v0 * ir * gm.x;
+                v1 = v1 * ir * gm.y;
+            }
+        }
+        const float sc = m.nx[3 * kMaxNb + r];
+        v0 *= sc;
+        v1 *= sc;
+        __half2 hi = __floats2half2_rn(v0, v1);
+        float2 hf = __half22float2(hi);
+        __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+        const int bl = kl >> 5, kk = kl & 31, st = kk >> 4, k16 = kk & 15;
+        const int nt = r >> 3, cols = min(8, nb - 8 * nt);
+        const int off = bl * xbs + nt * 1024 + st * 64 * cols + (4 * (r & 7) + ((k16 & 7) >> 1)) * 16 +
+                        (k16 >> 3) * 4;
+        *reinterpret_cast<__half2 *>(m.xs + off) = hi;
+        *reinterpret_cast<__half2 *>(m.xs + off + 8) = lo;
+    }
+    if (FMT == 1) {
+        const int nblk = p.Cs * kBlocksPerChunk;
+        for (int i = tid; i < GSW * nblk; i += NTH) {
+            const int r = i / nblk, bl = i - r * nblk;
+            const int kblk = kb + 32 * bl;
+            float s = 0.f;
+            if (r < nb && kblk < ke) {
+                if (p.gsum != nullptr && !norm) {
+                    s = __ldcg(p.gsum + (size_t)r * (p.K / 32) + kblk / 32);
+                } else {
+                    const float *xr = p.x + (size_t)r * p.K + kblk;
+                    const float ir = m.nx[2 * kMaxNb + r];
+                    float vv[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) vv[e] = __ldcg(xr + e);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float v = vv[e];
+                        if (norm) v = v * ir * p.gamma[kblk + e];
+                        s += v;
+                    }
+                }
+                s *= m.nx[3 * kMaxNb + r];
+            }
+            m.gs[bl * GSW + r] = s;
+        }
+    }
+    __syncthreads();
+}
 
-    // ---- main loop over this warp's contiguous (tile, chunk) units
+// This warp's records of one job: dequantise, tensor-core dot products,
+// per-block scaling; each tile's partial goes to this warp's slot.
+// Consumes one ring stage per record and refills it from `ws`.
+template <int FMT, int NT, bool NB1, int DEPTH, int NW>
+__device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m,
+                          WeightStream<FMT == 0 ? kRecQ4_0 : kRecAffine, NW> &ws, uint32_t &st_a, uint32_t &fill_a,
+                          uint32_t ring_a, int warp, int lane) {
+    constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
+    constexpr int GSW = 8 * NT;
+    const int g = lane >> 2, tq = lane & 3;
+    const int nb = NB1 ? 1 : p.nb;
+    const int xbs = 128 * nb;
+    const int cs_here = q.cs_here;
+    const uint32_t ring_end = ring_a + DEPTH * REC;
     // lanes beyond the batch read a duplicate column: its mma outputs are
     // never stored, and every lane loads unconditionally
-    const uint32_t xs_a = smem_u32(xs);
+    const uint32_t xs_a = smem_u32(m.xs);
     uint32_t xoff[NT];
     int hstr[NT];
 #pragma unroll
@@ -501,13 +575,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
     float acc[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    int ctl = first_tl, cc = ub - first_tl * cs_here;
+    int ctl = q.first_tl, cc = q.ub - q.first_tl * cs_here;
     const float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+    float *my_slots = m.slots + (size_t)warp * p.TG * kTileRows * nb;
 
     auto flush = [&](int tl) {
-        const bool complete = tl * cs_here >= ub && (tl + 1) * cs_here <= ue;
-        float *dst = complete ? red + (size_t)tl * kTileRows * nb
-                              : bslot + (size_t)(warp * 2 + (tl == first_tl ? 0 : 1)) * kTileRows * nb;
+        float *dst = my_slots + (size_t)tl * kTileRows * nb;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const int a0 = 8 * j + 2 * tq;
@@ -555,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
             }
             if (FMT == 1) {
                 const float2 mm = scale_pair<FMT>(mnw);
-                const float2 gv = *reinterpret_cast<const float2 *>(gs + blk * GSW + 8 * nt + 2 * tq);
+                const float2 gv = *reinterpret_cast<const float2 *>(m.gs + blk * GSW + 8 * nt + 2 * tq);
                 acc[nt][0] = fmaf(mm.x, gv.x, acc[nt][0]);
                 acc[nt][2] = fmaf(mm.y, gv.x, acc[nt][2]);
                 if (!NB1) {
@@ -566,13 +639,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
         }
     };
 
-    uint32_t st_a = ring_a;                           // stage being consumed
-    uint32_t fill_a = ring_a + (DEPTH - 1) * REC;     // stage to refill
-    const uint32_t ring_end = ring_a + DEPTH * REC;
-    for (int i = 0; i < n_my; ++i) {
-        cp_async_wait<DEPTH - 2>();  // this lane's copies of record i have landed
+    for (int i = 0; i < q.n_my; ++i) {
+        cp_async_wait<DEPTH - 2>();  // this lane's copies of the record have landed
         __syncwarp();                 // ... and every lane's; the previous stage is free
-        if (i + DEPTH - 1 < n_my) load_next(fill_a);
+        if (ws.left > 0) ws.issue(fill_a, lane);
         cp_async_commit();
         fill_a += REC;
         if (fill_a == ring_end) fill_a = ring_a;
@@ -595,63 +665,68 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
             ++ctl;
         }
     }
-    cp_async_wait<0>();
-    if (n_my > 0 && cc != 0) flush(ctl);  // the range ended inside a tile
-    __syncthreads();
+    if (q.n_my > 0 && cc != 0) flush(ctl);  // the range ended inside a tile
+}
 
-    // ---- tiles split between warps: add their parts in warp order; then
-    // undo the activation scale
-    const int total = tiles_here * kTileRows * nb;
-    for (int idx = tid; idx < total; idx += kThreads) {
+// Sum the warps' partials of each tile in warp order (only the warps whose
+// record range touched the tile), undo the activation scale; then (cluster)
+// fold the K-slices into rank 0.  Returns false on cluster ranks other than
+// 0, which have nothing left to do.
+template <bool NB1, int NW>
+__device__ bool fold_tiles(const GemvParams &p, const Geo &q, const Smem &m, int S, int rank, int tid) {
+    constexpr int NTH = NW * 32;
+    const int nb = NB1 ? 1 : p.nb;
+    const int cs = q.cs_here, U = q.U;
+    const int total = q.tiles_here * kTileRows * nb;
+    const size_t wstride = (size_t)p.TG * kTileRows * nb;
+    for (int idx = tid; idx < total; idx += NTH) {
         const int tl = idx / (kTileRows * nb);
-        const int rem = idx - tl * kTileRows * nb;
+        const int u0 = tl * cs, u1 = u0 + cs;  // this tile's records [u0, u1)
         float v = 0.f;
-        if (cs_here > 0) {
-            const int u_first = tl * cs_here, u_last = u_first + cs_here - 1;
-            const int w_first = (kWarps * (u_first + 1) + U - 1) / U - 1;
-            const int w_last = (kWarps * (u_last + 1) + U - 1) / U - 1;
-            if (w_first == w_last) {
-                v = red[idx];
-            } else {
-                for (int w = w_first; w <= w_last; ++w) {
-                    const int wub = (w * U) / kWarps;
-                    if (((w + 1) * U) / kWarps == wub) continue;  // this warp had no units
-                    const int slot = (tl == wub / cs_here) ? 0 : 1;
-                    v += bslot[(size_t)(w * 2 + slot) * kTileRows * nb + rem];
-                }
-            }
+#pragma unroll 4
+        for (int w = 0; w < NW; ++w) {
+            const int wub = (w * U) / NW, wue = ((w + 1) * U) / NW;
+            if (max(wub, u0) < min(wue, u1)) v += m.slots[(size_t)w * wstride + idx];
         }
-        red[idx] = v * nx[5 * kMaxNb + (rem % nb)];
+        m.red[idx] = v * m.nx[5 * kMaxNb + (idx % nb)];
     }
     if (S > 1) {
-        // fold the K-slices of the cluster into rank 0, in rank order
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();
         if (rank == 0) {
-            for (int idx = tid; idx < total; idx += kThreads) {
-                float v = red[idx];
-                for (int q = 1; q < S; ++q) v += cluster.map_shared_rank(red, q)[idx];
-                red[idx] = v;
+            for (int idx = tid; idx < total; idx += NTH) {
+                float v = m.red[idx];
+                for (int r = 1; r < S; ++r) v += cluster.map_shared_rank(m.red, r)[idx];
+                m.red[idx] = v;
             }
         }
         cluster.sync();
-        if (rank != 0) return;
+        if (rank != 0) return false;
     } else {
         __syncthreads();
     }
+    return true;
+}
 
-    // ---- epilogue
+// Write the job's outputs from `red`: store, residual add, SwiGLU over a
+// gate/up tile pair, or this group's (max, index) per activation row.
+template <bool NB1, int NW>
+__device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int group, int tid, int warp, int lane) {
+    constexpr int NTH = NW * 32;
+    const int nb = NB1 ? 1 : p.nb;
+    const int total = q.tiles_here * kTileRows * nb;
+    if (group >= p.groups) return;  // no tiles, no partials
     if (p.epi == EPI_ARGMAX) {
         const int N = p.n[0];
-        float *bvs = rbuf;                       // [warp]
-        int *bis = reinterpret_cast<int *>(rbuf + kWarps);
+        float *bvs = m.rbuf;  // [warp]
+        int *bis = reinterpret_cast<int *>(m.rbuf + NW);
         for (int r = 0; r < nb; ++r) {
             float bv = -INFINITY;
             int bi = 0x7fffffff;
-            for (int ri = tid; ri < tiles_here * kTileRows; ri += kThreads) {
-                const int n = (t0 + ri / kTileRows) * kTileRows + (ri % kTileRows);
+            for (int ri = tid; ri < q.tiles_here * kTileRows; ri += NTH) {
+                const int n = (q.t0 + ri / kTileRows) * kTileRows + (ri % kTileRows);
                 if (n >= N) continue;
-                const float v = red[ri * nb + r];
+                const float v = m.red[ri * nb + r];
                 if (p.out[0] != nullptr) p.out[0][(size_t)r * N + n] = v;
                 am_take(bv, bi, v, n);
             }
@@ -664,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
             if (tid == 0) {
                 float fv = bvs[0];
                 int fi = bis[0];
-                for (int w = 1; w < kWarps; ++w) {
+                for (int w = 1; w < NW; ++w) {
                     if (bvs[w] > fv || (bvs[w] == fv && bis[w] < fi)) {
                         fv = bvs[w];
                         fi = bis[w];
@@ -677,23 +752,215 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
         }
         return;
     }
-    for (int idx = tid; idx < total; idx += kThreads) {
+    for (int idx = tid; idx < total; idx += NTH) {
         const int tl = idx / (kTileRows * nb);
         const int rem = idx - tl * kTileRows * nb;
         const int row = rem / nb, r = rem - row * nb;
-        int m, tm;
-        map_tile(p, t0 + tl, m, tm);
+        int mi, tm;
+        map_tile(p, q.t0 + tl, mi, tm);
         const int n = tm * kTileRows + row;
-        const int N = p.n[m];
+        const int N = p.n[mi];
         if (n >= N) continue;
-        const float v = red[idx];
+        const float v = m.red[idx];
         if (p.epi == EPI_STORE) {
-            p.out[m][(size_t)r * N + n] = v;
+            p.out[mi][(size_t)r * N + n] = v;
         } else if (p.epi == EPI_RESIDUAL) {
-            p.out[0][(size_t)r * N + n] = v + p.res[(size_t)r * N + n];
-        } else if (m == 0) {  // EPI_SWIGLU: gate tile tl, up tile tl + 1
-            const float u = red[idx + kTileRows * nb];
+            p.out[0][(size_t)r * N + n] = v + __ldcg(p.res + (size_t)r * N + n);
+        } else if (mi == 0) {  // EPI_SWIGLU: gate tile tl, up tile tl + 1
+            const float u = m.red[idx + kTileRows * nb];
             p.out[0][(size_t)r * N + n] = v / (1.0f + expf(-v)) * u;
+        }
+    }
+    __syncthreads();
+}
+
+// Single K-slice, store / residual / SwiGLU jobs: fold each output's warp
+// partials (in warp order) and write it at once, with no round trip through
+// `red` and one barrier fewer than fold_tiles + epilogue.
+template <bool NB1, int NW>
+__device__ void fold_store(const GemvParams &p, const Geo &q, const Smem &m, int group, int tid) {
+    constexpr int NTH = NW * 32;
+    const int nb = NB1 ? 1 : p.nb;
+    if (group >= p.groups) return;  // no tiles
+    const int cs = q.cs_here, U = q.U;
+    const size_t wstride = (size_t)p.TG * kTileRows * nb;
+    const int tile_vals = kTileRows * nb;
+    auto fold = [&](int idx) -> float {
+        const int tl = idx / tile_vals;
+        const int u0 = tl * cs, u1 = u0 + cs;  // this tile's records [u0, u1)
+        float v = 0.f;
+#pragma unroll 4
+        for (int w = 0; w < NW; ++w) {
+            const int wub = (w * U) / NW, wue = ((w + 1) * U) / NW;
+            if (max(wub, u0) < min(wue, u1)) v += m.slots[(size_t)w * wstride + idx];
+        }
+        return v * m.nx[5 * kMaxNb + (idx % nb)];
+    };
+    const bool pairs = p.epi == EPI_SWIGLU;
+    const int total = (pairs ? q.tiles_here / 2 : q.tiles_here) * tile_vals;
+    for (int e = tid; e < total; e += NTH) {
+        const int tp = e / tile_vals, rem = e - tp * tile_vals;
+        const int idx = (pairs ? 2 * tp : tp) * tile_vals + rem;
+        const int row = rem / nb, r = rem - row * nb;
+        int mi, tm;
+        map_tile(p, q.t0 + idx / tile_vals, mi, tm);
+        const int n = tm * kTileRows + row;
+        const int N = p.n[mi];
+        if (n >= N) continue;
+        const float v = fold(idx);
+        if (p.epi == EPI_STORE) {
+            p.out[mi][(size_t)r * N + n] = v;
+        } else if (p.epi == EPI_RESIDUAL) {
+            p.out[0][(size_t)r * N + n] = v + __ldcg(p.res + (size_t)r * N + n);
+        } else {  // SwiGLU: gate tile, then its up tile
+            const float u = fold(idx + tile_vals);
+            p.out[0][(size_t)r * N + n] = v / (1.0f + expf(-v)) * u;
+        }
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Per-call kernel: one job, one group of tiles per cluster.
+template <int FMT, int NT, bool NB1>
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ GemvParams p) {
+    constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
+    constexpr int DEPTH = kRingDepth;
+    constexpr int NW = kWarps;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = p.S;
+    const int group = blockIdx.x / S, rank = blockIdx.x - group * S;
+    const int nb = NB1 ? 1 : p.nb;
+    const Smem m = carve<NW>(smem, FMT, nb, p.Cs, 8 * NT, p.TG);
+    const uint32_t ring_a = smem_u32(m.ring) + warp * DEPTH * REC;
+
+    // the next kernel may launch now; it waits for this one before it reads
+    // what this one writes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // weights do not depend on the previous kernel: start their copies first
+    WeightStream<REC, NW> ws;
+    ws.init(&p, 1, group, rank, warp);
+    for (int s = 0; s < DEPTH - 1; ++s) {
+        if (ws.left > 0) ws.issue(ring_a + s * REC, lane);
+        cp_async_commit();
+    }
+    const Geo q = make_geo<NW>(p, group, rank, warp);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    stage_x<FMT, NT, NB1, NW>(p, q, m, S, tid, warp, lane);
+    uint32_t st_a = ring_a, fill_a = ring_a + (DEPTH - 1) * REC;
+    run_units<FMT, NT, NB1, DEPTH, NW>(p, q, m, ws, st_a, fill_a, ring_a, warp, lane);
+    cp_async_wait<0>();
+    __syncthreads();
+    if (S == 1 && p.epi != EPI_ARGMAX) {
+        fold_store<NB1, NW>(p, q, m, group, tid);
+        return;
+    }
+    if (!fold_tiles<NB1, NW>(p, q, m, S, rank, tid)) return;
+    epilogue<NB1, NW>(p, q, m, group, tid, warp, lane);
+}
+
+// ---------------------------------------------------------------------------
+// Persistent decode-step kernel: one CTA per SM runs the step's jobs in
+// order, separated by grid-wide barriers; the weight stream of every warp
+// runs ahead across job boundaries, so weights keep arriving while the CTA
+// waits at a barrier or stages the next job's activations.
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid barrier number `b` (1-based).  Each CTA adds one to the arrival
+// counter; the CTA that completes the count publishes `b` in the release
+// word, which the others poll (a read-only line, away from the atomics).
+// The wait is bounded: after kBarrierSpins polls the CTA records the failure
+// in *err and the caller stops.
+__device__ __forceinline__ bool grid_barrier(unsigned *counter, unsigned *release, int *err, unsigned b) {
+    __syncthreads();
+    __shared__ int fail;
+    if (threadIdx.x == 0) {
+        fail = 0;
+        __threadfence();
+        const unsigned prev = atomicAdd(counter, 1u);
+        if (prev + 1 == b * gridDim.x) {
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(release), "r"(b) : "memory");
+        } else {
+            long long it = 0;
+            while (ld_acquire_u32(release) < b) {
+                if (++it > kBarrierSpins) {
+                    atomicExch(err, 1);
+                    fail = 1;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return fail == 0;
+}
+
+template <int FMT, int NT, bool NB1>
+__global__ void __launch_bounds__(kStepWarps * 32, 1) decode_kernel(const __grid_constant__ StepParams sp) {
+    constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
+    constexpr int DEPTH = kStepRingDepth;
+    constexpr int NW = kStepWarps;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int group = blockIdx.x;
+    const int nb = NB1 ? 1 : sp.nb;
+    const int cs_max = (sp.Kmax + kChunkK - 1) / kChunkK;  // as the host sized it
+    const Smem m = carve<NW>(smem, FMT, nb, cs_max, 8 * NT, sp.TGmax);
+    const uint32_t ring_a = smem_u32(m.ring) + warp * DEPTH * REC;
+
+    WeightStream<REC, NW> ws;
+    ws.init(sp.jobs, sp.njobs, group, 0, warp);
+    for (int s = 0; s < DEPTH - 1; ++s) {
+        if (ws.left > 0) ws.issue(ring_a + s * REC, lane);
+        cp_async_commit();
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    uint32_t st_a = ring_a, fill_a = ring_a + (DEPTH - 1) * REC;
+    for (int j = 0; j < sp.njobs; ++j) {
+        const GemvParams &p = sp.jobs[j];
+        if (j > 0 && !grid_barrier(sp.counter, sp.release, sp.err, (unsigned)j)) return;
+        const Geo q = make_geo<NW>(p, group, 0, warp);
+        stage_x<FMT, NT, NB1, NW>(p, q, m, 1, tid, warp, lane);
+        run_units<FMT, NT, NB1, DEPTH, NW>(p, q, m, ws, st_a, fill_a, ring_a, warp, lane);
+        __syncthreads();
+        if (p.epi != EPI_ARGMAX) {
+            fold_store<NB1, NW>(p, q, m, group, tid);
+        } else {
+            fold_tiles<NB1, NW>(p, q, m, 1, 0, tid);
+            epilogue<NB1, NW>(p, q, m, group, tid, warp, lane);
+        }
+    }
+    cp_async_wait<0>();
+    // the last job is the logits argmax: fold the groups' pairs in order
+    if (!grid_barrier(sp.counter, sp.release, sp.err, (unsigned)sp.njobs)) return;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const GemvParams &pl = sp.jobs[sp.njobs - 1];
+    if (group == 0 && tid < 32) {
+        for (int r = 0; r < nb; ++r) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int i = lane; i < pl.groups; i += 32) {
+                const float v = __ldcg(pl.am_val + (size_t)r * pl.groups + i);
+                const int k = __ldcg(pl.am_idx + (size_t)r * pl.groups + i);
+                if (v > bv || (v == bv && k < bi)) {
+                    bv = v;
+                    bi = k;
+                }
+            }
+            am_warp(bv, bi);
+            if (lane == 0) {
+                sp.idx[r] = bi;
+                if (sp.val) sp.val[r] = bv;
+            }
         }
     }
 }

@@ -47,48 +47,81 @@ inline int64_t chunks_of(int64_t k) { return (k + kChunkK - 1) / kChunkK; }
 enum Mode { MODE_SINGLE = 0, MODE_CONCAT = 1, MODE_PAIRS = 2 };
 enum Epi { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;                 // per-call kernel: 8 warps per CTA
 constexpr int kWarps = kThreads / 32;
+constexpr int kStepWarps = 16;               // persistent decode-step kernel: 16 warps per CTA
 constexpr int kMaxNb = 16;
 constexpr int kMaxCluster = 8;
 constexpr size_t kXsCap = 64 * 1024;          // activation slice staged per CTA
 constexpr int kRingDepth = 8;                 // weight records per warp in the cp.async ring
 
+constexpr int kMaxMats = 3;                // matrices of one job (q, k, v share one input)
+
 struct GemvParams {
-    const uint8_t *w[2];   // packed weights of (up to) two matrices
-    int n[2];              // output rows of each matrix
-    int tiles[2];          // 16-row tiles of each matrix
-    int mode;              // Mode
-    int T;                 // tiles of the launch (sum, or 2x for pairs)
-    int K;                 // input length
-    int C;                 // 128-column chunks per row
-    int nb;                // activation rows
-    int TG;                // most tiles one group holds (sizes shared memory)
-    int S;                 // K-split: CTAs per cluster
-    int Cs;                // chunks per K-slice
-    int groups;            // tile groups; group g holds tile units [g*P/groups, (g+1)*P/groups)
-    const float *x;        // [nb][K]
-    const float *gamma;    // [K] or nullptr (no RMSNorm)
+    const uint8_t *w[kMaxMats];  // packed weights
+    int n[kMaxMats];             // output rows of each matrix
+    int tiles[kMaxMats];         // 16-row tiles of each matrix
+    int nmat;                    // matrices in use
+    int mode;                    // Mode
+    int T;                       // tiles of the job (sum, or 2x for pairs)
+    int K;                       // input length
+    int C;                       // 128-column chunks per row
+    int nb;                      // activation rows
+    int TG;                      // most tiles one group holds (sizes shared memory)
+    int S;                       // K-split: CTAs per cluster
+    int Cs;                      // chunks per K-slice
+    int groups;                  // tile groups; group g holds tile units [g*P/groups, (g+1)*P/groups)
+    const float *x;              // [nb][K]
+    const float *gamma;          // [K] or nullptr (no RMSNorm)
     float eps;
-    const float *gsum;     // affine: caller group sums [nb][K/32] or nullptr
-    int epi;               // Epi
-    float *out[2];         // y per matrix (swiglu: out[0] = h; argmax: logits or nullptr)
-    const float *res;      // residual [nb][n0]
-    float *am_val;         // argmax partials [nb][groups]
+    const float *gsum;           // affine: caller group sums [nb][K/32] or nullptr
+    int epi;                     // Epi
+    float *out[kMaxMats];        // y per matrix (swiglu: out[0] = h; argmax: logits or nullptr)
+    const float *res;            // residual [nb][n0]
+    float *am_val;               // argmax partials [nb][groups]
     int *am_idx;
+};
+
+// The persistent decode-step kernel runs these jobs in order, one CTA per SM.
+constexpr int kMaxStepJobs = 4 * 32 + 1;      // four jobs per layer, up to 32 layers, + logits
+constexpr int kStepRingDepth = 8;             // weight records per warp of the decode-step kernel
+constexpr long long kBarrierSpins = 1ll << 22;  // polls before a grid barrier gives up
+
+struct StepParams {
+    int njobs;
+    int nb;
+    int Kmax;                    // largest K of the jobs (sizes the activation slice)
+    int TGmax;                   // most tiles any group holds in any job
+    unsigned *counter;           // grid-barrier arrivals (zeroed before each launch)
+    unsigned *release;           // number of the last completed barrier (zeroed before each launch)
+    int *err;                    // set to 1 if a barrier gave up
+    int32_t *idx;                // [nb] argmax of the last job
+    float *val;                  // [nb] or nullptr
+    GemvParams jobs[kMaxStepJobs];
 };
 
 inline int ntiles_for(int nb) { return nb <= 8 ? 1 : 2; }
 
-// Dynamic shared memory of one CTA.
+// Dynamic shared memory of one CTA of the engine: activation slice, group
+// sums (affine), per-warp tile partials, reductions, the weight ring.
+inline size_t engine_smem(int fmt, int TG, int Cs, int nb, int warps, int depth) {
+    size_t xs = (size_t)4 * nb * Cs * kChunkK;
+    size_t gs = fmt == 1 ? (size_t)4 * Cs * kBlocksPerChunk * 8 * ntiles_for(nb) : 0;
+    size_t red = (size_t)4 * TG * kTileRows * nb;
+    size_t slots = (size_t)4 * warps * TG * kTileRows * nb;
+    size_t misc = (size_t)4 * 4 * warps * kMaxNb + 4 * 8 * kMaxNb;
+    size_t ring = (size_t)warps * depth * rec_bytes(fmt);
+    return xs + gs + red + slots + misc + ring;
+}
+
 inline size_t smem_bytes(int fmt, int TG, int Cs, int nb) {
-    size_t xs = (size_t)4 * nb * Cs * kChunkK;                                   // hi/lo f16 activations
-    size_t gs = fmt == 1 ? (size_t)4 * Cs * kBlocksPerChunk * 8 * ntiles_for(nb) : 0;  // group sums
-    size_t red = (size_t)4 * TG * kTileRows * nb;                                // CTA partials
-    size_t bslot = (size_t)4 * kWarps * 2 * kTileRows * nb;                      // warp boundary tiles
-    size_t misc = (size_t)4 * 4 * kWarps * kMaxNb + 4 * 8 * kMaxNb;             // reductions
-    size_t ring = (size_t)kWarps * kRingDepth * rec_bytes(fmt);                  // weight records
-    return xs + gs + red + bslot + misc + ring;
+    return engine_smem(fmt, TG, Cs, nb, kWarps, kRingDepth);
+}
+
+// Dynamic shared memory of one decode-step CTA.
+inline size_t step_smem_bytes(int fmt, int TGmax, int Kmax, int nb) {
+    const int Cs = (Kmax + kChunkK - 1) / kChunkK;
+    return engine_smem(fmt, TGmax, Cs, nb, kStepWarps, kStepRingDepth);
 }
 
 struct Plan {
@@ -113,7 +146,7 @@ inline Plan make_plan(int fmt, int T, int C, int nb, bool pairs, int num_sms) {
         if (G < 1) G = 1;
         if (G > P) G = P;
         int per = (P + G - 1) / G;                      // units of the busiest group
-        const int cap = 128 / (nb * pw) > 0 ? 128 / (nb * pw) : 1;  // partials fit shared memory
+        const int cap = 128 / (nb * pw) > 0 ? 128 / (nb * pw) : 1;  // per-warp partials fit shared memory
         if (per > cap) {
             per = cap;
             G = (P + per - 1) / per;
@@ -139,5 +172,11 @@ inline Plan make_plan(int fmt, int T, int C, int nb, bool pairs, int num_sms) {
 // Launchers, one per kernel instantiation family (defined in the .cu files).
 int launch_gemv_q4_0(const GemvParams &p, const Plan &plan, void *stream);
 int launch_gemv_affine(const GemvParams &p, const Plan &plan, void *stream);
+// Cooperative launch of the decode-step kernel: one CTA per SM.
+int launch_step_q4_0(const StepParams &p, int ctas, size_t smem, void *stream);
+int launch_step_affine(const StepParams &p, int ctas, size_t smem, void *stream);
+// Decode-step CTAs that can be resident on one SM (0 on error).
+int step_occupancy_q4_0(int nb, size_t smem);
+int step_occupancy_affine(int nb, size_t smem);
 
 }  // namespace q4

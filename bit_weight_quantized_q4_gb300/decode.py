@@ -1,8 +1,14 @@
 """The synthetic Q4 decode step: per layer RMSNorm + q projection, dual K/V,
 o projection + residual (its input an attention stand-in), RMSNorm + gate/up
 + SwiGLU, down + residual; then a final RMSNorm, the logits projection and
-the greedy argmax.  All launches are libq4gemv calls on one stream and the
-whole step is captured once as a CUDA graph and replayed.
+the greedy argmax.
+
+Two ways to run it, same arithmetic per call:
+* ``run_fused()``: one ``q4_decode_step`` call -- a single persistent kernel
+  whose jobs are separated by grid-wide barriers while the weight stream runs
+  ahead across them (the benchmark's step);
+* ``run()``: the individual library calls (82 kernels for 16 layers) on one
+  stream, e.g. captured as a CUDA graph.
 
 The step order is the fused decode path of honeycrisp/mod.rs
 (forward_decode_fused_layers: one command buffer per step) with the final
@@ -18,8 +24,8 @@ from dataclasses import dataclass
 
 import torch
 
-from . import Q4Weight, q4_argmax, q4_argmax_workspace_bytes, q4_dual_gemv, q4_gus_nrm, q4_nrm_gemv, \
-    q4_res_gemv
+from . import DecodeLayers, Q4Weight, q4_argmax, q4_argmax_workspace_bytes, q4_decode_step, \
+    q4_decode_workspace_bytes, q4_dual_gemv, q4_gus_nrm, q4_nrm_gemv, q4_res_gemv
 
 
 @dataclass
@@ -68,6 +74,8 @@ class DecodeStep:
         self.idx = torch.empty(nb, dtype=torch.int32, device=device)
         self.val = torch.empty(nb, **f32)
         self.ws = torch.empty(q4_argmax_workspace_bytes(self.Wlogits.n, nb), dtype=torch.uint8, device=device)
+        self.step_ws = torch.empty(q4_decode_workspace_bytes(nb), dtype=torch.uint8, device=device)
+        self.descs = DecodeLayers(self.layers)
 
     @property
     def n_kernels(self) -> int:
@@ -104,16 +112,27 @@ class DecodeStep:
                                idx=self.idx, val=self.val))
         hook and hook("argmax", len(self.layers))
 
-    def capture(self, around=None) -> torch.cuda.CUDAGraph:
+    def run_fused(self, n_layers=None):
+        """Enqueue the step as one persistent kernel (the first ``n_layers``
+        layers then the logits argmax)."""
+        q4_decode_step(self.descs, self.Wlogits, self.gamma_final, self.eps, self.x_in, self.hid, self.q, self.k,
+                       self.v, self.h, self.idx, self.val, self.step_ws, n_layers=n_layers)
+
+    @property
+    def n_kernels_fused(self) -> int:
+        return 1
+
+    def capture(self, around=None, fused=False) -> torch.cuda.CUDAGraph:
         """Capture one step as a CUDA graph (after one eager warm-up run)."""
+        fn = (lambda: self.run_fused()) if fused else (lambda: self.run(around=around))
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            self.run()
+            self.run_fused() if fused else self.run()
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run(around=around)
+            fn()
         torch.cuda.synchronize()
         return g

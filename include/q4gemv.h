@@ -165,6 +165,50 @@ q4_status q4_argmax(const q4_weight *W, const float *x, const float *gamma, floa
                     int32_t nb, int32_t *idx, float *val, float *logits,
                     void *workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* One decoder layer of the decode step (q4_decode_step).  All seven weights
+ * share one format; hidden = Wo.n = Wd.n = the k of Wq, Wk, Wv, Wg, Wu and
+ * Wo; inter = Wg.n = Wu.n = Wd.k.  `attn` is the attention output the o
+ * projection consumes ([nb][hidden], device), gamma_in / gamma_post the
+ * RMSNorm weights before the q/k/v and the gate/up projections. */
+typedef struct {
+    q4_weight Wq, Wk, Wv, Wo, Wg, Wu, Wd;
+    const float *gamma_in;
+    const float *gamma_post;
+    const float *attn;
+} q4_decode_layer;
+
+/* Workspace bytes q4_decode_step needs for nb activation rows. */
+size_t q4_decode_workspace_bytes(int32_t nb);
+
+/* One decode step as a single persistent kernel (honeycrisp/mod.rs,
+ * forward_decode_fused_layers: the whole stack in one submission; Module
+ * gpu, module sampling: logits projection and greedy argmax).  Per layer:
+ *   q, k, v = (Wq, Wk, Wv) * rmsnorm(src, gamma_in)    src = x_in, then hid
+ *   hid     = src + Wo * attn
+ *   h       = silu(Wg * rmsnorm(hid, gamma_post)) * (Wu * rmsnorm(hid, gamma_post))
+ *   hid     = hid + Wd * h
+ * then idx[r] = argmax_i (Wlogits * rmsnorm(hid, gamma_final))[r][i] (ties to
+ * the lowest index), val[r] its logit (val may be NULL).
+ * layers: HOST array of n_layers (1..32) descriptors, read during the call.
+ * x_in [nb][hidden] is read only; hid [nb][hidden] receives the final hidden
+ * state; q, k, v, h ([nb][Wq.n], [nb][Wk.n], [nb][Wv.n], [nb][inter]) receive
+ * the last layer's projections and are scratch otherwise.  workspace: device
+ * memory of q4_decode_workspace_bytes(nb) bytes; the call zeroes the first
+ * 16 bytes (a grid-barrier counter and an error word) on `stream` before the
+ * launch.  The kernel is a cooperative launch of one CTA per SM whose jobs
+ * are separated by grid-wide barriers; a barrier that does not complete in
+ * bounded time sets the error word and the kernel returns early (see
+ * q4_decode_check).  Returns Q4_ERR_UNSUPPORTED when the shapes need more
+ * shared memory than one CTA has (large nb * inter). */
+q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_layers, const q4_weight *Wlogits,
+                         const float *gamma_final, float eps, int32_t nb, const float *x_in, float *hid,
+                         float *q, float *k, float *v, float *h, int32_t *idx, float *val, void *workspace,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronises `stream` and reports whether the last q4_decode_step on this
+ * workspace completed all its grid barriers (Q4_OK) or gave up (Q4_ERR_CUDA). */
+q4_status q4_decode_check(const void *workspace, cudaStream_t stream);
+
 /* Allocation-free variant of q4_argmax.  The pages have no counterpart: this
  * exists for callers that cannot allocate device memory where they need the
  * argmax, such as a plug-in whose host application owns all device memory and

@@ -122,3 +122,56 @@ def test_decode_step_teacher_forced(q4):
     torch.cuda.synchronize()
     assert torch.equal(step.idx, fin["idx"]) and torch.equal(step.val, fin["val"])
     assert torch.equal(step.hid, fin["final"])
+
+
+def test_fused_decode_step_teacher_forced(q4):
+    """The persistent-kernel step, layer by layer: running it on the first L
+    layers gives that prefix's hidden state (the same per-layer arithmetic
+    for every L), so layer L-1 is checked against the oracle run on the
+    GPU's own layer input.  Then the whole step against the call-by-call
+    step and the oracle argmax."""
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+    cfg = wl.cfg4()
+    step = DecodeStep(cfg)
+    prev = cfg.x.astype(np.float64)
+    for L in range(1, len(cfg.layers) + 1):
+        step.run_fused(n_layers=L)
+        q4.q4_decode_check(step.step_ws)
+        lay = cfg.layers[L - 1]
+        ref = oracle.decode_layer(lay, prev, cfg.eps)
+        check(to_np(step.q), ref["q"], ref["Sq"], what="fused layer %d q" % (L - 1))
+        check(to_np(step.k), ref["k"], ref["Sk"], what="fused layer %d k" % (L - 1))
+        check(to_np(step.v), ref["v"], ref["Sv"], what="fused layer %d v" % (L - 1))
+        check_swiglu(to_np(step.h), ref["g"], ref["Sg"], ref["u"], ref["Su"], what="fused layer %d gus" % (L - 1))
+        # hid = hid_o + Wd h: bound both residual adds with the oracle's scales
+        bound_extra = 1e-3 * ref["So"] + 2.0 ** -22 * np.abs(ref["hid"])
+        check(to_np(step.hid), ref["hid"], ref["Sd"], extra=bound_extra, what="fused layer %d hid" % (L - 1))
+        prev = to_np(step.hid)
+    _, lref, Sl = oracle.q4_argmax(oracle._hw(cfg.Wlogits), prev, cfg.gamma_final, cfg.eps)
+    check_argmax(step.idx.cpu().numpy(), lref, what="fused argmax")
+    assert abs(float(step.val[0]) - lref[0].max()) <= 1e-3 * Sl[0].max() + 1e-6
+    fused_idx, fused_hid = step.idx.clone(), step.hid.clone()
+    # the captured graph of the fused step gives the same bits
+    g = step.capture(fused=True)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(step.idx, fused_idx) and torch.equal(step.hid, fused_hid)
+    # and agrees with the call-by-call step
+    step.run()
+    torch.cuda.synchronize()
+    # (different but fixed summation orders: compare on the vector's scale)
+    assert float((step.hid - fused_hid).abs().max()) <= 1e-4 * float(fused_hid.abs().max())
+
+
+def test_fused_decode_step_small_shapes(q4):
+    """Ragged shapes and nb > 1 through the persistent kernel, against the
+    oracle step."""
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+    for (hidden, kv, inter, vocab, nb, layers) in [(256, 64, 384, 1000, 1, 3), (160, 48, 96, 333, 3, 2)]:
+        cfg = wl.cfg4(seed=9, layers=layers, hidden=hidden, kv=kv, inter=inter, vocab=vocab, nb=nb)
+        step = DecodeStep(cfg)
+        step.run_fused()
+        q4.q4_decode_check(step.step_ws)
+        idx_ref, lref, hid_ref = oracle.decode_step(cfg)
+        check_argmax(step.idx.cpu().numpy(), lref, what="small fused argmax")
+        assert np.allclose(to_np(step.hid), hid_ref, rtol=2e-3, atol=2e-3)
