@@ -83,9 +83,11 @@ q4_status run(const q4::GemvParams &p, int fmt, cudaStream_t stream, q4::Plan *p
     const int sms = num_sms();
     if (sms <= 0) return Q4_ERR_CUDA;
     q4::Plan plan = q4::make_plan(fmt, p.T, p.C, p.nb, p.mode == q4::MODE_PAIRS, sms);
-    if (plan.smem > (size_t)227 * 1024) return Q4_ERR_UNSUPPORTED;  // nb * k too large to stage
+    if (plan.smem > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;  // nb * k too large to stage
     q4::GemvParams pp = p;
     pp.TG = plan.TG;
+    pp.SW = plan.SW;
+    pp.upt = plan.upt;
     pp.S = plan.S;
     pp.Cs = plan.Cs;
     pp.groups = plan.groups;
@@ -377,16 +379,18 @@ void add_mat(q4::GemvParams &p, const q4_weight &W, float *out) {
     p.Cs = p.C;
 }
 
-void finish_job(q4::GemvParams &p, int &TGmax, int &Kmax) {
+void finish_job(q4::GemvParams &p, int &TGmax, int &Kmax, int &SWmax) {
     int T = 0;
     for (int i = 0; i < p.nmat; ++i) T += p.tiles[i];
     if (p.mode == q4::MODE_PAIRS) T = 2 * p.tiles[0];
     p.T = T;
-    const int pw = p.mode == q4::MODE_PAIRS ? 2 : 1;
-    const int P = T / pw;
-    if (p.groups > P) p.groups = P;  // never more groups than tile units
-    p.TG = (P + p.groups - 1) / p.groups * pw;
+    const int P = q4::units_of(T, p.mode == q4::MODE_PAIRS, p.groups, p.upt);
+    if (p.groups > P) p.groups = P;  // never more groups than units
+    const int per = (P + p.groups - 1) / p.groups, per_lo = P / p.groups;
+    p.TG = p.upt * per < T ? p.upt * per : T;
+    p.SW = q4::slots_per_warp(per, per_lo, p.C, p.C, q4::cls_warps(q4::cls_of(p.nb)), p.upt);
     if (p.TG > TGmax) TGmax = p.TG;
+    if (p.SW > SWmax) SWmax = p.SW;
     if (p.K > Kmax) Kmax = p.K;
 }
 
@@ -442,7 +446,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     sp.idx = idx;
     sp.val = val;
     sp.nb = nb;
-    int TGmax = 1, Kmax = 0;
+    int TGmax = 1, Kmax = 0, SWmax = 2;
     int nj = 0;
     for (int l = 0; l < n_layers; ++l) {
         const q4_decode_layer &L = layers[l];
@@ -456,7 +460,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
         a.gamma = L.gamma_in;
         a.eps = eps;
         a.epi = q4::EPI_STORE;
-        finish_job(a, TGmax, Kmax);
+        finish_job(a, TGmax, Kmax, SWmax);
         sp.jobs[nj++] = a;
         q4::GemvParams o = step_job(G, nb);  // o projection of the attention output + residual
         o.mode = q4::MODE_SINGLE;
@@ -464,7 +468,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
         o.x = L.attn;
         o.res = src;
         o.epi = q4::EPI_RESIDUAL;
-        finish_job(o, TGmax, Kmax);
+        finish_job(o, TGmax, Kmax, SWmax);
         sp.jobs[nj++] = o;
         q4::GemvParams gu = step_job(G, nb);  // RMSNorm + gate/up + SwiGLU
         gu.mode = q4::MODE_PAIRS;
@@ -474,7 +478,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
         gu.gamma = L.gamma_post;
         gu.eps = eps;
         gu.epi = q4::EPI_SWIGLU;
-        finish_job(gu, TGmax, Kmax);
+        finish_job(gu, TGmax, Kmax, SWmax);
         sp.jobs[nj++] = gu;
         q4::GemvParams d = step_job(G, nb);  // down projection + residual, in place
         d.mode = q4::MODE_SINGLE;
@@ -482,7 +486,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
         d.x = h;
         d.res = hid;
         d.epi = q4::EPI_RESIDUAL;
-        finish_job(d, TGmax, Kmax);
+        finish_job(d, TGmax, Kmax, SWmax);
         sp.jobs[nj++] = d;
     }
     q4::GemvParams lg = step_job(G, nb);  // final RMSNorm + logits + per-group argmax
@@ -494,16 +498,17 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     lg.epi = q4::EPI_ARGMAX;
     lg.am_val = (float *)(wsb + 16);
     lg.am_idx = (int *)(wsb + 16 + (size_t)4 * nb * kStepMaxGroups);
-    finish_job(lg, TGmax, Kmax);
+    finish_job(lg, TGmax, Kmax, SWmax);
     sp.jobs[nj++] = lg;
     sp.njobs = nj;
     sp.Kmax = Kmax;
     sp.TGmax = TGmax;
+    sp.SWmax = SWmax;
     // every job runs on all G CTAs; a job's groups may be fewer (clipped to
     // its tile units), and the CTAs beyond them skip that job's work
 
-    const size_t smem = q4::step_smem_bytes(fmt, TGmax, Kmax, nb);
-    if (smem > (size_t)227 * 1024) return Q4_ERR_UNSUPPORTED;
+    const size_t smem = q4::step_smem_bytes(fmt, nb, TGmax, Kmax, SWmax);
+    if (smem > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;
     const int occ = fmt == Q4_FMT_Q4_0 ? q4::step_occupancy_q4_0(nb, smem) : q4::step_occupancy_affine(nb, smem);
     if (occ < 1) return Q4_ERR_UNSUPPORTED;
     cudaGetLastError();

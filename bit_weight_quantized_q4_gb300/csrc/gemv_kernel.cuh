@@ -11,30 +11,38 @@
 // honeycrisp/mod.rs, forward_decode_fused_layers.
 //
 // How (GB300-first, not the pages' Metal/WGSL shapes):
-//  * One CTA = 8 warps owns a group of 16-row tiles and one K-slice, at most
-//    one CTA per SM; a thread-block cluster of S CTAs splits K and folds its
-//    partial sums over distributed shared memory in rank order
-//    (deterministic, no atomics).
-//  * At kernel start each CTA lets the next kernel in the stream launch and
-//    starts its first weight copies (and loads gamma); only then does it wait
-//    for the previous kernel.  Each warp streams its contiguous range of
-//    (tile, chunk) records through a private shared-memory ring with 16-byte
-//    cp.async copies, seven records in flight per warp.
-//  * Each 32-bit nibble word becomes four f16x2 registers of (q - 8) (or q)
-//    with one lop3 and one packed fma each -- exact integers in f16.
+//  * One CTA (16 warps; 8 for nb > 8) owns a group of 16-row tile pairs and
+//    one K-slice, at most one CTA per SM; a thread-block cluster of S CTAs
+//    splits K and folds its partial sums over distributed shared memory in
+//    rank order (deterministic, no atomics).
+//  * The unit of work is one 128-column chunk of a tile pair: two weight
+//    records that share one set of activation fragments.  Each warp streams
+//    its contiguous range of units through a private shared-memory ring with
+//    16-byte cp.async copies, two or three units ahead of its compute.
+//  * A nibble masked in place is an exact f16 subnormal (q * 2^-24, or
+//    q * 2^-20 for the upper nibble of a byte), so a 32-bit word of eight
+//    nibbles becomes four tensor-core A registers with one shift and four
+//    ANDs.  The activation operand carries the factor 16 at the positions
+//    of the lower nibbles, and products land in units of 2^-20.
 //  * Activations are staged once per CTA in shared memory as an exact
 //    power-of-two-scaled hi + lo pair of f16 values (about 22 significant
-//    bits), laid out so each lane loads its mma B fragment with one 64-bit
-//    shared load.
+//    bits) in mma B-fragment order.  For nb <= 4 the hi and lo halves of a
+//    row are two n columns of one product (two mma per 32-weight block); for
+//    nb > 4 they are two k-steps into one accumulator.
 //  * mma.sync m16n8k16 (f16 in, fp32 accumulate) forms the per-block dot
-//    products of 16 rows x 8 activation rows, the hi and lo halves as two
-//    k-steps into the same accumulator; each block's result is scaled by its
-//    fp32 scale and accumulated in fp32, so weights are never rounded.
+//    products.  The block's offset term (the -8 of Q4_0, the min m of the
+//    affine format) multiplies the block's activation sum: for Q4_0 that sum
+//    is the same tensor-core product with every nibble equal to 8, so a
+//    block of all-8 weights cancels exactly; for the affine format it is the
+//    fp32 group sum.  Each block's result is scaled by its fp32 scale and
+//    accumulated in fp32, so weights are never rounded.
 #pragma once
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cooperative_groups.h>
 #include <math.h>
+
+#include <type_traits>
 
 #include "q4_internal.h"
 
@@ -43,20 +51,6 @@ namespace dev {
 
 namespace cg = cooperative_groups;
 
-// 128-bit streaming load: read-only path, no L1 allocation.
-__device__ __forceinline__ uint4 ldg_stream(const uint8_t *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-// 16-byte asynchronous copy global -> shared (L2 only), and its group fences.
-__device__ __forceinline__ void cp_async16(uint8_t *dst, const uint8_t *src) {
-    const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
-}
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 template <int OFF>
 __device__ __forceinline__ void cp_async16_at(uint32_t dst, const uint8_t *src) {
@@ -74,19 +68,6 @@ __device__ __forceinline__ uint4 lds128_at(uint32_t a) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// (a & b) | c
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
 
 // D = A * B + (z0..z3), m16n8k16, f16 inputs, fp32 accumulate; the caller
 // passes four zero registers that stay live across the loop.
@@ -107,25 +88,23 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One nibble word -> four f16x2 registers holding (q - 8) for Q4_0 or q for
-// affine, exactly.  OR-ing a nibble into the mantissa of f16 1024.0 gives
-// 1024 + q (or 1024 + 16q for the upper nibble of a byte), and one packed
-// fma removes the bias (and the 16x):
-//   r0 = (nib0, nib4)  r1 = (nib1, nib5)  r2 = (nib2, nib6)  r3 = (nib3, nib7)
-template <int FMT>
+// One nibble word -> four tensor-core A registers of exact f16 subnormals:
+//   r0 = (nib0, nib4) * 2^-24   r1 = (nib1, nib5) * 2^-20
+//   r2 = (nib2, nib6) * 2^-24   r3 = (nib3, nib7) * 2^-20
+// (a nibble at bits 0..3 of a half is the mantissa q * 2^-24; at bits 4..7
+// it is q * 2^-20).  r0/r2 cover k positions 0..7 of their k16 step, r1/r3
+// positions 8..15.
 __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                             uint32_t &r3) {
-    const uint32_t kMagic = 0x64006400u;                                // 1024.0
-    const uint32_t kOne = 0x3C003C00u;                                  // 1.0
-    const uint32_t kSixteenth = 0x2C002C00u;                            // 1/16
-    const uint32_t kBiasLo = FMT == 0 ? 0xE408E408u : 0xE400E400u;      // -1032 / -1024
-    const uint32_t kBiasHi = FMT == 0 ? 0xD480D480u : 0xD400D400u;      // -72 / -64
     const uint32_t w8 = w >> 8;
-    r0 = hfma2(lop3_and_or(w, 0x000F000Fu, kMagic), kOne, kBiasLo);
-    r1 = hfma2(lop3_and_or(w, 0x00F000F0u, kMagic), kSixteenth, kBiasHi);
-    r2 = hfma2(lop3_and_or(w8, 0x000F000Fu, kMagic), kOne, kBiasLo);
-    r3 = hfma2(lop3_and_or(w8, 0x00F000F0u, kMagic), kSixteenth, kBiasHi);
+    r0 = w & 0x000F000Fu;
+    r1 = w & 0x00F000F0u;
+    r2 = w8 & 0x000F000Fu;
+    r3 = w8 & 0x00F000F0u;
 }
+// The A registers of a block whose every nibble is 8.
+constexpr uint32_t kEightLo = 0x00080008u;
+constexpr uint32_t kEightHi = 0x00800080u;
 
 // The two 16-bit scales (or mins) of a scale word as fp32.
 template <int FMT>
@@ -178,73 +157,95 @@ __device__ __forceinline__ void am_warp(float &bv, int &bi) {
 // The engine shared by the per-call kernel and the persistent decode-step
 // kernel.  A "job" (GemvParams) is one GEMV-shaped launch: up to three
 // matrices over one activation batch with one prologue and one epilogue.
-// Within a job, group g of `groups` owns a contiguous range of 16-row tiles
+// Within a job, group g of `groups` owns a contiguous range of tile pairs
 // (gate/up pairs for SwiGLU) and cluster rank r its K-slice; the CTA's
-// (tile, chunk) records are split into contiguous ranges, one per warp.
+// (pair, chunk) units are split into contiguous ranges, one per warp.
+
+template <int CLS>
+struct Cls {
+    static constexpr bool HLN = CLS <= 1;    // hi / lo of an activation row in two n columns
+    static constexpr int NT = CLS == 3 ? 2 : 1;  // 8-column n-tiles
+    static constexpr int NW = cls_warps(CLS);
+    static constexpr int DU = cls_depth(CLS);
+    static constexpr int GSW = cls_gsw(CLS);
+    static constexpr int NGR = HLN ? 1 : 2 * NT;    // group-sum rows one lane uses
+    static constexpr int NACC = HLN ? 2 : 4 * NT;   // accumulators per record and lane
+};
 
 struct Geo {
-    int t0, tiles_here;              // this group's tiles [t0, t0 + tiles_here)
-    int c0, cs_here, Ks, kb, ke;     // K-slice: chunks [c0, c0 + cs_here), columns [kb, ke)
-    int U, ub, ue, n_my, first_tl;   // records of the CTA; this warp's [ub, ue)
+    int t0, tiles_here, np;      // the group's first tile, its tiles and tile pairs
+    int c0, cs, kb, ke;          // K-slice: chunks [c0, c0 + cs), columns [kb, ke)
+    int U, ub, ue, n_my, fp;     // units of the CTA; this warp's [ub, ue) and its first pair
 };
 
 template <int NW>
 __device__ __forceinline__ Geo make_geo(const GemvParams &p, int group, int rank, int warp) {
     Geo q;
-    const int pw = p.mode == MODE_PAIRS ? 2 : 1;
-    const int P = p.T / pw;
-    if (group < p.groups) {
-        q.t0 = (int)(((long long)group * P) / p.groups) * pw;
-        const int t1 = (int)(((long long)(group + 1) * P) / p.groups) * pw;
-        q.tiles_here = t1 - q.t0;
-    } else {  // a job with fewer tile units than CTAs: this CTA has none
-        q.t0 = 0;
-        q.tiles_here = 0;
+    const int P = (p.T + p.upt - 1) / p.upt;  // units of upt tiles
+    int p0 = 0, p1 = 0;
+    if (group < p.groups) {  // a job with fewer units than CTAs leaves the rest without work
+        if (P < 65536 && p.groups < 65536) {
+            p0 = (int)((unsigned)group * (unsigned)P / (unsigned)p.groups);
+            p1 = (int)((unsigned)(group + 1) * (unsigned)P / (unsigned)p.groups);
+        } else {
+            p0 = (int)((unsigned long long)group * P / p.groups);
+            p1 = (int)((unsigned long long)(group + 1) * P / p.groups);
+        }
     }
+    q.np = p1 - p0;
+    q.t0 = p.upt * p0;
+    q.tiles_here = min(p.upt * q.np, p.T - q.t0);
     q.c0 = rank * p.Cs;
-    q.cs_here = max(0, min(p.Cs, p.C - q.c0));
-    q.Ks = p.Cs * kChunkK;
+    q.cs = max(0, min(p.Cs, p.C - q.c0));
     q.kb = q.c0 * kChunkK;
-    q.ke = min(p.K, q.kb + q.Ks);
-    q.U = q.tiles_here * q.cs_here;
-    q.ub = (warp * q.U) / NW;
-    q.ue = ((warp + 1) * q.U) / NW;
+    q.ke = min(p.K, q.kb + p.Cs * kChunkK);
+    q.U = q.np * q.cs;
+    q.ub = (int)((long long)warp * q.U / NW);
+    q.ue = (int)((long long)(warp + 1) * q.U / NW);
     q.n_my = q.ue - q.ub;
-    q.first_tl = q.cs_here > 0 ? q.ub / q.cs_here : 0;
+    q.fp = q.cs > 0 ? q.ub / q.cs : 0;
     return q;
 }
 
 template <int REC>
-__device__ __forceinline__ const uint8_t *tile_ptr(const GemvParams &p, int t0, int c0, int tl) {
+__device__ __forceinline__ const uint8_t *tile_base(const GemvParams &p, int t) {
     int m, tm;
-    map_tile(p, t0 + tl, m, tm);
-    return p.w[m] + ((size_t)tm * p.C + (size_t)c0) * REC;
+    map_tile(p, t, m, tm);
+    return p.w[m] + (size_t)tm * p.C * REC;
 }
 
-// The weight records a warp streams, in order, across the jobs of a launch:
+// The weight units a warp streams, in order, across the jobs of a launch:
 // each job's [ub, ue) range of this warp, job after job.  The load side runs
-// up to DEPTH-1 records ahead of the compute side, across job boundaries.
+// up to DU-1 units ahead of the compute side, across job boundaries.
 template <int REC, int NW>
 struct WeightStream {
     const GemvParams *jobs;
     int njobs, group, rank, warp;
-    int job, t0, c0, cs, tl, c, left, tiles;
-    const uint8_t *ptr;
+    int job, c0, cs, t0, pl, c, left;
+    const uint8_t *ptr0, *ptr1;  // the next unit's records (ptr1 null: the pair has one tile)
 
+    __device__ __forceinline__ void pair_ptrs() {
+        const GemvParams &p = jobs[job];
+        const int ta = t0 + p.upt * pl;
+        const size_t off = (size_t)(c0 + c) * REC;
+        ptr0 = tile_base<REC>(p, ta) + off;
+        ptr1 = p.upt == 2 && ta + 1 < p.T ? tile_base<REC>(p, ta + 1) + off : nullptr;
+    }
+    __device__ __forceinline__ void start(const Geo &q) {
+        if (q.n_my > 0) {
+            t0 = q.t0;
+            c0 = q.c0;
+            cs = q.cs;
+            pl = q.fp;
+            c = q.ub - q.fp * q.cs;
+            left = q.n_my;
+            pair_ptrs();
+        }
+    }
     __device__ __forceinline__ void next_job() {
         while (left == 0 && job + 1 < njobs) {
             ++job;
-            const Geo q = make_geo<NW>(jobs[job], group, rank, warp);
-            if (q.n_my > 0) {
-                t0 = q.t0;
-                c0 = q.c0;
-                cs = q.cs_here;
-                tiles = q.tiles_here;
-                tl = q.first_tl;
-                c = q.ub - tl * cs;
-                left = q.n_my;
-                ptr = tile_ptr<REC>(jobs[job], t0, c0, tl) + (size_t)c * REC;
-            }
+            start(make_geo<NW>(jobs[job], group, rank, warp));
         }
     }
     __device__ __forceinline__ void init(const GemvParams *j, int n, int grp, int rk, int w) {
@@ -255,23 +256,39 @@ struct WeightStream {
         warp = w;
         job = -1;
         left = 0;
-        ptr = nullptr;
+        ptr0 = ptr1 = nullptr;
         next_job();
     }
-    // copy the next record into the ring stage at shared address `dst`:
-    // each lane its two 16-byte nibble pieces, lanes 0..7 (0..15 affine) the
-    // scale (and min) words
-    __device__ __forceinline__ void issue(uint32_t dst, int lane) {
-        const uint8_t *src = ptr + lane * 16;
+    // one job whose geometry the caller already has
+    __device__ __forceinline__ void init_one(const GemvParams *j, const Geo &q) {
+        jobs = j;
+        njobs = 1;
+        job = 0;
+        left = 0;
+        ptr0 = ptr1 = nullptr;
+        start(q);
+    }
+    // one record: each lane its two 16-byte nibble pieces, lanes 0..7 (0..15
+    // affine) the scale (and min) words
+    __device__ __forceinline__ static void copy_rec(uint32_t dst, const uint8_t *src, int lane) {
+        const uint8_t *s = src + lane * 16;
         const uint32_t d = dst + lane * 16;
-        cp_async16_at<0>(d, src);
-        cp_async16_at<512>(d, src);
-        if (lane < (REC - 1024) / 16) cp_async16_at<1024>(d, src);
-        ptr += REC;
+        cp_async16_at<0>(d, s);
+        cp_async16_at<512>(d, s);
+        if (lane < (REC - 1024) / 16) cp_async16_at<1024>(d, s);
+    }
+    // copy the next unit into the ring stage at shared address `dst`
+    __device__ __forceinline__ void issue(uint32_t dst, int lane) {
+        copy_rec(dst, ptr0, lane);
+        if (ptr1 != nullptr) copy_rec(dst + REC, ptr1, lane);
         --left;
         if (++c == cs) {
             c = 0;
-            if (++tl < tiles && left > 0) ptr = tile_ptr<REC>(jobs[job], t0, c0, tl);
+            ++pl;
+            if (left > 0) pair_ptrs();
+        } else {
+            ptr0 += REC;
+            if (ptr1 != nullptr) ptr1 += REC;
         }
         if (left == 0) next_job();
     }
@@ -280,58 +297,141 @@ struct WeightStream {
 // Shared-memory regions of one CTA (sizes: engine_smem()).
 struct Smem {
     uint8_t *xs;     // activation slice, hi/lo f16 in mma B-fragment order
-    float *gs;       // affine: group sums [blocks][GSW]
-    float *red;      // CTA results [TG][16][nb]
-    float *slots;    // per-warp tile partials [warp][TG][16][nb]
+    float *gs;       // block offset sums [chunk][GSW rows][4 blocks], units of 2^-20
+    float *red;      // cluster fold (S > 1): CTA results [TG][16][nb]
+    float *slots;    // per-warp tile partials [warp][SW][16][nb]
     float *rbuf;     // reductions [4][warp][kMaxNb]
-    float *nx;       // row stats [8][kMaxNb]: 2 inv_rms, 3 scale, 5 inv_scale
-    uint8_t *ring;   // weight records [warp][DEPTH][REC]
+    float *nx;       // row stats [8][kMaxNb]: 2 inv_rms, 3 scale, 5 output factor
+    uint8_t *ring;   // weight units [warp][DU][2 records]
 };
 
-template <int NW>
-__device__ __forceinline__ Smem carve(uint8_t *smem, int fmt, int nb, int Cs, int GSW, int TG) {
+template <int CLS>
+__device__ __forceinline__ Smem carve(uint8_t *smem, int nb, int Cs, int TG, int SW, int S) {
+    using C = Cls<CLS>;
     Smem m;
     m.xs = smem;
-    m.gs = reinterpret_cast<float *>(smem + (size_t)4 * nb * Cs * kChunkK);
-    m.red = m.gs + (fmt == 1 ? Cs * kBlocksPerChunk * GSW : 0);
-    m.slots = m.red + TG * kTileRows * nb;
-    m.rbuf = m.slots + NW * TG * kTileRows * nb;
-    m.nx = m.rbuf + 4 * NW * kMaxNb;
+    m.gs = reinterpret_cast<float *>(smem + (size_t)512 * nb * Cs);
+    m.red = m.gs + (size_t)4 * C::GSW * Cs;
+    m.slots = m.red + (S > 1 ? (size_t)TG * kTileRows * nb : 0);
+    m.rbuf = m.slots + (size_t)C::NW * SW * kTileRows * nb;
+    m.nx = m.rbuf + 4 * C::NW * kMaxNb;
     m.ring = reinterpret_cast<uint8_t *>(m.nx + 8 * kMaxNb);
     return m;
 }
 
-// The activation scale of a row: 2^e with bound * 2^e in [2^14, 2^15), from
-// the exponent field of `bound` (e clamped to [-100, 100]; 1 for 0 or
-// non-finite bounds; subnormal bounds take the clamp).
-__device__ __forceinline__ void row_scale(float bound, float &scale, float &inv_scale) {
-    scale = 1.f;
-    inv_scale = 1.f;
+// The activation scale of a row: 2^e with bound * 2^e in [2^10, 2^11), from
+// the exponent field of `bound` (e clamped to [-100, 100]; 0 for a zero or
+// non-finite bound), and the output factor 2^(20-e), which also undoes the
+// 2^-20 unit of the products.
+__device__ __forceinline__ void row_scale(float bound, float &scale, float &out_factor) {
+    int e = 0;
     if (bound > 0.f && bound <= 3.0e38f) {
         const int be = (int)((__float_as_uint(bound) >> 23) & 0xFF);  // bound in [2^(be-127), 2^(be-126))
-        int e = 14 - (be - 127);
-        e = max(-100, min(100, e));
-        scale = __uint_as_float((uint32_t)(127 + e) << 23);
-        inv_scale = __uint_as_float((uint32_t)(127 - e) << 23);
+        e = max(-100, min(100, 10 - (be - 127)));
     }
+    scale = __uint_as_float((uint32_t)(127 + e) << 23);
+    out_factor = __uint_as_float((uint32_t)(127 + 20 - e) << 23);
+}
+
+// Byte offset in the staged slice of element kk (0..31) of 32-column block
+// b, activation row r, half `part` (0 hi, 1 lo); elements kk and kk+1 (kk
+// even) share one f16x2 word.  Within a k16 step s, position pp = 2t + 8h + e
+// belongs to lane-position t, B register h and half e.
+//   nb <= 4: per block [column 2r+part][t][s][h]         (16 bytes per lane)
+//   nb >  4: per block [n-tile][row][t][s][part][h]        (32 bytes per lane)
+template <int CLS>
+__device__ __forceinline__ int xs_off(int b, int r, int kk, int part, int xbs) {
+    const int s = kk >> 4, pp = kk & 15, h = pp >> 3, tt = (pp & 7) >> 1;
+    if (Cls<CLS>::HLN) return b * xbs + ((2 * r + part) * 4 + tt) * 16 + (2 * s + h) * 4;
+    return b * xbs + (r >> 3) * 1024 + ((r & 7) * 4 + tt) * 32 + s * 16 + part * 8 + h * 4;
+}
+
+// Store columns (kl, kl+1) of row r, already scaled, as hi + lo f16 pairs;
+// positions 0..7 of a k16 step carry the factor 16 of the lower nibbles.
+template <int CLS>
+__device__ __forceinline__ void put_pair(uint8_t *xs, int xbs, int r, int kl, float v0, float v1) {
+    const int b = kl >> 5, kk = kl & 31;
+    if ((kk & 8) == 0) {
+        v0 *= 16.f;
+        v1 *= 16.f;
+    }
+    const __half2 hi = __floats2half2_rn(v0, v1);
+    const float2 hf = __half22float2(hi);
+    const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+    *reinterpret_cast<__half2 *>(xs + xs_off<CLS>(b, r, kk, 0, xbs)) = hi;
+    *reinterpret_cast<__half2 *>(xs + xs_off<CLS>(b, r, kk, 1, xbs)) = lo;
+}
+
+__device__ __forceinline__ int gs_idx(int b, int row, int GSW) { return ((b >> 2) * GSW + row) * 4 + (b & 3); }
+
+// Q4_0 offset sums: for every block of the slice, the tensor-core product of
+// the staged activations with an all-8 weight block -- the exact value a
+// block of eights produces in the main loop, so that it cancels to zero.
+template <int CLS>
+__device__ void eights_pass(const Geo &q, const Smem &m, int nb, int warp, int lane) {
+    using C = Cls<CLS>;
+    const int g = lane >> 2, t = lane & 3;
+    const int xbs = 128 * nb;
+    const float z = 0.f;
+    const int nblk = q.cs * kBlocksPerChunk;
+    auto one = [&](int b) {
+        if (C::HLN) {
+            const uint4 bb = *reinterpret_cast<const uint4 *>(m.xs + b * xbs + ((g % (2 * nb)) * 4 + t) * 16);
+            float d[4];
+            mma16816_c(d, kEightLo, kEightLo, kEightHi, kEightHi, bb.x, bb.y, z, z, z, z);
+            mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, bb.z, bb.w);
+            if (g == 0) m.gs[gs_idx(b, t, C::GSW)] = d[0] + d[1];
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt) {
+                const int cnt = min(8, nb - 8 * nt);
+                const uint8_t *ba = m.xs + b * xbs + nt * 1024 + ((g % cnt) * 4 + t) * 32;
+                const uint4 B0 = *reinterpret_cast<const uint4 *>(ba);
+                const uint4 B1 = *reinterpret_cast<const uint4 *>(ba + 16);
+                float d[4];
+                mma16816_c(d, kEightLo, kEightLo, kEightHi, kEightHi, B0.x, B0.y, z, z, z, z);
+                mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, B0.z, B0.w);
+                mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, B1.x, B1.y);
+                mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, B1.z, B1.w);
+                if (g == 0) {
+                    m.gs[gs_idx(b, 8 * nt + 2 * t, C::GSW)] = d[0];
+                    m.gs[gs_idx(b, 8 * nt + 2 * t + 1, C::GSW)] = d[1];
+                }
+            }
+        }
+    };
+    // four independent blocks per step keep several products in flight
+    int b = warp;
+    for (; b + 3 * C::NW < nblk; b += 4 * C::NW) {
+        one(b);
+        one(b + C::NW);
+        one(b + 2 * C::NW);
+        one(b + 3 * C::NW);
+    }
+    for (; b < nblk; b += C::NW) one(b);
 }
 
 // Stage this CTA's activation slice of job p: per row, scale by a power of
 // two chosen from its largest magnitude (after RMSNorm when gamma is given)
-// and split into f16 hi + lo, stored in B-fragment order:
-//   per 32-column block: [n-tile][k16 step][lane g*4+t][hi(k=2t,2t+1), hi(2t+8,2t+9), lo(..), lo(..)]
-// Activation loads bypass L1 (.cg): in the persistent kernel another SM may
-// have rewritten them since this SM last read them.
-template <int FMT, int NT, bool NB1, int NW>
+// and split into f16 hi + lo in B-fragment order (xs_off); then the block
+// offset sums: Q4_0 by eights_pass, affine as fp32 sums of the scaled
+// values (pairs, then a butterfly over 16 lanes -- the order of
+// q4_group_sums) or from the caller's group sums.  Activation loads bypass
+// L1 (.cg): in the persistent kernel another SM may have rewritten them
+// since this SM last read them.
+// SP: column pairs per thread a multi-row slice may stage through registers
+template <int FMT, int CLS, int SP>
 __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S, int tid, int warp, int lane) {
-    constexpr int GSW = 8 * NT;
-    constexpr int NTH = NW * 32;
-    const int nb = NB1 ? 1 : p.nb;
-    const int Ks = q.Ks, kb = q.kb, ke = q.ke;
+    using C = Cls<CLS>;
+    constexpr int NW = C::NW, NTH = NW * 32, GSW = C::GSW;
+    const int nb = CLS == 0 ? 1 : p.nb;
+    const int Ks = p.Cs * kChunkK;  // staged columns; those at or beyond ke are zero
+    const int kb = q.kb, ke = q.ke;
     const int xbs = 128 * nb;
     const bool norm = p.gamma != nullptr;
+    const bool given = FMT == 1 && p.gsum != nullptr && !norm;  // affine sums from the caller
     constexpr int RP = 8192 / (2 * NTH);  // nb == 1: a slice up to 8192 columns passes through registers
-    if (NB1 && Ks <= 2 * NTH * RP) {
+    if (CLS == 0 && Ks <= 2 * NTH * RP) {
         const int npass = (Ks / 2 + NTH - 1) / NTH;  // pairs per thread actually used
         float2 xv[RP], gv[RP];
         float ss = 0.f, mx = 0.f;
@@ -375,17 +475,18 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
             for (int r = 0; r < S; ++r) tss += cluster.map_shared_rank(m.nx, r)[0];
         }
         const float inv_rms = norm ? 1.0f / sqrtf(tss / (float)p.K + p.eps) : 1.f;
-        float scale, inv_scale;
-        row_scale(tmx * inv_rms, scale, inv_scale);
+        float scale, out_factor;
+        row_scale(tmx * inv_rms, scale, out_factor);
         if (tid == 0) {
             m.nx[2 * kMaxNb] = inv_rms;
             m.nx[3 * kMaxNb] = scale;
-            m.nx[5 * kMaxNb] = inv_scale;
+            m.nx[5 * kMaxNb] = out_factor;
         }
 #pragma unroll
         for (int qq = 0; qq < RP; ++qq) {
             if (qq >= npass) break;
             const int kl = 2 * (tid + qq * NTH);
+            // warp-uniform: a warp's pairs are 64 consecutive columns and Ks is a multiple of 128
             if (kl < Ks) {
                 float v0 = xv[qq].x, v1 = xv[qq].y;
                 if (norm) {
@@ -394,326 +495,493 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
                 }
                 v0 *= scale;
                 v1 *= scale;
-                __half2 hi = __floats2half2_rn(v0, v1);
-                float2 hf = __half22float2(hi);
-                __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
-                const int kk = kl & 31, k16 = kk & 15;
-                const int off = (kl >> 5) * 128 + (kk >> 4) * 64 + ((k16 & 7) >> 1) * 16 + (k16 >> 3) * 4;
-                *reinterpret_cast<__half2 *>(m.xs + off) = hi;
-                *reinterpret_cast<__half2 *>(m.xs + off + 8) = lo;
+                put_pair<CLS>(m.xs, xbs, 0, kl, v0, v1);
+                if (FMT == 1 && !given) {
+                    const float bsum = half_warp_sum(v0 + v1);
+                    if ((lane & 15) == 0) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum * 0x1p-20f;
+                }
             }
         }
-        if (FMT == 1) {
-            const int nblk = p.Cs * kBlocksPerChunk;
-            for (int i = tid; i < GSW * nblk; i += NTH) {
-                const int r = i / nblk, bl = i - r * nblk;
-                const int kblk = kb + 32 * bl;
-                float sacc = 0.f;
-                if (r == 0 && kblk < ke) {
-                    if (p.gsum != nullptr && !norm) {
-                        sacc = __ldcg(p.gsum + kblk / 32);
-                    } else {
-                        float vv[32];
+        if (given) {
+            const float f = scale * 0x1p-20f;
+            for (int b = tid; b < p.Cs * kBlocksPerChunk; b += NTH)
+                m.gs[gs_idx(b, 0, GSW)] = kb + 32 * b < ke ? __ldcg(p.gsum + kb / 32 + b) * f : 0.f;
+        }
+    } else if (CLS != 0 && nb * (Ks >> 1) <= SP * NTH) {
+        // a slice of at most SP column pairs per thread: one batch
+        // of loads into registers, per-row statistics, then the writes
+        const int half_ks = Ks >> 1;
+        const int npairs = nb * half_ks;  // a multiple of 64; a warp's 32 pairs lie in one row
+        const int npass = (npairs + NTH - 1) / NTH;
+        float2 xv[SP], gv[SP];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) vv[e] = __ldcg(p.x + kblk + e);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            float v = vv[e];
-                            if (norm) v = v * inv_rms * p.gamma[kblk + e];
-                            sacc += v;
-                        }
-                    }
-                    sacc *= scale;
+        for (int j = 0; j < SP; ++j) {
+            if (j >= npass) break;
+            const int i = tid + j * NTH;
+            float2 v = make_float2(0.f, 0.f), gm = make_float2(1.f, 1.f);
+            if (i < npairs) {
+                const int r = i / half_ks, k = kb + 2 * (i - r * half_ks);
+                if (k < ke) {
+                    v = __ldcg(reinterpret_cast<const float2 *>(p.x + (size_t)r * p.K + k));
+                    if (norm) gm = *reinterpret_cast<const float2 *>(p.gamma + k);
                 }
-                m.gs[bl * GSW + r] = sacc;
+            }
+            xv[j] = v;
+            gv[j] = gm;
+        }
+        // per (pass, warp) partials: entry e = j*NW + warp covers pairs [32e, 32e+32)
+        float *part = m.rbuf;  // [2][npass * NW]
+#pragma unroll
+        for (int j = 0; j < SP; ++j) {
+            if (j >= npass) break;
+            const float2 v = xv[j], gm = gv[j];
+            float ss = fmaf(v.y, v.y, v.x * v.x);
+            float mx = fmaxf(fabsf(norm ? v.x * gm.x : v.x), fabsf(norm ? v.y * gm.y : v.y));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            }
+            if (lane == 0) {
+                part[j * NW + warp] = ss;
+                part[npass * NW + j * NW + warp] = mx;
             }
         }
         __syncthreads();
-        return;
-    }
-    // general nb: two passes over the slice
-    for (int r = 0; r < nb; ++r) {
-        float ss = 0.f, mx = 0.f;
-        const float *xr = p.x + (size_t)r * p.K;
-        for (int k = kb + 2 * tid; k < ke; k += 2 * NTH) {
-            float2 v = __ldcg(reinterpret_cast<const float2 *>(xr + k));
-            ss = fmaf(v.x, v.x, ss);
-            ss = fmaf(v.y, v.y, ss);
-            if (norm) {
-                float2 gm = *reinterpret_cast<const float2 *>(p.gamma + k);
-                mx = fmaxf(mx, fmaxf(fabsf(v.x * gm.x), fabsf(v.y * gm.y)));
-            } else {
-                mx = fmaxf(mx, fmaxf(fabsf(v.x), fabsf(v.y)));
+        // row r's entries are e in [r*half_ks/32, (r+1)*half_ks/32): one warp per row
+        for (int r = warp; r < nb; r += NW) {
+            const int e0 = r * (half_ks >> 5), e1 = e0 + (half_ks >> 5);
+            float ss = 0.f, mx = 0.f;
+            for (int e = e0 + lane; e < e1; e += 32) {
+                ss += part[e];
+                mx = fmaxf(mx, part[npass * NW + e]);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            }
+            if (lane == 0) {
+                m.nx[0 * kMaxNb + r] = ss;  // this slice's sum of squares
+                m.nx[1 * kMaxNb + r] = mx;
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (norm && S > 1) {
+            cg::cluster_group cluster = cg::this_cluster();
+            cluster.sync();
+            if (tid < nb) {
+                float tot = 0.f;
+                for (int rr = 0; rr < S; ++rr) tot += cluster.map_shared_rank(m.nx, rr)[tid];
+                m.nx[4 * kMaxNb + tid] = tot;
+            }
+        } else {
+            __syncthreads();
+            if (tid < nb) m.nx[4 * kMaxNb + tid] = m.nx[tid];
         }
-        if (lane == 0) {
-            m.rbuf[warp * kMaxNb + r] = ss;
-            m.rbuf[NW * kMaxNb + warp * kMaxNb + r] = mx;
-        }
-    }
-    __syncthreads();
-    if (tid < nb) {
-        float ss = 0.f, mx = 0.f;
-        for (int w = 0; w < NW; ++w) {
-            ss += m.rbuf[w * kMaxNb + tid];
-            mx = fmaxf(mx, m.rbuf[NW * kMaxNb + w * kMaxNb + tid]);
-        }
-        m.nx[0 * kMaxNb + tid] = ss;  // this slice's sum of squares
-        m.nx[1 * kMaxNb + tid] = mx;
-    }
-    if (norm && S > 1) {
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
+        __syncthreads();
         if (tid < nb) {
-            float tot = 0.f;
-            for (int r = 0; r < S; ++r) tot += cluster.map_shared_rank(m.nx, r)[tid];
-            m.nx[4 * kMaxNb + tid] = tot;
+            float inv_rms = 1.f;
+            if (norm) inv_rms = 1.0f / sqrtf(m.nx[4 * kMaxNb + tid] / (float)p.K + p.eps);
+            float scale, out_factor;
+            row_scale(m.nx[1 * kMaxNb + tid] * inv_rms, scale, out_factor);
+            m.nx[2 * kMaxNb + tid] = inv_rms;
+            m.nx[3 * kMaxNb + tid] = scale;
+            m.nx[5 * kMaxNb + tid] = out_factor;
         }
-    } else if (tid < nb) {
-        m.nx[4 * kMaxNb + tid] = m.nx[tid];
-    }
-    __syncthreads();
-    if (tid < nb) {
-        float inv_rms = 1.f;
-        if (norm) inv_rms = 1.0f / sqrtf(m.nx[4 * kMaxNb + tid] / (float)p.K + p.eps);
-        float scale, inv_scale;
-        row_scale(m.nx[1 * kMaxNb + tid] * inv_rms, scale, inv_scale);
-        m.nx[2 * kMaxNb + tid] = inv_rms;
-        m.nx[3 * kMaxNb + tid] = scale;
-        m.nx[5 * kMaxNb + tid] = inv_scale;
-    }
-    __syncthreads();
-    const int half_ks = Ks >> 1;
-    for (int i = tid; i < nb * half_ks; i += NTH) {
-        const int r = i / half_ks, kp = i - r * half_ks;
-        const int kl = 2 * kp, k = kb + kl;
-        float v0 = 0.f, v1 = 0.f;
-        if (k < ke) {
-            float2 v = __ldcg(reinterpret_cast<const float2 *>(p.x + (size_t)r * p.K + k));
-            v0 = v.x;
-            v1 = v.y;
-            if (norm) {
-                const float ir = m.nx[2 * kMaxNb + r];
-                float2 gm = *reinterpret_cast<const float2 *>(p.gamma + k);
-                v0 = v0 * ir * gm.x;
-                v1 = v1 * ir * gm.y;
-            }
-        }
-        const float sc = m.nx[3 * kMaxNb + r];
-        v0 *= sc;
-        v1 *= sc;
-        __half2 hi = __floats2half2_rn(v0, v1);
-        float2 hf = __half22float2(hi);
-        __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
-        const int bl = kl >> 5, kk = kl & 31, st = kk >> 4, k16 = kk & 15;
-        const int nt = r >> 3, cols = min(8, nb - 8 * nt);
-        const int off = bl * xbs + nt * 1024 + st * 64 * cols + (4 * (r & 7) + ((k16 & 7) >> 1)) * 16 +
-                        (k16 >> 3) * 4;
-        *reinterpret_cast<__half2 *>(m.xs + off) = hi;
-        *reinterpret_cast<__half2 *>(m.xs + off + 8) = lo;
-    }
-    if (FMT == 1) {
-        const int nblk = p.Cs * kBlocksPerChunk;
-        for (int i = tid; i < GSW * nblk; i += NTH) {
-            const int r = i / nblk, bl = i - r * nblk;
-            const int kblk = kb + 32 * bl;
-            float s = 0.f;
-            if (r < nb && kblk < ke) {
-                if (p.gsum != nullptr && !norm) {
-                    s = __ldcg(p.gsum + (size_t)r * (p.K / 32) + kblk / 32);
-                } else {
-                    const float *xr = p.x + (size_t)r * p.K + kblk;
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < SP; ++j) {
+            if (j >= npass) break;
+            const int i = tid + j * NTH;
+            if (i < npairs) {  // warp-uniform
+                const int r = i / half_ks, kl = 2 * (i - r * half_ks);
+                float v0 = xv[j].x, v1 = xv[j].y;
+                if (norm) {
                     const float ir = m.nx[2 * kMaxNb + r];
-                    float vv[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) vv[e] = __ldcg(xr + e);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float v = vv[e];
-                        if (norm) v = v * ir * p.gamma[kblk + e];
-                        s += v;
-                    }
+                    v0 = v0 * ir * gv[j].x;
+                    v1 = v1 * ir * gv[j].y;
                 }
-                s *= m.nx[3 * kMaxNb + r];
+                const float sc = m.nx[3 * kMaxNb + r];
+                v0 *= sc;
+                v1 *= sc;
+                put_pair<CLS>(m.xs, xbs, r, kl, v0, v1);
+                if (FMT == 1 && !given) {
+                    const float bsum = half_warp_sum(v0 + v1);
+                    if ((lane & 15) == 0) m.gs[gs_idx(kl >> 5, r, GSW)] = bsum * 0x1p-20f;
+                }
             }
-            m.gs[bl * GSW + r] = s;
         }
+        if (given) {
+            const int nblk = p.Cs * kBlocksPerChunk;
+            for (int i = tid; i < nb * nblk; i += NTH) {
+                const int r = i / nblk, b = i - r * nblk;
+                const float f = m.nx[3 * kMaxNb + r] * 0x1p-20f;
+                m.gs[gs_idx(b, r, GSW)] =
+                    kb + 32 * b < ke ? __ldcg(p.gsum + (size_t)r * (p.K / 32) + kb / 32 + b) * f : 0.f;
+            }
+        }
+    } else {
+        // general: two passes over the slice
+        for (int r = 0; r < nb; ++r) {
+            float ss = 0.f, mx = 0.f;
+            const float *xr = p.x + (size_t)r * p.K;
+            for (int k = kb + 2 * tid; k < ke; k += 2 * NTH) {
+                float2 v = __ldcg(reinterpret_cast<const float2 *>(xr + k));
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                if (norm) {
+                    float2 gm = *reinterpret_cast<const float2 *>(p.gamma + k);
+                    mx = fmaxf(mx, fmaxf(fabsf(v.x * gm.x), fabsf(v.y * gm.y)));
+                } else {
+                    mx = fmaxf(mx, fmaxf(fabsf(v.x), fabsf(v.y)));
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            }
+            if (lane == 0) {
+                m.rbuf[warp * kMaxNb + r] = ss;
+                m.rbuf[NW * kMaxNb + warp * kMaxNb + r] = mx;
+            }
+        }
+        __syncthreads();
+        if (tid < nb) {
+            float ss = 0.f, mx = 0.f;
+            for (int w = 0; w < NW; ++w) {
+                ss += m.rbuf[w * kMaxNb + tid];
+                mx = fmaxf(mx, m.rbuf[NW * kMaxNb + w * kMaxNb + tid]);
+            }
+            m.nx[0 * kMaxNb + tid] = ss;  // this slice's sum of squares
+            m.nx[1 * kMaxNb + tid] = mx;
+        }
+        if (norm && S > 1) {
+            cg::cluster_group cluster = cg::this_cluster();
+            cluster.sync();
+            if (tid < nb) {
+                float tot = 0.f;
+                for (int r = 0; r < S; ++r) tot += cluster.map_shared_rank(m.nx, r)[tid];
+                m.nx[4 * kMaxNb + tid] = tot;
+            }
+        } else if (tid < nb) {
+            m.nx[4 * kMaxNb + tid] = m.nx[tid];
+        }
+        __syncthreads();
+        if (tid < nb) {
+            float inv_rms = 1.f;
+            if (norm) inv_rms = 1.0f / sqrtf(m.nx[4 * kMaxNb + tid] / (float)p.K + p.eps);
+            float scale, out_factor;
+            row_scale(m.nx[1 * kMaxNb + tid] * inv_rms, scale, out_factor);
+            m.nx[2 * kMaxNb + tid] = inv_rms;
+            m.nx[3 * kMaxNb + tid] = scale;
+            m.nx[5 * kMaxNb + tid] = out_factor;
+        }
+        __syncthreads();
+        const int half_ks = Ks >> 1;
+        // warp-uniform trip count: nb * half_ks is a multiple of 64, and a
+        // warp's 32 pairs are consecutive columns of one row
+        for (int i = tid; i < nb * half_ks; i += NTH) {
+            const int r = i / half_ks, kp = i - r * half_ks;
+            const int kl = 2 * kp, k = kb + kl;
+            float v0 = 0.f, v1 = 0.f;
+            if (k < ke) {
+                float2 v = __ldcg(reinterpret_cast<const float2 *>(p.x + (size_t)r * p.K + k));
+                v0 = v.x;
+                v1 = v.y;
+                if (norm) {
+                    const float ir = m.nx[2 * kMaxNb + r];
+                    float2 gm = *reinterpret_cast<const float2 *>(p.gamma + k);
+                    v0 = v0 * ir * gm.x;
+                    v1 = v1 * ir * gm.y;
+                }
+            }
+            const float sc = m.nx[3 * kMaxNb + r];
+            v0 *= sc;
+            v1 *= sc;
+            put_pair<CLS>(m.xs, xbs, r, kl, v0, v1);
+            if (FMT == 1 && !given) {
+                const float bsum = half_warp_sum(v0 + v1);
+                if ((lane & 15) == 0) m.gs[gs_idx(kl >> 5, r, GSW)] = bsum * 0x1p-20f;
+            }
+        }
+        if (given) {
+            const int nblk = p.Cs * kBlocksPerChunk;
+            for (int i = tid; i < nb * nblk; i += NTH) {
+                const int r = i / nblk, b = i - r * nblk;
+                const float f = m.nx[3 * kMaxNb + r] * 0x1p-20f;
+                m.gs[gs_idx(b, r, GSW)] =
+                    kb + 32 * b < ke ? __ldcg(p.gsum + (size_t)r * (p.K / 32) + kb / 32 + b) * f : 0.f;
+            }
+        }
+    }
+    if (FMT == 0) {
+        __syncthreads();
+        eights_pass<CLS>(q, m, nb, warp, lane);
     }
     __syncthreads();
 }
 
-// This warp's records of one job: dequantise, tensor-core dot products,
-// per-block scaling; each tile's partial goes to this warp's slot.
-// Consumes one ring stage per record and refills it from `ws`.
-template <int FMT, int NT, bool NB1, int DEPTH, int NW>
+template <int I>
+__device__ __forceinline__ uint32_t word_of(const uint4 &v) {
+    return I == 0 ? v.x : I == 1 ? v.y : I == 2 ? v.z : v.w;
+}
+
+// This warp's units of one job: per unit, the activation fragments and
+// offset sums of its chunk, then for each of the pair's records and each of
+// the chunk's four blocks: unpack, tensor-core products, offset, scale.
+// Each tile's partial over this warp's chunks goes to one of its slots.
+// Consumes one ring stage per unit and refills it from `ws`.
+template <int FMT, int CLS>
 __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m,
-                          WeightStream<FMT == 0 ? kRecQ4_0 : kRecAffine, NW> &ws, uint32_t &st_a, uint32_t &fill_a,
-                          uint32_t ring_a, int warp, int lane) {
+                          WeightStream<FMT == 0 ? kRecQ4_0 : kRecAffine, Cls<CLS>::NW> &ws, uint32_t &st_a,
+                          uint32_t &fill_a, uint32_t ring_a, int warp, int lane) {
+    using C = Cls<CLS>;
     constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
-    constexpr int GSW = 8 * NT;
-    const int g = lane >> 2, tq = lane & 3;
-    const int nb = NB1 ? 1 : p.nb;
+    constexpr int UREC = 2 * REC;
+    constexpr int NT = C::NT, NGR = C::NGR, NACC = C::NACC;
+    const int g = lane >> 2, t = lane & 3;
+    const int nb = CLS == 0 ? 1 : p.nb;
     const int xbs = 128 * nb;
-    const int cs_here = q.cs_here;
-    const uint32_t ring_end = ring_a + DEPTH * REC;
-    // lanes beyond the batch read a duplicate column: its mma outputs are
-    // never stored, and every lane loads unconditionally
-    const uint32_t xs_a = smem_u32(m.xs);
-    uint32_t xoff[NT];
-    int hstr[NT];
+    const int cs = q.cs;
+    const uint32_t ring_end = ring_a + C::DU * UREC;
+    // this lane's B-fragment slot in a block (lanes past the batch read a
+    // duplicate column: their outputs are never stored)
+    int boff[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const int cols = min(8, nb - 8 * nt);
-        xoff[nt] = xs_a + nt * 1024 + (4 * (g % cols) + tq) * 16;
-        hstr[nt] = 64 * cols;
-    }
-    float acc[NT][4];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    int ctl = q.first_tl, cc = q.ub - q.first_tl * cs_here;
-    const float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
-    float *my_slots = m.slots + (size_t)warp * p.TG * kTileRows * nb;
-
-    auto flush = [&](int tl) {
-        float *dst = my_slots + (size_t)tl * kTileRows * nb;
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int a0 = 8 * j + 2 * tq;
-            if (a0 < nb) {
-                dst[g * nb + a0] = acc[j][0];
-                dst[(g + 8) * nb + a0] = acc[j][2];
-            }
-            if (!NB1 && a0 + 1 < nb) {
-                dst[g * nb + a0 + 1] = acc[j][1];
-                dst[(g + 8) * nb + a0 + 1] = acc[j][3];
-            }
-            acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        if (C::HLN) {
+            boff[nt] = ((g % (2 * nb)) * 4 + t) * 16;
+        } else {
+            const int cnt = min(8, nb - 8 * nt);
+            boff[nt] = nt * 1024 + ((g % cnt) * 4 + t) * 32;
         }
-    };
-
-    // One 32-column block: two nibble words (rows g, g+8) -> A fragments;
-    // per n-tile two 16-byte B loads and four mma (hi and lo halves of both
-    // k16 steps); the block scale applied in fp32.
-    auto block = [&](uint32_t w0, uint32_t w1, uint32_t scw, uint32_t mnw, uint32_t xblk, int blk) {
-        uint32_t a[8];
-        unpack_word<FMT>(w0, a[0], a[2], a[4], a[6]);  // row g
-        unpack_word<FMT>(w1, a[1], a[3], a[5], a[7]);  // row g + 8
-        const float2 d = scale_pair<FMT>(scw);
+    }
+    int grow[NGR];  // this lane's offset-sum rows
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const uint32_t xa = xblk + xoff[nt];
-            uint4 b0, b1;
-            if (NB1) {
-                b0 = lds128_at<0>(xa);
-                b1 = lds128_at<64>(xa);
-            } else {
-                b0 = lds128_at<0>(xa);
-                b1 = lds128_at<0>(xa + hstr[nt]);
-            }
-            float dd[4];
-            mma16816_c(dd, a[0], a[1], a[2], a[3], b0.x, b0.y, z0, z1, z2, z3);  // k 0..15, hi
-            mma16816(dd, a[0], a[1], a[2], a[3], b0.z, b0.w);                      // k 0..15, lo
-            mma16816(dd, a[4], a[5], a[6], a[7], b1.x, b1.y);                      // k 16..31, hi
-            mma16816(dd, a[4], a[5], a[6], a[7], b1.z, b1.w);                      // k 16..31, lo
-            acc[nt][0] = fmaf(d.x, dd[0], acc[nt][0]);
-            acc[nt][2] = fmaf(d.y, dd[2], acc[nt][2]);
-            if (!NB1) {
-                acc[nt][1] = fmaf(d.x, dd[1], acc[nt][1]);
-                acc[nt][3] = fmaf(d.y, dd[3], acc[nt][3]);
-            }
-            if (FMT == 1) {
-                const float2 mm = scale_pair<FMT>(mnw);
-                const float2 gv = *reinterpret_cast<const float2 *>(m.gs + blk * GSW + 8 * nt + 2 * tq);
-                acc[nt][0] = fmaf(mm.x, gv.x, acc[nt][0]);
-                acc[nt][2] = fmaf(mm.y, gv.x, acc[nt][2]);
-                if (!NB1) {
-                    acc[nt][1] = fmaf(mm.x, gv.y, acc[nt][1]);
-                    acc[nt][3] = fmaf(mm.y, gv.y, acc[nt][3]);
+    for (int j = 0; j < NGR; ++j) grow[j] = C::HLN ? t : 8 * (j >> 1) + 2 * t + (j & 1);
+    float acc[2][NACC];
+#pragma unroll
+    for (int rc = 0; rc < 2; ++rc)
+#pragma unroll
+        for (int j = 0; j < NACC; ++j) acc[rc][j] = 0.f;
+    const float z = 0.f;
+    int pl = q.fp, cc = q.ub - q.fp * cs;
+    const int upt = p.upt;
+    float *my_slots = m.slots + (size_t)warp * p.SW * kTileRows * nb;
+
+    auto flush = [&](int pair, bool two) {
+#pragma unroll
+        for (int rc = 0; rc < 2; ++rc) {
+            if (rc == 0 || two) {
+                float *dst = my_slots + (size_t)(upt * (pair - q.fp) + rc) * kTileRows * nb;
+                if (C::HLN) {
+                    if (t < nb) {
+                        dst[g * nb + t] = acc[rc][0];
+                        dst[(g + 8) * nb + t] = acc[rc][1];
+                    }
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int r0 = 8 * nt + 2 * t;
+                        if (r0 < nb) {
+                            dst[g * nb + r0] = acc[rc][4 * nt + 0];
+                            dst[(g + 8) * nb + r0] = acc[rc][4 * nt + 2];
+                        }
+                        if (r0 + 1 < nb) {
+                            dst[g * nb + r0 + 1] = acc[rc][4 * nt + 1];
+                            dst[(g + 8) * nb + r0 + 1] = acc[rc][4 * nt + 3];
+                        }
+                    }
                 }
             }
+#pragma unroll
+            for (int j = 0; j < NACC; ++j) acc[rc][j] = 0.f;
         }
     };
 
     for (int i = 0; i < q.n_my; ++i) {
-        cp_async_wait<DEPTH - 2>();  // this lane's copies of the record have landed
+        cp_async_wait<C::DU - 2>();  // this lane's copies of the unit have landed
         __syncwarp();                 // ... and every lane's; the previous stage is free
         if (ws.left > 0) ws.issue(fill_a, lane);
         cp_async_commit();
-        fill_a += REC;
+        fill_a += UREC;
         if (fill_a == ring_end) fill_a = ring_a;
-        const uint4 q0 = lds128_at<0>(st_a + lane * 16);
-        const uint4 q1 = lds128_at<512>(st_a + lane * 16);
-        const uint4 sc = lds128_at<1024>(st_a + g * 16);
-        uint4 mn = make_uint4(0u, 0u, 0u, 0u);
-        if (FMT == 1) mn = lds128_at<1152>(st_a + g * 16);
-        st_a += REC;
-        if (st_a == ring_end) st_a = ring_a;
-        const uint32_t xu = (uint32_t)(cc * kBlocksPerChunk * xbs);
-        const int blk0 = cc * kBlocksPerChunk;
-        block(q0.x, q1.x, sc.x, mn.x, xu, blk0);
-        block(q0.y, q1.y, sc.y, mn.y, xu + xbs, blk0 + 1);
-        block(q0.z, q1.z, sc.z, mn.z, xu + 2 * xbs, blk0 + 2);
-        block(q0.w, q1.w, sc.w, mn.w, xu + 3 * xbs, blk0 + 3);
-        if (++cc == cs_here) {  // end of this tile's slice: hand the tile over
-            flush(ctl);
-            cc = 0;
-            ++ctl;
+        const bool two = upt == 2 && q.t0 + 2 * pl + 1 < p.T;
+        // offset sums of the chunk's four blocks
+        float G[NGR][4];
+#pragma unroll
+        for (int j = 0; j < NGR; ++j) {
+            const float4 gv = *reinterpret_cast<const float4 *>(m.gs + (cc * C::GSW + grow[j]) * 4);
+            G[j][0] = gv.x;
+            G[j][1] = gv.y;
+            G[j][2] = gv.z;
+            G[j][3] = gv.w;
         }
-    }
-    if (q.n_my > 0 && cc != 0) flush(ctl);  // the range ended inside a tile
-}
-
-// Sum the warps' partials of each tile in warp order (only the warps whose
-// record range touched the tile), undo the activation scale; then (cluster)
-// fold the K-slices into rank 0.  Returns false on cluster ranks other than
-// 0, which have nothing left to do.
-template <bool NB1, int NW>
-__device__ bool fold_tiles(const GemvParams &p, const Geo &q, const Smem &m, int S, int rank, int tid) {
-    constexpr int NTH = NW * 32;
-    const int nb = NB1 ? 1 : p.nb;
-    const int cs = q.cs_here, U = q.U;
-    const int total = q.tiles_here * kTileRows * nb;
-    const size_t wstride = (size_t)p.TG * kTileRows * nb;
-    for (int idx = tid; idx < total; idx += NTH) {
-        const int tl = idx / (kTileRows * nb);
-        const int u0 = tl * cs, u1 = u0 + cs;  // this tile's records [u0, u1)
-        float v = 0.f;
-#pragma unroll 4
-        for (int w = 0; w < NW; ++w) {
-            const int wub = (w * U) / NW, wue = ((w + 1) * U) / NW;
-            if (max(wub, u0) < min(wue, u1)) v += m.slots[(size_t)w * wstride + idx];
-        }
-        m.red[idx] = v * m.nx[5 * kMaxNb + (idx % nb)];
-    }
-    if (S > 1) {
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        if (rank == 0) {
-            for (int idx = tid; idx < total; idx += NTH) {
-                float v = m.red[idx];
-                for (int r = 1; r < S; ++r) v += cluster.map_shared_rank(m.red, r)[idx];
-                m.red[idx] = v;
+        // the records' words: nibbles of rows g and g+8, scales (and mins)
+        uint4 w0[2], w1[2], sw[2], mw[2];
+#pragma unroll
+        for (int rc = 0; rc < 2; ++rc) {
+            w0[rc] = w1[rc] = sw[rc] = mw[rc] = make_uint4(0u, 0u, 0u, 0u);
+            if (rc == 0 || two) {
+                const uint32_t ra = st_a + rc * REC;
+                w0[rc] = lds128_at<0>(ra + lane * 16);
+                w1[rc] = lds128_at<512>(ra + lane * 16);
+                sw[rc] = lds128_at<1024>(ra + g * 16);
+                if (FMT == 1) mw[rc] = lds128_at<1152>(ra + g * 16);
             }
         }
-        cluster.sync();
-        if (rank != 0) return false;
-    } else {
-        __syncthreads();
+        st_a += UREC;
+        if (st_a == ring_end) st_a = ring_a;
+        const uint8_t *xchunk = m.xs + cc * kBlocksPerChunk * xbs;
+
+        auto block = [&](auto blk_c) {
+            constexpr int blk = decltype(blk_c)::value;
+            const uint8_t *xa = xchunk + blk * xbs;
+            uint4 B[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                B[nt][0] = *reinterpret_cast<const uint4 *>(xa + boff[nt]);
+                if (!C::HLN) B[nt][1] = *reinterpret_cast<const uint4 *>(xa + boff[nt] + 16);
+            }
+#pragma unroll
+            for (int rc = 0; rc < 2; ++rc) {
+                if (rc == 1 && !two) continue;
+                uint32_t a[8];
+                unpack_word(word_of<blk>(w0[rc]), a[0], a[2], a[4], a[6]);  // row g
+                unpack_word(word_of<blk>(w1[rc]), a[1], a[3], a[5], a[7]);  // row g + 8
+                const float2 s2 = scale_pair<FMT>(word_of<blk>(sw[rc]));
+                float2 m2 = make_float2(0.f, 0.f);
+                if (FMT == 1) m2 = scale_pair<FMT>(word_of<blk>(mw[rc]));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float d[4];
+                    if (C::HLN) {
+                        // columns (2t, 2t+1) = (hi, lo) of activation row t
+                        mma16816_c(d, a[0], a[1], a[2], a[3], B[nt][0].x, B[nt][0].y, z, z, z, z);
+                        mma16816(d, a[4], a[5], a[6], a[7], B[nt][0].z, B[nt][0].w);
+                        const float T0 = d[0] + d[1], T2 = d[2] + d[3];
+                        if (FMT == 0) {
+                            acc[rc][0] = fmaf(s2.x, T0 - G[0][blk], acc[rc][0]);
+                            acc[rc][1] = fmaf(s2.y, T2 - G[0][blk], acc[rc][1]);
+                        } else {
+                            acc[rc][0] = fmaf(m2.x, G[0][blk], fmaf(s2.x, T0, acc[rc][0]));
+                            acc[rc][1] = fmaf(m2.y, G[0][blk], fmaf(s2.y, T2, acc[rc][1]));
+                        }
+                    } else {
+                        // columns (2t, 2t+1) = activation rows 8nt+2t, 8nt+2t+1; hi, lo as k-steps
+                        mma16816_c(d, a[0], a[1], a[2], a[3], B[nt][0].x, B[nt][0].y, z, z, z, z);
+                        mma16816(d, a[0], a[1], a[2], a[3], B[nt][0].z, B[nt][0].w);
+                        mma16816(d, a[4], a[5], a[6], a[7], B[nt][1].x, B[nt][1].y);
+                        mma16816(d, a[4], a[5], a[6], a[7], B[nt][1].z, B[nt][1].w);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float sj = j < 2 ? s2.x : s2.y;
+                            const float gj = G[2 * nt + (j & 1)][blk];
+                            float &ac = acc[rc][4 * nt + j];
+                            if (FMT == 0) {
+                                ac = fmaf(sj, d[j] - gj, ac);
+                            } else {
+                                const float mj = j < 2 ? m2.x : m2.y;
+                                ac = fmaf(mj, gj, fmaf(sj, d[j], ac));
+                            }
+                        }
+                    }
+                }
+            }
+        };
+        block(std::integral_constant<int, 0>());
+        block(std::integral_constant<int, 1>());
+        block(std::integral_constant<int, 2>());
+        block(std::integral_constant<int, 3>());
+        if (++cc == cs) {  // end of this pair's slice: hand the tiles over
+            flush(pl, two);
+            cc = 0;
+            ++pl;
+        }
     }
-    return true;
+    if (q.n_my > 0 && cc != 0) flush(pl, upt == 2 && q.t0 + 2 * pl + 1 < p.T);  // the range ended inside a unit
 }
 
-// Write the job's outputs from `red`: store, residual add, SwiGLU over a
-// gate/up tile pair, or this group's (max, index) per activation row.
-template <bool NB1, int NW>
-__device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int group, int tid, int warp, int lane) {
-    constexpr int NTH = NW * 32;
-    const int nb = NB1 ? 1 : p.nb;
+// Sum of the partials of output (tile tl, row, activation row r) over the
+// warps whose unit range touched the tile, in warp order.  Warp w holds
+// units [w*U/NW, (w+1)*U/NW) (empty for some w when U < NW); the warp
+// holding unit u is floor(((u+1)*NW - 1) / U), so the walk goes from the
+// holder of the tile's first unit to the holder of the first unit past that
+// warp's range, and so on -- visiting exactly the warps that hold units.
+template <int CLS>
+__device__ __forceinline__ float fold_one(const GemvParams &p, const Geo &q, const Smem &m, int tl, int row, int r,
+                                          int nb) {
+    constexpr int NW = Cls<CLS>::NW;
+    const int pl = tl / p.upt, sub = tl - pl * p.upt;
+    const int u1 = (pl + 1) * q.cs;  // the tile's units: [pl*cs, u1)
+    float v = 0.f;
+    if (q.U < (1 << 26)) {
+        const unsigned U = (unsigned)q.U;
+        for (unsigned u = (unsigned)(pl * q.cs); u < (unsigned)u1;) {
+            const unsigned w = ((u + 1) * NW - 1) / U;
+            const unsigned wub = w * U / NW;
+            const int ls = p.upt * (pl - (int)wub / q.cs) + sub;
+            v += m.slots[((size_t)(w * p.SW + ls) * kTileRows + row) * nb + r];
+            u = (w + 1) * U / NW;
+        }
+    } else {
+        const long long U = q.U;
+        for (long long u = (long long)pl * q.cs; u < u1;) {
+            const long long w = ((u + 1) * NW - 1) / U;
+            const long long wub = w * U / NW;
+            const int ls = p.upt * (pl - (int)(wub / q.cs)) + sub;
+            v += m.slots[((size_t)(w * p.SW + ls) * kTileRows + row) * nb + r];
+            u = (w + 1) * U / NW;
+        }
+    }
+    return v;
+}
+
+// Cluster K-split (S > 1): fold the warps' partials of each tile into
+// `red`, apply the output factor, then fold the K-slices into rank 0 over
+// distributed shared memory in rank order.  Returns false on cluster ranks
+// other than 0, which have nothing left to do.
+template <int CLS>
+__device__ bool fold_tiles(const GemvParams &p, const Geo &q, const Smem &m, int S, int rank, int tid) {
+    constexpr int NTH = Cls<CLS>::NW * 32;
+    const int nb = CLS == 0 ? 1 : p.nb;
+    const int total = q.tiles_here * kTileRows * nb;
+    for (int idx = tid; idx < total; idx += NTH) {
+        const int tl = idx / (kTileRows * nb);
+        const int rem = idx - tl * kTileRows * nb;
+        const int row = rem / nb, r = rem - row * nb;
+        m.red[idx] = fold_one<CLS>(p, q, m, tl, row, r, nb) * m.nx[5 * kMaxNb + r];
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (rank == 0) {
+        for (int idx = tid; idx < total; idx += NTH) {
+            float v = m.red[idx];
+            for (int rr = 1; rr < S; ++rr) v += cluster.map_shared_rank(m.red, rr)[idx];
+            m.red[idx] = v;
+        }
+    }
+    cluster.sync();
+    return rank == 0;
+}
+
+// Output (tile tl, row, activation row r) of the CTA's group: from `red`
+// after a cluster fold, else folded from the warp partials here.
+template <int CLS>
+__device__ __forceinline__ float out_value(const GemvParams &p, const Geo &q, const Smem &m, int S, int tl, int row,
+                                           int r, int nb) {
+    if (S > 1) return m.red[(tl * kTileRows + row) * nb + r];
+    return fold_one<CLS>(p, q, m, tl, row, r, nb) * m.nx[5 * kMaxNb + r];
+}
+
+// Write the job's outputs: store, residual add, SwiGLU over a gate/up tile
+// pair, or this group's (max, index) per activation row.
+template <int CLS>
+__device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int S, int group, int tid, int warp,
+                         int lane) {
+    constexpr int NW = Cls<CLS>::NW, NTH = NW * 32;
+    const int nb = CLS == 0 ? 1 : p.nb;
     const int total = q.tiles_here * kTileRows * nb;
     if (group >= p.groups) return;  // no tiles, no partials
     if (p.epi == EPI_ARGMAX) {
@@ -726,7 +994,7 @@ __device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int g
             for (int ri = tid; ri < q.tiles_here * kTileRows; ri += NTH) {
                 const int n = (q.t0 + ri / kTileRows) * kTileRows + (ri % kTileRows);
                 if (n >= N) continue;
-                const float v = m.red[ri * nb + r];
+                const float v = out_value<CLS>(p, q, m, S, ri / kTileRows, ri % kTileRows, r, nb);
                 if (p.out[0] != nullptr) p.out[0][(size_t)r * N + n] = v;
                 am_take(bv, bi, v, n);
             }
@@ -761,13 +1029,13 @@ __device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int g
         const int n = tm * kTileRows + row;
         const int N = p.n[mi];
         if (n >= N) continue;
-        const float v = m.red[idx];
+        const float v = out_value<CLS>(p, q, m, S, tl, row, r, nb);
         if (p.epi == EPI_STORE) {
             p.out[mi][(size_t)r * N + n] = v;
         } else if (p.epi == EPI_RESIDUAL) {
             p.out[0][(size_t)r * N + n] = v + __ldcg(p.res + (size_t)r * N + n);
         } else if (mi == 0) {  // EPI_SWIGLU: gate tile tl, up tile tl + 1
-            const float u = m.red[idx + kTileRows * nb];
+            const float u = out_value<CLS>(p, q, m, S, tl + 1, row, r, nb);
             p.out[0][(size_t)r * N + n] = v / (1.0f + expf(-v)) * u;
         }
     }
@@ -775,45 +1043,32 @@ __device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int g
 }
 
 // Single K-slice, store / residual / SwiGLU jobs: fold each output's warp
-// partials (in warp order) and write it at once, with no round trip through
-// `red` and one barrier fewer than fold_tiles + epilogue.
-template <bool NB1, int NW>
+// partials and write it at once, with no round trip through `red`.
+template <int CLS>
 __device__ void fold_store(const GemvParams &p, const Geo &q, const Smem &m, int group, int tid) {
-    constexpr int NTH = NW * 32;
-    const int nb = NB1 ? 1 : p.nb;
+    constexpr int NTH = Cls<CLS>::NW * 32;
+    const int nb = CLS == 0 ? 1 : p.nb;
     if (group >= p.groups) return;  // no tiles
-    const int cs = q.cs_here, U = q.U;
-    const size_t wstride = (size_t)p.TG * kTileRows * nb;
     const int tile_vals = kTileRows * nb;
-    auto fold = [&](int idx) -> float {
-        const int tl = idx / tile_vals;
-        const int u0 = tl * cs, u1 = u0 + cs;  // this tile's records [u0, u1)
-        float v = 0.f;
-#pragma unroll 4
-        for (int w = 0; w < NW; ++w) {
-            const int wub = (w * U) / NW, wue = ((w + 1) * U) / NW;
-            if (max(wub, u0) < min(wue, u1)) v += m.slots[(size_t)w * wstride + idx];
-        }
-        return v * m.nx[5 * kMaxNb + (idx % nb)];
-    };
     const bool pairs = p.epi == EPI_SWIGLU;
     const int total = (pairs ? q.tiles_here / 2 : q.tiles_here) * tile_vals;
     for (int e = tid; e < total; e += NTH) {
         const int tp = e / tile_vals, rem = e - tp * tile_vals;
-        const int idx = (pairs ? 2 * tp : tp) * tile_vals + rem;
+        const int tl = pairs ? 2 * tp : tp;
         const int row = rem / nb, r = rem - row * nb;
         int mi, tm;
-        map_tile(p, q.t0 + idx / tile_vals, mi, tm);
+        map_tile(p, q.t0 + tl, mi, tm);
         const int n = tm * kTileRows + row;
         const int N = p.n[mi];
         if (n >= N) continue;
-        const float v = fold(idx);
+        const float f = m.nx[5 * kMaxNb + r];
+        const float v = fold_one<CLS>(p, q, m, tl, row, r, nb) * f;
         if (p.epi == EPI_STORE) {
             p.out[mi][(size_t)r * N + n] = v;
         } else if (p.epi == EPI_RESIDUAL) {
             p.out[0][(size_t)r * N + n] = v + __ldcg(p.res + (size_t)r * N + n);
         } else {  // SwiGLU: gate tile, then its up tile
-            const float u = fold(idx + tile_vals);
+            const float u = fold_one<CLS>(p, q, m, tl + 1, row, r, nb) * f;
             p.out[0][(size_t)r * N + n] = v / (1.0f + expf(-v)) * u;
         }
     }
@@ -821,44 +1076,44 @@ __device__ void fold_store(const GemvParams &p, const Geo &q, const Smem &m, int
 }
 
 // ---------------------------------------------------------------------------
-// Per-call kernel: one job, one group of tiles per cluster.
-template <int FMT, int NT, bool NB1>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ GemvParams p) {
+// Per-call kernel: one job, one group of tile pairs per cluster.
+template <int FMT, int CLS>
+__global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid_constant__ GemvParams p) {
+    using C = Cls<CLS>;
     constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
-    constexpr int DEPTH = kRingDepth;
-    constexpr int NW = kWarps;
+    constexpr int NW = C::NW;
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = p.S;
     const int group = blockIdx.x / S, rank = blockIdx.x - group * S;
-    const int nb = NB1 ? 1 : p.nb;
-    const Smem m = carve<NW>(smem, FMT, nb, p.Cs, 8 * NT, p.TG);
-    const uint32_t ring_a = smem_u32(m.ring) + warp * DEPTH * REC;
+    const int nb = CLS == 0 ? 1 : p.nb;
+    const Smem m = carve<CLS>(smem, nb, p.Cs, p.TG, p.SW, S);
+    const uint32_t ring_a = smem_u32(m.ring) + warp * C::DU * 2 * REC;
 
     // the next kernel may launch now; it waits for this one before it reads
     // what this one writes
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // weights do not depend on the previous kernel: start their copies first
+    const Geo q = make_geo<NW>(p, group, rank, warp);
     WeightStream<REC, NW> ws;
-    ws.init(&p, 1, group, rank, warp);
-    for (int s = 0; s < DEPTH - 1; ++s) {
-        if (ws.left > 0) ws.issue(ring_a + s * REC, lane);
+    ws.init_one(&p, q);
+    for (int s = 0; s < C::DU - 1; ++s) {
+        if (ws.left > 0) ws.issue(ring_a + s * 2 * REC, lane);
         cp_async_commit();
     }
-    const Geo q = make_geo<NW>(p, group, rank, warp);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    stage_x<FMT, NT, NB1, NW>(p, q, m, S, tid, warp, lane);
-    uint32_t st_a = ring_a, fill_a = ring_a + (DEPTH - 1) * REC;
-    run_units<FMT, NT, NB1, DEPTH, NW>(p, q, m, ws, st_a, fill_a, ring_a, warp, lane);
+    stage_x<FMT, CLS, 16>(p, q, m, S, tid, warp, lane);
+    uint32_t st_a = ring_a, fill_a = ring_a + (C::DU - 1) * 2 * REC;
+    run_units<FMT, CLS>(p, q, m, ws, st_a, fill_a, ring_a, warp, lane);
     cp_async_wait<0>();
     __syncthreads();
     if (S == 1 && p.epi != EPI_ARGMAX) {
-        fold_store<NB1, NW>(p, q, m, group, tid);
+        fold_store<CLS>(p, q, m, group, tid);
         return;
     }
-    if (!fold_tiles<NB1, NW>(p, q, m, S, rank, tid)) return;
-    epilogue<NB1, NW>(p, q, m, group, tid, warp, lane);
+    if (S > 1 && !fold_tiles<CLS>(p, q, m, S, rank, tid)) return;
+    epilogue<CLS>(p, q, m, S, group, tid, warp, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -903,40 +1158,40 @@ __device__ __forceinline__ bool grid_barrier(unsigned *counter, unsigned *releas
     return fail == 0;
 }
 
-template <int FMT, int NT, bool NB1>
-__global__ void __launch_bounds__(kStepWarps * 32, 1) decode_kernel(const __grid_constant__ StepParams sp) {
+template <int FMT, int CLS>
+__global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __grid_constant__ StepParams sp) {
+    using C = Cls<CLS>;
     constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
-    constexpr int DEPTH = kStepRingDepth;
-    constexpr int NW = kStepWarps;
+    constexpr int NW = C::NW;
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int group = blockIdx.x;
-    const int nb = NB1 ? 1 : sp.nb;
+    const int nb = CLS == 0 ? 1 : sp.nb;
     const int cs_max = (sp.Kmax + kChunkK - 1) / kChunkK;  // as the host sized it
-    const Smem m = carve<NW>(smem, FMT, nb, cs_max, 8 * NT, sp.TGmax);
-    const uint32_t ring_a = smem_u32(m.ring) + warp * DEPTH * REC;
+    const Smem m = carve<CLS>(smem, nb, cs_max, sp.TGmax, sp.SWmax, 1);
+    const uint32_t ring_a = smem_u32(m.ring) + warp * C::DU * 2 * REC;
 
     WeightStream<REC, NW> ws;
     ws.init(sp.jobs, sp.njobs, group, 0, warp);
-    for (int s = 0; s < DEPTH - 1; ++s) {
-        if (ws.left > 0) ws.issue(ring_a + s * REC, lane);
+    for (int s = 0; s < C::DU - 1; ++s) {
+        if (ws.left > 0) ws.issue(ring_a + s * 2 * REC, lane);
         cp_async_commit();
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    uint32_t st_a = ring_a, fill_a = ring_a + (DEPTH - 1) * REC;
+    uint32_t st_a = ring_a, fill_a = ring_a + (C::DU - 1) * 2 * REC;
     for (int j = 0; j < sp.njobs; ++j) {
         const GemvParams &p = sp.jobs[j];
         if (j > 0 && !grid_barrier(sp.counter, sp.release, sp.err, (unsigned)j)) return;
         const Geo q = make_geo<NW>(p, group, 0, warp);
-        stage_x<FMT, NT, NB1, NW>(p, q, m, 1, tid, warp, lane);
-        run_units<FMT, NT, NB1, DEPTH, NW>(p, q, m, ws, st_a, fill_a, ring_a, warp, lane);
+        if (q.tiles_here == 0) continue;  // no work in this job (CTA-uniform)
+        stage_x<FMT, CLS, 8>(p, q, m, 1, tid, warp, lane);
+        run_units<FMT, CLS>(p, q, m, ws, st_a, fill_a, ring_a, warp, lane);
         __syncthreads();
         if (p.epi != EPI_ARGMAX) {
-            fold_store<NB1, NW>(p, q, m, group, tid);
+            fold_store<CLS>(p, q, m, group, tid);
         } else {
-            fold_tiles<NB1, NW>(p, q, m, 1, 0, tid);
-            epilogue<NB1, NW>(p, q, m, group, tid, warp, lane);
+            epilogue<CLS>(p, q, m, 1, group, tid, warp, lane);
         }
     }
     cp_async_wait<0>();

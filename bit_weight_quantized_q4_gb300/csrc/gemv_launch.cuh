@@ -1,7 +1,7 @@
-// gemv_launch.cuh -- host launcher for the dequant-in-GEMV kernel: picks the
-// n-tile count from nb, raises the dynamic shared-memory limit once per
-// device, and launches with programmatic dependent launch (and a cluster
-// when K is split).
+// gemv_launch.cuh -- host launchers for the dequant-in-GEMV kernels: pick the
+// batch class from nb, raise the dynamic shared-memory limit once per device
+// and kernel, and launch with programmatic dependent launch (plus a cluster
+// when K is split, or cooperatively for the decode step).
 #pragma once
 #include <cuda_runtime.h>
 
@@ -9,21 +9,28 @@
 
 namespace q4 {
 
-template <int FMT, int NT, bool NB1>
-static int launch_nt(const GemvParams &p, const Plan &plan, cudaStream_t stream) {
-    auto kern = dev::gemv_kernel<FMT, NT, NB1>;
+template <typename Kern>
+static bool raise_smem(Kern kern, size_t smem, size_t (&set)[64]) {
     int devid = 0;
-    if (cudaGetDevice(&devid) != cudaSuccess) return -1;
-    static size_t smem_set[64] = {0};
-    if (devid < 64 && plan.smem > smem_set[devid]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem) !=
-            cudaSuccess)
-            return -1;
-        smem_set[devid] = plan.smem;
+    if (cudaGetDevice(&devid) != cudaSuccess) return false;
+    if (devid < 64 && smem > set[devid]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return false;
+        set[devid] = smem;
+    } else if (devid >= 64) {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess;
     }
+    return true;
+}
+
+template <int FMT, int CLS>
+static int launch_cls(const GemvParams &p, const Plan &plan, cudaStream_t stream) {
+    auto kern = dev::gemv_kernel<FMT, CLS>;
+    static size_t smem_set[64] = {0};
+    if (!raise_smem(kern, plan.smem, smem_set)) return -1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.ctas, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(cls_warps(CLS) * 32, 1, 1);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
@@ -45,25 +52,22 @@ static int launch_nt(const GemvParams &p, const Plan &plan, cudaStream_t stream)
 
 template <int FMT>
 static int launch_gemv_fmt(const GemvParams &p, const Plan &plan, cudaStream_t stream) {
-    if (p.nb == 1) return launch_nt<FMT, 1, true>(p, plan, stream);
-    if (p.nb <= 8) return launch_nt<FMT, 1, false>(p, plan, stream);
-    return launch_nt<FMT, 2, false>(p, plan, stream);
+    switch (cls_of(p.nb)) {
+        case 0: return launch_cls<FMT, 0>(p, plan, stream);
+        case 1: return launch_cls<FMT, 1>(p, plan, stream);
+        case 2: return launch_cls<FMT, 2>(p, plan, stream);
+        default: return launch_cls<FMT, 3>(p, plan, stream);
+    }
 }
 
-template <int FMT, int NT, bool NB1>
-static int launch_step_nt(const StepParams &p, int ctas, size_t smem, cudaStream_t stream) {
-    auto kern = dev::decode_kernel<FMT, NT, NB1>;
-    int devid = 0;
-    if (cudaGetDevice(&devid) != cudaSuccess) return -1;
+template <int FMT, int CLS>
+static int launch_step_cls(const StepParams &p, int ctas, size_t smem, cudaStream_t stream) {
+    auto kern = dev::decode_kernel<FMT, CLS>;
     static size_t smem_set[64] = {0};
-    if (devid < 64 && smem > smem_set[devid]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return -1;
-        smem_set[devid] = smem;
-    }
+    if (!raise_smem(kern, smem, smem_set)) return -1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas, 1, 1);
-    cfg.blockDim = dim3(kStepWarps * 32, 1, 1);
+    cfg.blockDim = dim3(cls_warps(CLS) * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
@@ -78,27 +82,33 @@ static int launch_step_nt(const StepParams &p, int ctas, size_t smem, cudaStream
 
 template <int FMT>
 static int launch_step_fmt(const StepParams &p, int ctas, size_t smem, cudaStream_t stream) {
-    if (p.nb == 1) return launch_step_nt<FMT, 1, true>(p, ctas, smem, stream);
-    if (p.nb <= 8) return launch_step_nt<FMT, 1, false>(p, ctas, smem, stream);
-    return launch_step_nt<FMT, 2, false>(p, ctas, smem, stream);
+    switch (cls_of(p.nb)) {
+        case 0: return launch_step_cls<FMT, 0>(p, ctas, smem, stream);
+        case 1: return launch_step_cls<FMT, 1>(p, ctas, smem, stream);
+        case 2: return launch_step_cls<FMT, 2>(p, ctas, smem, stream);
+        default: return launch_step_cls<FMT, 3>(p, ctas, smem, stream);
+    }
 }
 
-template <int FMT, int NT, bool NB1>
-static int step_occupancy(size_t smem) {
-    auto kern = dev::decode_kernel<FMT, NT, NB1>;
+template <int FMT, int CLS>
+static int step_occupancy_cls(size_t smem) {
+    auto kern = dev::decode_kernel<FMT, CLS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return 0;
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, kStepWarps * 32, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, cls_warps(CLS) * 32, smem) != cudaSuccess)
         return 0;
     return blocks;
 }
 
 template <int FMT>
 static int step_occupancy_fmt(int nb, size_t smem) {
-    if (nb == 1) return step_occupancy<FMT, 1, true>(smem);
-    if (nb <= 8) return step_occupancy<FMT, 1, false>(smem);
-    return step_occupancy<FMT, 2, false>(smem);
+    switch (cls_of(nb)) {
+        case 0: return step_occupancy_cls<FMT, 0>(smem);
+        case 1: return step_occupancy_cls<FMT, 1>(smem);
+        case 2: return step_occupancy_cls<FMT, 2>(smem);
+        default: return step_occupancy_cls<FMT, 3>(smem);
+    }
 }
 
 }  // namespace q4

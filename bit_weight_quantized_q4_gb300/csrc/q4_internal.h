@@ -47,16 +47,34 @@ inline int64_t chunks_of(int64_t k) { return (k + kChunkK - 1) / kChunkK; }
 enum Mode { MODE_SINGLE = 0, MODE_CONCAT = 1, MODE_PAIRS = 2 };
 enum Epi { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
 
-constexpr int kThreads = 256;                 // per-call kernel: 8 warps per CTA
-constexpr int kWarps = kThreads / 32;
-constexpr int kStepWarps = 16;               // persistent decode-step kernel: 16 warps per CTA
+#if defined(__CUDACC__)
+#define Q4_HD __host__ __device__
+#else
+#define Q4_HD
+#endif
+
 constexpr int kMaxNb = 16;
 constexpr int kMaxCluster = 8;
 constexpr size_t kXsCap = 64 * 1024;          // activation slice staged per CTA
-constexpr int kRingDepth = 8;                 // weight records per warp in the cp.async ring
+constexpr size_t kSmemMax = 227 * 1024;       // dynamic shared memory of one CTA
+constexpr int kMaxMats = 3;                   // matrices of one job (q, k, v share one input)
 
-constexpr int kMaxMats = 3;                // matrices of one job (q, k, v share one input)
+// Batch classes.  The activation rows of a launch become the n columns of
+// the m16n8k16 tensor-core products:
+//   class 0 (nb = 1) and 1 (nb = 2..4): the hi and lo halves of row r are
+//     columns 2r and 2r+1 -- two mma per 32-weight block;
+//   class 2 (nb = 5..8): row r is column r, hi and lo are two k-steps into
+//     one accumulator -- four mma per block;
+//   class 3 (nb = 9..16): as class 2 over two 8-column n-tiles -- eight.
+Q4_HD constexpr int cls_of(int nb) { return nb <= 1 ? 0 : nb <= 4 ? 1 : nb <= 8 ? 2 : 3; }
+Q4_HD constexpr int cls_warps(int c) { return c == 3 ? 8 : 16; }     // warps per CTA
+Q4_HD constexpr int cls_depth(int c) { return c == 0 ? 4 : 3; }      // ring stages (units) per warp
+Q4_HD constexpr int cls_gsw(int c) { return c <= 1 ? 4 : c == 2 ? 8 : 16; }  // group-sum rows per chunk
 
+// A unit of work is one 128-column chunk of upt consecutive 16-row tiles
+// (upt records).  upt is 2 -- a tile pair (2p, 2p+1), for gate/up jobs
+// (gate tile p, up tile p) -- unless a job has fewer pairs than the CTAs
+// that run it, then 1.
 struct GemvParams {
     const uint8_t *w[kMaxMats];  // packed weights
     int n[kMaxMats];             // output rows of each matrix
@@ -68,9 +86,11 @@ struct GemvParams {
     int C;                       // 128-column chunks per row
     int nb;                      // activation rows
     int TG;                      // most tiles one group holds (sizes shared memory)
+    int SW;                      // tile slots per warp for partial sums (sizes shared memory)
+    int upt;                     // tiles per unit: 2, or 1 for jobs with few tiles
     int S;                       // K-split: CTAs per cluster
     int Cs;                      // chunks per K-slice
-    int groups;                  // tile groups; group g holds tile units [g*P/groups, (g+1)*P/groups)
+    int groups;                  // groups; group g holds units [g*P/groups, (g+1)*P/groups) of the P = T/upt
     const float *x;              // [nb][K]
     const float *gamma;          // [K] or nullptr (no RMSNorm)
     float eps;
@@ -84,7 +104,6 @@ struct GemvParams {
 
 // The persistent decode-step kernel runs these jobs in order, one CTA per SM.
 constexpr int kMaxStepJobs = 4 * 32 + 1;      // four jobs per layer, up to 32 layers, + logits
-constexpr int kStepRingDepth = 8;             // weight records per warp of the decode-step kernel
 constexpr long long kBarrierSpins = 1ll << 22;  // polls before a grid barrier gives up
 
 struct StepParams {
@@ -92,6 +111,7 @@ struct StepParams {
     int nb;
     int Kmax;                    // largest K of the jobs (sizes the activation slice)
     int TGmax;                   // most tiles any group holds in any job
+    int SWmax;                   // most tile slots per warp of any job
     unsigned *counter;           // grid-barrier arrivals (zeroed before each launch)
     unsigned *release;           // number of the last completed barrier (zeroed before each launch)
     int *err;                    // set to 1 if a barrier gave up
@@ -100,73 +120,128 @@ struct StepParams {
     GemvParams jobs[kMaxStepJobs];
 };
 
-inline int ntiles_for(int nb) { return nb <= 8 ? 1 : 2; }
+#if defined(__CUDACC__)
+// Sum over each half-warp (lanes 0..15 and 16..31) as a butterfly over lane
+// xor 1, 2, 4, 8: every lane of the half ends with the same value.  The
+// affine block sums of the staged activations and q4_group_sums both add
+// this way (pair sums first), so the two give the same bits.
+__device__ __forceinline__ float half_warp_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    return v;
+}
+#endif
 
-// Dynamic shared memory of one CTA of the engine: activation slice, group
-// sums (affine), per-warp tile partials, reductions, the weight ring.
-inline size_t engine_smem(int fmt, int TG, int Cs, int nb, int warps, int depth) {
-    size_t xs = (size_t)4 * nb * Cs * kChunkK;
-    size_t gs = fmt == 1 ? (size_t)4 * Cs * kBlocksPerChunk * 8 * ntiles_for(nb) : 0;
-    size_t red = (size_t)4 * TG * kTileRows * nb;
-    size_t slots = (size_t)4 * warps * TG * kTileRows * nb;
-    size_t misc = (size_t)4 * 4 * warps * kMaxNb + 4 * 8 * kMaxNb;
-    size_t ring = (size_t)warps * depth * rec_bytes(fmt);
+// Dynamic shared memory of one engine CTA: activation slice (B fragments),
+// group sums, tile results (only for a cluster fold, S > 1), per-warp tile
+// partials, reductions, weight ring.
+inline size_t engine_smem(int fmt, int nb, int TG, int Cs, int SW, int S) {
+    const int c = cls_of(nb);
+    const size_t NW = (size_t)cls_warps(c);
+    const size_t xs = (size_t)512 * nb * Cs;
+    const size_t gs = (size_t)16 * cls_gsw(c) * Cs;
+    const size_t red = S > 1 ? (size_t)64 * TG * nb : 0;
+    const size_t slots = (size_t)64 * NW * SW * nb;
+    const size_t misc = (size_t)16 * NW * kMaxNb + 32 * kMaxNb;
+    const size_t ring = NW * cls_depth(c) * 2 * rec_bytes(fmt);
     return xs + gs + red + slots + misc + ring;
 }
 
-inline size_t smem_bytes(int fmt, int TG, int Cs, int nb) {
-    return engine_smem(fmt, TG, Cs, nb, kWarps, kRingDepth);
-}
-
-// Dynamic shared memory of one decode-step CTA.
-inline size_t step_smem_bytes(int fmt, int TGmax, int Kmax, int nb) {
-    const int Cs = (Kmax + kChunkK - 1) / kChunkK;
-    return engine_smem(fmt, TGmax, Cs, nb, kStepWarps, kStepRingDepth);
+// Most tile units one warp's contiguous unit range touches, over the group
+// sizes np in {np_a, np_b} and K-slice widths cs in {cs_a, cs_b}; upt times
+// that is the warp's tile-slot count.  A range of len units of a cs-chunk pair
+// sequence touches at most ceil(len / cs) + 1 pairs; this is the exact
+// maximum for the warp split the kernel uses.
+inline int slots_per_warp(int np_a, int np_b, int cs_a, int cs_b, int NW, int upt) {
+    int best = 1;
+    const int nps[2] = {np_a, np_b}, css[2] = {cs_a, cs_b};
+    for (int i = 0; i < 2; ++i) {
+        for (int j = 0; j < 2; ++j) {
+            const long long np = nps[i], cs = css[j];
+            if (np <= 0 || cs <= 0) continue;
+            const long long U = np * cs;
+            for (int w = 0; w < NW; ++w) {
+                const long long ub = w * U / NW, ue = (w + 1) * U / NW;
+                if (ue > ub) {
+                    const int touched = (int)((ue - 1) / cs - ub / cs + 1);
+                    if (touched > best) best = touched;
+                }
+            }
+        }
+    }
+    return upt * best;
 }
 
 struct Plan {
-    int TG, S, Cs, groups, ctas;
+    int TG, S, Cs, groups, ctas, SW, upt;
     size_t smem;
 };
 
-// Launch plan for T tiles x C chunks.  One group of tiles per cluster of S
-// CTAs (S splits K); at most one CTA per SM where the work allows, so that
+// Tiles per unit: pairs unless that leaves CTAs idle (gate/up jobs: always
+// pairs, so a gate tile and its up tile share a CTA).
+inline int units_of(int T, bool pairs, int ctas, int &upt) {
+    upt = pairs || (T + 1) / 2 >= ctas ? 2 : 1;
+    return (T + upt - 1) / upt;
+}
+
+// Launch plan for T tiles x C chunks.  One group of tile pairs per cluster of
+// S CTAs (S splits K); at most one CTA per SM where the work allows, so that
 // the next kernel in the stream can be resident beside it.  Chooses the
-// split whose busiest CTA has the least work; ties go to the smaller split.
+// split whose busiest SM streams the fewest records; ties go to the smaller
+// split.  A plan whose shared memory exceeds kSmemMax is never chosen while
+// another fits.
 inline Plan make_plan(int fmt, int T, int C, int nb, bool pairs, int num_sms) {
-    const int pw = pairs ? 2 : 1;
-    const int P = T / pw;                       // allocation units (tiles or gate/up pairs)
+    const int NW = cls_warps(cls_of(nb));
     Plan best{};
     long long best_cost = -1;
+    bool best_fits = false;
     for (int S = 1; S <= kMaxCluster; S *= 2) {
         if (S > 1 && S > C) break;
         const int Cs = (C + S - 1) / S;
-        if ((size_t)4 * nb * Cs * kChunkK > kXsCap && S < kMaxCluster) continue;
-        int G = num_sms / S;
-        if (G < 1) G = 1;
-        if (G > P) G = P;
-        int per = (P + G - 1) / G;                      // units of the busiest group
-        const int cap = 128 / (nb * pw) > 0 ? 128 / (nb * pw) : 1;  // per-warp partials fit shared memory
-        if (per > cap) {
-            per = cap;
-            G = (P + per - 1) / per;
+        if ((size_t)512 * nb * Cs > kXsCap && S < kMaxCluster) continue;
+        int G0 = num_sms / S;
+        if (G0 < 1) G0 = 1;
+        int upt = 2;
+        const int P = units_of(T, pairs, G0, upt);
+        // one wave of groups where the partial sums fit, else more groups
+        // (fewer pairs each) until they do
+        Plan pl;
+        for (int mult = 1;; ++mult) {
+            const int G = (int)((long long)G0 * mult < P ? (long long)G0 * mult : P);
+            const int per = (P + G - 1) / G, per_lo = P / G;
+            const int cs_last = C - ((C - 1) / Cs) * Cs;  // chunks of the last non-empty K-slice
+            pl.S = S;
+            pl.Cs = Cs;
+            pl.groups = G;
+            pl.ctas = G * S;
+            pl.upt = upt;
+            pl.TG = upt * per < T ? upt * per : T;
+            pl.SW = slots_per_warp(per, per_lo, Cs, cs_last, NW, upt);
+            pl.smem = engine_smem(fmt, nb, pl.TG, Cs, pl.SW, S);
+            if (pl.smem <= kSmemMax || G == P) break;
         }
-        const int ctas = G * S;
-        const int waves = (ctas + num_sms - 1) / num_sms;
+        const int per = (P + pl.groups - 1) / pl.groups;
+        const bool fits = pl.smem <= kSmemMax;
+        const int waves = (pl.ctas + num_sms - 1) / num_sms;
         // records on the busiest SM, plus about a microsecond of one SM's
-        // share of HBM (~40 records) for each cluster-wide exchange
-        const long long cost = (long long)per * pw * Cs * waves + (S > 1 ? 40 : 0);
-        if (best_cost < 0 || cost < best_cost) {
+        // share of HBM (~40 records) for each cluster-wide exchange and
+        // about 1.5 us (~60 records) of staging and folding per extra wave
+        const long long cost = (long long)per * upt * Cs * waves + (S > 1 ? 40 : 0) + 60 * (waves - 1);
+        if (best_cost < 0 || (fits && !best_fits) || (fits == best_fits && cost < best_cost)) {
             best_cost = cost;
-            best.TG = per * pw;
-            best.S = S;
-            best.Cs = Cs;
-            best.groups = G;
-            best.ctas = ctas;
+            best_fits = fits;
+            best = pl;
         }
     }
-    best.smem = smem_bytes(fmt, best.TG, best.Cs, nb);
     return best;
+}
+
+// Dynamic shared memory of one decode-step CTA.
+inline size_t step_smem_bytes(int fmt, int nb, int TGmax, int Kmax, int SWmax) {
+    const int Cs = (Kmax + kChunkK - 1) / kChunkK;
+    return engine_smem(fmt, nb, TGmax, Cs, SWmax, 1);
 }
 
 // Launchers, one per kernel instantiation family (defined in the .cu files).

@@ -73,21 +73,26 @@ def test_packed_sizes_and_padding():
 def test_plan_invariants(fmt, tiles, chunks, pairs, nb):
     sms = 152
     p = q4.plan(fmt, tiles, chunks, nb, pairs, sms)
-    pw = 2 if pairs else 1
-    units = tiles // pw
+    # work is handed out in tile pairs, or single tiles when pairs would
+    # leave CTAs idle (never for gate/up jobs)
+    upt = 2 if pairs or (tiles + 1) // 2 >= max(1, sms // p["S"]) else 1
+    units = -(-tiles // upt)
     assert 1 <= p["S"] <= 8 and (p["S"] & (p["S"] - 1)) == 0
     assert p["S"] * p["Cs"] >= chunks and p["Cs"] >= 1
+    assert (p["S"] - 1) * p["Cs"] < chunks         # no empty K-slice
     assert 1 <= p["groups"] <= units
-    # balanced contiguous ranges: the busiest group holds TG tiles and all fit
-    assert p["TG"] == -(-units // p["groups"]) * pw or p["TG"] == max(1, 128 // (nb * pw)) * pw
+    # balanced contiguous ranges of units: the busiest group holds TG tiles
+    assert p["TG"] == min(upt * -(-units // p["groups"]), tiles)
     assert p["groups"] * p["TG"] >= tiles
     assert p["ctas"] == p["groups"] * p["S"]
+    # one wave of CTAs (one per SM) unless the partial sums of a one-wave
+    # plan would not fit shared memory (large nb x many tiles)
+    if nb <= 4:
+        assert p["ctas"] <= sms
+    assert p["ctas"] <= 8 * sms
     assert p["smem"] <= 227 * 1024
-    assert p["TG"] * nb <= max(128, nb * pw)       # partial sums fit shared memory
     if pairs:
         assert p["TG"] % 2 == 0
-    if p["TG"] * nb < 128 // pw:                    # not capped: at most one CTA per SM
-        assert p["ctas"] <= sms
     # the activation slice fits the staging budget
     assert 4 * nb * p["Cs"] * 128 <= 64 * 1024 or p["S"] == 8
 

@@ -58,8 +58,19 @@ def test_noalloc_matches_workspace_argmax_twice(q4):
 
 
 def test_noalloc_rejects_beyond_its_fixed_array(q4):
-    # 2^20 rows at nb = 16 need far more (max, index) pairs than the array holds.
-    c = q4._CWeight(0, 1 << 20, 32, 0x10000, q4.packed_bytes(0, 1 << 20, 32))
-    st = q4.lib().q4_argmax_noalloc(ctypes.byref(c), ctypes.c_void_p(0x10000), None, ctypes.c_float(0.0),
-                                    ctypes.c_int32(16), ctypes.c_void_p(0x20000), None, None, None)
+    # 2^22 rows of 32 at nb = 16 need more (max, index) pairs than the array
+    # holds.  The buffers are real device memory (contents unused), so that a
+    # call accepted by mistake would compute on them, never touch a bogus
+    # address.
+    n, k, nb = 1 << 22, 32, 16
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    groups = q4.plan(0, n // 16, 1, nb, False, sms)["groups"]
+    assert groups * nb * 8 > 128 * 1024
+    wbuf = torch.empty(q4.packed_bytes(0, n, k), dtype=torch.uint8, device="cuda")
+    x = torch.zeros((nb, k), dtype=torch.float32, device="cuda")
+    idx = torch.empty(nb, dtype=torch.int32, device="cuda")
+    c = q4._CWeight(0, n, k, wbuf.data_ptr(), wbuf.numel())
+    st = q4.lib().q4_argmax_noalloc(ctypes.byref(c), ctypes.c_void_p(x.data_ptr()), None, ctypes.c_float(0.0),
+                                    ctypes.c_int32(nb), ctypes.c_void_p(idx.data_ptr()), None, None, None)
+    torch.cuda.synchronize()
     assert st == 5        # Q4_ERR_WORKSPACE, nothing launched
