@@ -302,6 +302,7 @@ struct Smem {
     float *slots;    // per-warp tile partials [warp][SW][16][nb]
     float *rbuf;     // reductions [4][warp][kMaxNb]
     float *nx;       // row stats [8][kMaxNb]: 2 inv_rms, 3 scale, 5 output factor
+    int *wtab;       // the warps' unit ranges: ub[NW + 1], fp[NW] (tail of rbuf)
     uint8_t *ring;   // weight units [warp][DU][2 records]
 };
 
@@ -315,6 +316,7 @@ __device__ __forceinline__ Smem carve(uint8_t *smem, int nb, int Cs, int TG, int
     m.slots = m.red + (S > 1 ? (size_t)TG * kTileRows * nb : 0);
     m.rbuf = m.slots + (size_t)C::NW * SW * kTileRows * nb;
     m.nx = m.rbuf + 4 * C::NW * kMaxNb;
+    m.wtab = reinterpret_cast<int *>(m.rbuf + 3 * C::NW * kMaxNb);
     m.ring = reinterpret_cast<uint8_t *>(m.nx + 8 * kMaxNb);
     return m;
 }
@@ -768,6 +770,11 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m,
     const float z = 0.f;
     int pl = q.fp, cc = q.ub - q.fp * cs;
     const int upt = p.upt;
+    if (lane == 0) {  // this warp's range for the fold (visible after the caller's barrier)
+        m.wtab[warp] = q.ub;
+        m.wtab[C::NW + 1 + warp] = q.fp;
+        if (warp == C::NW - 1) m.wtab[C::NW] = q.ue;
+    }
     float *my_slots = m.slots + (size_t)warp * p.SW * kTileRows * nb;
 
     auto flush = [&](int pair, bool two) {
@@ -903,37 +910,34 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m,
     if (q.n_my > 0 && cc != 0) flush(pl, upt == 2 && q.t0 + 2 * pl + 1 < p.T);  // the range ended inside a unit
 }
 
+// The warps' unit ranges, from the table run_units leaves in shared memory:
+// warp w holds units [ub[w], ub[w+1]) and its first unit lies in tile unit
+// fp[w].  Held in registers by each folding thread.
+template <int NW>
+struct WarpTable {
+    int ub[NW + 1], fp[NW];
+    __device__ __forceinline__ void load(const int *tab) {
+#pragma unroll
+        for (int w = 0; w <= NW; ++w) ub[w] = tab[w];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) fp[w] = tab[NW + 1 + w];
+    }
+};
+
 // Sum of the partials of output (tile tl, row, activation row r) over the
-// warps whose unit range touched the tile, in warp order.  Warp w holds
-// units [w*U/NW, (w+1)*U/NW) (empty for some w when U < NW); the warp
-// holding unit u is floor(((u+1)*NW - 1) / U), so the walk goes from the
-// holder of the tile's first unit to the holder of the first unit past that
-// warp's range, and so on -- visiting exactly the warps that hold units.
+// warps whose unit range touched the tile, in warp order.
 template <int CLS>
-__device__ __forceinline__ float fold_one(const GemvParams &p, const Geo &q, const Smem &m, int tl, int row, int r,
-                                          int nb) {
+__device__ __forceinline__ float fold_one(const GemvParams &p, const Geo &q, const Smem &m,
+                                          const WarpTable<Cls<CLS>::NW> &wt, int tl, int row, int r, int nb) {
     constexpr int NW = Cls<CLS>::NW;
     const int pl = tl / p.upt, sub = tl - pl * p.upt;
-    const int u1 = (pl + 1) * q.cs;  // the tile's units: [pl*cs, u1)
+    const int u0 = pl * q.cs, u1 = u0 + q.cs;  // the tile's units
+    const float *base = m.slots + (size_t)row * nb + r;
     float v = 0.f;
-    if (q.U < (1 << 26)) {
-        const unsigned U = (unsigned)q.U;
-        for (unsigned u = (unsigned)(pl * q.cs); u < (unsigned)u1;) {
-            const unsigned w = ((u + 1) * NW - 1) / U;
-            const unsigned wub = w * U / NW;
-            const int ls = p.upt * (pl - (int)wub / q.cs) + sub;
-            v += m.slots[((size_t)(w * p.SW + ls) * kTileRows + row) * nb + r];
-            u = (w + 1) * U / NW;
-        }
-    } else {
-        const long long U = q.U;
-        for (long long u = (long long)pl * q.cs; u < u1;) {
-            const long long w = ((u + 1) * NW - 1) / U;
-            const long long wub = w * U / NW;
-            const int ls = p.upt * (pl - (int)(wub / q.cs)) + sub;
-            v += m.slots[((size_t)(w * p.SW + ls) * kTileRows + row) * nb + r];
-            u = (w + 1) * U / NW;
-        }
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        if (max(wt.ub[w], u0) < min(wt.ub[w + 1], u1))
+            v += base[(size_t)(w * p.SW + p.upt * (pl - wt.fp[w]) + sub) * kTileRows * nb];
     }
     return v;
 }
@@ -947,11 +951,13 @@ __device__ bool fold_tiles(const GemvParams &p, const Geo &q, const Smem &m, int
     constexpr int NTH = Cls<CLS>::NW * 32;
     const int nb = CLS == 0 ? 1 : p.nb;
     const int total = q.tiles_here * kTileRows * nb;
+    WarpTable<Cls<CLS>::NW> wt;
+    wt.load(m.wtab);
     for (int idx = tid; idx < total; idx += NTH) {
         const int tl = idx / (kTileRows * nb);
         const int rem = idx - tl * kTileRows * nb;
         const int row = rem / nb, r = rem - row * nb;
-        m.red[idx] = fold_one<CLS>(p, q, m, tl, row, r, nb) * m.nx[5 * kMaxNb + r];
+        m.red[idx] = fold_one<CLS>(p, q, m, wt, tl, row, r, nb) * m.nx[5 * kMaxNb + r];
     }
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
@@ -964,15 +970,6 @@ __device__ bool fold_tiles(const GemvParams &p, const Geo &q, const Smem &m, int
     }
     cluster.sync();
     return rank == 0;
-}
-
-// Output (tile tl, row, activation row r) of the CTA's group: from `red`
-// after a cluster fold, else folded from the warp partials here.
-template <int CLS>
-__device__ __forceinline__ float out_value(const GemvParams &p, const Geo &q, const Smem &m, int S, int tl, int row,
-                                           int r, int nb) {
-    if (S > 1) return m.red[(tl * kTileRows + row) * nb + r];
-    return fold_one<CLS>(p, q, m, tl, row, r, nb) * m.nx[5 * kMaxNb + r];
 }
 
 // Write the job's outputs: store, residual add, SwiGLU over a gate/up tile
@@ -988,13 +985,17 @@ __device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int S
         const int N = p.n[0];
         float *bvs = m.rbuf;  // [warp]
         int *bis = reinterpret_cast<int *>(m.rbuf + NW);
+        WarpTable<NW> wt;
+        if (S == 1) wt.load(m.wtab);
         for (int r = 0; r < nb; ++r) {
             float bv = -INFINITY;
             int bi = 0x7fffffff;
             for (int ri = tid; ri < q.tiles_here * kTileRows; ri += NTH) {
                 const int n = (q.t0 + ri / kTileRows) * kTileRows + (ri % kTileRows);
                 if (n >= N) continue;
-                const float v = out_value<CLS>(p, q, m, S, ri / kTileRows, ri % kTileRows, r, nb);
+                const float v = S > 1 ? m.red[ri * nb + r]
+                                      : fold_one<CLS>(p, q, m, wt, ri / kTileRows, ri % kTileRows, r, nb) *
+                                            m.nx[5 * kMaxNb + r];
                 if (p.out[0] != nullptr) p.out[0][(size_t)r * N + n] = v;
                 am_take(bv, bi, v, n);
             }
@@ -1020,6 +1021,7 @@ __device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int S
         }
         return;
     }
+    // after a cluster fold (S > 1) the values are in `red`
     for (int idx = tid; idx < total; idx += NTH) {
         const int tl = idx / (kTileRows * nb);
         const int rem = idx - tl * kTileRows * nb;
@@ -1029,13 +1031,13 @@ __device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int S
         const int n = tm * kTileRows + row;
         const int N = p.n[mi];
         if (n >= N) continue;
-        const float v = out_value<CLS>(p, q, m, S, tl, row, r, nb);
+        const float v = m.red[idx];
         if (p.epi == EPI_STORE) {
             p.out[mi][(size_t)r * N + n] = v;
         } else if (p.epi == EPI_RESIDUAL) {
             p.out[0][(size_t)r * N + n] = v + __ldcg(p.res + (size_t)r * N + n);
         } else if (mi == 0) {  // EPI_SWIGLU: gate tile tl, up tile tl + 1
-            const float u = out_value<CLS>(p, q, m, S, tl + 1, row, r, nb);
+            const float u = m.red[idx + kTileRows * nb];
             p.out[0][(size_t)r * N + n] = v / (1.0f + expf(-v)) * u;
         }
     }
@@ -1043,12 +1045,14 @@ __device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int S
 }
 
 // Single K-slice, store / residual / SwiGLU jobs: fold each output's warp
-// partials and write it at once, with no round trip through `red`.
+// partials and write it at once.
 template <int CLS>
 __device__ void fold_store(const GemvParams &p, const Geo &q, const Smem &m, int group, int tid) {
     constexpr int NTH = Cls<CLS>::NW * 32;
     const int nb = CLS == 0 ? 1 : p.nb;
     if (group >= p.groups) return;  // no tiles
+    WarpTable<Cls<CLS>::NW> wt;
+    wt.load(m.wtab);
     const int tile_vals = kTileRows * nb;
     const bool pairs = p.epi == EPI_SWIGLU;
     const int total = (pairs ? q.tiles_here / 2 : q.tiles_here) * tile_vals;
@@ -1062,13 +1066,13 @@ __device__ void fold_store(const GemvParams &p, const Geo &q, const Smem &m, int
         const int N = p.n[mi];
         if (n >= N) continue;
         const float f = m.nx[5 * kMaxNb + r];
-        const float v = fold_one<CLS>(p, q, m, tl, row, r, nb) * f;
+        const float v = fold_one<CLS>(p, q, m, wt, tl, row, r, nb) * f;
         if (p.epi == EPI_STORE) {
             p.out[mi][(size_t)r * N + n] = v;
         } else if (p.epi == EPI_RESIDUAL) {
             p.out[0][(size_t)r * N + n] = v + __ldcg(p.res + (size_t)r * N + n);
         } else {  // SwiGLU: gate tile, then its up tile
-            const float u = fold_one<CLS>(p, q, m, tl + 1, row, r, nb) * f;
+            const float u = fold_one<CLS>(p, q, m, wt, tl + 1, row, r, nb) * f;
             p.out[0][(size_t)r * N + n] = v / (1.0f + expf(-v)) * u;
         }
     }
