@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
             "q4_decode_workspace_bytes": (SZ, [I32]),
             "q4_decode_step": (I32, [P, I32, W, P, F, I32, P, P, P, P, P, P, P, P, P, SZ, P]),
             "q4_decode_check": (I32, [P, P]),
+            "q4_device_check": (I32, [P]),
             "q4_plan": (I32, [I32, I32, I32, I32, I32, I32, ctypes.POINTER(ctypes.c_int32)]),
             "q4_status_str": (ctypes.c_char_p, [I32]),
         }
@@ -381,3 +382,9 @@ def q4_decode_step(layers: DecodeLayers, Wlogits: Q4Weight, gamma_final, eps: fl
 
 def q4_decode_check(workspace):
     _check(lib().q4_decode_check(workspace.data_ptr(), _stream()), "q4_decode_check")
+
+
+def q4_device_check():
+    """Synchronise the current stream; raise if a GEMV-family kernel gave up
+    waiting for its weight copies since the last check (the flag is cleared)."""
+    _check(lib().q4_device_check(_stream()), "q4_device_check")

@@ -79,12 +79,40 @@ q4::GemvParams base_params(const q4_weight *W0, const q4_weight *W1, int mode, c
     return p;
 }
 
+// The per-call kernels' error word: set (never cleared) by a kernel whose
+// bounded wait for its weight copies gave up; q4_device_check reads and
+// clears it.  One word per device, its address resolved once per device.
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mu;
+int *g_err_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+static __device__ int q4_kernel_error_word;
+
+namespace {
+
+q4_status kernel_err_ptr(int **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return Q4_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_err_mu);
+    if (g_err_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, q4_kernel_error_word) != cudaSuccess || p == nullptr) return Q4_ERR_CUDA;
+        g_err_ptr[dev] = (int *)p;
+    }
+    *out = g_err_ptr[dev];
+    return Q4_OK;
+}
+
 q4_status run(const q4::GemvParams &p, int fmt, cudaStream_t stream, q4::Plan *plan_out = nullptr) {
     const int sms = num_sms();
     if (sms <= 0) return Q4_ERR_CUDA;
     q4::Plan plan = q4::make_plan(fmt, p.T, p.C, p.nb, p.mode == q4::MODE_PAIRS, sms);
     if (plan.smem > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;  // nb * k too large to stage
     q4::GemvParams pp = p;
+    Q4_TRY(kernel_err_ptr(&pp.err));
     pp.TG = plan.TG;
     pp.SW = plan.SW;
     pp.upt = plan.upt;
@@ -359,9 +387,10 @@ q4_status check_layer_shapes(const q4_decode_layer &L, int fmt, int hidden, int 
     return Q4_OK;
 }
 
-q4::GemvParams step_job(int G, int nb) {
+q4::GemvParams step_job(int G, int nb, int *err) {
     q4::GemvParams p;
     memset(&p, 0, sizeof(p));
+    p.err = err;
     p.nb = nb;
     p.S = 1;
     p.groups = G;
@@ -451,7 +480,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     for (int l = 0; l < n_layers; ++l) {
         const q4_decode_layer &L = layers[l];
         const float *src = l == 0 ? x_in : hid;
-        q4::GemvParams a = step_job(G, nb);  // RMSNorm + q, k, v (one input, three weights)
+        q4::GemvParams a = step_job(G, nb, sp.err);  // RMSNorm + q, k, v (one input, three weights)
         a.mode = q4::MODE_CONCAT;
         add_mat(a, L.Wq, q);
         add_mat(a, L.Wk, k);
@@ -462,7 +491,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
         a.epi = q4::EPI_STORE;
         finish_job(a, TGmax, Kmax, SWmax);
         sp.jobs[nj++] = a;
-        q4::GemvParams o = step_job(G, nb);  // o projection of the attention output + residual
+        q4::GemvParams o = step_job(G, nb, sp.err);  // o projection of the attention output + residual
         o.mode = q4::MODE_SINGLE;
         add_mat(o, L.Wo, hid);
         o.x = L.attn;
@@ -470,7 +499,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
         o.epi = q4::EPI_RESIDUAL;
         finish_job(o, TGmax, Kmax, SWmax);
         sp.jobs[nj++] = o;
-        q4::GemvParams gu = step_job(G, nb);  // RMSNorm + gate/up + SwiGLU
+        q4::GemvParams gu = step_job(G, nb, sp.err);  // RMSNorm + gate/up + SwiGLU
         gu.mode = q4::MODE_PAIRS;
         add_mat(gu, L.Wg, h);
         add_mat(gu, L.Wu, nullptr);
@@ -480,7 +509,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
         gu.epi = q4::EPI_SWIGLU;
         finish_job(gu, TGmax, Kmax, SWmax);
         sp.jobs[nj++] = gu;
-        q4::GemvParams d = step_job(G, nb);  // down projection + residual, in place
+        q4::GemvParams d = step_job(G, nb, sp.err);  // down projection + residual, in place
         d.mode = q4::MODE_SINGLE;
         add_mat(d, L.Wd, hid);
         d.x = h;
@@ -489,7 +518,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
         finish_job(d, TGmax, Kmax, SWmax);
         sp.jobs[nj++] = d;
     }
-    q4::GemvParams lg = step_job(G, nb);  // final RMSNorm + logits + per-group argmax
+    q4::GemvParams lg = step_job(G, nb, sp.err);  // final RMSNorm + logits + per-group argmax
     lg.mode = q4::MODE_SINGLE;
     add_mat(lg, *Wlogits, nullptr);
     lg.x = hid;
@@ -526,4 +555,18 @@ extern "C" q4_status q4_decode_check(const void *workspace, cudaStream_t stream)
     if (cudaMemcpy(&err, (const unsigned char *)workspace + 4, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
         return Q4_ERR_CUDA;
     return err ? Q4_ERR_CUDA : Q4_OK;
+}
+
+extern "C" q4_status q4_device_check(cudaStream_t stream) {
+    int *dev_err = nullptr;
+    Q4_TRY(kernel_err_ptr(&dev_err));
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return Q4_ERR_CUDA;
+    int err = 0;
+    if (cudaMemcpy(&err, dev_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return Q4_ERR_CUDA;
+    if (err != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(dev_err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return Q4_ERR_CUDA;
+        return Q4_ERR_CUDA;
+    }
+    return Q4_OK;
 }

@@ -53,10 +53,6 @@ namespace cg = cooperative_groups;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 template <int OFF>
-__device__ __forceinline__ void cp_async16_at(uint32_t dst, const uint8_t *src) {
-    asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%2], 16;" ::"r"(dst), "l"(src), "n"(OFF) : "memory");
-}
-template <int OFF>
 __device__ __forceinline__ uint4 lds128_at(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+%5];"
@@ -65,9 +61,48 @@ __device__ __forceinline__ uint4 lds128_at(uint32_t a) {
                  : "memory");
     return v;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// mbarrier and bulk-copy (TMA engine) primitives for the weight ring.
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// global -> shared bulk copy of `bytes` (16-byte aligned, multiple of 16),
+// completing on mbarrier `bar`; evict-first in L2 (weights stream once)
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+constexpr long long kWaitCycles = 1ll << 31;  // about a second: bound of one mbarrier wait
+// Wait for phase `parity` of mbarrier `bar` to complete; false after
+// kWaitCycles (the caller records the failure and stops).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    long long t0 = 0;
+    for (int it = 0;; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2; selp.b32 %0, 1, 0, P; }"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (it == 0) {
+            t0 = clock64();
+        } else if (clock64() - t0 > kWaitCycles) {
+            return false;
+        }
+    }
+}
 
 // D = A * B + (z0..z3), m16n8k16, f16 inputs, fp32 accumulate; the caller
 // passes four zero registers that stay live across the loop.
@@ -268,19 +303,18 @@ struct WeightStream {
         ptr0 = ptr1 = nullptr;
         start(q);
     }
-    // one record: each lane its two 16-byte nibble pieces, lanes 0..7 (0..15
-    // affine) the scale (and min) words
-    __device__ __forceinline__ static void copy_rec(uint32_t dst, const uint8_t *src, int lane) {
-        const uint8_t *s = src + lane * 16;
-        const uint32_t d = dst + lane * 16;
-        cp_async16_at<0>(d, s);
-        cp_async16_at<512>(d, s);
-        if (lane < (REC - 1024) / 16) cp_async16_at<1024>(d, s);
-    }
-    // copy the next unit into the ring stage at shared address `dst`
-    __device__ __forceinline__ void issue(uint32_t dst, int lane) {
-        copy_rec(dst, ptr0, lane);
-        if (ptr1 != nullptr) copy_rec(dst + REC, ptr1, lane);
+    // copy the next unit (one or two whole records) into the ring stage at
+    // shared address `dst` with the TMA engine, completing on mbarrier
+    // `bar`; lane 0 issues, every lane advances the (warp-uniform) state
+    __device__ __forceinline__ void issue(uint32_t dst, uint32_t bar, int lane, uint64_t policy) {
+        if (lane == 0) {
+            // the warp's reads of this stage (ordered by the caller's
+            // __syncwarp) come before the async-proxy writes that refill it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect_tx(bar, ptr1 != nullptr ? 2 * REC : REC);
+            bulk_g2s(dst, ptr0, REC, bar, policy);
+            if (ptr1 != nullptr) bulk_g2s(dst + REC, ptr1, REC, bar, policy);
+        }
         --left;
         if (++c == cs) {
             c = 0;
@@ -294,6 +328,56 @@ struct WeightStream {
     }
 };
 
+// One warp's ring of DU stages of one unit each, with an mbarrier per
+// stage.  `fill` counts units issued, `cons` units consumed; stage k holds
+// unit k mod DU and completes phase (k / DU) mod 2 of its barrier.
+template <int DU, int UREC>
+struct Ring {
+    uint32_t base, bars;  // this warp's stages and barriers (shared addresses)
+    uint32_t fill, cons;
+    bool ok;              // false once a wait gave up
+    uint64_t policy;
+    __device__ __forceinline__ void init(uint32_t b, uint32_t br, int lane) {
+        base = b;
+        bars = br;
+        fill = cons = 0;
+        ok = true;
+        policy = evict_first_policy();
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < DU; ++i) mbar_init(bars + 8 * i, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+    }
+    __device__ __forceinline__ uint32_t stage(uint32_t k) const { return base + (k % DU) * UREC; }
+    __device__ __forceinline__ uint32_t bar(uint32_t k) const { return bars + (k % DU) * 8; }
+    template <class WS>
+    __device__ __forceinline__ void push(WS &ws, int lane) {
+        if (ok && ws.left > 0) {
+            ws.issue(stage(fill), bar(fill), lane, policy);
+            ++fill;
+        }
+    }
+    // wait for the unit `cons`; the warp agrees on the outcome
+    __device__ __forceinline__ bool wait(int *err, int lane) {
+        const bool mine = ok && mbar_wait(bar(cons), (cons / DU) & 1);
+        const bool all = __all_sync(0xffffffffu, mine);
+        if (!all && ok) {
+            ok = false;
+            if (lane == 0 && err != nullptr) atomicExch(err, 2);
+        }
+        return ok;
+    }
+    // after a failed wait: wait (bounded) for the copies still in flight
+    // into this warp's stages before the CTA may exit
+    __device__ __forceinline__ void drain() {
+        if (ok) return;
+        for (uint32_t k = cons; k < fill; ++k) mbar_wait(bar(k), (k / DU) & 1);
+        cons = fill;
+    }
+};
+
 // Shared-memory regions of one CTA (sizes: engine_smem()).
 struct Smem {
     uint8_t *xs;     // activation slice, hi/lo f16 in mma B-fragment order
@@ -303,6 +387,7 @@ struct Smem {
     float *rbuf;     // reductions [4][warp][kMaxNb]
     float *nx;       // row stats [8][kMaxNb]: 2 inv_rms, 3 scale, 5 output factor
     int *wtab;       // the warps' unit ranges: ub[NW + 1], fp[NW] (tail of rbuf)
+    uint64_t *bars;  // ring barriers [warp][DU]
     uint8_t *ring;   // weight units [warp][DU][2 records]
 };
 
@@ -317,7 +402,8 @@ __device__ __forceinline__ Smem carve(uint8_t *smem, int nb, int Cs, int TG, int
     m.rbuf = m.slots + (size_t)C::NW * SW * kTileRows * nb;
     m.nx = m.rbuf + 4 * C::NW * kMaxNb;
     m.wtab = reinterpret_cast<int *>(m.rbuf + 3 * C::NW * kMaxNb);
-    m.ring = reinterpret_cast<uint8_t *>(m.nx + 8 * kMaxNb);
+    m.bars = reinterpret_cast<uint64_t *>(m.nx + 8 * kMaxNb);
+    m.ring = reinterpret_cast<uint8_t *>(m.bars + C::NW * C::DU);
     return m;
 }
 
@@ -735,9 +821,13 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v) {
 // Each tile's partial over this warp's chunks goes to one of its slots.
 // Consumes one ring stage per unit and refills it from `ws`.
 template <int FMT, int CLS>
-__device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m,
-                          WeightStream<FMT == 0 ? kRecQ4_0 : kRecAffine, Cls<CLS>::NW> &ws, uint32_t &st_a,
-                          uint32_t &fill_a, uint32_t ring_a, int warp, int lane) {
+using RingOf = Ring<Cls<CLS>::DU, 2 * (FMT == 0 ? kRecQ4_0 : kRecAffine)>;
+template <int FMT, int CLS>
+using StreamOf = WeightStream<FMT == 0 ? kRecQ4_0 : kRecAffine, Cls<CLS>::NW>;
+
+template <int FMT, int CLS>
+__device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, StreamOf<FMT, CLS> &ws,
+                          RingOf<FMT, CLS> &ring, int warp, int lane) {
     using C = Cls<CLS>;
     constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
     constexpr int UREC = 2 * REC;
@@ -746,7 +836,6 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m,
     const int nb = CLS == 0 ? 1 : p.nb;
     const int xbs = 128 * nb;
     const int cs = q.cs;
-    const uint32_t ring_end = ring_a + C::DU * UREC;
     // this lane's B-fragment slot in a block (lanes past the batch read a
     // duplicate column: their outputs are never stored)
     int boff[NT];
@@ -808,12 +897,10 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m,
     };
 
     for (int i = 0; i < q.n_my; ++i) {
-        cp_async_wait<C::DU - 2>();  // this lane's copies of the unit have landed
-        __syncwarp();                 // ... and every lane's; the previous stage is free
-        if (ws.left > 0) ws.issue(fill_a, lane);
-        cp_async_commit();
-        fill_a += UREC;
-        if (fill_a == ring_end) fill_a = ring_a;
+        __syncwarp();             // every lane is done with the previous stage: refill it
+        ring.push(ws, lane);
+        if (!ring.wait(p.err, lane)) break;  // gave up: stop (the error is recorded)
+        const uint32_t st_a = ring.stage(ring.cons);
         const bool two = upt == 2 && q.t0 + 2 * pl + 1 < p.T;
         // offset sums of the chunk's four blocks
         float G[NGR][4];
@@ -838,8 +925,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m,
                 if (FMT == 1) mw[rc] = lds128_at<1152>(ra + g * 16);
             }
         }
-        st_a += UREC;
-        if (st_a == ring_end) st_a = ring_a;
+        ++ring.cons;
         const uint8_t *xchunk = m.xs + cc * kBlocksPerChunk * xbs;
 
         auto block = [&](auto blk_c) {
@@ -907,7 +993,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m,
             ++pl;
         }
     }
-    if (q.n_my > 0 && cc != 0) flush(pl, upt == 2 && q.t0 + 2 * pl + 1 < p.T);  // the range ended inside a unit
+    if (ring.ok && q.n_my > 0 && cc != 0) flush(pl, upt == 2 && q.t0 + 2 * pl + 1 < p.T);  // ended inside a unit
 }
 
 // The warps' unit ranges, from the table run_units leaves in shared memory:
@@ -1092,25 +1178,22 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid
     const int group = blockIdx.x / S, rank = blockIdx.x - group * S;
     const int nb = CLS == 0 ? 1 : p.nb;
     const Smem m = carve<CLS>(smem, nb, p.Cs, p.TG, p.SW, S);
-    const uint32_t ring_a = smem_u32(m.ring) + warp * C::DU * 2 * REC;
+    RingOf<FMT, CLS> ring;
+    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * REC, smem_u32(m.bars) + warp * C::DU * 8, lane);
 
     // the next kernel may launch now; it waits for this one before it reads
     // what this one writes
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // weights do not depend on the previous kernel: start their copies first
     const Geo q = make_geo<NW>(p, group, rank, warp);
-    WeightStream<REC, NW> ws;
+    StreamOf<FMT, CLS> ws;
     ws.init_one(&p, q);
-    for (int s = 0; s < C::DU - 1; ++s) {
-        if (ws.left > 0) ws.issue(ring_a + s * 2 * REC, lane);
-        cp_async_commit();
-    }
+    for (int s = 0; s < C::DU - 1; ++s) ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     stage_x<FMT, CLS, 16>(p, q, m, S, tid, warp, lane);
-    uint32_t st_a = ring_a, fill_a = ring_a + (C::DU - 1) * 2 * REC;
-    run_units<FMT, CLS>(p, q, m, ws, st_a, fill_a, ring_a, warp, lane);
-    cp_async_wait<0>();
+    run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
+    ring.drain();
     __syncthreads();
     if (S == 1 && p.epi != EPI_ARGMAX) {
         fold_store<CLS>(p, q, m, group, tid);
@@ -1133,30 +1216,25 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
 }
 
 // Grid barrier number `b` (1-based).  Each CTA adds one to the arrival
-// counter; the CTA that completes the count publishes `b` in the release
-// word, which the others poll (a read-only line, away from the atomics).
-// The wait is bounded: after kBarrierSpins polls the CTA records the failure
-// in *err and the caller stops.
-__device__ __forceinline__ bool grid_barrier(unsigned *counter, unsigned *release, int *err, unsigned b) {
+// counter with a release reduction (no reply to wait for), then polls the
+// counter with acquire loads until all b * gridDim.x arrivals are in.  The
+// wait is bounded: after kBarrierSpins polls the CTA records the failure in
+// *err and the caller stops.
+__device__ __forceinline__ bool grid_barrier(unsigned *counter, int *err, unsigned b) {
     __syncthreads();
     __shared__ int fail;
     if (threadIdx.x == 0) {
         fail = 0;
-        __threadfence();
-        const unsigned prev = atomicAdd(counter, 1u);
-        if (prev + 1 == b * gridDim.x) {
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(release), "r"(b) : "memory");
-        } else {
-            long long it = 0;
-            while (ld_acquire_u32(release) < b) {
-                if (++it > kBarrierSpins) {
-                    atomicExch(err, 1);
-                    fail = 1;
-                    break;
-                }
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
+        const unsigned target = b * gridDim.x;
+        long long it = 0;
+        while (ld_acquire_u32(counter) < target) {
+            if (++it > kBarrierSpins) {
+                atomicExch(err, 1);
+                fail = 1;
+                break;
             }
         }
-        __threadfence();
     }
     __syncthreads();
     return fail == 0;
@@ -1173,24 +1251,24 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
     const int nb = CLS == 0 ? 1 : sp.nb;
     const int cs_max = (sp.Kmax + kChunkK - 1) / kChunkK;  // as the host sized it
     const Smem m = carve<CLS>(smem, nb, cs_max, sp.TGmax, sp.SWmax, 1);
-    const uint32_t ring_a = smem_u32(m.ring) + warp * C::DU * 2 * REC;
+    RingOf<FMT, CLS> ring;
+    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * REC, smem_u32(m.bars) + warp * C::DU * 8, lane);
 
-    WeightStream<REC, NW> ws;
+    StreamOf<FMT, CLS> ws;
     ws.init(sp.jobs, sp.njobs, group, 0, warp);
-    for (int s = 0; s < C::DU - 1; ++s) {
-        if (ws.left > 0) ws.issue(ring_a + s * 2 * REC, lane);
-        cp_async_commit();
-    }
+    for (int s = 0; s < C::DU - 1; ++s) ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    uint32_t st_a = ring_a, fill_a = ring_a + (C::DU - 1) * 2 * REC;
     for (int j = 0; j < sp.njobs; ++j) {
         const GemvParams &p = sp.jobs[j];
-        if (j > 0 && !grid_barrier(sp.counter, sp.release, sp.err, (unsigned)j)) return;
+        if (j > 0 && !grid_barrier(sp.counter, sp.err, (unsigned)j)) {
+            ring.drain();
+            return;
+        }
         const Geo q = make_geo<NW>(p, group, 0, warp);
         if (q.tiles_here == 0) continue;  // no work in this job (CTA-uniform)
         stage_x<FMT, CLS, 8>(p, q, m, 1, tid, warp, lane);
-        run_units<FMT, CLS>(p, q, m, ws, st_a, fill_a, ring_a, warp, lane);
+        run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
         __syncthreads();
         if (p.epi != EPI_ARGMAX) {
             fold_store<CLS>(p, q, m, group, tid);
@@ -1198,9 +1276,9 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
             epilogue<CLS>(p, q, m, 1, group, tid, warp, lane);
         }
     }
-    cp_async_wait<0>();
+    ring.drain();
     // the last job is the logits argmax: fold the groups' pairs in order
-    if (!grid_barrier(sp.counter, sp.release, sp.err, (unsigned)sp.njobs)) return;
+    if (!grid_barrier(sp.counter, sp.err, (unsigned)sp.njobs)) return;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const GemvParams &pl = sp.jobs[sp.njobs - 1];
     if (group == 0 && tid < 32) {

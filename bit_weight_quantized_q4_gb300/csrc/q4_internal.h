@@ -100,6 +100,7 @@ struct GemvParams {
     const float *res;            // residual [nb][n0]
     float *am_val;               // argmax partials [nb][groups]
     int *am_idx;
+    int *err;                    // set nonzero if a kernel wait gave up
 };
 
 // The persistent decode-step kernel runs these jobs in order, one CTA per SM.
@@ -144,7 +145,7 @@ inline size_t engine_smem(int fmt, int nb, int TG, int Cs, int SW, int S) {
     const size_t gs = (size_t)16 * cls_gsw(c) * Cs;
     const size_t red = S > 1 ? (size_t)64 * TG * nb : 0;
     const size_t slots = (size_t)64 * NW * SW * nb;
-    const size_t misc = (size_t)16 * NW * kMaxNb + 32 * kMaxNb;
+    const size_t misc = (size_t)16 * NW * kMaxNb + 32 * kMaxNb + 8 * NW * cls_depth(c);  // + ring barriers
     const size_t ring = NW * cls_depth(c) * 2 * rec_bytes(fmt);
     return xs + gs + red + slots + misc + ring;
 }

@@ -206,8 +206,21 @@ q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_layers, const 
                          size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises `stream` and reports whether the last q4_decode_step on this
- * workspace completed all its grid barriers (Q4_OK) or gave up (Q4_ERR_CUDA). */
+ * workspace completed all its grid barriers and weight copies (Q4_OK) or
+ * gave up on one (Q4_ERR_CUDA). */
 q4_status q4_decode_check(const void *workspace, cudaStream_t stream);
+
+/* Synchronises `stream` and reports whether any GEMV-family kernel of this
+ * library on the current device (q4_gemv, q4_nrm_gemv, q4_dual_gemv,
+ * q4_gus_nrm, q4_res_gemv, q4_argmax, q4_argmax_noalloc) gave up waiting for
+ * its weight copies since the last check (Q4_ERR_CUDA; the flag is then
+ * cleared) or not (Q4_OK).  Each kernel bounds every such wait (about a
+ * second); a kernel that gives up records it in a per-device word of the
+ * library, stops streaming, waits (bounded) for its copies in flight and
+ * returns, leaving its outputs undefined.  The word's address is resolved
+ * on the first library call on a device; make that call before any stream
+ * capture.  Library-specific: the pages have no counterpart. */
+q4_status q4_device_check(cudaStream_t stream);
 
 /* Allocation-free variant of q4_argmax.  The pages have no counterpart: this
  * exists for callers that cannot allocate device memory where they need the

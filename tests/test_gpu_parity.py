@@ -237,3 +237,13 @@ def test_large_dynamic_range(q4):
     y = q4.q4_gemv(dev_weight(H), torch.from_numpy(x).cuda())
     y_ref, S = oracle.q4_gemv(host_weight(H), x)
     check(to_np(y), y_ref, S, what="dynamic range")
+
+
+def test_device_check_clear_after_calls(q4):
+    # every kernel above finished its bounded weight-copy waits
+    rng = np.random.default_rng(47)
+    H = wl.draw_q4_0(rng, 4096, 2048)
+    x = torch.from_numpy(wl.draw_x(rng, 2, 2048)).cuda()
+    for _ in range(3):
+        q4.q4_gemv(dev_weight(H), x)
+    q4.q4_device_check()
