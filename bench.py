@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--no-kernels", action="store_true", help="skip the per-shape kernel table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--gemv", metavar="FMT:N:K:NB", default=None,
+                    help="time one q4_gemv shape only (fmt q4_0 or affine; for profiling), then exit")
     return ap.parse_args(argv)
 
 
@@ -377,6 +379,11 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
         copies = max(2, -(-3 * l2_bytes // W0.nbytes))
         host = W0.tensor.cpu().numpy()
         Ws = [W0] + [q4.Q4Weight(W0.fmt, n, k, host, device) for _ in range(copies - 1)]
+        # context: a vendor reduction (torch.amax) reading the same packed bytes, same rotation
+        t_ref = bench_calls(Ws, lambda W: torch.amax(W.tensor))
+        out["%s_n%d_k%d_vendor_read" % (fmt, n, k)] = {
+            "us": round(t_ref * 1e6, 3), "packed_gbs": round(W0.nbytes / t_ref / 1e9, 1),
+            "what": "torch.amax over the packed weight bytes: a library kernel reading the same bytes"}
         for nb in ((1, 2, 4, 8, 16) if fmt == "affine" else (1,)):
             x = torch.from_numpy(wl.draw_x(rng, nb, k)).to(device)
             y = torch.empty((nb, n), dtype=torch.float32, device=device)
@@ -387,6 +394,41 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
         del Ws
         torch.cuda.empty_cache()
     return out
+
+
+def run_one_gemv(args) -> dict:
+    """One GEMV shape, `warmup` untimed then `steps` timed calls on one weight
+    (seeded synthetic, drawn like the kernel table's); for ncu captures."""
+    import numpy as np
+    import torch
+
+    import bit_weight_quantized_q4_gb300 as q4
+    import q4_workloads as wl
+    fmt, n, k, nb = args.gemv.split(":")
+    n, k, nb = int(n), int(k), int(nb)
+    q4.build()
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(3)
+    if fmt == "q4_0":
+        H = wl.draw_q4_0(rng, n, k)
+        W = q4.Q4Weight.from_q4_0(H.blocks, n, k, dev)
+    else:
+        H = wl.draw_affine(rng, n, k)
+        W = q4.Q4Weight.from_affine(H.nib, H.s, H.m, n, k, dev)
+    x = torch.from_numpy(wl.draw_x(rng, nb, k)).to(dev)
+    y = torch.empty((nb, n), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        q4.q4_gemv(W, x, out=y)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        q4.q4_gemv(W, x, out=y)
+    e1.record()
+    torch.cuda.synchronize()
+    q4.q4_device_check()
+    return {"gemv": args.gemv, "calls": args.steps, "us_per_call_warm_l2": round(e0.elapsed_time(e1) * 1e3 / args.steps, 3),
+            "note": "one weight reused: warm L2 for matrices under 129 MB; the kernel table times cold weights"}
 
 
 def run_ours(args, rank, world, local):
@@ -555,7 +597,9 @@ def run_reference(args, rank, world):
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
-    if args.impl == "reference":
+    if args.gemv:
+        line = run_one_gemv(args) if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:
         line = run_ours(args, rank, world, local)

@@ -536,7 +536,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     // every job runs on all G CTAs; a job's groups may be fewer (clipped to
     // its tile units), and the CTAs beyond them skip that job's work
 
-    const size_t smem = q4::step_smem_bytes(fmt, nb, TGmax, Kmax, SWmax);
+    const size_t smem = q4::step_smem_bytes(fmt, nb, TGmax, Kmax, SWmax, nj);
     if (smem > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;
     const int occ = fmt == Q4_FMT_Q4_0 ? q4::step_occupancy_q4_0(nb, smem) : q4::step_occupancy_affine(nb, smem);
     if (occ < 1) return Q4_ERR_UNSUPPORTED;

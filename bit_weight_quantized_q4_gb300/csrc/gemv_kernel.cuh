@@ -201,7 +201,8 @@ struct Cls {
     static constexpr bool HLN = CLS <= 1;    // hi / lo of an activation row in two n columns
     static constexpr int NT = CLS == 3 ? 2 : 1;  // 8-column n-tiles
     static constexpr int NW = cls_warps(CLS);
-    static constexpr int DU = cls_depth(CLS);
+    static constexpr int DU = cls_depth(CLS);     // ring stages per warp
+    static constexpr int SU = cls_stage(CLS);     // pair units per stage: stages of 2*SU records
     static constexpr int GSW = cls_gsw(CLS);
     static constexpr int NGR = HLN ? 1 : 2 * NT;    // group-sum rows one lane uses
     static constexpr int NACC = HLN ? 2 : 4 * NT;   // accumulators per record and lane
@@ -249,6 +250,17 @@ __device__ __forceinline__ const uint8_t *tile_base(const GemvParams &p, int t) 
     return p.w[m] + (size_t)tm * p.C * REC;
 }
 
+// Units in the next ring stage: at most SU tile-pair units (2*SU single-tile
+// units), never past the end of the current pair's K-slice (`to_pair_end`
+// units) or the warp's range (`left`).  Producer and consumer both use it.
+template <int SU>
+__device__ __forceinline__ int stage_units(int upt, int to_pair_end, int left) {
+    int n = upt == 2 ? SU : 2 * SU;
+    if (n > to_pair_end) n = to_pair_end;
+    if (n > left) n = left;
+    return n;
+}
+
 // The weight units a warp streams, in order, across the jobs of a launch:
 // each job's [ub, ue) range of this warp, job after job.  The load side runs
 // up to DU-1 units ahead of the compute side, across job boundaries.
@@ -256,8 +268,8 @@ template <int REC, int NW>
 struct WeightStream {
     const GemvParams *jobs;
     int njobs, group, rank, warp;
-    int job, c0, cs, t0, pl, c, left;
-    const uint8_t *ptr0, *ptr1;  // the next unit's records (ptr1 null: the pair has one tile)
+    int job, c0, cs, t0, pl, c, left, upt;
+    const uint8_t *ptr0, *ptr1;  // the next unit's records (ptr1 null: the unit has one tile)
 
     __device__ __forceinline__ void pair_ptrs() {
         const GemvParams &p = jobs[job];
@@ -268,6 +280,7 @@ struct WeightStream {
     }
     __device__ __forceinline__ void start(const Geo &q) {
         if (q.n_my > 0) {
+            upt = jobs[job].upt;
             t0 = q.t0;
             c0 = q.c0;
             cs = q.cs;
@@ -303,35 +316,41 @@ struct WeightStream {
         ptr0 = ptr1 = nullptr;
         start(q);
     }
-    // copy the next unit (one or two whole records) into the ring stage at
-    // shared address `dst` with the TMA engine, completing on mbarrier
-    // `bar`; lane 0 issues, every lane advances the (warp-uniform) state
+    // copy the next stage -- up to SU units of the current tile pair (2*SU
+    // for single-tile units), never past the pair or the warp's range -- into
+    // the ring stage at shared address `dst` with the TMA engine, completing
+    // on mbarrier `bar`: one copy of n consecutive records per tile (the
+    // second tile's records at dst + SU*REC).  Lane 0 issues; every lane
+    // advances the (warp-uniform) state.
+    template <int SU>
     __device__ __forceinline__ void issue(uint32_t dst, uint32_t bar, int lane, uint64_t policy) {
+        const int n = stage_units<SU>(upt, cs - c, left);
         if (lane == 0) {
             // the warp's reads of this stage (ordered by the caller's
             // __syncwarp) come before the async-proxy writes that refill it
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_expect_tx(bar, ptr1 != nullptr ? 2 * REC : REC);
-            bulk_g2s(dst, ptr0, REC, bar, policy);
-            if (ptr1 != nullptr) bulk_g2s(dst + REC, ptr1, REC, bar, policy);
+            mbar_expect_tx(bar, (ptr1 != nullptr ? 2 : 1) * n * REC);
+            bulk_g2s(dst, ptr0, n * REC, bar, policy);
+            if (ptr1 != nullptr) bulk_g2s(dst + SU * REC, ptr1, n * REC, bar, policy);
         }
-        --left;
-        if (++c == cs) {
+        left -= n;
+        c += n;
+        if (c == cs) {
             c = 0;
             ++pl;
             if (left > 0) pair_ptrs();
         } else {
-            ptr0 += REC;
-            if (ptr1 != nullptr) ptr1 += REC;
+            ptr0 += (size_t)n * REC;
+            if (ptr1 != nullptr) ptr1 += (size_t)n * REC;
         }
         if (left == 0) next_job();
     }
 };
 
-// One warp's ring of DU stages of one unit each, with an mbarrier per
-// stage.  `fill` counts units issued, `cons` units consumed; stage k holds
-// unit k mod DU and completes phase (k / DU) mod 2 of its barrier.
-template <int DU, int UREC>
+// One warp's ring of DU stages of SREC bytes, with an mbarrier per stage.
+// `fill` counts stages issued, `cons` stages consumed; stage k lives in
+// slot k mod DU and completes phase (k / DU) mod 2 of its barrier.
+template <int DU, int SU, int SREC>
 struct Ring {
     uint32_t base, bars;  // this warp's stages and barriers (shared addresses)
     uint32_t fill, cons;
@@ -350,12 +369,12 @@ struct Ring {
         }
         __syncwarp();
     }
-    __device__ __forceinline__ uint32_t stage(uint32_t k) const { return base + (k % DU) * UREC; }
+    __device__ __forceinline__ uint32_t stage(uint32_t k) const { return base + (k % DU) * SREC; }
     __device__ __forceinline__ uint32_t bar(uint32_t k) const { return bars + (k % DU) * 8; }
     template <class WS>
     __device__ __forceinline__ void push(WS &ws, int lane) {
         if (ok && ws.left > 0) {
-            ws.issue(stage(fill), bar(fill), lane, policy);
+            ws.template issue<SU>(stage(fill), bar(fill), lane, policy);
             ++fill;
         }
     }
@@ -388,7 +407,7 @@ struct Smem {
     float *nx;       // row stats [8][kMaxNb]: 2 inv_rms, 3 scale, 5 output factor
     int *wtab;       // the warps' unit ranges: ub[NW + 1], fp[NW] (tail of rbuf)
     uint64_t *bars;  // ring barriers [warp][DU]
-    uint8_t *ring;   // weight units [warp][DU][2 records]
+    uint8_t *ring;   // weight stages [warp][DU][2*SU records]
 };
 
 template <int CLS>
@@ -821,7 +840,7 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v) {
 // Each tile's partial over this warp's chunks goes to one of its slots.
 // Consumes one ring stage per unit and refills it from `ws`.
 template <int FMT, int CLS>
-using RingOf = Ring<Cls<CLS>::DU, 2 * (FMT == 0 ? kRecQ4_0 : kRecAffine)>;
+using RingOf = Ring<Cls<CLS>::DU, Cls<CLS>::SU, 2 * Cls<CLS>::SU * (FMT == 0 ? kRecQ4_0 : kRecAffine)>;
 template <int FMT, int CLS>
 using StreamOf = WeightStream<FMT == 0 ? kRecQ4_0 : kRecAffine, Cls<CLS>::NW>;
 
@@ -896,11 +915,17 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
         }
     };
 
-    for (int i = 0; i < q.n_my; ++i) {
+    for (int i = 0; i < q.n_my;) {
+        const int n_st = stage_units<C::SU>(upt, cs - cc, q.n_my - i);  // units of this stage
         __syncwarp();             // every lane is done with the previous stage: refill it
         ring.push(ws, lane);
         if (!ring.wait(p.err, lane)) break;  // gave up: stop (the error is recorded)
-        const uint32_t st_a = ring.stage(ring.cons);
+        const uint32_t st_base = ring.stage(ring.cons);
+        ++ring.cons;
+        i += n_st;
+      for (int su = 0; su < n_st; ++su) {
+        // unit su of the stage: its record(s) at st_base + su*REC (and + SU*REC)
+        const uint32_t st_a = st_base + su * REC;
         const bool two = upt == 2 && q.t0 + 2 * pl + 1 < p.T;
         // offset sums of the chunk's four blocks
         float G[NGR][4];
@@ -918,14 +943,13 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
         for (int rc = 0; rc < 2; ++rc) {
             w0[rc] = w1[rc] = sw[rc] = mw[rc] = make_uint4(0u, 0u, 0u, 0u);
             if (rc == 0 || two) {
-                const uint32_t ra = st_a + rc * REC;
+                const uint32_t ra = st_a + rc * C::SU * REC;
                 w0[rc] = lds128_at<0>(ra + lane * 16);
                 w1[rc] = lds128_at<512>(ra + lane * 16);
                 sw[rc] = lds128_at<1024>(ra + g * 16);
                 if (FMT == 1) mw[rc] = lds128_at<1152>(ra + g * 16);
             }
         }
-        ++ring.cons;
         const uint8_t *xchunk = m.xs + cc * kBlocksPerChunk * xbs;
 
         auto block = [&](auto blk_c) {
@@ -992,6 +1016,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             cc = 0;
             ++pl;
         }
+      }
     }
     if (ring.ok && q.n_my > 0 && cc != 0) flush(pl, upt == 2 && q.t0 + 2 * pl + 1 < p.T);  // ended inside a unit
 }
@@ -1165,21 +1190,35 @@ __device__ void fold_store(const GemvParams &p, const Geo &q, const Smem &m, int
     __syncthreads();
 }
 
+// Copy a job's parameter block into shared memory with one round of
+// independent 8-byte loads (a first touch of the constant bank costs a
+// miss per line; this takes them all at once).  Visible after a barrier.
+static_assert(sizeof(GemvParams) % 8 == 0, "parameter block must be whole 8-byte words");
+constexpr int kParamWords = (int)(sizeof(GemvParams) / 8);
+__device__ __forceinline__ void copy_params(GemvParams *dst, const GemvParams *src, int tid) {
+    if (tid < kParamWords)
+        reinterpret_cast<unsigned long long *>(dst)[tid] = reinterpret_cast<const unsigned long long *>(src)[tid];
+}
+
 // ---------------------------------------------------------------------------
 // Per-call kernel: one job, one group of tile pairs per cluster.
 template <int FMT, int CLS>
-__global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid_constant__ GemvParams p) {
+__global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid_constant__ GemvParams prm) {
     using C = Cls<CLS>;
     constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
     constexpr int NW = C::NW;
     extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ GemvParams ps;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    copy_params(&ps, &prm, tid);
+    __syncthreads();
+    const GemvParams &p = ps;
     const int S = p.S;
     const int group = blockIdx.x / S, rank = blockIdx.x - group * S;
     const int nb = CLS == 0 ? 1 : p.nb;
     const Smem m = carve<CLS>(smem, nb, p.Cs, p.TG, p.SW, S);
     RingOf<FMT, CLS> ring;
-    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * REC, smem_u32(m.bars) + warp * C::DU * 8, lane);
+    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * C::SU * REC, smem_u32(m.bars) + warp * C::DU * 8, lane);
 
     // the next kernel may launch now; it waits for this one before it reads
     // what this one writes
@@ -1252,15 +1291,21 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
     const int cs_max = (sp.Kmax + kChunkK - 1) / kChunkK;  // as the host sized it
     const Smem m = carve<CLS>(smem, nb, cs_max, sp.TGmax, sp.SWmax, 1);
     RingOf<FMT, CLS> ring;
-    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * REC, smem_u32(m.bars) + warp * C::DU * 8, lane);
+    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * C::SU * REC, smem_u32(m.bars) + warp * C::DU * 8, lane);
 
+    // every job's parameter block in shared memory (after the engine's
+    // regions), copied once: the weight stream and the job loop read them there
+    GemvParams *jobs = reinterpret_cast<GemvParams *>(m.ring + (size_t)NW * C::DU * 2 * C::SU * REC);
+    for (int i = tid; i < sp.njobs * kParamWords; i += NW * 32)
+        reinterpret_cast<unsigned long long *>(jobs)[i] = reinterpret_cast<const unsigned long long *>(sp.jobs)[i];
+    __syncthreads();
     StreamOf<FMT, CLS> ws;
-    ws.init(sp.jobs, sp.njobs, group, 0, warp);
+    ws.init(jobs, sp.njobs, group, 0, warp);
     for (int s = 0; s < C::DU - 1; ++s) ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     for (int j = 0; j < sp.njobs; ++j) {
-        const GemvParams &p = sp.jobs[j];
+        const GemvParams &p = jobs[j];
         if (j > 0 && !grid_barrier(sp.counter, sp.err, (unsigned)j)) {
             ring.drain();
             return;
@@ -1280,7 +1325,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
     // the last job is the logits argmax: fold the groups' pairs in order
     if (!grid_barrier(sp.counter, sp.err, (unsigned)sp.njobs)) return;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const GemvParams &pl = sp.jobs[sp.njobs - 1];
+    const GemvParams &pl = jobs[sp.njobs - 1];
     if (group == 0 && tid < 32) {
         for (int r = 0; r < nb; ++r) {
             float bv = -INFINITY;

@@ -68,7 +68,8 @@ constexpr int kMaxMats = 3;                   // matrices of one job (q, k, v sh
 //   class 3 (nb = 9..16): as class 2 over two 8-column n-tiles -- eight.
 Q4_HD constexpr int cls_of(int nb) { return nb <= 1 ? 0 : nb <= 4 ? 1 : nb <= 8 ? 2 : 3; }
 Q4_HD constexpr int cls_warps(int c) { return c == 3 ? 8 : 16; }     // warps per CTA
-Q4_HD constexpr int cls_depth(int c) { return c == 0 ? 4 : 3; }      // ring stages (units) per warp
+Q4_HD constexpr int cls_depth(int c) { return c == 0 || c == 3 ? 2 : 3; }  // ring stages per warp
+Q4_HD constexpr int cls_stage(int c) { return c == 0 || c == 3 ? 2 : 1; }  // pair units per stage (2x as many single-tile units)
 Q4_HD constexpr int cls_gsw(int c) { return c <= 1 ? 4 : c == 2 ? 8 : 16; }  // group-sum rows per chunk
 
 // A unit of work is one 128-column chunk of upt consecutive 16-row tiles
@@ -146,7 +147,7 @@ inline size_t engine_smem(int fmt, int nb, int TG, int Cs, int SW, int S) {
     const size_t red = S > 1 ? (size_t)64 * TG * nb : 0;
     const size_t slots = (size_t)64 * NW * SW * nb;
     const size_t misc = (size_t)16 * NW * kMaxNb + 32 * kMaxNb + 8 * NW * cls_depth(c);  // + ring barriers
-    const size_t ring = NW * cls_depth(c) * 2 * rec_bytes(fmt);
+    const size_t ring = NW * cls_depth(c) * 2 * cls_stage(c) * rec_bytes(fmt);
     return xs + gs + red + slots + misc + ring;
 }
 
@@ -239,10 +240,11 @@ inline Plan make_plan(int fmt, int T, int C, int nb, bool pairs, int num_sms) {
     return best;
 }
 
-// Dynamic shared memory of one decode-step CTA.
-inline size_t step_smem_bytes(int fmt, int nb, int TGmax, int Kmax, int SWmax) {
+// Dynamic shared memory of one decode-step CTA: the engine's regions plus a
+// copy of every job's parameter block.
+inline size_t step_smem_bytes(int fmt, int nb, int TGmax, int Kmax, int SWmax, int njobs) {
     const int Cs = (Kmax + kChunkK - 1) / kChunkK;
-    return engine_smem(fmt, nb, TGmax, Cs, SWmax, 1);
+    return engine_smem(fmt, nb, TGmax, Cs, SWmax, 1) + (size_t)njobs * sizeof(GemvParams);
 }
 
 // Launchers, one per kernel instantiation family (defined in the .cu files).
