@@ -471,59 +471,12 @@ __device__ __forceinline__ void put_pair(uint8_t *xs, int xbs, int r, int kl, fl
 
 __device__ __forceinline__ int gs_idx(int b, int row, int GSW) { return ((b >> 2) * GSW + row) * 4 + (b & 3); }
 
-// Q4_0 offset sums: for every block of the slice, the tensor-core product of
-// the staged activations with an all-8 weight block -- the exact value a
-// block of eights produces in the main loop, so that it cancels to zero.
-template <int CLS>
-__device__ void eights_pass(const Geo &q, const Smem &m, int nb, int warp, int lane) {
-    using C = Cls<CLS>;
-    const int g = lane >> 2, t = lane & 3;
-    const int xbs = 128 * nb;
-    const float z = 0.f;
-    const int nblk = q.cs * kBlocksPerChunk;
-    auto one = [&](int b) {
-        if (C::HLN) {
-            const uint4 bb = *reinterpret_cast<const uint4 *>(m.xs + b * xbs + ((g % (2 * nb)) * 4 + t) * 16);
-            float d[4];
-            mma16816_c(d, kEightLo, kEightLo, kEightHi, kEightHi, bb.x, bb.y, z, z, z, z);
-            mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, bb.z, bb.w);
-            if (g == 0) m.gs[gs_idx(b, t, C::GSW)] = d[0] + d[1];
-        } else {
-#pragma unroll
-            for (int nt = 0; nt < C::NT; ++nt) {
-                const int cnt = min(8, nb - 8 * nt);
-                const uint8_t *ba = m.xs + b * xbs + nt * 1024 + ((g % cnt) * 4 + t) * 32;
-                const uint4 B0 = *reinterpret_cast<const uint4 *>(ba);
-                const uint4 B1 = *reinterpret_cast<const uint4 *>(ba + 16);
-                float d[4];
-                mma16816_c(d, kEightLo, kEightLo, kEightHi, kEightHi, B0.x, B0.y, z, z, z, z);
-                mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, B0.z, B0.w);
-                mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, B1.x, B1.y);
-                mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, B1.z, B1.w);
-                if (g == 0) {
-                    m.gs[gs_idx(b, 8 * nt + 2 * t, C::GSW)] = d[0];
-                    m.gs[gs_idx(b, 8 * nt + 2 * t + 1, C::GSW)] = d[1];
-                }
-            }
-        }
-    };
-    // four independent blocks per step keep several products in flight
-    int b = warp;
-    for (; b + 3 * C::NW < nblk; b += 4 * C::NW) {
-        one(b);
-        one(b + C::NW);
-        one(b + 2 * C::NW);
-        one(b + 3 * C::NW);
-    }
-    for (; b < nblk; b += C::NW) one(b);
-}
-
 // Stage this CTA's activation slice of job p: per row, scale by a power of
 // two chosen from its largest magnitude (after RMSNorm when gamma is given)
-// and split into f16 hi + lo in B-fragment order (xs_off); then the block
-// offset sums: Q4_0 by eights_pass, affine as fp32 sums of the scaled
-// values (pairs, then a butterfly over 16 lanes -- the order of
-// q4_group_sums) or from the caller's group sums.  Activation loads bypass
+// and split into f16 hi + lo in B-fragment order (xs_off); then, for the
+// affine format, the block sums: fp32 sums of the scaled values (pairs, then
+// a butterfly over 16 lanes -- the order of q4_group_sums) or the caller's
+// group sums.  (Q4_0's offset products are formed in run_units.)  Activation loads bypass
 // L1 (.cg): in the persistent kernel another SM may have rewritten them
 // since this SM last read them.
 // SP: column pairs per thread a multi-row slice may stage through registers
@@ -822,10 +775,6 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
             }
         }
     }
-    if (FMT == 0) {
-        __syncthreads();
-        eights_pass<CLS>(q, m, nb, warp, lane);
-    }
     __syncthreads();
 }
 
@@ -927,15 +876,18 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
         // unit su of the stage: its record(s) at st_base + su*REC (and + SU*REC)
         const uint32_t st_a = st_base + su * REC;
         const bool two = upt == 2 && q.t0 + 2 * pl + 1 < p.T;
-        // offset sums of the chunk's four blocks
+        // affine: the staged group sums of the chunk's four blocks (Q4_0 forms
+        // its offset products per block below)
         float G[NGR][4];
+        if (FMT == 1) {
 #pragma unroll
-        for (int j = 0; j < NGR; ++j) {
-            const float4 gv = *reinterpret_cast<const float4 *>(m.gs + (cc * C::GSW + grow[j]) * 4);
-            G[j][0] = gv.x;
-            G[j][1] = gv.y;
-            G[j][2] = gv.z;
-            G[j][3] = gv.w;
+            for (int j = 0; j < NGR; ++j) {
+                const float4 gv = *reinterpret_cast<const float4 *>(m.gs + (cc * C::GSW + grow[j]) * 4);
+                G[j][0] = gv.x;
+                G[j][1] = gv.y;
+                G[j][2] = gv.z;
+                G[j][3] = gv.w;
+            }
         }
         // the records' words: nibbles of rows g and g+8, scales (and mins)
         uint4 w0[2], w1[2], sw[2], mw[2];
@@ -960,6 +912,27 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             for (int nt = 0; nt < NT; ++nt) {
                 B[nt][0] = *reinterpret_cast<const uint4 *>(xa + boff[nt]);
                 if (!C::HLN) B[nt][1] = *reinterpret_cast<const uint4 *>(xa + boff[nt] + 16);
+            }
+            if (FMT == 0) {
+                // the block's offset product: the same tensor-core chain as the
+                // weights' below, with every nibble 8 (exactly what a block of
+                // eights gives, so such a block cancels to zero)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float e[4];
+                    if (C::HLN) {
+                        mma16816_c(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][0].x, B[nt][0].y, z, z, z, z);
+                        mma16816(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][0].z, B[nt][0].w);
+                        G[0][blk] = e[0] + e[1];
+                    } else {
+                        mma16816_c(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][0].x, B[nt][0].y, z, z, z, z);
+                        mma16816(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][0].z, B[nt][0].w);
+                        mma16816(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][1].x, B[nt][1].y);
+                        mma16816(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][1].z, B[nt][1].w);
+                        G[2 * nt][blk] = e[0];
+                        G[2 * nt + 1][blk] = e[1];
+                    }
+                }
             }
 #pragma unroll
             for (int rc = 0; rc < 2; ++rc) {
