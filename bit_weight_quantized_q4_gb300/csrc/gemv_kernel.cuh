@@ -495,17 +495,22 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
         const int npass = (Ks / 2 + NTH - 1) / NTH;  // pairs per thread actually used
         float2 xv[RP], gv[RP];
         float ss = 0.f, mx = 0.f;
+        // every load first (guarded, not a loop exit, so that they can all
+        // be in flight together), then the statistics
 #pragma unroll
         for (int qq = 0; qq < RP; ++qq) {
-            if (qq >= npass) break;
             float2 v = make_float2(0.f, 0.f), gm = make_float2(1.f, 1.f);
             const int k = kb + 2 * (tid + qq * NTH);
-            if (k < ke) {
+            if (qq < npass && k < ke) {
                 v = __ldcg(reinterpret_cast<const float2 *>(p.x + k));
                 if (norm) gm = *reinterpret_cast<const float2 *>(p.gamma + k);
             }
             xv[qq] = v;
             gv[qq] = gm;
+        }
+#pragma unroll
+        for (int qq = 0; qq < RP; ++qq) {
+            const float2 v = xv[qq], gm = gv[qq];  // zero beyond npass
             ss = fmaf(v.x, v.x, ss);
             ss = fmaf(v.y, v.y, ss);
             mx = fmaxf(mx, fmaxf(fabsf(norm ? v.x * gm.x : v.x), fabsf(norm ? v.y * gm.y : v.y)));
@@ -575,11 +580,10 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
         const int npass = (npairs + NTH - 1) / NTH;
         float2 xv[SP], gv[SP];
 #pragma unroll
-        for (int j = 0; j < SP; ++j) {
-            if (j >= npass) break;
+        for (int j = 0; j < SP; ++j) {  // guarded, not a loop exit: the loads overlap
             const int i = tid + j * NTH;
             float2 v = make_float2(0.f, 0.f), gm = make_float2(1.f, 1.f);
-            if (i < npairs) {
+            if (j < npass && i < npairs) {
                 const int r = i / half_ks, k = kb + 2 * (i - r * half_ks);
                 if (k < ke) {
                     v = __ldcg(reinterpret_cast<const float2 *>(p.x + (size_t)r * p.K + k));
@@ -589,42 +593,52 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
             xv[j] = v;
             gv[j] = gm;
         }
-        // per (pass, warp) partials: entry e = j*NW + warp covers pairs [32e, 32e+32)
-        float *part = m.rbuf;  // [2][npass * NW]
+        // per (row, warp) partials: a warp's passes j cover pairs
+        // [j*NTH + 32*warp, +32), all in one row, and consecutive passes stay in
+        // a row until it ends -- accumulate in registers, reduce once per row.
+        // Entries of warps that cover no pair of a row stay zero (neutral for
+        // both the sum and the max).
+        float *part = m.rbuf;  // [2][nb][NW]
+        for (int e = tid; e < 2 * nb * NW; e += NTH) part[e] = 0.f;
+        __syncthreads();  // (the loads above are still in flight)
+        {
+            float ss = 0.f, mx = 0.f;
 #pragma unroll
-        for (int j = 0; j < SP; ++j) {
-            if (j >= npass) break;
-            const float2 v = xv[j], gm = gv[j];
-            float ss = fmaf(v.y, v.y, v.x * v.x);
-            float mx = fmaxf(fabsf(norm ? v.x * gm.x : v.x), fabsf(norm ? v.y * gm.y : v.y));
+            for (int j = 0; j < SP; ++j) {
+                if (j >= npass) break;
+                const int i0 = j * NTH + warp * 32;  // this warp's first pair of pass j
+                const float2 v = xv[j], gm = gv[j];
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                mx = fmaxf(mx, fmaxf(fabsf(norm ? v.x * gm.x : v.x), fabsf(norm ? v.y * gm.y : v.y)));
+                const int r = i0 / half_ks;
+                const bool last = j + 1 == npass || (i0 + NTH) / half_ks != r || i0 + NTH >= npairs;
+                if (last) {  // warp-uniform
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            }
-            if (lane == 0) {
-                part[j * NW + warp] = ss;
-                part[npass * NW + j * NW + warp] = mx;
+                    for (int off = 16; off > 0; off >>= 1) {
+                        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    }
+                    if (lane == 0 && i0 < npairs) {
+                        part[r * NW + warp] = ss;
+                        part[nb * NW + r * NW + warp] = mx;
+                    }
+                    ss = 0.f;
+                    mx = 0.f;
+                }
             }
         }
         __syncthreads();
-        // row r's entries are e in [r*half_ks/32, (r+1)*half_ks/32): one warp per row
-        for (int r = warp; r < nb; r += NW) {
-            const int e0 = r * (half_ks >> 5), e1 = e0 + (half_ks >> 5);
+        // row r: the warps' partials in warp order
+        if (tid < nb) {
+            const int r = tid;
             float ss = 0.f, mx = 0.f;
-            for (int e = e0 + lane; e < e1; e += 32) {
-                ss += part[e];
-                mx = fmaxf(mx, part[npass * NW + e]);
+            for (int w = 0; w < NW; ++w) {
+                ss += part[r * NW + w];
+                mx = fmaxf(mx, part[nb * NW + r * NW + w]);
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            }
-            if (lane == 0) {
-                m.nx[0 * kMaxNb + r] = ss;  // this slice's sum of squares
-                m.nx[1 * kMaxNb + r] = mx;
-            }
+            m.nx[0 * kMaxNb + r] = ss;  // this slice's sum of squares
+            m.nx[1 * kMaxNb + r] = mx;
         }
         if (norm && S > 1) {
             cg::cluster_group cluster = cg::this_cluster();
