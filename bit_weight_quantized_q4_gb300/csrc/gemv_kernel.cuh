@@ -1040,34 +1040,125 @@ __device__ __forceinline__ float fold_one(const GemvParams &p, const Geo &q, con
     return v;
 }
 
-// Cluster K-split (S > 1): fold the warps' partials of each tile into
-// `red`, apply the output factor, then fold the K-slices into rank 0 over
-// distributed shared memory in rank order.  Returns false on cluster ranks
-// other than 0, which have nothing left to do.
+// Cluster K-split (S > 1): each rank folds its warps' partials of all the
+// group's outputs into `red` (its K-slice's share, output factor applied);
+// then each rank finishes one slice of the outputs -- adding the ranks'
+// shares in rank order over distributed shared memory -- and writes that
+// slice (store, residual, SwiGLU on whole gate/up pairs).  For the argmax,
+// each rank reduces its slice to (max, index) pairs and rank 0 combines the
+// ranks' pairs in rank order.  A final cluster barrier keeps every CTA alive
+// until the others are done reading its shared memory.
 template <int CLS>
-__device__ bool fold_tiles(const GemvParams &p, const Geo &q, const Smem &m, int S, int rank, int tid) {
-    constexpr int NTH = Cls<CLS>::NW * 32;
+__device__ void cluster_finish(const GemvParams &p, const Geo &q, const Smem &m, int S, int rank, int group, int tid,
+                               int warp, int lane) {
+    constexpr int NW = Cls<CLS>::NW, NTH = NW * 32;
     const int nb = CLS == 0 ? 1 : p.nb;
-    const int total = q.tiles_here * kTileRows * nb;
-    WarpTable<Cls<CLS>::NW> wt;
-    wt.load(m.wtab);
-    for (int idx = tid; idx < total; idx += NTH) {
-        const int tl = idx / (kTileRows * nb);
-        const int rem = idx - tl * kTileRows * nb;
-        const int row = rem / nb, r = rem - row * nb;
-        m.red[idx] = fold_one<CLS>(p, q, m, wt, tl, row, r, nb) * m.nx[5 * kMaxNb + r];
+    const int tile_vals = kTileRows * nb;
+    const int total = q.tiles_here * tile_vals;
+    {
+        WarpTable<NW> wt;
+        wt.load(m.wtab);
+        for (int idx = tid; idx < total; idx += NTH) {
+            const int tl = idx / tile_vals;
+            const int rem = idx - tl * tile_vals;
+            const int row = rem / nb, r = rem - row * nb;
+            m.red[idx] = fold_one<CLS>(p, q, m, wt, tl, row, r, nb) * m.nx[5 * kMaxNb + r];
+        }
     }
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
-    if (rank == 0) {
-        for (int idx = tid; idx < total; idx += NTH) {
-            float v = m.red[idx];
-            for (int rr = 1; rr < S; ++rr) v += cluster.map_shared_rank(m.red, rr)[idx];
-            m.red[idx] = v;
+    // this rank's slice: whole tiles (whole gate/up pairs for SwiGLU)
+    const int tpu = p.epi == EPI_SWIGLU ? 2 : 1;
+    const int nu = q.tiles_here / tpu;
+    const int i0 = (rank * nu / S) * tpu * tile_vals, i1 = ((rank + 1) * nu / S) * tpu * tile_vals;
+    float *reds[kMaxCluster];
+#pragma unroll
+    for (int rr = 0; rr < kMaxCluster; ++rr) reds[rr] = rr < S ? cluster.map_shared_rank(m.red, rr) : nullptr;
+    // (no other rank reads this rank's slice, so it is overwritten in place)
+    for (int idx = i0 + tid; idx < i1; idx += NTH) {
+        float v = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < kMaxCluster; ++rr)
+            if (rr < S) v += reds[rr][idx];
+        m.red[idx] = v;
+    }
+    __syncthreads();
+    if (group < p.groups) {
+        if (p.epi == EPI_ARGMAX) {
+            const int N = p.n[0];
+            float *bvs = m.rbuf;  // [warp], then this rank's pairs [nb] at rbuf + 2*NW
+            int *bis = reinterpret_cast<int *>(m.rbuf + NW);
+            float *rv = m.rbuf + 2 * NW;
+            int *ri_ = reinterpret_cast<int *>(m.rbuf + 2 * NW + kMaxNb);
+            const int row0 = i0 / nb, row1 = i1 / nb;  // rows (tile * 16 + row) of the slice
+            for (int r = 0; r < nb; ++r) {
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+                for (int ri = row0 + tid; ri < row1; ri += NTH) {
+                    const int n = (q.t0 + ri / kTileRows) * kTileRows + (ri % kTileRows);
+                    if (n >= N) continue;
+                    const float v = m.red[ri * nb + r];
+                    if (p.out[0] != nullptr) p.out[0][(size_t)r * N + n] = v;
+                    am_take(bv, bi, v, n);
+                }
+                am_warp(bv, bi);
+                if (lane == 0) {
+                    bvs[warp] = bv;
+                    bis[warp] = bi;
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    float fv = bvs[0];
+                    int fi = bis[0];
+                    for (int w = 1; w < NW; ++w) {
+                        if (bvs[w] > fv || (bvs[w] == fv && bis[w] < fi)) {
+                            fv = bvs[w];
+                            fi = bis[w];
+                        }
+                    }
+                    rv[r] = fv;
+                    ri_[r] = fi;
+                }
+                __syncthreads();
+            }
+            cluster.sync();  // every rank's pairs are in its shared memory
+            if (rank == 0 && tid < nb) {
+                float fv = -INFINITY;
+                int fi = 0x7fffffff;
+                for (int rr = 0; rr < S; ++rr) {
+                    const float v = cluster.map_shared_rank(rv, rr)[tid];
+                    const int k = cluster.map_shared_rank(ri_, rr)[tid];
+                    if (v > fv || (v == fv && k < fi)) {
+                        fv = v;
+                        fi = k;
+                    }
+                }
+                p.am_val[(size_t)tid * p.groups + group] = fv;
+                p.am_idx[(size_t)tid * p.groups + group] = fi;
+            }
+        } else {
+            for (int idx = i0 + tid; idx < i1; idx += NTH) {
+                const int tl = idx / tile_vals;
+                const int rem = idx - tl * tile_vals;
+                const int row = rem / nb, r = rem - row * nb;
+                int mi, tm;
+                map_tile(p, q.t0 + tl, mi, tm);
+                const int n = tm * kTileRows + row;
+                const int N = p.n[mi];
+                if (n >= N) continue;
+                const float v = m.red[idx];
+                if (p.epi == EPI_STORE) {
+                    p.out[mi][(size_t)r * N + n] = v;
+                } else if (p.epi == EPI_RESIDUAL) {
+                    p.out[0][(size_t)r * N + n] = v + __ldcg(p.res + (size_t)r * N + n);
+                } else if (mi == 0) {  // EPI_SWIGLU: gate tile tl, up tile tl + 1 (same slice)
+                    const float u = m.red[idx + tile_vals];
+                    p.out[0][(size_t)r * N + n] = v / (1.0f + expf(-v)) * u;
+                }
+            }
         }
     }
-    cluster.sync();
-    return rank == 0;
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // Write the job's outputs: store, residual add, SwiGLU over a gate/up tile
@@ -1225,7 +1316,10 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid
         fold_store<CLS>(p, q, m, group, tid);
         return;
     }
-    if (S > 1 && !fold_tiles<CLS>(p, q, m, S, rank, tid)) return;
+    if (S > 1) {
+        cluster_finish<CLS>(p, q, m, S, rank, group, tid, warp, lane);
+        return;
+    }
     epilogue<CLS>(p, q, m, S, group, tid, warp, lane);
 }
 
