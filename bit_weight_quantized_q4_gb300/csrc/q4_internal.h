@@ -68,8 +68,8 @@ constexpr int kMaxMats = 3;                   // matrices of one job (q, k, v sh
 //   class 3 (nb = 9..16): as class 2 over two 8-column n-tiles -- eight.
 Q4_HD constexpr int cls_of(int nb) { return nb <= 1 ? 0 : nb <= 4 ? 1 : nb <= 8 ? 2 : 3; }
 Q4_HD constexpr int cls_warps(int c) { return c == 3 ? 8 : 16; }     // warps per CTA
-Q4_HD constexpr int cls_depth(int c) { return c == 0 || c == 3 ? 2 : 3; }  // ring stages per warp
-Q4_HD constexpr int cls_stage(int c) { return c == 0 || c == 3 ? 2 : 1; }  // pair units per stage (2x as many single-tile units)
+Q4_HD constexpr int cls_depth(int c) { return (void)c, 2; }  // ring stages per warp
+Q4_HD constexpr int cls_stage(int c) { return c == 2 ? 1 : 2; }  // pair units per stage (2x as many single-tile units)
 Q4_HD constexpr int cls_gsw(int c) { return c <= 1 ? 4 : c == 2 ? 8 : 16; }  // group-sum rows per chunk
 
 // A unit of work is one 128-column chunk of upt consecutive 16-row tiles
