@@ -54,23 +54,22 @@ __global__ void __launch_bounds__(256) argmax_fold_kernel(const float *am_val, c
 }
 
 // gsum[r][g] = sum of x[r][32g .. 32g+31] (Module gpu, Struct HalfSet: per-32
-// group sums of a row batch).  One half-warp per group: lane j adds the pair
-// (x[2j], x[2j+1]), then half_warp_sum -- the order the GEMV's staging uses
-// for its own affine block sums, so either source gives the same bits.
+// group sums of a row batch).  Eight lanes per group, four columns each,
+// added by block8_sum -- the order the GEMV's staging uses for its own affine
+// block sums, so either source gives the same bits.
 __global__ void __launch_bounds__(256) group_sums_kernel(const float *x, int nb, int k, float *gsum) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int G = k / 32;
     const int total = nb * G;
     const int lane = threadIdx.x & 31;
-    const int gi_all = 2 * ((blockIdx.x * 256 + threadIdx.x) >> 5) + (lane >> 4);  // (row, group) index
-    float ps = 0.f;
+    const int gi_all = (blockIdx.x * 256 + threadIdx.x) >> 3;  // (row, group) index
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (gi_all < total) {
         const int r = gi_all / G, gi = gi_all - r * G;
-        const float2 v = *reinterpret_cast<const float2 *>(x + (size_t)r * k + 32 * gi + 2 * (lane & 15));
-        ps = v.x + v.y;
+        v = *reinterpret_cast<const float4 *>(x + (size_t)r * k + 32 * gi + 4 * (lane & 7));
     }
-    ps = half_warp_sum(ps);
-    if (gi_all < total && (lane & 15) == 0) gsum[gi_all] = ps;
+    const float t = block8_sum(v);
+    if (gi_all < total && (lane & 7) == 0) gsum[gi_all] = t;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
@@ -98,8 +97,8 @@ int launch_argmax_fold(const float *am_val, const int *am_idx, int groups, int n
 
 int launch_group_sums(const float *x, int nb, int k, float *gsum, void *stream) {
     void *args[] = {(void *)&x, (void *)&nb, (void *)&k, (void *)&gsum};
-    const int total = nb * (k / 32);  // 16 threads per group
-    return launch_pdl((const void *)dev::group_sums_kernel, dim3((16 * total + 255) / 256), dim3(256), args,
+    const int total = nb * (k / 32);  // 8 threads per group
+    return launch_pdl((const void *)dev::group_sums_kernel, dim3((8 * total + 255) / 256), dim3(256), args,
                       (cudaStream_t)stream);
 }
 

@@ -471,322 +471,326 @@ __device__ __forceinline__ void put_pair(uint8_t *xs, int xbs, int r, int kl, fl
 
 __device__ __forceinline__ int gs_idx(int b, int row, int GSW) { return ((b >> 2) * GSW + row) * 4 + (b & 3); }
 
+// One activation row whose slice has at most 8192 columns (Ks): column
+// pairs through registers, thread t holding pairs t, t + NTH, ...; the block
+// sums add pairs and then half_warp_sum -- the same order as block8_sum.
+template <int FMT, int CLS>
+__device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int S, int tid, int warp, int lane) {
+    using C = Cls<CLS>;
+    constexpr int NW = C::NW, NTH = NW * 32, GSW = C::GSW;
+    constexpr int RP = 8192 / (2 * NTH);
+    const int Ks = p.Cs * kChunkK;  // staged columns; those at or beyond ke are zero
+    const int kb = q.kb, ke = q.ke;
+    const int xbs = 128;
+    const bool norm = p.gamma != nullptr;
+    const bool given = FMT == 1 && p.gsum != nullptr && !norm;  // affine sums from the caller
+    const int npass = (Ks / 2 + NTH - 1) / NTH;  // pairs per thread actually used
+    float2 xv[RP], gv[RP];
+    float ss = 0.f, mx = 0.f;
+    // every load first (guarded, not a loop exit, so that they can all
+    // be in flight together), then the statistics
+#pragma unroll
+    for (int qq = 0; qq < RP; ++qq) {
+        float2 v = make_float2(0.f, 0.f), gm = make_float2(1.f, 1.f);
+        const int k = kb + 2 * (tid + qq * NTH);
+        if (qq < npass && k < ke) {
+            v = __ldcg(reinterpret_cast<const float2 *>(p.x + k));
+            if (norm) gm = *reinterpret_cast<const float2 *>(p.gamma + k);
+        }
+        xv[qq] = v;
+        gv[qq] = gm;
+    }
+#pragma unroll
+    for (int qq = 0; qq < RP; ++qq) {
+        const float2 v = xv[qq], gm = gv[qq];  // zero beyond npass
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        mx = fmaxf(mx, fmaxf(fabsf(norm ? v.x * gm.x : v.x), fabsf(norm ? v.y * gm.y : v.y)));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    if (lane == 0) {
+        m.rbuf[warp] = ss;
+        m.rbuf[NW + warp] = mx;
+    }
+    __syncthreads();
+    float tss = 0.f, tmx = 0.f;  // every thread adds the warps in the same order
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        tss += m.rbuf[w];
+        tmx = fmaxf(tmx, m.rbuf[NW + w]);
+    }
+    if (norm && S > 1) {
+        // the RMS needs the whole row: add the slices' sums in rank order
+        cg::cluster_group cluster = cg::this_cluster();
+        if (tid == 0) m.nx[0] = tss;
+        cluster.sync();
+        tss = 0.f;
+        for (int r = 0; r < S; ++r) tss += cluster.map_shared_rank(m.nx, r)[0];
+    }
+    const float inv_rms = norm ? 1.0f / sqrtf(tss / (float)p.K + p.eps) : 1.f;
+    float scale, out_factor;
+    row_scale(tmx * inv_rms, scale, out_factor);
+    if (tid == 0) {
+        m.nx[2 * kMaxNb] = inv_rms;
+        m.nx[3 * kMaxNb] = scale;
+        m.nx[5 * kMaxNb] = out_factor;
+    }
+#pragma unroll
+    for (int qq = 0; qq < RP; ++qq) {
+        if (qq >= npass) break;
+        const int kl = 2 * (tid + qq * NTH);
+        // warp-uniform: a warp's pairs are 64 consecutive columns and Ks is a multiple of 128
+        if (kl < Ks) {
+            float v0 = xv[qq].x, v1 = xv[qq].y;
+            if (norm) {
+                v0 = v0 * inv_rms * gv[qq].x;
+                v1 = v1 * inv_rms * gv[qq].y;
+            }
+            v0 *= scale;
+            v1 *= scale;
+            put_pair<CLS>(m.xs, xbs, 0, kl, v0, v1);
+            if (FMT == 1 && !given) {
+                const float bsum = half_warp_sum(v0 + v1);
+                if ((lane & 15) == 0) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum * 0x1p-20f;
+            }
+        }
+    }
+    if (given) {
+        const float f = scale * 0x1p-20f;
+        for (int b = tid; b < p.Cs * kBlocksPerChunk; b += NTH)
+            m.gs[gs_idx(b, 0, GSW)] = kb + 32 * b < ke ? __ldcg(p.gsum + kb / 32 + b) * f : 0.f;
+    }
+}
+
 // Stage this CTA's activation slice of job p: per row, scale by a power of
 // two chosen from its largest magnitude (after RMSNorm when gamma is given)
 // and split into f16 hi + lo in B-fragment order (xs_off); then, for the
-// affine format, the block sums: fp32 sums of the scaled values (pairs, then
-// a butterfly over 16 lanes -- the order of q4_group_sums) or the caller's
-// group sums.  (Q4_0's offset products are formed in run_units.)  Activation loads bypass
-// L1 (.cg): in the persistent kernel another SM may have rewritten them
-// since this SM last read them.
-// SP: column pairs per thread a multi-row slice may stage through registers
-template <int FMT, int CLS, int SP>
+// affine format, the block sums: fp32 sums of the scaled values in the order
+// of q4_group_sums (block8_sum), or the caller's group sums.  (Q4_0's offset
+// products are formed in run_units.)
+//
+// One row of at most 8192 columns takes stage_row1.  Otherwise the slice is
+// nb rows x Cs chunks of 128 columns; a segment is one row of
+// one chunk, a float4 per lane.  Warp w takes a contiguous range of segments
+// in row-major order, so it touches few rows: its per-row statistics are
+// summed in registers and reduced once per row, into per-(row, warp)
+// partials.  After one CTA barrier, lane i of each warp adds the partials of
+// the warp's i-th row in warp order (every warp the same way), and the
+// writes take the row's scale from that lane.  Up to SEG segments per warp
+// stay in registers between the statistics and the writes; a longer range is
+// read twice, SEG segments at a time.  Activation loads bypass L1 (.cg): in
+// the persistent kernel another SM may have rewritten them since this SM
+// last read them.
+template <int FMT, int CLS, int SEG>
 __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S, int tid, int warp, int lane) {
     using C = Cls<CLS>;
     constexpr int NW = C::NW, NTH = NW * 32, GSW = C::GSW;
     const int nb = CLS == 0 ? 1 : p.nb;
-    const int Ks = p.Cs * kChunkK;  // staged columns; those at or beyond ke are zero
+    const int Cs = p.Cs;
     const int kb = q.kb, ke = q.ke;
     const int xbs = 128 * nb;
     const bool norm = p.gamma != nullptr;
     const bool given = FMT == 1 && p.gsum != nullptr && !norm;  // affine sums from the caller
-    constexpr int RP = 8192 / (2 * NTH);  // nb == 1: a slice up to 8192 columns passes through registers
-    if (CLS == 0 && Ks <= 2 * NTH * RP) {
-        const int npass = (Ks / 2 + NTH - 1) / NTH;  // pairs per thread actually used
-        float2 xv[RP], gv[RP];
-        float ss = 0.f, mx = 0.f;
-        // every load first (guarded, not a loop exit, so that they can all
-        // be in flight together), then the statistics
+    if (CLS == 0 && Cs * kChunkK <= 8192) {
+        stage_row1<FMT, CLS>(p, q, m, S, tid, warp, lane);
+        __syncthreads();
+        return;
+    }
+    const int nseg = nb * Cs;
+    const int spw = (nseg + NW - 1) / NW;
+    const int s0 = min(warp * spw, nseg), s1 = min(s0 + spw, nseg);
+    const int r0 = CLS == 0 ? 0 : s0 / Cs, c0 = s0 - r0 * Cs;  // row and chunk of this warp's first segment
+    const bool held = s1 - s0 <= SEG;                          // the whole range stays in registers
+
+    // this warp's partials start at zero for every row (neutral for the sum
+    // and the max); the flushes below overwrite the rows it touches
+    float *part = m.rbuf;  // [2][nb][NW]
+    if (lane < nb) {
+        part[lane * NW + warp] = 0.f;
+        part[(nb + lane) * NW + warp] = 0.f;
+    }
+    __syncwarp();
+
+    float4 xv[SEG];
+    // the batch of SEG segments from `base` (row rb, chunk cb); loads are
+    // predicated, not branched around, so that they are all in flight
+    // together; segments past the warp's range read as zeros
+    auto load_batch = [&](int base, int rb, int cb) {
+        int r = rb, c = cb;
 #pragma unroll
-        for (int qq = 0; qq < RP; ++qq) {
-            float2 v = make_float2(0.f, 0.f), gm = make_float2(1.f, 1.f);
-            const int k = kb + 2 * (tid + qq * NTH);
-            if (qq < npass && k < ke) {
-                v = __ldcg(reinterpret_cast<const float2 *>(p.x + k));
-                if (norm) gm = *reinterpret_cast<const float2 *>(p.gamma + k);
+        for (int j = 0; j < SEG; ++j) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int k = kb + 128 * c + 4 * lane;
+            if (base + j < s1 && k < ke) v = __ldcg(reinterpret_cast<const float4 *>(p.x + (size_t)r * p.K + k));
+            xv[j] = v;
+            if (++c == Cs) {
+                c = 0;
+                ++r;
             }
-            xv[qq] = v;
-            gv[qq] = gm;
         }
-#pragma unroll
-        for (int qq = 0; qq < RP; ++qq) {
-            const float2 v = xv[qq], gm = gv[qq];  // zero beyond npass
-            ss = fmaf(v.x, v.x, ss);
-            ss = fmaf(v.y, v.y, ss);
-            mx = fmaxf(mx, fmaxf(fabsf(norm ? v.x * gm.x : v.x), fabsf(norm ? v.y * gm.y : v.y)));
-        }
+    };
+
+    // ---- per-row statistics: sum of squares and largest |x (* gamma)|
+    float ss = 0.f, mx = 0.f;
+    int rcur = r0;
+    auto flush = [&]() {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             ss += __shfl_xor_sync(0xffffffffu, ss, off);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         }
         if (lane == 0) {
-            m.rbuf[warp] = ss;
-            m.rbuf[NW + warp] = mx;
+            part[rcur * NW + warp] = ss;
+            part[(nb + rcur) * NW + warp] = mx;
         }
-        __syncthreads();
-        float tss = 0.f, tmx = 0.f;  // every thread adds the warps in the same order
+        ss = 0.f;
+        mx = 0.f;
+    };
+    {
+        int rb = r0, cb = c0;
+        for (int base = s0; base < s1; base += SEG) {
+            load_batch(base, rb, cb);
+            int r = rb, c = cb;
+#pragma unroll
+            for (int j = 0; j < SEG; ++j) {
+                if (CLS != 0 && base + j < s1 && r != rcur) {  // warp-uniform: a new row
+                    flush();
+                    rcur = r;
+                }
+                const float4 v = xv[j];  // zero past the range: neutral
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss);
+                ss = fmaf(v.w, v.w, ss);
+                float4 a = v;
+                const int k = kb + 128 * c + 4 * lane;
+                if (norm && base + j < s1 && k < ke) {
+                    const float4 g = __ldg(reinterpret_cast<const float4 *>(p.gamma + k));
+                    a.x *= g.x;
+                    a.y *= g.y;
+                    a.z *= g.z;
+                    a.w *= g.w;
+                }
+                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+                if (++c == Cs) {
+                    c = 0;
+                    ++r;
+                }
+            }
+            rb = r;
+            cb = c;
+        }
+        if (s0 < s1) flush();
+    }
+    __syncthreads();
+
+    // row r's inverse RMS and scales from the warps' partials in warp order
+    // (and, for a split RMSNorm, the cluster ranks' slice sums in rank order)
+    auto row_stats = [&](int r, float &ir, float &sc, float &of) {
+        float tss = 0.f, tmx = 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-            tss += m.rbuf[w];
-            tmx = fmaxf(tmx, m.rbuf[NW + w]);
+            tss += part[r * NW + w];
+            tmx = fmaxf(tmx, part[(nb + r) * NW + w]);
         }
         if (norm && S > 1) {
-            // the RMS needs the whole row: add the slices' sums in rank order
             cg::cluster_group cluster = cg::this_cluster();
-            if (tid == 0) m.nx[0] = tss;
-            cluster.sync();
             tss = 0.f;
-            for (int r = 0; r < S; ++r) tss += cluster.map_shared_rank(m.nx, r)[0];
+            for (int rr = 0; rr < S; ++rr) tss += cluster.map_shared_rank(m.nx, rr)[r];
         }
-        const float inv_rms = norm ? 1.0f / sqrtf(tss / (float)p.K + p.eps) : 1.f;
-        float scale, out_factor;
-        row_scale(tmx * inv_rms, scale, out_factor);
-        if (tid == 0) {
-            m.nx[2 * kMaxNb] = inv_rms;
-            m.nx[3 * kMaxNb] = scale;
-            m.nx[5 * kMaxNb] = out_factor;
-        }
-#pragma unroll
-        for (int qq = 0; qq < RP; ++qq) {
-            if (qq >= npass) break;
-            const int kl = 2 * (tid + qq * NTH);
-            // warp-uniform: a warp's pairs are 64 consecutive columns and Ks is a multiple of 128
-            if (kl < Ks) {
-                float v0 = xv[qq].x, v1 = xv[qq].y;
-                if (norm) {
-                    v0 = v0 * inv_rms * gv[qq].x;
-                    v1 = v1 * inv_rms * gv[qq].y;
-                }
-                v0 *= scale;
-                v1 *= scale;
-                put_pair<CLS>(m.xs, xbs, 0, kl, v0, v1);
-                if (FMT == 1 && !given) {
-                    const float bsum = half_warp_sum(v0 + v1);
-                    if ((lane & 15) == 0) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum * 0x1p-20f;
-                }
-            }
-        }
-        if (given) {
-            const float f = scale * 0x1p-20f;
-            for (int b = tid; b < p.Cs * kBlocksPerChunk; b += NTH)
-                m.gs[gs_idx(b, 0, GSW)] = kb + 32 * b < ke ? __ldcg(p.gsum + kb / 32 + b) * f : 0.f;
-        }
-    } else if (CLS != 0 && nb * (Ks >> 1) <= SP * NTH) {
-        // a slice of at most SP column pairs per thread: one batch
-        // of loads into registers, per-row statistics, then the writes
-        const int half_ks = Ks >> 1;
-        const int npairs = nb * half_ks;  // a multiple of 64; a warp's 32 pairs lie in one row
-        const int npass = (npairs + NTH - 1) / NTH;
-        float2 xv[SP], gv[SP];
-#pragma unroll
-        for (int j = 0; j < SP; ++j) {  // guarded, not a loop exit: the loads overlap
-            const int i = tid + j * NTH;
-            float2 v = make_float2(0.f, 0.f), gm = make_float2(1.f, 1.f);
-            if (j < npass && i < npairs) {
-                const int r = i / half_ks, k = kb + 2 * (i - r * half_ks);
-                if (k < ke) {
-                    v = __ldcg(reinterpret_cast<const float2 *>(p.x + (size_t)r * p.K + k));
-                    if (norm) gm = *reinterpret_cast<const float2 *>(p.gamma + k);
-                }
-            }
-            xv[j] = v;
-            gv[j] = gm;
-        }
-        // per (row, warp) partials: a warp's passes j cover pairs
-        // [j*NTH + 32*warp, +32), all in one row, and consecutive passes stay in
-        // a row until it ends -- accumulate in registers, reduce once per row.
-        // Entries of warps that cover no pair of a row stay zero (neutral for
-        // both the sum and the max).
-        float *part = m.rbuf;  // [2][nb][NW]
-        for (int e = tid; e < 2 * nb * NW; e += NTH) part[e] = 0.f;
-        __syncthreads();  // (the loads above are still in flight)
-        {
-            float ss = 0.f, mx = 0.f;
-#pragma unroll
-            for (int j = 0; j < SP; ++j) {
-                if (j >= npass) break;
-                const int i0 = j * NTH + warp * 32;  // this warp's first pair of pass j
-                const float2 v = xv[j], gm = gv[j];
-                ss = fmaf(v.x, v.x, ss);
-                ss = fmaf(v.y, v.y, ss);
-                mx = fmaxf(mx, fmaxf(fabsf(norm ? v.x * gm.x : v.x), fabsf(norm ? v.y * gm.y : v.y)));
-                const int r = i0 / half_ks;
-                const bool last = j + 1 == npass || (i0 + NTH) / half_ks != r || i0 + NTH >= npairs;
-                if (last) {  // warp-uniform
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                    }
-                    if (lane == 0 && i0 < npairs) {
-                        part[r * NW + warp] = ss;
-                        part[nb * NW + r * NW + warp] = mx;
-                    }
-                    ss = 0.f;
-                    mx = 0.f;
-                }
-            }
-        }
-        __syncthreads();
-        // row r: the warps' partials in warp order
+        ir = norm ? 1.0f / sqrtf(tss / (float)p.K + p.eps) : 1.f;
+        row_scale(tmx * ir, sc, of);
+    };
+    if (norm && S > 1) {
+        // the RMS needs the whole row: publish this slice's sums, then every
+        // rank reads all of them
         if (tid < nb) {
-            const int r = tid;
-            float ss = 0.f, mx = 0.f;
-            for (int w = 0; w < NW; ++w) {
-                ss += part[r * NW + w];
-                mx = fmaxf(mx, part[nb * NW + r * NW + w]);
-            }
-            m.nx[0 * kMaxNb + r] = ss;  // this slice's sum of squares
-            m.nx[1 * kMaxNb + r] = mx;
-        }
-        if (norm && S > 1) {
-            cg::cluster_group cluster = cg::this_cluster();
-            cluster.sync();
-            if (tid < nb) {
-                float tot = 0.f;
-                for (int rr = 0; rr < S; ++rr) tot += cluster.map_shared_rank(m.nx, rr)[tid];
-                m.nx[4 * kMaxNb + tid] = tot;
-            }
-        } else {
-            __syncthreads();
-            if (tid < nb) m.nx[4 * kMaxNb + tid] = m.nx[tid];
-        }
-        __syncthreads();
-        if (tid < nb) {
-            float inv_rms = 1.f;
-            if (norm) inv_rms = 1.0f / sqrtf(m.nx[4 * kMaxNb + tid] / (float)p.K + p.eps);
-            float scale, out_factor;
-            row_scale(m.nx[1 * kMaxNb + tid] * inv_rms, scale, out_factor);
-            m.nx[2 * kMaxNb + tid] = inv_rms;
-            m.nx[3 * kMaxNb + tid] = scale;
-            m.nx[5 * kMaxNb + tid] = out_factor;
-        }
-        __syncthreads();
+            float tss = 0.f;
 #pragma unroll
-        for (int j = 0; j < SP; ++j) {
-            if (j >= npass) break;
-            const int i = tid + j * NTH;
-            if (i < npairs) {  // warp-uniform
-                const int r = i / half_ks, kl = 2 * (i - r * half_ks);
-                float v0 = xv[j].x, v1 = xv[j].y;
-                if (norm) {
-                    const float ir = m.nx[2 * kMaxNb + r];
-                    v0 = v0 * ir * gv[j].x;
-                    v1 = v1 * ir * gv[j].y;
-                }
-                const float sc = m.nx[3 * kMaxNb + r];
-                v0 *= sc;
-                v1 *= sc;
-                put_pair<CLS>(m.xs, xbs, r, kl, v0, v1);
-                if (FMT == 1 && !given) {
-                    const float bsum = half_warp_sum(v0 + v1);
-                    if ((lane & 15) == 0) m.gs[gs_idx(kl >> 5, r, GSW)] = bsum * 0x1p-20f;
-                }
-            }
+            for (int w = 0; w < NW; ++w) tss += part[tid * NW + w];
+            m.nx[tid] = tss;
         }
-        if (given) {
-            const int nblk = p.Cs * kBlocksPerChunk;
-            for (int i = tid; i < nb * nblk; i += NTH) {
-                const int r = i / nblk, b = i - r * nblk;
-                const float f = m.nx[3 * kMaxNb + r] * 0x1p-20f;
-                m.gs[gs_idx(b, r, GSW)] =
-                    kb + 32 * b < ke ? __ldcg(p.gsum + (size_t)r * (p.K / 32) + kb / 32 + b) * f : 0.f;
-            }
-        }
-    } else {
-        // general: two passes over the slice
-        for (int r = 0; r < nb; ++r) {
-            float ss = 0.f, mx = 0.f;
-            const float *xr = p.x + (size_t)r * p.K;
-            for (int k = kb + 2 * tid; k < ke; k += 2 * NTH) {
-                float2 v = __ldcg(reinterpret_cast<const float2 *>(xr + k));
-                ss = fmaf(v.x, v.x, ss);
-                ss = fmaf(v.y, v.y, ss);
-                if (norm) {
-                    float2 gm = *reinterpret_cast<const float2 *>(p.gamma + k);
-                    mx = fmaxf(mx, fmaxf(fabsf(v.x * gm.x), fabsf(v.y * gm.y)));
-                } else {
-                    mx = fmaxf(mx, fmaxf(fabsf(v.x), fabsf(v.y)));
-                }
-            }
+        cg::this_cluster().sync();
+    }
+    if (tid < nb) {  // for the epilogue (read after later barriers)
+        float ir, sc, of;
+        row_stats(tid, ir, sc, of);
+        m.nx[2 * kMaxNb + tid] = ir;
+        m.nx[3 * kMaxNb + tid] = sc;
+        m.nx[5 * kMaxNb + tid] = of;
+    }
+    const int nr = s1 > s0 ? (s1 - 1) / Cs - r0 + 1 : 0;  // rows this warp touches
+    float l_ir = 1.f, l_sc = 1.f;
+    if (lane < nr) {
+        float of;
+        row_stats(r0 + lane, l_ir, l_sc, of);
+    }
+
+    // ---- the writes: x (* inv_rms * gamma) * scale as f16 hi + lo; the
+    // first 8 of every 16 columns carry an extra factor 16 (see unpack_word)
+    const float f16x = (lane & 2) ? 1.f : 16.f;
+    constexpr int LO = C::HLN ? 64 : 8, P2 = C::HLN ? 16 : 32;  // lo part, second pair
+    const int lane_off = C::HLN ? (lane >> 3) * xbs + (lane & 1) * 32 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4
+                                : (lane >> 3) * xbs + (lane & 1) * 64 + ((lane >> 2) & 1) * 16 + ((lane >> 1) & 1) * 4;
+    {
+        int rb = r0, cb = c0;
+        for (int base = s0; base < s1; base += SEG) {
+            if (!held) load_batch(base, rb, cb);
+            int r = rb, c = cb;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            }
-            if (lane == 0) {
-                m.rbuf[warp * kMaxNb + r] = ss;
-                m.rbuf[NW * kMaxNb + warp * kMaxNb + r] = mx;
-            }
-        }
-        __syncthreads();
-        if (tid < nb) {
-            float ss = 0.f, mx = 0.f;
-            for (int w = 0; w < NW; ++w) {
-                ss += m.rbuf[w * kMaxNb + tid];
-                mx = fmaxf(mx, m.rbuf[NW * kMaxNb + w * kMaxNb + tid]);
-            }
-            m.nx[0 * kMaxNb + tid] = ss;  // this slice's sum of squares
-            m.nx[1 * kMaxNb + tid] = mx;
-        }
-        if (norm && S > 1) {
-            cg::cluster_group cluster = cg::this_cluster();
-            cluster.sync();
-            if (tid < nb) {
-                float tot = 0.f;
-                for (int r = 0; r < S; ++r) tot += cluster.map_shared_rank(m.nx, r)[tid];
-                m.nx[4 * kMaxNb + tid] = tot;
-            }
-        } else if (tid < nb) {
-            m.nx[4 * kMaxNb + tid] = m.nx[tid];
-        }
-        __syncthreads();
-        if (tid < nb) {
-            float inv_rms = 1.f;
-            if (norm) inv_rms = 1.0f / sqrtf(m.nx[4 * kMaxNb + tid] / (float)p.K + p.eps);
-            float scale, out_factor;
-            row_scale(m.nx[1 * kMaxNb + tid] * inv_rms, scale, out_factor);
-            m.nx[2 * kMaxNb + tid] = inv_rms;
-            m.nx[3 * kMaxNb + tid] = scale;
-            m.nx[5 * kMaxNb + tid] = out_factor;
-        }
-        __syncthreads();
-        const int half_ks = Ks >> 1;
-        // warp-uniform trip count: nb * half_ks is a multiple of 64, and a
-        // warp's 32 pairs are consecutive columns of one row
-        for (int i = tid; i < nb * half_ks; i += NTH) {
-            const int r = i / half_ks, kp = i - r * half_ks;
-            const int kl = 2 * kp, k = kb + kl;
-            float v0 = 0.f, v1 = 0.f;
-            if (k < ke) {
-                float2 v = __ldcg(reinterpret_cast<const float2 *>(p.x + (size_t)r * p.K + k));
-                v0 = v.x;
-                v1 = v.y;
+            for (int j = 0; j < SEG; ++j) {
+                const bool valid = base + j < s1;  // warp-uniform
+                const int kl = 128 * c + 4 * lane, k = kb + kl;
+                const float ir = __shfl_sync(0xffffffffu, l_ir, r - r0);
+                const float sc = __shfl_sync(0xffffffffu, l_sc, r - r0);
+                float4 v = xv[j];
                 if (norm) {
-                    const float ir = m.nx[2 * kMaxNb + r];
-                    float2 gm = *reinterpret_cast<const float2 *>(p.gamma + k);
-                    v0 = v0 * ir * gm.x;
-                    v1 = v1 * ir * gm.y;
+                    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (valid && k < ke) g = __ldg(reinterpret_cast<const float4 *>(p.gamma + k));
+                    v.x = v.x * ir * g.x;
+                    v.y = v.y * ir * g.y;
+                    v.z = v.z * ir * g.z;
+                    v.w = v.w * ir * g.w;
+                }
+                const float f = sc * f16x;
+                const __half2 h0 = __floats2half2_rn(v.x * f, v.y * f);
+                const __half2 h1 = __floats2half2_rn(v.z * f, v.w * f);
+                const float2 b0 = __half22float2(h0), b1 = __half22float2(h1);
+                const __half2 l0 = __floats2half2_rn(v.x * f - b0.x, v.y * f - b0.y);
+                const __half2 l1 = __floats2half2_rn(v.z * f - b1.x, v.w * f - b1.y);
+                float bsum = 0.f;
+                if (FMT == 1 && !given) bsum = block8_sum(v);  // sum of scaled values = sc * this
+                if (valid) {
+                    const int seg = C::HLN ? 4 * c * xbs + 128 * r : 4 * c * xbs + (r >> 3) * 1024 + (r & 7) * 128;
+                    uint8_t *d = m.xs + seg + lane_off;
+                    *reinterpret_cast<__half2 *>(d) = h0;
+                    *reinterpret_cast<__half2 *>(d + LO) = l0;
+                    *reinterpret_cast<__half2 *>(d + P2) = h1;
+                    *reinterpret_cast<__half2 *>(d + P2 + LO) = l1;
+                    if (FMT == 1 && !given && (lane & 7) == 0)
+                        m.gs[gs_idx(kl >> 5, r, GSW)] = bsum * (sc * 0x1p-20f);
+                }
+                if (++c == Cs) {
+                    c = 0;
+                    ++r;
                 }
             }
-            const float sc = m.nx[3 * kMaxNb + r];
-            v0 *= sc;
-            v1 *= sc;
-            put_pair<CLS>(m.xs, xbs, r, kl, v0, v1);
-            if (FMT == 1 && !given) {
-                const float bsum = half_warp_sum(v0 + v1);
-                if ((lane & 15) == 0) m.gs[gs_idx(kl >> 5, r, GSW)] = bsum * 0x1p-20f;
-            }
+            rb = r;
+            cb = c;
         }
-        if (given) {
-            const int nblk = p.Cs * kBlocksPerChunk;
-            for (int i = tid; i < nb * nblk; i += NTH) {
-                const int r = i / nblk, b = i - r * nblk;
-                const float f = m.nx[3 * kMaxNb + r] * 0x1p-20f;
-                m.gs[gs_idx(b, r, GSW)] =
-                    kb + 32 * b < ke ? __ldcg(p.gsum + (size_t)r * (p.K / 32) + kb / 32 + b) * f : 0.f;
-            }
+    }
+    if (given) {
+        __syncthreads();  // the row scales in nx
+        const int nblk = Cs * kBlocksPerChunk;
+        for (int i = tid; i < nb * nblk; i += NTH) {
+            const int r = i / nblk, b = i - r * nblk;
+            const float f = m.nx[3 * kMaxNb + r] * 0x1p-20f;
+            m.gs[gs_idx(b, r, GSW)] =
+                kb + 32 * b < ke ? __ldcg(p.gsum + (size_t)r * (p.K / 32) + kb / 32 + b) * f : 0.f;
         }
     }
     __syncthreads();
@@ -1308,7 +1312,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid
     for (int s = 0; s < C::DU - 1; ++s) ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    stage_x<FMT, CLS, 16>(p, q, m, S, tid, warp, lane);
+    stage_x<FMT, CLS, CLS == 0 ? 4 : CLS == 3 ? 16 : 8>(p, q, m, S, tid, warp, lane);
     run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
     ring.drain();
     __syncthreads();
@@ -1393,7 +1397,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
         }
         const Geo q = make_geo<NW>(p, group, 0, warp);
         if (q.tiles_here == 0) continue;  // no work in this job (CTA-uniform)
-        stage_x<FMT, CLS, 8>(p, q, m, 1, tid, warp, lane);
+        stage_x<FMT, CLS, 2>(p, q, m, 1, tid, warp, lane);
         run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
         __syncthreads();
         if (p.epi != EPI_ARGMAX) {

@@ -123,10 +123,20 @@ struct StepParams {
 };
 
 #if defined(__CUDACC__)
-// Sum over each half-warp (lanes 0..15 and 16..31) as a butterfly over lane
-// xor 1, 2, 4, 8: every lane of the half ends with the same value.  The
-// affine block sums of the staged activations and q4_group_sums both add
-// this way (pair sums first), so the two give the same bits.
+// Block sum of 32 activations held as a float4 by each of 8 consecutive
+// lanes: (v.x + v.y) + (v.z + v.w) per lane, then a butterfly over lane xor
+// 1, 2, 4; every lane of the 8 ends with the same value.  The affine block
+// sums of the staged activations and q4_group_sums both add this way, so the
+// two give the same bits.  half_warp_sum over column pairs (lanes 0..15 and
+// 16..31 holding x[2j] + x[2j+1]) adds in the same order: its first step
+// forms the same four-column sums, its other three the same butterfly.
+__device__ __forceinline__ float block8_sum(float4 v) {
+    float t = (v.x + v.y) + (v.z + v.w);
+    t += __shfl_xor_sync(0xffffffffu, t, 1);
+    t += __shfl_xor_sync(0xffffffffu, t, 2);
+    t += __shfl_xor_sync(0xffffffffu, t, 4);
+    return t;
+}
 __device__ __forceinline__ float half_warp_sum(float v) {
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
