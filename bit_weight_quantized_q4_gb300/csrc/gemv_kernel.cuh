@@ -400,7 +400,8 @@ struct Ring {
 // Shared-memory regions of one CTA (sizes: engine_smem()).
 struct Smem {
     uint8_t *xs;     // activation slice, hi/lo f16 in mma B-fragment order
-    float *gs;       // block offset sums [chunk][GSW rows][4 blocks], units of 2^-20
+    float *gs;       // affine block sums of x (* gamma) [chunk][GSW rows][4 blocks]
+    float *fs;       // block factors back to the input's units (times 2^20), same shape
     float *red;      // cluster fold (S > 1): CTA results [TG][16][nb]
     float *slots;    // per-warp tile partials [warp][SW][16][nb]
     float *rbuf;     // reductions [4][warp][kMaxNb]
@@ -415,8 +416,9 @@ __device__ __forceinline__ Smem carve(uint8_t *smem, int nb, int Cs, int TG, int
     using C = Cls<CLS>;
     Smem m;
     m.xs = smem;
-    m.gs = reinterpret_cast<float *>(smem + (size_t)512 * nb * Cs);
-    m.red = m.gs + (size_t)4 * C::GSW * Cs;
+    m.gs = reinterpret_cast<float *>(smem + (size_t)4 * cls_xrow(CLS) * nb * Cs);
+    m.fs = m.gs + (size_t)4 * C::GSW * Cs;
+    m.red = m.fs + (size_t)4 * C::GSW * Cs;
     m.slots = m.red + (S > 1 ? (size_t)TG * kTileRows * nb : 0);
     m.rbuf = m.slots + (size_t)C::NW * SW * kTileRows * nb;
     m.nx = m.rbuf + 4 * C::NW * kMaxNb;
@@ -426,18 +428,18 @@ __device__ __forceinline__ Smem carve(uint8_t *smem, int nb, int Cs, int TG, int
     return m;
 }
 
-// The activation scale of a row: 2^e with bound * 2^e in [2^10, 2^11), from
+// The activation scale of a block: 2^e with bound * 2^e in [2^10, 2^11), from
 // the exponent field of `bound` (e clamped to [-100, 100]; 0 for a zero or
-// non-finite bound), and the output factor 2^(20-e), which also undoes the
+// non-finite bound), and the factor back 2^(20-e), which also undoes the
 // 2^-20 unit of the products.
-__device__ __forceinline__ void row_scale(float bound, float &scale, float &out_factor) {
+__device__ __forceinline__ void block_scale(float bound, float &scale, float &back) {
     int e = 0;
     if (bound > 0.f && bound <= 3.0e38f) {
         const int be = (int)((__float_as_uint(bound) >> 23) & 0xFF);  // bound in [2^(be-127), 2^(be-126))
         e = max(-100, min(100, 10 - (be - 127)));
     }
     scale = __uint_as_float((uint32_t)(127 + e) << 23);
-    out_factor = __uint_as_float((uint32_t)(127 + 20 - e) << 23);
+    back = __uint_as_float((uint32_t)(127 + 20 - e) << 23);
 }
 
 // Byte offset in the staged slice of element kk (0..31) of 32-column block
@@ -450,7 +452,7 @@ template <int CLS>
 __device__ __forceinline__ int xs_off(int b, int r, int kk, int part, int xbs) {
     const int s = kk >> 4, pp = kk & 15, h = pp >> 3, tt = (pp & 7) >> 1;
     if (Cls<CLS>::HLN) return b * xbs + ((2 * r + part) * 4 + tt) * 16 + (2 * s + h) * 4;
-    return b * xbs + (r >> 3) * 1024 + ((r & 7) * 4 + tt) * 32 + s * 16 + part * 8 + h * 4;
+    return b * xbs + (r >> 3) * 512 + ((r & 7) * 4 + tt) * 16 + s * 8 + h * 4;  // f16 value only (part 0)
 }
 
 // Store columns (kl, kl+1) of row r, already scaled, as hi + lo f16 pairs;
@@ -471,24 +473,67 @@ __device__ __forceinline__ void put_pair(uint8_t *xs, int xbs, int r, int kl, fl
 
 __device__ __forceinline__ int gs_idx(int b, int row, int GSW) { return ((b >> 2) * GSW + row) * 4 + (b & 3); }
 
-// One activation row whose slice has at most 8192 columns (Ks): column
-// pairs through registers, thread t holding pairs t, t + NTH, ...; the block
-// sums add pairs and then half_warp_sum -- the same order as block8_sum.
+// Activation staging.  Each 32-column block of a row gets its own power-of-
+// two scale, chosen from the block's largest magnitude (of x * gamma when
+// gamma is given) so that it lands in [2^10, 2^11); the scaled values go to
+// shared memory in mma B-fragment order (xs_off) as f16 hi + lo parts (nb <= 4)
+// or as f16 alone (nb > 4), the first 8 of every 16 columns times 16 (see
+// unpack_word).  The block's factor back to the input's units, times the
+// 2^20 of the nibble unpack, goes to fs, and run_units folds it into the
+// block's weight scale.  For the affine format gs holds the block sums of
+// x (* gamma) in the input's units: in-kernel in the order of q4_group_sums
+// (pairs, then a butterfly), or the caller's group sums.  (Q4_0's offset
+// products are formed in run_units.)  With gamma, the RMS factor of each row
+// multiplies the row's outputs at the end (nx[5]); its sum of squares is
+// reduced per warp here and per row after the staging barrier.  Activation
+// loads bypass L1 (.cg): in the persistent kernel another SM may have
+// rewritten them since this SM last read them.
+
+// After the writes: the staging barrier, then each row's output factor --
+// its inverse RMS from the warps' partial sums of squares in warp order (and,
+// for a split K, the cluster ranks' slice sums in rank order), or 1.
+template <int CLS>
+__device__ void stage_finish(const GemvParams &p, const Smem &m, int S, int nb, int tid) {
+    constexpr int NW = Cls<CLS>::NW;
+    const bool norm = p.gamma != nullptr;
+    __syncthreads();
+    if (!norm) {
+        if (tid < nb) m.nx[5 * kMaxNb + tid] = 1.f;
+        return;
+    }
+    float tss = 0.f;
+    if (tid < nb) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) tss += m.rbuf[tid * NW + w];
+    }
+    if (S > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        if (tid < nb) m.nx[tid] = tss;
+        cluster.sync();
+        if (tid < nb) {
+            tss = 0.f;
+            for (int rr = 0; rr < S; ++rr) tss += cluster.map_shared_rank(m.nx, rr)[tid];
+        }
+    }
+    if (tid < nb) m.nx[5 * kMaxNb + tid] = 1.0f / sqrtf(tss / (float)p.K + p.eps);
+}
+
+// One activation row whose slice has at most 8192 columns: column pairs
+// through registers, thread t holding pairs t, t + NTH, ...; a block's 32
+// columns are the pairs of 16 lanes.
 template <int FMT, int CLS>
-__device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int S, int tid, int warp, int lane) {
+__device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int tid, int warp, int lane) {
     using C = Cls<CLS>;
     constexpr int NW = C::NW, NTH = NW * 32, GSW = C::GSW;
     constexpr int RP = 8192 / (2 * NTH);
     const int Ks = p.Cs * kChunkK;  // staged columns; those at or beyond ke are zero
     const int kb = q.kb, ke = q.ke;
-    const int xbs = 128;
     const bool norm = p.gamma != nullptr;
     const bool given = FMT == 1 && p.gsum != nullptr && !norm;  // affine sums from the caller
-    const int npass = (Ks / 2 + NTH - 1) / NTH;  // pairs per thread actually used
+    const int npass = (Ks / 2 + NTH - 1) / NTH;                 // pairs per thread actually used
     float2 xv[RP], gv[RP];
-    float ss = 0.f, mx = 0.f;
-    // every load first (guarded, not a loop exit, so that they can all
-    // be in flight together), then the statistics
+    // every load first (guarded, not a loop exit, so that they can all be in
+    // flight together)
 #pragma unroll
     for (int qq = 0; qq < RP; ++qq) {
         float2 v = make_float2(0.f, 0.f), gm = make_float2(1.f, 1.f);
@@ -500,300 +545,182 @@ __device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int
         xv[qq] = v;
         gv[qq] = gm;
     }
-#pragma unroll
-    for (int qq = 0; qq < RP; ++qq) {
-        const float2 v = xv[qq], gm = gv[qq];  // zero beyond npass
-        ss = fmaf(v.x, v.x, ss);
-        ss = fmaf(v.y, v.y, ss);
-        mx = fmaxf(mx, fmaxf(fabsf(norm ? v.x * gm.x : v.x), fabsf(norm ? v.y * gm.y : v.y)));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    }
-    if (lane == 0) {
-        m.rbuf[warp] = ss;
-        m.rbuf[NW + warp] = mx;
-    }
-    __syncthreads();
-    float tss = 0.f, tmx = 0.f;  // every thread adds the warps in the same order
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-        tss += m.rbuf[w];
-        tmx = fmaxf(tmx, m.rbuf[NW + w]);
-    }
-    if (norm && S > 1) {
-        // the RMS needs the whole row: add the slices' sums in rank order
-        cg::cluster_group cluster = cg::this_cluster();
-        if (tid == 0) m.nx[0] = tss;
-        cluster.sync();
-        tss = 0.f;
-        for (int r = 0; r < S; ++r) tss += cluster.map_shared_rank(m.nx, r)[0];
-    }
-    const float inv_rms = norm ? 1.0f / sqrtf(tss / (float)p.K + p.eps) : 1.f;
-    float scale, out_factor;
-    row_scale(tmx * inv_rms, scale, out_factor);
-    if (tid == 0) {
-        m.nx[2 * kMaxNb] = inv_rms;
-        m.nx[3 * kMaxNb] = scale;
-        m.nx[5 * kMaxNb] = out_factor;
-    }
+    float ss = 0.f;
 #pragma unroll
     for (int qq = 0; qq < RP; ++qq) {
         if (qq >= npass) break;
         const int kl = 2 * (tid + qq * NTH);
         // warp-uniform: a warp's pairs are 64 consecutive columns and Ks is a multiple of 128
         if (kl < Ks) {
-            float v0 = xv[qq].x, v1 = xv[qq].y;
+            float a0 = xv[qq].x, a1 = xv[qq].y;
+            ss = fmaf(a0, a0, ss);
+            ss = fmaf(a1, a1, ss);
             if (norm) {
-                v0 = v0 * inv_rms * gv[qq].x;
-                v1 = v1 * inv_rms * gv[qq].y;
+                a0 *= gv[qq].x;
+                a1 *= gv[qq].y;
             }
-            v0 *= scale;
-            v1 *= scale;
-            put_pair<CLS>(m.xs, xbs, 0, kl, v0, v1);
-            if (FMT == 1 && !given) {
-                const float bsum = half_warp_sum(v0 + v1);
-                if ((lane & 15) == 0) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum * 0x1p-20f;
+            float bm = fmaxf(fabsf(a0), fabsf(a1));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+            float sc, back;
+            block_scale(bm, sc, back);
+            put_pair<CLS>(m.xs, 128, 0, kl, a0 * sc, a1 * sc);
+            float bsum = 0.f;
+            if (FMT == 1 && !given) bsum = half_warp_sum(a0 + a1);
+            if ((lane & 15) == 0) {
+                m.fs[gs_idx(kl >> 5, 0, GSW)] = back;
+                if (FMT == 1 && !given) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum;
             }
         }
     }
     if (given) {
-        const float f = scale * 0x1p-20f;
         for (int b = tid; b < p.Cs * kBlocksPerChunk; b += NTH)
-            m.gs[gs_idx(b, 0, GSW)] = kb + 32 * b < ke ? __ldcg(p.gsum + kb / 32 + b) * f : 0.f;
+            m.gs[gs_idx(b, 0, GSW)] = kb + 32 * b < ke ? __ldcg(p.gsum + kb / 32 + b) : 0.f;
+    }
+    if (norm) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) m.rbuf[warp] = ss;
     }
 }
 
-// Stage this CTA's activation slice of job p: per row, scale by a power of
-// two chosen from its largest magnitude (after RMSNorm when gamma is given)
-// and split into f16 hi + lo in B-fragment order (xs_off); then, for the
-// affine format, the block sums: fp32 sums of the scaled values in the order
-// of q4_group_sums (block8_sum), or the caller's group sums.  (Q4_0's offset
-// products are formed in run_units.)
-//
-// One row of at most 8192 columns takes stage_row1.  Otherwise the slice is
-// nb rows x Cs chunks of 128 columns; a segment is one row of
-// one chunk, a float4 per lane.  Warp w takes a contiguous range of segments
-// in row-major order, so it touches few rows: its per-row statistics are
-// summed in registers and reduced once per row, into per-(row, warp)
-// partials.  After one CTA barrier, lane i of each warp adds the partials of
-// the warp's i-th row in warp order (every warp the same way), and the
-// writes take the row's scale from that lane.  Up to SEG segments per warp
-// stay in registers between the statistics and the writes; a longer range is
-// read twice, SEG segments at a time.  Activation loads bypass L1 (.cg): in
-// the persistent kernel another SM may have rewritten them since this SM
-// last read them.
+// Stage this CTA's activation slice of job p.  One row of at most 8192
+// columns takes stage_row1.  Otherwise the slice is nb rows x Cs chunks of
+// 128 columns; a segment is one row of one chunk, a float4 per lane (a
+// block's 32 columns are 8 lanes).  Warp w takes a contiguous range of
+// segments in row-major order, SEG at a time with all their loads in flight.
 template <int FMT, int CLS, int SEG>
 __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S, int tid, int warp, int lane) {
     using C = Cls<CLS>;
     constexpr int NW = C::NW, NTH = NW * 32, GSW = C::GSW;
     const int nb = CLS == 0 ? 1 : p.nb;
     const int Cs = p.Cs;
-    const int kb = q.kb, ke = q.ke;
-    const int xbs = 128 * nb;
-    const bool norm = p.gamma != nullptr;
-    const bool given = FMT == 1 && p.gsum != nullptr && !norm;  // affine sums from the caller
     if (CLS == 0 && Cs * kChunkK <= 8192) {
-        stage_row1<FMT, CLS>(p, q, m, S, tid, warp, lane);
-        __syncthreads();
+        stage_row1<FMT, CLS>(p, q, m, tid, warp, lane);
+        stage_finish<CLS>(p, m, S, 1, tid);
         return;
     }
+    const int kb = q.kb, ke = q.ke;
+    const int xbs = cls_xrow(CLS) * nb;
+    const bool norm = p.gamma != nullptr;
+    const bool given = FMT == 1 && p.gsum != nullptr && !norm;  // affine sums from the caller
     const int nseg = nb * Cs;
     const int spw = (nseg + NW - 1) / NW;
     const int s0 = min(warp * spw, nseg), s1 = min(s0 + spw, nseg);
     const int r0 = CLS == 0 ? 0 : s0 / Cs, c0 = s0 - r0 * Cs;  // row and chunk of this warp's first segment
-    const bool held = s1 - s0 <= SEG;                          // the whole range stays in registers
 
-    // this warp's partials start at zero for every row (neutral for the sum
-    // and the max); the flushes below overwrite the rows it touches
-    float *part = m.rbuf;  // [2][nb][NW]
-    if (lane < nb) {
-        part[lane * NW + warp] = 0.f;
-        part[(nb + lane) * NW + warp] = 0.f;
-    }
+    // with gamma: this warp's partial sums of squares, [nb][NW], zero for
+    // every row until a flush below overwrites the rows it touches
+    float *part = m.rbuf;
+    if (norm && lane < nb) part[lane * NW + warp] = 0.f;
     __syncwarp();
+    float ss = 0.f;
+    int rcur = r0;
 
-    float4 xv[SEG];
-    // the batch of SEG segments from `base` (row rb, chunk cb); loads are
-    // predicated, not branched around, so that they are all in flight
-    // together; segments past the warp's range read as zeros
-    auto load_batch = [&](int base, int rb, int cb) {
+    const float f16x = (lane & 2) ? 1.f : 16.f;
+    constexpr int LO = 64, P2 = 16;  // lo part (nb <= 4), second column pair
+    const int lane_off = (lane >> 3) * xbs + (lane & 1) * 32 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4;
+    int rb = r0, cb = c0;
+    for (int base = s0; base < s1; base += SEG) {
+        // the batch's loads are predicated, not branched around, so that they
+        // are all in flight together; segments past the range read as zeros
+        float4 xv[SEG], gv[SEG];
+        {
+            int r = rb, c = cb;
+#pragma unroll
+            for (int j = 0; j < SEG; ++j) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f), g = make_float4(1.f, 1.f, 1.f, 1.f);
+                const int k = kb + 128 * c + 4 * lane;
+                if (base + j < s1 && k < ke) {
+                    v = __ldcg(reinterpret_cast<const float4 *>(p.x + (size_t)r * p.K + k));
+                    if (norm) g = __ldg(reinterpret_cast<const float4 *>(p.gamma + k));
+                }
+                xv[j] = v;
+                gv[j] = g;
+                if (++c == Cs) {
+                    c = 0;
+                    ++r;
+                }
+            }
+        }
         int r = rb, c = cb;
 #pragma unroll
         for (int j = 0; j < SEG; ++j) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            const int k = kb + 128 * c + 4 * lane;
-            if (base + j < s1 && k < ke) v = __ldcg(reinterpret_cast<const float4 *>(p.x + (size_t)r * p.K + k));
-            xv[j] = v;
+            const bool valid = base + j < s1;  // warp-uniform
+            if (norm && valid && r != rcur) {  // a new row: this warp's sum for the previous one
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (lane == 0) part[rcur * NW + warp] = ss;
+                ss = 0.f;
+                rcur = r;
+            }
+            const int kl = 128 * c + 4 * lane;
+            const float4 v = xv[j];
+            float4 a = v;
+            if (norm) {
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss);
+                ss = fmaf(v.w, v.w, ss);
+                a.x *= gv[j].x;
+                a.y *= gv[j].y;
+                a.z *= gv[j].z;
+                a.w *= gv[j].w;
+            }
+            float bm = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w)));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+            float sc, back;
+            block_scale(bm, sc, back);
+            const float f = sc * f16x;
+            const __half2 h0 = __floats2half2_rn(a.x * f, a.y * f);
+            const __half2 h1 = __floats2half2_rn(a.z * f, a.w * f);
+            __half2 l0 = h0, l1 = h1;
+            if (C::HLN) {
+                const float2 b0 = __half22float2(h0), b1 = __half22float2(h1);
+                l0 = __floats2half2_rn(a.x * f - b0.x, a.y * f - b0.y);
+                l1 = __floats2half2_rn(a.z * f - b1.x, a.w * f - b1.y);
+            }
+            float bsum = 0.f;
+            if (FMT == 1 && !given) bsum = block8_sum(a);
+            if (valid) {
+                const int seg = C::HLN ? 4 * c * xbs + 128 * r : 4 * c * xbs + (r >> 3) * 512 + (r & 7) * 64;
+                uint8_t *d = m.xs + seg + lane_off;
+                *reinterpret_cast<__half2 *>(d) = h0;
+                *reinterpret_cast<__half2 *>(d + P2) = h1;
+                if (C::HLN) {
+                    *reinterpret_cast<__half2 *>(d + LO) = l0;
+                    *reinterpret_cast<__half2 *>(d + P2 + LO) = l1;
+                }
+                if ((lane & 7) == 0) {
+                    m.fs[gs_idx(kl >> 5, r, GSW)] = back;
+                    if (FMT == 1 && !given) m.gs[gs_idx(kl >> 5, r, GSW)] = bsum;
+                }
+            }
             if (++c == Cs) {
                 c = 0;
                 ++r;
             }
         }
-    };
-
-    // ---- per-row statistics: sum of squares and largest |x (* gamma)|
-    float ss = 0.f, mx = 0.f;
-    int rcur = r0;
-    auto flush = [&]() {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        }
-        if (lane == 0) {
-            part[rcur * NW + warp] = ss;
-            part[(nb + rcur) * NW + warp] = mx;
-        }
-        ss = 0.f;
-        mx = 0.f;
-    };
-    {
-        int rb = r0, cb = c0;
-        for (int base = s0; base < s1; base += SEG) {
-            load_batch(base, rb, cb);
-            int r = rb, c = cb;
-#pragma unroll
-            for (int j = 0; j < SEG; ++j) {
-                if (CLS != 0 && base + j < s1 && r != rcur) {  // warp-uniform: a new row
-                    flush();
-                    rcur = r;
-                }
-                const float4 v = xv[j];  // zero past the range: neutral
-                ss = fmaf(v.x, v.x, ss);
-                ss = fmaf(v.y, v.y, ss);
-                ss = fmaf(v.z, v.z, ss);
-                ss = fmaf(v.w, v.w, ss);
-                float4 a = v;
-                const int k = kb + 128 * c + 4 * lane;
-                if (norm && base + j < s1 && k < ke) {
-                    const float4 g = __ldg(reinterpret_cast<const float4 *>(p.gamma + k));
-                    a.x *= g.x;
-                    a.y *= g.y;
-                    a.z *= g.z;
-                    a.w *= g.w;
-                }
-                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
-                if (++c == Cs) {
-                    c = 0;
-                    ++r;
-                }
-            }
-            rb = r;
-            cb = c;
-        }
-        if (s0 < s1) flush();
+        rb = r;
+        cb = c;
     }
-    __syncthreads();
-
-    // row r's inverse RMS and scales from the warps' partials in warp order
-    // (and, for a split RMSNorm, the cluster ranks' slice sums in rank order)
-    auto row_stats = [&](int r, float &ir, float &sc, float &of) {
-        float tss = 0.f, tmx = 0.f;
+    if (norm && s0 < s1) {
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            tss += part[r * NW + w];
-            tmx = fmaxf(tmx, part[(nb + r) * NW + w]);
-        }
-        if (norm && S > 1) {
-            cg::cluster_group cluster = cg::this_cluster();
-            tss = 0.f;
-            for (int rr = 0; rr < S; ++rr) tss += cluster.map_shared_rank(m.nx, rr)[r];
-        }
-        ir = norm ? 1.0f / sqrtf(tss / (float)p.K + p.eps) : 1.f;
-        row_scale(tmx * ir, sc, of);
-    };
-    if (norm && S > 1) {
-        // the RMS needs the whole row: publish this slice's sums, then every
-        // rank reads all of them
-        if (tid < nb) {
-            float tss = 0.f;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) tss += part[tid * NW + w];
-            m.nx[tid] = tss;
-        }
-        cg::this_cluster().sync();
-    }
-    if (tid < nb) {  // for the epilogue (read after later barriers)
-        float ir, sc, of;
-        row_stats(tid, ir, sc, of);
-        m.nx[2 * kMaxNb + tid] = ir;
-        m.nx[3 * kMaxNb + tid] = sc;
-        m.nx[5 * kMaxNb + tid] = of;
-    }
-    const int nr = s1 > s0 ? (s1 - 1) / Cs - r0 + 1 : 0;  // rows this warp touches
-    float l_ir = 1.f, l_sc = 1.f;
-    if (lane < nr) {
-        float of;
-        row_stats(r0 + lane, l_ir, l_sc, of);
-    }
-
-    // ---- the writes: x (* inv_rms * gamma) * scale as f16 hi + lo; the
-    // first 8 of every 16 columns carry an extra factor 16 (see unpack_word)
-    const float f16x = (lane & 2) ? 1.f : 16.f;
-    constexpr int LO = C::HLN ? 64 : 8, P2 = C::HLN ? 16 : 32;  // lo part, second pair
-    const int lane_off = C::HLN ? (lane >> 3) * xbs + (lane & 1) * 32 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4
-                                : (lane >> 3) * xbs + (lane & 1) * 64 + ((lane >> 2) & 1) * 16 + ((lane >> 1) & 1) * 4;
-    {
-        int rb = r0, cb = c0;
-        for (int base = s0; base < s1; base += SEG) {
-            if (!held) load_batch(base, rb, cb);
-            int r = rb, c = cb;
-#pragma unroll
-            for (int j = 0; j < SEG; ++j) {
-                const bool valid = base + j < s1;  // warp-uniform
-                const int kl = 128 * c + 4 * lane, k = kb + kl;
-                const float ir = __shfl_sync(0xffffffffu, l_ir, r - r0);
-                const float sc = __shfl_sync(0xffffffffu, l_sc, r - r0);
-                float4 v = xv[j];
-                if (norm) {
-                    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (valid && k < ke) g = __ldg(reinterpret_cast<const float4 *>(p.gamma + k));
-                    v.x = v.x * ir * g.x;
-                    v.y = v.y * ir * g.y;
-                    v.z = v.z * ir * g.z;
-                    v.w = v.w * ir * g.w;
-                }
-                const float f = sc * f16x;
-                const __half2 h0 = __floats2half2_rn(v.x * f, v.y * f);
-                const __half2 h1 = __floats2half2_rn(v.z * f, v.w * f);
-                const float2 b0 = __half22float2(h0), b1 = __half22float2(h1);
-                const __half2 l0 = __floats2half2_rn(v.x * f - b0.x, v.y * f - b0.y);
-                const __half2 l1 = __floats2half2_rn(v.z * f - b1.x, v.w * f - b1.y);
-                float bsum = 0.f;
-                if (FMT == 1 && !given) bsum = block8_sum(v);  // sum of scaled values = sc * this
-                if (valid) {
-                    const int seg = C::HLN ? 4 * c * xbs + 128 * r : 4 * c * xbs + (r >> 3) * 1024 + (r & 7) * 128;
-                    uint8_t *d = m.xs + seg + lane_off;
-                    *reinterpret_cast<__half2 *>(d) = h0;
-                    *reinterpret_cast<__half2 *>(d + LO) = l0;
-                    *reinterpret_cast<__half2 *>(d + P2) = h1;
-                    *reinterpret_cast<__half2 *>(d + P2 + LO) = l1;
-                    if (FMT == 1 && !given && (lane & 7) == 0)
-                        m.gs[gs_idx(kl >> 5, r, GSW)] = bsum * (sc * 0x1p-20f);
-                }
-                if (++c == Cs) {
-                    c = 0;
-                    ++r;
-                }
-            }
-            rb = r;
-            cb = c;
-        }
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) part[rcur * NW + warp] = ss;
     }
     if (given) {
-        __syncthreads();  // the row scales in nx
         const int nblk = Cs * kBlocksPerChunk;
         for (int i = tid; i < nb * nblk; i += NTH) {
             const int r = i / nblk, b = i - r * nblk;
-            const float f = m.nx[3 * kMaxNb + r] * 0x1p-20f;
-            m.gs[gs_idx(b, r, GSW)] =
-                kb + 32 * b < ke ? __ldcg(p.gsum + (size_t)r * (p.K / 32) + kb / 32 + b) * f : 0.f;
+            m.gs[gs_idx(b, r, GSW)] = kb + 32 * b < ke ? __ldcg(p.gsum + (size_t)r * (p.K / 32) + kb / 32 + b) : 0.f;
         }
     }
-    __syncthreads();
+    stage_finish<CLS>(p, m, S, nb, tid);
 }
 
 template <int I>
@@ -816,11 +743,10 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                           RingOf<FMT, CLS> &ring, int warp, int lane) {
     using C = Cls<CLS>;
     constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
-    constexpr int UREC = 2 * REC;
     constexpr int NT = C::NT, NGR = C::NGR, NACC = C::NACC;
     const int g = lane >> 2, t = lane & 3;
     const int nb = CLS == 0 ? 1 : p.nb;
-    const int xbs = 128 * nb;
+    const int xbs = cls_xrow(CLS) * nb;
     const int cs = q.cs;
     // this lane's B-fragment slot in a block (lanes past the batch read a
     // duplicate column: their outputs are never stored)
@@ -831,7 +757,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             boff[nt] = ((g % (2 * nb)) * 4 + t) * 16;
         } else {
             const int cnt = min(8, nb - 8 * nt);
-            boff[nt] = nt * 1024 + ((g % cnt) * 4 + t) * 32;
+            boff[nt] = nt * 512 + ((g % cnt) * 4 + t) * 16;
         }
     }
     int grow[NGR];  // this lane's offset-sum rows
@@ -894,12 +820,18 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
         // unit su of the stage: its record(s) at st_base + su*REC (and + SU*REC)
         const uint32_t st_a = st_base + su * REC;
         const bool two = upt == 2 && q.t0 + 2 * pl + 1 < p.T;
-        // affine: the staged group sums of the chunk's four blocks (Q4_0 forms
-        // its offset products per block below)
-        float G[NGR][4];
-        if (FMT == 1) {
+        // the chunk's four block factors of this lane's activation rows, and
+        // for the affine format their block sums (Q4_0 forms its offset
+        // products per block below)
+        float G[NGR][4], F[NGR][4];
 #pragma unroll
-            for (int j = 0; j < NGR; ++j) {
+        for (int j = 0; j < NGR; ++j) {
+            const float4 fv = *reinterpret_cast<const float4 *>(m.fs + (cc * C::GSW + grow[j]) * 4);
+            F[j][0] = fv.x;
+            F[j][1] = fv.y;
+            F[j][2] = fv.z;
+            F[j][3] = fv.w;
+            if (FMT == 1) {
                 const float4 gv = *reinterpret_cast<const float4 *>(m.gs + (cc * C::GSW + grow[j]) * 4);
                 G[j][0] = gv.x;
                 G[j][1] = gv.y;
@@ -925,12 +857,9 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
         auto block = [&](auto blk_c) {
             constexpr int blk = decltype(blk_c)::value;
             const uint8_t *xa = xchunk + blk * xbs;
-            uint4 B[NT][2];
+            uint4 B[NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                B[nt][0] = *reinterpret_cast<const uint4 *>(xa + boff[nt]);
-                if (!C::HLN) B[nt][1] = *reinterpret_cast<const uint4 *>(xa + boff[nt] + 16);
-            }
+            for (int nt = 0; nt < NT; ++nt) B[nt] = *reinterpret_cast<const uint4 *>(xa + boff[nt]);
             if (FMT == 0) {
                 // the block's offset product: the same tensor-core chain as the
                 // weights' below, with every nibble 8 (exactly what a block of
@@ -938,15 +867,11 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     float e[4];
+                    mma16816_c(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt].x, B[nt].y, z, z, z, z);
+                    mma16816(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt].z, B[nt].w);
                     if (C::HLN) {
-                        mma16816_c(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][0].x, B[nt][0].y, z, z, z, z);
-                        mma16816(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][0].z, B[nt][0].w);
                         G[0][blk] = e[0] + e[1];
                     } else {
-                        mma16816_c(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][0].x, B[nt][0].y, z, z, z, z);
-                        mma16816(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][0].z, B[nt][0].w);
-                        mma16816(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][1].x, B[nt][1].y);
-                        mma16816(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt][1].z, B[nt][1].w);
                         G[2 * nt][blk] = e[0];
                         G[2 * nt + 1][blk] = e[1];
                     }
@@ -966,25 +891,24 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                     float d[4];
                     if (C::HLN) {
                         // columns (2t, 2t+1) = (hi, lo) of activation row t
-                        mma16816_c(d, a[0], a[1], a[2], a[3], B[nt][0].x, B[nt][0].y, z, z, z, z);
-                        mma16816(d, a[4], a[5], a[6], a[7], B[nt][0].z, B[nt][0].w);
+                        mma16816_c(d, a[0], a[1], a[2], a[3], B[nt].x, B[nt].y, z, z, z, z);
+                        mma16816(d, a[4], a[5], a[6], a[7], B[nt].z, B[nt].w);
                         const float T0 = d[0] + d[1], T2 = d[2] + d[3];
+                        const float fb = F[0][blk];
                         if (FMT == 0) {
-                            acc[rc][0] = fmaf(s2.x, T0 - G[0][blk], acc[rc][0]);
-                            acc[rc][1] = fmaf(s2.y, T2 - G[0][blk], acc[rc][1]);
+                            acc[rc][0] = fmaf(s2.x * fb, T0 - G[0][blk], acc[rc][0]);
+                            acc[rc][1] = fmaf(s2.y * fb, T2 - G[0][blk], acc[rc][1]);
                         } else {
-                            acc[rc][0] = fmaf(m2.x, G[0][blk], fmaf(s2.x, T0, acc[rc][0]));
-                            acc[rc][1] = fmaf(m2.y, G[0][blk], fmaf(s2.y, T2, acc[rc][1]));
+                            acc[rc][0] = fmaf(m2.x, G[0][blk], fmaf(s2.x * fb, T0, acc[rc][0]));
+                            acc[rc][1] = fmaf(m2.y, G[0][blk], fmaf(s2.y * fb, T2, acc[rc][1]));
                         }
                     } else {
-                        // columns (2t, 2t+1) = activation rows 8nt+2t, 8nt+2t+1; hi, lo as k-steps
-                        mma16816_c(d, a[0], a[1], a[2], a[3], B[nt][0].x, B[nt][0].y, z, z, z, z);
-                        mma16816(d, a[0], a[1], a[2], a[3], B[nt][0].z, B[nt][0].w);
-                        mma16816(d, a[4], a[5], a[6], a[7], B[nt][1].x, B[nt][1].y);
-                        mma16816(d, a[4], a[5], a[6], a[7], B[nt][1].z, B[nt][1].w);
+                        // columns (2t, 2t+1) = activation rows 8nt+2t, 8nt+2t+1
+                        mma16816_c(d, a[0], a[1], a[2], a[3], B[nt].x, B[nt].y, z, z, z, z);
+                        mma16816(d, a[4], a[5], a[6], a[7], B[nt].z, B[nt].w);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const float sj = j < 2 ? s2.x : s2.y;
+                            const float sj = (j < 2 ? s2.x : s2.y) * F[2 * nt + (j & 1)][blk];
                             const float gj = G[2 * nt + (j & 1)][blk];
                             float &ac = acc[rc][4 * nt + j];
                             if (FMT == 0) {
@@ -1312,7 +1236,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid
     for (int s = 0; s < C::DU - 1; ++s) ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    stage_x<FMT, CLS, CLS == 0 ? 4 : CLS == 3 ? 16 : 8>(p, q, m, S, tid, warp, lane);
+    stage_x<FMT, CLS, CLS == 0 ? 4 : 8>(p, q, m, S, tid, warp, lane);
     run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
     ring.drain();
     __syncthreads();
@@ -1397,7 +1321,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
         }
         const Geo q = make_geo<NW>(p, group, 0, warp);
         if (q.tiles_here == 0) continue;  // no work in this job (CTA-uniform)
-        stage_x<FMT, CLS, 2>(p, q, m, 1, tid, warp, lane);
+        stage_x<FMT, CLS, 4>(p, q, m, 1, tid, warp, lane);
         run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
         __syncthreads();
         if (p.epi != EPI_ARGMAX) {

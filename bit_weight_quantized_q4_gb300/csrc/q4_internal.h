@@ -71,6 +71,9 @@ Q4_HD constexpr int cls_warps(int c) { return c == 3 ? 8 : 16; }     // warps pe
 Q4_HD constexpr int cls_depth(int c) { return (void)c, 2; }  // ring stages per warp
 Q4_HD constexpr int cls_stage(int c) { return c == 2 ? 1 : 2; }  // pair units per stage (2x as many single-tile units)
 Q4_HD constexpr int cls_gsw(int c) { return c <= 1 ? 4 : c == 2 ? 8 : 16; }  // group-sum rows per chunk
+// bytes of one activation row per 32-column block in shared memory: f16 hi
+// and lo parts for nb <= 4, the f16 value alone for larger batches
+Q4_HD constexpr int cls_xrow(int c) { return c <= 1 ? 128 : 64; }
 
 // A unit of work is one 128-column chunk of upt consecutive 16-row tiles
 // (upt records).  upt is 2 -- a tile pair (2p, 2p+1), for gate/up jobs
@@ -152,8 +155,8 @@ __device__ __forceinline__ float half_warp_sum(float v) {
 inline size_t engine_smem(int fmt, int nb, int TG, int Cs, int SW, int S) {
     const int c = cls_of(nb);
     const size_t NW = (size_t)cls_warps(c);
-    const size_t xs = (size_t)512 * nb * Cs;
-    const size_t gs = (size_t)16 * cls_gsw(c) * Cs;
+    const size_t xs = (size_t)4 * cls_xrow(c) * nb * Cs;
+    const size_t gs = (size_t)2 * 16 * cls_gsw(c) * Cs;  // block sums and block factors
     const size_t red = S > 1 ? (size_t)64 * TG * nb : 0;
     const size_t slots = (size_t)64 * NW * SW * nb;
     const size_t misc = (size_t)16 * NW * kMaxNb + 32 * kMaxNb + 8 * NW * cls_depth(c);  // + ring barriers
@@ -212,7 +215,7 @@ inline Plan make_plan(int fmt, int T, int C, int nb, bool pairs, int num_sms) {
     for (int S = 1; S <= kMaxCluster; S *= 2) {
         if (S > 1 && S > C) break;
         const int Cs = (C + S - 1) / S;
-        if ((size_t)512 * nb * Cs > kXsCap && S < kMaxCluster) continue;
+        if ((size_t)4 * cls_xrow(cls_of(nb)) * nb * Cs > kXsCap && S < kMaxCluster) continue;
         int G0 = num_sms / S;
         if (G0 < 1) G0 = 1;
         int upt = 2;

@@ -93,8 +93,10 @@ def test_plan_invariants(fmt, tiles, chunks, pairs, nb):
     assert p["smem"] <= 227 * 1024
     if pairs:
         assert p["TG"] % 2 == 0
-    # the activation slice fits the staging budget
-    assert 4 * nb * p["Cs"] * 128 <= 64 * 1024 or p["S"] == 8
+    # the activation slice fits the staging budget: f16 hi + lo parts (4 bytes
+    # a value) for nb <= 4, the f16 value alone (2 bytes) for larger batches
+    bytes_per_value = 4 if nb <= 4 else 2
+    assert bytes_per_value * nb * p["Cs"] * 128 <= 64 * 1024 or p["S"] == 8
 
 
 def test_plan_rejects_bad_arguments():
