@@ -402,7 +402,7 @@ struct Smem {
     uint8_t *xs;     // activation slice, hi/lo f16 in mma B-fragment order
     float *gs;       // affine block sums of x (* gamma) [chunk][GSW rows][4 blocks]
     float *fs;       // block factors back to the input's units (times 2^20), same shape
-    float *red;      // cluster fold (S > 1): CTA results [TG][16][nb]
+    float *red;      // cluster fold (S > 1): partials pushed by each rank [S][slice]
     float *slots;    // per-warp tile partials [warp][SW][16][nb]
     float *rbuf;     // reductions [4][warp][kMaxNb]
     float *nx;       // row stats [8][kMaxNb]: 2 inv_rms, 3 scale, 5 output factor
@@ -419,7 +419,7 @@ __device__ __forceinline__ Smem carve(uint8_t *smem, int nb, int Cs, int TG, int
     m.gs = reinterpret_cast<float *>(smem + (size_t)4 * cls_xrow(CLS) * nb * Cs);
     m.fs = m.gs + (size_t)4 * C::GSW * Cs;
     m.red = m.fs + (size_t)4 * C::GSW * Cs;
-    m.slots = m.red + (S > 1 ? (size_t)TG * kTileRows * nb : 0);
+    m.slots = m.red + (S > 1 ? (size_t)(TG + 2 * S) * kTileRows * nb : 0);
     m.rbuf = m.slots + (size_t)C::NW * SW * kTileRows * nb;
     m.nx = m.rbuf + 4 * C::NW * kMaxNb;
     m.wtab = reinterpret_cast<int *>(m.rbuf + 3 * C::NW * kMaxNb);
@@ -497,6 +497,9 @@ __device__ void stage_finish(const GemvParams &p, const Smem &m, int S, int nb, 
     constexpr int NW = Cls<CLS>::NW;
     const bool norm = p.gamma != nullptr;
     __syncthreads();
+    // every CTA of the cluster has started (the kernel's first arrive): from
+    // here on the ranks may access each other's shared memory
+    if (S > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     if (!norm) {
         if (tid < nb) m.nx[5 * kMaxNb + tid] = 1.f;
         return;
@@ -983,6 +986,13 @@ __device__ void cluster_finish(const GemvParams &p, const Geo &q, const Smem &m,
     const int nb = CLS == 0 ? 1 : p.nb;
     const int tile_vals = kTileRows * nb;
     const int total = q.tiles_here * tile_vals;
+    // rank j finishes units [j*nu/S, (j+1)*nu/S): whole tiles (whole gate/up
+    // pairs for SwiGLU).  Every rank pushes its partials of a unit into the
+    // owner's shared memory, at red[source rank][position in the slice]
+    const int tpu = p.epi == EPI_SWIGLU ? 2 : 1;
+    const int nu = q.tiles_here / tpu, uv = tpu * tile_vals;
+    const int L = (nu + S - 1) / S * uv;  // the longest slice
+    cg::cluster_group cluster = cg::this_cluster();
     {
         WarpTable<NW> wt;
         wt.load(m.wtab);
@@ -990,34 +1000,28 @@ __device__ void cluster_finish(const GemvParams &p, const Geo &q, const Smem &m,
             const int tl = idx / tile_vals;
             const int rem = idx - tl * tile_vals;
             const int row = rem / nb, r = rem - row * nb;
-            m.red[idx] = fold_one<CLS>(p, q, m, wt, tl, row, r, nb) * m.nx[5 * kMaxNb + r];
+            const float v = fold_one<CLS>(p, q, m, wt, tl, row, r, nb) * m.nx[5 * kMaxNb + r];
+            const int j = ((tl / tpu + 1) * S - 1) / nu;  // the owner of unit tl / tpu
+            *cluster.map_shared_rank(m.red + rank * L + idx - (j * nu / S) * uv, j) = v;
         }
     }
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    // this rank's slice: whole tiles (whole gate/up pairs for SwiGLU)
-    const int tpu = p.epi == EPI_SWIGLU ? 2 : 1;
-    const int nu = q.tiles_here / tpu;
-    const int i0 = (rank * nu / S) * tpu * tile_vals, i1 = ((rank + 1) * nu / S) * tpu * tile_vals;
-    float *reds[kMaxCluster];
-#pragma unroll
-    for (int rr = 0; rr < kMaxCluster; ++rr) reds[rr] = rr < S ? cluster.map_shared_rank(m.red, rr) : nullptr;
-    // (no other rank reads this rank's slice, so it is overwritten in place)
-    for (int idx = i0 + tid; idx < i1; idx += NTH) {
+    cluster.sync();  // every partial is in its owner's shared memory
+    const int i0 = (rank * nu / S) * uv, i1 = ((rank + 1) * nu / S) * uv;
+    // this rank's slice: the sources in rank order (the sum replaces source
+    // 0's entry, which only this thread reads)
+    for (int i = tid; i < i1 - i0; i += NTH) {
         float v = 0.f;
-#pragma unroll
-        for (int rr = 0; rr < kMaxCluster; ++rr)
-            if (rr < S) v += reds[rr][idx];
-        m.red[idx] = v;
+        for (int rr = 0; rr < S; ++rr) v += m.red[rr * L + i];
+        m.red[i] = v;
     }
     __syncthreads();
     if (group < p.groups) {
         if (p.epi == EPI_ARGMAX) {
             const int N = p.n[0];
-            float *bvs = m.rbuf;  // [warp], then this rank's pairs [nb] at rbuf + 2*NW
+            float *bvs = m.rbuf;  // [warp], then every rank's pairs [S][kMaxNb] (rank 0's copy is read)
             int *bis = reinterpret_cast<int *>(m.rbuf + NW);
             float *rv = m.rbuf + 2 * NW;
-            int *ri_ = reinterpret_cast<int *>(m.rbuf + 2 * NW + kMaxNb);
+            int *ri_ = reinterpret_cast<int *>(m.rbuf + 2 * NW + kMaxCluster * kMaxNb);
             const int row0 = i0 / nb, row1 = i1 / nb;  // rows (tile * 16 + row) of the slice
             for (int r = 0; r < nb; ++r) {
                 float bv = -INFINITY;
@@ -1025,7 +1029,7 @@ __device__ void cluster_finish(const GemvParams &p, const Geo &q, const Smem &m,
                 for (int ri = row0 + tid; ri < row1; ri += NTH) {
                     const int n = (q.t0 + ri / kTileRows) * kTileRows + (ri % kTileRows);
                     if (n >= N) continue;
-                    const float v = m.red[ri * nb + r];
+                    const float v = m.red[ri * nb + r - i0];
                     if (p.out[0] != nullptr) p.out[0][(size_t)r * N + n] = v;
                     am_take(bv, bi, v, n);
                 }
@@ -1044,18 +1048,18 @@ __device__ void cluster_finish(const GemvParams &p, const Geo &q, const Smem &m,
                             fi = bis[w];
                         }
                     }
-                    rv[r] = fv;
-                    ri_[r] = fi;
+                    *cluster.map_shared_rank(rv + rank * kMaxNb + r, 0) = fv;
+                    *cluster.map_shared_rank(ri_ + rank * kMaxNb + r, 0) = fi;
                 }
                 __syncthreads();
             }
-            cluster.sync();  // every rank's pairs are in its shared memory
+            cluster.sync();  // every rank's pairs are in rank 0's shared memory
             if (rank == 0 && tid < nb) {
                 float fv = -INFINITY;
                 int fi = 0x7fffffff;
                 for (int rr = 0; rr < S; ++rr) {
-                    const float v = cluster.map_shared_rank(rv, rr)[tid];
-                    const int k = cluster.map_shared_rank(ri_, rr)[tid];
+                    const float v = rv[rr * kMaxNb + tid];
+                    const int k = ri_[rr * kMaxNb + tid];
                     if (v > fv || (v == fv && k < fi)) {
                         fv = v;
                         fi = k;
@@ -1074,19 +1078,18 @@ __device__ void cluster_finish(const GemvParams &p, const Geo &q, const Smem &m,
                 const int n = tm * kTileRows + row;
                 const int N = p.n[mi];
                 if (n >= N) continue;
-                const float v = m.red[idx];
+                const float v = m.red[idx - i0];
                 if (p.epi == EPI_STORE) {
                     p.out[mi][(size_t)r * N + n] = v;
                 } else if (p.epi == EPI_RESIDUAL) {
                     p.out[0][(size_t)r * N + n] = v + __ldcg(p.res + (size_t)r * N + n);
                 } else if (mi == 0) {  // EPI_SWIGLU: gate tile tl, up tile tl + 1 (same slice)
-                    const float u = m.red[idx + tile_vals];
+                    const float u = m.red[idx - i0 + tile_vals];
                     p.out[0][(size_t)r * N + n] = v / (1.0f + expf(-v)) * u;
                 }
             }
         }
     }
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // Write the job's outputs: store, residual add, SwiGLU over a gate/up tile
@@ -1225,6 +1228,8 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid
     const Smem m = carve<CLS>(smem, nb, p.Cs, p.TG, p.SW, S);
     RingOf<FMT, CLS> ring;
     ring.init(smem_u32(m.ring) + warp * C::DU * 2 * C::SU * REC, smem_u32(m.bars) + warp * C::DU * 8, lane);
+    // this CTA has started; the matching wait ends the activation staging
+    if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     // the next kernel may launch now; it waits for this one before it reads
     // what this one writes

@@ -157,7 +157,7 @@ inline size_t engine_smem(int fmt, int nb, int TG, int Cs, int SW, int S) {
     const size_t NW = (size_t)cls_warps(c);
     const size_t xs = (size_t)4 * cls_xrow(c) * nb * Cs;
     const size_t gs = (size_t)2 * 16 * cls_gsw(c) * Cs;  // block sums and block factors
-    const size_t red = S > 1 ? (size_t)64 * TG * nb : 0;
+    const size_t red = S > 1 ? (size_t)64 * (TG + 2 * S) * nb : 0;  // S slices of at most TG / S + 2 tiles
     const size_t slots = (size_t)64 * NW * SW * nb;
     const size_t misc = (size_t)16 * NW * kMaxNb + 32 * kMaxNb + 8 * NW * cls_depth(c);  // + ring barriers
     const size_t ring = NW * cls_depth(c) * 2 * cls_stage(c) * rec_bytes(fmt);
