@@ -508,7 +508,7 @@ def run_ours(args, rank, world, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "precision": "Q4_0 weights dequantised exactly to f16; activations as f16 hi+lo pairs; fp32 accumulate",
+        "precision": "Q4_0 nibbles exact in f16; activations scaled per 32-column block by a power of two and split into f16 hi+lo; fp32 accumulate",
         "data": "synthetic (seeded PCG64; q~U{0..15}, d~U[0.005,0.02] fp16, x~N(0,1), gamma=1+0.1N(0,1))",
         "config": {"workload": WORKLOAD, "layers": args.layers, "nb": 1, "kernels_per_step": 1,
                    "weight_bytes_per_step": wbytes,

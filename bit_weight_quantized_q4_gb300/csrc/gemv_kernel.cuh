@@ -17,18 +17,20 @@
 //    rank order (deterministic, no atomics).
 //  * The unit of work is one 128-column chunk of a tile pair: two weight
 //    records that share one set of activation fragments.  Each warp streams
-//    its contiguous range of units through a private shared-memory ring with
-//    16-byte cp.async copies, two or three units ahead of its compute.
+//    its contiguous range of units through a private two-stage shared-memory
+//    ring filled by TMA bulk copies on mbarriers, a stage ahead of its
+//    compute.
 //  * A nibble masked in place is an exact f16 subnormal (q * 2^-24, or
 //    q * 2^-20 for the upper nibble of a byte), so a 32-bit word of eight
 //    nibbles becomes four tensor-core A registers with one shift and four
 //    ANDs.  The activation operand carries the factor 16 at the positions
 //    of the lower nibbles, and products land in units of 2^-20.
-//  * Activations are staged once per CTA in shared memory as an exact
-//    power-of-two-scaled hi + lo pair of f16 values (about 22 significant
-//    bits) in mma B-fragment order.  For nb <= 4 the hi and lo halves of a
-//    row are two n columns of one product (two mma per 32-weight block); for
-//    nb > 4 they are two k-steps into one accumulator.
+//  * Activations are staged once per CTA in shared memory in mma B-fragment
+//    order, each 32-column block scaled by its own power of two: as an f16
+//    hi + lo pair (about 22 significant bits) for nb <= 4, where hi and lo
+//    of a row are two n columns of one product, and as one f16 for nb > 4.
+//    The block's factor back to the input's units multiplies its weight
+//    scale.
 //  * mma.sync m16n8k16 (f16 in, fp32 accumulate) forms the per-block dot
 //    products.  The block's offset term (the -8 of Q4_0, the min m of the
 //    affine format) multiplies the block's activation sum: for Q4_0 that sum
@@ -399,7 +401,7 @@ struct Ring {
 
 // Shared-memory regions of one CTA (sizes: engine_smem()).
 struct Smem {
-    uint8_t *xs;     // activation slice, hi/lo f16 in mma B-fragment order
+    uint8_t *xs;     // activation slice, f16 (hi + lo for nb <= 4) in mma B-fragment order
     float *gs;       // affine block sums of x (* gamma) [chunk][GSW rows][4 blocks]
     float *fs;       // block factors back to the input's units (times 2^20), same shape
     float *red;      // cluster fold (S > 1): partials pushed by each rank [S][slice]
