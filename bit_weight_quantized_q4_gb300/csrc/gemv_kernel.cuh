@@ -216,9 +216,10 @@ struct Geo {
     int U, ub, ue, n_my, fp;     // units of the CTA; this warp's [ub, ue) and its first pair
 };
 
-template <int NW>
-__device__ __forceinline__ Geo make_geo(const GemvParams &p, int group, int rank, int warp) {
-    Geo q;
+// The group's span of a job: balanced contiguous ranges of the job's
+// P = T / upt units (pairs, or single tiles).
+__device__ __forceinline__ JobSpan span_of(const GemvParams &p, int group) {
+    JobSpan sp;
     const int P = (p.T + p.upt - 1) / p.upt;  // units of upt tiles
     int p0 = 0, p1 = 0;
     if (group < p.groups) {  // a job with fewer units than CTAs leaves the rest without work
@@ -230,9 +231,28 @@ __device__ __forceinline__ Geo make_geo(const GemvParams &p, int group, int rank
             p1 = (int)((unsigned long long)(group + 1) * P / p.groups);
         }
     }
-    q.np = p1 - p0;
-    q.t0 = p.upt * p0;
-    q.tiles_here = min(p.upt * q.np, p.T - q.t0);
+    sp.np = p1 - p0;
+    sp.t0 = p.upt * p0;
+    sp.tiles = min(p.upt * sp.np, p.T - sp.t0);
+    sp.pad = 0;
+    return sp;
+}
+// a / b for 0 <= a < 2^24 and b >= 1: a float quotient (a few units off at
+// most), corrected to the floor
+__device__ __forceinline__ int div_small(int a, int b) {
+    int d = (int)__fdividef((float)a, (float)b);
+    while (d > 0 && d * b > a) --d;
+    while ((d + 1) * b <= a) ++d;
+    return d;
+}
+// One warp's geometry of a job from the group's span: the K-slice of `rank`
+// and the warp's contiguous run [ub, ue) of the group's (pair, chunk) units.
+template <int NW>
+__device__ __forceinline__ Geo geo_of(const GemvParams &p, const JobSpan &sp, int rank, int warp) {
+    Geo q;
+    q.np = sp.np;
+    q.t0 = sp.t0;
+    q.tiles_here = sp.tiles;
     q.c0 = rank * p.Cs;
     q.cs = max(0, min(p.Cs, p.C - q.c0));
     q.kb = q.c0 * kChunkK;
@@ -241,8 +261,12 @@ __device__ __forceinline__ Geo make_geo(const GemvParams &p, int group, int rank
     q.ub = (int)((long long)warp * q.U / NW);
     q.ue = (int)((long long)(warp + 1) * q.U / NW);
     q.n_my = q.ue - q.ub;
-    q.fp = q.cs > 0 ? q.ub / q.cs : 0;
+    q.fp = q.cs > 0 ? (q.U < (1 << 24) ? div_small(q.ub, q.cs) : q.ub / q.cs) : 0;
     return q;
+}
+template <int NW>
+__device__ __forceinline__ Geo make_geo(const GemvParams &p, int group, int rank, int warp) {
+    return geo_of<NW>(p, span_of(p, group), rank, warp);
 }
 
 template <int REC>
@@ -269,6 +293,7 @@ __device__ __forceinline__ int stage_units(int upt, int to_pair_end, int left) {
 template <int REC, int NW>
 struct WeightStream {
     const GemvParams *jobs;
+    const JobSpan *spans;  // the group's span of every job, or null (computed)
     int njobs, group, rank, warp;
     int job, c0, cs, t0, pl, c, left, upt;
     const uint8_t *ptr0, *ptr1;  // the next unit's records (ptr1 null: the unit has one tile)
@@ -295,11 +320,13 @@ struct WeightStream {
     __device__ __forceinline__ void next_job() {
         while (left == 0 && job + 1 < njobs) {
             ++job;
-            start(make_geo<NW>(jobs[job], group, rank, warp));
+            start(spans != nullptr ? geo_of<NW>(jobs[job], spans[job], rank, warp)
+                                   : make_geo<NW>(jobs[job], group, rank, warp));
         }
     }
-    __device__ __forceinline__ void init(const GemvParams *j, int n, int grp, int rk, int w) {
+    __device__ __forceinline__ void init(const GemvParams *j, const JobSpan *sp, int n, int grp, int rk, int w) {
         jobs = j;
+        spans = sp;
         njobs = n;
         group = grp;
         rank = rk;
@@ -312,6 +339,7 @@ struct WeightStream {
     // one job whose geometry the caller already has
     __device__ __forceinline__ void init_one(const GemvParams *j, const Geo &q) {
         jobs = j;
+        spans = nullptr;
         njobs = 1;
         job = 0;
         left = 0;
@@ -1315,8 +1343,12 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
     for (int i = tid; i < sp.njobs * kParamWords; i += NW * 32)
         reinterpret_cast<unsigned long long *>(jobs)[i] = reinterpret_cast<const unsigned long long *>(sp.jobs)[i];
     __syncthreads();
+    // and this group's span of every job (the divisions, once)
+    JobSpan *spans = reinterpret_cast<JobSpan *>(jobs + sp.njobs);
+    for (int j = tid; j < sp.njobs; j += NW * 32) spans[j] = span_of(jobs[j], group);
+    __syncthreads();
     StreamOf<FMT, CLS> ws;
-    ws.init(jobs, sp.njobs, group, 0, warp);
+    ws.init(jobs, spans, sp.njobs, group, 0, warp);
     for (int s = 0; s < C::DU - 1; ++s) ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -1326,7 +1358,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
             ring.drain();
             return;
         }
-        const Geo q = make_geo<NW>(p, group, 0, warp);
+        const Geo q = geo_of<NW>(p, spans[j], 0, warp);
         if (q.tiles_here == 0) continue;  // no work in this job (CTA-uniform)
         stage_x<FMT, CLS, 4>(p, q, m, 1, tid, warp, lane);
         run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);

@@ -107,6 +107,13 @@ struct GemvParams {
     int *err;                    // set nonzero if a kernel wait gave up
 };
 
+// One CTA group's share of a job: its first tile, tile pairs (units of upt
+// tiles) and tiles.  The persistent kernel computes every job's once at
+// start, so that moving to the next job costs no division.
+struct JobSpan {
+    int t0, np, tiles, pad;
+};
+
 // The persistent decode-step kernel runs these jobs in order, one CTA per SM.
 constexpr int kMaxStepJobs = 4 * 32 + 1;      // four jobs per layer, up to 32 layers, + logits
 constexpr long long kBarrierSpins = 1ll << 22;  // polls before a grid barrier gives up
@@ -254,10 +261,10 @@ inline Plan make_plan(int fmt, int T, int C, int nb, bool pairs, int num_sms) {
 }
 
 // Dynamic shared memory of one decode-step CTA: the engine's regions plus a
-// copy of every job's parameter block.
+// copy of every job's parameter block and the CTA's span of every job.
 inline size_t step_smem_bytes(int fmt, int nb, int TGmax, int Kmax, int SWmax, int njobs) {
     const int Cs = (Kmax + kChunkK - 1) / kChunkK;
-    return engine_smem(fmt, nb, TGmax, Cs, SWmax, 1) + (size_t)njobs * sizeof(GemvParams);
+    return engine_smem(fmt, nb, TGmax, Cs, SWmax, 1) + (size_t)njobs * (sizeof(GemvParams) + sizeof(JobSpan));
 }
 
 // Launchers, one per kernel instantiation family (defined in the .cu files).
