@@ -216,16 +216,24 @@ struct Geo {
     int U, ub, ue, n_my, fp;     // units of the CTA; this warp's [ub, ue) and its first pair
 };
 
+// a / b for 0 <= a < 2^24 and b >= 1: a float quotient (a few units off at
+// most), corrected to the floor
+__device__ __forceinline__ int div_small(int a, int b) {
+    int d = (int)__fdividef((float)a, (float)b);
+    while (d > 0 && d * b > a) --d;
+    while ((d + 1) * b <= a) ++d;
+    return d;
+}
 // The group's span of a job: balanced contiguous ranges of the job's
 // P = T / upt units (pairs, or single tiles).
 __device__ __forceinline__ JobSpan span_of(const GemvParams &p, int group) {
     JobSpan sp;
-    const int P = (p.T + p.upt - 1) / p.upt;  // units of upt tiles
+    const int P = p.upt == 2 ? (p.T + 1) >> 1 : p.T;  // units of upt (1 or 2) tiles
     int p0 = 0, p1 = 0;
     if (group < p.groups) {  // a job with fewer units than CTAs leaves the rest without work
-        if (P < 65536 && p.groups < 65536) {
-            p0 = (int)((unsigned)group * (unsigned)P / (unsigned)p.groups);
-            p1 = (int)((unsigned)(group + 1) * (unsigned)P / (unsigned)p.groups);
+        if ((long long)(group + 1) * P < (1 << 24)) {
+            p0 = div_small(group * P, p.groups);
+            p1 = div_small((group + 1) * P, p.groups);
         } else {
             p0 = (int)((unsigned long long)group * P / p.groups);
             p1 = (int)((unsigned long long)(group + 1) * P / p.groups);
@@ -236,14 +244,6 @@ __device__ __forceinline__ JobSpan span_of(const GemvParams &p, int group) {
     sp.tiles = min(p.upt * sp.np, p.T - sp.t0);
     sp.pad = 0;
     return sp;
-}
-// a / b for 0 <= a < 2^24 and b >= 1: a float quotient (a few units off at
-// most), corrected to the floor
-__device__ __forceinline__ int div_small(int a, int b) {
-    int d = (int)__fdividef((float)a, (float)b);
-    while (d > 0 && d * b > a) --d;
-    while ((d + 1) * b <= a) ++d;
-    return d;
 }
 // One warp's geometry of a job from the group's span: the K-slice of `rank`
 // and the warp's contiguous run [ub, ue) of the group's (pair, chunk) units.
