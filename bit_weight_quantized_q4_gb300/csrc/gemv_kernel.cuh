@@ -1122,76 +1122,49 @@ __device__ void cluster_finish(const GemvParams &p, const Geo &q, const Smem &m,
     }
 }
 
-// Write the job's outputs: store, residual add, SwiGLU over a gate/up tile
-// pair, or this group's (max, index) per activation row.
+// Single K-slice logits job: this group's (max, index) per activation row
+// over its folded outputs (and the outputs themselves when asked for).
 template <int CLS>
-__device__ void epilogue(const GemvParams &p, const Geo &q, const Smem &m, int S, int group, int tid, int warp,
-                         int lane) {
+__device__ void argmax_epilogue(const GemvParams &p, const Geo &q, const Smem &m, int group, int tid, int warp,
+                                int lane) {
     constexpr int NW = Cls<CLS>::NW, NTH = NW * 32;
     const int nb = CLS == 0 ? 1 : p.nb;
-    const int total = q.tiles_here * kTileRows * nb;
     if (group >= p.groups) return;  // no tiles, no partials
-    if (p.epi == EPI_ARGMAX) {
-        const int N = p.n[0];
-        float *bvs = m.rbuf;  // [warp]
-        int *bis = reinterpret_cast<int *>(m.rbuf + NW);
-        WarpTable<NW> wt;
-        if (S == 1) wt.load(m.wtab);
-        for (int r = 0; r < nb; ++r) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-            for (int ri = tid; ri < q.tiles_here * kTileRows; ri += NTH) {
-                const int n = (q.t0 + ri / kTileRows) * kTileRows + (ri % kTileRows);
-                if (n >= N) continue;
-                const float v = S > 1 ? m.red[ri * nb + r]
-                                      : fold_one<CLS>(p, q, m, wt, ri / kTileRows, ri % kTileRows, r, nb) *
-                                            m.nx[5 * kMaxNb + r];
-                if (p.out[0] != nullptr) p.out[0][(size_t)r * N + n] = v;
-                am_take(bv, bi, v, n);
-            }
-            am_warp(bv, bi);
-            if (lane == 0) {
-                bvs[warp] = bv;
-                bis[warp] = bi;
-            }
-            __syncthreads();
-            if (tid == 0) {
-                float fv = bvs[0];
-                int fi = bis[0];
-                for (int w = 1; w < NW; ++w) {
-                    if (bvs[w] > fv || (bvs[w] == fv && bis[w] < fi)) {
-                        fv = bvs[w];
-                        fi = bis[w];
-                    }
+    const int N = p.n[0];
+    float *bvs = m.rbuf;  // [warp]
+    int *bis = reinterpret_cast<int *>(m.rbuf + NW);
+    WarpTable<NW> wt;
+    wt.load(m.wtab);
+    for (int r = 0; r < nb; ++r) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int ri = tid; ri < q.tiles_here * kTileRows; ri += NTH) {
+            const int n = (q.t0 + ri / kTileRows) * kTileRows + (ri % kTileRows);
+            if (n >= N) continue;
+            const float v = fold_one<CLS>(p, q, m, wt, ri / kTileRows, ri % kTileRows, r, nb) * m.nx[5 * kMaxNb + r];
+            if (p.out[0] != nullptr) p.out[0][(size_t)r * N + n] = v;
+            am_take(bv, bi, v, n);
+        }
+        am_warp(bv, bi);
+        if (lane == 0) {
+            bvs[warp] = bv;
+            bis[warp] = bi;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float fv = bvs[0];
+            int fi = bis[0];
+            for (int w = 1; w < NW; ++w) {
+                if (bvs[w] > fv || (bvs[w] == fv && bis[w] < fi)) {
+                    fv = bvs[w];
+                    fi = bis[w];
                 }
-                p.am_val[(size_t)r * p.groups + group] = fv;
-                p.am_idx[(size_t)r * p.groups + group] = fi;
             }
-            __syncthreads();
+            p.am_val[(size_t)r * p.groups + group] = fv;
+            p.am_idx[(size_t)r * p.groups + group] = fi;
         }
-        return;
+        __syncthreads();
     }
-    // after a cluster fold (S > 1) the values are in `red`
-    for (int idx = tid; idx < total; idx += NTH) {
-        const int tl = idx / (kTileRows * nb);
-        const int rem = idx - tl * kTileRows * nb;
-        const int row = rem / nb, r = rem - row * nb;
-        int mi, tm;
-        map_tile(p, q.t0 + tl, mi, tm);
-        const int n = tm * kTileRows + row;
-        const int N = p.n[mi];
-        if (n >= N) continue;
-        const float v = m.red[idx];
-        if (p.epi == EPI_STORE) {
-            p.out[mi][(size_t)r * N + n] = v;
-        } else if (p.epi == EPI_RESIDUAL) {
-            p.out[0][(size_t)r * N + n] = v + __ldcg(p.res + (size_t)r * N + n);
-        } else if (mi == 0) {  // EPI_SWIGLU: gate tile tl, up tile tl + 1
-            const float u = m.red[idx + kTileRows * nb];
-            p.out[0][(size_t)r * N + n] = v / (1.0f + expf(-v)) * u;
-        }
-    }
-    __syncthreads();
 }
 
 // Single K-slice, store / residual / SwiGLU jobs: fold each output's warp
@@ -1283,7 +1256,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid
         cluster_finish<CLS>(p, q, m, S, rank, group, tid, warp, lane);
         return;
     }
-    epilogue<CLS>(p, q, m, S, group, tid, warp, lane);
+    argmax_epilogue<CLS>(p, q, m, group, tid, warp, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -1366,7 +1339,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
         if (p.epi != EPI_ARGMAX) {
             fold_store<CLS>(p, q, m, group, tid);
         } else {
-            epilogue<CLS>(p, q, m, 1, group, tid, warp, lane);
+            argmax_epilogue<CLS>(p, q, m, group, tid, warp, lane);
         }
     }
     ring.drain();
