@@ -623,8 +623,9 @@ __device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int
 // columns takes stage_row1.  Otherwise the slice is nb rows x Cs chunks of
 // 128 columns; a segment is one row of one chunk, a float4 per lane (a
 // block's 32 columns are 8 lanes).  Warp w takes a contiguous range of
-// segments in row-major order, SEG at a time with all their loads in flight.
-template <int FMT, int CLS, int SEG>
+// segments in row-major order, SEG at a time with all their loads in flight
+// (with PIPE, the next SEG load while the current SEG are converted).
+template <int FMT, int CLS, int SEG, bool PIPE>
 __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S, int tid, int warp, int lane) {
     using C = Cls<CLS>;
     constexpr int NW = C::NW, NTH = NW * 32, GSW = C::GSW;
@@ -655,30 +656,27 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
     const float f16x = (lane & 2) ? 1.f : 16.f;
     constexpr int LO = 64, P2 = 16;  // lo part (nb <= 4), second column pair
     const int lane_off = (lane >> 3) * xbs + (lane & 1) * 32 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4;
-    int rb = r0, cb = c0;
-    for (int base = s0; base < s1; base += SEG) {
-        // the batch's loads are predicated, not branched around, so that they
-        // are all in flight together; segments past the range read as zeros
-        float4 xv[SEG], gv[SEG];
-        {
-            int r = rb, c = cb;
+    // a batch's loads are predicated, not branched around, so that they are
+    // all in flight together; segments past the range read as zeros
+    auto load_batch = [&](float4 (&xv)[SEG], float4 (&gv)[SEG], int base, int r, int c) {
 #pragma unroll
-            for (int j = 0; j < SEG; ++j) {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f), g = make_float4(1.f, 1.f, 1.f, 1.f);
-                const int k = kb + 128 * c + 4 * lane;
-                if (base + j < s1 && k < ke) {
-                    v = __ldcg(reinterpret_cast<const float4 *>(p.x + (size_t)r * p.K + k));
-                    if (norm) g = __ldg(reinterpret_cast<const float4 *>(p.gamma + k));
-                }
-                xv[j] = v;
-                gv[j] = g;
-                if (++c == Cs) {
-                    c = 0;
-                    ++r;
-                }
+        for (int j = 0; j < SEG; ++j) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f), g = make_float4(1.f, 1.f, 1.f, 1.f);
+            const int k = kb + 128 * c + 4 * lane;
+            if (base + j < s1 && k < ke) {
+                v = __ldcg(reinterpret_cast<const float4 *>(p.x + (size_t)r * p.K + k));
+                if (norm) g = __ldg(reinterpret_cast<const float4 *>(p.gamma + k));
+            }
+            xv[j] = v;
+            gv[j] = g;
+            if (++c == Cs) {
+                c = 0;
+                ++r;
             }
         }
-        int r = rb, c = cb;
+    };
+    // convert a batch; (r, c) advance past it
+    auto convert_batch = [&](const float4 (&xv)[SEG], const float4 (&gv)[SEG], int base, int &r, int &c) {
 #pragma unroll
         for (int j = 0; j < SEG; ++j) {
             const bool valid = base + j < s1;  // warp-uniform
@@ -738,8 +736,36 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
                 ++r;
             }
         }
-        rb = r;
-        cb = c;
+    };
+    auto advance = [&](int &r, int &c, int n) {
+        c += n;
+        while (c >= Cs) {
+            c -= Cs;
+            ++r;
+        }
+    };
+    int rc = r0, cc = c0;  // the next segment to convert
+    if (PIPE) {
+        // two batches in registers: the next one's loads are in flight while
+        // the current one is converted
+        float4 xa[SEG], ga[SEG], xb[SEG], gb[SEG];
+        int rl = r0, cl = c0;  // the next segment to load
+        if (s0 < s1) load_batch(xa, ga, s0, rl, cl);
+        advance(rl, cl, SEG);
+        for (int base = s0; base < s1; base += 2 * SEG) {
+            if (base + SEG < s1) load_batch(xb, gb, base + SEG, rl, cl);
+            advance(rl, cl, SEG);
+            convert_batch(xa, ga, base, rc, cc);
+            if (base + 2 * SEG < s1) load_batch(xa, ga, base + 2 * SEG, rl, cl);
+            advance(rl, cl, SEG);
+            if (base + SEG < s1) convert_batch(xb, gb, base + SEG, rc, cc);
+        }
+    } else {
+        float4 xa[SEG], ga[SEG];
+        for (int base = s0; base < s1; base += SEG) {
+            load_batch(xa, ga, base, rc, cc);
+            convert_batch(xa, ga, base, rc, cc);
+        }
     }
     if (norm && s0 < s1) {
 #pragma unroll
@@ -1024,15 +1050,21 @@ __device__ void cluster_finish(const GemvParams &p, const Geo &q, const Smem &m,
     const int L = (nu + S - 1) / S * uv;  // the longest slice
     cg::cluster_group cluster = cg::this_cluster();
     {
-        WarpTable<NW> wt;
-        wt.load(m.wtab);
-        for (int idx = tid; idx < total; idx += NTH) {
-            const int tl = idx / tile_vals;
-            const int rem = idx - tl * tile_vals;
+        // thread tid folds output `rem` of tiles tl0, tl0 + per, ... (a tile's
+        // 16 * nb outputs fit the CTA's threads)
+        const int per = NTH / tile_vals;
+        const int tl0 = tid / tile_vals, rem = tid - tl0 * tile_vals;
+        if (tl0 < per && tl0 < q.tiles_here) {
+            WarpTable<NW> wt;
+            wt.load(m.wtab);
             const int row = rem / nb, r = rem - row * nb;
-            const float v = fold_one<CLS>(p, q, m, wt, tl, row, r, nb) * m.nx[5 * kMaxNb + r];
-            const int j = ((tl / tpu + 1) * S - 1) / nu;  // the owner of unit tl / tpu
-            *cluster.map_shared_rank(m.red + rank * L + idx - (j * nu / S) * uv, j) = v;
+            const float fr = m.nx[5 * kMaxNb + r];
+            for (int tl = tl0; tl < q.tiles_here; tl += per) {
+                const float v = fold_one<CLS>(p, q, m, wt, tl, row, r, nb) * fr;
+                const int u = tpu == 2 ? tl >> 1 : tl;
+                const int j = ((u + 1) * S - 1) / nu;  // the owner of unit u
+                *cluster.map_shared_rank(m.red + rank * L + tl * tile_vals + rem - (j * nu / S) * uv, j) = v;
+            }
         }
     }
     cluster.sync();  // every partial is in its owner's shared memory
@@ -1178,11 +1210,13 @@ __device__ void fold_store(const GemvParams &p, const Geo &q, const Smem &m, int
     wt.load(m.wtab);
     const int tile_vals = kTileRows * nb;
     const bool pairs = p.epi == EPI_SWIGLU;
-    const int total = (pairs ? q.tiles_here / 2 : q.tiles_here) * tile_vals;
-    for (int e = tid; e < total; e += NTH) {
-        const int tp = e / tile_vals, rem = e - tp * tile_vals;
+    const int ntp = pairs ? q.tiles_here / 2 : q.tiles_here;  // tiles, or gate/up pairs
+    // thread tid handles output `rem` of tiles (pairs) tp0, tp0 + per, ...
+    const int per = NTH / tile_vals;
+    const int tp0 = tid / tile_vals, rem = tid - tp0 * tile_vals;
+    const int row = rem / nb, r = rem - row * nb;
+    for (int tp = tp0 < per ? tp0 : ntp; tp < ntp; tp += per) {
         const int tl = pairs ? 2 * tp : tp;
-        const int row = rem / nb, r = rem - row * nb;
         int mi, tm;
         map_tile(p, q.t0 + tl, mi, tm);
         const int n = tm * kTileRows + row;
@@ -1244,7 +1278,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid
     for (int s = 0; s < C::DU - 1; ++s) ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    stage_x<FMT, CLS, CLS == 0 ? 4 : 8>(p, q, m, S, tid, warp, lane);
+    stage_x<FMT, CLS, CLS == 3 ? 8 : 4, true>(p, q, m, S, tid, warp, lane);
     run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
     ring.drain();
     __syncthreads();
@@ -1333,7 +1367,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
         }
         const Geo q = geo_of<NW>(p, spans[j], 0, warp);
         if (q.tiles_here == 0) continue;  // no work in this job (CTA-uniform)
-        stage_x<FMT, CLS, 4>(p, q, m, 1, tid, warp, lane);
+        stage_x<FMT, CLS, 4, false>(p, q, m, 1, tid, warp, lane);
         run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
         __syncthreads();
         if (p.epi != EPI_ARGMAX) {
