@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import q4_workloads as wl
-from parity import check, check_argmax, check_residual, check_swiglu, dev_weight, host_weight, to_np
+from parity import case_seed, check, check_argmax, check_residual, check_swiglu, dev_weight, host_weight, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ SHAPES = [(1, 32), (7, 96), (33, 160), (100, 544), (512, 2048), (1000, 4096), (4
 @pytest.mark.parametrize("nb", [1, 2, 3, 4, 5, 8, 9, 16])
 @pytest.mark.parametrize("n,k", SHAPES)
 def test_gemv(q4, fmt, nb, n, k):
-    rng = np.random.default_rng(hash((fmt, nb, n, k)) & 0xFFFF)
+    rng = np.random.default_rng(case_seed(fmt, nb, n, k))
     H = _draw(fmt, rng, n, k)
     x = wl.draw_x(rng, nb, k)
     y = q4.q4_gemv(dev_weight(H), torch.from_numpy(x).cuda())
@@ -62,7 +62,7 @@ def test_affine_with_given_group_sums(q4, nb):
 @pytest.mark.parametrize("nb", [1, 3, 16])
 @pytest.mark.parametrize("n,k", [(64, 64), (2048, 2048), (37, 4096), (130, 8192)])
 def test_nrm_gemv(q4, fmt, nb, n, k):
-    rng = np.random.default_rng(hash(("nrm", fmt, nb, n, k)) & 0xFFFF)
+    rng = np.random.default_rng(case_seed("nrm", fmt, nb, n, k))
     H = _draw(fmt, rng, n, k)
     x = wl.draw_x(rng, nb, k)
     gamma = wl.draw_gamma(rng, k)
@@ -75,7 +75,7 @@ def test_nrm_gemv(q4, fmt, nb, n, k):
 @pytest.mark.parametrize("norm", [True, False])
 @pytest.mark.parametrize("na,nbr,k,nb", [(512, 512, 2048, 1), (40, 17, 96, 2), (2048, 512, 2048, 4)])
 def test_dual(q4, fmt, norm, na, nbr, k, nb):
-    rng = np.random.default_rng(hash(("dual", fmt, norm, na, nbr, k, nb)) & 0xFFFF)
+    rng = np.random.default_rng(case_seed("dual", fmt, norm, na, nbr, k, nb))
     Ha, Hb = _draw(fmt, rng, na, k), _draw(fmt, rng, nbr, k)
     x = wl.draw_x(rng, nb, k)
     gamma = wl.draw_gamma(rng, k) if norm else None
@@ -89,7 +89,7 @@ def test_dual(q4, fmt, norm, na, nbr, k, nb):
 @pytest.mark.parametrize("fmt", ["q4_0", "affine"])
 @pytest.mark.parametrize("n,k,nb", [(8192, 2048, 1), (40, 96, 3), (1000, 1024, 8), (256, 512, 16)])
 def test_gus_nrm(q4, fmt, n, k, nb):
-    rng = np.random.default_rng(hash(("gus", fmt, n, k, nb)) & 0xFFFF)
+    rng = np.random.default_rng(case_seed("gus", fmt, n, k, nb))
     Hg, Hu = _draw(fmt, rng, n, k), _draw(fmt, rng, n, k)
     x = wl.draw_x(rng, nb, k)
     gamma = wl.draw_gamma(rng, k)
@@ -103,7 +103,7 @@ def test_gus_nrm(q4, fmt, n, k, nb):
 @pytest.mark.parametrize("n,k,nb", [(2048, 8192, 1), (2048, 2048, 1), (33, 160, 5), (700, 1024, 16)])
 @pytest.mark.parametrize("inplace", [False, True])
 def test_res_gemv(q4, fmt, n, k, nb, inplace):
-    rng = np.random.default_rng(hash(("res", fmt, n, k, nb)) & 0xFFFF)
+    rng = np.random.default_rng(case_seed("res", fmt, n, k, nb))
     H = _draw(fmt, rng, n, k)
     x = wl.draw_x(rng, nb, k)
     r = wl.draw_x(rng, nb, n)
@@ -119,7 +119,7 @@ def test_res_gemv(q4, fmt, n, k, nb, inplace):
 @pytest.mark.parametrize("fmt", ["q4_0", "affine"])
 @pytest.mark.parametrize("n,k,nb,norm", [(65536, 2048, 1, True), (1000, 256, 3, False), (77, 96, 16, True)])
 def test_argmax(q4, fmt, n, k, nb, norm):
-    rng = np.random.default_rng(hash(("am", fmt, n, k, nb)) & 0xFFFF)
+    rng = np.random.default_rng(case_seed("am", fmt, n, k, nb))
     H = _draw(fmt, rng, n, k)
     x = wl.draw_x(rng, nb, k)
     gamma = wl.draw_gamma(rng, k) if norm else None
