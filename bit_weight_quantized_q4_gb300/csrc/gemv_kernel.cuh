@@ -1278,7 +1278,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid
     for (int s = 0; s < C::DU - 1; ++s) ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    stage_x<FMT, CLS, CLS == 3 ? 8 : 4, true>(p, q, m, S, tid, warp, lane);
+    stage_x<FMT, CLS, CLS == 3 ? 8 : 4, CLS != 0>(p, q, m, S, tid, warp, lane);
     run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
     ring.drain();
     __syncthreads();
