@@ -225,18 +225,29 @@ def test_nrm_constant_vector(q4):
     check(to_np(y), ref, S, what="nrm constant")
 
 
-def test_large_dynamic_range(q4):
-    # activations far outside f16 range in both directions stay within tolerance
-    rng = np.random.default_rng(46)
+@pytest.mark.parametrize("nb", [3, 5, 9])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+def test_large_dynamic_range(q4, fmt, nb):
+    # activations far outside f16 range in both directions, and 32-column
+    # blocks of very different magnitude inside one row, stay within
+    # tolerance: each block carries its own power-of-two scale (hi + lo f16
+    # parts for nb <= 4, one f16 for larger batches)
+    rng = np.random.default_rng(case_seed("range", fmt, nb))
     n, k = 128, 1024
-    H = wl.draw_q4_0(rng, n, k)
-    x = wl.draw_x(rng, 3, k)
+    H = _draw(fmt, rng, n, k)
+    x = wl.draw_x(rng, nb, k)
     x[0] *= 1e6
     x[1] *= 1e-9
     x[2, ::7] *= 3e4
+    for r in range(3, nb):
+        x[r] *= np.repeat(10.0 ** rng.integers(-15, 16, size=k // 32), 32).astype(np.float32)
     y = q4.q4_gemv(dev_weight(H), torch.from_numpy(x).cuda())
     y_ref, S = oracle.q4_gemv(host_weight(H), x)
-    check(to_np(y), y_ref, S, what="dynamic range")
+    check(to_np(y), y_ref, S, what="dynamic range %s nb=%d" % (fmt, nb))
+    gamma = wl.draw_gamma(rng, k)
+    y = q4.q4_nrm_gemv(dev_weight(H), torch.from_numpy(x).cuda(), torch.from_numpy(gamma).cuda(), 1e-6)
+    y_ref, S = oracle.q4_nrm_gemv(host_weight(H), x, gamma, 1e-6)
+    check(to_np(y), y_ref, S, what="dynamic range nrm %s nb=%d" % (fmt, nb))
 
 
 def test_device_check_clear_after_calls(q4):
