@@ -393,6 +393,24 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
                                                       "frac_of_hbm": round(gbs / peak, 4)}
         del Ws
         torch.cuda.empty_cache()
+    # the same nb = 1 Q4_0 kernel on a 4x taller matrix (132 MB per call): the
+    # per-launch ramp and tail are amortised over 4x the bytes, which shows how
+    # fast the kernel streams once it is running
+    n4 = 4 * n
+    H = wl.draw_q4_0(rng, n4, k)
+    W0 = q4.Q4Weight.from_q4_0(H.blocks, n4, k, device)
+    copies = max(2, -(-3 * l2_bytes // W0.nbytes))
+    host = W0.tensor.cpu().numpy()
+    Ws = [W0] + [q4.Q4Weight(W0.fmt, n4, k, host, device) for _ in range(copies - 1)]
+    x = torch.from_numpy(wl.draw_x(rng, 1, k)).to(device)
+    y = torch.empty((1, n4), dtype=torch.float32, device=device)
+    t = bench_calls(Ws, lambda W: q4.q4_gemv(W, x, out=y))
+    gbs = W0.weight_bytes / t / 1e9
+    out["q4_0_n%d_k%d_nb1" % (n4, k)] = {"us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1),
+                                         "frac_of_hbm": round(gbs / peak, 4),
+                                         "what": "4x the rows of the 14336 x 4096 case: launch overhead amortised"}
+    del Ws
+    torch.cuda.empty_cache()
     return out
 
 
