@@ -358,11 +358,13 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     n, k = 14336, 4096
 
     def bench_calls(weights, fn):
+        # every copy at least once per replay, so a replay touches > 3x L2
+        n_calls = max(reps, len(weights))
         g = torch.cuda.CUDAGraph()
         fn(weights[0])
         torch.cuda.synchronize()
         with torch.cuda.graph(g):
-            for i in range(reps):
+            for i in range(n_calls):
                 fn(weights[i % len(weights)])
         g.replay()
         torch.cuda.synchronize()
@@ -370,7 +372,7 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
         for _ in range(3):
             t = time_replays(g, 1, torch.cuda.current_stream())
             best = t if best is None else min(best, t)
-        return best / reps
+        return best / n_calls
 
     for fmt in ("affine", "q4_0"):
         H = wl.draw_affine(rng, n, k) if fmt == "affine" else wl.draw_q4_0(rng, n, k)
@@ -393,6 +395,60 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
                                                       "frac_of_hbm": round(gbs / peak, 4)}
         del Ws
         torch.cuda.empty_cache()
+    # the fused calls at the small workload shapes (cfg 0..2), cold: each
+    # call's weights rotate over copies totalling more than 3x L2
+    def copies_of(H, count):
+        W0 = q4.Q4Weight.from_q4_0(H.blocks, H.n, H.k, device)
+        host = W0.tensor.cpu().numpy()
+        return [W0] + [q4.Q4Weight(W0.fmt, H.n, H.k, host, device) for _ in range(count - 1)]
+
+    def count_for(*Hs):
+        total = sum(wl_bytes(H) for H in Hs)
+        return max(2, -(-3 * l2_bytes // total))
+
+    def wl_bytes(H):
+        return H.n * H.k // 32 * 18
+
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    c0 = wl.cfg0()
+    Ws = copies_of(c0.W, count_for(c0.W))
+    x0, y0 = T(c0.x), torch.empty((1, c0.W.n), dtype=torch.float32, device=device)
+    t = bench_calls(Ws, lambda W: q4.q4_gemv(W, x0, out=y0))
+    out["cfg0_q4_gemv_1024x1024"] = {"us": round(t * 1e6, 3), "weight_gbs": round(Ws[0].weight_bytes / t / 1e9, 1)}
+    del Ws
+    c1 = wl.cfg1()
+    cnt = count_for(c1.Wq, c1.Wk, c1.Wv)
+    Wq, Wk, Wv = copies_of(c1.Wq, cnt), copies_of(c1.Wk, cnt), copies_of(c1.Wv, cnt)
+    x1, g1 = T(c1.x), T(c1.gamma)
+    yq = torch.empty((1, c1.Wq.n), dtype=torch.float32, device=device)
+    yk = torch.empty((1, c1.Wk.n), dtype=torch.float32, device=device)
+    yv = torch.empty((1, c1.Wv.n), dtype=torch.float32, device=device)
+    t = bench_calls(list(range(cnt)), lambda i: q4.q4_nrm_gemv(Wq[i], x1, g1, c1.eps, out=yq))
+    out["cfg1_q4_nrm_gemv_2048x2048"] = {"us": round(t * 1e6, 3), "weight_gbs": round(Wq[0].weight_bytes / t / 1e9, 1)}
+    t = bench_calls(list(range(cnt)), lambda i: q4.q4_dual_gemv(Wk[i], Wv[i], x1, g1, c1.eps, out_a=yk, out_b=yv))
+    out["cfg1_q4_dual_gemv_2x512x2048"] = {"us": round(t * 1e6, 3),
+                                           "weight_gbs": round(2 * Wk[0].weight_bytes / t / 1e9, 1)}
+    del Wq, Wk, Wv
+    c2 = wl.cfg2()
+    cnt = count_for(c2.Wg, c2.Wu)
+    Wg, Wu = copies_of(c2.Wg, cnt), copies_of(c2.Wu, cnt)
+    x2, g2 = T(c2.x), T(c2.gamma)
+    h2 = torch.empty((1, c2.Wg.n), dtype=torch.float32, device=device)
+    t = bench_calls(list(range(cnt)), lambda i: q4.q4_gus_nrm(Wg[i], Wu[i], x2, g2, c2.eps, out=h2))
+    out["cfg2_q4_gus_nrm_2x8192x2048"] = {"us": round(t * 1e6, 3),
+                                          "weight_gbs": round(2 * Wg[0].weight_bytes / t / 1e9, 1),
+                                          "frac_of_hbm": round(2 * Wg[0].weight_bytes / t / 1e9 / peak, 4)}
+    del Wg, Wu
+    cnt = count_for(c2.Wd)
+    Wd = copies_of(c2.Wd, cnt)
+    r2 = T(c2.r)
+    yd = torch.empty((1, c2.Wd.n), dtype=torch.float32, device=device)
+    t = bench_calls(list(range(cnt)), lambda i: q4.q4_res_gemv(Wd[i], h2, r2, out=yd))
+    out["cfg2_q4_res_gemv_2048x8192"] = {"us": round(t * 1e6, 3),
+                                         "weight_gbs": round(Wd[0].weight_bytes / t / 1e9, 1),
+                                         "frac_of_hbm": round(Wd[0].weight_bytes / t / 1e9 / peak, 4)}
+    del Wd
+    torch.cuda.empty_cache()
     # the same nb = 1 Q4_0 kernel on a 4x taller matrix (132 MB per call): the
     # per-launch ramp and tail are amortised over 4x the bytes, which shows how
     # fast the kernel streams once it is running
