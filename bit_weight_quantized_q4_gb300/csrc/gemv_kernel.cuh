@@ -435,7 +435,7 @@ struct Smem {
     float *red;      // cluster fold (S > 1): partials pushed by each rank [S][slice]
     float *slots;    // per-warp tile partials [warp][SW][16][nb]
     float *rbuf;     // reductions [4][warp][kMaxNb]
-    float *nx;       // row stats [8][kMaxNb]: 2 inv_rms, 3 scale, 5 output factor
+    float *nx;       // per row [8][kMaxNb]: 0 this slice's sum of squares, 5 output factor
     int *wtab;       // the warps' unit ranges: ub[NW + 1], fp[NW] (tail of rbuf)
     uint64_t *bars;  // ring barriers [warp][DU]
     uint8_t *ring;   // weight stages [warp][DU][2*SU records]
@@ -1028,13 +1028,16 @@ __device__ __forceinline__ float fold_one(const GemvParams &p, const Geo &q, con
 }
 
 // Cluster K-split (S > 1): each rank folds its warps' partials of all the
-// group's outputs into `red` (its K-slice's share, output factor applied);
-// then each rank finishes one slice of the outputs -- adding the ranks'
-// shares in rank order over distributed shared memory -- and writes that
-// slice (store, residual, SwiGLU on whole gate/up pairs).  For the argmax,
-// each rank reduces its slice to (max, index) pairs and rank 0 combines the
-// ranks' pairs in rank order.  A final cluster barrier keeps every CTA alive
-// until the others are done reading its shared memory.
+// group's outputs (its K-slice's share, output factor applied) and pushes
+// each into the shared memory of the rank that finishes that output's tile
+// (distributed shared memory stores into `red`); after one cluster barrier
+// each rank adds the ranks' shares of its slice in rank order from its own
+// memory and writes the slice (store, residual, SwiGLU on whole gate/up
+// pairs).  For the argmax, each rank reduces its slice to (max, index) pairs
+// and pushes them to rank 0, which combines them in rank order after a
+// second barrier.  No rank reads another's shared memory after the first
+// barrier here (the RMSNorm exchange of the staging comes before it), so
+// none has to wait for the others before it exits.
 template <int CLS>
 __device__ void cluster_finish(const GemvParams &p, const Geo &q, const Smem &m, int S, int rank, int group, int tid,
                                int warp, int lane) {
