@@ -22,6 +22,7 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 from . import DecodeLayers, Q4Weight, q4_argmax, q4_argmax_workspace_bytes, q4_decode_step, \
@@ -57,22 +58,30 @@ class DecodeStep:
         T = lambda a: torch.from_numpy(a.copy()).to(device)
         W = lambda H: Q4Weight.from_q4_0(H.blocks, H.n, H.k, device)
         self.eps = float(cfg.eps)
-        self.layers = [DeviceLayer(T(L.gamma_in), W(L.Wq), W(L.Wk), W(L.Wv), W(L.Wo), T(L.attn),
-                                   T(L.gamma_post), W(L.Wg), W(L.Wu), W(L.Wd)) for L in cfg.layers]
+        nb, hidden = cfg.x.shape
+        # the step's inputs -- x and every layer's attention stand-in -- in one
+        # device buffer, so that a caller brings them in with one copy
+        self.inputs = torch.from_numpy(np.concatenate([cfg.x.reshape(-1)] + [L.attn.reshape(-1) for L in cfg.layers])
+                                       .astype(np.float32)).to(device)
+        rows = lambda i: self.inputs[i * nb * hidden:(i + 1) * nb * hidden].view(nb, hidden)
+        self.layers = [DeviceLayer(T(L.gamma_in), W(L.Wq), W(L.Wk), W(L.Wv), W(L.Wo), rows(1 + l),
+                                   T(L.gamma_post), W(L.Wg), W(L.Wu), W(L.Wd)) for l, L in enumerate(cfg.layers)]
         self.gamma_final = T(cfg.gamma_final)
         self.Wlogits = W(cfg.Wlogits)
-        nb, hidden = cfg.x.shape
         L0 = self.layers[0]
         f32 = dict(dtype=torch.float32, device=device)
         self.nb, self.hidden = nb, hidden
-        self.x_in = T(cfg.x)
+        self.x_in = rows(0)
         self.hid = torch.empty((nb, hidden), **f32)
         self.q = torch.empty((nb, L0.Wq.n), **f32)
         self.k = torch.empty((nb, L0.Wk.n), **f32)
         self.v = torch.empty((nb, L0.Wv.n), **f32)
         self.h = torch.empty((nb, L0.Wg.n), **f32)
-        self.idx = torch.empty(nb, dtype=torch.int32, device=device)
-        self.val = torch.empty(nb, **f32)
+        # the step's results -- the argmax indices, then (16-byte aligned) their
+        # logits -- in one device buffer, read back with one copy
+        self.results = torch.empty(32, dtype=torch.int32, device=device)
+        self.idx = self.results[:nb]
+        self.val = self.results[16:16 + nb].view(torch.float32)
         self.ws = torch.empty(q4_argmax_workspace_bytes(self.Wlogits.n, nb), dtype=torch.uint8, device=device)
         self.step_ws = torch.empty(q4_decode_workspace_bytes(nb), dtype=torch.uint8, device=device)
         self.descs = DecodeLayers(self.layers)
