@@ -55,10 +55,13 @@ def test_split_store_and_norm(q4, fmt, nb, S):
     x = wl.draw_x(rng, nb, k)
     gamma = wl.draw_gamma(rng, k)
     W = dev_weight(H)
-    y = q4.q4_gemv(W, torch.from_numpy(x).cuda())
+    xd, gd = torch.from_numpy(x).cuda(), torch.from_numpy(gamma).cuda()
+    y = q4.q4_gemv(W, xd)
+    assert torch.equal(y, q4.q4_gemv(W, xd))  # the ranks' shares are added in a fixed order
     y_ref, Sr = oracle.q4_gemv(host_weight(H), x)
     check(to_np(y), y_ref, Sr, what="split gemv %s nb=%d S=%d %dx%d" % (fmt, nb, S, n, k))
-    y = q4.q4_nrm_gemv(W, torch.from_numpy(x).cuda(), torch.from_numpy(gamma).cuda(), 1e-6)
+    y = q4.q4_nrm_gemv(W, xd, gd, 1e-6)
+    assert torch.equal(y, q4.q4_nrm_gemv(W, xd, gd, 1e-6))
     y_ref, Sr = oracle.q4_nrm_gemv(host_weight(H), x, gamma, 1e-6)
     check(to_np(y), y_ref, Sr, what="split nrm %s nb=%d S=%d %dx%d" % (fmt, nb, S, n, k))
 
