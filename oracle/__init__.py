@@ -20,7 +20,10 @@ each is the plain definition written out (decode, sequential dot, then the
 fused neighbour), with the passage it follows named in its docstring.
 
 Parity note: every function here is pinned by ``tests/test_oracle_pins.py``
-(closed forms, exhaustive decodes, exact rationals, invariants, brute force).
+(closed forms, exhaustive decodes, exact rationals, invariants, brute force);
+the decode-step composition (``decode_layer``, ``decode_step``) by
+``tests/test_oracle_decode_pin.py`` (an independent numpy composition, and
+wiring mutants it must catch).
 """
 from __future__ import annotations
 
@@ -51,6 +54,16 @@ def build(force: bool = False) -> str:
 
 
 _lib = None
+_threads = 1
+
+
+def set_threads(n: int) -> int:
+    """Run the GEMV's output rows on ``n`` host threads (rows are
+    independent; every output is computed by the same code either way, so
+    the results do not depend on ``n``).  Returns the previous setting."""
+    global _threads
+    old, _threads = _threads, max(1, int(n))
+    return old
 
 
 def lib() -> ctypes.CDLL:
@@ -71,6 +84,7 @@ def lib() -> ctypes.CDLL:
         L.q4o_q4_0_row.argtypes = [P, I64, I64, P]
         L.q4o_affine_row.argtypes = [P, P, P, I64, I64, P]
         L.q4o_gemv.argtypes = [ctypes.c_int, P, P, P, I64, I64, P, I64, P, P, P]
+        L.q4o_gemv_rows.argtypes = [ctypes.c_int, P, P, P, I64, I64, P, I64, P, P, P, I64, I64]
         L.q4o_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double, P]
         L.q4o_silu.restype = ctypes.c_double
         L.q4o_silu.argtypes = [ctypes.c_double]
@@ -159,10 +173,26 @@ def gemv(W: HostWeight, x) -> tuple[np.ndarray, np.ndarray]:
     assert k == W.k
     y = np.empty((nb, W.n), dtype=np.float64)
     S = np.empty((nb, W.n), dtype=np.float64)
-    wrow = np.empty(W.k, dtype=np.float64)
     b = W.s if W.s is not None else W.a
     c = W.m if W.m is not None else W.a
-    lib().q4o_gemv(W.fmt, _p(W.a), _p(b), _p(c), W.n, W.k, _p(x), nb, _p(y), _p(S), _p(wrow))
+    T = min(_threads, W.n)
+    if T <= 1:
+        wrow = np.empty(W.k, dtype=np.float64)
+        lib().q4o_gemv(W.fmt, _p(W.a), _p(b), _p(c), W.n, W.k, _p(x), nb, _p(y), _p(S), _p(wrow))
+        return y, S
+    # disjoint row ranges on a thread pool (ctypes releases the GIL during
+    # the call), each thread with its own scratch row
+    from concurrent.futures import ThreadPoolExecutor
+    L = lib()
+    cuts = [W.n * t // T for t in range(T + 1)]
+
+    def part(t):
+        wrow = np.empty(W.k, dtype=np.float64)
+        L.q4o_gemv_rows(W.fmt, _p(W.a), _p(b), _p(c), W.n, W.k, _p(x), nb, _p(y), _p(S), _p(wrow),
+                        cuts[t], cuts[t + 1])
+
+    with ThreadPoolExecutor(max_workers=T) as ex:
+        list(ex.map(part, range(T)))
     return y, S
 
 
@@ -271,7 +301,10 @@ def q4_argmax(W: HostWeight, x, gamma=None, eps=0.0):
 # gpu, module sampling.  The attention output is the layer's given stand-in.
 
 def _hw(H) -> HostWeight:
-    return HostWeight.q4_0(H.blocks, H.n, H.k)
+    """The oracle's view of a generator's host weight (either format)."""
+    if hasattr(H, "blocks"):
+        return HostWeight.q4_0(H.blocks, H.n, H.k)
+    return HostWeight.affine(H.nib, H.s, H.m, H.n, H.k)
 
 
 def decode_layer(L, src, eps: float) -> dict:

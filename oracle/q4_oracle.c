@@ -106,14 +106,16 @@ void q4o_affine_row(const uint8_t *nib, const uint16_t *s, const uint16_t *m,
 }
 
 /* y[r][i] = sum_k w[i][k] * x[r][k], summed sequentially in ascending k, and
- * bound[r][i] = sum_k |w[i][k]| * |x[r][k]| (the scale of the parity tolerance).
+ * bound[r][i] = sum_k |w[i][k]| * |x[r][k]| (the scale of the parity tolerance),
+ * for the output rows i in [row0, row1) (rows are independent; callers may
+ * run disjoint ranges at the same time, each with its own scratch).
  * fmt 0: a = Q4_0 blocks.  fmt 1: a = nibbles, b = s, c = m.
  * x: [nb][k] f64; y, bound: [nb][n]; wrow: scratch of k doubles. */
-void q4o_gemv(int fmt, const void *a, const void *b, const void *c,
-              int64_t n, int64_t k, const double *x, int64_t nb,
-              double *y, double *bound, double *wrow)
+void q4o_gemv_rows(int fmt, const void *a, const void *b, const void *c,
+                   int64_t n, int64_t k, const double *x, int64_t nb,
+                   double *y, double *bound, double *wrow, int64_t row0, int64_t row1)
 {
-    for (int64_t i = 0; i < n; ++i) {
+    for (int64_t i = row0; i < row1; ++i) {
         if (fmt == 0)
             q4o_q4_0_row((const uint8_t *)a, k, i, wrow);
         else
@@ -131,6 +133,14 @@ void q4o_gemv(int fmt, const void *a, const void *b, const void *c,
                 bound[r * n + i] = mag;
         }
     }
+}
+
+/* All n output rows of the GEMV above. */
+void q4o_gemv(int fmt, const void *a, const void *b, const void *c,
+              int64_t n, int64_t k, const double *x, int64_t nb,
+              double *y, double *bound, double *wrow)
+{
+    q4o_gemv_rows(fmt, a, b, c, n, k, x, nb, y, bound, wrow, 0, n);
 }
 
 /* xhat[r][e] = x[r][e] / sqrt(mean_e' x[r][e']^2 + eps) * gamma[e]. */

@@ -203,35 +203,47 @@ class Cfg4:
     x: np.ndarray
     layers: list = field(default_factory=list)
     gamma_final: np.ndarray | None = None
-    Wlogits: Q4_0Host | None = None
+    Wlogits: Q4_0Host | AffineHost | None = None
     eps: float = EPS
 
 
+def _draw_fmt(fmt: str):
+    if fmt == "q4_0":
+        return draw_q4_0
+    if fmt == "affine":
+        return draw_affine
+    raise ValueError("fmt must be 'q4_0' or 'affine'")
+
+
 def cfg4_layer(seed: int, layer: int, hidden: int = 2048, kv: int = 512,
-               inter: int = 8192, nb: int = 1) -> Layer:
+               inter: int = 8192, nb: int = 1, fmt: str = "q4_0") -> Layer:
+    draw = _draw_fmt(fmt)
     rng = np.random.default_rng(seed * 1000 + layer)
     gamma_in = draw_gamma(rng, hidden)
-    Wq = draw_q4_0(rng, hidden, hidden)
-    Wk = draw_q4_0(rng, kv, hidden)
-    Wv = draw_q4_0(rng, kv, hidden)
-    Wo = draw_q4_0(rng, hidden, hidden)
+    Wq = draw(rng, hidden, hidden)
+    Wk = draw(rng, kv, hidden)
+    Wv = draw(rng, kv, hidden)
+    Wo = draw(rng, hidden, hidden)
     attn = draw_x(rng, nb, hidden)
     gamma_post = draw_gamma(rng, hidden)
-    Wg = draw_q4_0(rng, inter, hidden)
-    Wu = draw_q4_0(rng, inter, hidden)
-    Wd = draw_q4_0(rng, hidden, inter)
+    Wg = draw(rng, inter, hidden)
+    Wu = draw(rng, inter, hidden)
+    Wd = draw(rng, hidden, inter)
     return Layer(gamma_in, Wq, Wk, Wv, Wo, attn, gamma_post, Wg, Wu, Wd)
 
 
 def cfg4(seed: int = 4, layers: int = 16, hidden: int = 2048, kv: int = 512,
-         inter: int = 8192, vocab: int = 65536, nb: int = 1) -> Cfg4:
+         inter: int = 8192, vocab: int = 65536, nb: int = 1, fmt: str = "q4_0") -> Cfg4:
+    """``fmt`` picks the weight format of every matrix (the workload itself is
+    Q4_0; the affine variant serves the parity tests)."""
+    draw = _draw_fmt(fmt)
     rng = np.random.default_rng(seed)
     x = draw_x(rng, nb, hidden)
     gamma_final = draw_gamma(rng, hidden)
-    Wlogits = draw_q4_0(rng, vocab, hidden)
+    Wlogits = draw(rng, vocab, hidden)
     c = Cfg4(x, [], gamma_final, Wlogits)
     for l in range(layers):
-        c.layers.append(cfg4_layer(seed, l, hidden, kv, inter, nb))
+        c.layers.append(cfg4_layer(seed, l, hidden, kv, inter, nb, fmt))
     return c
 
 

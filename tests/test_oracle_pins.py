@@ -407,3 +407,20 @@ def test_argmax_planted_unique_max():
     W = _q4_0_weight(wl.pack_q4_0(q, d), n, k)
     idx, logits, _ = oracle.q4_argmax(W, np.ones((1, k), np.float32))
     assert idx[0] == 41 == int(np.argmax(logits[0]))
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+def test_threaded_rows_give_the_same_bits(fmt):
+    # the CPU baseline runs the oracle's rows on several threads: every
+    # output must be the same bits as the single-threaded walk
+    rng = np.random.default_rng(5)
+    H = wl.draw_q4_0(rng, 333, 256) if fmt == "q4_0" else wl.draw_affine(rng, 333, 256)
+    W = oracle._hw(H)
+    x = wl.draw_x(rng, 3, 256)
+    y1, S1 = oracle.gemv(W, x)
+    old = oracle.set_threads(7)
+    try:
+        y7, S7 = oracle.gemv(W, x)
+    finally:
+        oracle.set_threads(old)
+    assert np.array_equal(y1, y7) and np.array_equal(S1, S7)
