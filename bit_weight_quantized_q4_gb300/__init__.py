@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
             "q4_decode_step": (I32, [P, I32, W, P, F, I32, P, P, P, P, P, P, P, P, P, SZ, P]),
             "q4_decode_check": (I32, [P, P]),
             "q4_device_check": (I32, [P]),
+            "q4_debug_wait_limits": (I32, [ctypes.c_int64, I32, ctypes.c_int64, I32]),
             "q4_plan": (I32, [I32, I32, I32, I32, I32, I32, ctypes.POINTER(ctypes.c_int32)]),
             "q4_status_str": (ctypes.c_char_p, [I32]),
         }
@@ -220,6 +221,42 @@ def _dev_f32(t, name, shape=None):
     return t
 
 
+def _dev_buf(t, name, dtype, shape, device, min_numel=None):
+    """A caller-supplied output or workspace: a contiguous CUDA tensor of
+    `dtype` on `device`, of exactly `shape` (or, for a workspace, at least
+    `min_numel` elements).  The C ABI carries no sizes for these buffers, so
+    everything is checked here, before any launch."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != dtype:
+        raise TypeError("%s must be a CUDA %s tensor" % (name, dtype))
+    if t.device != device:
+        raise ValueError("%s is on %s, the activations on %s" % (name, t.device, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if min_numel is not None:
+        if t.numel() < min_numel:
+            raise ValueError("%s has %d elements, needs at least %d" % (name, t.numel(), min_numel))
+    elif tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    return t
+
+
+def _argmax_outs(W, x, nb, want_val, want_logits, idx, val, logits):
+    torch = _torch()
+    if idx is None:
+        idx = torch.empty(nb, dtype=torch.int32, device=x.device)
+    idx = _dev_buf(idx, "idx", torch.int32, (nb,), x.device)
+    if want_val and val is None:
+        val = torch.empty(nb, dtype=torch.float32, device=x.device)
+    if val is not None:
+        val = _dev_buf(val, "val", torch.float32, (nb,), x.device)
+    if want_logits and logits is None:
+        logits = torch.empty((nb, W.n), dtype=torch.float32, device=x.device)
+    if logits is not None:
+        logits = _dev_buf(logits, "logits", torch.float32, (nb, W.n), x.device)
+    return idx, val, logits
+
+
 def _rows(x, k):
     x = _dev_f32(x, "x")
     if x.dim() == 1:
@@ -309,12 +346,8 @@ def q4_argmax(W: Q4Weight, x, gamma=None, eps: float = 0.0, want_val=False, want
     ws_bytes = q4_argmax_workspace_bytes(W.n, nb)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
-    if idx is None:
-        idx = torch.empty(nb, dtype=torch.int32, device=x.device)
-    if want_val and val is None:
-        val = torch.empty(nb, dtype=torch.float32, device=x.device)
-    if want_logits and logits is None:
-        logits = torch.empty((nb, W.n), dtype=torch.float32, device=x.device)
+    workspace = _dev_buf(workspace, "workspace", torch.uint8, None, x.device, min_numel=ws_bytes)
+    idx, val, logits = _argmax_outs(W, x, nb, want_val, want_logits, idx, val, logits)
     _check(lib().q4_argmax(W.cref(), x.data_ptr(), gp, float(eps), nb, idx.data_ptr(),
                            None if val is None else val.data_ptr(),
                            None if logits is None else logits.data_ptr(),
@@ -328,15 +361,9 @@ def q4_argmax_noalloc(W: Q4Weight, x, gamma=None, eps: float = 0.0, want_val=Fal
     fixed array inside the library (for callers that cannot allocate device
     memory; see ``q4_argmax_noalloc`` in the C header for the size limit and
     the sharing rules).  Returns ``(idx, val or None, logits or None)``."""
-    torch = _torch()
     x, nb = _rows(x, W.k)
     gp = None if gamma is None else _dev_f32(gamma, "gamma", (W.k,)).data_ptr()
-    if idx is None:
-        idx = torch.empty(nb, dtype=torch.int32, device=x.device)
-    if want_val and val is None:
-        val = torch.empty(nb, dtype=torch.float32, device=x.device)
-    if want_logits and logits is None:
-        logits = torch.empty((nb, W.n), dtype=torch.float32, device=x.device)
+    idx, val, logits = _argmax_outs(W, x, nb, want_val, want_logits, idx, val, logits)
     _check(lib().q4_argmax_noalloc(W.cref(), x.data_ptr(), gp, float(eps), nb, idx.data_ptr(),
                                    None if val is None else val.data_ptr(),
                                    None if logits is None else logits.data_ptr(), _stream()),
@@ -369,8 +396,20 @@ def q4_decode_step(layers: DecodeLayers, Wlogits: Q4Weight, gamma_final, eps: fl
                    idx, val, workspace, n_layers: int | None = None):
     """One decode step as a single persistent kernel (see ``q4_decode_step``
     in the C header).  All buffers are caller-owned CUDA tensors."""
+    torch = _torch()
     n = len(layers) if n_layers is None else int(n_layers)
+    x_in = _dev_f32(x_in, "x_in")
     nb = x_in.shape[0]
+    idx = _dev_buf(idx, "idx", torch.int32, (nb,), x_in.device)
+    if val is not None:
+        val = _dev_buf(val, "val", torch.float32, (nb,), x_in.device)
+    workspace = _dev_buf(workspace, "workspace", torch.uint8, None, x_in.device,
+                         min_numel=q4_decode_workspace_bytes(nb))
+    L0 = layers.layers[0]
+    hidden = L0.Wo.n
+    for t, name, width in ((x_in, "x_in", hidden), (hid, "hid", hidden), (q, "q", L0.Wq.n), (k, "k", L0.Wk.n),
+                           (v, "v", L0.Wv.n), (h, "h", L0.Wg.n)):
+        _dev_buf(t, name, torch.float32, (nb, width), x_in.device)
     _check(lib().q4_decode_step(ctypes.cast(layers.arr, ctypes.c_void_p), n, Wlogits.cref(),
                                 _dev_f32(gamma_final, "gamma_final").data_ptr(), float(eps), nb,
                                 _dev_f32(x_in, "x_in").data_ptr(), _dev_f32(hid, "hid").data_ptr(),
@@ -381,7 +420,17 @@ def q4_decode_step(layers: DecodeLayers, Wlogits: Q4Weight, gamma_final, eps: fl
 
 
 def q4_decode_check(workspace):
+    workspace = _dev_buf(workspace, "workspace", _torch().uint8, None, workspace.device, min_numel=16)
     _check(lib().q4_decode_check(workspace.data_ptr(), _stream()), "q4_decode_check")
+
+
+def q4_debug_wait_limits(barrier_polls: int = 0, barrier_extra: int = 0, copy_wait_cycles: int = 0,
+                         copy_extra_bytes: int = 0):
+    """Testing hook: shorten the kernels' wait bounds and make their waits
+    expect arrivals or bytes that never come (see ``q4_debug_wait_limits`` in
+    the C header).  ``q4_debug_wait_limits()`` restores the defaults."""
+    _check(lib().q4_debug_wait_limits(int(barrier_polls), int(barrier_extra), int(copy_wait_cycles),
+                                      int(copy_extra_bytes)), "q4_debug_wait_limits")
 
 
 def q4_device_check():

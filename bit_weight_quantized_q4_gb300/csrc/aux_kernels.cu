@@ -10,7 +10,7 @@ namespace dev {
 // Pass 2 of the greedy argmax (Module gpu, module sampling): one CTA per
 // activation row folds the per-group (max, index) pairs of pass 1.  Larger
 // value wins, ties go to the lower index; pass 1 already ranked NaN lowest.
-__global__ void __launch_bounds__(256) argmax_fold_kernel(const float *am_val, const int *am_idx,
+__global__ void __launch_bounds__(256) q4gemv_argmax_fold_kernel(const float *am_val, const int *am_idx,
                                                           int groups, int32_t *idx, float *val) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float sv[8];
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(256) argmax_fold_kernel(const float *am_val, c
 // group sums of a row batch).  Eight lanes per group, four columns each,
 // added by block8_sum -- the order the GEMV's staging uses for its own affine
 // block sums, so either source gives the same bits.
-__global__ void __launch_bounds__(256) group_sums_kernel(const float *x, int nb, int k, float *gsum) {
+__global__ void __launch_bounds__(256) q4gemv_group_sums_kernel(const float *x, int nb, int k, float *gsum) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int G = k / 32;
     const int total = nb * G;
@@ -91,14 +91,14 @@ static int launch_pdl(const void *func, dim3 grid, dim3 block, void **args, cuda
 int launch_argmax_fold(const float *am_val, const int *am_idx, int groups, int nb, int32_t *idx,
                        float *val, void *stream) {
     void *args[] = {(void *)&am_val, (void *)&am_idx, (void *)&groups, (void *)&idx, (void *)&val};
-    return launch_pdl((const void *)dev::argmax_fold_kernel, dim3(nb), dim3(256), args,
+    return launch_pdl((const void *)dev::q4gemv_argmax_fold_kernel, dim3(nb), dim3(256), args,
                       (cudaStream_t)stream);
 }
 
 int launch_group_sums(const float *x, int nb, int k, float *gsum, void *stream) {
     void *args[] = {(void *)&x, (void *)&nb, (void *)&k, (void *)&gsum};
     const int total = nb * (k / 32);  // 8 threads per group
-    return launch_pdl((const void *)dev::group_sums_kernel, dim3((8 * total + 255) / 256), dim3(256), args,
+    return launch_pdl((const void *)dev::q4gemv_group_sums_kernel, dim3((8 * total + 255) / 256), dim3(256), args,
                       (cudaStream_t)stream);
 }
 

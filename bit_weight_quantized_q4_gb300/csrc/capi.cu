@@ -79,6 +79,14 @@ q4::GemvParams base_params(const q4_weight *W0, const q4_weight *W1, int mode, c
     return p;
 }
 
+// Bounds of the kernels' waits and the extra counts a wait expects, applied
+// to every launch (q4_debug_wait_limits changes them to test the give-up
+// path; the defaults are about a second and nothing extra).
+long long g_barrier_polls = q4::kBarrierSpins;
+int g_barrier_extra = 0;
+long long g_wait_cycles = q4::kWaitCycles;
+int g_extra_tx = 0;
+
 // The per-call kernels' error word: set (never cleared) by a kernel whose
 // bounded wait for its weight copies gave up; q4_device_check reads and
 // clears it.  One word per device, its address resolved once per device.
@@ -106,25 +114,39 @@ q4_status kernel_err_ptr(int **out) {
     return Q4_OK;
 }
 
-q4_status run(const q4::GemvParams &p, int fmt, cudaStream_t stream, q4::Plan *plan_out = nullptr) {
+// The launch plan of job p on this device.
+q4_status plan_of(const q4::GemvParams &p, int fmt, q4::Plan *plan) {
     const int sms = num_sms();
     if (sms <= 0) return Q4_ERR_CUDA;
-    q4::Plan plan = q4::make_plan(fmt, p.T, p.C, p.nb, p.mode == q4::MODE_PAIRS, sms);
-    if (plan.smem > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;  // nb * k too large to stage
+    *plan = q4::make_plan(fmt, p.T, p.C, p.nb, p.mode == q4::MODE_PAIRS, sms);
+    if (plan->smem > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;  // nb * k too large to stage
+    return Q4_OK;
+}
+
+// Launch job p with `plan` (from plan_of on the same job): the caller sizes
+// any per-group buffer from the plan that is launched.
+q4_status launch_planned(const q4::GemvParams &p, int fmt, const q4::Plan &plan, cudaStream_t stream) {
     q4::GemvParams pp = p;
     Q4_TRY(kernel_err_ptr(&pp.err));
+    pp.wait_cycles = g_wait_cycles;
+    pp.extra_tx = g_extra_tx;
     pp.TG = plan.TG;
     pp.SW = plan.SW;
     pp.upt = plan.upt;
     pp.S = plan.S;
     pp.Cs = plan.Cs;
     pp.groups = plan.groups;
-    if (plan_out) *plan_out = plan;
     cudaGetLastError();  // clear a stale error so the check below is ours
     int rc = fmt == Q4_FMT_Q4_0 ? q4::launch_gemv_q4_0(pp, plan, stream)
                                 : q4::launch_gemv_affine(pp, plan, stream);
     if (rc != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
     return Q4_OK;
+}
+
+q4_status run(const q4::GemvParams &p, int fmt, cudaStream_t stream) {
+    q4::Plan plan;
+    Q4_TRY(plan_of(p, fmt, &plan));
+    return launch_planned(p, fmt, plan, stream);
 }
 
 inline bool nb_ok(int32_t nb) { return nb >= 1 && nb <= q4::kMaxNb; }
@@ -276,9 +298,9 @@ q4_status q4_argmax(const q4_weight *W, const float *x, const float *gamma, floa
     p.am_val = (float *)workspace;
     p.am_idx = (int *)((uint8_t *)workspace + ((groups_max * nb * 4 + 15) & ~(size_t)15));
     q4::Plan plan;
-    Q4_TRY(run(p, W->fmt, stream, &plan));
-    // the groups of this plan: pass 2 folds exactly those
-    // (run() recomputed p.groups into its own copy; the plan carries it)
+    Q4_TRY(plan_of(p, W->fmt, &plan));
+    Q4_TRY(launch_planned(p, W->fmt, plan, stream));
+    // pass 2 folds exactly the groups of the plan that was launched
     cudaGetLastError();
     if (q4::launch_argmax_fold(p.am_val, p.am_idx, plan.groups, nb, idx, val, stream) != 0 ||
         cudaGetLastError() != cudaSuccess)
@@ -343,24 +365,22 @@ extern "C" q4_status q4_argmax_noalloc(const q4_weight *W, const float *x, const
         (gamma && !aligned16(gamma)))
         return Q4_ERR_ALIGN;
     if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
-    const int sms = num_sms();
-    if (sms <= 0) return Q4_ERR_CUDA;
-    // The pairs this call needs: one per (thread-block group, activation row).
-    const q4::Plan plan = q4::make_plan(W->fmt, (int)q4::tiles_of(W->n), (int)q4::chunks_of(W->k), nb,
-                                        false, sms);
+    q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, x, gamma, eps, nb);
+    p.epi = q4::EPI_ARGMAX;
+    p.out[0] = logits;
+    // The pairs this call needs: one per (thread-block group, activation
+    // row) of the plan below, which is the plan that is launched.
+    q4::Plan plan;
+    Q4_TRY(plan_of(p, W->fmt, &plan));
     const size_t val_bytes = ((size_t)plan.groups * nb * 4 + 15) & ~(size_t)15;
     if (val_bytes + (size_t)plan.groups * nb * 4 > kNoAllocScratchBytes) return Q4_ERR_WORKSPACE;
     void *scratch = nullptr;
     Q4_TRY(noalloc_scratch(&scratch));
-    q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, x, gamma, eps, nb);
-    p.epi = q4::EPI_ARGMAX;
-    p.out[0] = logits;
     p.am_val = (float *)scratch;
     p.am_idx = (int *)((unsigned char *)scratch + val_bytes);
-    q4::Plan used;
-    Q4_TRY(run(p, W->fmt, stream, &used));
+    Q4_TRY(launch_planned(p, W->fmt, plan, stream));
     cudaGetLastError();
-    if (q4::launch_argmax_fold(p.am_val, p.am_idx, used.groups, nb, idx, val, stream) != 0 ||
+    if (q4::launch_argmax_fold(p.am_val, p.am_idx, plan.groups, nb, idx, val, stream) != 0 ||
         cudaGetLastError() != cudaSuccess)
         return Q4_ERR_CUDA;
     return Q4_OK;
@@ -391,6 +411,8 @@ q4::GemvParams step_job(int G, int nb, int *err) {
     q4::GemvParams p;
     memset(&p, 0, sizeof(p));
     p.err = err;
+    p.wait_cycles = g_wait_cycles;
+    p.extra_tx = g_extra_tx;
     p.nb = nb;
     p.S = 1;
     p.groups = G;
@@ -475,6 +497,8 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     sp.idx = idx;
     sp.val = val;
     sp.nb = nb;
+    sp.barrier_polls = g_barrier_polls;
+    sp.barrier_extra = g_barrier_extra;
     int TGmax = 1, Kmax = 0, SWmax = 2;
     int nj = 0;
     for (int l = 0; l < n_layers; ++l) {
@@ -555,6 +579,18 @@ extern "C" q4_status q4_decode_check(const void *workspace, cudaStream_t stream)
     if (cudaMemcpy(&err, (const unsigned char *)workspace + 4, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
         return Q4_ERR_CUDA;
     return err ? Q4_ERR_CUDA : Q4_OK;
+}
+
+extern "C" q4_status q4_debug_wait_limits(int64_t barrier_polls, int32_t barrier_extra, int64_t copy_wait_cycles,
+                                          int32_t copy_extra_bytes) {
+    if (barrier_extra < 0 || barrier_extra > 1 || copy_extra_bytes < 0 || copy_extra_bytes > 4096 ||
+        copy_extra_bytes % 16 != 0)
+        return Q4_ERR_SHAPE;
+    g_barrier_polls = barrier_polls > 0 ? (long long)barrier_polls : q4::kBarrierSpins;
+    g_barrier_extra = barrier_extra;
+    g_wait_cycles = copy_wait_cycles > 0 ? (long long)copy_wait_cycles : q4::kWaitCycles;
+    g_extra_tx = copy_extra_bytes;
+    return Q4_OK;
 }
 
 extern "C" q4_status q4_device_check(cudaStream_t stream) {

@@ -85,10 +85,9 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
-constexpr long long kWaitCycles = 1ll << 31;  // about a second: bound of one mbarrier wait
-// Wait for phase `parity` of mbarrier `bar` to complete; false after
-// kWaitCycles (the caller records the failure and stops).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of mbarrier `bar` to complete; false after `limit`
+// SM clock cycles (the caller records the failure and stops).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit) {
     long long t0 = 0;
     for (int it = 0;; ++it) {
         uint32_t done;
@@ -100,10 +99,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         if (done) return true;
         if (it == 0) {
             t0 = clock64();
-        } else if (clock64() - t0 > kWaitCycles) {
+        } else if (clock64() - t0 > limit) {
             return false;
         }
     }
+}
+
+// Barrier over the NW warps of a CTA (named barrier 1): every warp of the
+// kernels, used by the engine's functions.
+template <int NW>
+__device__ __forceinline__ void csync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
 }
 
 // D = A * B + (z0..z3), m16n8k16, f16 inputs, fp32 accumulate; the caller
@@ -350,16 +356,16 @@ struct WeightStream {
     // for single-tile units), never past the pair or the warp's range -- into
     // the ring stage at shared address `dst` with the TMA engine, completing
     // on mbarrier `bar`: one copy of n consecutive records per tile (the
-    // second tile's records at dst + SU*REC).  Lane 0 issues; every lane
-    // advances the (warp-uniform) state.
+    // second tile's records at dst + SU*REC).  The issuer issues; every
+    // thread that holds this stream advances its state.
     template <int SU>
-    __device__ __forceinline__ void issue(uint32_t dst, uint32_t bar, int lane, uint64_t policy) {
+    __device__ __forceinline__ void issue(uint32_t dst, uint32_t bar, bool issuer, uint64_t policy, int extra_tx) {
         const int n = stage_units<SU>(upt, cs - c, left);
-        if (lane == 0) {
+        if (issuer) {
             // the warp's reads of this stage (ordered by the caller's
             // __syncwarp) come before the async-proxy writes that refill it
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_expect_tx(bar, (ptr1 != nullptr ? 2 : 1) * n * REC);
+            mbar_expect_tx(bar, (ptr1 != nullptr ? 2 : 1) * n * REC + extra_tx);
             bulk_g2s(dst, ptr0, n * REC, bar, policy);
             if (ptr1 != nullptr) bulk_g2s(dst + SU * REC, ptr1, n * REC, bar, policy);
         }
@@ -373,24 +379,30 @@ struct WeightStream {
             ptr0 += (size_t)n * REC;
             if (ptr1 != nullptr) ptr1 += (size_t)n * REC;
         }
-        if (left == 0) next_job();
+        // the move to the warp's next job (next_job) is left to the caller
     }
 };
 
 // One warp's ring of DU stages of SREC bytes, with an mbarrier per stage.
 // `fill` counts stages issued, `cons` stages consumed; stage k lives in
-// slot k mod DU and completes phase (k / DU) mod 2 of its barrier.
+// slot k mod DU and completes phase (k / DU) mod 2 of its barrier.  A slot is
+// refilled as soon as the warp has consumed it, so between two jobs of the
+// persistent kernel (and before the first one) all DU stages are in flight.
 template <int DU, int SU, int SREC>
 struct Ring {
     uint32_t base, bars;  // this warp's stages and barriers (shared addresses)
     uint32_t fill, cons;
     bool ok;              // false once a wait gave up
     uint64_t policy;
-    __device__ __forceinline__ void init(uint32_t b, uint32_t br, int lane) {
+    long long limit;      // bound of one wait (cycles)
+    int extra_tx;         // expected bytes beyond the copies (testing only; 0)
+    __device__ __forceinline__ void init(uint32_t b, uint32_t br, int lane, long long lim, int extra) {
         base = b;
         bars = br;
         fill = cons = 0;
         ok = true;
+        limit = lim;
+        extra_tx = extra;
         policy = evict_first_policy();
         if (lane == 0) {
 #pragma unroll
@@ -401,16 +413,25 @@ struct Ring {
     }
     __device__ __forceinline__ uint32_t stage(uint32_t k) const { return base + (k % DU) * SREC; }
     __device__ __forceinline__ uint32_t bar(uint32_t k) const { return bars + (k % DU) * 8; }
+    // Refill one free slot from the stream; with cross == false only from
+    // the stream's current job (moving to the next job recomputes its
+    // geometry, which the persistent kernel does while it waits at a grid
+    // barrier).  True if a stage was issued.
     template <class WS>
-    __device__ __forceinline__ void push(WS &ws, int lane) {
-        if (ok && ws.left > 0) {
-            ws.template issue<SU>(stage(fill), bar(fill), lane, policy);
-            ++fill;
+    __device__ __forceinline__ bool push(WS &ws, int lane, bool cross = true) {
+        if (!ok || fill - cons >= (uint32_t)DU) return false;
+        if (ws.left == 0) {
+            if (!cross) return false;
+            ws.next_job();
+            if (ws.left == 0) return false;
         }
+        ws.template issue<SU>(stage(fill), bar(fill), lane == 0, policy, extra_tx);
+        ++fill;
+        return true;
     }
     // wait for the unit `cons`; the warp agrees on the outcome
     __device__ __forceinline__ bool wait(int *err, int lane) {
-        const bool mine = ok && mbar_wait(bar(cons), (cons / DU) & 1);
+        const bool mine = ok && mbar_wait(bar(cons), (cons / DU) & 1, limit);
         const bool all = __all_sync(0xffffffffu, mine);
         if (!all && ok) {
             ok = false;
@@ -418,11 +439,12 @@ struct Ring {
         }
         return ok;
     }
-    // after a failed wait: wait (bounded) for the copies still in flight
-    // into this warp's stages before the CTA may exit
+    // after a failed wait: wait (bounded, always by the full second, whatever
+    // `limit` is) for the copies still in flight into this warp's stages
+    // before the CTA may exit
     __device__ __forceinline__ void drain() {
         if (ok) return;
-        for (uint32_t k = cons; k < fill; ++k) mbar_wait(bar(k), (k / DU) & 1);
+        for (uint32_t k = cons; k < fill; ++k) mbar_wait(bar(k), (k / DU) & 1, kWaitCycles);
         cons = fill;
     }
 };
@@ -519,6 +541,52 @@ __device__ __forceinline__ int gs_idx(int b, int row, int GSW) { return ((b >> 2
 // loads bypass L1 (.cg): in the persistent kernel another SM may have
 // rewritten them since this SM last read them.
 
+// nb = 1 (class 0).  The tensor-core products of a chunk run as one chain of
+// eight m16n8k16 products (two k16 steps per 32-column block) in which block
+// j's activations occupy only the column pair (2j, 2j+1) -- hi and lo -- and
+// are zero in the other columns; a lane's B registers are kept when its
+// column belongs to the block and zeroed otherwise.  At the end of the chain
+// lane (g, t) holds block t's hi and lo products of rows g and g+8.
+// chunk_b() loads those B registers for block j of a chunk.
+__device__ __forceinline__ uint4 chunk_b(const uint8_t *xchunk, int j, int boff, int g) {
+    uint4 b = *reinterpret_cast<const uint4 *>(xchunk + j * 128 + boff);
+    if ((g >> 1) != j) b = make_uint4(0u, 0u, 0u, 0u);
+    return b;
+}
+
+// The offset products of Q4_0 for nb = 1: per chunk, the product chain above
+// with every nibble equal to 8, once per CTA and job; block j's hi + lo goes
+// to the block-sum slot of block j.  A weight block of all eights then gives
+// exactly the same chain values, so (hi + lo) - offset is exactly zero for it.
+// Runs after the staging barrier; ends with a CTA barrier.
+template <int CLS>
+__device__ __forceinline__ void eights_chunk(const Smem &m, int c, int lane) {
+    constexpr int GSW = Cls<CLS>::GSW;
+    const int g = lane >> 2, t = lane & 3;
+    const int boff = (g & 1) * 64 + t * 16;
+    const float z = 0.f;
+    const uint8_t *xchunk = m.xs + c * kBlocksPerChunk * 128;
+    float d[4];
+#pragma unroll
+    for (int j = 0; j < kBlocksPerChunk; ++j) {
+        const uint4 b = chunk_b(xchunk, j, boff, g);
+        if (j == 0) {
+            mma16816_c(d, kEightLo, kEightLo, kEightHi, kEightHi, b.x, b.y, z, z, z, z);
+        } else {
+            mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, b.x, b.y);
+        }
+        mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, b.z, b.w);
+    }
+    if (g == 0) m.gs[gs_idx(c * kBlocksPerChunk + t, 0, GSW)] = d[0] + d[1];
+}
+// All chunks, after the staging barrier (the generic staging path of nb = 1,
+// slices over 8192 columns); ends with a CTA barrier.
+template <int CLS>
+__device__ void eights_c0(const Smem &m, int Cs, int warp, int lane) {
+    for (int c = warp; c < Cs; c += Cls<CLS>::NW) eights_chunk<CLS>(m, c, lane);
+    csync<Cls<CLS>::NW>();
+}
+
 // After the writes: the staging barrier, then each row's output factor --
 // its inverse RMS from the warps' partial sums of squares in warp order (and,
 // for a split K, the cluster ranks' slice sums in rank order), or 1.
@@ -526,7 +594,7 @@ template <int CLS>
 __device__ void stage_finish(const GemvParams &p, const Smem &m, int S, int nb, int tid) {
     constexpr int NW = Cls<CLS>::NW;
     const bool norm = p.gamma != nullptr;
-    __syncthreads();
+    csync<NW>();
     // every CTA of the cluster has started (the kernel's first arrive): from
     // here on the ranks may access each other's shared memory
     if (S > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
@@ -534,46 +602,68 @@ __device__ void stage_finish(const GemvParams &p, const Smem &m, int S, int nb, 
         if (tid < nb) m.nx[5 * kMaxNb + tid] = 1.f;
         return;
     }
-    float tss = 0.f;
-    if (tid < nb) {
+    // warp w adds the NW warps' partial sums of rows w and w + NW by a fixed
+    // butterfly (lane l < NW holds warp l's partial)
+    const int warp = tid >> 5, lane = tid & 31;
+    float tss[2] = {0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < NW; ++w) tss += m.rbuf[tid * NW + w];
+    for (int h = 0; h < 2; ++h) {
+        const int r = warp + h * NW;
+        if (r < nb) {  // warp-uniform
+            float v = lane < NW ? m.rbuf[r * NW + lane] : 0.f;
+#pragma unroll
+            for (int off = NW / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            tss[h] = v;
+        }
     }
     if (S > 1) {
         cg::cluster_group cluster = cg::this_cluster();
-        if (tid < nb) m.nx[tid] = tss;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            if (warp + h * NW < nb && lane == 0) m.nx[warp + h * NW] = tss[h];
         cluster.sync();
-        if (tid < nb) {
-            tss = 0.f;
-            for (int rr = 0; rr < S; ++rr) tss += cluster.map_shared_rank(m.nx, rr)[tid];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = warp + h * NW;
+            if (r < nb && lane == 0) {
+                tss[h] = 0.f;
+                for (int rr = 0; rr < S; ++rr) tss[h] += cluster.map_shared_rank(m.nx, rr)[r];
+            }
         }
     }
-    if (tid < nb) m.nx[5 * kMaxNb + tid] = 1.0f / sqrtf(tss / (float)p.K + p.eps);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int r = warp + h * NW;
+        if (r < nb && lane == 0) m.nx[5 * kMaxNb + r] = 1.0f / sqrtf(tss[h] / (float)p.K + p.eps);
+    }
 }
 
-// One activation row whose slice has at most 8192 columns: column pairs
-// through registers, thread t holding pairs t, t + NTH, ...; a block's 32
-// columns are the pairs of 16 lanes.
+// One activation row whose slice has at most 8192 columns (nb = 1).  Warp w
+// stages the 128-column chunks w, w + NW, ...: lane l converts column pairs
+// l and l + 32 of a chunk (a block's 32 columns are the pairs of 16 lanes).
+// For Q4_0 the warp then forms the eights product of each of its chunks
+// (eights_chunk) as soon as the chunk is written, so no CTA barrier is added
+// for it.
 template <int FMT, int CLS>
 __device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int tid, int warp, int lane) {
     using C = Cls<CLS>;
     constexpr int NW = C::NW, NTH = NW * 32, GSW = C::GSW;
-    constexpr int RP = 8192 / (2 * NTH);
-    const int Ks = p.Cs * kChunkK;  // staged columns; those at or beyond ke are zero
+    constexpr int RP = 8192 / (2 * NTH);  // pairs per lane at most
+    const int Cs = p.Cs;                  // staged chunks; columns at or beyond ke are zero
     const int kb = q.kb, ke = q.ke;
     const bool norm = p.gamma != nullptr;
     const bool given = FMT == 1 && p.gsum != nullptr && !norm;  // affine sums from the caller
-    const int npass = (Ks / 2 + NTH - 1) / NTH;                 // pairs per thread actually used
+    const int nch = warp < Cs ? (Cs - 1 - warp) / NW + 1 : 0;   // chunks of this warp
     float2 xv[RP], gv[RP];
     // every load first (guarded, not a loop exit, so that they can all be in
-    // flight together)
+    // flight together); pass qq: chunk warp + (qq / 2) * NW, half qq & 1
 #pragma unroll
     for (int qq = 0; qq < RP; ++qq) {
         float2 v = make_float2(0.f, 0.f), gm = make_float2(1.f, 1.f);
-        const int k = kb + 2 * (tid + qq * NTH);
-        if (qq < npass && k < ke) {
-            v = __ldcg(reinterpret_cast<const float2 *>(p.x + k));
-            if (norm) gm = *reinterpret_cast<const float2 *>(p.gamma + k);
+        const int kl = 128 * (warp + (qq >> 1) * NW) + 64 * (qq & 1) + 2 * lane;
+        if ((qq >> 1) < nch && kb + kl < ke) {
+            v = __ldcg(reinterpret_cast<const float2 *>(p.x + kb + kl));
+            if (norm) gm = *reinterpret_cast<const float2 *>(p.gamma + kb + kl);
         }
         xv[qq] = v;
         gv[qq] = gm;
@@ -581,35 +671,37 @@ __device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int
     float ss = 0.f;
 #pragma unroll
     for (int qq = 0; qq < RP; ++qq) {
-        if (qq >= npass) break;
-        const int kl = 2 * (tid + qq * NTH);
-        // warp-uniform: a warp's pairs are 64 consecutive columns and Ks is a multiple of 128
-        if (kl < Ks) {
-            float a0 = xv[qq].x, a1 = xv[qq].y;
-            ss = fmaf(a0, a0, ss);
-            ss = fmaf(a1, a1, ss);
-            if (norm) {
-                a0 *= gv[qq].x;
-                a1 *= gv[qq].y;
-            }
-            float bm = fmaxf(fabsf(a0), fabsf(a1));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-            float sc, back;
-            block_scale(bm, sc, back);
-            put_pair<CLS>(m.xs, 128, 0, kl, a0 * sc, a1 * sc);
-            float bsum = 0.f;
-            if (FMT == 1 && !given) bsum = half_warp_sum(a0 + a1);
-            if ((lane & 15) == 0) {
-                m.fs[gs_idx(kl >> 5, 0, GSW)] = back;
-                if (FMT == 1 && !given) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum;
-            }
+        if ((qq >> 1) >= nch) break;  // warp-uniform
+        const int c = warp + (qq >> 1) * NW;
+        const int kl = 128 * c + 64 * (qq & 1) + 2 * lane;
+        float a0 = xv[qq].x, a1 = xv[qq].y;
+        ss = fmaf(a0, a0, ss);
+        ss = fmaf(a1, a1, ss);
+        if (norm) {
+            a0 *= gv[qq].x;
+            a1 *= gv[qq].y;
+        }
+        float bm = fmaxf(fabsf(a0), fabsf(a1));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+        float sc, back;
+        block_scale(bm, sc, back);
+        put_pair<CLS>(m.xs, 128, 0, kl, a0 * sc, a1 * sc);
+        float bsum = 0.f;
+        if (FMT == 1 && !given) bsum = half_warp_sum(a0 + a1);
+        if ((lane & 15) == 0) {
+            m.fs[gs_idx(kl >> 5, 0, GSW)] = back;
+            if (FMT == 1 && !given) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum;
+        }
+        if (FMT == 0 && (qq & 1)) {  // the chunk is written: its eights product
+            __syncwarp();
+            eights_chunk<CLS>(m, c, lane);
         }
     }
     if (given) {
-        for (int b = tid; b < p.Cs * kBlocksPerChunk; b += NTH)
+        for (int b = tid; b < Cs * kBlocksPerChunk; b += NTH)
             m.gs[gs_idx(b, 0, GSW)] = kb + 32 * b < ke ? __ldcg(p.gsum + kb / 32 + b) : 0.f;
     }
     if (norm) {
@@ -780,6 +872,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
         }
     }
     stage_finish<CLS>(p, m, S, nb, tid);
+    if (CLS == 0 && FMT == 0) eights_c0<CLS>(m, Cs, warp, lane);
 }
 
 template <int I>
@@ -797,9 +890,180 @@ using RingOf = Ring<Cls<CLS>::DU, Cls<CLS>::SU, 2 * Cls<CLS>::SU * (FMT == 0 ? k
 template <int FMT, int CLS>
 using StreamOf = WeightStream<FMT == 0 ? kRecQ4_0 : kRecAffine, Cls<CLS>::NW>;
 
-template <int FMT, int CLS>
+// nb = 1: the unit loop on the chunk-wide product chain (see chunk_b).  Per
+// record: the chain's eight products as two independent chains of four
+// (blocks 0-1 and 2-3; their sum is the single chain's value, since each
+// column only ever adds exact zeros from the other chain's blocks), then one
+// block's offset and scale per lane -- block t's (hi + lo - offset) * d * f
+// for rows g and g+8 (Q4_0; affine: s * f * (hi + lo) + m * block sum) --
+// added to the lane's running sums; the four lanes of a row are added at the
+// end of each tile's slice.  Two records are in flight at a time: the two
+// tiles of a pair unit, or two consecutive chunks of a single-tile stage.
+
+// The chunk's activation registers (chunk_b) and block t's offset term and
+// activation factor, for lane (g, t).
+struct ChunkX {
+    uint4 B[kBlocksPerChunk];
+    float G, F;
+};
+template <int CLS>
+__device__ __forceinline__ void load_chunk(ChunkX &x, const Smem &m, int cc, int boff, int g, int t) {
+    const uint8_t *xchunk = m.xs + cc * kBlocksPerChunk * 128;
+#pragma unroll
+    for (int j = 0; j < kBlocksPerChunk; ++j) x.B[j] = chunk_b(xchunk, j, boff, g);
+    const int gi = gs_idx(cc * kBlocksPerChunk + t, 0, Cls<CLS>::GSW);
+    x.G = m.gs[gi];
+    x.F = m.fs[gi];
+}
+
+// One record at shared address ra against chunk x: this lane's block's share
+// of rows g and g+8, added to a0 and a1.
+template <int FMT>
+__device__ __forceinline__ void record_c0(uint32_t ra, const ChunkX &x, int lane, float &a0, float &a1) {
+    const uint4 w0 = lds128_at<0>(ra + lane * 16);    // row g: word j for block j
+    const uint4 w1 = lds128_at<512>(ra + lane * 16);  // row g + 8
+    uint32_t sw, mw = 0u;                            // scales (mins) of (row g, block t), (row g + 8, block t)
+    asm volatile("ld.shared.u32 %0, [%1+1024];" : "=r"(sw) : "r"(ra + lane * 4) : "memory");
+    if (FMT == 1) asm volatile("ld.shared.u32 %0, [%1+1152];" : "=r"(mw) : "r"(ra + lane * 4) : "memory");
+    const float z = 0.f;
+    float dA[4], dB[4];
+    uint32_t a[8], b[8];
+    unpack_word(w0.x, a[0], a[2], a[4], a[6]);
+    unpack_word(w1.x, a[1], a[3], a[5], a[7]);
+    unpack_word(w0.z, b[0], b[2], b[4], b[6]);
+    unpack_word(w1.z, b[1], b[3], b[5], b[7]);
+    mma16816_c(dA, a[0], a[1], a[2], a[3], x.B[0].x, x.B[0].y, z, z, z, z);
+    mma16816_c(dB, b[0], b[1], b[2], b[3], x.B[2].x, x.B[2].y, z, z, z, z);
+    mma16816(dA, a[4], a[5], a[6], a[7], x.B[0].z, x.B[0].w);
+    mma16816(dB, b[4], b[5], b[6], b[7], x.B[2].z, x.B[2].w);
+    unpack_word(w0.y, a[0], a[2], a[4], a[6]);
+    unpack_word(w1.y, a[1], a[3], a[5], a[7]);
+    unpack_word(w0.w, b[0], b[2], b[4], b[6]);
+    unpack_word(w1.w, b[1], b[3], b[5], b[7]);
+    mma16816(dA, a[0], a[1], a[2], a[3], x.B[1].x, x.B[1].y);
+    mma16816(dB, b[0], b[1], b[2], b[3], x.B[3].x, x.B[3].y);
+    mma16816(dA, a[4], a[5], a[6], a[7], x.B[1].z, x.B[1].w);
+    mma16816(dB, b[4], b[5], b[6], b[7], x.B[3].z, x.B[3].w);
+    const float T0 = (dA[0] + dB[0]) + (dA[1] + dB[1]);  // block t, row g: hi + lo
+    const float T2 = (dA[2] + dB[2]) + (dA[3] + dB[3]);  // row g + 8
+    const float2 s2 = scale_pair<FMT>(sw);
+    if (FMT == 0) {
+        a0 = fmaf(s2.x * x.F, T0 - x.G, a0);
+        a1 = fmaf(s2.y * x.F, T2 - x.G, a1);
+    } else {
+        const float2 m2 = scale_pair<FMT>(mw);
+        a0 = fmaf(m2.x, x.G, fmaf(s2.x * x.F, T0, a0));
+        a1 = fmaf(m2.y, x.G, fmaf(s2.y * x.F, T2, a1));
+    }
+}
+
+template <int FMT, class RING>
+__device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, StreamOf<FMT, 0> &ws,
+                             RING &ring, int warp, int lane, bool cross) {
+    using C = Cls<0>;
+    constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
+    const int g = lane >> 2, t = lane & 3;
+    const int boff = (g & 1) * 64 + t * 16;
+    const int cs = q.cs;
+    float acc[2][2];  // [record][row g, row g + 8]: this lane's block's share
+#pragma unroll
+    for (int rc = 0; rc < 2; ++rc) acc[rc][0] = acc[rc][1] = 0.f;
+    int pl = q.fp, cc = q.ub - q.fp * cs;
+    const int upt = p.upt;
+    if (lane == 0) {  // this warp's range for the fold (visible after the caller's barrier)
+        m.wtab[warp] = q.ub;
+        m.wtab[C::NW + 1 + warp] = q.fp;
+        if (warp == C::NW - 1) m.wtab[C::NW] = q.ue;
+    }
+    float *my_slots = m.slots + (size_t)warp * p.SW * kTileRows;
+
+    // a tile's slice is done: add the four lanes of each row (a fixed
+    // butterfly) and hand the sums to the fold
+    auto flush = [&](int pair, bool two) {
+#pragma unroll
+        for (int rc = 0; rc < 2; ++rc) {
+            if (rc == 0 || two) {
+                float a0 = acc[rc][0], a1 = acc[rc][1];
+                a0 += __shfl_xor_sync(0xffffffffu, a0, 1);
+                a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
+                a0 += __shfl_xor_sync(0xffffffffu, a0, 2);
+                a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
+                if (t == 0) {
+                    float *dst = my_slots + (size_t)(upt * (pair - q.fp) + rc) * kTileRows;
+                    dst[g] = a0;
+                    dst[g + 8] = a1;
+                }
+            }
+            acc[rc][0] = acc[rc][1] = 0.f;
+        }
+    };
+
+    for (int i = 0; i < q.n_my;) {
+        const int n_st = stage_units<C::SU>(upt, cs - cc, q.n_my - i);  // units of this stage
+        if (!ring.wait(p.err, lane)) break;  // gave up: stop (the error is recorded)
+        const uint32_t st_base = ring.stage(ring.cons);
+        i += n_st;
+        if (upt == 2) {
+            for (int su = 0; su < n_st; ++su) {  // a pair unit: its two records side by side
+                const uint32_t st_a = st_base + su * REC;
+                const bool two = q.t0 + 2 * pl + 1 < p.T;
+                ChunkX x;
+                load_chunk<0>(x, m, cc, boff, g, t);
+                record_c0<FMT>(st_a, x, lane, acc[0][0], acc[0][1]);
+                if (two) record_c0<FMT>(st_a + C::SU * REC, x, lane, acc[1][0], acc[1][1]);
+                if (++cc == cs) {  // end of this pair's slice: hand the tiles over
+                    flush(pl, two);
+                    cc = 0;
+                    ++pl;
+                }
+            }
+        } else {
+            // single-tile units: consecutive chunks of one tile (a stage never
+            // crosses the tile's slice), two at a time
+            int su = 0;
+            for (; su + 1 < n_st; su += 2) {
+                ChunkX x0, x1;
+                load_chunk<0>(x0, m, cc, boff, g, t);
+                load_chunk<0>(x1, m, cc + 1, boff, g, t);
+                float b0 = 0.f, b1 = 0.f;
+                record_c0<FMT>(st_base + su * REC, x0, lane, acc[0][0], acc[0][1]);
+                record_c0<FMT>(st_base + (su + 1) * REC, x1, lane, b0, b1);
+                acc[0][0] += b0;
+                acc[0][1] += b1;
+                cc += 2;
+                if (cc == cs) {
+                    flush(pl, false);
+                    cc = 0;
+                    ++pl;
+                }
+            }
+            if (su < n_st) {
+                ChunkX x0;
+                load_chunk<0>(x0, m, cc, boff, g, t);
+                record_c0<FMT>(st_base + su * REC, x0, lane, acc[0][0], acc[0][1]);
+                if (++cc == cs) {
+                    flush(pl, false);
+                    cc = 0;
+                    ++pl;
+                }
+            }
+        }
+        __syncwarp();             // every lane is done with this stage: refill its slot
+        ++ring.cons;
+        ring.push(ws, lane, cross);
+    }
+    if (ring.ok && q.n_my > 0 && cc != 0) flush(pl, upt == 2 && q.t0 + 2 * pl + 1 < p.T);  // ended inside a unit
+}
+
+// cross: whether a refill may move the stream to its next job (false in the
+// persistent kernel, which refills across jobs at the grid barrier).
+template <int FMT, int CLS, class RING>
 __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, StreamOf<FMT, CLS> &ws,
-                          RingOf<FMT, CLS> &ring, int warp, int lane) {
+                          RING &ring, int warp, int lane, bool cross) {
+    if constexpr (CLS == 0) {
+        run_units_c0<FMT>(p, q, m, ws, ring, warp, lane, cross);
+        return;
+    }
     using C = Cls<CLS>;
     constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
     constexpr int NT = C::NT, NGR = C::NGR, NACC = C::NACC;
@@ -869,11 +1133,8 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
 
     for (int i = 0; i < q.n_my;) {
         const int n_st = stage_units<C::SU>(upt, cs - cc, q.n_my - i);  // units of this stage
-        __syncwarp();             // every lane is done with the previous stage: refill it
-        ring.push(ws, lane);
         if (!ring.wait(p.err, lane)) break;  // gave up: stop (the error is recorded)
         const uint32_t st_base = ring.stage(ring.cons);
-        ++ring.cons;
         i += n_st;
       for (int su = 0; su < n_st; ++su) {
         // unit su of the stage: its record(s) at st_base + su*REC (and + SU*REC)
@@ -991,6 +1252,9 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             ++pl;
         }
       }
+        __syncwarp();             // every lane is done with this stage: refill its slot
+        ++ring.cons;
+        ring.push(ws, lane, cross);
     }
     if (ring.ok && q.n_my > 0 && cc != 0) flush(pl, upt == 2 && q.t0 + 2 * pl + 1 < p.T);  // ended inside a unit
 }
@@ -1044,7 +1308,6 @@ __device__ void cluster_finish(const GemvParams &p, const Geo &q, const Smem &m,
     constexpr int NW = Cls<CLS>::NW, NTH = NW * 32;
     const int nb = CLS == 0 ? 1 : p.nb;
     const int tile_vals = kTileRows * nb;
-    const int total = q.tiles_here * tile_vals;
     // rank j finishes units [j*nu/S, (j+1)*nu/S): whole tiles (whole gate/up
     // pairs for SwiGLU).  Every rank pushes its partials of a unit into the
     // owner's shared memory, at red[source rank][position in the slice]
@@ -1185,7 +1448,7 @@ __device__ void argmax_epilogue(const GemvParams &p, const Geo &q, const Smem &m
             bvs[warp] = bv;
             bis[warp] = bi;
         }
-        __syncthreads();
+        csync<NW>();
         if (tid == 0) {
             float fv = bvs[0];
             int fi = bis[0];
@@ -1198,14 +1461,30 @@ __device__ void argmax_epilogue(const GemvParams &p, const Geo &q, const Smem &m
             p.am_val[(size_t)r * p.groups + group] = fv;
             p.am_idx[(size_t)r * p.groups + group] = fi;
         }
-        __syncthreads();
+        csync<NW>();
     }
 }
 
-// Single K-slice, store / residual / SwiGLU jobs: fold each output's warp
-// partials and write it at once.
+// The residual a folding thread adds to its first output (fold_store's
+// thread mapping), loaded as soon as the job starts so that its latency is
+// hidden behind the staging and the unit loop; 0 when there is none.
 template <int CLS>
-__device__ void fold_store(const GemvParams &p, const Geo &q, const Smem &m, int group, int tid) {
+__device__ __forceinline__ float residual_prefetch(const GemvParams &p, const Geo &q, int tid) {
+    constexpr int NTH = Cls<CLS>::NW * 32;
+    const int nb = CLS == 0 ? 1 : p.nb;
+    const int tile_vals = kTileRows * nb;
+    const int tp0 = tid / tile_vals, rem = tid - tp0 * tile_vals;
+    const int row = rem / nb, r = rem - row * nb;
+    if (p.epi != EPI_RESIDUAL || tp0 >= NTH / tile_vals || tp0 >= q.tiles_here) return 0.f;
+    const int n = (q.t0 + tp0) * kTileRows + row;  // single-matrix job
+    return n < p.n[0] ? __ldcg(p.res + (size_t)r * p.n[0] + n) : 0.f;
+}
+
+// Single K-slice, store / residual / SwiGLU jobs: fold each output's warp
+// partials and write it at once.  res0: this thread's first residual, from
+// residual_prefetch.
+template <int CLS>
+__device__ void fold_store(const GemvParams &p, const Geo &q, const Smem &m, int group, int tid, float res0) {
     constexpr int NTH = Cls<CLS>::NW * 32;
     const int nb = CLS == 0 ? 1 : p.nb;
     if (group >= p.groups) return;  // no tiles
@@ -1230,13 +1509,13 @@ __device__ void fold_store(const GemvParams &p, const Geo &q, const Smem &m, int
         if (p.epi == EPI_STORE) {
             p.out[mi][(size_t)r * N + n] = v;
         } else if (p.epi == EPI_RESIDUAL) {
-            p.out[0][(size_t)r * N + n] = v + __ldcg(p.res + (size_t)r * N + n);
+            p.out[0][(size_t)r * N + n] = v + (tp == tp0 ? res0 : __ldcg(p.res + (size_t)r * N + n));
         } else {  // SwiGLU: gate tile, then its up tile
             const float u = fold_one<CLS>(p, q, m, wt, tl + 1, row, r, nb) * f;
             p.out[0][(size_t)r * N + n] = v / (1.0f + expf(-v)) * u;
         }
     }
-    __syncthreads();
+    csync<Cls<CLS>::NW>();
 }
 
 // Copy a job's parameter block into shared memory with one round of
@@ -1252,7 +1531,7 @@ __device__ __forceinline__ void copy_params(GemvParams *dst, const GemvParams *s
 // ---------------------------------------------------------------------------
 // Per-call kernel: one job, one group of tile pairs per cluster.
 template <int FMT, int CLS>
-__global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid_constant__ GemvParams prm) {
+__global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_engine_kernel(const __grid_constant__ GemvParams prm) {
     using C = Cls<CLS>;
     constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
     constexpr int NW = C::NW;
@@ -1267,7 +1546,8 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid
     const int nb = CLS == 0 ? 1 : p.nb;
     const Smem m = carve<CLS>(smem, nb, p.Cs, p.TG, p.SW, S);
     RingOf<FMT, CLS> ring;
-    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * C::SU * REC, smem_u32(m.bars) + warp * C::DU * 8, lane);
+    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * C::SU * REC, smem_u32(m.bars) + warp * C::DU * 8, lane,
+              p.wait_cycles, p.extra_tx);
     // this CTA has started; the matching wait ends the activation staging
     if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
@@ -1278,15 +1558,16 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) gemv_kernel(const __grid
     const Geo q = make_geo<NW>(p, group, rank, warp);
     StreamOf<FMT, CLS> ws;
     ws.init_one(&p, q);
-    for (int s = 0; s < C::DU - 1; ++s) ring.push(ws, lane);
+    for (int s = 0; s < C::DU; ++s) ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    const float res0 = S == 1 ? residual_prefetch<CLS>(p, q, tid) : 0.f;
 
     stage_x<FMT, CLS, CLS == 3 ? 8 : 4, CLS != 0>(p, q, m, S, tid, warp, lane);
-    run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
+    run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane, true);
     ring.drain();
     __syncthreads();
     if (S == 1 && p.epi != EPI_ARGMAX) {
-        fold_store<CLS>(p, q, m, group, tid);
+        fold_store<CLS>(p, q, m, group, tid, res0);
         return;
     }
     if (S > 1) {
@@ -1308,33 +1589,40 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     return v;
 }
 
-// Grid barrier number `b` (1-based).  Each CTA adds one to the arrival
-// counter with a release reduction (no reply to wait for), then polls the
-// counter with acquire loads until all b * gridDim.x arrivals are in.  The
-// wait is bounded: after kBarrierSpins polls the CTA records the failure in
-// *err and the caller stops.
-__device__ __forceinline__ bool grid_barrier(unsigned *counter, int *err, unsigned b) {
-    __syncthreads();
+// Grid barrier number `b` (1-based) over the NW warps of every CTA.  Each
+// CTA adds one to the arrival counter with a release reduction (no reply to
+// wait for), then polls the counter with acquire loads until all
+// b * gridDim.x (+ extra) arrivals are in.  The wait is bounded: after
+// `polls` polls the CTA records the failure in *err and the caller stops.
+// Between its arrival and its wait, each warp runs `work` (the persistent
+// kernel refills its weight ring there).
+template <int NW, class Work>
+__device__ __forceinline__ bool grid_barrier(unsigned *counter, int *err, unsigned b, long long polls,
+                                             unsigned extra, Work &&work) {
+    csync<NW>();
     __shared__ int fail;
     if (threadIdx.x == 0) {
         fail = 0;
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
-        const unsigned target = b * gridDim.x;
+    }
+    work();
+    if (threadIdx.x == 0) {
+        const unsigned target = b * gridDim.x + extra;
         long long it = 0;
         while (ld_acquire_u32(counter) < target) {
-            if (++it > kBarrierSpins) {
+            if (++it > polls) {
                 atomicExch(err, 1);
                 fail = 1;
                 break;
             }
         }
     }
-    __syncthreads();
+    csync<NW>();
     return fail == 0;
 }
 
 template <int FMT, int CLS>
-__global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __grid_constant__ StepParams sp) {
+__global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_step_kernel(const __grid_constant__ StepParams sp) {
     using C = Cls<CLS>;
     constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
     constexpr int NW = C::NW;
@@ -1345,43 +1633,53 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) decode_kernel(const __gr
     const int cs_max = (sp.Kmax + kChunkK - 1) / kChunkK;  // as the host sized it
     const Smem m = carve<CLS>(smem, nb, cs_max, sp.TGmax, sp.SWmax, 1);
     RingOf<FMT, CLS> ring;
-    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * C::SU * REC, smem_u32(m.bars) + warp * C::DU * 8, lane);
+    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * C::SU * REC, smem_u32(m.bars) + warp * C::DU * 8, lane,
+              sp.jobs[0].wait_cycles, sp.jobs[0].extra_tx);
 
     // every job's parameter block in shared memory (after the engine's
     // regions), copied once: the weight stream and the job loop read them there
     GemvParams *jobs = reinterpret_cast<GemvParams *>(m.ring + (size_t)NW * C::DU * 2 * C::SU * REC);
     for (int i = tid; i < sp.njobs * kParamWords; i += NW * 32)
         reinterpret_cast<unsigned long long *>(jobs)[i] = reinterpret_cast<const unsigned long long *>(sp.jobs)[i];
-    __syncthreads();
+    csync<NW>();
     // and this group's span of every job (the divisions, once)
     JobSpan *spans = reinterpret_cast<JobSpan *>(jobs + sp.njobs);
     for (int j = tid; j < sp.njobs; j += NW * 32) spans[j] = span_of(jobs[j], group);
-    __syncthreads();
+    csync<NW>();
     StreamOf<FMT, CLS> ws;
     ws.init(jobs, spans, sp.njobs, group, 0, warp);
-    for (int s = 0; s < C::DU - 1; ++s) ring.push(ws, lane);
+    for (int s = 0; s < C::DU; ++s) ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // at a grid barrier: refill every free slot, moving across jobs
+    auto refill = [&]() {
+        while (ring.push(ws, lane)) {
+        }
+    };
 
     for (int j = 0; j < sp.njobs; ++j) {
         const GemvParams &p = jobs[j];
-        if (j > 0 && !grid_barrier(sp.counter, sp.err, (unsigned)j)) {
+        if (j > 0 &&
+            !grid_barrier<NW>(sp.counter, sp.err, (unsigned)j, sp.barrier_polls, (unsigned)sp.barrier_extra, refill)) {
             ring.drain();
             return;
         }
         const Geo q = geo_of<NW>(p, spans[j], 0, warp);
         if (q.tiles_here == 0) continue;  // no work in this job (CTA-uniform)
+        const float res0 = residual_prefetch<CLS>(p, q, tid);
         stage_x<FMT, CLS, 4, false>(p, q, m, 1, tid, warp, lane);
-        run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane);
-        __syncthreads();
+        run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane, false);
+        csync<NW>();
         if (p.epi != EPI_ARGMAX) {
-            fold_store<CLS>(p, q, m, group, tid);
+            fold_store<CLS>(p, q, m, group, tid, res0);
         } else {
             argmax_epilogue<CLS>(p, q, m, group, tid, warp, lane);
         }
     }
     ring.drain();
     // the last job is the logits argmax: fold the groups' pairs in order
-    if (!grid_barrier(sp.counter, sp.err, (unsigned)sp.njobs)) return;
+    if (!grid_barrier<NW>(sp.counter, sp.err, (unsigned)sp.njobs, sp.barrier_polls, (unsigned)sp.barrier_extra,
+                          [] {}))
+        return;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const GemvParams &pl = jobs[sp.njobs - 1];
     if (group == 0 && tid < 32) {

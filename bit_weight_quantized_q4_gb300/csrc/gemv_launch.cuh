@@ -25,7 +25,7 @@ static bool raise_smem(Kern kern, size_t smem, size_t (&set)[64]) {
 
 template <int FMT, int CLS>
 static int launch_cls(const GemvParams &p, const Plan &plan, cudaStream_t stream) {
-    auto kern = dev::gemv_kernel<FMT, CLS>;
+    auto kern = dev::q4gemv_engine_kernel<FMT, CLS>;
     static size_t smem_set[64] = {0};
     if (!raise_smem(kern, plan.smem, smem_set)) return -1;
     cudaLaunchConfig_t cfg = {};
@@ -62,7 +62,7 @@ static int launch_gemv_fmt(const GemvParams &p, const Plan &plan, cudaStream_t s
 
 template <int FMT, int CLS>
 static int launch_step_cls(const StepParams &p, int ctas, size_t smem, cudaStream_t stream) {
-    auto kern = dev::decode_kernel<FMT, CLS>;
+    auto kern = dev::q4gemv_step_kernel<FMT, CLS>;
     static size_t smem_set[64] = {0};
     if (!raise_smem(kern, smem, smem_set)) return -1;
     cudaLaunchConfig_t cfg = {};
@@ -92,7 +92,7 @@ static int launch_step_fmt(const StepParams &p, int ctas, size_t smem, cudaStrea
 
 template <int FMT, int CLS>
 static int step_occupancy_cls(size_t smem) {
-    auto kern = dev::decode_kernel<FMT, CLS>;
+    auto kern = dev::q4gemv_step_kernel<FMT, CLS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return 0;
     int blocks = 0;

@@ -105,6 +105,9 @@ struct GemvParams {
     float *am_val;               // argmax partials [nb][groups]
     int *am_idx;
     int *err;                    // set nonzero if a kernel wait gave up
+    long long wait_cycles;       // bound of one weight-copy wait (SM clock cycles)
+    int extra_tx;                // bytes a copy stage expects beyond its copies (0; testing the give-up path only)
+    int pad_;
 };
 
 // One CTA group's share of a job: its first tile, tile pairs (units of upt
@@ -117,6 +120,7 @@ struct JobSpan {
 // The persistent decode-step kernel runs these jobs in order, one CTA per SM.
 constexpr int kMaxStepJobs = 4 * 32 + 1;      // four jobs per layer, up to 32 layers, + logits
 constexpr long long kBarrierSpins = 1ll << 22;  // polls before a grid barrier gives up
+constexpr long long kWaitCycles = 1ll << 31;    // about a second: bound of one mbarrier wait
 
 struct StepParams {
     int njobs;
@@ -129,6 +133,9 @@ struct StepParams {
     int *err;                    // set to 1 if a barrier gave up
     int32_t *idx;                // [nb] argmax of the last job
     float *val;                  // [nb] or nullptr
+    long long barrier_polls;     // polls before a grid barrier gives up
+    int barrier_extra;           // arrivals a barrier expects beyond the CTAs (0; testing the give-up path only)
+    int pad_;
     GemvParams jobs[kMaxStepJobs];
 };
 

@@ -222,6 +222,23 @@ q4_status q4_decode_check(const void *workspace, cudaStream_t stream);
  * capture.  Library-specific: the pages have no counterpart. */
 q4_status q4_device_check(cudaStream_t stream);
 
+/* Testing hook for the give-up path of the kernels' bounded waits.  The pages
+ * have no counterpart.  Sets, for every later launch of this process:
+ * barrier_polls, the polls before a grid barrier of q4_decode_step gives up
+ * (<= 0: the default, 2^22); barrier_extra (0 or 1), arrivals each grid
+ * barrier expects beyond its CTAs; copy_wait_cycles, the SM clock cycles
+ * before a wait for a weight-copy stage gives up (<= 0: the default, 2^31,
+ * about a second); copy_extra_bytes (0..4096, a multiple of 16), bytes each
+ * weight-copy stage expects beyond its copies.  A non-zero extra makes every
+ * such wait run out: the kernel then records the failure (q4_decode_check,
+ * q4_device_check), waits for its copies in flight (always bounded by the
+ * default second) and returns with its outputs undefined; nothing faults or
+ * hangs.  q4_debug_wait_limits(0, 0, 0, 0) restores the defaults.  Not for
+ * use while other threads launch this library's kernels.  Q4_ERR_SHAPE on an
+ * argument out of range (nothing changes). */
+q4_status q4_debug_wait_limits(int64_t barrier_polls, int32_t barrier_extra, int64_t copy_wait_cycles,
+                               int32_t copy_extra_bytes);
+
 /* Allocation-free variant of q4_argmax.  The pages have no counterpart: this
  * exists for callers that cannot allocate device memory where they need the
  * argmax, such as a plug-in whose host application owns all device memory and
@@ -230,10 +247,12 @@ q4_status q4_device_check(cudaStream_t stream);
  * Same arguments and results as q4_argmax without the workspace: the pass-1
  * (max, index) pairs live in a 128 KiB array compiled into the library, which
  * every GPU that loads the library holds until the process exits.
- * - Limit: the call needs (groups of its launch plan) x nb pairs of 8 bytes;
- *   ceil(n/16) * nb <= 16382 always fits (the 65536-row logits projection
- *   fits at every nb).  A larger need returns Q4_ERR_WORKSPACE and launches
- *   nothing.
+ * - Limit: the call needs G x nb (max, index) pairs of 8 bytes, G being the
+ *   thread-block groups of its launch plan (G <= ceil(n/16)); it is accepted
+ *   when G x nb <= 16384 (4-byte values rounded up to 16 bytes, then the
+ *   4-byte indices, within the 131072 bytes).  So ceil(n/16) * nb <= 16384
+ *   always fits (the 65536-row logits projection fits at every nb).  A larger
+ *   need returns Q4_ERR_WORKSPACE and launches nothing.
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current) and caches it; make that
  *   first call before any stream capture.

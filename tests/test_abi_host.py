@@ -187,3 +187,12 @@ def test_repack_validation():
     assert L.q4_repack_q4_0(None, 1, 32, buf.ctypes.data, buf.size) == 1
     assert L.q4_repack_q4_0(buf.ctypes.data, 1, 33, buf.ctypes.data, buf.size) == 2
     assert L.q4_repack_q4_0(buf.ctypes.data, 1, 32, buf.ctypes.data, 10) == 2
+
+
+def test_debug_wait_limits_validation():
+    L = q4.lib()
+    assert L.q4_debug_wait_limits(0, 2, 0, 0) == 2          # at most one extra arrival
+    assert L.q4_debug_wait_limits(0, -1, 0, 0) == 2
+    assert L.q4_debug_wait_limits(0, 0, 0, 8) == 2          # bytes in multiples of 16
+    assert L.q4_debug_wait_limits(0, 0, 0, 8192) == 2
+    assert L.q4_debug_wait_limits(0, 0, 0, 0) == 0          # the defaults

@@ -175,3 +175,79 @@ def test_fused_decode_step_small_shapes(q4):
         idx_ref, lref, hid_ref = oracle.decode_step(cfg)
         check_argmax(step.idx.cpu().numpy(), lref, what="small fused argmax")
         assert np.allclose(to_np(step.hid), hid_ref, rtol=2e-3, atol=2e-3)
+
+
+def _teacher_forced_step(q4, cfg, what):
+    """The persistent-kernel step on the first L layers for L = 1..layers:
+    layer L-1's outputs against the oracle run on the GPU's own input of that
+    layer, then the argmax against the oracle on the GPU's final state.
+
+    Within a layer the down projection is checked on the GPU's own h (the
+    kernel keeps the last layer's h): its reference is Wd h_gpu + hid_o, with
+    hid_o the oracle's o projection plus residual of the GPU's layer input.
+    Checking it on the oracle's h instead would charge the down projection
+    with the gate/up error amplified by the SwiGLU, which the per-output
+    bound does not cover when activations are carried as one f16 (nb > 4)."""
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+    step = DecodeStep(cfg)
+    prev = cfg.x.astype(np.float64)
+    for L in range(1, len(cfg.layers) + 1):
+        step.run_fused(n_layers=L)
+        q4.q4_decode_check(step.step_ws)
+        ref = oracle.decode_layer(cfg.layers[L - 1], prev, cfg.eps)
+        tag = "%s layer %d" % (what, L - 1)
+        check(to_np(step.q), ref["q"], ref["Sq"], what=tag + " q")
+        check(to_np(step.k), ref["k"], ref["Sk"], what=tag + " k")
+        check(to_np(step.v), ref["v"], ref["Sv"], what=tag + " v")
+        check_swiglu(to_np(step.h), ref["g"], ref["Sg"], ref["u"], ref["Su"], what=tag + " gus")
+        hid_ref, Sd = oracle.q4_res_gemv(oracle._hw(cfg.layers[L - 1].Wd), to_np(step.h), ref["hid_o"])
+        bound_extra = 1e-3 * ref["So"] + 2.0 ** -22 * np.abs(hid_ref)
+        check(to_np(step.hid), hid_ref, Sd, extra=bound_extra, what=tag + " hid")
+        prev = to_np(step.hid)
+    _, lref, Sl = oracle.q4_argmax(oracle._hw(cfg.Wlogits), prev, cfg.gamma_final, cfg.eps)
+    check_argmax(step.idx.cpu().numpy(), lref, what=what + " argmax")
+    rows = np.arange(cfg.x.shape[0])
+    best = lref[rows, step.idx.cpu().numpy()]
+    assert np.all(np.abs(to_np(step.val) - best) <= 1e-3 * Sl.max(axis=1) + 1e-6), what + " argmax value"
+    return step
+
+
+# (fmt, nb, layers, hidden, kv, inter, vocab): every batch class in both
+# formats, ragged shapes, and the 32-layer maximum
+STEP_CASES = [
+    ("affine", 1, 3, 256, 64, 384, 1000),
+    ("affine", 3, 2, 160, 48, 96, 333),
+    ("q4_0", 5, 2, 256, 64, 384, 1000),
+    ("affine", 5, 2, 192, 32, 320, 777),
+    ("q4_0", 8, 2, 192, 64, 320, 500),
+    ("affine", 8, 2, 256, 64, 384, 1000),
+    ("q4_0", 16, 2, 256, 64, 384, 1000),
+    ("affine", 16, 2, 160, 48, 224, 333),
+    ("q4_0", 1, 32, 128, 32, 192, 300),
+    ("affine", 2, 32, 128, 32, 192, 300),
+]
+
+
+@pytest.mark.parametrize("fmt,nb,layers,hidden,kv,inter,vocab", STEP_CASES)
+def test_fused_step_every_class_and_format(q4, fmt, nb, layers, hidden, kv, inter, vocab):
+    cfg = wl.cfg4(seed=13, layers=layers, hidden=hidden, kv=kv, inter=inter, vocab=vocab, nb=nb, fmt=fmt)
+    _teacher_forced_step(q4, cfg, "fused %s nb=%d L=%d" % (fmt, nb, layers))
+
+
+def test_fused_step_full_size_nb5(q4):
+    # the workload's shapes (hidden 2048, inter 8192, 65536 logits) with a
+    # batch of 5 rows: the one-f16 activation class
+    cfg = wl.cfg4(seed=14, layers=2, nb=5)
+    _teacher_forced_step(q4, cfg, "fused full nb=5")
+
+
+@pytest.mark.parametrize("nb", [8, 16])
+def test_fused_step_rejects_what_one_cta_cannot_stage(q4, nb):
+    # at inter 8192 a batch of 8 or more rows needs more shared memory per
+    # CTA than there is: the call says so and launches nothing
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+    cfg = wl.cfg4(seed=15, layers=1, hidden=2048, kv=512, inter=8192, vocab=256, nb=nb)
+    step = DecodeStep(cfg)
+    with pytest.raises(q4.Q4Error) as e:
+        step.run_fused()
+    assert e.value.status == 4
