@@ -345,6 +345,31 @@ def e2e_timing(step, graph, steps: int, warmup: int):
     return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
+def stream_ceiling(Ws, bench_calls, peak: float, tag: str) -> dict:
+    """What one launch of a library kernel reaches on the same packed bytes,
+    over the same rotation and back-to-back graph as the GEMV rows: a
+    device-to-device copy (cudaMemcpyAsync through tensor.copy_; it reads
+    and writes every byte) and a library reduction that only reads them (a
+    sum over their int32 view).  The per-launch ceiling for streaming this
+    many bytes once, measured beside the GEMV on every run."""
+    import torch
+    nbytes = Ws[0].tensor.numel()
+    dsts = [torch.empty_like(W.tensor) for W in Ws]
+    by_id = {id(W): i for i, W in enumerate(Ws)}
+    t_copy = bench_calls(Ws, lambda W: dsts[by_id[id(W)]].copy_(W.tensor))
+    t_read = bench_calls(Ws, lambda W: W.tensor.view(torch.int32).sum())
+    del dsts
+    return {
+        tag + "_copy": {"us": round(t_copy * 1e6, 3), "read_gbs": round(nbytes / t_copy / 1e9, 1),
+                        "read_write_gbs": round(2 * nbytes / t_copy / 1e9, 1),
+                        "frac_of_hbm": round(2 * nbytes / t_copy / 1e9 / peak, 4),
+                        "what": "device-to-device copy of the packed bytes (reads and writes each byte)"},
+        tag + "_library_read": {"us": round(t_read * 1e6, 3), "read_gbs": round(nbytes / t_read / 1e9, 1),
+                                "frac_of_hbm": round(nbytes / t_read / 1e9 / peak, 4),
+                                "what": "torch int32 sum over the packed bytes: a library kernel reading each byte once"},
+    }
+
+
 def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     """Per-shape cold timings of single calls: a graph of `reps` back-to-back
     calls over rotating weight copies whose total exceeds 3x L2."""
@@ -393,6 +418,8 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
             gbs = W0.weight_bytes / t / 1e9
             out["%s_n%d_k%d_nb%d" % (fmt, n, k, nb)] = {"us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1),
                                                       "frac_of_hbm": round(gbs / peak, 4)}
+        if fmt == "q4_0":
+            out.update(stream_ceiling(Ws, bench_calls, peak, "%s_n%d_k%d" % (fmt, n, k)))
         del Ws
         torch.cuda.empty_cache()
     # the fused calls at the small workload shapes (cfg 0..2), cold: each
@@ -465,6 +492,7 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     out["q4_0_n%d_k%d_nb1" % (n4, k)] = {"us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1),
                                          "frac_of_hbm": round(gbs / peak, 4),
                                          "what": "4x the rows of the 14336 x 4096 case: launch overhead amortised"}
+    out.update(stream_ceiling(Ws, bench_calls, peak, "q4_0_n%d_k%d" % (n4, k)))
     del Ws
     torch.cuda.empty_cache()
     return out
@@ -503,6 +531,23 @@ def run_one_gemv(args) -> dict:
     q4.q4_device_check()
     return {"gemv": args.gemv, "calls": args.steps, "us_per_call_warm_l2": round(e0.elapsed_time(e1) * 1e3 / args.steps, 3),
             "note": "one weight reused: warm L2 for matrices under 129 MB; the kernel table times cold weights"}
+
+
+def workload_config(args, wbytes: int, l2: int, world: int) -> dict:
+    """The `config` object of both arms (same keys, same values)."""
+    return {"workload": WORKLOAD, "layers": args.layers, "nb": 1, "weight_bytes_per_step": wbytes,
+            "l2": "inputs larger than L2: %d weight bytes per step vs %d B L2" % (wbytes, l2),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def l2_bytes() -> int:
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0) or 0)
+    except Exception:
+        pass
+    return 0
 
 
 def run_ours(args, rank, world, local):
@@ -564,7 +609,7 @@ def run_ours(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline_sample(cfg, wbytes, budget_s=12.0)
+        cpu = cpu_baseline_sample(cfg, wbytes, budget_s=8.0)
 
     if rank != 0:
         return None
@@ -581,13 +626,11 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
-        "precision": "Q4_0 nibbles exact in f16; activations scaled per 32-column block by a power of two and split into f16 hi+lo; fp32 accumulate",
+        "dtype": "f16 hi+lo activations x exact f16 nibbles, f32 accumulate",
+        "precision": "Q4_0 nibbles exact in f16; activations scaled per 32-column block by a power of two and split into f16 hi+lo (about 22 significant bits); fp32 accumulate",
         "data": "synthetic (seeded PCG64; q~U{0..15}, d~U[0.005,0.02] fp16, x~N(0,1), gamma=1+0.1N(0,1))",
-        "config": {"workload": WORKLOAD, "layers": args.layers, "nb": 1, "kernels_per_step": 1,
-                   "weight_bytes_per_step": wbytes,
-                   "l2": "inputs larger than L2: %d weight bytes per step vs %d B L2" % (wbytes, l2),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": workload_config(args, wbytes, l2, world),
+        "kernels_per_step": 1,
         "gpu_launches": 1 * args.steps,
         "clocks": clk,
         "e2e": {"value": round(job_rate(wbytes, args.steps, world, e2e_max), 2), "unit": "GB/s",
@@ -612,22 +655,60 @@ def run_ours(args, rank, world, local):
 
 # ---------------------------------------------------------- oracle arms
 
-def cpu_baseline_sample(cfg, wbytes: int, budget_s: float = 12.0) -> dict:
-    """The f64 C oracle (single thread) on whole decode steps of the same
-    workload, repeated until about `budget_s` seconds have passed."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _oracle_steps(cfg, threads: int, budget_s: float, max_steps: int):
+    import oracle
+    old = oracle.set_threads(threads)
+    try:
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            oracle.decode_step(cfg)
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or n >= max_steps:
+                return n, el
+    finally:
+        oracle.set_threads(old)
+
+
+def cpu_baseline_sample(cfg, wbytes: int, budget_s: float = 8.0) -> dict:
+    """The f64 C oracle on whole decode steps of the same workload: on all
+    host cores (the output rows of every GEMV split over threads; rows are
+    independent and each output is computed by the same code), and on one
+    thread, each repeated until about `budget_s` seconds have passed."""
     import oracle
     oracle.build()
-    t0 = time.perf_counter()
-    n = 0
-    while True:
-        oracle.decode_step(cfg)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or n >= 10:
-            break
-    return {"value": round(wbytes * n / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d full decode step(s) (%d weight bytes each) in the f64 C oracle, 1 thread, %.1f s"
-                      % (n, wbytes, el)}
+    cores = os.cpu_count() or 1
+    n_all, el_all = _oracle_steps(cfg, cores, budget_s, 40)
+    n_one, el_one = _oracle_steps(cfg, 1, budget_s, 10)
+    return {"value": round(wbytes * n_all / el_all / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d full decode step(s) (%d weight bytes each) in the f64 C oracle on %d threads, %.1f s"
+                      % (n_all, wbytes, cores, el_all),
+            "cpu_model": cpu_model(), "nproc": cores,
+            "ms_per_step": round(el_all * 1e3 / n_all, 1),
+            "single_thread": {"value": round(wbytes * n_one / el_one / 1e9, 4), "unit": "GB/s", "cores": 1,
+                              "ms_per_step": round(el_one * 1e3 / n_one, 1),
+                              "sample": "%d full decode step(s) on 1 thread, %.1f s" % (n_one, el_one)}}
 
 
 def run_reference(args, rank, world):
@@ -661,9 +742,11 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded PCG64, same workload as the GPU arm)",
-        "config": {"workload": WORKLOAD, "layers": args.layers, "nb": 1, "weight_bytes_per_step": wbytes},
+        "config": workload_config(args, wbytes, l2_bytes(), world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "one full decode step per timed step in the f64 C oracle, 1 thread"},
+                         "sample": "one full decode step per timed step in the f64 C oracle, 1 thread "
+                                   "(this arm is single-threaded; the GPU arm's cpu_baseline also reports all cores)",
+                         "cpu_model": cpu_model(), "nproc": os.cpu_count() or 1},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
