@@ -636,7 +636,7 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": round(job_rate(wbytes, args.steps, world, e2e_max), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_max * 1e3 / args.steps, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "roofline": {"kernel": "decode_kernel (q4_decode_step: the whole step, one persistent kernel)",
+        "roofline": {"kernel": "q4gemv_step_kernel (q4_decode_step: the whole step, one persistent kernel)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src + " (MEASURED_PEAKS hbm_gbs)",
                      "algorithmic_bytes_per_launch": wbytes, "launch_us": round(k_us, 3),
