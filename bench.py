@@ -418,6 +418,17 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
             gbs = W0.weight_bytes / t / 1e9
             out["%s_n%d_k%d_nb%d" % (fmt, n, k, nb)] = {"us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1),
                                                       "frac_of_hbm": round(gbs / peak, 4)}
+        if fmt == "affine":
+            # the same matvec fed a HalfSet (f16 even/odd streams + group sums,
+            # packed once): what a caller verifying several drafts per step runs
+            for nb in (8, 16):
+                x = torch.from_numpy(wl.draw_x(rng, nb, k)).to(device)
+                xe, xo, gs = q4.q4_pack_half(x)
+                y = torch.empty((nb, n), dtype=torch.float32, device=device)
+                t = bench_calls(Ws, lambda W: q4.q4_gemv_half(W, xe, xo, gsum=gs, out=y))
+                gbs = W0.weight_bytes / t / 1e9
+                out["%s_n%d_k%d_nb%d_halfset" % (fmt, n, k, nb)] = {
+                    "us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
         if fmt == "q4_0":
             out.update(stream_ceiling(Ws, bench_calls, peak, "%s_n%d_k%d" % (fmt, n, k)))
         del Ws

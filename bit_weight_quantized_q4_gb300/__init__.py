@@ -8,7 +8,8 @@ no CPU fallback: if the library is missing the calls raise.
 
 Entry points (same names as the C ABI in ``include/q4gemv.h``):
 ``q4_gemv``, ``q4_nrm_gemv``, ``q4_dual_gemv``, ``q4_gus_nrm``,
-``q4_res_gemv``, ``q4_argmax``, ``q4_group_sums``; plus ``Q4Weight`` for
+``q4_res_gemv``, ``q4_argmax``, ``q4_group_sums``, ``q4_pack_half``,
+``q4_gemv_half``; plus ``Q4Weight`` for
 repacking host weights into the device layout.
 """
 from __future__ import annotations
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
             "q4_unpack_affine": (I32, [P, SZ, I32, I32, P, P, P]),
             "q4_group_sums": (I32, [P, I32, I32, P, P]),
             "q4_gemv": (I32, [W, P, P, I32, P, P]),
+            "q4_pack_half": (I32, [P, I32, I32, P, P, P, P]),
+            "q4_gemv_half": (I32, [W, P, P, P, I32, P, P]),
             "q4_nrm_gemv": (I32, [W, P, P, F, I32, P, P]),
             "q4_dual_gemv": (I32, [W, W, P, P, F, I32, P, P, P]),
             "q4_gus_nrm": (I32, [W, W, P, P, F, I32, P, P]),
@@ -291,6 +294,41 @@ def q4_gemv(W: Q4Weight, x, gsum=None, out=None):
     if gsum is not None:
         gp = _dev_f32(gsum, "gsum", (nb, W.k // 32)).data_ptr()
     _check(lib().q4_gemv(W.cref(), x.data_ptr(), gp, nb, out.data_ptr(), _stream()), "q4_gemv")
+    return out
+
+
+def q4_pack_half(x, with_gsum: bool = True):
+    """The HalfSet of fp32 activations ``x [nb, k]``: ``(x_even, x_odd,
+    gsum)`` -- float16 ``[nb, k/2]`` streams of the even- and odd-indexed
+    elements and the fp32 per-32 group sums of the f16 values (or None)."""
+    torch = _torch()
+    x = _dev_f32(x, "x")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    nb, k = x.shape
+    xe = torch.empty((nb, k // 2), dtype=torch.float16, device=x.device)
+    xo = torch.empty((nb, k // 2), dtype=torch.float16, device=x.device)
+    gs = torch.empty((nb, k // 32), dtype=torch.float32, device=x.device) if with_gsum else None
+    _check(lib().q4_pack_half(x.data_ptr(), nb, k, xe.data_ptr(), xo.data_ptr(),
+                              None if gs is None else gs.data_ptr(), _stream()), "q4_pack_half")
+    return xe, xo, gs
+
+
+def q4_gemv_half(W: Q4Weight, x_even, x_odd, gsum=None, out=None):
+    """``y = W x`` for a batch given as a HalfSet (see ``q4_pack_half``)."""
+    torch = _torch()
+    if x_even.dim() == 1:
+        x_even, x_odd = x_even.view(1, -1), x_odd.view(1, -1)
+    nb = x_even.shape[0]
+    dev = x_even.device
+    x_even = _dev_buf(x_even, "x_even", torch.float16, (nb, W.k // 2), dev)
+    x_odd = _dev_buf(x_odd, "x_odd", torch.float16, (nb, W.k // 2), dev)
+    gp = None
+    if gsum is not None:
+        gp = _dev_buf(gsum, "gsum", torch.float32, (nb, W.k // 32), dev).data_ptr()
+    out = _out(out, (nb, W.n), x_even)
+    _check(lib().q4_gemv_half(W.cref(), x_even.data_ptr(), x_odd.data_ptr(), gp, nb, out.data_ptr(), _stream()),
+           "q4_gemv_half")
     return out
 
 

@@ -1,4 +1,6 @@
-// aux_kernels.cu -- the argmax fold (pass 2) and the activation group sums.
+// aux_kernels.cu -- the argmax fold (pass 2), the activation group sums and
+// the HalfSet packing.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -73,6 +75,37 @@ __global__ void __launch_bounds__(256) q4gemv_group_sums_kernel(const float *x, 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// HalfSet packing (Module gpu, Struct HalfSet): each activation rounded to
+// f16 (nearest, ties to even), the even-indexed elements of a row into
+// x_even, the odd-indexed into x_odd, and the per-32 group sums of the f16
+// values (as fp32) into gsum, added by block8_sum -- the order the GEMV's
+// staging uses, so either source gives the same bits.  Eight lanes per group,
+// four columns each.
+__global__ void __launch_bounds__(256) q4gemv_pack_half_kernel(const float *x, int nb, int k, uint16_t *xe,
+                                                               uint16_t *xo, float *gsum) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int G = k / 32;
+    const int total = nb * G;
+    const int lane = threadIdx.x & 31;
+    const int gi_all = (blockIdx.x * 256 + threadIdx.x) >> 3;  // (row, group) index
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    size_t e0 = 0;
+    if (gi_all < total) {
+        const int r = gi_all / G, gi = gi_all - r * G;
+        const size_t off = (size_t)r * k + 32 * gi + 4 * (lane & 7);
+        const float4 a = *reinterpret_cast<const float4 *>(x + off);
+        const __half2 ev = __floats2half2_rn(a.x, a.z), od = __floats2half2_rn(a.y, a.w);
+        e0 = off >> 1;
+        *reinterpret_cast<__half2 *>(xe + e0) = ev;
+        *reinterpret_cast<__half2 *>(xo + e0) = od;
+        const float2 fe = __half22float2(ev), fo = __half22float2(od);
+        v = make_float4(fe.x, fo.x, fe.y, fo.y);
+    }
+    const float t = block8_sum(v);
+    if (gi_all < total && (lane & 7) == 0 && gsum != nullptr) gsum[gi_all] = t;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace dev
 
 static int launch_pdl(const void *func, dim3 grid, dim3 block, void **args, cudaStream_t stream) {
@@ -92,6 +125,13 @@ int launch_argmax_fold(const float *am_val, const int *am_idx, int groups, int n
                        float *val, void *stream) {
     void *args[] = {(void *)&am_val, (void *)&am_idx, (void *)&groups, (void *)&idx, (void *)&val};
     return launch_pdl((const void *)dev::q4gemv_argmax_fold_kernel, dim3(nb), dim3(256), args,
+                      (cudaStream_t)stream);
+}
+
+int launch_pack_half(const float *x, int nb, int k, uint16_t *xe, uint16_t *xo, float *gsum, void *stream) {
+    void *args[] = {(void *)&x, (void *)&nb, (void *)&k, (void *)&xe, (void *)&xo, (void *)&gsum};
+    const int total = nb * (k / 32);  // 8 threads per group
+    return launch_pdl((const void *)dev::q4gemv_pack_half_kernel, dim3((8 * total + 255) / 256), dim3(256), args,
                       (cudaStream_t)stream);
 }
 

@@ -14,6 +14,7 @@ namespace q4 {
 int launch_argmax_fold(const float *am_val, const int *am_idx, int groups, int nb, int32_t *idx,
                        float *val, void *stream);
 int launch_group_sums(const float *x, int nb, int k, float *gsum, void *stream);
+int launch_pack_half(const float *x, int nb, int k, uint16_t *xe, uint16_t *xo, float *gsum, void *stream);
 }  // namespace q4
 
 namespace {
@@ -203,6 +204,37 @@ q4_status q4_gemv(const q4_weight *W, const float *x, const float *gsum, int32_t
     if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
     if (gsum && !aligned16(gsum)) return Q4_ERR_ALIGN;
     q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, x, nullptr, 0.f, nb);
+    p.gsum = W->fmt == Q4_FMT_AFFINE ? gsum : nullptr;
+    p.epi = q4::EPI_STORE;
+    p.out[0] = y;
+    return run(p, W->fmt, stream);
+}
+
+q4_status q4_pack_half(const float *x, int32_t nb, int32_t k, uint16_t *x_even, uint16_t *x_odd, float *gsum,
+                       cudaStream_t stream) {
+    Q4_TRY(check_act(x));
+    Q4_TRY(check_act(x_even));
+    Q4_TRY(check_act(x_odd));
+    if (gsum && !aligned16(gsum)) return Q4_ERR_ALIGN;
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    if (!shape_ok(1, k)) return Q4_ERR_SHAPE;
+    cudaGetLastError();
+    if (q4::launch_pack_half(x, nb, k, x_even, x_odd, gsum, stream) != 0 || cudaGetLastError() != cudaSuccess)
+        return Q4_ERR_CUDA;
+    return Q4_OK;
+}
+
+q4_status q4_gemv_half(const q4_weight *W, const uint16_t *x_even, const uint16_t *x_odd, const float *gsum,
+                       int32_t nb, float *y, cudaStream_t stream) {
+    Q4_TRY(check_weight(W));
+    Q4_TRY(check_act(x_even));
+    Q4_TRY(check_act(x_odd));
+    Q4_TRY(check_act(y));
+    if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
+    if (gsum && !aligned16(gsum)) return Q4_ERR_ALIGN;
+    q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, nullptr, nullptr, 0.f, nb);
+    p.xe = x_even;
+    p.xo = x_odd;
     p.gsum = W->fmt == Q4_FMT_AFFINE ? gsum : nullptr;
     p.epi = q4::EPI_STORE;
     p.out[0] = y;

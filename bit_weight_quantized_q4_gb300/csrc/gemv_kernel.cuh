@@ -587,6 +587,28 @@ __device__ void eights_c0(const Smem &m, int Cs, int warp, int lane) {
     csync<Cls<CLS>::NW>();
 }
 
+// Activation loads of the staging: columns (k, k+1) or (k .. k+3) of the row
+// starting at element `roff` of x, read from the fp32 rows, or from the
+// HalfSet streams (Module gpu, Struct HalfSet), where x[2i] is element i of
+// the even stream and x[2i+1] element i of the odd stream, each an f16.
+__device__ __forceinline__ float half_at(const uint16_t *s, size_t i) {
+    return __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(s) + i)));
+}
+__device__ __forceinline__ float2 load_x2(const GemvParams &p, size_t roff, int k) {
+    if (p.xe == nullptr) return __ldcg(reinterpret_cast<const float2 *>(p.x + roff + k));
+    const size_t i = (roff + k) >> 1;
+    return make_float2(half_at(p.xe, i), half_at(p.xo, i));
+}
+__device__ __forceinline__ float4 load_x4(const GemvParams &p, size_t roff, int k) {
+    if (p.xe == nullptr) return __ldcg(reinterpret_cast<const float4 *>(p.x + roff + k));
+    const size_t i = (roff + k) >> 1;  // even: one f16 pair per stream
+    const unsigned e = __ldcg(reinterpret_cast<const unsigned *>(p.xe + i));
+    const unsigned o = __ldcg(reinterpret_cast<const unsigned *>(p.xo + i));
+    const float2 fe = __half22float2(*reinterpret_cast<const __half2 *>(&e));
+    const float2 fo = __half22float2(*reinterpret_cast<const __half2 *>(&o));
+    return make_float4(fe.x, fo.x, fe.y, fo.y);
+}
+
 // After the writes: the staging barrier, then each row's output factor --
 // its inverse RMS from the warps' partial sums of squares in warp order (and,
 // for a split K, the cluster ranks' slice sums in rank order), or 1.
@@ -662,7 +684,7 @@ __device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int
         float2 v = make_float2(0.f, 0.f), gm = make_float2(1.f, 1.f);
         const int kl = 128 * (warp + (qq >> 1) * NW) + 64 * (qq & 1) + 2 * lane;
         if ((qq >> 1) < nch && kb + kl < ke) {
-            v = __ldcg(reinterpret_cast<const float2 *>(p.x + kb + kl));
+            v = load_x2(p, 0, kb + kl);
             if (norm) gm = *reinterpret_cast<const float2 *>(p.gamma + kb + kl);
         }
         xv[qq] = v;
@@ -756,7 +778,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f), g = make_float4(1.f, 1.f, 1.f, 1.f);
             const int k = kb + 128 * c + 4 * lane;
             if (base + j < s1 && k < ke) {
-                v = __ldcg(reinterpret_cast<const float4 *>(p.x + (size_t)r * p.K + k));
+                v = load_x4(p, (size_t)r * p.K, k);
                 if (norm) g = __ldg(reinterpret_cast<const float4 *>(p.gamma + k));
             }
             xv[j] = v;

@@ -95,7 +95,8 @@ struct GemvParams {
     int S;                       // K-split: CTAs per cluster
     int Cs;                      // chunks per K-slice
     int groups;                  // groups; group g holds units [g*P/groups, (g+1)*P/groups) of the P = T/upt
-    const float *x;              // [nb][K]
+    const float *x;              // [nb][K], or nullptr when the activations come as a HalfSet (xe, xo)
+    const uint16_t *xe, *xo;     // HalfSet: f16 bits of x[r][2i] and x[r][2i+1], [nb][K/2] each; or nullptr
     const float *gamma;          // [K] or nullptr (no RMSNorm)
     float eps;
     const float *gsum;           // affine: caller group sums [nb][K/32] or nullptr

@@ -150,6 +150,27 @@ q4_status q4_gus_nrm(const q4_weight *Wg, const q4_weight *Wu, const float *x,
 q4_status q4_res_gemv(const q4_weight *W, const float *x, const float *r_in, int32_t nb,
                       float *y, cudaStream_t stream);
 
+/* HalfSet packing (Module gpu, Struct HalfSet: "half even/odd streams plus
+ * per-32 group sums", the input format of the multi-row Q4 matvecs).  For each
+ * activation row r of x ([nb][k] fp32, device): x_even[r][i] = f16(x[r][2i])
+ * and x_odd[r][i] = f16(x[r][2i+1]) ([nb][k/2] f16 bits each, device;
+ * round to nearest, ties to even), and gsum[r][g] ([nb][k/32] fp32, device,
+ * or NULL for none) = the fp32 sum of the 32 f16 values of group g, added in
+ * the order q4_group_sums and the GEMV's own staging use.  A caller that
+ * runs several multi-row matvecs on one batch (speculative verification)
+ * converts once.  Same validation as q4_group_sums. */
+q4_status q4_pack_half(const float *x, int32_t nb, int32_t k, uint16_t *x_even, uint16_t *x_odd, float *gsum,
+                       cudaStream_t stream);
+
+/* y = W x for nb rows (1..16) given as a HalfSet: x[r][2i] = x_even[r][i],
+ * x[r][2i+1] = x_odd[r][i] (f16 bits, [nb][k/2] each, device).  gsum
+ * ([nb][k/32] fp32, device): for affine weights the group sums of those f16
+ * values (q4_pack_half writes them), or NULL to have the kernel form them; it
+ * must match the streams; ignored for Q4_0.  Results are those of q4_gemv on
+ * the f16 values widened to fp32 (bit for bit). */
+q4_status q4_gemv_half(const q4_weight *W, const uint16_t *x_even, const uint16_t *x_odd, const float *gsum,
+                       int32_t nb, float *y, cudaStream_t stream);
+
 /* Workspace bytes q4_argmax needs for an n-row logits projection and nb rows. */
 size_t q4_argmax_workspace_bytes(int32_t n, int32_t nb);
 

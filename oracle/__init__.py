@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
         L.q4o_gemv.argtypes = [ctypes.c_int, P, P, P, I64, I64, P, I64, P, P, P]
         L.q4o_gemv_rows.argtypes = [ctypes.c_int, P, P, P, I64, I64, P, I64, P, P, P, I64, I64]
         L.q4o_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double, P]
+        L.q4o_halfset_rows.argtypes = [P, P, I64, I64, P]
         L.q4o_silu.restype = ctypes.c_double
         L.q4o_silu.argtypes = [ctypes.c_double]
         L.q4o_swiglu.argtypes = [P, P, I64, P]
@@ -246,6 +247,27 @@ def argmax(v) -> int:
 def q4_gemv(W: HostWeight, x):
     """Plain dequant-in-GEMV: returns (y, S)."""
     return gemv(W, x)
+
+
+def halfset_rows(x_even, x_odd) -> np.ndarray:
+    """HalfSet activations as f64 rows ``[nb, k]``: element ``2i`` of a row
+    from the even stream, ``2i+1`` from the odd one (f16 bit patterns,
+    ``uint16[nb, k/2]`` each; Module gpu, Struct HalfSet)."""
+    xe = np.ascontiguousarray(x_even, dtype=np.uint16)
+    xo = np.ascontiguousarray(x_odd, dtype=np.uint16)
+    if xe.ndim == 1:
+        xe, xo = xe[None, :], xo[None, :]
+    assert xe.shape == xo.shape
+    nb, h = xe.shape
+    x = np.empty((nb, 2 * h), dtype=np.float64)
+    lib().q4o_halfset_rows(_p(xe), _p(xo), nb, 2 * h, _p(x))
+    return x
+
+
+def q4_gemv_half(W: HostWeight, x_even, x_odd):
+    """GEMV over a HalfSet batch (the multi-row matvec's input format):
+    returns (y, S) as ``q4_gemv`` on the decoded rows."""
+    return gemv(W, halfset_rows(x_even, x_odd))
 
 
 def q4_nrm_gemv(W: HostWeight, x, gamma, eps):

@@ -143,6 +143,18 @@ void q4o_gemv(int fmt, const void *a, const void *b, const void *c,
     q4o_gemv_rows(fmt, a, b, c, n, k, x, nb, y, bound, wrow, 0, n);
 }
 
+/* HalfSet activations (Module gpu, Struct HalfSet: half even/odd streams)
+ * as f64 rows: x[r][2i] = half(xe[r][i]), x[r][2i+1] = half(xo[r][i]).
+ * xe, xo: [nb][k/2] f16 bits; x: [nb][k]. */
+void q4o_halfset_rows(const uint16_t *xe, const uint16_t *xo, int64_t nb, int64_t k, double *x)
+{
+    for (int64_t r = 0; r < nb; ++r)
+        for (int64_t i = 0; i < k / 2; ++i) {
+            x[r * k + 2 * i] = q4o_half(xe[r * (k / 2) + i]);
+            x[r * k + 2 * i + 1] = q4o_half(xo[r * (k / 2) + i]);
+        }
+}
+
 /* xhat[r][e] = x[r][e] / sqrt(mean_e' x[r][e']^2 + eps) * gamma[e]. */
 void q4o_rmsnorm(const double *x, const double *gamma, int64_t nb, int64_t k,
                  double eps, double *xhat)

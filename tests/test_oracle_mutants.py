@@ -34,6 +34,10 @@ MUTANTS = [
     ("swiglu factors swapped", "h[i] = q4o_silu(g[i]) * u[i];", "h[i] = q4o_silu(u[i]) * g[i];"),
     ("residual subtracted", "out[i] = a[i] + b[i];", "out[i] = a[i] - b[i];"),
     ("argmax tie to last", "if (v[i] > v[best])", "if (v[i] >= v[best])"),
+    ("halfset streams swapped", "x[r * k + 2 * i] = q4o_half(xe[r * (k / 2) + i]);",
+     "x[r * k + 2 * i] = q4o_half(xo[r * (k / 2) + i]);"),
+    ("halfset rows concatenated", "x[r * k + 2 * i + 1] = q4o_half(xo[r * (k / 2) + i]);",
+     "x[r * k + k / 2 + i] = q4o_half(xo[r * (k / 2) + i]);"),
 ]
 
 

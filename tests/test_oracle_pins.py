@@ -424,3 +424,35 @@ def test_threaded_rows_give_the_same_bits(fmt):
     finally:
         oracle.set_threads(old)
     assert np.array_equal(y1, y7) and np.array_equal(S1, S7)
+
+
+def test_halfset_rows_interleave_and_decode():
+    # HalfSet reading: element 2i of a row from the even stream, 2i+1 from
+    # the odd one; every f16 bit pattern decodes as numpy's float16 does
+    rng = np.random.default_rng(6)
+    bits = rng.integers(0, 1 << 16, size=(4, 256), dtype=np.uint16)
+    bits[(bits & 0x7C00) == 0x7C00] = 0x3C00          # finite values only (no inf / NaN)
+    x = oracle.halfset_rows(bits[:, 0::2], bits[:, 1::2])
+    assert np.array_equal(x, bits.view(np.float16).astype(np.float64))
+
+
+def test_halfset_gemv_one_hot_and_equivalence():
+    rng = np.random.default_rng(7)
+    n, k = 40, 128
+    H = wl.draw_q4_0(rng, n, k)
+    W = oracle._hw(H)
+    dense = oracle.dequant(W)
+    # a one in the even stream at i is column 2i, in the odd stream column 2i + 1
+    for i in (0, 5, 63):
+        e = np.zeros((1, k // 2), np.float16)
+        o = np.zeros((1, k // 2), np.float16)
+        e[0, i] = 1.0
+        y, _ = oracle.q4_gemv_half(W, e.view(np.uint16), o.view(np.uint16))
+        assert np.array_equal(y[0], dense[:, 2 * i])
+        y, _ = oracle.q4_gemv_half(W, o.view(np.uint16), e.view(np.uint16))
+        assert np.array_equal(y[0], dense[:, 2 * i + 1])
+    # and the HalfSet of f16 activations gives the plain GEMV of those values
+    x16 = rng.standard_normal((3, k)).astype(np.float16)
+    y1, S1 = oracle.q4_gemv_half(W, x16[:, 0::2].view(np.uint16), x16[:, 1::2].view(np.uint16))
+    y2, S2 = oracle.q4_gemv(W, x16.astype(np.float64))
+    assert np.array_equal(y1, y2) and np.array_equal(S1, S2)
