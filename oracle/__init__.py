@@ -11,6 +11,9 @@ bytes before any device repack) and computes in IEEE double precision:
   endian) then 16 nibble bytes; element ``i`` of a block is the low nibble of
   byte ``i`` and element ``i+16`` its high nibble; ``w = d*(q-8)``
   (crate inferencelayer, Functions: q4_0_to_q8_0n, gemv_q1_k_lcpp_src).
+* ``q8_0``: blocks ``uint8[n, k/32, 34]`` -- fp16 scale ``d`` then 32
+  signed bytes; ``w = d*q`` (crate inferencelayer, Functions: q4_0_to_q8_0n,
+  gemv_q8_0n_k_lcpp_src).
 * ``affine``: nibbles ``uint8[n, k/2]`` (element ``2i`` low nibble of byte
   ``i``, ``2i+1`` high nibble), ``s`` and ``m`` as bf16 bits
   ``uint16[n, k/32]``; ``w = s*q + m`` (Module gpu, Structs Q and HalfSet).
@@ -40,6 +43,7 @@ _LIB = os.path.join(_HERE, "libq4oracle.so")
 
 FMT_Q4_0 = 0
 FMT_AFFINE = 1
+FMT_Q8_0 = 2
 
 
 def build(force: bool = False) -> str:
@@ -82,6 +86,7 @@ def lib() -> ctypes.CDLL:
         L.q4o_bf16.restype = ctypes.c_double
         L.q4o_bf16.argtypes = [ctypes.c_uint16]
         L.q4o_q4_0_row.argtypes = [P, I64, I64, P]
+        L.q4o_q8_0_row.argtypes = [P, I64, I64, P]
         L.q4o_affine_row.argtypes = [P, P, P, I64, I64, P]
         L.q4o_gemv.argtypes = [ctypes.c_int, P, P, P, I64, I64, P, I64, P, P, P]
         L.q4o_gemv_rows.argtypes = [ctypes.c_int, P, P, P, I64, I64, P, I64, P, P, P, I64, I64]
@@ -120,6 +125,8 @@ class HostWeight:
         self.a = np.ascontiguousarray(self.a, dtype=np.uint8)
         if self.fmt == FMT_Q4_0:
             assert self.a.size == self.n * (self.k // 32) * 18
+        elif self.fmt == FMT_Q8_0:
+            assert self.a.size == self.n * (self.k // 32) * 34
         else:
             assert self.a.size == self.n * self.k // 2
             self.s = np.ascontiguousarray(self.s, dtype=np.uint16)
@@ -129,6 +136,10 @@ class HostWeight:
     @staticmethod
     def q4_0(blocks: np.ndarray, n: int, k: int) -> "HostWeight":
         return HostWeight(FMT_Q4_0, n, k, blocks)
+
+    @staticmethod
+    def q8_0(blocks: np.ndarray, n: int, k: int) -> "HostWeight":
+        return HostWeight(FMT_Q8_0, n, k, blocks)
 
     @staticmethod
     def affine(nib: np.ndarray, s: np.ndarray, m: np.ndarray, n: int, k: int) -> "HostWeight":
@@ -152,6 +163,8 @@ def dequant_row(W: HostWeight, row: int) -> np.ndarray:
     out = np.empty(W.k, dtype=np.float64)
     if W.fmt == FMT_Q4_0:
         lib().q4o_q4_0_row(_p(W.a), W.k, row, _p(out))
+    elif W.fmt == FMT_Q8_0:
+        lib().q4o_q8_0_row(_p(W.a), W.k, row, _p(out))
     else:
         lib().q4o_affine_row(_p(W.a), _p(W.s), _p(W.m), W.k, row, _p(out))
     return out
@@ -323,7 +336,9 @@ def q4_argmax(W: HostWeight, x, gamma=None, eps=0.0):
 # gpu, module sampling.  The attention output is the layer's given stand-in.
 
 def _hw(H) -> HostWeight:
-    """The oracle's view of a generator's host weight (either format)."""
+    """The oracle's view of a generator's host weight (any format)."""
+    if hasattr(H, "blocks8"):
+        return HostWeight.q8_0(H.blocks8, H.n, H.k)
     if hasattr(H, "blocks"):
         return HostWeight.q4_0(H.blocks, H.n, H.k)
     return HostWeight.affine(H.nib, H.s, H.m, H.n, H.k)

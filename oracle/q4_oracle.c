@@ -20,6 +20,10 @@
  *    the 16 bytes is not stated on the pages; the reading taken is the GGUF
  *    order the pages read as-is (gemv_q8_0n_k_lcpp_src): byte i holds element i
  *    in its low nibble and element i+16 in its high nibble.
+ *  - Q8_0 block (32 weights in 34 bytes: fp16 scale d, then 32 signed bytes;
+ *    weight = d * q): crate inferencelayer, Functions, entries q4_0_to_q8_0n
+ *    (the lossless upcast of a Q4_0 block keeps d and maps q to nib - 8) and
+ *    gemv_q8_0n_k_lcpp_src (Q8_0 blocks read as-is).
  *  - Affine-Q4 group (32 weights, bf16 scale s and bf16 min m, weight =
  *    s*q + m): Module gpu (qwen4_exp), Structs Q (affine-Q4 projection with
  *    byte offsets into a bf16 weight buffer) and HalfSet (even/odd streams plus
@@ -88,6 +92,23 @@ void q4o_q4_0_row(const uint8_t *blocks, int64_t k, int64_t row, double *w)
     }
 }
 
+/* One row of Q8_0 weights, dequantised to f64: blocks of 34 bytes, the fp16
+ * scale d (little endian) then 32 signed bytes q; weight = d * q.
+ * blocks: [n][k/32][34] bytes; w: [k]. */
+void q4o_q8_0_row(const uint8_t *blocks, int64_t k, int64_t row, double *w)
+{
+    int64_t nblk = k / 32;
+    const uint8_t *r = blocks + row * nblk * 34;
+    for (int64_t b = 0; b < nblk; ++b) {
+        const uint8_t *blk = r + b * 34;
+        double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));
+        for (int j = 0; j < 32; ++j) {
+            int q = blk[2 + j] < 128 ? blk[2 + j] : blk[2 + j] - 256;   /* two's complement byte */
+            w[b * 32 + j] = d * (double)q;
+        }
+    }
+}
+
 /* One row of affine-Q4 weights, dequantised to f64.
  * nib: [n][k/2] bytes; s, m: [n][k/32] bf16 bits; w: [k]. */
 void q4o_affine_row(const uint8_t *nib, const uint16_t *s, const uint16_t *m,
@@ -109,7 +130,7 @@ void q4o_affine_row(const uint8_t *nib, const uint16_t *s, const uint16_t *m,
  * bound[r][i] = sum_k |w[i][k]| * |x[r][k]| (the scale of the parity tolerance),
  * for the output rows i in [row0, row1) (rows are independent; callers may
  * run disjoint ranges at the same time, each with its own scratch).
- * fmt 0: a = Q4_0 blocks.  fmt 1: a = nibbles, b = s, c = m.
+ * fmt 0: a = Q4_0 blocks.  fmt 1: a = nibbles, b = s, c = m.  fmt 2: a = Q8_0 blocks.
  * x: [nb][k] f64; y, bound: [nb][n]; wrow: scratch of k doubles. */
 void q4o_gemv_rows(int fmt, const void *a, const void *b, const void *c,
                    int64_t n, int64_t k, const double *x, int64_t nb,
@@ -118,6 +139,8 @@ void q4o_gemv_rows(int fmt, const void *a, const void *b, const void *c,
     for (int64_t i = row0; i < row1; ++i) {
         if (fmt == 0)
             q4o_q4_0_row((const uint8_t *)a, k, i, wrow);
+        else if (fmt == 2)
+            q4o_q8_0_row((const uint8_t *)a, k, i, wrow);
         else
             q4o_affine_row((const uint8_t *)a, (const uint16_t *)b,
                            (const uint16_t *)c, k, i, wrow);

@@ -11,6 +11,8 @@ Host storage formats (the readings of the pages, stated once):
 * Q4_0: ``uint8[n, k/32, 18]``; bytes 0-1 = fp16 scale ``d`` little endian;
   bytes 2..17 = 16 nibble bytes, byte ``i`` holding element ``i`` in its low
   nibble and element ``i + 16`` in its high nibble (GGUF order).
+* Q8_0: ``uint8[n, k/32, 34]``; bytes 0-1 = fp16 scale ``d``; bytes 2..33 =
+  the 32 weights as signed bytes (two's complement).
 * affine-Q4: nibbles ``uint8[n, k/2]`` with byte ``i`` holding element ``2i``
   (low nibble) and ``2i + 1`` (high nibble); ``s`` and ``m`` as bf16 bit
   patterns ``uint16[n, k/32]``.
@@ -52,6 +54,19 @@ def pack_q4_0(q: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
     return out
 
 
+def pack_q8_0(q: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
+    """Pack signed bytes ``q[n, k]`` (-128..127) and fp16 scale bits
+    ``d_bits[n, k/32]`` into Q8_0 host blocks ``uint8[n, k/32, 34]``."""
+    n, k = q.shape
+    nb = k // 32
+    out = np.empty((n, nb, 34), dtype=np.uint8)
+    d = np.ascontiguousarray(d_bits, dtype=np.uint16).reshape(n, nb)
+    out[:, :, 0] = (d & 0xFF).astype(np.uint8)
+    out[:, :, 1] = (d >> 8).astype(np.uint8)
+    out[:, :, 2:] = q.astype(np.int8).reshape(n, nb, 32).view(np.uint8)
+    return out
+
+
 def pack_affine_nibbles(q: np.ndarray) -> np.ndarray:
     """Pack nibbles ``q[n, k]`` into ``uint8[n, k/2]`` (even element low)."""
     q = q.astype(np.uint8)
@@ -63,6 +78,13 @@ class Q4_0Host:
     n: int
     k: int
     blocks: np.ndarray          # uint8[n, k/32, 18]
+
+
+@dataclass
+class Q8_0Host:
+    n: int
+    k: int
+    blocks8: np.ndarray         # uint8[n, k/32, 34]
 
 
 @dataclass
@@ -80,6 +102,26 @@ def draw_q4_0(rng: np.random.Generator, n: int, k: int, d_range=D_RANGE) -> Q4_0
     q = rng.integers(0, 16, size=(n, k), dtype=np.uint8)
     d = rng.uniform(d_range[0], d_range[1], size=(n, k // 32)).astype(np.float16)
     return Q4_0Host(n, k, pack_q4_0(q, d.view(np.uint16)))
+
+
+def draw_q8_0(rng: np.random.Generator, n: int, k: int, d_range=(0.0003, 0.0012)) -> Q8_0Host:
+    """q ~ U{-128..127}, d ~ U[d_range] rounded to fp16 (the scale range gives
+    weights of the magnitude of the Q4_0 draws)."""
+    assert k % 32 == 0
+    q = rng.integers(-128, 128, size=(n, k), dtype=np.int16)
+    d = rng.uniform(d_range[0], d_range[1], size=(n, k // 32)).astype(np.float16)
+    return Q8_0Host(n, k, pack_q8_0(q, d.view(np.uint16)))
+
+
+def q4_0_to_q8_0(H: Q4_0Host) -> Q8_0Host:
+    """The lossless upcast of Q4_0 blocks to Q8_0 (same d, q8 = nibble - 8):
+    a storage re-encoding, used by the tests as an identity between formats."""
+    b = H.blocks
+    nib = np.concatenate([b[:, :, 2:] & 0x0F, b[:, :, 2:] >> 4], axis=2).astype(np.int16) - 8
+    out = np.empty((H.n, H.k // 32, 34), dtype=np.uint8)
+    out[:, :, :2] = b[:, :, :2]
+    out[:, :, 2:] = nib.astype(np.int8).view(np.uint8)
+    return Q8_0Host(H.n, H.k, out)
 
 
 def draw_affine(rng: np.random.Generator, n: int, k: int,
@@ -212,7 +254,9 @@ def _draw_fmt(fmt: str):
         return draw_q4_0
     if fmt == "affine":
         return draw_affine
-    raise ValueError("fmt must be 'q4_0' or 'affine'")
+    if fmt == "q8_0":
+        return draw_q8_0
+    raise ValueError("fmt must be 'q4_0', 'affine' or 'q8_0'")
 
 
 def cfg4_layer(seed: int, layer: int, hidden: int = 2048, kv: int = 512,

@@ -16,8 +16,8 @@ MUTANTS = [
      "int q = (qs[j / 2] >> (4 * (j & 1))) & 0x0f;"),
     ("q4_0 offset dropped", "w[b * 32 + j] = d * (double)(q - 8);", "w[b * 32 + j] = d * (double)q;"),
     ("q4_0 offset sign", "w[b * 32 + j] = d * (double)(q - 8);", "w[b * 32 + j] = d * (double)(8 - q);"),
-    ("fp16 scale byte order", "double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));",
-     "double d = q4o_half((uint16_t)(blk[1] | (blk[0] << 8)));"),
+    ("fp16 scale byte order", "double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));\n        const uint8_t *qs",
+     "double d = q4o_half((uint16_t)(blk[1] | (blk[0] << 8)));\n        const uint8_t *qs"),
     ("fp16 exponent bias", "v = ldexp((double)(f | 0x400), e - 25);", "v = ldexp((double)(f | 0x400), e - 24);"),
     ("fp16 subnormal scale", "v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
     ("bf16 exponent bias", "v = ldexp((double)(f | 0x80), e - 134);", "v = ldexp((double)(f | 0x80), e - 133);"),
@@ -34,6 +34,11 @@ MUTANTS = [
     ("swiglu factors swapped", "h[i] = q4o_silu(g[i]) * u[i];", "h[i] = q4o_silu(u[i]) * g[i];"),
     ("residual subtracted", "out[i] = a[i] + b[i];", "out[i] = a[i] - b[i];"),
     ("argmax tie to last", "if (v[i] > v[best])", "if (v[i] >= v[best])"),
+    ("q8_0 bytes read unsigned", "int q = blk[2 + j] < 128 ? blk[2 + j] : blk[2 + j] - 256;",
+     "int q = blk[2 + j];"),
+    ("q8_0 block stride", "const uint8_t *blk = r + b * 34;", "const uint8_t *blk = r + b * 32;"),
+    ("q8_0 scale byte order", "double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));\n        for (int j = 0; j < 32; ++j) {\n            int q = blk[2 + j]",
+     "double d = q4o_half((uint16_t)(blk[1] | (blk[0] << 8)));\n        for (int j = 0; j < 32; ++j) {\n            int q = blk[2 + j]"),
     ("halfset streams swapped", "x[r * k + 2 * i] = q4o_half(xe[r * (k / 2) + i]);",
      "x[r * k + 2 * i] = q4o_half(xo[r * (k / 2) + i]);"),
     ("halfset rows concatenated", "x[r * k + 2 * i + 1] = q4o_half(xo[r * (k / 2) + i]);",

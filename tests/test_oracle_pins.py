@@ -456,3 +456,43 @@ def test_halfset_gemv_one_hot_and_equivalence():
     y1, S1 = oracle.q4_gemv_half(W, x16[:, 0::2].view(np.uint16), x16[:, 1::2].view(np.uint16))
     y2, S2 = oracle.q4_gemv(W, x16.astype(np.float64))
     assert np.array_equal(y1, y2) and np.array_equal(S1, S2)
+
+
+def test_q8_0_decode_every_byte():
+    # every signed byte value, against numpy's own int8 and float16 reading
+    rng = np.random.default_rng(8)
+    n, k = 8, 256
+    q = np.arange(-128, 128, dtype=np.int16).reshape(8, 32)
+    q = np.repeat(q[:, None, :], k // 32, axis=1).reshape(n, k)
+    d = rng.uniform(0.0003, 0.0012, (n, k // 32)).astype(np.float16)
+    H = wl.Q8_0Host(n, k, wl.pack_q8_0(q, d.view(np.uint16)))
+    blk = H.blocks8
+    ref = blk[:, :, 0:2].copy().view("<f2")[:, :, 0].astype(np.float64)[:, :, None] * \
+        blk[:, :, 2:].view(np.int8).astype(np.float64)
+    assert np.array_equal(oracle.dequant(oracle._hw(H)), ref.reshape(n, k))
+
+
+def test_q8_0_upcast_of_q4_0_is_the_same_matrix():
+    # crate inferencelayer, q4_0_to_q8_0n: the upcast keeps d and maps a
+    # nibble q to q - 8, so both decoders must give the same weights
+    rng = np.random.default_rng(9)
+    H = wl.draw_q4_0(rng, 33, 160)
+    H8 = wl.q4_0_to_q8_0(H)
+    assert np.array_equal(oracle.dequant(oracle._hw(H)), oracle.dequant(oracle._hw(H8)))
+    x = wl.draw_x(rng, 2, 160)
+    assert np.array_equal(oracle.q4_gemv(oracle._hw(H), x)[0], oracle.q4_gemv(oracle._hw(H8), x)[0])
+
+
+def test_q8_0_brute_force_fsum():
+    rng = np.random.default_rng(10)
+    H = wl.draw_q8_0(rng, 12, 96)
+    x = wl.draw_x(rng, 2, 96)
+    y, S = oracle.q4_gemv(oracle._hw(H), x)
+    blk = H.blocks8
+    dense = (blk[:, :, 0:2].copy().view("<f2")[:, :, 0].astype(np.float64)[:, :, None] *
+             blk[:, :, 2:].view(np.int8).astype(np.float64)).reshape(12, 96)
+    for r in range(2):
+        for i in range(12):
+            terms = dense[i] * x[r].astype(np.float64)
+            assert abs(y[r, i] - math.fsum(terms)) <= 1e-12 * math.fsum(np.abs(terms))
+            assert abs(S[r, i] - math.fsum(np.abs(terms))) <= 1e-12 * S[r, i]
