@@ -399,18 +399,20 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
             best = t if best is None else min(best, t)
         return best / n_calls
 
-    for fmt in ("affine", "q4_0"):
-        H = wl.draw_affine(rng, n, k) if fmt == "affine" else wl.draw_q4_0(rng, n, k)
+    for fmt in ("affine", "q4_0", "q8_0"):
+        H = wl._draw_fmt(fmt)(rng, n, k)
         W0 = (q4.Q4Weight.from_affine(H.nib, H.s, H.m, n, k, device) if fmt == "affine"
+              else q4.Q4Weight.from_q8_0(H.blocks8, n, k, device) if fmt == "q8_0"
               else q4.Q4Weight.from_q4_0(H.blocks, n, k, device))
         copies = max(2, -(-3 * l2_bytes // W0.nbytes))
         host = W0.tensor.cpu().numpy()
         Ws = [W0] + [q4.Q4Weight(W0.fmt, n, k, host, device) for _ in range(copies - 1)]
-        # context: a vendor reduction (torch.amax) reading the same packed bytes, same rotation
-        t_ref = bench_calls(Ws, lambda W: torch.amax(W.tensor))
-        out["%s_n%d_k%d_vendor_read" % (fmt, n, k)] = {
-            "us": round(t_ref * 1e6, 3), "packed_gbs": round(W0.nbytes / t_ref / 1e9, 1),
-            "what": "torch.amax over the packed weight bytes: a library kernel reading the same bytes"}
+        if fmt != "q8_0":
+            # context: a vendor reduction (torch.amax) reading the same packed bytes, same rotation
+            t_ref = bench_calls(Ws, lambda W: torch.amax(W.tensor))
+            out["%s_n%d_k%d_vendor_read" % (fmt, n, k)] = {
+                "us": round(t_ref * 1e6, 3), "packed_gbs": round(W0.nbytes / t_ref / 1e9, 1),
+                "what": "torch.amax over the packed weight bytes: a library kernel reading the same bytes"}
         for nb in ((1, 2, 4, 8, 16) if fmt == "affine" else (1,)):
             x = torch.from_numpy(wl.draw_x(rng, nb, k)).to(device)
             y = torch.empty((nb, n), dtype=torch.float32, device=device)

@@ -145,14 +145,38 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &r0, uint32_t &
     r2 = w8 & 0x000F000Fu;
     r3 = w8 & 0x00F000F0u;
 }
-// The A registers of a block whose every nibble is 8.
+// The A registers of a block whose every nibble is 8 (Q4_0), and of a Q8_0
+// block whose every weight is 0 (every biased byte 128): the value of a zero
+// weight in the format's A encoding, for the registers of k positions 0..7
+// (lo) and 8..15 (hi) of a k16 step.
 constexpr uint32_t kEightLo = 0x00080008u;
 constexpr uint32_t kEightHi = 0x00800080u;
+template <int FMT>
+__device__ __forceinline__ constexpr uint32_t zero_lo() { return FMT == 2 ? 0x00800080u : kEightLo; }
+
+// Two biased Q8_0 bytes -> one tensor-core A register of exact f16
+// subnormals u * 2^-24: bytes 0-1 of w (sel 0x4140) or bytes 2-3 (0x4342)
+// into the low byte of each half.
+template <unsigned SEL>
+__device__ __forceinline__ uint32_t bytes_to_half2(uint32_t w) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(w), "n"(SEL));
+    return r;
+}
+// A registers of one block of a Q8_0 record for rows g (a[0], a[2], a[4],
+// a[6]) and g + 8 (odd): lo / hi are the lane's two words of the block.
+__device__ __forceinline__ void unpack_q8(uint32_t lo, uint32_t hi, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    r0 = bytes_to_half2<0x4140>(lo);
+    r1 = bytes_to_half2<0x4342>(lo);
+    r2 = bytes_to_half2<0x4140>(hi);
+    r3 = bytes_to_half2<0x4342>(hi);
+}
 
 // The two 16-bit scales (or mins) of a scale word as fp32.
 template <int FMT>
 __device__ __forceinline__ float2 scale_pair(uint32_t w) {
-    if (FMT == 0) {
+    if (FMT != 1) {  // fp16 scales (Q4_0, Q8_0); affine: bf16
         __half2 h = *reinterpret_cast<const __half2 *>(&w);
         return __half22float2(h);
     } else {
@@ -482,16 +506,19 @@ __device__ __forceinline__ Smem carve(uint8_t *smem, int nb, int Cs, int TG, int
 
 // The activation scale of a block: 2^e with bound * 2^e in [2^10, 2^11), from
 // the exponent field of `bound` (e clamped to [-100, 100]; 0 for a zero or
-// non-finite bound), and the factor back 2^(20-e), which also undoes the
-// 2^-20 unit of the products.
+// non-finite bound), and the factor back 2^(U-e), which also undoes the 2^-U
+// unit of the products: U = 20 for the nibble formats (their lower nibbles
+// meet activations times 16), 24 for Q8_0 (bytes are f16 subnormals u * 2^-24).
+template <int FMT>
 __device__ __forceinline__ void block_scale(float bound, float &scale, float &back) {
+    constexpr int U = FMT == 2 ? 24 : 20;
     int e = 0;
     if (bound > 0.f && bound <= 3.0e38f) {
         const int be = (int)((__float_as_uint(bound) >> 23) & 0xFF);  // bound in [2^(be-127), 2^(be-126))
         e = max(-100, min(100, 10 - (be - 127)));
     }
     scale = __uint_as_float((uint32_t)(127 + e) << 23);
-    back = __uint_as_float((uint32_t)(127 + 20 - e) << 23);
+    back = __uint_as_float((uint32_t)(127 + U - e) << 23);
 }
 
 // Byte offset in the staged slice of element kk (0..31) of 32-column block
@@ -508,11 +535,12 @@ __device__ __forceinline__ int xs_off(int b, int r, int kk, int part, int xbs) {
 }
 
 // Store columns (kl, kl+1) of row r, already scaled, as hi + lo f16 pairs;
-// positions 0..7 of a k16 step carry the factor 16 of the lower nibbles.
-template <int CLS>
+// for the nibble formats, positions 0..7 of a k16 step carry the factor 16 of
+// the lower nibbles.
+template <int FMT, int CLS>
 __device__ __forceinline__ void put_pair(uint8_t *xs, int xbs, int r, int kl, float v0, float v1) {
     const int b = kl >> 5, kk = kl & 31;
-    if ((kk & 8) == 0) {
+    if (FMT != 2 && (kk & 8) == 0) {
         v0 *= 16.f;
         v1 *= 16.f;
     }
@@ -559,8 +587,9 @@ __device__ __forceinline__ uint4 chunk_b(const uint8_t *xchunk, int j, int boff,
 // to the block-sum slot of block j.  A weight block of all eights then gives
 // exactly the same chain values, so (hi + lo) - offset is exactly zero for it.
 // Runs after the staging barrier; ends with a CTA barrier.
-template <int CLS>
+template <int FMT, int CLS>
 __device__ __forceinline__ void eights_chunk(const Smem &m, int c, int lane) {
+    constexpr uint32_t EL = zero_lo<FMT>();
     constexpr int GSW = Cls<CLS>::GSW;
     const int g = lane >> 2, t = lane & 3;
     const int boff = (g & 1) * 64 + t * 16;
@@ -571,19 +600,19 @@ __device__ __forceinline__ void eights_chunk(const Smem &m, int c, int lane) {
     for (int j = 0; j < kBlocksPerChunk; ++j) {
         const uint4 b = chunk_b(xchunk, j, boff, g);
         if (j == 0) {
-            mma16816_c(d, kEightLo, kEightLo, kEightHi, kEightHi, b.x, b.y, z, z, z, z);
+            mma16816_c(d, EL, EL, kEightHi, kEightHi, b.x, b.y, z, z, z, z);
         } else {
-            mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, b.x, b.y);
+            mma16816(d, EL, EL, kEightHi, kEightHi, b.x, b.y);
         }
-        mma16816(d, kEightLo, kEightLo, kEightHi, kEightHi, b.z, b.w);
+        mma16816(d, EL, EL, kEightHi, kEightHi, b.z, b.w);
     }
     if (g == 0) m.gs[gs_idx(c * kBlocksPerChunk + t, 0, GSW)] = d[0] + d[1];
 }
 // All chunks, after the staging barrier (the generic staging path of nb = 1,
 // slices over 8192 columns); ends with a CTA barrier.
-template <int CLS>
+template <int FMT, int CLS>
 __device__ void eights_c0(const Smem &m, int Cs, int warp, int lane) {
-    for (int c = warp; c < Cs; c += Cls<CLS>::NW) eights_chunk<CLS>(m, c, lane);
+    for (int c = warp; c < Cs; c += Cls<CLS>::NW) eights_chunk<FMT, CLS>(m, c, lane);
     csync<Cls<CLS>::NW>();
 }
 
@@ -709,17 +738,17 @@ __device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
         float sc, back;
-        block_scale(bm, sc, back);
-        put_pair<CLS>(m.xs, 128, 0, kl, a0 * sc, a1 * sc);
+        block_scale<FMT>(bm, sc, back);
+        put_pair<FMT, CLS>(m.xs, 128, 0, kl, a0 * sc, a1 * sc);
         float bsum = 0.f;
         if (FMT == 1 && !given) bsum = half_warp_sum(a0 + a1);
         if ((lane & 15) == 0) {
             m.fs[gs_idx(kl >> 5, 0, GSW)] = back;
             if (FMT == 1 && !given) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum;
         }
-        if (FMT == 0 && (qq & 1)) {  // the chunk is written: its eights product
+        if (FMT != 1 && (qq & 1)) {  // the chunk is written: its eights (zero-weight) product
             __syncwarp();
-            eights_chunk<CLS>(m, c, lane);
+            eights_chunk<FMT, CLS>(m, c, lane);
         }
     }
     if (given) {
@@ -767,7 +796,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
     float ss = 0.f;
     int rcur = r0;
 
-    const float f16x = (lane & 2) ? 1.f : 16.f;
+    const float f16x = FMT == 2 || (lane & 2) ? 1.f : 16.f;  // the lower nibbles' factor 16
     constexpr int LO = 64, P2 = 16;  // lo part (nb <= 4), second column pair
     const int lane_off = (lane >> 3) * xbs + (lane & 1) * 32 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4;
     // a batch's loads are predicated, not branched around, so that they are
@@ -819,7 +848,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
             float sc, back;
-            block_scale(bm, sc, back);
+            block_scale<FMT>(bm, sc, back);
             const float f = sc * f16x;
             const __half2 h0 = __floats2half2_rn(a.x * f, a.y * f);
             const __half2 h1 = __floats2half2_rn(a.z * f, a.w * f);
@@ -894,7 +923,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
         }
     }
     stage_finish<CLS>(p, m, S, nb, tid);
-    if (CLS == 0 && FMT == 0) eights_c0<CLS>(m, Cs, warp, lane);
+    if (CLS == 0 && FMT != 1) eights_c0<FMT, CLS>(m, Cs, warp, lane);
 }
 
 template <int I>
@@ -908,9 +937,9 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v) {
 // Each tile's partial over this warp's chunks goes to one of its slots.
 // Consumes one ring stage per unit and refills it from `ws`.
 template <int FMT, int CLS>
-using RingOf = Ring<Cls<CLS>::DU, Cls<CLS>::SU, 2 * Cls<CLS>::SU * (FMT == 0 ? kRecQ4_0 : kRecAffine)>;
+using RingOf = Ring<Cls<CLS>::DU, stage_su(FMT, CLS), 2 * stage_su(FMT, CLS) * rec_bytes(FMT)>;
 template <int FMT, int CLS>
-using StreamOf = WeightStream<FMT == 0 ? kRecQ4_0 : kRecAffine, Cls<CLS>::NW>;
+using StreamOf = WeightStream<rec_bytes(FMT), Cls<CLS>::NW>;
 
 // nb = 1: the unit loop on the chunk-wide product chain (see chunk_b).  Per
 // record: the chain's eight products as two independent chains of four
@@ -938,30 +967,57 @@ __device__ __forceinline__ void load_chunk(ChunkX &x, const Smem &m, int cc, int
     x.F = m.fs[gi];
 }
 
+// A lane's weight words of one record: the nibble formats' two 16-byte words
+// (rows g and g+8, word j for block j), or Q8_0's four (rows g and g+8,
+// blocks 0-1 and 2-3).  regs<J>() gives the eight tensor-core A registers of
+// block J: rows g (even) and g+8 (odd), k positions in unpack_word's order.
+template <int FMT>
+struct RecWords {
+    uint4 w[FMT == 2 ? 4 : 2];
+    __device__ __forceinline__ void load(uint32_t ra, int lane) {
+        w[0] = lds128_at<0>(ra + lane * 16);
+        w[1] = lds128_at<FMT == 2 ? 1024 : 512>(ra + lane * 16);
+        if constexpr (FMT == 2) {
+            w[2] = lds128_at<512>(ra + lane * 16);
+            w[3] = lds128_at<1536>(ra + lane * 16);
+        }
+    }
+    template <int J>
+    __device__ __forceinline__ void regs(uint32_t (&a)[8]) const {
+        if constexpr (FMT == 2) {
+            const uint4 &r0 = w[J < 2 ? 0 : 2], &r1 = w[J < 2 ? 1 : 3];
+            unpack_q8((J & 1) ? r0.z : r0.x, (J & 1) ? r0.w : r0.y, a[0], a[2], a[4], a[6]);
+            unpack_q8((J & 1) ? r1.z : r1.x, (J & 1) ? r1.w : r1.y, a[1], a[3], a[5], a[7]);
+        } else {
+            unpack_word(J == 0 ? w[0].x : J == 1 ? w[0].y : J == 2 ? w[0].z : w[0].w, a[0], a[2], a[4], a[6]);
+            unpack_word(J == 0 ? w[1].x : J == 1 ? w[1].y : J == 2 ? w[1].z : w[1].w, a[1], a[3], a[5], a[7]);
+        }
+    }
+};
+// Byte offset of the scale words in a record, and of the mins (affine).
+template <int FMT>
+__device__ __forceinline__ constexpr int scale_off() { return FMT == 2 ? 2048 : 1024; }
+
 // One record at shared address ra against chunk x: this lane's block's share
 // of rows g and g+8, added to a0 and a1.
 template <int FMT>
 __device__ __forceinline__ void record_c0(uint32_t ra, const ChunkX &x, int lane, float &a0, float &a1) {
-    const uint4 w0 = lds128_at<0>(ra + lane * 16);    // row g: word j for block j
-    const uint4 w1 = lds128_at<512>(ra + lane * 16);  // row g + 8
+    RecWords<FMT> rw;
+    rw.load(ra, lane);
     uint32_t sw, mw = 0u;                            // scales (mins) of (row g, block t), (row g + 8, block t)
-    asm volatile("ld.shared.u32 %0, [%1+1024];" : "=r"(sw) : "r"(ra + lane * 4) : "memory");
+    asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(sw) : "r"(ra + lane * 4), "n"(scale_off<FMT>()) : "memory");
     if (FMT == 1) asm volatile("ld.shared.u32 %0, [%1+1152];" : "=r"(mw) : "r"(ra + lane * 4) : "memory");
     const float z = 0.f;
     float dA[4], dB[4];
     uint32_t a[8], b[8];
-    unpack_word(w0.x, a[0], a[2], a[4], a[6]);
-    unpack_word(w1.x, a[1], a[3], a[5], a[7]);
-    unpack_word(w0.z, b[0], b[2], b[4], b[6]);
-    unpack_word(w1.z, b[1], b[3], b[5], b[7]);
+    rw.template regs<0>(a);
+    rw.template regs<2>(b);
     mma16816_c(dA, a[0], a[1], a[2], a[3], x.B[0].x, x.B[0].y, z, z, z, z);
     mma16816_c(dB, b[0], b[1], b[2], b[3], x.B[2].x, x.B[2].y, z, z, z, z);
     mma16816(dA, a[4], a[5], a[6], a[7], x.B[0].z, x.B[0].w);
     mma16816(dB, b[4], b[5], b[6], b[7], x.B[2].z, x.B[2].w);
-    unpack_word(w0.y, a[0], a[2], a[4], a[6]);
-    unpack_word(w1.y, a[1], a[3], a[5], a[7]);
-    unpack_word(w0.w, b[0], b[2], b[4], b[6]);
-    unpack_word(w1.w, b[1], b[3], b[5], b[7]);
+    rw.template regs<1>(a);
+    rw.template regs<3>(b);
     mma16816(dA, a[0], a[1], a[2], a[3], x.B[1].x, x.B[1].y);
     mma16816(dB, b[0], b[1], b[2], b[3], x.B[3].x, x.B[3].y);
     mma16816(dA, a[4], a[5], a[6], a[7], x.B[1].z, x.B[1].w);
@@ -969,7 +1025,7 @@ __device__ __forceinline__ void record_c0(uint32_t ra, const ChunkX &x, int lane
     const float T0 = (dA[0] + dB[0]) + (dA[1] + dB[1]);  // block t, row g: hi + lo
     const float T2 = (dA[2] + dB[2]) + (dA[3] + dB[3]);  // row g + 8
     const float2 s2 = scale_pair<FMT>(sw);
-    if (FMT == 0) {
+    if (FMT != 1) {
         a0 = fmaf(s2.x * x.F, T0 - x.G, a0);
         a1 = fmaf(s2.y * x.F, T2 - x.G, a1);
     } else {
@@ -983,7 +1039,8 @@ template <int FMT, class RING>
 __device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, StreamOf<FMT, 0> &ws,
                              RING &ring, int warp, int lane, bool cross) {
     using C = Cls<0>;
-    constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
+    constexpr int REC = rec_bytes(FMT);
+    constexpr int SU = stage_su(FMT, 0);
     const int g = lane >> 2, t = lane & 3;
     const int boff = (g & 1) * 64 + t * 16;
     const int cs = q.cs;
@@ -1021,7 +1078,7 @@ __device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, S
     };
 
     for (int i = 0; i < q.n_my;) {
-        const int n_st = stage_units<C::SU>(upt, cs - cc, q.n_my - i);  // units of this stage
+        const int n_st = stage_units<SU>(upt, cs - cc, q.n_my - i);  // units of this stage
         if (!ring.wait(p.err, lane)) break;  // gave up: stop (the error is recorded)
         const uint32_t st_base = ring.stage(ring.cons);
         i += n_st;
@@ -1032,7 +1089,7 @@ __device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, S
                 ChunkX x;
                 load_chunk<0>(x, m, cc, boff, g, t);
                 record_c0<FMT>(st_a, x, lane, acc[0][0], acc[0][1]);
-                if (two) record_c0<FMT>(st_a + C::SU * REC, x, lane, acc[1][0], acc[1][1]);
+                if (two) record_c0<FMT>(st_a + SU * REC, x, lane, acc[1][0], acc[1][1]);
                 if (++cc == cs) {  // end of this pair's slice: hand the tiles over
                     flush(pl, two);
                     cc = 0;
@@ -1087,7 +1144,8 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
         return;
     }
     using C = Cls<CLS>;
-    constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
+    constexpr int REC = rec_bytes(FMT);
+    constexpr int SU = stage_su(FMT, CLS);
     constexpr int NT = C::NT, NGR = C::NGR, NACC = C::NACC;
     const int g = lane >> 2, t = lane & 3;
     const int nb = CLS == 0 ? 1 : p.nb;
@@ -1154,7 +1212,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
     };
 
     for (int i = 0; i < q.n_my;) {
-        const int n_st = stage_units<C::SU>(upt, cs - cc, q.n_my - i);  // units of this stage
+        const int n_st = stage_units<SU>(upt, cs - cc, q.n_my - i);  // units of this stage
         if (!ring.wait(p.err, lane)) break;  // gave up: stop (the error is recorded)
         const uint32_t st_base = ring.stage(ring.cons);
         i += n_st;
@@ -1181,16 +1239,16 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                 G[j][3] = gv.w;
             }
         }
-        // the records' words: nibbles of rows g and g+8, scales (and mins)
-        uint4 w0[2], w1[2], sw[2], mw[2];
+        // the records' words: weights of rows g and g+8, scales (and mins)
+        RecWords<FMT> rw[2];
+        uint4 sw[2], mw[2];
 #pragma unroll
         for (int rc = 0; rc < 2; ++rc) {
-            w0[rc] = w1[rc] = sw[rc] = mw[rc] = make_uint4(0u, 0u, 0u, 0u);
+            sw[rc] = mw[rc] = make_uint4(0u, 0u, 0u, 0u);
             if (rc == 0 || two) {
-                const uint32_t ra = st_a + rc * C::SU * REC;
-                w0[rc] = lds128_at<0>(ra + lane * 16);
-                w1[rc] = lds128_at<512>(ra + lane * 16);
-                sw[rc] = lds128_at<1024>(ra + g * 16);
+                const uint32_t ra = st_a + rc * SU * REC;
+                rw[rc].load(ra, lane);
+                sw[rc] = lds128_at<scale_off<FMT>()>(ra + g * 16);
                 if (FMT == 1) mw[rc] = lds128_at<1152>(ra + g * 16);
             }
         }
@@ -1202,15 +1260,17 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             uint4 B[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) B[nt] = *reinterpret_cast<const uint4 *>(xa + boff[nt]);
-            if (FMT == 0) {
+            if (FMT != 1) {
                 // the block's offset product: the same tensor-core chain as the
-                // weights' below, with every nibble 8 (exactly what a block of
-                // eights gives, so such a block cancels to zero)
+                // weights' below, with every weight zero (every nibble 8 for
+                // Q4_0, every biased byte 128 for Q8_0): exactly what such a
+                // block gives, so it cancels to zero
+                constexpr uint32_t EL = zero_lo<FMT>();
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     float e[4];
-                    mma16816_c(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt].x, B[nt].y, z, z, z, z);
-                    mma16816(e, kEightLo, kEightLo, kEightHi, kEightHi, B[nt].z, B[nt].w);
+                    mma16816_c(e, EL, EL, kEightHi, kEightHi, B[nt].x, B[nt].y, z, z, z, z);
+                    mma16816(e, EL, EL, kEightHi, kEightHi, B[nt].z, B[nt].w);
                     if (C::HLN) {
                         G[0][blk] = e[0] + e[1];
                     } else {
@@ -1223,8 +1283,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             for (int rc = 0; rc < 2; ++rc) {
                 if (rc == 1 && !two) continue;
                 uint32_t a[8];
-                unpack_word(word_of<blk>(w0[rc]), a[0], a[2], a[4], a[6]);  // row g
-                unpack_word(word_of<blk>(w1[rc]), a[1], a[3], a[5], a[7]);  // row g + 8
+                rw[rc].template regs<blk>(a);  // rows g (even) and g + 8 (odd)
                 const float2 s2 = scale_pair<FMT>(word_of<blk>(sw[rc]));
                 float2 m2 = make_float2(0.f, 0.f);
                 if (FMT == 1) m2 = scale_pair<FMT>(word_of<blk>(mw[rc]));
@@ -1237,7 +1296,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                         mma16816(d, a[4], a[5], a[6], a[7], B[nt].z, B[nt].w);
                         const float T0 = d[0] + d[1], T2 = d[2] + d[3];
                         const float fb = F[0][blk];
-                        if (FMT == 0) {
+                        if (FMT != 1) {
                             acc[rc][0] = fmaf(s2.x * fb, T0 - G[0][blk], acc[rc][0]);
                             acc[rc][1] = fmaf(s2.y * fb, T2 - G[0][blk], acc[rc][1]);
                         } else {
@@ -1253,7 +1312,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                             const float sj = (j < 2 ? s2.x : s2.y) * F[2 * nt + (j & 1)][blk];
                             const float gj = G[2 * nt + (j & 1)][blk];
                             float &ac = acc[rc][4 * nt + j];
-                            if (FMT == 0) {
+                            if (FMT != 1) {
                                 ac = fmaf(sj, d[j] - gj, ac);
                             } else {
                                 const float mj = j < 2 ? m2.x : m2.y;
@@ -1555,7 +1614,7 @@ __device__ __forceinline__ void copy_params(GemvParams *dst, const GemvParams *s
 template <int FMT, int CLS>
 __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_engine_kernel(const __grid_constant__ GemvParams prm) {
     using C = Cls<CLS>;
-    constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
+    constexpr int REC = rec_bytes(FMT);
     constexpr int NW = C::NW;
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ GemvParams ps;
@@ -1568,7 +1627,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_engine_kernel(con
     const int nb = CLS == 0 ? 1 : p.nb;
     const Smem m = carve<CLS>(smem, nb, p.Cs, p.TG, p.SW, S);
     RingOf<FMT, CLS> ring;
-    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * C::SU * REC, smem_u32(m.bars) + warp * C::DU * 8, lane,
+    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * stage_su(FMT, CLS) * REC, smem_u32(m.bars) + warp * C::DU * 8, lane,
               p.wait_cycles, p.extra_tx);
     // this CTA has started; the matching wait ends the activation staging
     if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -1646,7 +1705,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned *counter, int *err, unsign
 template <int FMT, int CLS>
 __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_step_kernel(const __grid_constant__ StepParams sp) {
     using C = Cls<CLS>;
-    constexpr int REC = FMT == 0 ? kRecQ4_0 : kRecAffine;
+    constexpr int REC = rec_bytes(FMT);
     constexpr int NW = C::NW;
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1655,12 +1714,12 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_step_kernel(const
     const int cs_max = (sp.Kmax + kChunkK - 1) / kChunkK;  // as the host sized it
     const Smem m = carve<CLS>(smem, nb, cs_max, sp.TGmax, sp.SWmax, 1);
     RingOf<FMT, CLS> ring;
-    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * C::SU * REC, smem_u32(m.bars) + warp * C::DU * 8, lane,
+    ring.init(smem_u32(m.ring) + warp * C::DU * 2 * stage_su(FMT, CLS) * REC, smem_u32(m.bars) + warp * C::DU * 8, lane,
               sp.jobs[0].wait_cycles, sp.jobs[0].extra_tx);
 
     // every job's parameter block in shared memory (after the engine's
     // regions), copied once: the weight stream and the job loop read them there
-    GemvParams *jobs = reinterpret_cast<GemvParams *>(m.ring + (size_t)NW * C::DU * 2 * C::SU * REC);
+    GemvParams *jobs = reinterpret_cast<GemvParams *>(m.ring + (size_t)NW * C::DU * 2 * stage_su(FMT, CLS) * REC);
     for (int i = tid; i < sp.njobs * kParamWords; i += NW * 32)
         reinterpret_cast<unsigned long long *>(jobs)[i] = reinterpret_cast<const unsigned long long *>(sp.jobs)[i];
     csync<NW>();

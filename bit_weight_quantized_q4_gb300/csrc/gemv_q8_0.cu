@@ -1,0 +1,12 @@
+// gemv_q8_0.cu -- Q8_0 instantiations of the dequant-in-GEMV kernel.
+#include "gemv_launch.cuh"
+
+namespace q4 {
+int launch_gemv_q8_0(const GemvParams &p, const Plan &plan, void *stream) {
+    return launch_gemv_fmt<2>(p, plan, (cudaStream_t)stream);
+}
+int launch_step_q8_0(const StepParams &p, int ctas, size_t smem, void *stream) {
+    return launch_step_fmt<2>(p, ctas, smem, (cudaStream_t)stream);
+}
+int step_occupancy_q8_0(int nb, size_t smem) { return step_occupancy_fmt<2>(nb, smem); }
+}  // namespace q4

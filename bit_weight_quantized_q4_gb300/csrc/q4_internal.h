@@ -4,6 +4,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__CUDACC__)
+#define Q4_HD __host__ __device__
+#else
+#define Q4_HD
+#endif
+
 namespace q4 {
 
 // ---------------------------------------------------------------- layout
@@ -27,6 +33,13 @@ constexpr int kChunkK = 128;
 constexpr int kBlocksPerChunk = 4;
 constexpr int kRecQ4_0 = 1152;
 constexpr int kRecAffine = 1280;
+// Q8_0 records (2176 bytes): the biased bytes u = q + 128 of rows 0..7 in
+// [0, 1024) and of rows 8..15 in [1024, 2048), then the scales as for Q4_0
+// at [2048, 2176).  In each half, blocks 0-1 come first ([0, 512)) and
+// blocks 2-3 after ([512, 1024)); lane L owns 16 bytes of each: the 8 bytes of
+// its row's first block of the pair, then of the second.  Byte i of a lane's
+// 8 holds block element q8_elem(t, i).
+constexpr int kRecQ8_0 = 2176;
 
 // Block element (0..31) stored in nibble i of lane-position t's word.
 // Pairs (i, i+4) are (k, k+1) of one f16x2 fragment register:
@@ -39,7 +52,16 @@ inline int nib_elem(int t, int i) {
     return base[i & 3] + 2 * t + (i >> 2);
 }
 
-inline int rec_bytes(int fmt) { return fmt == 0 ? kRecQ4_0 : kRecAffine; }
+// Block element (0..31) stored in byte i of lane-position t's 8 bytes of a
+// Q8_0 block: pairs (i, i+1) are (k, k+1) of one f16x2 fragment register
+// (bytes 0-1: k = 2t, 2t+1; 2-3: 2t+8, 2t+9; 4-5: 16+2t, 17+2t; 6-7: 24+2t,
+// 25+2t).
+inline int q8_elem(int t, int i) {
+    const int base[4] = {0, 8, 16, 24};
+    return base[i >> 1] + 2 * t + (i & 1);
+}
+
+Q4_HD constexpr int rec_bytes(int fmt) { return fmt == 0 ? kRecQ4_0 : fmt == 1 ? kRecAffine : kRecQ8_0; }
 inline int64_t tiles_of(int64_t n) { return (n + kTileRows - 1) / kTileRows; }
 inline int64_t chunks_of(int64_t k) { return (k + kChunkK - 1) / kChunkK; }
 
@@ -47,11 +69,6 @@ inline int64_t chunks_of(int64_t k) { return (k + kChunkK - 1) / kChunkK; }
 enum Mode { MODE_SINGLE = 0, MODE_CONCAT = 1, MODE_PAIRS = 2 };
 enum Epi { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
 
-#if defined(__CUDACC__)
-#define Q4_HD __host__ __device__
-#else
-#define Q4_HD
-#endif
 
 constexpr int kMaxNb = 16;
 constexpr int kMaxCluster = 8;
@@ -70,6 +87,9 @@ Q4_HD constexpr int cls_of(int nb) { return nb <= 1 ? 0 : nb <= 4 ? 1 : nb <= 8 
 Q4_HD constexpr int cls_warps(int c) { return c == 3 ? 8 : 16; }     // warps per CTA
 Q4_HD constexpr int cls_depth(int c) { return (void)c, 2; }  // ring stages per warp
 Q4_HD constexpr int cls_stage(int c) { return c == 2 ? 1 : 2; }  // pair units per stage (2x as many single-tile units)
+// pair units per ring stage for a format: Q8_0 records are nearly twice as
+// large, so its stages hold one
+Q4_HD constexpr int stage_su(int fmt, int c) { return fmt == 2 ? 1 : cls_stage(c); }
 Q4_HD constexpr int cls_gsw(int c) { return c <= 1 ? 4 : c == 2 ? 8 : 16; }  // group-sum rows per chunk
 // bytes of one activation row per 32-column block in shared memory: f16 hi
 // and lo parts for nb <= 4, the f16 value alone for larger batches
@@ -175,7 +195,7 @@ inline size_t engine_smem(int fmt, int nb, int TG, int Cs, int SW, int S) {
     const size_t red = S > 1 ? (size_t)64 * (TG + 2 * S) * nb : 0;  // S slices of at most TG / S + 2 tiles
     const size_t slots = (size_t)64 * NW * SW * nb;
     const size_t misc = (size_t)16 * NW * kMaxNb + 32 * kMaxNb + 8 * NW * cls_depth(c);  // + ring barriers
-    const size_t ring = NW * cls_depth(c) * 2 * cls_stage(c) * rec_bytes(fmt);
+    const size_t ring = NW * cls_depth(c) * 2 * stage_su(fmt, c) * rec_bytes(fmt);
     return xs + gs + red + slots + misc + ring;
 }
 
@@ -278,11 +298,14 @@ inline size_t step_smem_bytes(int fmt, int nb, int TGmax, int Kmax, int SWmax, i
 // Launchers, one per kernel instantiation family (defined in the .cu files).
 int launch_gemv_q4_0(const GemvParams &p, const Plan &plan, void *stream);
 int launch_gemv_affine(const GemvParams &p, const Plan &plan, void *stream);
+int launch_gemv_q8_0(const GemvParams &p, const Plan &plan, void *stream);
 // Cooperative launch of the decode-step kernel: one CTA per SM.
 int launch_step_q4_0(const StepParams &p, int ctas, size_t smem, void *stream);
 int launch_step_affine(const StepParams &p, int ctas, size_t smem, void *stream);
+int launch_step_q8_0(const StepParams &p, int ctas, size_t smem, void *stream);
 // Decode-step CTAs that can be resident on one SM (0 on error).
 int step_occupancy_q4_0(int nb, size_t smem);
 int step_occupancy_affine(int nb, size_t smem);
+int step_occupancy_q8_0(int nb, size_t smem);
 
 }  // namespace q4

@@ -24,6 +24,14 @@ bool shape_ok(int32_t n, int32_t k) {
     return n >= 1 && k >= 32 && k % 32 == 0 && k <= 65536 && n <= (1 << 24);
 }
 
+// Byte offset in a Q8_0 record of element e (0..31) of block j (0..3) of row
+// rr (0..15): the lane-position t and byte i with q8_elem(t, i) == e.
+inline int q8_off(int rr, int j, int e) {
+    const int h = rr >> 3, g = rr & 7;
+    const int t = (e & 7) >> 1, i = 2 * (e >> 3) + (e & 1);  // inverse of q8_elem
+    return h * 1024 + (j >> 1) * 512 + (4 * g + t) * 16 + (j & 1) * 8 + i;
+}
+
 // Nibble q of element e (0..31) of block `blk` of a Q4_0 row (GGUF order).
 inline int q4_0_nib(const uint8_t *blk, int e) {
     const uint8_t *qs = blk + 2;
@@ -38,14 +46,16 @@ inline int affine_nib(const uint8_t *row, int64_t e) {
 
 }  // namespace
 
+inline bool fmt_ok(int32_t fmt) { return fmt == Q4_FMT_Q4_0 || fmt == Q4_FMT_AFFINE || fmt == Q4_FMT_Q8_0; }
+
 extern "C" size_t q4_packed_bytes(int32_t fmt, int32_t n, int32_t k) {
-    if ((fmt != Q4_FMT_Q4_0 && fmt != Q4_FMT_AFFINE) || !shape_ok(n, k)) return 0;
+    if (!fmt_ok(fmt) || !shape_ok(n, k)) return 0;
     return (size_t)q4::tiles_of(n) * (size_t)q4::chunks_of(k) * (size_t)q4::rec_bytes(fmt);
 }
 
 extern "C" size_t q4_weight_bytes(int32_t fmt, int32_t n, int32_t k) {
-    if ((fmt != Q4_FMT_Q4_0 && fmt != Q4_FMT_AFFINE) || !shape_ok(n, k)) return 0;
-    return (size_t)n * (size_t)(k / 32) * (fmt == Q4_FMT_Q4_0 ? 18u : 20u);
+    if (!fmt_ok(fmt) || !shape_ok(n, k)) return 0;
+    return (size_t)n * (size_t)(k / 32) * (fmt == Q4_FMT_Q4_0 ? 18u : fmt == Q4_FMT_AFFINE ? 20u : 34u);
 }
 
 // Generic packer: `get_q(row, blk, e)` gives the nibble of element e of a
@@ -115,6 +125,65 @@ extern "C" q4_status q4_repack_affine(const uint8_t *nib, const uint16_t *s, con
          [&](int64_t row, int64_t blk, int e) { return affine_nib(nib + row * (k / 2), blk * 32 + e); },
          [&](int64_t row, int64_t blk) { return (uint32_t)s[row * B + blk]; },
          [&](int64_t row, int64_t blk) { return (uint32_t)m[row * B + blk]; });
+    return Q4_OK;
+}
+
+extern "C" q4_status q4_repack_q8_0(const void *host_blocks, int32_t n, int32_t k, void *host_out,
+                                    size_t out_bytes) {
+    if (!host_blocks || !host_out) return Q4_ERR_NULL;
+    if (!shape_ok(n, k)) return Q4_ERR_SHAPE;
+    if (out_bytes < q4_packed_bytes(Q4_FMT_Q8_0, n, k)) return Q4_ERR_SHAPE;
+    const uint8_t *src = (const uint8_t *)host_blocks;
+    uint8_t *out = (uint8_t *)host_out;
+    const int64_t T = q4::tiles_of(n), C = q4::chunks_of(k), B = k / 32;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < C; ++c) {
+            uint8_t *r = out + (t * C + c) * q4::kRecQ8_0;
+            for (int rr = 0; rr < 16; ++rr)
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t row = t * 16 + rr, blk = c * 4 + j;
+                    const bool real = row < n && blk < B;
+                    const uint8_t *b = real ? src + (row * B + blk) * 34 : nullptr;
+                    // biased bytes u = q + 128; padding is q = 0 with d = 0
+                    for (int e = 0; e < 32; ++e) r[q8_off(rr, j, e)] = (uint8_t)(real ? b[2 + e] ^ 0x80u : 0x80u);
+                }
+            for (int g = 0; g < 8; ++g)
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t blk = c * 4 + j, r0 = t * 16 + g, r1 = r0 + 8;
+                    auto scale = [&](int64_t row) -> uint32_t {
+                        if (row >= n || blk >= B) return 0;
+                        const uint8_t *b = src + (row * B + blk) * 34;
+                        return (uint32_t)b[0] | ((uint32_t)b[1] << 8);
+                    };
+                    store_u32(r + 2048 + g * 16 + j * 4, scale(r0) | (scale(r1) << 16));
+                }
+        }
+    return Q4_OK;
+}
+
+extern "C" q4_status q4_unpack_q8_0(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,
+                                    void *host_blocks) {
+    if (!host_packed || !host_blocks) return Q4_ERR_NULL;
+    if (!shape_ok(n, k)) return Q4_ERR_SHAPE;
+    if (packed_bytes < q4_packed_bytes(Q4_FMT_Q8_0, n, k)) return Q4_ERR_SHAPE;
+    const uint8_t *in = (const uint8_t *)host_packed;
+    uint8_t *dst = (uint8_t *)host_blocks;
+    const int64_t T = q4::tiles_of(n), C = q4::chunks_of(k), B = k / 32;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < C; ++c) {
+            const uint8_t *r = in + (t * C + c) * q4::kRecQ8_0;
+            for (int rr = 0; rr < 16; ++rr)
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t row = t * 16 + rr, blk = c * 4 + j;
+                    if (row >= n || blk >= B) continue;
+                    uint8_t *b = dst + (row * B + blk) * 34;
+                    const uint32_t sw = load_u32(r + 2048 + (rr & 7) * 16 + j * 4);
+                    const uint16_t sv = (uint16_t)((rr >> 3) ? (sw >> 16) : (sw & 0xFFFF));
+                    b[0] = (uint8_t)(sv & 0xFF);
+                    b[1] = (uint8_t)(sv >> 8);
+                    for (int e = 0; e < 32; ++e) b[2 + e] = (uint8_t)(r[q8_off(rr, j, e)] ^ 0x80u);
+                }
+        }
     return Q4_OK;
 }
 

@@ -63,7 +63,8 @@ typedef enum {
 
 typedef enum {
     Q4_FMT_Q4_0 = 0,    /* 32 weights: fp16 scale d + 16 nibble bytes; w = d*(q-8) */
-    Q4_FMT_AFFINE = 1   /* 32 weights: bf16 scale s, bf16 min m, 16 nibble bytes; w = s*q + m */
+    Q4_FMT_AFFINE = 1,  /* 32 weights: bf16 scale s, bf16 min m, 16 nibble bytes; w = s*q + m */
+    Q4_FMT_Q8_0 = 2     /* 32 weights: fp16 scale d + 32 signed bytes; w = d*q */
 } q4_format;
 
 /* A non-owning view of one repacked weight matrix in device memory.
@@ -104,6 +105,15 @@ q4_status q4_repack_affine(const uint8_t *nib, const uint16_t *s, const uint16_t
 /* Inverse of q4_repack_q4_0 (host -> host); used to check the round trip. */
 q4_status q4_unpack_q4_0(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,
                          void *host_blocks);
+
+/* Q8_0 host blocks (crate inferencelayer, Functions: q4_0_to_q8_0n,
+ * gemv_q8_0n_k_lcpp_src): [n][k/32] blocks of 34 bytes, the fp16 scale d
+ * (little endian) then 32 signed bytes q; w = d*q.  Lossless, host -> host,
+ * like q4_repack_q4_0; host_out holds q4_packed_bytes(Q4_FMT_Q8_0, n, k). */
+q4_status q4_repack_q8_0(const void *host_blocks, int32_t n, int32_t k, void *host_out, size_t out_bytes);
+
+/* Inverse of q4_repack_q8_0 (host -> host). */
+q4_status q4_unpack_q8_0(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k, void *host_blocks);
 
 /* Inverse of q4_repack_affine (host -> host). */
 q4_status q4_unpack_affine(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,

@@ -19,6 +19,8 @@ def case_seed(*key):
 
 
 def host_weight(H):
+    if hasattr(H, "blocks8"):
+        return oracle.HostWeight.q8_0(H.blocks8, H.n, H.k)
     if hasattr(H, "blocks"):
         return oracle.HostWeight.q4_0(H.blocks, H.n, H.k)
     return oracle.HostWeight.affine(H.nib, H.s, H.m, H.n, H.k)
@@ -26,6 +28,8 @@ def host_weight(H):
 
 def dev_weight(H, device="cuda"):
     import bit_weight_quantized_q4_gb300 as q4
+    if hasattr(H, "blocks8"):
+        return q4.Q4Weight.from_q8_0(H.blocks8, H.n, H.k, device)
     if hasattr(H, "blocks"):
         return q4.Q4Weight.from_q4_0(H.blocks, H.n, H.k, device)
     return q4.Q4Weight.from_affine(H.nib, H.s, H.m, H.n, H.k, device)

@@ -41,6 +41,21 @@ def test_repack_roundtrip_random(n, k):
     P = q4.repack_affine(A.nib, A.s, A.m, n, k)
     nib, s, m = q4.unpack_affine(P, n, k)
     assert np.array_equal(nib, A.nib) and np.array_equal(s, A.s) and np.array_equal(m, A.m)
+    Q = wl.draw_q8_0(rng, n, k)
+    P = q4.repack_q8_0(Q.blocks8, n, k)
+    assert P.size == q4.packed_bytes(2, n, k)
+    assert np.array_equal(q4.unpack_q8_0(P, n, k), Q.blocks8)
+
+
+def test_q8_0_layout_bytes():
+    # the device record of a 16 x 128 Q8_0 tile holds exactly the 2048 biased
+    # weight bytes (q + 128) and the 64 fp16 scales: nothing else, no padding
+    rng = np.random.default_rng(11)
+    Q = wl.draw_q8_0(rng, 16, 128)
+    P = q4.repack_q8_0(Q.blocks8, 16, 128)
+    assert P.size == 2176 == q4.weight_bytes(2, 16, 128)
+    assert np.array_equal(np.sort(P[:2048]), np.sort((Q.blocks8[:, :, 2:] ^ 0x80).ravel()))
+    assert np.array_equal(np.sort(P[2048:].view(np.uint16)), np.sort(Q.blocks8[:, :, :2].copy().view(np.uint16).ravel()))
 
 
 def test_repack_roundtrip_edge_values():
@@ -62,10 +77,12 @@ def test_packed_sizes_and_padding():
     assert q4.weight_bytes(0, 1, 32) == 18 and q4.weight_bytes(1, 1, 32) == 20
     assert q4.packed_bytes(0, 1, 32) == 1152       # one padded tile chunk
     assert q4.packed_bytes(0, 0, 32) == 0 and q4.packed_bytes(0, 4, 33) == 0
-    assert q4.packed_bytes(2, 4, 32) == 0
+    assert q4.packed_bytes(2, 14336, 4096) == q4.weight_bytes(2, 14336, 4096) == 14336 * 128 * 34
+    assert q4.weight_bytes(2, 1, 32) == 34 and q4.packed_bytes(2, 1, 32) == 2176
+    assert q4.packed_bytes(3, 4, 32) == 0
 
 
-@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
 @pytest.mark.parametrize("tiles,chunks,pairs", [(896, 32, False), (1024, 16, True), (128, 16, False),
                                                 (64, 16, False), (4096, 16, False), (1, 1, False),
                                                 (2, 1, True), (7, 3, False), (128, 64, False)])

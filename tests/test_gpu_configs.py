@@ -223,6 +223,9 @@ STEP_CASES = [
     ("affine", 8, 2, 256, 64, 384, 1000),
     ("q4_0", 16, 2, 256, 64, 384, 1000),
     ("affine", 16, 2, 160, 48, 224, 333),
+    ("q8_0", 1, 2, 256, 64, 384, 1000),
+    ("q8_0", 4, 2, 160, 48, 224, 333),
+    ("q8_0", 9, 2, 128, 32, 192, 300),
     ("q4_0", 1, 32, 128, 32, 192, 300),
     ("affine", 2, 32, 128, 32, 192, 300),
 ]

@@ -25,7 +25,7 @@ def q4():
 
 
 def _draw(fmt, rng, n, k):
-    return wl.draw_q4_0(rng, n, k) if fmt == "q4_0" else wl.draw_affine(rng, n, k)
+    return wl._draw_fmt(fmt)(rng, n, k)
 
 
 @pytest.mark.parametrize("nb,k", [(1, 32), (3, 544), (16, 4096)])
@@ -41,7 +41,7 @@ def test_pack_rounds_and_sums(q4, nb, k):
     assert torch.equal(gs, ref)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("nb", [1, 3, 5, 9, 16])
 @pytest.mark.parametrize("n,k", [(33, 160), (700, 1024), (64, 8192)])
 def test_gemv_half_parity(q4, fmt, nb, n, k):

@@ -23,13 +23,13 @@ def q4():
 
 
 def _draw(fmt, rng, n, k):
-    return wl.draw_q4_0(rng, n, k) if fmt == "q4_0" else wl.draw_affine(rng, n, k)
+    return wl._draw_fmt(fmt)(rng, n, k)
 
 
 SHAPES = [(1, 32), (7, 96), (33, 160), (100, 544), (512, 2048), (1000, 4096), (48, 8192)]
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("nb", [1, 2, 3, 4, 5, 8, 9, 16])
 @pytest.mark.parametrize("n,k", SHAPES)
 def test_gemv(q4, fmt, nb, n, k):
@@ -58,7 +58,7 @@ def test_affine_with_given_group_sums(q4, nb):
     check(to_np(y1), y_ref, S, what="affine given gsum")
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("nb", [1, 3, 16])
 @pytest.mark.parametrize("n,k", [(64, 64), (2048, 2048), (37, 4096), (130, 8192)])
 def test_nrm_gemv(q4, fmt, nb, n, k):
@@ -71,7 +71,7 @@ def test_nrm_gemv(q4, fmt, nb, n, k):
     check(to_np(y), y_ref, S, what="nrm %s nb=%d %dx%d" % (fmt, nb, n, k))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("norm", [True, False])
 @pytest.mark.parametrize("na,nbr,k,nb", [(512, 512, 2048, 1), (40, 17, 96, 2), (2048, 512, 2048, 4)])
 def test_dual(q4, fmt, norm, na, nbr, k, nb):
@@ -86,7 +86,7 @@ def test_dual(q4, fmt, norm, na, nbr, k, nb):
     check(to_np(yb), rb, Sb, what="dual b")
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("n,k,nb", [(8192, 2048, 1), (40, 96, 3), (1000, 1024, 8), (256, 512, 16)])
 def test_gus_nrm(q4, fmt, n, k, nb):
     rng = np.random.default_rng(case_seed("gus", fmt, n, k, nb))
@@ -99,7 +99,7 @@ def test_gus_nrm(q4, fmt, n, k, nb):
     check_swiglu(to_np(h), g, Sg, u, Su, what="gus %s %dx%d nb=%d" % (fmt, n, k, nb))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("n,k,nb", [(2048, 8192, 1), (2048, 2048, 1), (33, 160, 5), (700, 1024, 16)])
 @pytest.mark.parametrize("inplace", [False, True])
 def test_res_gemv(q4, fmt, n, k, nb, inplace):
@@ -116,7 +116,7 @@ def test_res_gemv(q4, fmt, n, k, nb, inplace):
     check_residual(to_np(y), y_ref, S, what="res %s" % fmt)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("n,k,nb,norm", [(65536, 2048, 1, True), (1000, 256, 3, False), (77, 96, 16, True)])
 def test_argmax(q4, fmt, n, k, nb, norm):
     rng = np.random.default_rng(case_seed("am", fmt, n, k, nb))
@@ -148,13 +148,16 @@ def test_argmax_planted_and_ties(q4):
     assert val.cpu().tolist() == [7.0 * 64, 0.0]
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 def test_zero_weights_exact(q4, fmt):
     rng = np.random.default_rng(41)
     n, k = 200, 1024
     if fmt == "q4_0":
         d = rng.uniform(0.005, 0.02, (n, k // 32)).astype(np.float16).view(np.uint16)
         H = wl.Q4_0Host(n, k, wl.pack_q4_0(np.full((n, k), 8, np.uint8), d))
+    elif fmt == "q8_0":
+        d = rng.uniform(0.0003, 0.0012, (n, k // 32)).astype(np.float16).view(np.uint16)
+        H = wl.Q8_0Host(n, k, wl.pack_q8_0(np.zeros((n, k), np.int16), d))
     else:
         z = np.zeros((n, k // 32), np.uint16)
         H = wl.AffineHost(n, k, rng.integers(0, 256, (n, k // 2), dtype=np.uint8), z, z)
@@ -180,12 +183,21 @@ def test_power_of_two_scaling_bitwise(q4):
     assert torch.equal(y2, 2.0 * y1)
     y4 = q4.q4_gemv(dev_weight(H), 4.0 * x)
     assert torch.equal(y4, 4.0 * y1)
+    # Q8_0: d -> 2d doubles every output exactly too
+    H8 = wl.draw_q8_0(rng, n, k)
+    b8 = H8.blocks8.copy()
+    dd = (b8[:, :, 0].astype(np.uint16) | (b8[:, :, 1].astype(np.uint16) << 8)) + 0x0400
+    b8[:, :, 0] = (dd & 0xFF).astype(np.uint8)
+    b8[:, :, 1] = (dd >> 8).astype(np.uint8)
+    z1 = q4.q4_gemv(dev_weight(H8), x)
+    assert torch.equal(q4.q4_gemv(dev_weight(wl.Q8_0Host(n, k, b8)), x), 2.0 * z1)
 
 
-def test_one_hot_columns(q4):
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+def test_one_hot_columns(q4, fmt):
     rng = np.random.default_rng(43)
     n, k = 96, 256
-    H = wl.draw_q4_0(rng, n, k)
+    H = _draw(fmt, rng, n, k)
     cols = [0, 5, 16, 31, 32, 130, 255]
     x = np.zeros((len(cols), k), np.float32)
     for r, c in enumerate(cols):
@@ -226,7 +238,7 @@ def test_nrm_constant_vector(q4):
 
 
 @pytest.mark.parametrize("nb", [3, 5, 9])
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 def test_large_dynamic_range(q4, fmt, nb):
     # activations far outside f16 range in both directions, and 32-column
     # blocks of very different magnitude inside one row, stay within

@@ -42,10 +42,10 @@ def _shape(q4, fmt, nb, S, pairs=False):
 
 
 def _draw(fmt, rng, n, k):
-    return wl.draw_q4_0(rng, n, k) if fmt == "q4_0" else wl.draw_affine(rng, n, k)
+    return wl._draw_fmt(fmt)(rng, n, k)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("nb", [1, 4, 16])
 @pytest.mark.parametrize("S", [2, 4, 8])
 def test_split_store_and_norm(q4, fmt, nb, S):
@@ -66,7 +66,7 @@ def test_split_store_and_norm(q4, fmt, nb, S):
     check(to_np(y), y_ref, Sr, what="split nrm %s nb=%d S=%d %dx%d" % (fmt, nb, S, n, k))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("nb", [1, 16])
 @pytest.mark.parametrize("S", [2, 8])
 def test_split_residual(q4, fmt, nb, S):
@@ -80,7 +80,7 @@ def test_split_residual(q4, fmt, nb, S):
     check_residual(to_np(y), y_ref, Sr, what="split res %s nb=%d S=%d" % (fmt, nb, S))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("nb", [1, 8])
 @pytest.mark.parametrize("S", [2, 4, 8])
 def test_split_swiglu(q4, fmt, nb, S):
@@ -95,7 +95,7 @@ def test_split_swiglu(q4, fmt, nb, S):
     check_swiglu(to_np(h), g, Sg, u, Su, what="split gus %s nb=%d S=%d %dx%d" % (fmt, nb, S, n, k))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
 @pytest.mark.parametrize("nb", [1, 3])
 @pytest.mark.parametrize("S", [2, 8])
 def test_split_argmax(q4, fmt, nb, S):
