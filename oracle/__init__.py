@@ -14,6 +14,11 @@ bytes before any device repack) and computes in IEEE double precision:
 * ``q8_0``: blocks ``uint8[n, k/32, 34]`` -- fp16 scale ``d`` then 32
   signed bytes; ``w = d*q`` (crate inferencelayer, Functions: q4_0_to_q8_0n,
   gemv_q8_0n_k_lcpp_src).
+* ``q4_k``: superblocks ``uint8[n, k/256, 144]`` -- fp16 ``d``, fp16
+  ``dmin``, 12 bytes of 6-bit sub-scales and sub-mins (GGUF pack), 128 nibble
+  bytes (runs of 32 holding sub-blocks 2r / 2r+1 in the low / high nibbles);
+  ``w = d*sc*q - dmin*mn`` (crate inferencelayer, Functions:
+  gemv_q5k_k_lcpp_src; honeycrisp/mod.rs, quant_matmul's Q4_K branch).
 * ``affine``: nibbles ``uint8[n, k/2]`` (element ``2i`` low nibble of byte
   ``i``, ``2i+1`` high nibble), ``s`` and ``m`` as bf16 bits
   ``uint16[n, k/32]``; ``w = s*q + m`` (Module gpu, Structs Q and HalfSet).
@@ -44,6 +49,7 @@ _LIB = os.path.join(_HERE, "libq4oracle.so")
 FMT_Q4_0 = 0
 FMT_AFFINE = 1
 FMT_Q8_0 = 2
+FMT_Q4_K = 3
 
 
 def build(force: bool = False) -> str:
@@ -87,6 +93,8 @@ def lib() -> ctypes.CDLL:
         L.q4o_bf16.argtypes = [ctypes.c_uint16]
         L.q4o_q4_0_row.argtypes = [P, I64, I64, P]
         L.q4o_q8_0_row.argtypes = [P, I64, I64, P]
+        L.q4o_q4_k_row.argtypes = [P, I64, I64, P]
+        L.q4o_q4_k_scale_min.argtypes = [P, ctypes.c_int, P, P]
         L.q4o_affine_row.argtypes = [P, P, P, I64, I64, P]
         L.q4o_gemv.argtypes = [ctypes.c_int, P, P, P, I64, I64, P, I64, P, P, P]
         L.q4o_gemv_rows.argtypes = [ctypes.c_int, P, P, P, I64, I64, P, I64, P, P, P, I64, I64]
@@ -116,7 +124,7 @@ class HostWeight:
     fmt: int
     n: int
     k: int
-    a: np.ndarray                   # q4_0: blocks; affine: nibbles
+    a: np.ndarray                   # q4_0 / q8_0 / q4_k: blocks; affine: nibbles
     s: np.ndarray | None = None     # affine: bf16 scale bits
     m: np.ndarray | None = None     # affine: bf16 min bits
 
@@ -127,6 +135,8 @@ class HostWeight:
             assert self.a.size == self.n * (self.k // 32) * 18
         elif self.fmt == FMT_Q8_0:
             assert self.a.size == self.n * (self.k // 32) * 34
+        elif self.fmt == FMT_Q4_K:
+            assert self.k % 256 == 0 and self.a.size == self.n * (self.k // 256) * 144
         else:
             assert self.a.size == self.n * self.k // 2
             self.s = np.ascontiguousarray(self.s, dtype=np.uint16)
@@ -140,6 +150,10 @@ class HostWeight:
     @staticmethod
     def q8_0(blocks: np.ndarray, n: int, k: int) -> "HostWeight":
         return HostWeight(FMT_Q8_0, n, k, blocks)
+
+    @staticmethod
+    def q4_k(blocks: np.ndarray, n: int, k: int) -> "HostWeight":
+        return HostWeight(FMT_Q4_K, n, k, blocks)
 
     @staticmethod
     def affine(nib: np.ndarray, s: np.ndarray, m: np.ndarray, n: int, k: int) -> "HostWeight":
@@ -165,9 +179,21 @@ def dequant_row(W: HostWeight, row: int) -> np.ndarray:
         lib().q4o_q4_0_row(_p(W.a), W.k, row, _p(out))
     elif W.fmt == FMT_Q8_0:
         lib().q4o_q8_0_row(_p(W.a), W.k, row, _p(out))
+    elif W.fmt == FMT_Q4_K:
+        lib().q4o_q4_k_row(_p(W.a), W.k, row, _p(out))
     else:
         lib().q4o_affine_row(_p(W.a), _p(W.s), _p(W.m), W.k, row, _p(out))
     return out
+
+
+def q4_k_scale_min(scale_bytes, j: int) -> tuple[int, int]:
+    """Sub-block ``j``'s 6-bit (scale, min) from a Q4_K superblock's 12 scale
+    bytes."""
+    sb = np.ascontiguousarray(np.asarray(scale_bytes, dtype=np.uint8))
+    assert sb.size == 12 and 0 <= j < 8
+    sc, mn = ctypes.c_int(), ctypes.c_int()
+    lib().q4o_q4_k_scale_min(_p(sb), j, ctypes.byref(sc), ctypes.byref(mn))
+    return sc.value, mn.value
 
 
 def dequant(W: HostWeight) -> np.ndarray:
@@ -339,6 +365,8 @@ def _hw(H) -> HostWeight:
     """The oracle's view of a generator's host weight (any format)."""
     if hasattr(H, "blocks8"):
         return HostWeight.q8_0(H.blocks8, H.n, H.k)
+    if hasattr(H, "blocks_k"):
+        return HostWeight.q4_k(H.blocks_k, H.n, H.k)
     if hasattr(H, "blocks"):
         return HostWeight.q4_0(H.blocks, H.n, H.k)
     return HostWeight.affine(H.nib, H.s, H.m, H.n, H.k)

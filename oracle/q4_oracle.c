@@ -1,6 +1,7 @@
 /*
  * q4_oracle.c -- plain, slow, obviously correct CPU oracle for the weight-only
- * 4-bit dequant-in-GEMV family (Q4_0 blocks and affine-Q4 groups) and its fused
+ * dequant-in-GEMV family (Q4_0 blocks, affine-Q4 groups, Q8_0 blocks and Q4_K
+ * superblocks) and its fused
  * neighbours (RMSNorm, SwiGLU, residual add, greedy argmax).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
@@ -24,6 +25,20 @@
  *    weight = d * q): crate inferencelayer, Functions, entries q4_0_to_q8_0n
  *    (the lossless upcast of a Q4_0 block keeps d and maps q to nib - 8) and
  *    gemv_q8_0n_k_lcpp_src (Q8_0 blocks read as-is).
+ *  - Q4_K superblock (256 weights in 144 bytes: fp16 d, fp16 dmin, 12 bytes
+ *    of 6-bit sub-scales sc and sub-mins mn for eight 32-weight sub-blocks,
+ *    128 nibble bytes; weight = d * sc * q - dmin * mn): crate inferencelayer,
+ *    Functions, entries gemv_q5k_k_lcpp_src (the superblock's fields in this
+ *    order, "the SAME 6-bit pack as Q4_K", and w = d*sc*nib - dmin*mn with the
+ *    fifth bit plane, which Q4_K does not have) and honeycrisp/mod.rs
+ *    (quant_matmul's Q4_K branch: k a multiple of 256).  The pages do not
+ *    print the 6-bit pack or the nibble order; the reading taken is the GGUF
+ *    one the pages load as-is.  Sub-blocks 0-3 keep sc and mn in the low six
+ *    bits of scale bytes 0-3 and 4-7; sub-blocks 4-7 keep their low four bits
+ *    in the two nibbles of bytes 8-11 (sc low, mn high) and their top two bits
+ *    in the top two bits of bytes 0-3 (sc) and 4-7 (mn).  The 128 nibble bytes
+ *    are four runs of 32: run r holds sub-block 2r in its low nibbles and
+ *    sub-block 2r+1 in its high nibbles, in element order.
  *  - Affine-Q4 group (32 weights, bf16 scale s and bf16 min m, weight =
  *    s*q + m): Module gpu (qwen4_exp), Structs Q (affine-Q4 projection with
  *    byte offsets into a bf16 weight buffer) and HalfSet (even/odd streams plus
@@ -109,6 +124,42 @@ void q4o_q8_0_row(const uint8_t *blocks, int64_t k, int64_t row, double *w)
     }
 }
 
+/* Sub-block j's 6-bit scale and min of a Q4_K superblock's 12 scale bytes. */
+void q4o_q4_k_scale_min(const uint8_t *sb, int j, int *sc, int *mn)
+{
+    if (j < 4) {
+        *sc = sb[j] & 63;
+        *mn = sb[j + 4] & 63;
+    } else {
+        *sc = (sb[j + 4] & 0x0f) | ((sb[j - 4] >> 6) << 4);
+        *mn = (sb[j + 4] >> 4) | ((sb[j] >> 6) << 4);
+    }
+}
+
+/* One row of Q4_K weights, dequantised to f64: superblocks of 144 bytes,
+ * fp16 d and dmin (little endian), 12 scale bytes, 128 nibble bytes;
+ * weight = d * sc * q - dmin * mn.  blocks: [n][k/256][144] bytes; w: [k]. */
+void q4o_q4_k_row(const uint8_t *blocks, int64_t k, int64_t row, double *w)
+{
+    int64_t nsb = k / 256;
+    const uint8_t *r = blocks + row * nsb * 144;
+    for (int64_t b = 0; b < nsb; ++b) {
+        const uint8_t *blk = r + b * 144;
+        double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));
+        double dmin = q4o_half((uint16_t)(blk[2] | (blk[3] << 8)));
+        const uint8_t *sb = blk + 4, *qs = blk + 16;
+        for (int e = 0; e < 256; ++e) {
+            int j = e / 32;                       /* sub-block */
+            int l = e % 32;                       /* element within it */
+            int byte = qs[32 * (j / 2) + l];
+            int q = (j & 1) ? (byte >> 4) : (byte & 0x0f);
+            int sc, mn;
+            q4o_q4_k_scale_min(sb, j, &sc, &mn);
+            w[b * 256 + e] = d * (double)sc * (double)q - dmin * (double)mn;
+        }
+    }
+}
+
 /* One row of affine-Q4 weights, dequantised to f64.
  * nib: [n][k/2] bytes; s, m: [n][k/32] bf16 bits; w: [k]. */
 void q4o_affine_row(const uint8_t *nib, const uint16_t *s, const uint16_t *m,
@@ -131,6 +182,7 @@ void q4o_affine_row(const uint8_t *nib, const uint16_t *s, const uint16_t *m,
  * for the output rows i in [row0, row1) (rows are independent; callers may
  * run disjoint ranges at the same time, each with its own scratch).
  * fmt 0: a = Q4_0 blocks.  fmt 1: a = nibbles, b = s, c = m.  fmt 2: a = Q8_0 blocks.
+ * fmt 3: a = Q4_K superblocks.
  * x: [nb][k] f64; y, bound: [nb][n]; wrow: scratch of k doubles. */
 void q4o_gemv_rows(int fmt, const void *a, const void *b, const void *c,
                    int64_t n, int64_t k, const double *x, int64_t nb,
@@ -141,6 +193,8 @@ void q4o_gemv_rows(int fmt, const void *a, const void *b, const void *c,
             q4o_q4_0_row((const uint8_t *)a, k, i, wrow);
         else if (fmt == 2)
             q4o_q8_0_row((const uint8_t *)a, k, i, wrow);
+        else if (fmt == 3)
+            q4o_q4_k_row((const uint8_t *)a, k, i, wrow);
         else
             q4o_affine_row((const uint8_t *)a, (const uint16_t *)b,
                            (const uint16_t *)c, k, i, wrow);

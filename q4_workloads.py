@@ -13,6 +13,10 @@ Host storage formats (the readings of the pages, stated once):
   nibble and element ``i + 16`` in its high nibble (GGUF order).
 * Q8_0: ``uint8[n, k/32, 34]``; bytes 0-1 = fp16 scale ``d``; bytes 2..33 =
   the 32 weights as signed bytes (two's complement).
+* Q4_K: ``uint8[n, k/256, 144]``; bytes 0-1 = fp16 ``d``, 2-3 = fp16 ``dmin``,
+  4..15 = the eight sub-blocks' 6-bit scales and mins (GGUF pack, see
+  ``Q4K_SCALE_BITS``), 16..143 = four runs of 32 nibble bytes, run ``r``
+  holding sub-block ``2r`` in its low nibbles and ``2r + 1`` in its high ones.
 * affine-Q4: nibbles ``uint8[n, k/2]`` with byte ``i`` holding element ``2i``
   (low nibble) and ``2i + 1`` (high nibble); ``s`` and ``m`` as bf16 bit
   patterns ``uint16[n, k/32]``.
@@ -67,6 +71,55 @@ def pack_q8_0(q: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
     return out
 
 
+def _q4k_scale_bits():
+    """Where each bit of the Q4_K 6-bit fields lives in the 12 scale bytes:
+    ``table[f, j, b] = (byte, bit)`` for field f (0 scale, 1 min) of sub-block
+    j, bit b.  Sub-blocks 0-3: six bits in bytes j (scale) and j + 4 (min).
+    Sub-blocks 4-7: the low four bits in byte j + 4 (scale in the low nibble,
+    min in the high one), the top two in bits 6-7 of byte j - 4 (scale) and of
+    byte j (min)."""
+    t = np.zeros((2, 8, 6, 2), dtype=np.int64)
+    for j in range(8):
+        for b in range(6):
+            if j < 4:
+                t[0, j, b] = (j, b)
+                t[1, j, b] = (j + 4, b)
+            elif b < 4:
+                t[0, j, b] = (j + 4, b)
+                t[1, j, b] = (j + 4, b + 4)
+            else:
+                t[0, j, b] = (j - 4, b + 2)
+                t[1, j, b] = (j, b + 2)
+    return t
+
+
+Q4K_SCALE_BITS = _q4k_scale_bits()
+
+
+def pack_q4_k(q: np.ndarray, sc: np.ndarray, mn: np.ndarray, d_bits: np.ndarray,
+              dmin_bits: np.ndarray) -> np.ndarray:
+    """Pack nibbles ``q[n, k]`` (0..15), 6-bit sub-block scales and mins
+    ``sc, mn[n, k/32]`` (0..63) and fp16 bits ``d_bits, dmin_bits[n, k/256]``
+    into Q4_K host superblocks ``uint8[n, k/256, 144]``."""
+    n, k = q.shape
+    assert k % 256 == 0
+    ns = k // 256
+    out = np.zeros((n, ns, 144), dtype=np.uint8)
+    d = np.ascontiguousarray(d_bits, dtype=np.uint16).reshape(n, ns)
+    dm = np.ascontiguousarray(dmin_bits, dtype=np.uint16).reshape(n, ns)
+    out[:, :, 0], out[:, :, 1] = (d & 0xFF).astype(np.uint8), (d >> 8).astype(np.uint8)
+    out[:, :, 2], out[:, :, 3] = (dm & 0xFF).astype(np.uint8), (dm >> 8).astype(np.uint8)
+    fields = (np.asarray(sc).reshape(n, ns, 8).astype(np.int64), np.asarray(mn).reshape(n, ns, 8).astype(np.int64))
+    for f in range(2):
+        for j in range(8):
+            for b in range(6):
+                byte, bit = Q4K_SCALE_BITS[f, j, b]
+                out[:, :, 4 + byte] |= (((fields[f][:, :, j] >> b) & 1) << bit).astype(np.uint8)
+    qq = q.reshape(n, ns, 4, 2, 32).astype(np.uint8)   # superblock, run, low / high, element
+    out[:, :, 16:] = (qq[:, :, :, 0, :] | (qq[:, :, :, 1, :] << 4)).reshape(n, ns, 128)
+    return out
+
+
 def pack_affine_nibbles(q: np.ndarray) -> np.ndarray:
     """Pack nibbles ``q[n, k]`` into ``uint8[n, k/2]`` (even element low)."""
     q = q.astype(np.uint8)
@@ -85,6 +138,13 @@ class Q8_0Host:
     n: int
     k: int
     blocks8: np.ndarray         # uint8[n, k/32, 34]
+
+
+@dataclass
+class Q4_KHost:
+    n: int
+    k: int
+    blocks_k: np.ndarray        # uint8[n, k/256, 144]
 
 
 @dataclass
@@ -122,6 +182,19 @@ def q4_0_to_q8_0(H: Q4_0Host) -> Q8_0Host:
     out[:, :, :2] = b[:, :, :2]
     out[:, :, 2:] = nib.astype(np.int8).view(np.uint8)
     return Q8_0Host(H.n, H.k, out)
+
+
+def draw_q4_k(rng: np.random.Generator, n: int, k: int, d_range=(0.0001, 0.0004),
+              dmin_range=(0.0002, 0.0008)) -> Q4_KHost:
+    """q ~ U{0..15}, sub-block scales and mins ~ U{0..63}, d and dmin ~
+    U[range] rounded to fp16 (weights of about the Q4_0 draws' magnitude)."""
+    assert k % 256 == 0
+    q = rng.integers(0, 16, size=(n, k), dtype=np.uint8)
+    sc = rng.integers(0, 64, size=(n, k // 32))
+    mn = rng.integers(0, 64, size=(n, k // 32))
+    d = rng.uniform(d_range[0], d_range[1], size=(n, k // 256)).astype(np.float16)
+    dm = rng.uniform(dmin_range[0], dmin_range[1], size=(n, k // 256)).astype(np.float16)
+    return Q4_KHost(n, k, pack_q4_k(q, sc, mn, d.view(np.uint16), dm.view(np.uint16)))
 
 
 def draw_affine(rng: np.random.Generator, n: int, k: int,
@@ -256,7 +329,9 @@ def _draw_fmt(fmt: str):
         return draw_affine
     if fmt == "q8_0":
         return draw_q8_0
-    raise ValueError("fmt must be 'q4_0', 'affine' or 'q8_0'")
+    if fmt == "q4_k":
+        return draw_q4_k
+    raise ValueError("fmt must be 'q4_0', 'affine', 'q8_0' or 'q4_k'")
 
 
 def cfg4_layer(seed: int, layer: int, hidden: int = 2048, kv: int = 512,

@@ -39,6 +39,18 @@ MUTANTS = [
     ("q8_0 block stride", "const uint8_t *blk = r + b * 34;", "const uint8_t *blk = r + b * 32;"),
     ("q8_0 scale byte order", "double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));\n        for (int j = 0; j < 32; ++j) {\n            int q = blk[2 + j]",
      "double d = q4o_half((uint16_t)(blk[1] | (blk[0] << 8)));\n        for (int j = 0; j < 32; ++j) {\n            int q = blk[2 + j]"),
+    ("q4_k min sign", "w[b * 256 + e] = d * (double)sc * (double)q - dmin * (double)mn;",
+     "w[b * 256 + e] = d * (double)sc * (double)q + dmin * (double)mn;"),
+    ("q4_k d and dmin swapped", "double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));\n        double dmin",
+     "double d = q4o_half((uint16_t)(blk[2] | (blk[3] << 8)));\n        double dmin"),
+    ("q4_k nibble halves swapped", "int q = (j & 1) ? (byte >> 4) : (byte & 0x0f);",
+     "int q = (j & 1) ? (byte & 0x0f) : (byte >> 4);"),
+    ("q4_k nibbles interleaved", "int byte = qs[32 * (j / 2) + l];", "int byte = qs[e / 2];"),
+    ("q4_k high scale bits from the min byte", "*sc = (sb[j + 4] & 0x0f) | ((sb[j - 4] >> 6) << 4);",
+     "*sc = (sb[j + 4] & 0x0f) | ((sb[j] >> 6) << 4);"),
+    ("q4_k high min nibble", "*mn = (sb[j + 4] >> 4) | ((sb[j] >> 6) << 4);",
+     "*mn = (sb[j + 4] & 0x0f) | ((sb[j] >> 6) << 4);"),
+    ("q4_k low mins from the scale bytes", "*mn = sb[j + 4] & 63;", "*mn = sb[j] & 63;"),
     ("halfset streams swapped", "x[r * k + 2 * i] = q4o_half(xe[r * (k / 2) + i]);",
      "x[r * k + 2 * i] = q4o_half(xo[r * (k / 2) + i]);"),
     ("halfset rows concatenated", "x[r * k + 2 * i + 1] = q4o_half(xo[r * (k / 2) + i]);",

@@ -496,3 +496,93 @@ def test_q8_0_brute_force_fsum():
             terms = dense[i] * x[r].astype(np.float64)
             assert abs(y[r, i] - math.fsum(terms)) <= 1e-12 * math.fsum(np.abs(terms))
             assert abs(S[r, i] - math.fsum(np.abs(terms))) <= 1e-12 * S[r, i]
+
+
+# ---- Q4_K superblocks (crate inferencelayer, gemv_q5k_k_lcpp_src: f16 d and
+# dmin, 12 bytes of 6-bit sub-scales and sub-mins, 128 nibble bytes;
+# w = d*sc*q - dmin*mn).  The generator's bit-position table is written from
+# the pack's description independently of the oracle's shift-and-mask decoder.
+
+def test_q4_k_scale_table_is_a_bijection():
+    # every one of the 96 bits of the 12 scale bytes holds exactly one bit of
+    # one field
+    pos = wl.Q4K_SCALE_BITS.reshape(-1, 2)
+    flat = pos[:, 0] * 8 + pos[:, 1]
+    assert sorted(flat.tolist()) == list(range(96))
+
+
+@pytest.mark.parametrize("j", range(8))
+def test_q4_k_scale_min_every_value(j):
+    # every 6-bit value of both fields of sub-block j, the other fields random
+    rng = np.random.default_rng(100 + j)
+    for v in range(64):
+        sc = rng.integers(0, 64, size=8)
+        mn = rng.integers(0, 64, size=8)
+        sc[j], mn[j] = v, 63 - v
+        q = np.zeros((1, 256), dtype=np.uint8)
+        blk = wl.pack_q4_k(q, sc[None], mn[None], np.zeros((1, 1), np.uint16), np.zeros((1, 1), np.uint16))
+        for jj in range(8):
+            assert oracle.q4_k_scale_min(blk[0, 0, 4:16], jj) == (sc[jj], mn[jj])
+
+
+def test_q4_k_value_formula_exact():
+    # each weight is d*sc*q - dmin*mn with one rounding (exact rationals)
+    rng = np.random.default_rng(110)
+    n, k = 6, 512
+    q = rng.integers(0, 16, size=(n, k), dtype=np.uint8)
+    sc = rng.integers(0, 64, size=(n, k // 32))
+    mn = rng.integers(0, 64, size=(n, k // 32))
+    d = rng.uniform(1e-4, 4e-4, (n, k // 256)).astype(np.float16)
+    dm = rng.uniform(2e-4, 8e-4, (n, k // 256)).astype(np.float16)
+    H = wl.Q4_KHost(n, k, wl.pack_q4_k(q, sc, mn, d.view(np.uint16), dm.view(np.uint16)))
+    W = oracle.dequant(oracle._hw(H))
+    for i in range(n):
+        for e in range(0, k, 7):
+            exact = (Fraction(float(d[i, e // 256])) * int(sc[i, e // 32]) * int(q[i, e])
+                     - Fraction(float(dm[i, e // 256])) * int(mn[i, e // 32]))
+            assert W[i, e] == float(exact)
+
+
+def test_q4_k_nibble_order_one_hot():
+    # row e of a 256 x 256 matrix has nibble 15 at element e and 0 elsewhere,
+    # every scale 1, every min 0, d = 1: the decode is 15 * identity
+    n = k = 256
+    q = np.eye(n, k, dtype=np.uint8) * 15
+    one = np.full((n, 1), np.float16(1.0)).view(np.uint16)
+    H = wl.Q4_KHost(n, k, wl.pack_q4_k(q, np.ones((n, 8), int), np.zeros((n, 8), int), one,
+                                       np.zeros((n, 1), np.uint16)))
+    assert np.array_equal(oracle.dequant(oracle._hw(H)), 15.0 * np.eye(n))
+
+
+def test_q4_k_equals_q4_0_with_shared_scale():
+    # Q4_0 blocks whose eight scales in a superblock are equal are the Q4_K
+    # superblock with d = dmin = that scale, every sc = 1 and every mn = 8:
+    # d*q - 8d = d*(q - 8)
+    rng = np.random.default_rng(111)
+    n, k = 9, 512
+    q = rng.integers(0, 16, size=(n, k), dtype=np.uint8)
+    d = rng.uniform(0.005, 0.02, (n, k // 256)).astype(np.float16)
+    H0 = wl.Q4_0Host(n, k, wl.pack_q4_0(q, np.repeat(d, 8, axis=1).view(np.uint16)))
+    HK = wl.Q4_KHost(n, k, wl.pack_q4_k(q, np.ones((n, k // 32), int), np.full((n, k // 32), 8),
+                                        d.view(np.uint16), d.view(np.uint16)))
+    assert np.array_equal(oracle.dequant(oracle._hw(H0)), oracle.dequant(oracle._hw(HK)))
+
+
+def test_q4_k_brute_force_fsum():
+    rng = np.random.default_rng(112)
+    n, k = 10, 256
+    q = rng.integers(0, 16, size=(n, k), dtype=np.uint8)
+    sc = rng.integers(0, 64, size=(n, k // 32))
+    mn = rng.integers(0, 64, size=(n, k // 32))
+    d = rng.uniform(1e-4, 4e-4, (n, 1)).astype(np.float16)
+    dm = rng.uniform(2e-4, 8e-4, (n, 1)).astype(np.float16)
+    H = wl.Q4_KHost(n, k, wl.pack_q4_k(q, sc, mn, d.view(np.uint16), dm.view(np.uint16)))
+    x = wl.draw_x(rng, 2, k)
+    y, S = oracle.q4_gemv(oracle._hw(H), x)
+    dense = (d.astype(np.float64) * np.repeat(sc, 32, axis=1) * q
+             - dm.astype(np.float64) * np.repeat(mn, 32, axis=1))
+    for r in range(2):
+        for i in range(n):
+            terms = dense[i] * x[r].astype(np.float64)
+            assert abs(y[r, i] - math.fsum(terms)) <= 1e-12 * math.fsum(np.abs(terms))
+            assert abs(S[r, i] - math.fsum(np.abs(terms))) <= 1e-12 * S[r, i]
