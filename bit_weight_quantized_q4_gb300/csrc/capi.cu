@@ -25,11 +25,16 @@ bool shape_ok(int32_t n, int32_t k) {
     return n >= 1 && k >= 32 && k % 32 == 0 && k <= 65536 && n <= (1 << 24);
 }
 
+inline bool fmt_known(int32_t fmt) {
+    return fmt == Q4_FMT_Q4_0 || fmt == Q4_FMT_AFFINE || fmt == Q4_FMT_Q8_0 || fmt == Q4_FMT_Q4_K;
+}
+
 q4_status check_weight(const q4_weight *W) {
     if (!W || !W->dev) return Q4_ERR_NULL;
-    if (W->fmt != Q4_FMT_Q4_0 && W->fmt != Q4_FMT_AFFINE && W->fmt != Q4_FMT_Q8_0) return Q4_ERR_UNSUPPORTED;
+    if (!fmt_known(W->fmt)) return Q4_ERR_UNSUPPORTED;
     if (!shape_ok(W->n, W->k)) return Q4_ERR_SHAPE;
-    if (W->bytes < q4_packed_bytes(W->fmt, W->n, W->k)) return Q4_ERR_SHAPE;
+    const size_t need = q4_packed_bytes(W->fmt, W->n, W->k);  // 0: k not whole superblocks (Q4_K)
+    if (need == 0 || W->bytes < need) return Q4_ERR_SHAPE;
     if (!aligned16(W->dev)) return Q4_ERR_ALIGN;
     return Q4_OK;
 }
@@ -140,7 +145,8 @@ q4_status launch_planned(const q4::GemvParams &p, int fmt, const q4::Plan &plan,
     cudaGetLastError();  // clear a stale error so the check below is ours
     int rc = fmt == Q4_FMT_Q4_0     ? q4::launch_gemv_q4_0(pp, plan, stream)
              : fmt == Q4_FMT_AFFINE ? q4::launch_gemv_affine(pp, plan, stream)
-                                    : q4::launch_gemv_q8_0(pp, plan, stream);
+             : fmt == Q4_FMT_Q8_0   ? q4::launch_gemv_q8_0(pp, plan, stream)
+                                    : q4::launch_gemv_q4_k(pp, plan, stream);
     if (rc != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
     return Q4_OK;
 }
@@ -173,7 +179,7 @@ const char *q4_status_str(q4_status s) {
 q4_status q4_plan(int32_t fmt, int32_t tiles, int32_t chunks, int32_t nb, int32_t pairs, int32_t sms,
                   int32_t out[6]) {
     if (!out) return Q4_ERR_NULL;
-    if (fmt != Q4_FMT_Q4_0 && fmt != Q4_FMT_AFFINE && fmt != Q4_FMT_Q8_0) return Q4_ERR_UNSUPPORTED;
+    if (!fmt_known(fmt)) return Q4_ERR_UNSUPPORTED;
     if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
     if (tiles < 1 || chunks < 1 || sms < 1 || (pairs && (tiles & 1))) return Q4_ERR_SHAPE;
     q4::Plan p = q4::make_plan(fmt, tiles, chunks, nb, pairs != 0, sms);
@@ -205,7 +211,7 @@ q4_status q4_gemv(const q4_weight *W, const float *x, const float *gsum, int32_t
     if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
     if (gsum && !aligned16(gsum)) return Q4_ERR_ALIGN;
     q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, x, nullptr, 0.f, nb);
-    p.gsum = W->fmt == Q4_FMT_AFFINE ? gsum : nullptr;
+    p.gsum = q4::has_min(W->fmt) ? gsum : nullptr;
     p.epi = q4::EPI_STORE;
     p.out[0] = y;
     return run(p, W->fmt, stream);
@@ -236,7 +242,7 @@ q4_status q4_gemv_half(const q4_weight *W, const uint16_t *x_even, const uint16_
     q4::GemvParams p = base_params(W, nullptr, q4::MODE_SINGLE, nullptr, nullptr, 0.f, nb);
     p.xe = x_even;
     p.xo = x_odd;
-    p.gsum = W->fmt == Q4_FMT_AFFINE ? gsum : nullptr;
+    p.gsum = q4::has_min(W->fmt) ? gsum : nullptr;
     p.epi = q4::EPI_STORE;
     p.out[0] = y;
     return run(p, W->fmt, stream);
@@ -597,13 +603,15 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     if (smem > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;
     const int occ = fmt == Q4_FMT_Q4_0     ? q4::step_occupancy_q4_0(nb, smem)
                     : fmt == Q4_FMT_AFFINE ? q4::step_occupancy_affine(nb, smem)
-                                           : q4::step_occupancy_q8_0(nb, smem);
+                    : fmt == Q4_FMT_Q8_0   ? q4::step_occupancy_q8_0(nb, smem)
+                                           : q4::step_occupancy_q4_k(nb, smem);
     if (occ < 1) return Q4_ERR_UNSUPPORTED;
     cudaGetLastError();
     if (cudaMemsetAsync(workspace, 0, 16, stream) != cudaSuccess) return Q4_ERR_CUDA;
     const int rc = fmt == Q4_FMT_Q4_0     ? q4::launch_step_q4_0(sp, G, smem, stream)
                    : fmt == Q4_FMT_AFFINE ? q4::launch_step_affine(sp, G, smem, stream)
-                                          : q4::launch_step_q8_0(sp, G, smem, stream);
+                   : fmt == Q4_FMT_Q8_0   ? q4::launch_step_q8_0(sp, G, smem, stream)
+                                          : q4::launch_step_q4_k(sp, G, smem, stream);
     if (rc != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
     return Q4_OK;
 }

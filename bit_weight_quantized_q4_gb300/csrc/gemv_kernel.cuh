@@ -184,6 +184,27 @@ __device__ __forceinline__ float2 scale_pair(uint32_t w) {
     }
 }
 
+// Q4_K: the rows' fp16 d and dmin (words {row g, row g+8}) as d * 2^24 and
+// -dmin * 2^24, the factors q4k_pair takes.
+__device__ __forceinline__ void q4k_rows(uint32_t dw, uint32_t mw, float2 &dd, float2 &dm) {
+    const float2 d = __half22float2(*reinterpret_cast<const __half2 *>(&dw));
+    const float2 m = __half22float2(*reinterpret_cast<const __half2 *>(&mw));
+    constexpr float P = 16777216.f;  // 2^24
+    dd = make_float2(d.x * P, d.y * P);
+    dm = make_float2(-m.x * P, -m.y * P);
+}
+// Q4_K: block scale d*sc and min -dmin*mn of rows g and g+8 from the record's
+// byte word {sc(g), mn(g), sc(g+8), mn(g+8)}.  prmt makes each 6-bit byte an
+// exact f16 subnormal v * 2^-24, so with dd, dm from q4k_rows both products
+// are exact in fp32.
+__device__ __forceinline__ void q4k_pair(uint32_t w, float2 dd, float2 dm, float2 &s2, float2 &m2) {
+    const uint32_t scw = bytes_to_half2<0x4240>(w), mnw = bytes_to_half2<0x4341>(w);
+    const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(&scw));
+    const float2 mn = __half22float2(*reinterpret_cast<const __half2 *>(&mnw));
+    s2 = make_float2(dd.x * sc.x, dd.y * sc.y);
+    m2 = make_float2(dm.x * mn.x, dm.y * mn.y);
+}
+
 __device__ __forceinline__ void map_tile(const GemvParams &p, int t, int &m, int &tm) {
     if (p.mode == MODE_PAIRS) {
         m = t & 1;
@@ -703,7 +724,7 @@ __device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int
     const int Cs = p.Cs;                  // staged chunks; columns at or beyond ke are zero
     const int kb = q.kb, ke = q.ke;
     const bool norm = p.gamma != nullptr;
-    const bool given = FMT == 1 && p.gsum != nullptr && !norm;  // affine sums from the caller
+    const bool given = has_min(FMT) && p.gsum != nullptr && !norm;  // block sums from the caller
     const int nch = warp < Cs ? (Cs - 1 - warp) / NW + 1 : 0;   // chunks of this warp
     float2 xv[RP], gv[RP];
     // every load first (guarded, not a loop exit, so that they can all be in
@@ -741,12 +762,12 @@ __device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int
         block_scale<FMT>(bm, sc, back);
         put_pair<FMT, CLS>(m.xs, 128, 0, kl, a0 * sc, a1 * sc);
         float bsum = 0.f;
-        if (FMT == 1 && !given) bsum = half_warp_sum(a0 + a1);
+        if (has_min(FMT) && !given) bsum = half_warp_sum(a0 + a1);
         if ((lane & 15) == 0) {
             m.fs[gs_idx(kl >> 5, 0, GSW)] = back;
-            if (FMT == 1 && !given) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum;
+            if (has_min(FMT) && !given) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum;
         }
-        if (FMT != 1 && (qq & 1)) {  // the chunk is written: its eights (zero-weight) product
+        if (!has_min(FMT) && (qq & 1)) {  // the chunk is written: its eights (zero-weight) product
             __syncwarp();
             eights_chunk<FMT, CLS>(m, c, lane);
         }
@@ -782,7 +803,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
     const int kb = q.kb, ke = q.ke;
     const int xbs = cls_xrow(CLS) * nb;
     const bool norm = p.gamma != nullptr;
-    const bool given = FMT == 1 && p.gsum != nullptr && !norm;  // affine sums from the caller
+    const bool given = has_min(FMT) && p.gsum != nullptr && !norm;  // block sums from the caller
     const int nseg = nb * Cs;
     const int spw = (nseg + NW - 1) / NW;
     const int s0 = min(warp * spw, nseg), s1 = min(s0 + spw, nseg);
@@ -859,7 +880,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
                 l1 = __floats2half2_rn(a.z * f - b1.x, a.w * f - b1.y);
             }
             float bsum = 0.f;
-            if (FMT == 1 && !given) bsum = block8_sum(a);
+            if (has_min(FMT) && !given) bsum = block8_sum(a);
             if (valid) {
                 const int seg = C::HLN ? 4 * c * xbs + 128 * r : 4 * c * xbs + (r >> 3) * 512 + (r & 7) * 64;
                 uint8_t *d = m.xs + seg + lane_off;
@@ -871,7 +892,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
                 }
                 if ((lane & 7) == 0) {
                     m.fs[gs_idx(kl >> 5, r, GSW)] = back;
-                    if (FMT == 1 && !given) m.gs[gs_idx(kl >> 5, r, GSW)] = bsum;
+                    if (has_min(FMT) && !given) m.gs[gs_idx(kl >> 5, r, GSW)] = bsum;
                 }
             }
             if (++c == Cs) {
@@ -923,7 +944,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
         }
     }
     stage_finish<CLS>(p, m, S, nb, tid);
-    if (CLS == 0 && FMT != 1) eights_c0<FMT, CLS>(m, Cs, warp, lane);
+    if (CLS == 0 && !has_min(FMT)) eights_c0<FMT, CLS>(m, Cs, warp, lane);
 }
 
 template <int I>
@@ -1005,8 +1026,13 @@ __device__ __forceinline__ void record_c0(uint32_t ra, const ChunkX &x, int lane
     RecWords<FMT> rw;
     rw.load(ra, lane);
     uint32_t sw, mw = 0u;                            // scales (mins) of (row g, block t), (row g + 8, block t)
+    uint32_t dw = 0u, dmw = 0u;                      // Q4_K: d and dmin of rows g, g + 8
     asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(sw) : "r"(ra + lane * 4), "n"(scale_off<FMT>()) : "memory");
     if (FMT == 1) asm volatile("ld.shared.u32 %0, [%1+1152];" : "=r"(mw) : "r"(ra + lane * 4) : "memory");
+    if (FMT == 3) {
+        asm volatile("ld.shared.u32 %0, [%1+1152];" : "=r"(dw) : "r"(ra + (lane >> 2) * 4) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1+1184];" : "=r"(dmw) : "r"(ra + (lane >> 2) * 4) : "memory");
+    }
     const float z = 0.f;
     float dA[4], dB[4];
     uint32_t a[8], b[8];
@@ -1024,12 +1050,19 @@ __device__ __forceinline__ void record_c0(uint32_t ra, const ChunkX &x, int lane
     mma16816(dB, b[4], b[5], b[6], b[7], x.B[3].z, x.B[3].w);
     const float T0 = (dA[0] + dB[0]) + (dA[1] + dB[1]);  // block t, row g: hi + lo
     const float T2 = (dA[2] + dB[2]) + (dA[3] + dB[3]);  // row g + 8
-    const float2 s2 = scale_pair<FMT>(sw);
-    if (FMT != 1) {
+    float2 s2, m2 = make_float2(0.f, 0.f);
+    if constexpr (FMT == 3) {
+        float2 dd, dm;
+        q4k_rows(dw, dmw, dd, dm);
+        q4k_pair(sw, dd, dm, s2, m2);
+    } else {
+        s2 = scale_pair<FMT>(sw);
+        if (FMT == 1) m2 = scale_pair<FMT>(mw);
+    }
+    if (!has_min(FMT)) {
         a0 = fmaf(s2.x * x.F, T0 - x.G, a0);
         a1 = fmaf(s2.y * x.F, T2 - x.G, a1);
     } else {
-        const float2 m2 = scale_pair<FMT>(mw);
         a0 = fmaf(m2.x, x.G, fmaf(s2.x * x.F, T0, a0));
         a1 = fmaf(m2.y, x.G, fmaf(s2.y * x.F, T2, a1));
     }
@@ -1231,7 +1264,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             F[j][1] = fv.y;
             F[j][2] = fv.z;
             F[j][3] = fv.w;
-            if (FMT == 1) {
+            if (has_min(FMT)) {
                 const float4 gv = *reinterpret_cast<const float4 *>(m.gs + (cc * C::GSW + grow[j]) * 4);
                 G[j][0] = gv.x;
                 G[j][1] = gv.y;
@@ -1242,14 +1275,22 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
         // the records' words: weights of rows g and g+8, scales (and mins)
         RecWords<FMT> rw[2];
         uint4 sw[2], mw[2];
+        float2 dd[2], dm[2];  // Q4_K: the rows' d and dmin factors (q4k_rows)
 #pragma unroll
         for (int rc = 0; rc < 2; ++rc) {
             sw[rc] = mw[rc] = make_uint4(0u, 0u, 0u, 0u);
+            dd[rc] = dm[rc] = make_float2(0.f, 0.f);
             if (rc == 0 || two) {
                 const uint32_t ra = st_a + rc * SU * REC;
                 rw[rc].load(ra, lane);
                 sw[rc] = lds128_at<scale_off<FMT>()>(ra + g * 16);
                 if (FMT == 1) mw[rc] = lds128_at<1152>(ra + g * 16);
+                if (FMT == 3) {
+                    uint32_t dw, dmw;
+                    asm volatile("ld.shared.u32 %0, [%1+1152];" : "=r"(dw) : "r"(ra + g * 4) : "memory");
+                    asm volatile("ld.shared.u32 %0, [%1+1184];" : "=r"(dmw) : "r"(ra + g * 4) : "memory");
+                    q4k_rows(dw, dmw, dd[rc], dm[rc]);
+                }
             }
         }
         const uint8_t *xchunk = m.xs + cc * kBlocksPerChunk * xbs;
@@ -1260,7 +1301,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             uint4 B[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) B[nt] = *reinterpret_cast<const uint4 *>(xa + boff[nt]);
-            if (FMT != 1) {
+            if (!has_min(FMT)) {
                 // the block's offset product: the same tensor-core chain as the
                 // weights' below, with every weight zero (every nibble 8 for
                 // Q4_0, every biased byte 128 for Q8_0): exactly what such a
@@ -1284,9 +1325,13 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                 if (rc == 1 && !two) continue;
                 uint32_t a[8];
                 rw[rc].template regs<blk>(a);  // rows g (even) and g + 8 (odd)
-                const float2 s2 = scale_pair<FMT>(word_of<blk>(sw[rc]));
-                float2 m2 = make_float2(0.f, 0.f);
-                if (FMT == 1) m2 = scale_pair<FMT>(word_of<blk>(mw[rc]));
+                float2 s2, m2 = make_float2(0.f, 0.f);
+                if constexpr (FMT == 3) {
+                    q4k_pair(word_of<blk>(sw[rc]), dd[rc], dm[rc], s2, m2);
+                } else {
+                    s2 = scale_pair<FMT>(word_of<blk>(sw[rc]));
+                    if (FMT == 1) m2 = scale_pair<FMT>(word_of<blk>(mw[rc]));
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     float d[4];
@@ -1296,7 +1341,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                         mma16816(d, a[4], a[5], a[6], a[7], B[nt].z, B[nt].w);
                         const float T0 = d[0] + d[1], T2 = d[2] + d[3];
                         const float fb = F[0][blk];
-                        if (FMT != 1) {
+                        if (!has_min(FMT)) {
                             acc[rc][0] = fmaf(s2.x * fb, T0 - G[0][blk], acc[rc][0]);
                             acc[rc][1] = fmaf(s2.y * fb, T2 - G[0][blk], acc[rc][1]);
                         } else {
@@ -1312,7 +1357,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                             const float sj = (j < 2 ? s2.x : s2.y) * F[2 * nt + (j & 1)][blk];
                             const float gj = G[2 * nt + (j & 1)][blk];
                             float &ac = acc[rc][4 * nt + j];
-                            if (FMT != 1) {
+                            if (!has_min(FMT)) {
                                 ac = fmaf(sj, d[j] - gj, ac);
                             } else {
                                 const float mj = j < 2 ? m2.x : m2.y;

@@ -40,6 +40,13 @@ constexpr int kRecAffine = 1280;
 // its row's first block of the pair, then of the second.  Byte i of a lane's
 // 8 holds block element q8_elem(t, i).
 constexpr int kRecQ8_0 = 2176;
+// Q4_K records (1216 bytes): the nibble words as for Q4_0 at [0, 1024); at
+// [1024, 1152) word j of group g holds the bytes sc(g, j), mn(g, j),
+// sc(g+8, j), mn(g+8, j) -- the 6-bit scale and min of block j of rows g and
+// g+8; at [1152, 1184) word g holds the fp16 d of rows g (low half) and g+8
+// (high half) of the superblock the chunk belongs to, and at [1184, 1216) their
+// fp16 dmin.  A 256-column superblock spans two chunks; each carries d, dmin.
+constexpr int kRecQ4_K = 1216;
 
 // Block element (0..31) stored in nibble i of lane-position t's word.
 // Pairs (i, i+4) are (k, k+1) of one f16x2 fragment register:
@@ -61,7 +68,12 @@ inline int q8_elem(int t, int i) {
     return base[i >> 1] + 2 * t + (i & 1);
 }
 
-Q4_HD constexpr int rec_bytes(int fmt) { return fmt == 0 ? kRecQ4_0 : fmt == 1 ? kRecAffine : kRecQ8_0; }
+Q4_HD constexpr int rec_bytes(int fmt) {
+    return fmt == 0 ? kRecQ4_0 : fmt == 1 ? kRecAffine : fmt == 2 ? kRecQ8_0 : kRecQ4_K;
+}
+// Formats whose weights carry a per-block min (w = s*q + m): the products
+// need the activation block sums.
+Q4_HD constexpr bool has_min(int fmt) { return fmt == 1 || fmt == 3; }
 inline int64_t tiles_of(int64_t n) { return (n + kTileRows - 1) / kTileRows; }
 inline int64_t chunks_of(int64_t k) { return (k + kChunkK - 1) / kChunkK; }
 
@@ -299,13 +311,16 @@ inline size_t step_smem_bytes(int fmt, int nb, int TGmax, int Kmax, int SWmax, i
 int launch_gemv_q4_0(const GemvParams &p, const Plan &plan, void *stream);
 int launch_gemv_affine(const GemvParams &p, const Plan &plan, void *stream);
 int launch_gemv_q8_0(const GemvParams &p, const Plan &plan, void *stream);
+int launch_gemv_q4_k(const GemvParams &p, const Plan &plan, void *stream);
 // Cooperative launch of the decode-step kernel: one CTA per SM.
 int launch_step_q4_0(const StepParams &p, int ctas, size_t smem, void *stream);
 int launch_step_affine(const StepParams &p, int ctas, size_t smem, void *stream);
 int launch_step_q8_0(const StepParams &p, int ctas, size_t smem, void *stream);
+int launch_step_q4_k(const StepParams &p, int ctas, size_t smem, void *stream);
 // Decode-step CTAs that can be resident on one SM (0 on error).
 int step_occupancy_q4_0(int nb, size_t smem);
 int step_occupancy_affine(int nb, size_t smem);
 int step_occupancy_q8_0(int nb, size_t smem);
+int step_occupancy_q4_k(int nb, size_t smem);
 
 }  // namespace q4

@@ -1,4 +1,4 @@
-// repack.cpp -- host-side lossless re-layout of Q4_0 / affine-Q4 weights into
+// repack.cpp -- host-side lossless re-layout of Q4_0 / affine-Q4 / Q8_0 / Q4_K weights into
 // the coalesced device layout described in q4_internal.h, and its inverse.
 //
 // The pages re-lay block formats once at load time so that the GEMV reads
@@ -44,17 +44,56 @@ inline int affine_nib(const uint8_t *row, int64_t e) {
     return (e & 1) ? (b >> 4) : (b & 15);
 }
 
+// Q4_K superblock (144 bytes: fp16 d, fp16 dmin, 12 scale bytes, 128
+// nibble bytes).  Sub-block j's 6-bit scale and min: for j < 4 the low six
+// bits of bytes j and j + 4; for j >= 4 the low and high nibbles of byte
+// j + 4, topped by the upper two bits of bytes j - 4 and j.
+inline void q4k_get(const uint8_t *sb, int j, int &sc, int &mn) {
+    const uint8_t *s = sb + 4;
+    if (j < 4) {
+        sc = s[j] & 0x3F;
+        mn = s[j + 4] & 0x3F;
+    } else {
+        sc = (s[j + 4] & 0x0F) | ((s[j - 4] & 0xC0) >> 2);
+        mn = (s[j + 4] >> 4) | ((s[j] & 0xC0) >> 2);
+    }
+}
+inline void q4k_put(uint8_t *sb, int j, int sc, int mn) {
+    uint8_t *s = sb + 4;
+    if (j < 4) {
+        s[j] = (uint8_t)((s[j] & 0xC0) | sc);
+        s[j + 4] = (uint8_t)((s[j + 4] & 0xC0) | mn);
+    } else {
+        s[j + 4] = (uint8_t)((sc & 0x0F) | ((mn & 0x0F) << 4));
+        s[j - 4] = (uint8_t)((s[j - 4] & 0x3F) | ((sc >> 4) << 6));
+        s[j] = (uint8_t)((s[j] & 0x3F) | ((mn >> 4) << 6));
+    }
+}
+// Nibble of element e (0..31) of sub-block j: runs of 32 bytes, sub-block 2r
+// in the low nibbles of run r and 2r + 1 in the high ones.
+inline int q4k_nib(const uint8_t *sb, int j, int e) {
+    const int b = sb[16 + 32 * (j >> 1) + e];
+    return (j & 1) ? (b >> 4) : (b & 15);
+}
+
 }  // namespace
 
-inline bool fmt_ok(int32_t fmt) { return fmt == Q4_FMT_Q4_0 || fmt == Q4_FMT_AFFINE || fmt == Q4_FMT_Q8_0; }
+inline bool fmt_ok(int32_t fmt) {
+    return fmt == Q4_FMT_Q4_0 || fmt == Q4_FMT_AFFINE || fmt == Q4_FMT_Q8_0 || fmt == Q4_FMT_Q4_K;
+}
+// Q4_K rows are whole 256-column superblocks.
+inline bool fmt_shape_ok(int32_t fmt, int32_t n, int32_t k) {
+    return fmt_ok(fmt) && shape_ok(n, k) && (fmt != Q4_FMT_Q4_K || k % 256 == 0);
+}
 
 extern "C" size_t q4_packed_bytes(int32_t fmt, int32_t n, int32_t k) {
-    if (!fmt_ok(fmt) || !shape_ok(n, k)) return 0;
+    if (!fmt_shape_ok(fmt, n, k)) return 0;
     return (size_t)q4::tiles_of(n) * (size_t)q4::chunks_of(k) * (size_t)q4::rec_bytes(fmt);
 }
 
 extern "C" size_t q4_weight_bytes(int32_t fmt, int32_t n, int32_t k) {
-    if (!fmt_ok(fmt) || !shape_ok(n, k)) return 0;
+    if (!fmt_shape_ok(fmt, n, k)) return 0;
+    if (fmt == Q4_FMT_Q4_K) return (size_t)n * (size_t)(k / 256) * 144u;
     return (size_t)n * (size_t)(k / 32) * (fmt == Q4_FMT_Q4_0 ? 18u : fmt == Q4_FMT_AFFINE ? 20u : 34u);
 }
 
@@ -125,6 +164,45 @@ extern "C" q4_status q4_repack_affine(const uint8_t *nib, const uint16_t *s, con
          [&](int64_t row, int64_t blk, int e) { return affine_nib(nib + row * (k / 2), blk * 32 + e); },
          [&](int64_t row, int64_t blk) { return (uint32_t)s[row * B + blk]; },
          [&](int64_t row, int64_t blk) { return (uint32_t)m[row * B + blk]; });
+    return Q4_OK;
+}
+
+extern "C" q4_status q4_repack_q4_k(const void *host_blocks, int32_t n, int32_t k, void *host_out,
+                                    size_t out_bytes) {
+    if (!host_blocks || !host_out) return Q4_ERR_NULL;
+    if (!fmt_shape_ok(Q4_FMT_Q4_K, n, k)) return Q4_ERR_SHAPE;
+    if (out_bytes < q4_packed_bytes(Q4_FMT_Q4_K, n, k)) return Q4_ERR_SHAPE;
+    const uint8_t *src = (const uint8_t *)host_blocks;
+    uint8_t *out = (uint8_t *)host_out;
+    const int64_t NS = k / 256;
+    auto sb_ptr = [&](int64_t row, int64_t blk) { return src + (row * NS + blk / 8) * 144; };
+    // nibble words, and the 6-bit scale and min of each block as the two
+    // bytes of its 16-bit "scale" (padding: all zero, d = 0)
+    pack(Q4_FMT_Q4_K, n, k, out,
+         [&](int64_t row, int64_t blk, int e) { return q4k_nib(sb_ptr(row, blk), (int)(blk % 8), e); },
+         [&](int64_t row, int64_t blk) {
+             int sc, mn;
+             q4k_get(sb_ptr(row, blk), (int)(blk % 8), sc, mn);
+             return (uint32_t)sc | ((uint32_t)mn << 8);
+         },
+         [&](int64_t, int64_t) { return 0u; });
+    const int64_t T = q4::tiles_of(n), C = q4::chunks_of(k);
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < C; ++c) {
+            uint8_t *r = out + (t * C + c) * q4::kRecQ4_K;
+            for (int g = 0; g < 8; ++g) {
+                uint32_t dw = 0, mw = 0;
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t row = t * 16 + h * 8 + g;
+                    if (row >= n) continue;
+                    const uint8_t *sb = src + (row * NS + c / 2) * 144;
+                    dw |= ((uint32_t)sb[0] | ((uint32_t)sb[1] << 8)) << (16 * h);
+                    mw |= ((uint32_t)sb[2] | ((uint32_t)sb[3] << 8)) << (16 * h);
+                }
+                store_u32(r + 1152 + g * 4, dw);
+                store_u32(r + 1184 + g * 4, mw);
+            }
+        }
     return Q4_OK;
 }
 
@@ -248,5 +326,33 @@ extern "C" q4_status q4_unpack_affine(const void *host_packed, size_t packed_byt
                s[row * B + blk] = sv;
                m[row * B + blk] = mv;
            });
+    return Q4_OK;
+}
+
+extern "C" q4_status q4_unpack_q4_k(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,
+                                    void *host_blocks) {
+    if (!host_packed || !host_blocks) return Q4_ERR_NULL;
+    if (!fmt_shape_ok(Q4_FMT_Q4_K, n, k)) return Q4_ERR_SHAPE;
+    if (packed_bytes < q4_packed_bytes(Q4_FMT_Q4_K, n, k)) return Q4_ERR_SHAPE;
+    const uint8_t *in = (const uint8_t *)host_packed;
+    uint8_t *dst = (uint8_t *)host_blocks;
+    const int64_t NS = k / 256, C = q4::chunks_of(k);
+    memset(dst, 0, (size_t)n * (size_t)NS * 144);
+    unpack(Q4_FMT_Q4_K, n, k, in, [&](int64_t row, int64_t blk, const int *q, uint16_t sv, uint16_t) {
+        uint8_t *sb = dst + (row * NS + blk / 8) * 144;
+        const int j = (int)(blk % 8);
+        q4k_put(sb, j, sv & 0xFF, sv >> 8);
+        for (int e = 0; e < 32; ++e) sb[16 + 32 * (j >> 1) + e] |= (uint8_t)(q[e] << (4 * (j & 1)));
+        if (j == 0) {  // d and dmin from the superblock's first chunk
+            const uint8_t *r = in + ((row / 16) * C + blk / 4) * q4::kRecQ4_K;
+            const int g = (int)(row % 8), h = (int)((row % 16) / 8);
+            const uint32_t dw = load_u32(r + 1152 + g * 4), mw = load_u32(r + 1184 + g * 4);
+            const uint16_t d = (uint16_t)(dw >> (16 * h)), dm = (uint16_t)(mw >> (16 * h));
+            sb[0] = (uint8_t)(d & 0xFF);
+            sb[1] = (uint8_t)(d >> 8);
+            sb[2] = (uint8_t)(dm & 0xFF);
+            sb[3] = (uint8_t)(dm >> 8);
+        }
+    });
     return Q4_OK;
 }

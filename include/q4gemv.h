@@ -64,7 +64,9 @@ typedef enum {
 typedef enum {
     Q4_FMT_Q4_0 = 0,    /* 32 weights: fp16 scale d + 16 nibble bytes; w = d*(q-8) */
     Q4_FMT_AFFINE = 1,  /* 32 weights: bf16 scale s, bf16 min m, 16 nibble bytes; w = s*q + m */
-    Q4_FMT_Q8_0 = 2     /* 32 weights: fp16 scale d + 32 signed bytes; w = d*q */
+    Q4_FMT_Q8_0 = 2,    /* 32 weights: fp16 scale d + 32 signed bytes; w = d*q */
+    Q4_FMT_Q4_K = 3     /* 256-weight superblocks: fp16 d, dmin, 6-bit sub-scales sc and mins mn
+                           per 32 weights, nibbles; w = d*sc*q - dmin*mn (k a multiple of 256) */
 } q4_format;
 
 /* A non-owning view of one repacked weight matrix in device memory.
@@ -73,7 +75,7 @@ typedef enum {
 typedef struct {
     int32_t fmt;        /* q4_format */
     int32_t n;          /* output rows */
-    int32_t k;          /* input length, multiple of 32 */
+    int32_t k;          /* input length, multiple of 32 (of 256 for Q4_K) */
     const void *dev;    /* device pointer, 16-byte aligned */
     size_t bytes;       /* size of the packed buffer */
 } q4_weight;
@@ -82,11 +84,13 @@ typedef struct {
  * The layout is 16-row tiles x 128-column chunks; rows are padded to a
  * multiple of 16 and columns to a multiple of 128 with zero-valued weights,
  * so the size may exceed the algorithmic 18 (Q4_0) or 20 (affine) bytes per
- * 32 weights when n % 16 or k % 128 is not zero. */
+ * 32 weights when n % 16 or k % 128 is not zero.  Q8_0 takes 2176 bytes per
+ * 16 x 128 tile chunk (34 per 32 weights); Q4_K takes 1216 (19 per 32
+ * weights: each chunk repeats its superblock's d and dmin). */
 size_t q4_packed_bytes(int32_t fmt, int32_t n, int32_t k);
 
-/* Algorithmic weight bytes of an n x k matrix: 18 (Q4_0) or 20 (affine) per
- * 32 weights; 0 on bad shape. */
+/* Algorithmic weight bytes of an n x k matrix: 18 (Q4_0), 20 (affine) or 34
+ * (Q8_0) per 32 weights, 144 per 256 (Q4_K); 0 on bad shape. */
 size_t q4_weight_bytes(int32_t fmt, int32_t n, int32_t k);
 
 /* Host -> host, lossless, deterministic repack of Q4_0 blocks into the
@@ -114,6 +118,20 @@ q4_status q4_repack_q8_0(const void *host_blocks, int32_t n, int32_t k, void *ho
 
 /* Inverse of q4_repack_q8_0 (host -> host). */
 q4_status q4_unpack_q8_0(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k, void *host_blocks);
+
+/* Q4_K host superblocks (crate inferencelayer, Functions:
+ * gemv_q5k_k_lcpp_src, whose layout minus the fifth-bit plane this is;
+ * honeycrisp/mod.rs, quant_matmul's Q4_K branch): [n][k/256] superblocks of
+ * 144 bytes -- fp16 d, fp16 dmin (little endian), 12 bytes of 6-bit sub-block
+ * scales and mins (sub-blocks 0-3: low six bits of bytes j and j+4; 4-7: the
+ * nibbles of byte j+4 topped by bits 6-7 of bytes j-4 and j), 128 nibble bytes
+ * (run r of 32 holds sub-block 2r in its low nibbles, 2r+1 in its high ones);
+ * w = d*sc*q - dmin*mn.  k must be a multiple of 256 (else Q4_ERR_SHAPE).
+ * Lossless, host -> host; host_out holds q4_packed_bytes(Q4_FMT_Q4_K, n, k). */
+q4_status q4_repack_q4_k(const void *host_blocks, int32_t n, int32_t k, void *host_out, size_t out_bytes);
+
+/* Inverse of q4_repack_q4_k (host -> host). */
+q4_status q4_unpack_q4_k(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k, void *host_blocks);
 
 /* Inverse of q4_repack_affine (host -> host). */
 q4_status q4_unpack_affine(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,

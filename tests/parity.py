@@ -18,9 +18,20 @@ def case_seed(*key):
     return zlib.crc32(repr(key).encode()) & 0xFFFF
 
 
+FMT_ID = {"q4_0": 0, "affine": 1, "q8_0": 2, "q4_k": 3}
+
+
+def fmt_k(fmt, k):
+    """A test shape's k for a format: Q4_K rows are whole 256-column
+    superblocks, so its k is rounded up to one."""
+    return -(-k // 256) * 256 if fmt == "q4_k" else k
+
+
 def host_weight(H):
     if hasattr(H, "blocks8"):
         return oracle.HostWeight.q8_0(H.blocks8, H.n, H.k)
+    if hasattr(H, "blocks_k"):
+        return oracle.HostWeight.q4_k(H.blocks_k, H.n, H.k)
     if hasattr(H, "blocks"):
         return oracle.HostWeight.q4_0(H.blocks, H.n, H.k)
     return oracle.HostWeight.affine(H.nib, H.s, H.m, H.n, H.k)
@@ -30,6 +41,8 @@ def dev_weight(H, device="cuda"):
     import bit_weight_quantized_q4_gb300 as q4
     if hasattr(H, "blocks8"):
         return q4.Q4Weight.from_q8_0(H.blocks8, H.n, H.k, device)
+    if hasattr(H, "blocks_k"):
+        return q4.Q4Weight.from_q4_k(H.blocks_k, H.n, H.k, device)
     if hasattr(H, "blocks"):
         return q4.Q4Weight.from_q4_0(H.blocks, H.n, H.k, device)
     return q4.Q4Weight.from_affine(H.nib, H.s, H.m, H.n, H.k, device)

@@ -58,6 +58,51 @@ def test_q8_0_layout_bytes():
     assert np.array_equal(np.sort(P[2048:].view(np.uint16)), np.sort(Q.blocks8[:, :, :2].copy().view(np.uint16).ravel()))
 
 
+@pytest.mark.parametrize("n,k", [(1, 256), (16, 256), (17, 512), (33, 768), (100, 1024)])
+def test_repack_roundtrip_q4_k(n, k):
+    rng = np.random.default_rng(n * 7 + k)
+    H = wl.draw_q4_k(rng, n, k)
+    P = q4.repack_q4_k(H.blocks_k, n, k)
+    assert P.size == q4.packed_bytes(3, n, k)
+    assert np.array_equal(q4.unpack_q4_k(P, n, k), H.blocks_k)
+
+
+def test_q4_k_layout_bytes():
+    # one 16 x 256 superblock row-set is two 1216-byte records; each holds the
+    # 1024 nibble bytes of its half, one byte word per (row pair, block) with
+    # the 6-bit scale and min, and the rows' fp16 d and dmin
+    rng = np.random.default_rng(12)
+    H = wl.draw_q4_k(rng, 16, 256)
+    P = q4.repack_q4_k(H.blocks_k, 16, 256)
+    assert P.size == 2 * 1216 and q4.weight_bytes(3, 16, 256) == 16 * 144
+    b = H.blocks_k[:, 0, :]
+    for c in range(2):
+        r = P[c * 1216:(c + 1) * 1216]
+        d = r[1152:1184].view(np.uint16).reshape(8, 2)
+        dm = r[1184:1216].view(np.uint16).reshape(8, 2)
+        assert np.array_equal(d[:, 0], b[0:8, 0:2].copy().view(np.uint16)[:, 0])
+        assert np.array_equal(d[:, 1], b[8:16, 0:2].copy().view(np.uint16)[:, 0])
+        assert np.array_equal(dm[:, 0], b[0:8, 2:4].copy().view(np.uint16)[:, 0])
+        w = r[1024:1152].reshape(8, 4, 4)            # [g][block][sc_g, mn_g, sc_g8, mn_g8]
+        assert w.max() < 64
+        for g in range(8):
+            for j in range(4):
+                sc, mn = oracle_free_q4k_field(b[g, 4:16], 4 * c + j)
+                assert (w[g, j, 0], w[g, j, 1]) == (sc, mn)
+
+
+def oracle_free_q4k_field(scale_bytes, j):
+    # the generator's bit-position table read backwards
+    vals = []
+    for f in range(2):
+        v = 0
+        for bit in range(6):
+            byte, pos = wl.Q4K_SCALE_BITS[f, j, bit]
+            v |= ((int(scale_bytes[byte]) >> int(pos)) & 1) << bit
+        vals.append(v)
+    return tuple(vals)
+
+
 def test_repack_roundtrip_edge_values():
     # scales: +-0, smallest subnormal, largest finite, inf; every nibble value
     n, k = 5, 64
@@ -79,10 +124,13 @@ def test_packed_sizes_and_padding():
     assert q4.packed_bytes(0, 0, 32) == 0 and q4.packed_bytes(0, 4, 33) == 0
     assert q4.packed_bytes(2, 14336, 4096) == q4.weight_bytes(2, 14336, 4096) == 14336 * 128 * 34
     assert q4.weight_bytes(2, 1, 32) == 34 and q4.packed_bytes(2, 1, 32) == 2176
-    assert q4.packed_bytes(3, 4, 32) == 0
+    assert q4.packed_bytes(3, 4, 32) == 0 and q4.packed_bytes(3, 4, 128) == 0   # Q4_K: whole superblocks
+    assert q4.packed_bytes(3, 14336, 4096) == 896 * 32 * 1216
+    assert q4.weight_bytes(3, 14336, 4096) == 14336 * 16 * 144
+    assert q4.packed_bytes(4, 4, 256) == 0
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3])
 @pytest.mark.parametrize("tiles,chunks,pairs", [(896, 32, False), (1024, 16, True), (128, 16, False),
                                                 (64, 16, False), (4096, 16, False), (1, 1, False),
                                                 (2, 1, True), (7, 3, False), (128, 64, False)])
@@ -196,6 +244,18 @@ def test_fused_validation():
     # group sums
     assert L.q4_group_sums(A, 1, 48, A, None) == 2
     assert L.q4_group_sums(None, 1, 64, A, None) == 1
+
+
+def test_q4_k_rejects_partial_superblocks():
+    L = q4.lib()
+    buf = np.zeros(1 << 16, np.uint8)
+    assert L.q4_repack_q4_k(buf.ctypes.data, 16, 128, buf.ctypes.data, buf.size) == 2
+    assert L.q4_repack_q4_k(None, 16, 256, buf.ctypes.data, buf.size) == 1
+    # a Q4_K weight view whose k is not whole superblocks fails before launch
+    W = _cw(3, 16, 128, nbytes=1 << 20)
+    assert L.q4_gemv(ctypes.byref(W), A, None, 1, A + 4096, None) == 2
+    with pytest.raises(ValueError):
+        q4.repack_q4_k(np.zeros((16, 1, 144), np.uint8), 16, 128)
 
 
 def test_repack_validation():

@@ -212,8 +212,8 @@ def _teacher_forced_step(q4, cfg, what):
     return step
 
 
-# (fmt, nb, layers, hidden, kv, inter, vocab): every batch class in both
-# formats, ragged shapes, and the 32-layer maximum
+# (fmt, nb, layers, hidden, kv, inter, vocab): every batch class, every
+# format, ragged shapes, and the 32-layer maximum
 STEP_CASES = [
     ("affine", 1, 3, 256, 64, 384, 1000),
     ("affine", 3, 2, 160, 48, 96, 333),
@@ -226,6 +226,9 @@ STEP_CASES = [
     ("q8_0", 1, 2, 256, 64, 384, 1000),
     ("q8_0", 4, 2, 160, 48, 224, 333),
     ("q8_0", 9, 2, 128, 32, 192, 300),
+    ("q4_k", 1, 2, 256, 64, 512, 1000),
+    ("q4_k", 3, 2, 256, 48, 256, 333),
+    ("q4_k", 9, 2, 256, 32, 256, 300),
     ("q4_0", 1, 32, 128, 32, 192, 300),
     ("affine", 2, 32, 128, 32, 192, 300),
 ]

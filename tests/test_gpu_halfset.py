@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import q4_workloads as wl
-from parity import case_seed, check, dev_weight, host_weight, to_np
+from parity import case_seed, check, dev_weight, fmt_k, host_weight, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -41,10 +41,11 @@ def test_pack_rounds_and_sums(q4, nb, k):
     assert torch.equal(gs, ref)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("nb", [1, 3, 5, 9, 16])
 @pytest.mark.parametrize("n,k", [(33, 160), (700, 1024), (64, 8192)])
 def test_gemv_half_parity(q4, fmt, nb, n, k):
+    k = fmt_k(fmt, k)
     rng = np.random.default_rng(case_seed("half", fmt, nb, n, k))
     H = _draw(fmt, rng, n, k)
     x16 = wl.draw_x(rng, nb, k).astype(np.float16)

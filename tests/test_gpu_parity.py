@@ -7,7 +7,8 @@ import pytest
 
 import oracle
 import q4_workloads as wl
-from parity import case_seed, check, check_argmax, check_residual, check_swiglu, dev_weight, host_weight, to_np
+from parity import (case_seed, check, check_argmax, check_residual, check_swiglu, dev_weight, fmt_k, host_weight,
+                    to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,10 +30,11 @@ def _draw(fmt, rng, n, k):
 SHAPES = [(1, 32), (7, 96), (33, 160), (100, 544), (512, 2048), (1000, 4096), (48, 8192)]
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("nb", [1, 2, 3, 4, 5, 8, 9, 16])
 @pytest.mark.parametrize("n,k", SHAPES)
 def test_gemv(q4, fmt, nb, n, k):
+    k = fmt_k(fmt, k)
     rng = np.random.default_rng(case_seed(fmt, nb, n, k))
     H = _draw(fmt, rng, n, k)
     x = wl.draw_x(rng, nb, k)
@@ -58,10 +60,11 @@ def test_affine_with_given_group_sums(q4, nb):
     check(to_np(y1), y_ref, S, what="affine given gsum")
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("nb", [1, 3, 16])
 @pytest.mark.parametrize("n,k", [(64, 64), (2048, 2048), (37, 4096), (130, 8192)])
 def test_nrm_gemv(q4, fmt, nb, n, k):
+    k = fmt_k(fmt, k)
     rng = np.random.default_rng(case_seed("nrm", fmt, nb, n, k))
     H = _draw(fmt, rng, n, k)
     x = wl.draw_x(rng, nb, k)
@@ -71,10 +74,11 @@ def test_nrm_gemv(q4, fmt, nb, n, k):
     check(to_np(y), y_ref, S, what="nrm %s nb=%d %dx%d" % (fmt, nb, n, k))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("norm", [True, False])
 @pytest.mark.parametrize("na,nbr,k,nb", [(512, 512, 2048, 1), (40, 17, 96, 2), (2048, 512, 2048, 4)])
 def test_dual(q4, fmt, norm, na, nbr, k, nb):
+    k = fmt_k(fmt, k)
     rng = np.random.default_rng(case_seed("dual", fmt, norm, na, nbr, k, nb))
     Ha, Hb = _draw(fmt, rng, na, k), _draw(fmt, rng, nbr, k)
     x = wl.draw_x(rng, nb, k)
@@ -86,9 +90,10 @@ def test_dual(q4, fmt, norm, na, nbr, k, nb):
     check(to_np(yb), rb, Sb, what="dual b")
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("n,k,nb", [(8192, 2048, 1), (40, 96, 3), (1000, 1024, 8), (256, 512, 16)])
 def test_gus_nrm(q4, fmt, n, k, nb):
+    k = fmt_k(fmt, k)
     rng = np.random.default_rng(case_seed("gus", fmt, n, k, nb))
     Hg, Hu = _draw(fmt, rng, n, k), _draw(fmt, rng, n, k)
     x = wl.draw_x(rng, nb, k)
@@ -99,10 +104,11 @@ def test_gus_nrm(q4, fmt, n, k, nb):
     check_swiglu(to_np(h), g, Sg, u, Su, what="gus %s %dx%d nb=%d" % (fmt, n, k, nb))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("n,k,nb", [(2048, 8192, 1), (2048, 2048, 1), (33, 160, 5), (700, 1024, 16)])
 @pytest.mark.parametrize("inplace", [False, True])
 def test_res_gemv(q4, fmt, n, k, nb, inplace):
+    k = fmt_k(fmt, k)
     rng = np.random.default_rng(case_seed("res", fmt, n, k, nb))
     H = _draw(fmt, rng, n, k)
     x = wl.draw_x(rng, nb, k)
@@ -116,9 +122,10 @@ def test_res_gemv(q4, fmt, n, k, nb, inplace):
     check_residual(to_np(y), y_ref, S, what="res %s" % fmt)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("n,k,nb,norm", [(65536, 2048, 1, True), (1000, 256, 3, False), (77, 96, 16, True)])
 def test_argmax(q4, fmt, n, k, nb, norm):
+    k = fmt_k(fmt, k)
     rng = np.random.default_rng(case_seed("am", fmt, n, k, nb))
     H = _draw(fmt, rng, n, k)
     x = wl.draw_x(rng, nb, k)
@@ -148,7 +155,7 @@ def test_argmax_planted_and_ties(q4):
     assert val.cpu().tolist() == [7.0 * 64, 0.0]
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 def test_zero_weights_exact(q4, fmt):
     rng = np.random.default_rng(41)
     n, k = 200, 1024
@@ -158,6 +165,11 @@ def test_zero_weights_exact(q4, fmt):
     elif fmt == "q8_0":
         d = rng.uniform(0.0003, 0.0012, (n, k // 32)).astype(np.float16).view(np.uint16)
         H = wl.Q8_0Host(n, k, wl.pack_q8_0(np.zeros((n, k), np.int16), d))
+    elif fmt == "q4_k":
+        # nonzero nibbles, d and dmin; every sub-block scale and min zero
+        d = rng.uniform(1e-4, 4e-4, (n, k // 256)).astype(np.float16).view(np.uint16)
+        z = np.zeros((n, k // 32), int)
+        H = wl.Q4_KHost(n, k, wl.pack_q4_k(rng.integers(1, 16, (n, k), dtype=np.uint8), z, z, d, d))
     else:
         z = np.zeros((n, k // 32), np.uint16)
         H = wl.AffineHost(n, k, rng.integers(0, 256, (n, k // 2), dtype=np.uint8), z, z)
@@ -191,9 +203,18 @@ def test_power_of_two_scaling_bitwise(q4):
     b8[:, :, 1] = (dd >> 8).astype(np.uint8)
     z1 = q4.q4_gemv(dev_weight(H8), x)
     assert torch.equal(q4.q4_gemv(dev_weight(wl.Q8_0Host(n, k, b8)), x), 2.0 * z1)
+    # Q4_K: d -> 2d and dmin -> 2 dmin together
+    HK = wl.draw_q4_k(rng, n, k)
+    bk = HK.blocks_k.copy()
+    for o in (0, 2):
+        dd = (bk[:, :, o].astype(np.uint16) | (bk[:, :, o + 1].astype(np.uint16) << 8)) + 0x0400
+        bk[:, :, o] = (dd & 0xFF).astype(np.uint8)
+        bk[:, :, o + 1] = (dd >> 8).astype(np.uint8)
+    k1 = q4.q4_gemv(dev_weight(HK), x)
+    assert torch.equal(q4.q4_gemv(dev_weight(wl.Q4_KHost(n, k, bk)), x), 2.0 * k1)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q4_k"])
 def test_one_hot_columns(q4, fmt):
     rng = np.random.default_rng(43)
     n, k = 96, 256
@@ -238,7 +259,7 @@ def test_nrm_constant_vector(q4):
 
 
 @pytest.mark.parametrize("nb", [3, 5, 9])
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 def test_large_dynamic_range(q4, fmt, nb):
     # activations far outside f16 range in both directions, and 32-column
     # blocks of very different magnitude inside one row, stay within

@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 import q4_workloads as wl
-from parity import case_seed, check, check_argmax, check_residual, check_swiglu, dev_weight, host_weight, to_np
+from parity import (FMT_ID, case_seed, check, check_argmax, check_residual, check_swiglu, dev_weight, host_weight,
+                    to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +34,7 @@ def _sms():
 
 def _shape(q4, fmt, nb, S, pairs=False):
     """The smallest candidate (n, k) whose plan splits K over S ranks."""
-    f = 0 if fmt == "q4_0" else 1
+    f = FMT_ID[fmt]
     for n, k in sorted(CANDIDATES, key=lambda s: s[0] * s[1]):
         tiles = 2 * ((n + 15) // 16) if pairs else (n + 15) // 16
         if q4.plan(f, tiles, (k + 127) // 128, nb, pairs, _sms())["S"] == S:
@@ -45,7 +46,7 @@ def _draw(fmt, rng, n, k):
     return wl._draw_fmt(fmt)(rng, n, k)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("nb", [1, 4, 16])
 @pytest.mark.parametrize("S", [2, 4, 8])
 def test_split_store_and_norm(q4, fmt, nb, S):
@@ -66,7 +67,7 @@ def test_split_store_and_norm(q4, fmt, nb, S):
     check(to_np(y), y_ref, Sr, what="split nrm %s nb=%d S=%d %dx%d" % (fmt, nb, S, n, k))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("nb", [1, 16])
 @pytest.mark.parametrize("S", [2, 8])
 def test_split_residual(q4, fmt, nb, S):
@@ -80,7 +81,7 @@ def test_split_residual(q4, fmt, nb, S):
     check_residual(to_np(y), y_ref, Sr, what="split res %s nb=%d S=%d" % (fmt, nb, S))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("nb", [1, 8])
 @pytest.mark.parametrize("S", [2, 4, 8])
 def test_split_swiglu(q4, fmt, nb, S):
@@ -95,7 +96,7 @@ def test_split_swiglu(q4, fmt, nb, S):
     check_swiglu(to_np(h), g, Sg, u, Su, what="split gus %s nb=%d S=%d %dx%d" % (fmt, nb, S, n, k))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
 @pytest.mark.parametrize("nb", [1, 3])
 @pytest.mark.parametrize("S", [2, 8])
 def test_split_argmax(q4, fmt, nb, S):
