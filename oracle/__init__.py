@@ -19,6 +19,10 @@ bytes before any device repack) and computes in IEEE double precision:
   bytes (runs of 32 holding sub-blocks 2r / 2r+1 in the low / high nibbles);
   ``w = d*sc*q - dmin*mn`` (crate inferencelayer, Functions:
   gemv_q5k_k_lcpp_src; honeycrisp/mod.rs, quant_matmul's Q4_K branch).
+* ``q1``: superblocks ``uint8[n, k/128, 18]`` -- fp16 ``d`` then 16 bytes of
+  sign bits, byte ``i`` holding elements ``8i..8i+7`` from its lowest bit;
+  ``w = +d`` for a set bit, ``-d`` for a clear one (crate inferencelayer,
+  Functions: gemv_q1_k_lcpp_src, gemm_q1_src).
 * ``affine``: nibbles ``uint8[n, k/2]`` (element ``2i`` low nibble of byte
   ``i``, ``2i+1`` high nibble), ``s`` and ``m`` as bf16 bits
   ``uint16[n, k/32]``; ``w = s*q + m`` (Module gpu, Structs Q and HalfSet).
@@ -50,6 +54,7 @@ FMT_Q4_0 = 0
 FMT_AFFINE = 1
 FMT_Q8_0 = 2
 FMT_Q4_K = 3
+FMT_Q1 = 4
 
 
 def build(force: bool = False) -> str:
@@ -94,6 +99,7 @@ def lib() -> ctypes.CDLL:
         L.q4o_q4_0_row.argtypes = [P, I64, I64, P]
         L.q4o_q8_0_row.argtypes = [P, I64, I64, P]
         L.q4o_q4_k_row.argtypes = [P, I64, I64, P]
+        L.q4o_q1_row.argtypes = [P, I64, I64, P]
         L.q4o_q4_k_scale_min.argtypes = [P, ctypes.c_int, P, P]
         L.q4o_affine_row.argtypes = [P, P, P, I64, I64, P]
         L.q4o_gemv.argtypes = [ctypes.c_int, P, P, P, I64, I64, P, I64, P, P, P]
@@ -137,6 +143,8 @@ class HostWeight:
             assert self.a.size == self.n * (self.k // 32) * 34
         elif self.fmt == FMT_Q4_K:
             assert self.k % 256 == 0 and self.a.size == self.n * (self.k // 256) * 144
+        elif self.fmt == FMT_Q1:
+            assert self.k % 128 == 0 and self.a.size == self.n * (self.k // 128) * 18
         else:
             assert self.a.size == self.n * self.k // 2
             self.s = np.ascontiguousarray(self.s, dtype=np.uint16)
@@ -154,6 +162,10 @@ class HostWeight:
     @staticmethod
     def q4_k(blocks: np.ndarray, n: int, k: int) -> "HostWeight":
         return HostWeight(FMT_Q4_K, n, k, blocks)
+
+    @staticmethod
+    def q1(blocks: np.ndarray, n: int, k: int) -> "HostWeight":
+        return HostWeight(FMT_Q1, n, k, blocks)
 
     @staticmethod
     def affine(nib: np.ndarray, s: np.ndarray, m: np.ndarray, n: int, k: int) -> "HostWeight":
@@ -181,6 +193,8 @@ def dequant_row(W: HostWeight, row: int) -> np.ndarray:
         lib().q4o_q8_0_row(_p(W.a), W.k, row, _p(out))
     elif W.fmt == FMT_Q4_K:
         lib().q4o_q4_k_row(_p(W.a), W.k, row, _p(out))
+    elif W.fmt == FMT_Q1:
+        lib().q4o_q1_row(_p(W.a), W.k, row, _p(out))
     else:
         lib().q4o_affine_row(_p(W.a), _p(W.s), _p(W.m), W.k, row, _p(out))
     return out
@@ -367,6 +381,8 @@ def _hw(H) -> HostWeight:
         return HostWeight.q8_0(H.blocks8, H.n, H.k)
     if hasattr(H, "blocks_k"):
         return HostWeight.q4_k(H.blocks_k, H.n, H.k)
+    if hasattr(H, "blocks1"):
+        return HostWeight.q1(H.blocks1, H.n, H.k)
     if hasattr(H, "blocks"):
         return HostWeight.q4_0(H.blocks, H.n, H.k)
     return HostWeight.affine(H.nib, H.s, H.m, H.n, H.k)

@@ -1,7 +1,7 @@
 /*
  * q4_oracle.c -- plain, slow, obviously correct CPU oracle for the weight-only
- * dequant-in-GEMV family (Q4_0 blocks, affine-Q4 groups, Q8_0 blocks and Q4_K
- * superblocks) and its fused
+ * dequant-in-GEMV family (Q4_0 blocks, affine-Q4 groups, Q8_0 blocks, Q4_K
+ * superblocks and Q1 sign-bit superblocks) and its fused
  * neighbours (RMSNorm, SwiGLU, residual add, greedy argmax).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
@@ -39,6 +39,14 @@
  *    in the top two bits of bytes 0-3 (sc) and 4-7 (mn).  The 128 nibble bytes
  *    are four runs of 32: run r holds sub-block 2r in its low nibbles and
  *    sub-block 2r+1 in its high nibbles, in element order.
+ *  - Q1 superblock (128 binary weights in 18 bytes: fp16 scale d, then 16
+ *    bytes of sign bits; weight = +d for a set bit, -d for a clear one):
+ *    crate inferencelayer, Functions, entries gemv_q1_k_lcpp_src (bit i of a
+ *    weight word is element i's sign, 1 -> +1 and 0 -> -1; one f16 scale per
+ *    128 weights; 4.5 bytes per 32 weights) and gemm_q1_src (the sign bits
+ *    and one f16 scale per 128-weight superblock).  Reading: the scale comes
+ *    first, as in Q4_0's block, and the bits follow as little-endian words,
+ *    so byte i holds elements 8i..8i+7 from its lowest bit up.
  *  - Affine-Q4 group (32 weights, bf16 scale s and bf16 min m, weight =
  *    s*q + m): Module gpu (qwen4_exp), Structs Q (affine-Q4 projection with
  *    byte offsets into a bf16 weight buffer) and HalfSet (even/odd streams plus
@@ -160,6 +168,23 @@ void q4o_q4_k_row(const uint8_t *blocks, int64_t k, int64_t row, double *w)
     }
 }
 
+/* One row of Q1 weights, dequantised to f64: superblocks of 18 bytes, the
+ * fp16 scale d (little endian) then 16 bytes of sign bits; weight = d for a
+ * set bit, -d for a clear one.  blocks: [n][k/128][18] bytes; w: [k]. */
+void q4o_q1_row(const uint8_t *blocks, int64_t k, int64_t row, double *w)
+{
+    int64_t nsb = k / 128;
+    const uint8_t *r = blocks + row * nsb * 18;
+    for (int64_t b = 0; b < nsb; ++b) {
+        const uint8_t *blk = r + b * 18;
+        double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));
+        for (int e = 0; e < 128; ++e) {
+            int bit = (blk[2 + e / 8] >> (e % 8)) & 1;
+            w[b * 128 + e] = bit ? d : -d;
+        }
+    }
+}
+
 /* One row of affine-Q4 weights, dequantised to f64.
  * nib: [n][k/2] bytes; s, m: [n][k/32] bf16 bits; w: [k]. */
 void q4o_affine_row(const uint8_t *nib, const uint16_t *s, const uint16_t *m,
@@ -182,7 +207,7 @@ void q4o_affine_row(const uint8_t *nib, const uint16_t *s, const uint16_t *m,
  * for the output rows i in [row0, row1) (rows are independent; callers may
  * run disjoint ranges at the same time, each with its own scratch).
  * fmt 0: a = Q4_0 blocks.  fmt 1: a = nibbles, b = s, c = m.  fmt 2: a = Q8_0 blocks.
- * fmt 3: a = Q4_K superblocks.
+ * fmt 3: a = Q4_K superblocks.  fmt 4: a = Q1 superblocks.
  * x: [nb][k] f64; y, bound: [nb][n]; wrow: scratch of k doubles. */
 void q4o_gemv_rows(int fmt, const void *a, const void *b, const void *c,
                    int64_t n, int64_t k, const double *x, int64_t nb,
@@ -195,6 +220,8 @@ void q4o_gemv_rows(int fmt, const void *a, const void *b, const void *c,
             q4o_q8_0_row((const uint8_t *)a, k, i, wrow);
         else if (fmt == 3)
             q4o_q4_k_row((const uint8_t *)a, k, i, wrow);
+        else if (fmt == 4)
+            q4o_q1_row((const uint8_t *)a, k, i, wrow);
         else
             q4o_affine_row((const uint8_t *)a, (const uint16_t *)b,
                            (const uint16_t *)c, k, i, wrow);

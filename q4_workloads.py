@@ -17,6 +17,9 @@ Host storage formats (the readings of the pages, stated once):
   4..15 = the eight sub-blocks' 6-bit scales and mins (GGUF pack, see
   ``Q4K_SCALE_BITS``), 16..143 = four runs of 32 nibble bytes, run ``r``
   holding sub-block ``2r`` in its low nibbles and ``2r + 1`` in its high ones.
+* Q1: ``uint8[n, k/128, 18]``; bytes 0-1 = fp16 scale ``d``; bytes 2..17 =
+  the sign bits, byte ``i`` holding elements ``8i..8i+7`` from its lowest
+  bit (1 for ``+d``, 0 for ``-d``).
 * affine-Q4: nibbles ``uint8[n, k/2]`` with byte ``i`` holding element ``2i``
   (low nibble) and ``2i + 1`` (high nibble); ``s`` and ``m`` as bf16 bit
   patterns ``uint16[n, k/32]``.
@@ -120,6 +123,20 @@ def pack_q4_k(q: np.ndarray, sc: np.ndarray, mn: np.ndarray, d_bits: np.ndarray,
     return out
 
 
+def pack_q1(bits: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
+    """Pack sign bits ``bits[n, k]`` (1 for +d, 0 for -d) and fp16 scale bits
+    ``d_bits[n, k/128]`` into Q1 host superblocks ``uint8[n, k/128, 18]``."""
+    n, k = bits.shape
+    assert k % 128 == 0
+    ns = k // 128
+    out = np.empty((n, ns, 18), dtype=np.uint8)
+    d = np.ascontiguousarray(d_bits, dtype=np.uint16).reshape(n, ns)
+    out[:, :, 0] = (d & 0xFF).astype(np.uint8)
+    out[:, :, 1] = (d >> 8).astype(np.uint8)
+    out[:, :, 2:] = np.packbits(bits.astype(np.uint8).reshape(n, ns, 128), axis=2, bitorder="little")
+    return out
+
+
 def pack_affine_nibbles(q: np.ndarray) -> np.ndarray:
     """Pack nibbles ``q[n, k]`` into ``uint8[n, k/2]`` (even element low)."""
     q = q.astype(np.uint8)
@@ -145,6 +162,13 @@ class Q4_KHost:
     n: int
     k: int
     blocks_k: np.ndarray        # uint8[n, k/256, 144]
+
+
+@dataclass
+class Q1Host:
+    n: int
+    k: int
+    blocks1: np.ndarray         # uint8[n, k/128, 18]
 
 
 @dataclass
@@ -195,6 +219,15 @@ def draw_q4_k(rng: np.random.Generator, n: int, k: int, d_range=(0.0001, 0.0004)
     d = rng.uniform(d_range[0], d_range[1], size=(n, k // 256)).astype(np.float16)
     dm = rng.uniform(dmin_range[0], dmin_range[1], size=(n, k // 256)).astype(np.float16)
     return Q4_KHost(n, k, pack_q4_k(q, sc, mn, d.view(np.uint16), dm.view(np.uint16)))
+
+
+def draw_q1(rng: np.random.Generator, n: int, k: int, d_range=(0.02, 0.06)) -> Q1Host:
+    """Signs ~ U{0, 1}, d ~ U[d_range] rounded to fp16 (weights of the Q4_0
+    draws' magnitude)."""
+    assert k % 128 == 0
+    bits = rng.integers(0, 2, size=(n, k), dtype=np.uint8)
+    d = rng.uniform(d_range[0], d_range[1], size=(n, k // 128)).astype(np.float16)
+    return Q1Host(n, k, pack_q1(bits, d.view(np.uint16)))
 
 
 def draw_affine(rng: np.random.Generator, n: int, k: int,
@@ -331,7 +364,9 @@ def _draw_fmt(fmt: str):
         return draw_q8_0
     if fmt == "q4_k":
         return draw_q4_k
-    raise ValueError("fmt must be 'q4_0', 'affine', 'q8_0' or 'q4_k'")
+    if fmt == "q1":
+        return draw_q1
+    raise ValueError("fmt must be 'q4_0', 'affine', 'q8_0', 'q4_k' or 'q1'")
 
 
 def cfg4_layer(seed: int, layer: int, hidden: int = 2048, kv: int = 512,

@@ -51,6 +51,13 @@ MUTANTS = [
     ("q4_k high min nibble", "*mn = (sb[j + 4] >> 4) | ((sb[j] >> 6) << 4);",
      "*mn = (sb[j + 4] & 0x0f) | ((sb[j] >> 6) << 4);"),
     ("q4_k low mins from the scale bytes", "*mn = sb[j + 4] & 63;", "*mn = sb[j] & 63;"),
+    ("q1 sign convention", "w[b * 128 + e] = bit ? d : -d;", "w[b * 128 + e] = bit ? -d : d;"),
+    ("q1 bits most significant first", "int bit = (blk[2 + e / 8] >> (e % 8)) & 1;",
+     "int bit = (blk[2 + e / 8] >> (7 - e % 8)) & 1;"),
+    ("q1 bits start at the scale", "int bit = (blk[2 + e / 8] >> (e % 8)) & 1;",
+     "int bit = (blk[e / 8] >> (e % 8)) & 1;"),
+    ("q1 superblock stride", "const uint8_t *blk = r + b * 18;\n        double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));\n        for (int e = 0; e < 128",
+     "const uint8_t *blk = r + b * 16;\n        double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));\n        for (int e = 0; e < 128"),
     ("halfset streams swapped", "x[r * k + 2 * i] = q4o_half(xe[r * (k / 2) + i]);",
      "x[r * k + 2 * i] = q4o_half(xo[r * (k / 2) + i]);"),
     ("halfset rows concatenated", "x[r * k + 2 * i + 1] = q4o_half(xo[r * (k / 2) + i]);",

@@ -586,3 +586,63 @@ def test_q4_k_brute_force_fsum():
             terms = dense[i] * x[r].astype(np.float64)
             assert abs(y[r, i] - math.fsum(terms)) <= 1e-12 * math.fsum(np.abs(terms))
             assert abs(S[r, i] - math.fsum(np.abs(terms))) <= 1e-12 * S[r, i]
+
+
+# ---- Q1 sign-bit superblocks (crate inferencelayer, gemv_q1_k_lcpp_src:
+# bit i of a weight word is element i's sign, 1 -> +1, 0 -> -1; one f16 scale
+# per 128 weights; 4.5 bytes per 32 weights)
+
+def test_q1_every_byte_value():
+    # every value of every sign byte, against numpy's own little-endian bit
+    # reading and float16 decode
+    rng = np.random.default_rng(120)
+    n, k = 16, 2048
+    blocks = np.empty((n, k // 128, 18), np.uint8)
+    blocks[:, :, 2:] = np.arange(256, dtype=np.uint8).reshape(1, 16, 16).repeat(n, 0)
+    d = rng.uniform(0.02, 0.06, (n, k // 128)).astype(np.float16)
+    blocks[:, :, 0:2] = d.view(np.uint8).reshape(n, k // 128, 2)
+    H = wl.Q1Host(n, k, blocks)
+    bits = np.unpackbits(blocks[:, :, 2:], axis=2, bitorder="little").astype(np.float64)
+    ref = (2.0 * bits - 1.0) * d.astype(np.float64)[:, :, None]
+    assert np.array_equal(oracle.dequant(oracle._hw(H)), ref.reshape(n, k))
+    # 16 bytes per superblock of 128, two of scale: 4.5 bytes per 32 weights
+    assert blocks.size / (n * k / 32) == 4.5
+
+
+def test_q1_sign_convention_and_positions():
+    # all bits set is +d, none is -d; a single set bit lands on its element
+    n, k = 130, 128
+    bits = np.zeros((n, k), np.uint8)
+    bits[0] = 1
+    for e in range(k):
+        bits[2 + e, e] = 1
+    d = np.full((n, 1), np.float16(0.5)).view(np.uint16)
+    W = oracle.dequant(oracle._hw(wl.Q1Host(n, k, wl.pack_q1(bits, d))))
+    assert np.all(W[0] == 0.5) and np.all(W[1] == -0.5)
+    assert np.array_equal(W[2:], np.where(np.eye(k, dtype=bool), 0.5, -0.5))
+
+
+def test_q1_equals_q8_0_of_signs():
+    # a Q1 superblock is the four Q8_0 blocks with the same d and q = +-1
+    rng = np.random.default_rng(121)
+    n, k = 21, 512
+    bits = rng.integers(0, 2, (n, k), dtype=np.uint8)
+    d = rng.uniform(0.02, 0.06, (n, k // 128)).astype(np.float16)
+    H1 = wl.Q1Host(n, k, wl.pack_q1(bits, d.view(np.uint16)))
+    H8 = wl.Q8_0Host(n, k, wl.pack_q8_0(2 * bits.astype(np.int16) - 1, np.repeat(d, 4, axis=1).view(np.uint16)))
+    assert np.array_equal(oracle.dequant(oracle._hw(H1)), oracle.dequant(oracle._hw(H8)))
+
+
+def test_q1_brute_force_fsum():
+    rng = np.random.default_rng(122)
+    H = wl.draw_q1(rng, 11, 384)
+    x = wl.draw_x(rng, 3, 384)
+    y, S = oracle.q4_gemv(oracle._hw(H), x)
+    b = H.blocks1
+    signs = 2.0 * np.unpackbits(b[:, :, 2:], axis=2, bitorder="little").astype(np.float64) - 1.0
+    dense = (signs * b[:, :, 0:2].copy().view("<f2").astype(np.float64)).reshape(11, 384)
+    for r in range(3):
+        for i in range(11):
+            terms = dense[i] * x[r].astype(np.float64)
+            assert abs(y[r, i] - math.fsum(terms)) <= 1e-12 * math.fsum(np.abs(terms))
+            assert abs(S[r, i] - math.fsum(np.abs(terms))) <= 1e-12 * S[r, i]
