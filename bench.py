@@ -399,11 +399,12 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
             best = t if best is None else min(best, t)
         return best / n_calls
 
-    for fmt in ("affine", "q4_0", "q8_0", "q4_k"):
+    for fmt in ("affine", "q4_0", "q8_0", "q4_k", "q1"):
         H = wl._draw_fmt(fmt)(rng, n, k)
         W0 = (q4.Q4Weight.from_affine(H.nib, H.s, H.m, n, k, device) if fmt == "affine"
               else q4.Q4Weight.from_q8_0(H.blocks8, n, k, device) if fmt == "q8_0"
               else q4.Q4Weight.from_q4_k(H.blocks_k, n, k, device) if fmt == "q4_k"
+              else q4.Q4Weight.from_q1(H.blocks1, n, k, device) if fmt == "q1"
               else q4.Q4Weight.from_q4_0(H.blocks, n, k, device))
         copies = max(2, -(-3 * l2_bytes // W0.nbytes))
         host = W0.tensor.cpu().numpy()

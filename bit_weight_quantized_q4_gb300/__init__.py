@@ -29,6 +29,7 @@ Q4_FMT_Q4_0 = 0
 Q4_FMT_AFFINE = 1
 Q4_FMT_Q8_0 = 2
 Q4_FMT_Q4_K = 3
+Q4_FMT_Q1 = 4
 MAX_NB = 16
 
 STATUS = {0: "Q4_OK", 1: "Q4_ERR_NULL", 2: "Q4_ERR_SHAPE", 3: "Q4_ERR_ALIGN",
@@ -80,6 +81,8 @@ def lib() -> ctypes.CDLL:
             "q4_unpack_q8_0": (I32, [P, SZ, I32, I32, P]),
             "q4_repack_q4_k": (I32, [P, I32, I32, P, SZ]),
             "q4_unpack_q4_k": (I32, [P, SZ, I32, I32, P]),
+            "q4_repack_q1": (I32, [P, I32, I32, P, SZ]),
+            "q4_unpack_q1": (I32, [P, SZ, I32, I32, P]),
             "q4_unpack_q4_0": (I32, [P, SZ, I32, I32, P]),
             "q4_unpack_affine": (I32, [P, SZ, I32, I32, P, P, P]),
             "q4_group_sums": (I32, [P, I32, I32, P, P]),
@@ -181,6 +184,25 @@ def unpack_q4_k(packed: np.ndarray, n: int, k: int) -> np.ndarray:
     return out
 
 
+def repack_q1(blocks: np.ndarray, n: int, k: int) -> np.ndarray:
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    if k % 128 != 0 or blocks.size != n * (k // 128) * 18:
+        raise ValueError("Q1 superblocks must be uint8[n, k/128, 18] with k a multiple of 128")
+    nbytes = packed_bytes(Q4_FMT_Q1, n, k)
+    if nbytes == 0:
+        raise ValueError("bad shape n=%d k=%d" % (n, k))
+    out = np.empty(nbytes, dtype=np.uint8)
+    _check(lib().q4_repack_q1(blocks.ctypes.data, n, k, out.ctypes.data, nbytes), "q4_repack_q1")
+    return out
+
+
+def unpack_q1(packed: np.ndarray, n: int, k: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    out = np.zeros((n, k // 128, 18), dtype=np.uint8)
+    _check(lib().q4_unpack_q1(packed.ctypes.data, packed.size, n, k, out.ctypes.data), "q4_unpack_q1")
+    return out
+
+
 def repack_affine(nib: np.ndarray, s: np.ndarray, m: np.ndarray, n: int, k: int) -> np.ndarray:
     nib = np.ascontiguousarray(nib, dtype=np.uint8)
     s = np.ascontiguousarray(s, dtype=np.uint16)
@@ -249,13 +271,17 @@ class Q4Weight:
         return cls(Q4_FMT_Q4_K, n, k, repack_q4_k(blocks, n, k), device)
 
     @classmethod
+    def from_q1(cls, blocks: np.ndarray, n: int, k: int, device="cuda") -> "Q4Weight":
+        return cls(Q4_FMT_Q1, n, k, repack_q1(blocks, n, k), device)
+
+    @classmethod
     def from_affine(cls, nib, s, m, n: int, k: int, device="cuda") -> "Q4Weight":
         return cls(Q4_FMT_AFFINE, n, k, repack_affine(nib, s, m, n, k), device)
 
     @property
     def weight_bytes(self) -> int:
         """Algorithmic bytes: 18 (Q4_0), 20 (affine) or 34 (Q8_0) per 32
-        weights, 144 per 256 (Q4_K)."""
+        weights, 144 per 256 (Q4_K), 18 per 128 (Q1)."""
         return weight_bytes(self.fmt, self.n, self.k)
 
     def cref(self):

@@ -26,7 +26,7 @@ bool shape_ok(int32_t n, int32_t k) {
 }
 
 inline bool fmt_known(int32_t fmt) {
-    return fmt == Q4_FMT_Q4_0 || fmt == Q4_FMT_AFFINE || fmt == Q4_FMT_Q8_0 || fmt == Q4_FMT_Q4_K;
+    return fmt == Q4_FMT_Q4_0 || fmt == Q4_FMT_AFFINE || fmt == Q4_FMT_Q8_0 || fmt == Q4_FMT_Q4_K || fmt == Q4_FMT_Q1;
 }
 
 q4_status check_weight(const q4_weight *W) {
@@ -146,7 +146,8 @@ q4_status launch_planned(const q4::GemvParams &p, int fmt, const q4::Plan &plan,
     int rc = fmt == Q4_FMT_Q4_0     ? q4::launch_gemv_q4_0(pp, plan, stream)
              : fmt == Q4_FMT_AFFINE ? q4::launch_gemv_affine(pp, plan, stream)
              : fmt == Q4_FMT_Q8_0   ? q4::launch_gemv_q8_0(pp, plan, stream)
-                                    : q4::launch_gemv_q4_k(pp, plan, stream);
+             : fmt == Q4_FMT_Q4_K   ? q4::launch_gemv_q4_k(pp, plan, stream)
+                                    : q4::launch_gemv_q1(pp, plan, stream);
     if (rc != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
     return Q4_OK;
 }
@@ -604,14 +605,16 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     const int occ = fmt == Q4_FMT_Q4_0     ? q4::step_occupancy_q4_0(nb, smem)
                     : fmt == Q4_FMT_AFFINE ? q4::step_occupancy_affine(nb, smem)
                     : fmt == Q4_FMT_Q8_0   ? q4::step_occupancy_q8_0(nb, smem)
-                                           : q4::step_occupancy_q4_k(nb, smem);
+                    : fmt == Q4_FMT_Q4_K   ? q4::step_occupancy_q4_k(nb, smem)
+                                           : q4::step_occupancy_q1(nb, smem);
     if (occ < 1) return Q4_ERR_UNSUPPORTED;
     cudaGetLastError();
     if (cudaMemsetAsync(workspace, 0, 16, stream) != cudaSuccess) return Q4_ERR_CUDA;
     const int rc = fmt == Q4_FMT_Q4_0     ? q4::launch_step_q4_0(sp, G, smem, stream)
                    : fmt == Q4_FMT_AFFINE ? q4::launch_step_affine(sp, G, smem, stream)
                    : fmt == Q4_FMT_Q8_0   ? q4::launch_step_q8_0(sp, G, smem, stream)
-                                          : q4::launch_step_q4_k(sp, G, smem, stream);
+                   : fmt == Q4_FMT_Q4_K   ? q4::launch_step_q4_k(sp, G, smem, stream)
+                                          : q4::launch_step_q1(sp, G, smem, stream);
     if (rc != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
     return Q4_OK;
 }

@@ -173,6 +173,12 @@ __device__ __forceinline__ void unpack_q8(uint32_t lo, uint32_t hi, uint32_t &r0
     r3 = bytes_to_half2<0x4342>(hi);
 }
 
+// Q1: the tensor-core A register rho of a lane's sign word -- bits rho and
+// 16 + rho (stored inverted) become the f16 sign bits of +1.0 halves.
+__device__ __forceinline__ uint32_t q1_signs(uint32_t w, int rho) {
+    return ((w << (15 - rho)) & 0x80008000u) | 0x3C003C00u;  // one shift, one lop3 (rho is unrolled)
+}
+
 // The two 16-bit scales (or mins) of a scale word as fp32.
 template <int FMT>
 __device__ __forceinline__ float2 scale_pair(uint32_t w) {
@@ -529,10 +535,11 @@ __device__ __forceinline__ Smem carve(uint8_t *smem, int nb, int Cs, int TG, int
 // the exponent field of `bound` (e clamped to [-100, 100]; 0 for a zero or
 // non-finite bound), and the factor back 2^(U-e), which also undoes the 2^-U
 // unit of the products: U = 20 for the nibble formats (their lower nibbles
-// meet activations times 16), 24 for Q8_0 (bytes are f16 subnormals u * 2^-24).
+// meet activations times 16), 24 for Q8_0 (bytes are f16 subnormals u * 2^-24),
+// 0 for Q1 (signs are f16 +-1).
 template <int FMT>
 __device__ __forceinline__ void block_scale(float bound, float &scale, float &back) {
-    constexpr int U = FMT == 2 ? 24 : 20;
+    constexpr int U = FMT == 2 ? 24 : FMT == 4 ? 0 : 20;
     int e = 0;
     if (bound > 0.f && bound <= 3.0e38f) {
         const int be = (int)((__float_as_uint(bound) >> 23) & 0xFF);  // bound in [2^(be-127), 2^(be-126))
@@ -561,7 +568,7 @@ __device__ __forceinline__ int xs_off(int b, int r, int kk, int part, int xbs) {
 template <int FMT, int CLS>
 __device__ __forceinline__ void put_pair(uint8_t *xs, int xbs, int r, int kl, float v0, float v1) {
     const int b = kl >> 5, kk = kl & 31;
-    if (FMT != 2 && (kk & 8) == 0) {
+    if (is_nibble(FMT) && (kk & 8) == 0) {
         v0 *= 16.f;
         v1 *= 16.f;
     }
@@ -767,7 +774,7 @@ __device__ void stage_row1(const GemvParams &p, const Geo &q, const Smem &m, int
             m.fs[gs_idx(kl >> 5, 0, GSW)] = back;
             if (has_min(FMT) && !given) m.gs[gs_idx(kl >> 5, 0, GSW)] = bsum;
         }
-        if (!has_min(FMT) && (qq & 1)) {  // the chunk is written: its eights (zero-weight) product
+        if (has_offset(FMT) && (qq & 1)) {  // the chunk is written: its eights (zero-weight) product
             __syncwarp();
             eights_chunk<FMT, CLS>(m, c, lane);
         }
@@ -817,7 +824,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
     float ss = 0.f;
     int rcur = r0;
 
-    const float f16x = FMT == 2 || (lane & 2) ? 1.f : 16.f;  // the lower nibbles' factor 16
+    const float f16x = !is_nibble(FMT) || (lane & 2) ? 1.f : 16.f;  // the lower nibbles' factor 16
     constexpr int LO = 64, P2 = 16;  // lo part (nb <= 4), second column pair
     const int lane_off = (lane >> 3) * xbs + (lane & 1) * 32 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4;
     // a batch's loads are predicated, not branched around, so that they are
@@ -944,7 +951,7 @@ __device__ void stage_x(const GemvParams &p, const Geo &q, const Smem &m, int S,
         }
     }
     stage_finish<CLS>(p, m, S, nb, tid);
-    if (CLS == 0 && !has_min(FMT)) eights_c0<FMT, CLS>(m, Cs, warp, lane);
+    if (CLS == 0 && has_offset(FMT)) eights_c0<FMT, CLS>(m, Cs, warp, lane);
 }
 
 template <int I>
@@ -994,8 +1001,12 @@ __device__ __forceinline__ void load_chunk(ChunkX &x, const Smem &m, int cc, int
 // block J: rows g (even) and g+8 (odd), k positions in unpack_word's order.
 template <int FMT>
 struct RecWords {
-    uint4 w[FMT == 2 ? 4 : 2];
+    uint4 w[FMT == 2 ? 4 : FMT == 4 ? 1 : 2];  // Q1: w[0].x, .y = the sign words of rows g, g + 8
     __device__ __forceinline__ void load(uint32_t ra, int lane) {
+        if constexpr (FMT == 4) {
+            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(w[0].x), "=r"(w[0].y) : "r"(ra + lane * 8) : "memory");
+            return;
+        }
         w[0] = lds128_at<0>(ra + lane * 16);
         w[1] = lds128_at<FMT == 2 ? 1024 : 512>(ra + lane * 16);
         if constexpr (FMT == 2) {
@@ -1005,7 +1016,13 @@ struct RecWords {
     }
     template <int J>
     __device__ __forceinline__ void regs(uint32_t (&a)[8]) const {
-        if constexpr (FMT == 2) {
+        if constexpr (FMT == 4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a[2 * i] = q1_signs(w[0].x, 4 * J + i);
+                a[2 * i + 1] = q1_signs(w[0].y, 4 * J + i);
+            }
+        } else if constexpr (FMT == 2) {
             const uint4 &r0 = w[J < 2 ? 0 : 2], &r1 = w[J < 2 ? 1 : 3];
             unpack_q8((J & 1) ? r0.z : r0.x, (J & 1) ? r0.w : r0.y, a[0], a[2], a[4], a[6]);
             unpack_q8((J & 1) ? r1.z : r1.x, (J & 1) ? r1.w : r1.y, a[1], a[3], a[5], a[7]);
@@ -1017,7 +1034,7 @@ struct RecWords {
 };
 // Byte offset of the scale words in a record, and of the mins (affine).
 template <int FMT>
-__device__ __forceinline__ constexpr int scale_off() { return FMT == 2 ? 2048 : 1024; }
+__device__ __forceinline__ constexpr int scale_off() { return FMT == 2 ? 2048 : FMT == 4 ? 256 : 1024; }
 
 // One record at shared address ra against chunk x: this lane's block's share
 // of rows g and g+8, added to a0 and a1.
@@ -1027,7 +1044,10 @@ __device__ __forceinline__ void record_c0(uint32_t ra, const ChunkX &x, int lane
     rw.load(ra, lane);
     uint32_t sw, mw = 0u;                            // scales (mins) of (row g, block t), (row g + 8, block t)
     uint32_t dw = 0u, dmw = 0u;                      // Q4_K: d and dmin of rows g, g + 8
-    asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(sw) : "r"(ra + lane * 4), "n"(scale_off<FMT>()) : "memory");
+    if constexpr (FMT == 4)  // Q1: one scale per row and chunk
+        asm volatile("ld.shared.u32 %0, [%1+256];" : "=r"(sw) : "r"(ra + (lane >> 2) * 4) : "memory");
+    else
+        asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(sw) : "r"(ra + lane * 4), "n"(scale_off<FMT>()) : "memory");
     if (FMT == 1) asm volatile("ld.shared.u32 %0, [%1+1152];" : "=r"(mw) : "r"(ra + lane * 4) : "memory");
     if (FMT == 3) {
         asm volatile("ld.shared.u32 %0, [%1+1152];" : "=r"(dw) : "r"(ra + (lane >> 2) * 4) : "memory");
@@ -1059,9 +1079,12 @@ __device__ __forceinline__ void record_c0(uint32_t ra, const ChunkX &x, int lane
         s2 = scale_pair<FMT>(sw);
         if (FMT == 1) m2 = scale_pair<FMT>(mw);
     }
-    if (!has_min(FMT)) {
+    if (has_offset(FMT)) {
         a0 = fmaf(s2.x * x.F, T0 - x.G, a0);
         a1 = fmaf(s2.y * x.F, T2 - x.G, a1);
+    } else if (!has_min(FMT)) {  // Q1: the signs' product alone
+        a0 = fmaf(s2.x * x.F, T0, a0);
+        a1 = fmaf(s2.y * x.F, T2, a1);
     } else {
         a0 = fmaf(m2.x, x.G, fmaf(s2.x * x.F, T0, a0));
         a1 = fmaf(m2.y, x.G, fmaf(s2.y * x.F, T2, a1));
@@ -1254,8 +1277,8 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
         const uint32_t st_a = st_base + su * REC;
         const bool two = upt == 2 && q.t0 + 2 * pl + 1 < p.T;
         // the chunk's four block factors of this lane's activation rows, and
-        // for the affine format their block sums (Q4_0 forms its offset
-        // products per block below)
+        // for the formats with a min their block sums (Q4_0 and Q8_0 form
+        // their offset products per block below; Q1 has neither)
         float G[NGR][4], F[NGR][4];
 #pragma unroll
         for (int j = 0; j < NGR; ++j) {
@@ -1270,6 +1293,8 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                 G[j][1] = gv.y;
                 G[j][2] = gv.z;
                 G[j][3] = gv.w;
+            } else if (!has_offset(FMT)) {  // Q1: no offset term
+                G[j][0] = G[j][1] = G[j][2] = G[j][3] = 0.f;
             }
         }
         // the records' words: weights of rows g and g+8, scales (and mins)
@@ -1283,7 +1308,13 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             if (rc == 0 || two) {
                 const uint32_t ra = st_a + rc * SU * REC;
                 rw[rc].load(ra, lane);
-                sw[rc] = lds128_at<scale_off<FMT>()>(ra + g * 16);
+                if constexpr (FMT == 4) {  // Q1: one scale word per row pair, for every block
+                    uint32_t w1;
+                    asm volatile("ld.shared.u32 %0, [%1+256];" : "=r"(w1) : "r"(ra + g * 4) : "memory");
+                    sw[rc] = make_uint4(w1, w1, w1, w1);
+                } else {
+                    sw[rc] = lds128_at<scale_off<FMT>()>(ra + g * 16);
+                }
                 if (FMT == 1) mw[rc] = lds128_at<1152>(ra + g * 16);
                 if (FMT == 3) {
                     uint32_t dw, dmw;
@@ -1301,7 +1332,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             uint4 B[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) B[nt] = *reinterpret_cast<const uint4 *>(xa + boff[nt]);
-            if (!has_min(FMT)) {
+            if (has_offset(FMT)) {
                 // the block's offset product: the same tensor-core chain as the
                 // weights' below, with every weight zero (every nibble 8 for
                 // Q4_0, every biased byte 128 for Q8_0): exactly what such a
@@ -1341,9 +1372,12 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                         mma16816(d, a[4], a[5], a[6], a[7], B[nt].z, B[nt].w);
                         const float T0 = d[0] + d[1], T2 = d[2] + d[3];
                         const float fb = F[0][blk];
-                        if (!has_min(FMT)) {
+                        if (has_offset(FMT)) {
                             acc[rc][0] = fmaf(s2.x * fb, T0 - G[0][blk], acc[rc][0]);
                             acc[rc][1] = fmaf(s2.y * fb, T2 - G[0][blk], acc[rc][1]);
+                        } else if (!has_min(FMT)) {
+                            acc[rc][0] = fmaf(s2.x * fb, T0, acc[rc][0]);
+                            acc[rc][1] = fmaf(s2.y * fb, T2, acc[rc][1]);
                         } else {
                             acc[rc][0] = fmaf(m2.x, G[0][blk], fmaf(s2.x * fb, T0, acc[rc][0]));
                             acc[rc][1] = fmaf(m2.y, G[0][blk], fmaf(s2.y * fb, T2, acc[rc][1]));
@@ -1357,8 +1391,10 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                             const float sj = (j < 2 ? s2.x : s2.y) * F[2 * nt + (j & 1)][blk];
                             const float gj = G[2 * nt + (j & 1)][blk];
                             float &ac = acc[rc][4 * nt + j];
-                            if (!has_min(FMT)) {
+                            if (has_offset(FMT)) {
                                 ac = fmaf(sj, d[j] - gj, ac);
+                            } else if (!has_min(FMT)) {
+                                ac = fmaf(sj, d[j], ac);
                             } else {
                                 const float mj = j < 2 ? m2.x : m2.y;
                                 ac = fmaf(mj, gj, fmaf(sj, d[j], ac));

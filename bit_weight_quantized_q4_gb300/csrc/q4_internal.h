@@ -47,6 +47,17 @@ constexpr int kRecQ8_0 = 2176;
 // (high half) of the superblock the chunk belongs to, and at [1184, 1216) their
 // fp16 dmin.  A 256-column superblock spans two chunks; each carries d, dmin.
 constexpr int kRecQ4_K = 1216;
+// Q1 records (288 bytes): a 128-column chunk is one Q1 superblock.  Lane
+// L = 4g + t owns 8 bytes at [8L, 8L + 8): the 32 sign bits of row g, then of
+// row g + 8, each bit inverted (a set stored bit is -d), bit rho (0..15) for
+// element q1_elem(t, rho) and bit 16 + rho for the element after it; then at
+// [256, 288) word g holds the fp16 d of rows g (low half) and g + 8.
+constexpr int kRecQ1 = 288;
+
+// Chunk element (0..127) of Q1 bit rho (0..15) of lane-position t: register
+// rho = 2s + h of the tensor-core A fragment of k16 step s, its first k
+// (h = 0: columns 2t, 2t+1 of the step; h = 1: 2t+8, 2t+9).
+inline int q1_elem(int t, int rho) { return 16 * (rho >> 1) + 8 * (rho & 1) + 2 * t; }
 
 // Block element (0..31) stored in nibble i of lane-position t's word.
 // Pairs (i, i+4) are (k, k+1) of one f16x2 fragment register:
@@ -69,11 +80,16 @@ inline int q8_elem(int t, int i) {
 }
 
 Q4_HD constexpr int rec_bytes(int fmt) {
-    return fmt == 0 ? kRecQ4_0 : fmt == 1 ? kRecAffine : fmt == 2 ? kRecQ8_0 : kRecQ4_K;
+    return fmt == 0 ? kRecQ4_0 : fmt == 1 ? kRecAffine : fmt == 2 ? kRecQ8_0 : fmt == 3 ? kRecQ4_K : kRecQ1;
 }
 // Formats whose weights carry a per-block min (w = s*q + m): the products
 // need the activation block sums.
 Q4_HD constexpr bool has_min(int fmt) { return fmt == 1 || fmt == 3; }
+// Formats stored with an offset (Q4_0's q - 8, Q8_0's bias of 128): the
+// products need the block's zero-weight (offset) product.
+Q4_HD constexpr bool has_offset(int fmt) { return fmt == 0 || fmt == 2; }
+// Nibble formats: a lower nibble meets its activation times 16.
+Q4_HD constexpr bool is_nibble(int fmt) { return fmt == 0 || fmt == 1 || fmt == 3; }
 inline int64_t tiles_of(int64_t n) { return (n + kTileRows - 1) / kTileRows; }
 inline int64_t chunks_of(int64_t k) { return (k + kChunkK - 1) / kChunkK; }
 
@@ -100,8 +116,9 @@ Q4_HD constexpr int cls_warps(int c) { return c == 3 ? 8 : 16; }     // warps pe
 Q4_HD constexpr int cls_depth(int c) { return (void)c, 2; }  // ring stages per warp
 Q4_HD constexpr int cls_stage(int c) { return c == 2 ? 1 : 2; }  // pair units per stage (2x as many single-tile units)
 // pair units per ring stage for a format: Q8_0 records are nearly twice as
-// large, so its stages hold one
-Q4_HD constexpr int stage_su(int fmt, int c) { return fmt == 2 ? 1 : cls_stage(c); }
+// large, so its stages hold one; Q1 records a quarter, so its stages hold
+// four times as many
+Q4_HD constexpr int stage_su(int fmt, int c) { return fmt == 2 ? 1 : fmt == 4 ? 4 * cls_stage(c) : cls_stage(c); }
 Q4_HD constexpr int cls_gsw(int c) { return c <= 1 ? 4 : c == 2 ? 8 : 16; }  // group-sum rows per chunk
 // bytes of one activation row per 32-column block in shared memory: f16 hi
 // and lo parts for nb <= 4, the f16 value alone for larger batches
@@ -312,15 +329,18 @@ int launch_gemv_q4_0(const GemvParams &p, const Plan &plan, void *stream);
 int launch_gemv_affine(const GemvParams &p, const Plan &plan, void *stream);
 int launch_gemv_q8_0(const GemvParams &p, const Plan &plan, void *stream);
 int launch_gemv_q4_k(const GemvParams &p, const Plan &plan, void *stream);
+int launch_gemv_q1(const GemvParams &p, const Plan &plan, void *stream);
 // Cooperative launch of the decode-step kernel: one CTA per SM.
 int launch_step_q4_0(const StepParams &p, int ctas, size_t smem, void *stream);
 int launch_step_affine(const StepParams &p, int ctas, size_t smem, void *stream);
 int launch_step_q8_0(const StepParams &p, int ctas, size_t smem, void *stream);
 int launch_step_q4_k(const StepParams &p, int ctas, size_t smem, void *stream);
+int launch_step_q1(const StepParams &p, int ctas, size_t smem, void *stream);
 // Decode-step CTAs that can be resident on one SM (0 on error).
 int step_occupancy_q4_0(int nb, size_t smem);
 int step_occupancy_affine(int nb, size_t smem);
 int step_occupancy_q8_0(int nb, size_t smem);
 int step_occupancy_q4_k(int nb, size_t smem);
+int step_occupancy_q1(int nb, size_t smem);
 
 }  // namespace q4

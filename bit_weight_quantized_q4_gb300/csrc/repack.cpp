@@ -1,4 +1,4 @@
-// repack.cpp -- host-side lossless re-layout of Q4_0 / affine-Q4 / Q8_0 / Q4_K weights into
+// repack.cpp -- host-side lossless re-layout of Q4_0 / affine-Q4 / Q8_0 / Q4_K / Q1 weights into
 // the coalesced device layout described in q4_internal.h, and its inverse.
 //
 // The pages re-lay block formats once at load time so that the GEMV reads
@@ -79,11 +79,11 @@ inline int q4k_nib(const uint8_t *sb, int j, int e) {
 }  // namespace
 
 inline bool fmt_ok(int32_t fmt) {
-    return fmt == Q4_FMT_Q4_0 || fmt == Q4_FMT_AFFINE || fmt == Q4_FMT_Q8_0 || fmt == Q4_FMT_Q4_K;
+    return fmt == Q4_FMT_Q4_0 || fmt == Q4_FMT_AFFINE || fmt == Q4_FMT_Q8_0 || fmt == Q4_FMT_Q4_K || fmt == Q4_FMT_Q1;
 }
-// Q4_K rows are whole 256-column superblocks.
+// Q4_K rows are whole 256-column superblocks, Q1 rows whole 128-column ones.
 inline bool fmt_shape_ok(int32_t fmt, int32_t n, int32_t k) {
-    return fmt_ok(fmt) && shape_ok(n, k) && (fmt != Q4_FMT_Q4_K || k % 256 == 0);
+    return fmt_ok(fmt) && shape_ok(n, k) && (fmt != Q4_FMT_Q4_K || k % 256 == 0) && (fmt != Q4_FMT_Q1 || k % 128 == 0);
 }
 
 extern "C" size_t q4_packed_bytes(int32_t fmt, int32_t n, int32_t k) {
@@ -94,6 +94,7 @@ extern "C" size_t q4_packed_bytes(int32_t fmt, int32_t n, int32_t k) {
 extern "C" size_t q4_weight_bytes(int32_t fmt, int32_t n, int32_t k) {
     if (!fmt_shape_ok(fmt, n, k)) return 0;
     if (fmt == Q4_FMT_Q4_K) return (size_t)n * (size_t)(k / 256) * 144u;
+    if (fmt == Q4_FMT_Q1) return (size_t)n * (size_t)(k / 128) * 18u;
     return (size_t)n * (size_t)(k / 32) * (fmt == Q4_FMT_Q4_0 ? 18u : fmt == Q4_FMT_AFFINE ? 20u : 34u);
 }
 
@@ -201,6 +202,73 @@ extern "C" q4_status q4_repack_q4_k(const void *host_blocks, int32_t n, int32_t 
                 }
                 store_u32(r + 1152 + g * 4, dw);
                 store_u32(r + 1184 + g * 4, mw);
+            }
+        }
+    return Q4_OK;
+}
+
+// Q1 superblock (18 bytes: fp16 d, 16 bytes of sign bits, byte i holding
+// elements 8i..8i+7 from its lowest bit; 1 is +d).  The device record keeps
+// each bit inverted, so that a set bit is the f16 sign of -1.
+inline int q1_bit(const uint8_t *sb, int e) { return (sb[2 + (e >> 3)] >> (e & 7)) & 1; }
+
+extern "C" q4_status q4_repack_q1(const void *host_blocks, int32_t n, int32_t k, void *host_out, size_t out_bytes) {
+    if (!host_blocks || !host_out) return Q4_ERR_NULL;
+    if (!fmt_shape_ok(Q4_FMT_Q1, n, k)) return Q4_ERR_SHAPE;
+    if (out_bytes < q4_packed_bytes(Q4_FMT_Q1, n, k)) return Q4_ERR_SHAPE;
+    const uint8_t *src = (const uint8_t *)host_blocks;
+    uint8_t *out = (uint8_t *)host_out;
+    const int64_t T = q4::tiles_of(n), C = k / 128;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < C; ++c) {
+            uint8_t *r = out + (t * C + c) * q4::kRecQ1;
+            for (int g = 0; g < 8; ++g) {
+                uint32_t dw = 0;
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t row = t * 16 + h * 8 + g;
+                    const uint8_t *sb = row < n ? src + (row * C + c) * 18 : nullptr;
+                    for (int tp = 0; tp < 4; ++tp) {
+                        uint32_t word = 0;  // padding rows: d = 0, any bits
+                        if (sb)
+                            for (int rho = 0; rho < 16; ++rho) {
+                                const int e = q4::q1_elem(tp, rho);
+                                word |= (uint32_t)(q1_bit(sb, e) ^ 1) << rho;
+                                word |= (uint32_t)(q1_bit(sb, e + 1) ^ 1) << (16 + rho);
+                            }
+                        store_u32(r + (4 * g + tp) * 8 + 4 * h, word);
+                    }
+                    if (sb) dw |= ((uint32_t)sb[0] | ((uint32_t)sb[1] << 8)) << (16 * h);
+                }
+                store_u32(r + 256 + 4 * g, dw);
+            }
+        }
+    return Q4_OK;
+}
+
+extern "C" q4_status q4_unpack_q1(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,
+                                  void *host_blocks) {
+    if (!host_packed || !host_blocks) return Q4_ERR_NULL;
+    if (!fmt_shape_ok(Q4_FMT_Q1, n, k)) return Q4_ERR_SHAPE;
+    if (packed_bytes < q4_packed_bytes(Q4_FMT_Q1, n, k)) return Q4_ERR_SHAPE;
+    const uint8_t *in = (const uint8_t *)host_packed;
+    uint8_t *dst = (uint8_t *)host_blocks;
+    const int64_t C = k / 128;
+    memset(dst, 0, (size_t)n * (size_t)C * 18);
+    for (int64_t row = 0; row < n; ++row)
+        for (int64_t c = 0; c < C; ++c) {
+            const uint8_t *r = in + ((row / 16) * C + c) * q4::kRecQ1;
+            const int g = (int)(row % 8), h = (int)((row % 16) / 8);
+            uint8_t *sb = dst + (row * C + c) * 18;
+            const uint16_t d = (uint16_t)(load_u32(r + 256 + 4 * g) >> (16 * h));
+            sb[0] = (uint8_t)(d & 0xFF);
+            sb[1] = (uint8_t)(d >> 8);
+            for (int tp = 0; tp < 4; ++tp) {
+                const uint32_t word = load_u32(r + (4 * g + tp) * 8 + 4 * h);
+                for (int rho = 0; rho < 16; ++rho) {
+                    const int e = q4::q1_elem(tp, rho);
+                    sb[2 + (e >> 3)] |= (uint8_t)((((word >> rho) & 1) ^ 1) << (e & 7));
+                    sb[2 + ((e + 1) >> 3)] |= (uint8_t)((((word >> (16 + rho)) & 1) ^ 1) << ((e + 1) & 7));
+                }
             }
         }
     return Q4_OK;

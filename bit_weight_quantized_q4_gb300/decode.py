@@ -58,6 +58,7 @@ class DecodeStep:
         T = lambda a: torch.from_numpy(a.copy()).to(device)
         W = lambda H: (Q4Weight.from_q8_0(H.blocks8, H.n, H.k, device) if hasattr(H, "blocks8")
                        else Q4Weight.from_q4_k(H.blocks_k, H.n, H.k, device) if hasattr(H, "blocks_k")
+                       else Q4Weight.from_q1(H.blocks1, H.n, H.k, device) if hasattr(H, "blocks1")
                        else Q4Weight.from_q4_0(H.blocks, H.n, H.k, device) if hasattr(H, "blocks")
                        else Q4Weight.from_affine(H.nib, H.s, H.m, H.n, H.k, device))
         self.eps = float(cfg.eps)

@@ -65,8 +65,10 @@ typedef enum {
     Q4_FMT_Q4_0 = 0,    /* 32 weights: fp16 scale d + 16 nibble bytes; w = d*(q-8) */
     Q4_FMT_AFFINE = 1,  /* 32 weights: bf16 scale s, bf16 min m, 16 nibble bytes; w = s*q + m */
     Q4_FMT_Q8_0 = 2,    /* 32 weights: fp16 scale d + 32 signed bytes; w = d*q */
-    Q4_FMT_Q4_K = 3     /* 256-weight superblocks: fp16 d, dmin, 6-bit sub-scales sc and mins mn
+    Q4_FMT_Q4_K = 3,    /* 256-weight superblocks: fp16 d, dmin, 6-bit sub-scales sc and mins mn
                            per 32 weights, nibbles; w = d*sc*q - dmin*mn (k a multiple of 256) */
+    Q4_FMT_Q1 = 4       /* 128-weight superblocks: fp16 d + 128 sign bits; w = +d (bit 1) or -d
+                           (bit 0) (k a multiple of 128) */
 } q4_format;
 
 /* A non-owning view of one repacked weight matrix in device memory.
@@ -75,7 +77,7 @@ typedef enum {
 typedef struct {
     int32_t fmt;        /* q4_format */
     int32_t n;          /* output rows */
-    int32_t k;          /* input length, multiple of 32 (of 256 for Q4_K) */
+    int32_t k;          /* input length, multiple of 32 (of 256 for Q4_K, of 128 for Q1) */
     const void *dev;    /* device pointer, 16-byte aligned */
     size_t bytes;       /* size of the packed buffer */
 } q4_weight;
@@ -86,11 +88,12 @@ typedef struct {
  * so the size may exceed the algorithmic 18 (Q4_0) or 20 (affine) bytes per
  * 32 weights when n % 16 or k % 128 is not zero.  Q8_0 takes 2176 bytes per
  * 16 x 128 tile chunk (34 per 32 weights); Q4_K takes 1216 (19 per 32
- * weights: each chunk repeats its superblock's d and dmin). */
+ * weights: each chunk repeats its superblock's d and dmin); Q1 takes 288
+ * (4.5 per 32 weights). */
 size_t q4_packed_bytes(int32_t fmt, int32_t n, int32_t k);
 
 /* Algorithmic weight bytes of an n x k matrix: 18 (Q4_0), 20 (affine) or 34
- * (Q8_0) per 32 weights, 144 per 256 (Q4_K); 0 on bad shape. */
+ * (Q8_0) per 32 weights, 144 per 256 (Q4_K), 18 per 128 (Q1); 0 on bad shape. */
 size_t q4_weight_bytes(int32_t fmt, int32_t n, int32_t k);
 
 /* Host -> host, lossless, deterministic repack of Q4_0 blocks into the
@@ -132,6 +135,17 @@ q4_status q4_repack_q4_k(const void *host_blocks, int32_t n, int32_t k, void *ho
 
 /* Inverse of q4_repack_q4_k (host -> host). */
 q4_status q4_unpack_q4_k(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k, void *host_blocks);
+
+/* Q1 host superblocks (crate inferencelayer, Functions: gemv_q1_k_lcpp_src,
+ * gemm_q1_src): [n][k/128] superblocks of 18 bytes -- the fp16 scale d
+ * (little endian), then 16 bytes of sign bits, byte i holding elements
+ * 8i..8i+7 from its lowest bit; w = +d for a set bit, -d for a clear one.  k
+ * must be a multiple of 128 (else Q4_ERR_SHAPE).  Lossless, host -> host;
+ * host_out holds q4_packed_bytes(Q4_FMT_Q1, n, k). */
+q4_status q4_repack_q1(const void *host_blocks, int32_t n, int32_t k, void *host_out, size_t out_bytes);
+
+/* Inverse of q4_repack_q1 (host -> host). */
+q4_status q4_unpack_q1(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k, void *host_blocks);
 
 /* Inverse of q4_repack_affine (host -> host). */
 q4_status q4_unpack_affine(const void *host_packed, size_t packed_bytes, int32_t n, int32_t k,

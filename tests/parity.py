@@ -18,13 +18,15 @@ def case_seed(*key):
     return zlib.crc32(repr(key).encode()) & 0xFFFF
 
 
-FMT_ID = {"q4_0": 0, "affine": 1, "q8_0": 2, "q4_k": 3}
+FMT_ID = {"q4_0": 0, "affine": 1, "q8_0": 2, "q4_k": 3, "q1": 4}
+_SUPERBLOCK = {"q4_k": 256, "q1": 128}
 
 
 def fmt_k(fmt, k):
-    """A test shape's k for a format: Q4_K rows are whole 256-column
-    superblocks, so its k is rounded up to one."""
-    return -(-k // 256) * 256 if fmt == "q4_k" else k
+    """A test shape's k for a format: Q4_K and Q1 rows are whole 256- and
+    128-column superblocks, so their k is rounded up to one."""
+    sb = _SUPERBLOCK.get(fmt, 32)
+    return -(-k // sb) * sb
 
 
 def host_weight(H):
@@ -32,6 +34,8 @@ def host_weight(H):
         return oracle.HostWeight.q8_0(H.blocks8, H.n, H.k)
     if hasattr(H, "blocks_k"):
         return oracle.HostWeight.q4_k(H.blocks_k, H.n, H.k)
+    if hasattr(H, "blocks1"):
+        return oracle.HostWeight.q1(H.blocks1, H.n, H.k)
     if hasattr(H, "blocks"):
         return oracle.HostWeight.q4_0(H.blocks, H.n, H.k)
     return oracle.HostWeight.affine(H.nib, H.s, H.m, H.n, H.k)
@@ -43,6 +47,8 @@ def dev_weight(H, device="cuda"):
         return q4.Q4Weight.from_q8_0(H.blocks8, H.n, H.k, device)
     if hasattr(H, "blocks_k"):
         return q4.Q4Weight.from_q4_k(H.blocks_k, H.n, H.k, device)
+    if hasattr(H, "blocks1"):
+        return q4.Q4Weight.from_q1(H.blocks1, H.n, H.k, device)
     if hasattr(H, "blocks"):
         return q4.Q4Weight.from_q4_0(H.blocks, H.n, H.k, device)
     return q4.Q4Weight.from_affine(H.nib, H.s, H.m, H.n, H.k, device)

@@ -67,6 +67,30 @@ def test_repack_roundtrip_q4_k(n, k):
     assert np.array_equal(q4.unpack_q4_k(P, n, k), H.blocks_k)
 
 
+@pytest.mark.parametrize("n,k", [(1, 128), (16, 128), (17, 384), (33, 1024), (100, 256)])
+def test_repack_roundtrip_q1(n, k):
+    rng = np.random.default_rng(n * 11 + k)
+    H = wl.draw_q1(rng, n, k)
+    P = q4.repack_q1(H.blocks1, n, k)
+    assert P.size == q4.packed_bytes(4, n, k) == -(-n // 16) * (k // 128) * 288
+    assert np.array_equal(q4.unpack_q1(P, n, k), H.blocks1)
+
+
+def test_q1_layout_bytes():
+    # a 16 x 128 tile is one 288-byte record: the 2048 sign bits, each
+    # inverted (a set stored bit is -d), then the 16 rows' fp16 d
+    rng = np.random.default_rng(13)
+    H = wl.draw_q1(rng, 16, 128)
+    P = q4.repack_q1(H.blocks1, 16, 128)
+    assert P.size == 288 and q4.weight_bytes(4, 16, 128) == 16 * 18
+    signs = np.unpackbits(H.blocks1[:, 0, 2:], axis=1, bitorder="little")
+    stored = np.unpackbits(P[:256], bitorder="little")
+    assert int(stored.sum()) == int((1 - signs).sum())   # the same bits, inverted
+    d = P[256:288].view(np.uint16).reshape(8, 2)
+    dh = H.blocks1[:, 0, 0:2].copy().view(np.uint16)[:, 0]
+    assert np.array_equal(d[:, 0], dh[:8]) and np.array_equal(d[:, 1], dh[8:])
+
+
 def test_q4_k_layout_bytes():
     # one 16 x 256 superblock row-set is two 1216-byte records; each holds the
     # 1024 nibble bytes of its half, one byte word per (row pair, block) with
@@ -127,10 +151,12 @@ def test_packed_sizes_and_padding():
     assert q4.packed_bytes(3, 4, 32) == 0 and q4.packed_bytes(3, 4, 128) == 0   # Q4_K: whole superblocks
     assert q4.packed_bytes(3, 14336, 4096) == 896 * 32 * 1216
     assert q4.weight_bytes(3, 14336, 4096) == 14336 * 16 * 144
-    assert q4.packed_bytes(4, 4, 256) == 0
+    assert q4.packed_bytes(4, 4, 64) == 0 and q4.packed_bytes(4, 4, 256) == 2 * 288   # Q1: whole 128-superblocks
+    assert q4.weight_bytes(4, 14336, 4096) == 14336 * 32 * 18
+    assert q4.packed_bytes(5, 4, 256) == 0
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2, 3])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("tiles,chunks,pairs", [(896, 32, False), (1024, 16, True), (128, 16, False),
                                                 (64, 16, False), (4096, 16, False), (1, 1, False),
                                                 (2, 1, True), (7, 3, False), (128, 64, False)])
@@ -256,6 +282,14 @@ def test_q4_k_rejects_partial_superblocks():
     assert L.q4_gemv(ctypes.byref(W), A, None, 1, A + 4096, None) == 2
     with pytest.raises(ValueError):
         q4.repack_q4_k(np.zeros((16, 1, 144), np.uint8), 16, 128)
+
+
+def test_q1_rejects_partial_superblocks():
+    L = q4.lib()
+    buf = np.zeros(1 << 16, np.uint8)
+    assert L.q4_repack_q1(buf.ctypes.data, 16, 96, buf.ctypes.data, buf.size) == 2
+    W = _cw(4, 16, 96, nbytes=1 << 20)
+    assert L.q4_gemv(ctypes.byref(W), A, None, 1, A + 4096, None) == 2
 
 
 def test_repack_validation():

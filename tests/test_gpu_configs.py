@@ -229,6 +229,9 @@ STEP_CASES = [
     ("q4_k", 1, 2, 256, 64, 512, 1000),
     ("q4_k", 3, 2, 256, 48, 256, 333),
     ("q4_k", 9, 2, 256, 32, 256, 300),
+    ("q1", 1, 2, 256, 64, 384, 1000),
+    ("q1", 4, 2, 128, 48, 256, 333),
+    ("q1", 9, 2, 128, 32, 128, 300),
     ("q4_0", 1, 32, 128, 32, 192, 300),
     ("affine", 2, 32, 128, 32, 192, 300),
 ]

@@ -41,7 +41,7 @@ def test_pack_rounds_and_sums(q4, nb, k):
     assert torch.equal(gs, ref)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("nb", [1, 3, 5, 9, 16])
 @pytest.mark.parametrize("n,k", [(33, 160), (700, 1024), (64, 8192)])
 def test_gemv_half_parity(q4, fmt, nb, n, k):

@@ -30,7 +30,7 @@ def _draw(fmt, rng, n, k):
 SHAPES = [(1, 32), (7, 96), (33, 160), (100, 544), (512, 2048), (1000, 4096), (48, 8192)]
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("nb", [1, 2, 3, 4, 5, 8, 9, 16])
 @pytest.mark.parametrize("n,k", SHAPES)
 def test_gemv(q4, fmt, nb, n, k):
@@ -60,7 +60,7 @@ def test_affine_with_given_group_sums(q4, nb):
     check(to_np(y1), y_ref, S, what="affine given gsum")
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("nb", [1, 3, 16])
 @pytest.mark.parametrize("n,k", [(64, 64), (2048, 2048), (37, 4096), (130, 8192)])
 def test_nrm_gemv(q4, fmt, nb, n, k):
@@ -74,7 +74,7 @@ def test_nrm_gemv(q4, fmt, nb, n, k):
     check(to_np(y), y_ref, S, what="nrm %s nb=%d %dx%d" % (fmt, nb, n, k))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("norm", [True, False])
 @pytest.mark.parametrize("na,nbr,k,nb", [(512, 512, 2048, 1), (40, 17, 96, 2), (2048, 512, 2048, 4)])
 def test_dual(q4, fmt, norm, na, nbr, k, nb):
@@ -90,7 +90,7 @@ def test_dual(q4, fmt, norm, na, nbr, k, nb):
     check(to_np(yb), rb, Sb, what="dual b")
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("n,k,nb", [(8192, 2048, 1), (40, 96, 3), (1000, 1024, 8), (256, 512, 16)])
 def test_gus_nrm(q4, fmt, n, k, nb):
     k = fmt_k(fmt, k)
@@ -104,7 +104,7 @@ def test_gus_nrm(q4, fmt, n, k, nb):
     check_swiglu(to_np(h), g, Sg, u, Su, what="gus %s %dx%d nb=%d" % (fmt, n, k, nb))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("n,k,nb", [(2048, 8192, 1), (2048, 2048, 1), (33, 160, 5), (700, 1024, 16)])
 @pytest.mark.parametrize("inplace", [False, True])
 def test_res_gemv(q4, fmt, n, k, nb, inplace):
@@ -122,7 +122,7 @@ def test_res_gemv(q4, fmt, n, k, nb, inplace):
     check_residual(to_np(y), y_ref, S, what="res %s" % fmt)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("n,k,nb,norm", [(65536, 2048, 1, True), (1000, 256, 3, False), (77, 96, 16, True)])
 def test_argmax(q4, fmt, n, k, nb, norm):
     k = fmt_k(fmt, k)
@@ -155,7 +155,7 @@ def test_argmax_planted_and_ties(q4):
     assert val.cpu().tolist() == [7.0 * 64, 0.0]
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 def test_zero_weights_exact(q4, fmt):
     rng = np.random.default_rng(41)
     n, k = 200, 1024
@@ -165,6 +165,10 @@ def test_zero_weights_exact(q4, fmt):
     elif fmt == "q8_0":
         d = rng.uniform(0.0003, 0.0012, (n, k // 32)).astype(np.float16).view(np.uint16)
         H = wl.Q8_0Host(n, k, wl.pack_q8_0(np.zeros((n, k), np.int16), d))
+    elif fmt == "q1":
+        # random signs, every scale zero
+        z = np.zeros((n, k // 128), np.uint16)
+        H = wl.Q1Host(n, k, wl.pack_q1(rng.integers(0, 2, (n, k), dtype=np.uint8), z))
     elif fmt == "q4_k":
         # nonzero nibbles, d and dmin; every sub-block scale and min zero
         d = rng.uniform(1e-4, 4e-4, (n, k // 256)).astype(np.float16).view(np.uint16)
@@ -212,9 +216,17 @@ def test_power_of_two_scaling_bitwise(q4):
         bk[:, :, o + 1] = (dd >> 8).astype(np.uint8)
     k1 = q4.q4_gemv(dev_weight(HK), x)
     assert torch.equal(q4.q4_gemv(dev_weight(wl.Q4_KHost(n, k, bk)), x), 2.0 * k1)
+    # Q1: d -> 2d
+    H1 = wl.draw_q1(rng, n, k)
+    b1 = H1.blocks1.copy()
+    dd = (b1[:, :, 0].astype(np.uint16) | (b1[:, :, 1].astype(np.uint16) << 8)) + 0x0400
+    b1[:, :, 0] = (dd & 0xFF).astype(np.uint8)
+    b1[:, :, 1] = (dd >> 8).astype(np.uint8)
+    o1 = q4.q4_gemv(dev_weight(H1), x)
+    assert torch.equal(q4.q4_gemv(dev_weight(wl.Q1Host(n, k, b1)), x), 2.0 * o1)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q4_k", "q1"])
 def test_one_hot_columns(q4, fmt):
     rng = np.random.default_rng(43)
     n, k = 96, 256
@@ -259,7 +271,7 @@ def test_nrm_constant_vector(q4):
 
 
 @pytest.mark.parametrize("nb", [3, 5, 9])
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 def test_large_dynamic_range(q4, fmt, nb):
     # activations far outside f16 range in both directions, and 32-column
     # blocks of very different magnitude inside one row, stay within

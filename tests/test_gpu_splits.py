@@ -46,7 +46,7 @@ def _draw(fmt, rng, n, k):
     return wl._draw_fmt(fmt)(rng, n, k)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("nb", [1, 4, 16])
 @pytest.mark.parametrize("S", [2, 4, 8])
 def test_split_store_and_norm(q4, fmt, nb, S):
@@ -67,7 +67,7 @@ def test_split_store_and_norm(q4, fmt, nb, S):
     check(to_np(y), y_ref, Sr, what="split nrm %s nb=%d S=%d %dx%d" % (fmt, nb, S, n, k))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("nb", [1, 16])
 @pytest.mark.parametrize("S", [2, 8])
 def test_split_residual(q4, fmt, nb, S):
@@ -81,7 +81,7 @@ def test_split_residual(q4, fmt, nb, S):
     check_residual(to_np(y), y_ref, Sr, what="split res %s nb=%d S=%d" % (fmt, nb, S))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("nb", [1, 8])
 @pytest.mark.parametrize("S", [2, 4, 8])
 def test_split_swiglu(q4, fmt, nb, S):
@@ -96,7 +96,7 @@ def test_split_swiglu(q4, fmt, nb, S):
     check_swiglu(to_np(h), g, Sg, u, Su, what="split gus %s nb=%d S=%d %dx%d" % (fmt, nb, S, n, k))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k"])
+@pytest.mark.parametrize("fmt", ["q4_0", "affine", "q8_0", "q4_k", "q1"])
 @pytest.mark.parametrize("nb", [1, 3])
 @pytest.mark.parametrize("S", [2, 8])
 def test_split_argmax(q4, fmt, nb, S):
