@@ -111,6 +111,10 @@ def lib() -> ctypes.CDLL:
         L.q4o_swiglu.argtypes = [P, P, I64, P]
         L.q4o_add.argtypes = [P, P, I64, P]
         L.q4o_argmax.restype = I64
+        L.q4o_rope_table.argtypes = [I64, I64, ctypes.c_double, P, P]
+        L.q4o_rope_apply.argtypes = [P, I64, P, P]
+        L.q4o_attn_decode.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_double,
+                                      P, P, P, P, P]
         L.q4o_argmax.argtypes = [P, I64]
         _lib = L
     return _lib
@@ -409,3 +413,48 @@ def decode_step(cfg, layers=None):
         hid = decode_layer(L, hid, cfg.eps)["hid"]
     idx, logits, _ = q4_argmax(_hw(cfg.Wlogits), hid, cfg.gamma_final, cfg.eps)
     return idx, logits, hid
+
+
+# ---------------------------------------------------------------- attention
+# Decode attention of honeycrisp/mod.rs (attn_state, gpu_attention, and the
+# fused RoPE + KV-append + SDPA dispatch of forward_decode_fused_layers).
+
+def rope_table(max_seq: int, d: int, rope_theta: float):
+    """cos and sin tables ``[max_seq, d/2]`` (f64) of theta = pos /
+    rope_theta^(2j/d)."""
+    c = np.empty((max_seq, d // 2), np.float64)
+    s = np.empty((max_seq, d // 2), np.float64)
+    lib().q4o_rope_table(max_seq, d, float(rope_theta), _p(c), _p(s))
+    return c, s
+
+
+def rope_apply(x, c_row, s_row) -> np.ndarray:
+    """One head vector rotated by a table row (element j pairs with j + d/2)."""
+    x = _f64(x).copy()
+    c_row, s_row = _f64(c_row), _f64(s_row)
+    lib().q4o_rope_apply(_p(x), x.size, _p(c_row), _p(s_row))
+    return x
+
+
+def attn_decode(q, k_new, v_new, k_cache, v_cache, position: int, window: int, scale: float,
+                cosv=None, sinv=None):
+    """Decode attention of one token.  q ``[H, d]``, k_new / v_new
+    ``[Hkv, d]``, caches ``[Hkv, max_seq, d]`` (not modified: the appended
+    copies are returned), tables ``[max_seq, d/2]`` or None.  Returns
+    ``(out [H, d], bound [H, d], k_cache', v_cache')``, all f64."""
+    q, k_new, v_new = _f64(q), _f64(k_new), _f64(v_new)
+    kc, vc = _f64(k_cache).copy(), _f64(v_cache).copy()
+    H, d = q.shape
+    Hkv, max_seq, _ = kc.shape
+    assert H % Hkv == 0 and 0 <= position < max_seq
+    out = np.empty((H, d), np.float64)
+    bound = np.empty((H, d), np.float64)
+    scratch = np.empty(max_seq + 2 * d, np.float64)
+    cp = sp = None
+    if cosv is not None:
+        cosv, sinv = _f64(cosv), _f64(sinv)
+        assert cosv.shape == (max_seq, d // 2) and sinv.shape == (max_seq, d // 2)
+        cp, sp = _p(cosv), _p(sinv)
+    lib().q4o_attn_decode(_p(q), _p(k_new), _p(v_new), _p(kc), _p(vc), max_seq, position, H, Hkv, d,
+                          int(window), float(scale), cp, sp, _p(out), _p(bound), _p(scratch))
+    return out, bound, kc, vc

@@ -61,6 +61,12 @@
  *    matmul + residual dispatch in forward_decode_fused_layers.
  *  - Greedy argmax over logits: Module gpu, module sampling.  Reading: ties go
  *    to the lowest index.
+ *  - Decode attention with KV append, GQA, sliding window and RoPE tables:
+ *    honeycrisp/mod.rs, attn_state (f32 caches of kv_heads x max_seq x
+ *    head_dim per layer; RoPE tables theta = pos / rope_theta^(2j/head_dim)),
+ *    gpu_attention (append k and v at position, then scores = q K^T, softmax,
+ *    times V over total_seq = position + 1 with a window and a scale) and the
+ *    fused RoPE + KV-append + SDPA dispatch of forward_decode_fused_layers.
  */
 #include <math.h>
 #include <stddef.h>
@@ -302,4 +308,98 @@ int64_t q4o_argmax(const double *v, int64_t n)
         if (v[i] > v[best])
             best = i;
     return best;
+}
+
+/* RoPE tables (honeycrisp/mod.rs, attn_state: theta = pos / rope_theta^(2j /
+ * head_dim) for j < rope_dim / 2, tables of cos and sin per position):
+ * cosv[p][j], sinv[p][j] for p < max_seq, j < d / 2 (rope_dim = d). */
+void q4o_rope_table(int64_t max_seq, int64_t d, double rope_theta, double *cosv, double *sinv)
+{
+    for (int64_t p = 0; p < max_seq; ++p)
+        for (int64_t j = 0; j < d / 2; ++j) {
+            double th = (double)p / pow(rope_theta, 2.0 * (double)j / (double)d);
+            cosv[p * (d / 2) + j] = cos(th);
+            sinv[p * (d / 2) + j] = sin(th);
+        }
+}
+
+/* Rotate one head vector x[d] in place by the table row (c, s) of its
+ * position.  Reading (the pages do not print the pairing): element j pairs
+ * with element j + d/2 (the rotate-half form of the transformers models the
+ * pages mirror): (a, b) -> (a c - b s, b c + a s). */
+void q4o_rope_apply(double *x, int64_t d, const double *c, const double *s)
+{
+    for (int64_t j = 0; j < d / 2; ++j) {
+        double a = x[j], b = x[j + d / 2];
+        x[j] = a * c[j] - b * s[j];
+        x[j + d / 2] = b * c[j] + a * s[j];
+    }
+}
+
+/* Decode attention of the token at `position` (honeycrisp/mod.rs,
+ * gpu_attention and the fused RoPE + KV-append + SDPA dispatch of
+ * forward_decode_fused_layers):
+ *  1. with tables, q (every head) and k_new (every kv head) are rotated by
+ *     the table rows of `position`;
+ *  2. k_new and v_new are appended: cache[hk][position] = k, v;
+ *  3. total = position + 1; the attended positions are [lo, total) with
+ *     lo = max(0, total - window) for window > 0, else 0;
+ *  4. query head h reads kv head h / (H / Hkv) (consecutive heads share one);
+ *     its scores are scale * q_h . k_t, softmax over the attended positions
+ *     (shifted by their maximum), and out_h = sum_t p_t v_t.
+ * q: [H][d]; k_new, v_new: [Hkv][d]; k_cache, v_cache: [Hkv][max_seq][d]
+ * (updated); cosv, sinv: [max_seq][d/2] or NULL (no rotation);
+ * out, bound: [H][d] (bound = sum_t p_t |v_t|, the tolerance scale);
+ * scratch: max_seq + 2 d doubles. */
+void q4o_attn_decode(const double *q, const double *k_new, const double *v_new,
+                     double *k_cache, double *v_cache, int64_t max_seq, int64_t position,
+                     int64_t H, int64_t Hkv, int64_t d, int64_t window, double scale,
+                     const double *cosv, const double *sinv, double *out, double *bound,
+                     double *scratch)
+{
+    double *p = scratch, *qh = scratch + max_seq, *kh = qh + d;
+    int64_t G = H / Hkv;
+    for (int64_t hk = 0; hk < Hkv; ++hk) {
+        for (int64_t e = 0; e < d; ++e)
+            kh[e] = k_new[hk * d + e];
+        if (cosv)
+            q4o_rope_apply(kh, d, cosv + position * (d / 2), sinv + position * (d / 2));
+        for (int64_t e = 0; e < d; ++e) {
+            k_cache[(hk * max_seq + position) * d + e] = kh[e];
+            v_cache[(hk * max_seq + position) * d + e] = v_new[hk * d + e];
+        }
+    }
+    int64_t total = position + 1;
+    int64_t lo = (window > 0 && total > window) ? total - window : 0;
+    for (int64_t h = 0; h < H; ++h) {
+        int64_t hk = h / G;
+        for (int64_t e = 0; e < d; ++e)
+            qh[e] = q[h * d + e];
+        if (cosv)
+            q4o_rope_apply(qh, d, cosv + position * (d / 2), sinv + position * (d / 2));
+        double mx = -INFINITY;
+        for (int64_t t = lo; t < total; ++t) {
+            double s = 0.0;
+            for (int64_t e = 0; e < d; ++e)
+                s += qh[e] * k_cache[(hk * max_seq + t) * d + e];
+            p[t] = scale * s;
+            if (p[t] > mx)
+                mx = p[t];
+        }
+        double z = 0.0;
+        for (int64_t t = lo; t < total; ++t) {
+            p[t] = exp(p[t] - mx);
+            z += p[t];
+        }
+        for (int64_t e = 0; e < d; ++e) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t t = lo; t < total; ++t) {
+                double v = v_cache[(hk * max_seq + t) * d + e];
+                acc += p[t] / z * v;
+                mag += p[t] / z * fabs(v);
+            }
+            out[h * d + e] = acc;
+            bound[h * d + e] = mag;
+        }
+    }
 }

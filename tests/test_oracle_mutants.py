@@ -58,6 +58,14 @@ MUTANTS = [
      "int bit = (blk[e / 8] >> (e % 8)) & 1;"),
     ("q1 superblock stride", "const uint8_t *blk = r + b * 18;\n        double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));\n        for (int e = 0; e < 128",
      "const uint8_t *blk = r + b * 16;\n        double d = q4o_half((uint16_t)(blk[0] | (blk[1] << 8)));\n        for (int e = 0; e < 128"),
+    ("attn kv head by modulo", "int64_t hk = h / G;", "int64_t hk = h % Hkv;"),
+    ("attn window one short", "int64_t lo = (window > 0 && total > window) ? total - window : 0;",
+     "int64_t lo = (window > 0 && total > window) ? total - window + 1 : 0;"),
+    ("attn scale dropped", "p[t] = scale * s;", "p[t] = s;"),
+    ("attn softmax unnormalised", "acc += p[t] / z * v;", "acc += p[t] * v;"),
+    ("attn appended k not rotated", "if (cosv)\n            q4o_rope_apply(kh,", "if (0)\n            q4o_rope_apply(kh,"),
+    ("rope sign", "x[j] = a * c[j] - b * s[j];", "x[j] = a * c[j] + b * s[j];"),
+    ("rope angle exponent", "pow(rope_theta, 2.0 * (double)j / (double)d)", "pow(rope_theta, (double)j / (double)d)"),
     ("halfset streams swapped", "x[r * k + 2 * i] = q4o_half(xe[r * (k / 2) + i]);",
      "x[r * k + 2 * i] = q4o_half(xo[r * (k / 2) + i]);"),
     ("halfset rows concatenated", "x[r * k + 2 * i + 1] = q4o_half(xo[r * (k / 2) + i]);",

@@ -646,3 +646,104 @@ def test_q1_brute_force_fsum():
             terms = dense[i] * x[r].astype(np.float64)
             assert abs(y[r, i] - math.fsum(terms)) <= 1e-12 * math.fsum(np.abs(terms))
             assert abs(S[r, i] - math.fsum(np.abs(terms))) <= 1e-12 * S[r, i]
+
+
+# ---- decode attention (honeycrisp/mod.rs: attn_state, gpu_attention and the
+# fused RoPE + KV-append + SDPA dispatch)
+
+def _attn_case(rng, H=8, Hkv=2, d=64, max_seq=48, position=29):
+    q = rng.standard_normal((H, d))
+    kn, vn = rng.standard_normal((Hkv, d)), rng.standard_normal((Hkv, d))
+    kc = rng.standard_normal((Hkv, max_seq, d))
+    vc = rng.standard_normal((Hkv, max_seq, d))
+    kc[:, position + 1:] = np.nan       # never read: beyond the token
+    vc[:, position + 1:] = np.nan
+    return q, kn, vn, kc, vc
+
+
+@pytest.mark.parametrize("window", [0, 1, 3, 30, 100])
+def test_attn_brute_force_softmax(window):
+    from scipy.special import softmax
+    rng = np.random.default_rng(130 + window)
+    H, Hkv, d, pos, scale = 8, 2, 64, 29, 0.125
+    q, kn, vn, kc, vc = _attn_case(rng, H, Hkv, d, position=pos)
+    out, bound, kc2, vc2 = oracle.attn_decode(q, kn, vn, kc, vc, pos, window, scale)
+    # the append, and nothing else written
+    assert np.array_equal(kc2[:, pos], kn) and np.array_equal(vc2[:, pos], vn)
+    assert np.array_equal(kc2[:, :pos], kc[:, :pos]) and np.array_equal(vc2[:, :pos], vc[:, :pos])
+    lo = max(0, pos + 1 - window) if window > 0 else 0
+    G = H // Hkv
+    for h in range(H):
+        K, V = kc2[h // G, lo:pos + 1], vc2[h // G, lo:pos + 1]
+        p = softmax(scale * (K @ q[h]))
+        for e in range(0, d, 5):
+            terms = p * V[:, e]
+            assert abs(out[h, e] - math.fsum(terms)) <= 1e-12 * (1 + math.fsum(np.abs(terms)))
+            assert abs(bound[h, e] - math.fsum(np.abs(terms))) <= 1e-12 * (1 + bound[h, e])
+
+
+def test_attn_zero_query_is_the_window_mean():
+    rng = np.random.default_rng(140)
+    q, kn, vn, kc, vc = _attn_case(rng)
+    out, _, _, vc2 = oracle.attn_decode(np.zeros_like(q), kn, vn, kc, vc, 29, 7, 0.3)
+    for h in range(8):
+        assert np.allclose(out[h], vc2[h // 4, 23:30].mean(axis=0), rtol=0, atol=1e-12)
+
+
+def test_attn_gqa_grouping():
+    # V of kv head j is the constant j + 1: consecutive query heads share one
+    rng = np.random.default_rng(141)
+    H, Hkv = 12, 3
+    q, kn, vn, kc, vc = _attn_case(rng, H, Hkv)
+    for j in range(Hkv):
+        vc[j, :30] = j + 1.0
+        vn[j] = j + 1.0
+    out, _, _, _ = oracle.attn_decode(q, kn, vn, kc, vc, 29, 0, 0.2)
+    for h in range(H):
+        assert np.allclose(out[h], h // 4 + 1.0, rtol=0, atol=1e-12)
+
+
+def test_attn_large_scale_is_the_argmax_row():
+    rng = np.random.default_rng(142)
+    q, kn, vn, kc, vc = _attn_case(rng)
+    out, _, kc2, vc2 = oracle.attn_decode(q, kn, vn, kc, vc, 29, 0, 1e4)
+    for h in range(8):
+        t = int(np.argmax(kc2[h // 4, :30] @ q[h]))
+        assert np.allclose(out[h], vc2[h // 4, t], rtol=0, atol=1e-9)
+
+
+def test_rope_table_and_rotation():
+    # the table against the pages' angle pos / theta^(2j/d), computed here
+    # with numpy's vectorised functions
+    c, s = oracle.rope_table(64, 16, 10000.0)
+    ang = np.arange(64)[:, None] / 10000.0 ** (2.0 * np.arange(8)[None, :] / 16)
+    assert np.allclose(c, np.cos(ang), rtol=0, atol=1e-15) and np.allclose(s, np.sin(ang), rtol=0, atol=1e-15)
+    # a hand-worked rotation: d = 4, angles pi/2 and 0; element j pairs with j + 2
+    x = oracle.rope_apply([1.0, 2.0, 3.0, 4.0], [0.0, 1.0], [1.0, 0.0])
+    assert np.array_equal(x, [-3.0, 2.0, 1.0, 4.0])
+    # rotations preserve each pair's norm, position 0 is the identity, and
+    # dot products depend only on the position difference
+    rng = np.random.default_rng(143)
+    c, s = oracle.rope_table(512, 64, 10000.0)
+    a, b = rng.standard_normal(64), rng.standard_normal(64)
+    assert np.array_equal(oracle.rope_apply(a, c[0], s[0]), a)
+    ra = oracle.rope_apply(a, c[77], s[77])
+    assert np.allclose(ra[:32] ** 2 + ra[32:] ** 2, a[:32] ** 2 + a[32:] ** 2, rtol=1e-13)
+    for p1, p2, dlt in [(5, 3, 100), (300, 17, 150), (40, 40, 471)]:
+        d1 = oracle.rope_apply(a, c[p1], s[p1]) @ oracle.rope_apply(b, c[p2], s[p2])
+        d2 = oracle.rope_apply(a, c[p1 + dlt], s[p1 + dlt]) @ oracle.rope_apply(b, c[p2 + dlt], s[p2 + dlt])
+        assert abs(d1 - d2) <= 1e-11
+
+
+def test_attn_rotates_q_and_appended_k():
+    rng = np.random.default_rng(144)
+    q, kn, vn, kc, vc = _attn_case(rng)
+    c, s = oracle.rope_table(48, 64, 10000.0)
+    out, bound, kc2, _ = oracle.attn_decode(q, kn, vn, kc, vc, 29, 0, 0.125, c, s)
+    for j in range(2):
+        assert np.allclose(kc2[j, 29], oracle.rope_apply(kn[j], c[29], s[29]), rtol=0, atol=0)
+    # the same as attending with pre-rotated q and k and no tables
+    qr = np.stack([oracle.rope_apply(q[h], c[29], s[29]) for h in range(8)])
+    kr = np.stack([oracle.rope_apply(kn[j], c[29], s[29]) for j in range(2)])
+    out2, bound2, _, _ = oracle.attn_decode(qr, kr, vn, kc, vc, 29, 0, 0.125)
+    assert np.array_equal(out, out2) and np.array_equal(bound, bound2)
