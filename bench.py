@@ -510,6 +510,29 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     out.update(stream_ceiling(Ws, bench_calls, peak, "q4_0_n%d_k%d" % (n4, k)))
     del Ws
     torch.cuda.empty_cache()
+    # decode attention of one token (RoPE, KV append, softmax(q K^T) V) at
+    # 32 query heads, 8 kv heads, head size 64, over 4096 and 32768 cached
+    # positions; the f32 caches rotate over copies totalling > 3x L2
+    H_, Hkv_, D_ = 32, 8, 64
+    for ctx in (4096, 32768):
+        kv_bytes = 2 * Hkv_ * ctx * D_ * 4
+        copies = max(2, -(-3 * l2_bytes // kv_bytes))
+        caches = [(torch.randn(Hkv_, ctx, D_, device=device), torch.randn(Hkv_, ctx, D_, device=device))
+                  for _ in range(copies)]
+        c_, s_ = q4.rope_table(ctx, D_, 10000.0)
+        tables = (torch.from_numpy(c_).to(device), torch.from_numpy(s_).to(device))
+        qa = torch.randn(H_, D_, device=device)
+        kn_, vn_ = torch.randn(Hkv_, D_, device=device), torch.randn(Hkv_, D_, device=device)
+        oa = torch.empty(H_, D_, device=device)
+        ws = torch.empty(int(q4.lib().q4_attn_workspace_bytes(H_, D_, ctx)), dtype=torch.uint8, device=device)
+        t = bench_calls(caches, lambda kv: q4.q4_attn_decode(qa, kn_, vn_, kv[0], kv[1], ctx - 1, 0, None,
+                                                            rope=tables, out=oa, workspace=ws))
+        gbs = kv_bytes / t / 1e9
+        out["attn_decode_h%d_kv%d_d%d_ctx%d" % (H_, Hkv_, D_, ctx)] = {
+            "us": round(t * 1e6, 3), "kv_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
+            "what": "f32 K and V rows of every kv head read once per call"}
+        del caches
+        torch.cuda.empty_cache()
     return out
 
 

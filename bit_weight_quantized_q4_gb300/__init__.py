@@ -9,8 +9,8 @@ no CPU fallback: if the library is missing the calls raise.
 Entry points (same names as the C ABI in ``include/q4gemv.h``):
 ``q4_gemv``, ``q4_nrm_gemv``, ``q4_dual_gemv``, ``q4_gus_nrm``,
 ``q4_res_gemv``, ``q4_argmax``, ``q4_group_sums``, ``q4_pack_half``,
-``q4_gemv_half``; plus ``Q4Weight`` for
-repacking host weights into the device layout.
+``q4_gemv_half``, ``q4_decode_step``, ``q4_attn_decode``; plus ``Q4Weight``
+for repacking host weights into the device layout and ``rope_table``.
 """
 from __future__ import annotations
 
@@ -102,6 +102,9 @@ def lib() -> ctypes.CDLL:
             "q4_device_check": (I32, [P]),
             "q4_debug_wait_limits": (I32, [ctypes.c_int64, I32, ctypes.c_int64, I32]),
             "q4_plan": (I32, [I32, I32, I32, I32, I32, I32, ctypes.POINTER(ctypes.c_int32)]),
+            "q4_attn_workspace_bytes": (SZ, [I32, I32, I32]),
+            "q4_attn_decode": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I32, F, P, P, P, P, SZ, P]),
+            "q4_rope_table": (I32, [I32, I32, ctypes.c_double, P, P]),
             "q4_status_str": (ctypes.c_char_p, [I32]),
         }
         for name, (res, args) in sig.items():
@@ -554,3 +557,55 @@ def q4_device_check():
     """Synchronise the current stream; raise if a GEMV-family kernel gave up
     waiting for its weight copies since the last check (the flag is cleared)."""
     _check(lib().q4_device_check(_stream()), "q4_device_check")
+
+
+# ---------------------------------------------------------------- attention
+
+def rope_table(max_seq: int, d: int, rope_theta: float = 10000.0):
+    """Host RoPE tables (cos, sin), float32 ``[max_seq, d/2]`` (q4_rope_table)."""
+    c = np.empty((max_seq, d // 2), np.float32)
+    sn = np.empty((max_seq, d // 2), np.float32)
+    _check(lib().q4_rope_table(max_seq, d, float(rope_theta), c.ctypes.data, sn.ctypes.data), "q4_rope_table")
+    return c, sn
+
+
+def q4_attn_decode(q, k_new, v_new, k_cache, v_cache, position: int, window: int = 0, scale=None, rope=None,
+                   out=None, workspace=None):
+    """Decode attention of one token: q ``[H, D]``, k_new / v_new ``[Hkv, D]``,
+    caches ``[Hkv, max_seq, D]`` (row ``position`` is written), ``rope`` an
+    optional (cos, sin) pair of ``[max_seq, D/2]`` device tables.  Returns
+    out ``[H, D]``; ``scale`` defaults to 1/sqrt(D)."""
+    torch = _torch()
+    q = _dev_f32(q, "q")
+    if q.dim() != 2:
+        raise ValueError("q must be [H, D]")
+    H, D = q.shape
+    dev = q.device
+    k_cache = _dev_buf(k_cache, "k_cache", torch.float32, None, dev, min_numel=0)
+    if k_cache.dim() != 3 or k_cache.shape[2] != D:
+        raise ValueError("k_cache must be [Hkv, max_seq, D]")
+    Hkv, max_seq = int(k_cache.shape[0]), int(k_cache.shape[1])
+    _dev_buf(v_cache, "v_cache", torch.float32, (Hkv, max_seq, D), dev)
+    _dev_buf(k_new, "k_new", torch.float32, (Hkv, D), dev)
+    _dev_buf(v_new, "v_new", torch.float32, (Hkv, D), dev)
+    cp = sp = None
+    if rope is not None:
+        cos_t, sin_t = rope
+        cp = _dev_buf(cos_t, "rope cos", torch.float32, (max_seq, D // 2), dev).data_ptr()
+        sp = _dev_buf(sin_t, "rope sin", torch.float32, (max_seq, D // 2), dev).data_ptr()
+    if out is None:
+        out = torch.empty((H, D), dtype=torch.float32, device=dev)
+    else:
+        _dev_buf(out, "out", torch.float32, (H, D), dev)
+    wsb = int(lib().q4_attn_workspace_bytes(H, D, max_seq))
+    if workspace is None:
+        workspace = torch.empty(max(16, wsb), dtype=torch.uint8, device=dev)
+    else:
+        _dev_buf(workspace, "workspace", torch.uint8, None, dev, min_numel=wsb)
+    if scale is None:
+        scale = 1.0 / float(D) ** 0.5
+    _check(lib().q4_attn_decode(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+                                v_cache.data_ptr(), max_seq, int(position), H, Hkv, D, int(window), float(scale),
+                                cp, sp, out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream()),
+           "q4_attn_decode")
+    return out

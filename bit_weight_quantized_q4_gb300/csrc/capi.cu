@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/q4gemv.h"
@@ -626,6 +627,87 @@ extern "C" q4_status q4_decode_check(const void *workspace, cudaStream_t stream)
     if (cudaMemcpy(&err, (const unsigned char *)workspace + 4, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
         return Q4_ERR_CUDA;
     return err ? Q4_ERR_CUDA : Q4_OK;
+}
+
+// ---------------------------------------------------------------- attention
+
+namespace {
+constexpr int kAttnMinChunk = 16;  // positions per chunk at least
+
+bool attn_geometry_ok(int32_t H, int32_t Hkv, int32_t D) {
+    if (Hkv < 1 || H < Hkv || H % Hkv != 0 || H > 4096) return false;
+    const int G = H / Hkv;
+    if (D == 64) return G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
+    if (D == 128) return G == 1 || G == 2 || G == 4 || G == 8;
+    return false;
+}
+}  // namespace
+
+extern "C" size_t q4_attn_workspace_bytes(int32_t H, int32_t D, int32_t max_seq) {
+    if (H < 1 || max_seq < 1 || (D != 64 && D != 128)) return 0;
+    const size_t splits = ((size_t)max_seq + kAttnMinChunk - 1) / kAttnMinChunk;
+    return splits * (size_t)H * (size_t)(D + 2) * sizeof(float);
+}
+
+extern "C" q4_status q4_attn_decode(const float *q, const float *k_new, const float *v_new, float *k_cache,
+                                    float *v_cache, int32_t max_seq, int32_t position, int32_t H, int32_t Hkv,
+                                    int32_t D, int32_t window, float scale, const float *rope_cos,
+                                    const float *rope_sin, float *out, void *workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+    Q4_TRY(check_act(q));
+    Q4_TRY(check_act(k_new));
+    Q4_TRY(check_act(v_new));
+    Q4_TRY(check_act(k_cache));
+    Q4_TRY(check_act(v_cache));
+    Q4_TRY(check_act(out));
+    if ((rope_cos == nullptr) != (rope_sin == nullptr)) return Q4_ERR_NULL;
+    if (rope_cos) {
+        Q4_TRY(check_act(rope_cos));
+        Q4_TRY(check_act(rope_sin));
+    }
+    if (!attn_geometry_ok(H, Hkv, D)) return Q4_ERR_UNSUPPORTED;
+    if (max_seq < 1 || max_seq > (1 << 24) || position < 0 || position >= max_seq || window < 0)
+        return Q4_ERR_SHAPE;
+    const int sms = num_sms();
+    if (sms <= 0) return Q4_ERR_CUDA;
+    q4::AttnParams p{};
+    p.q = q;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.rope_cos = rope_cos;
+    p.rope_sin = rope_sin;
+    p.out = out;
+    p.max_seq = max_seq;
+    p.position = position;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.D = D;
+    p.scale = scale;
+    p.total = position + 1;
+    p.lo = (window > 0 && p.total > window) ? p.total - window : 0;
+    // about one CTA per SM over all kv heads, chunks of kAttnMinChunk..Lmax
+    // positions (both the chunk's K and V rows are staged in shared memory)
+    const int len = p.total - p.lo;
+    const int target = std::max(1, sms / Hkv);
+    const int lmax = D == 64 ? 256 : 128;
+    p.Lc = std::min(lmax, std::max(kAttnMinChunk, (len + target - 1) / target));
+    p.nsplit = (len + p.Lc - 1) / p.Lc;
+    if (p.nsplit > 1) {
+        const size_t need = (size_t)p.nsplit * H * (D + 2) * sizeof(float);
+        if (!workspace || workspace_bytes < need) return Q4_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return Q4_ERR_ALIGN;
+        p.ws_o = (float *)workspace;
+        p.ws_m = p.ws_o + (size_t)p.nsplit * H * D;
+        p.ws_l = p.ws_m + (size_t)p.nsplit * H;
+    }
+    if (q4::attn_smem_bytes(D, H / Hkv, p.Lc) > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;
+    Q4_TRY(kernel_err_ptr(&p.err));
+    p.wait_cycles = g_wait_cycles;
+    cudaGetLastError();
+    if (q4::launch_attn(p, stream) != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
+    return Q4_OK;
 }
 
 extern "C" q4_status q4_debug_wait_limits(int64_t barrier_polls, int32_t barrier_extra, int64_t copy_wait_cycles,

@@ -6,6 +6,7 @@
 // inferencelayer: q1_rp4_repack_src, the ROWPACK4 layout).  Here each 16-row x
 // 128-column tile chunk becomes one contiguous record whose 16-byte lanes are
 // exactly the tensor-core operand fragments of the kernel's warps.
+#include <math.h>
 #include <string.h>
 
 #include "../../include/q4gemv.h"
@@ -422,5 +423,21 @@ extern "C" q4_status q4_unpack_q4_k(const void *host_packed, size_t packed_bytes
             sb[3] = (uint8_t)(dm >> 8);
         }
     });
+    return Q4_OK;
+}
+
+// RoPE tables (honeycrisp/mod.rs, attn_state: theta = pos / rope_theta^(2j /
+// head_dim) for j < head_dim / 2), computed in double and rounded to fp32.
+extern "C" q4_status q4_rope_table(int32_t max_seq, int32_t D, double rope_theta, float *host_cos,
+                                   float *host_sin) {
+    if (!host_cos || !host_sin) return Q4_ERR_NULL;
+    if (max_seq < 1 || max_seq > (1 << 24) || D < 2 || D % 2 != 0 || !(rope_theta > 0.0)) return Q4_ERR_SHAPE;
+    const int half = D / 2;
+    for (int64_t p = 0; p < max_seq; ++p)
+        for (int j = 0; j < half; ++j) {
+            const double th = (double)p / pow(rope_theta, 2.0 * j / D);
+            host_cos[p * half + j] = (float)cos(th);
+            host_sin[p * half + j] = (float)sin(th);
+        }
     return Q4_OK;
 }

@@ -326,6 +326,43 @@ q4_status q4_debug_wait_limits(int64_t barrier_polls, int32_t barrier_extra, int
 q4_status q4_argmax_noalloc(const q4_weight *W, const float *x, const float *gamma, float eps,
                             int32_t nb, int32_t *idx, float *val, float *logits, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- attention
+ * Decode attention of one token (honeycrisp/mod.rs: attn_state, gpu_attention
+ * and the fused RoPE + KV-append + SDPA dispatch of
+ * forward_decode_fused_layers), one call on `stream`:
+ *  1. with tables, q (every head) and k_new (every kv head) are rotated by
+ *     the tables' row `position`: element j pairs with element j + D/2,
+ *     (a, b) -> (a c - b s, b c + a s);
+ *  2. k_new (rotated) and v_new are written to row `position` of the caches;
+ *  3. the attended positions are [lo, position + 1), lo = max(0, position + 1
+ *     - window) for window > 0, else 0;
+ *  4. query head h reads kv head h / (H / Hkv); out_h = sum_t p_t v_t with p
+ *     the softmax over t of scale * q_h . k_t.
+ * Arguments (device pointers, fp32, 16-byte aligned, row-major):
+ *   q [H][D], k_new and v_new [Hkv][D]; k_cache and v_cache [Hkv][max_seq][D]
+ *   (row `position` is written, rows >= position + 1 are never read); rope_cos
+ *   and rope_sin [max_seq][D/2] or both NULL (no rotation; q4_rope_table
+ *   fills them); out [H][D].
+ * Supported: D = 64 with H / Hkv in {1, 2, 4, 8, 16}, D = 128 with H / Hkv
+ * in {1, 2, 4, 8}, else Q4_ERR_UNSUPPORTED; 0 <= position < max_seq <= 2^24
+ * and window >= 0, else Q4_ERR_SHAPE.
+ * Workspace: a device buffer of q4_attn_workspace_bytes(H, D, max_seq)
+ * bytes (16-byte aligned) holds the sequence chunks' partial results when
+ * the attended positions are split over several chunks; it may be NULL when
+ * they are not (Q4_ERR_WORKSPACE if it is needed and missing or short).
+ * The caller owns every buffer; out must not overlap the inputs.  Results
+ * do not depend on run-to-run scheduling (chunks are folded in order). */
+size_t q4_attn_workspace_bytes(int32_t H, int32_t D, int32_t max_seq);
+q4_status q4_attn_decode(const float *q, const float *k_new, const float *v_new, float *k_cache, float *v_cache,
+                         int32_t max_seq, int32_t position, int32_t H, int32_t Hkv, int32_t D, int32_t window,
+                         float scale, const float *rope_cos, const float *rope_sin, float *out, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
+/* Host: RoPE tables cos and sin [max_seq][D/2] (fp32, computed in double) of
+ * the angle pos / rope_theta^(2j/D) (honeycrisp/mod.rs, attn_state).  D even,
+ * rope_theta > 0, 1 <= max_seq <= 2^24, else Q4_ERR_SHAPE. */
+q4_status q4_rope_table(int32_t max_seq, int32_t D, double rope_theta, float *host_cos, float *host_sin);
+
 /* Launch plan the library uses for a GEMV-shaped call (host-only; exposed
  * for tests and tuning).  tiles: 16-row tiles of the launch, chunks: 128-k
  * chunks per row, pairs: 1 when tiles come in gate/up pairs, num_sms:

@@ -292,6 +292,49 @@ def test_q1_rejects_partial_superblocks():
     assert L.q4_gemv(ctypes.byref(W), A, None, 1, A + 4096, None) == 2
 
 
+def test_rope_table_host():
+    import oracle
+    c, s = q4.rope_table(300, 64, 10000.0)
+    co, so = oracle.rope_table(300, 64, 10000.0)
+    assert np.abs(c - co).max() <= 6e-8 and np.abs(s - so).max() <= 6e-8
+    L = q4.lib()
+    buf = np.zeros(64, np.float32)
+    assert L.q4_rope_table(4, 7, 10000.0, buf.ctypes.data, buf.ctypes.data) == 2
+    assert L.q4_rope_table(4, 8, 0.0, buf.ctypes.data, buf.ctypes.data) == 2
+    assert L.q4_rope_table(4, 8, 10000.0, None, buf.ctypes.data) == 1
+
+
+def test_attn_workspace_bytes():
+    L = q4.lib()
+    assert L.q4_attn_workspace_bytes(32, 64, 4096) == 256 * 32 * 66 * 4
+    assert L.q4_attn_workspace_bytes(32, 96, 4096) == 0 and L.q4_attn_workspace_bytes(0, 64, 16) == 0
+
+
+@pytest.mark.parametrize("case,expect", [("ok_shape_g3", 4), ("d96", 4), ("pos_past", 2), ("neg_window", 2),
+                                         ("null_q", 1), ("one_table", 1), ("misaligned_q", 3)])
+def test_attn_validation(case, expect):
+    # every case fails before any CUDA call (fake 16-byte aligned addresses)
+    L = q4.lib()
+    H, Hkv, D, ms, pos, win = 32, 8, 64, 128, 5, 0
+    q, cs, sn = A, A, A
+    if case == "ok_shape_g3":
+        H, Hkv = 9, 3
+    elif case == "d96":
+        D = 96
+    elif case == "pos_past":
+        pos = ms
+    elif case == "neg_window":
+        win = -1
+    elif case == "null_q":
+        q = None
+    elif case == "one_table":
+        sn = None
+    elif case == "misaligned_q":
+        q = A + 4
+    st = L.q4_attn_decode(q, A, A, A, A, ms, pos, H, Hkv, D, win, 0.125, cs, sn, A, A, 1 << 20, None)
+    assert st == expect
+
+
 def test_repack_validation():
     L = q4.lib()
     buf = np.zeros(4096, np.uint8)
