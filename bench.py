@@ -524,7 +524,7 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
         qa = torch.randn(H_, D_, device=device)
         kn_, vn_ = torch.randn(Hkv_, D_, device=device), torch.randn(Hkv_, D_, device=device)
         oa = torch.empty(H_, D_, device=device)
-        ws = torch.empty(int(q4.lib().q4_attn_workspace_bytes(H_, D_, ctx)), dtype=torch.uint8, device=device)
+        ws = torch.zeros(int(q4.lib().q4_attn_workspace_bytes(H_, D_, ctx)), dtype=torch.uint8, device=device)
         t = bench_calls(caches, lambda kv: q4.q4_attn_decode(qa, kn_, vn_, kv[0], kv[1], ctx - 1, 0, None,
                                                             rope=tables, out=oa, workspace=ws))
         gbs = kv_bytes / t / 1e9

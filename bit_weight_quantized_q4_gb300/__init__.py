@@ -598,8 +598,8 @@ def q4_attn_decode(q, k_new, v_new, k_cache, v_cache, position: int, window: int
     else:
         _dev_buf(out, "out", torch.float32, (H, D), dev)
     wsb = int(lib().q4_attn_workspace_bytes(H, D, max_seq))
-    if workspace is None:
-        workspace = torch.empty(max(16, wsb), dtype=torch.uint8, device=dev)
+    if workspace is None:  # zero-filled: its split counters start at zero
+        workspace = torch.zeros(max(16, wsb), dtype=torch.uint8, device=dev)
     else:
         _dev_buf(workspace, "workspace", torch.uint8, None, dev, min_numel=wsb)
     if scale is None:

@@ -5,11 +5,14 @@
 // of scale * q K^T over the attended positions times V.
 //
 // The work is HBM-bound on the cache rows.  CTA (s, hk) takes kv head hk and
-// the s-th chunk of the attended positions: its K and V rows are contiguous
-// in the cache, so two TMA bulk copies bring them into shared memory (each on
-// its own mbarrier: the scores start while V is still arriving), and every
-// query head of the group reuses them.  Chunks are folded in a second pass
-// (their maxima and sums, in chunk order) unless there is only one.
+// the s-th split of the attended positions, about one CTA per SM slot.  Its K
+// and V rows are contiguous in the cache: it walks them in sub-chunks of LS
+// positions through a ring of shared-memory stages that TMA bulk copies fill
+// (K and V on their own mbarriers, two stages ahead), each warp keeping a
+// running softmax per head over its positions (flash decoding); every query
+// head of the group reuses each row.  The last split of a kv head to finish folds the splits' shares in
+// split order: one launch, and a result that does not depend on the order in
+// which the CTAs ran.
 #include "gemv_launch.cuh"
 
 namespace q4 {
@@ -63,41 +66,64 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
 }
 
 constexpr int kAttnWarps = 8;
+constexpr int kAttnStages = 2;  // ring stages of K and V sub-chunks
 
+// Positions per sub-chunk: a stage holds LS rows of K and LS rows of V.
+Q4_HD constexpr int attn_sub(int D) { return D == 64 ? 64 : 32; }
+
+// Shared memory of a CTA: 2 mbarriers per stage (64 bytes in all), the ring
+// (per stage LS rows of K, then of V; at the end it holds the fold weights),
+// the warps' outputs [NW][G * D], their running maxima and sums [NW][G], the
+// fold's sums [G] and the last-split flag.
+//
+// Each warp keeps its own running softmax over the positions it scores (per
+// head: maximum, sum, and the output, rescaled whenever the maximum grows), so
+// a sub-chunk needs one CTA barrier, the one that frees its stage; the warps'
+// states are merged at the end.
 template <int D, int G>
-__global__ void __launch_bounds__(kAttnWarps * 32, 1) q4attn_split_kernel(const __grid_constant__ AttnParams p) {
-    constexpr int DL = D / 32, P = 32 / G, NW = kAttnWarps;
+__global__ void __launch_bounds__(kAttnWarps * 32, (G * D <= 512 ? 2 : 1))
+    q4attn_split_kernel(const __grid_constant__ AttnParams p) {
+    constexpr int DL = D / 32, P = 32 / G, NW = kAttnWarps, S = kAttnStages, LS = attn_sub(D);
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, hk = blockIdx.y;
-    const int Lc = p.Lc;
-    const int t0 = p.lo + split * Lc;
-    const int n = min(Lc, p.total - t0);  // >= 1
-    const bool owner = t0 + n == p.total;  // this chunk ends with the new token
-    const uint32_t barK = smem_u32(smem), barV = barK + 8;
-    float *Ks = reinterpret_cast<float *>(smem + 16);
-    float *Vs = Ks + (size_t)Lc * D;
-    float *sc = Vs + (size_t)Lc * D;  // [G][Lc]: scores, then exp(score - max)
-    float *red = sc + (size_t)G * Lc;  // [NW][G * D]
-    float *stat = red + NW * G * D;   // max[G], sum[G]
+    const int per = p.Lc;  // positions of each split (the last may have fewer)
+    const int t0 = p.lo + split * per;
+    const int n = min(per, p.total - t0);  // >= 1
+    const int nsub = (n + LS - 1) / LS;
+    const bool owner = t0 + n == p.total;  // this split ends with the new token
+    const uint32_t bars = smem_u32(smem);  // stage s: K barrier at bars + 16 s, V barrier 8 bytes on
+    float *ring = reinterpret_cast<float *>(smem + 64);
+    float *red = ring + (size_t)S * 2 * LS * D;
+    float *wm = red + NW * G * D, *wl = wm + NW * G, *Lg = wl + NW * G;
+    int *flag = reinterpret_cast<int *>(Lg + G);
     const size_t row0 = ((size_t)hk * p.max_seq + t0) * D;
+    const uint64_t pol = evict_first_policy();
 
+    // sub-chunk j's K and V rows into stage j % S (thread 0 only)
+    auto issue = [&](int j) {
+        const int st = j % S, rows = min(LS, n - j * LS);
+        const uint32_t bytes = (uint32_t)rows * D * 4;
+        float *kst = ring + (size_t)st * 2 * LS * D;
+        const uint32_t bk = bars + 16 * st, bv = bk + 8;
+        mbar_expect_tx(bk, bytes + (j == 0 ? p.extra_tx : 0));  // extra_tx: testing the give-up path only
+        bulk_g2s(smem_u32(kst), p.k_cache + row0 + (size_t)j * LS * D, bytes, bk, pol);
+        mbar_expect_tx(bv, bytes);
+        bulk_g2s(smem_u32(kst + LS * D), p.v_cache + row0 + (size_t)j * LS * D, bytes, bv, pol);
+    };
     if (tid == 0) {
-        mbar_init(barK, 1);
-        mbar_init(barV, 1);
+        for (int st = 0; st < S; ++st) {
+            mbar_init(bars + 16 * st, 1);
+            mbar_init(bars + 16 * st + 8, 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    if (tid == 0) {
-        const uint32_t bytes = (uint32_t)n * D * 4;
-        const uint64_t pol = evict_first_policy();
-        mbar_expect_tx(barK, bytes);
-        bulk_g2s(smem_u32(Ks), p.k_cache + row0, bytes, barK, pol);
-        mbar_expect_tx(barV, bytes);
-        bulk_g2s(smem_u32(Vs), p.v_cache + row0, bytes, barV, pol);
-    }
-    // while the rows arrive: this group's query heads (rotated) in registers,
-    // and for the last chunk the new token's k (rotated) and v
+    if (tid == 0)
+        for (int j = 0; j < min(S, nsub); ++j) issue(j);
+
+    // while the rows arrive: the group's query heads (rotated) in registers,
+    // and for the split with the new token its k (rotated) and v
     const float *cosr = p.rope_cos ? p.rope_cos + (size_t)p.position * (D / 2) : nullptr;
     const float *sinr = p.rope_sin ? p.rope_sin + (size_t)p.position * (D / 2) : nullptr;
     float qr[G][DL];
@@ -111,173 +137,230 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1) q4attn_split_kernel(const 
         load_row<DL>(kv, (warp == 0 ? p.k_new : p.v_new) + (size_t)hk * D + lane * DL);
         if (warp == 0 && cosr) rope_lane<DL>(kv, cosr, sinr, lane);
     }
-
-    // K rows in
-    bool ok = mbar_wait(barK, 0, p.wait_cycles);
-    if (!__syncthreads_and(ok)) {
-        // gave up: record it, and let the copies land before the CTA leaves
-        if (tid == 0) {
-            atomicExch(p.err, 3);
-            mbar_wait(barK, 0, kWaitCycles);
-            mbar_wait(barV, 0, kWaitCycles);
-        }
-        __syncthreads();
-        return;
-    }
-    if (owner && warp == 0) {  // append k: the cache, and this chunk's copy of it
-#pragma unroll
-        for (int j = 0; j < DL; ++j) {
-            Ks[(size_t)(n - 1) * D + lane * DL + j] = kv[j];
-            p.k_cache[row0 + (size_t)(n - 1) * D + lane * DL + j] = kv[j];
-        }
-    }
-    __syncthreads();
-
-    // scores: a warp takes P positions at a time, lane l dims l*DL.., every
-    // head of the group; one transpose-reduce gives lane l the score of
-    // position l / G, head l % G
-    for (int i = warp; i * P < n; i += NW) {
-        float v[32];
-#pragma unroll
-        for (int pp = 0; pp < P; ++pp) {
-            const int tl = i * P + pp;
-            float kr[DL];
-            if (tl < n) {
-                load_row<DL>(kr, Ks + (size_t)tl * D + lane * DL);
-            } else {
-#pragma unroll
-                for (int j = 0; j < DL; ++j) kr[j] = 0.f;
-            }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float s = 0.f;
-#pragma unroll
-                for (int j = 0; j < DL; ++j) s = fmaf(qr[g][j], kr[j], s);
-                v[pp * G + g] = s;
-            }
-        }
-        const float s = transpose_reduce(v, lane);
-        const int tl = i * P + lane / G, g = lane % G;
-        if (tl < n) sc[(size_t)g * Lc + tl] = s * p.scale;
-    }
-    __syncthreads();
-
-    // softmax of each head over the chunk: its maximum, exp(s - max), sum
-    for (int g = warp; g < G; g += NW) {
-        float* row = sc + (size_t)g * Lc;
-        float mx = -INFINITY;
-        for (int t = lane; t < n; t += 32) mx = fmaxf(mx, row[t]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float sum = 0.f;
-        for (int t = lane; t < n; t += 32) {
-            const float e = expf(row[t] - mx);
-            row[t] = e;
-            sum += e;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) {
-            stat[g] = mx;
-            stat[G + g] = sum;
-        }
-    }
-
-    // V rows in (usually long since), and the new token's v
-    ok = mbar_wait(barV, 0, p.wait_cycles);
-    if (!__syncthreads_and(ok)) {
-        if (tid == 0) {
-            atomicExch(p.err, 3);
-            mbar_wait(barV, 0, kWaitCycles);
-        }
-        __syncthreads();
-        return;
-    }
-    if (owner && warp == 1) {
-#pragma unroll
-        for (int j = 0; j < DL; ++j) {
-            Vs[(size_t)(n - 1) * D + lane * DL + j] = kv[j];
-            p.v_cache[row0 + (size_t)(n - 1) * D + lane * DL + j] = kv[j];
-        }
-    }
-    __syncthreads();
-
-    // sum_t p_t v_t: warp w takes positions w, w + NW, ...; lane l dims
-    // l*DL.. of every head; then the warps' shares are added in warp order
+    // this warp's running softmax: lane l keeps head l % G's maximum and sum
+    // (the same in every lane of that head), and every lane the output share
+    // of its dims for every head
+    float mh = -INFINITY, lh = 0.f;
     float acc[G][DL];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int j = 0; j < DL; ++j) acc[g][j] = 0.f;
-    for (int tl = warp; tl < n; tl += NW) {
-        float vr[DL];
-        load_row<DL>(vr, Vs + (size_t)tl * D + lane * DL);
+        for (int e = 0; e < DL; ++e) acc[g][e] = 0.f;
+
+    bool ok = true;
+    int waited = 0;  // sub-chunks whose copies have landed
+    for (int j = 0; j < nsub; ++j) {
+        const int st = j % S, rows = min(LS, n - j * LS);
+        const uint32_t par = (uint32_t)(j / S) & 1u;
+        float *Ks = ring + (size_t)st * 2 * LS * D, *Vs = Ks + LS * D;
+        bool mine = mbar_wait(bars + 16 * st, par, p.wait_cycles);
+        mine = mine && mbar_wait(bars + 16 * st + 8, par, p.wait_cycles);
+        ok = __syncthreads_and(mine);
+        if (!ok) break;
+        waited = j + 1;
+        if (owner && j == nsub - 1) {  // append k and v: the caches, and this stage's copies
+            if (warp < 2) {
+                float *srow = (warp == 0 ? Ks : Vs) + (size_t)(rows - 1) * D + lane * DL;
+                float *grow = (warp == 0 ? p.k_cache : p.v_cache) + row0 + (size_t)(n - 1) * D + lane * DL;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float pg = sc[(size_t)g * Lc + tl];
+                for (int e = 0; e < DL; ++e) {
+                    srow[e] = kv[e];
+                    grow[e] = kv[e];
+                }
+            }
+            __syncthreads();
+        }
+        for (int i = warp; i * P < rows; i += NW) {
+            // scores of positions i*P .. i*P+P-1 for every head: lane l ends
+            // with position l / G, head l % G
+            float v[32];
 #pragma unroll
-            for (int j = 0; j < DL; ++j) acc[g][j] = fmaf(pg, vr[j], acc[g][j]);
+            for (int pp = 0; pp < P; ++pp) {
+                const int r = i * P + pp;
+                float kr[DL];
+                if (r < rows) {
+                    load_row<DL>(kr, Ks + (size_t)r * D + lane * DL);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < DL; ++e) kr[e] = 0.f;
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int e = 0; e < DL; ++e) s = fmaf(qr[g][e], kr[e], s);
+                    v[pp * G + g] = s;
+                }
+            }
+            const float t = transpose_reduce(v, lane);
+            const bool valid = i * P + lane / G < rows;
+            const float s = valid ? t * p.scale : -INFINITY;
+            // the head's maximum over these positions (lanes l, l ^ G, ...),
+            // the factor that rescales what came before, exp(s - max), sum
+            float mx = s;
+#pragma unroll
+            for (int o = G; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float mnew = fmaxf(mh, mx);  // finite: position i*P is valid
+            const float alpha = expf(mh - mnew);  // 0 the first time
+            const float e = valid ? expf(s - mnew) : 0.f;
+            float sum = e;
+#pragma unroll
+            for (int o = G; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            lh = fmaf(lh, alpha, sum);
+            mh = mnew;
+            // output: rescale each head (lane g holds head g's factor), then
+            // add these positions' rows of V weighted by their exp(s - max)
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float a = __shfl_sync(0xffffffffu, alpha, g);
+#pragma unroll
+                for (int q2 = 0; q2 < DL; ++q2) acc[g][q2] *= a;
+            }
+#pragma unroll
+            for (int pp = 0; pp < P; ++pp) {
+                const int r = i * P + pp;
+                if (r < rows) {  // warp-uniform
+                    float vr[DL];
+                    load_row<DL>(vr, Vs + (size_t)r * D + lane * DL);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float w = __shfl_sync(0xffffffffu, e, pp * G + g);
+#pragma unroll
+                        for (int q2 = 0; q2 < DL; ++q2) acc[g][q2] = fmaf(w, vr[q2], acc[g][q2]);
+                    }
+                }
+            }
+        }
+        __syncthreads();  // the stage is free again
+        if (tid == 0 && j + S < nsub) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(j + S);
         }
     }
+    if (!ok) {
+        // a wait gave up: record it and let the copies in flight land before
+        // the CTA goes on (its share is not valid; it still joins the fold
+        // count, so the count is right for the next call)
+        if (tid == 0) {
+            atomicExch(p.err, 3);
+            for (int j = waited; j < min(nsub, waited + S); ++j) {
+                const uint32_t par = (uint32_t)(j / S) & 1u;
+                mbar_wait(bars + 16 * (j % S), par, kWaitCycles);
+                mbar_wait(bars + 16 * (j % S) + 8, par, kWaitCycles);
+            }
+        }
+        __syncthreads();
+    }
+
+    // merge the warps, in warp order: M = max_w m_w, L = sum_w l_w e^(m_w - M),
+    // o = sum_w o_w e^(m_w - M) (a warp without positions has m_w = -inf)
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int j = 0; j < DL; ++j) red[(size_t)warp * G * D + g * D + lane * DL + j] = acc[g][j];
+        for (int e = 0; e < DL; ++e) red[(size_t)warp * G * D + g * D + lane * DL + e] = acc[g][e];
+    if (lane < G) {
+        wm[warp * G + lane] = mh;
+        wl[warp * G + lane] = lh;
+    }
     __syncthreads();
     for (int idx = tid; idx < G * D; idx += NW * 32) {
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) o += red[(size_t)w * G * D + idx];
         const int g = idx / D, d = idx - g * D, hq = hk * G + g;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w * G + g]);
+        float o = 0.f, L = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float f = expf(wm[w * G + g] - M);
+            o = fmaf(red[(size_t)w * G * D + idx], f, o);
+            L = fmaf(wl[w * G + g], f, L);
+        }
         if (p.nsplit == 1) {
-            p.out[(size_t)hq * D + d] = o / stat[G + g];
+            p.out[(size_t)hq * D + d] = o / L;
         } else {
             p.ws_o[((size_t)split * p.H + hq) * D + d] = o;
             if (d == 0) {
-                p.ws_m[(size_t)split * p.H + hq] = stat[g];
-                p.ws_l[(size_t)split * p.H + hq] = stat[G + g];
+                p.ws_m[(size_t)split * p.H + hq] = M;
+                p.ws_l[(size_t)split * p.H + hq] = L;
             }
         }
     }
-}
+    if (p.nsplit == 1) return;
 
-// Fold the chunks of query head blockIdx.x: with M the largest chunk maximum,
-// out = sum_s o_s e^(m_s - M) / sum_s l_s e^(m_s - M), in chunk order.
-__global__ void q4attn_combine_kernel(const __grid_constant__ AttnParams p) {
-    const int hq = blockIdx.x, D = p.D;
-    float M = -INFINITY;
-    for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, p.ws_m[(size_t)s * p.H + hq]);
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float L = 0.f, o = 0.f;
-        for (int s = 0; s < p.nsplit; ++s) {
-            const float w = expf(p.ws_m[(size_t)s * p.H + hq] - M);
-            L = fmaf(p.ws_l[(size_t)s * p.H + hq], w, L);
-            o = fmaf(p.ws_o[((size_t)s * p.H + hq) * D + d], w, o);
+    // the last split of this kv head to finish folds every split's share in
+    // split order: out = sum_s o_s e^(m_s - M) / sum_s l_s e^(m_s - M)
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) *flag = atomicAdd(p.ws_count + hk, 1) == p.nsplit - 1;
+    __syncthreads();
+    if (!*flag) return;
+    __threadfence();
+    float *wts = ring;  // [nsplit][G]: the splits' weights e^(m_s - M)
+    for (int g = warp; g < G; g += NW) {
+        const int hq = hk * G + g;
+        float M = -INFINITY;
+        for (int s2 = lane; s2 < p.nsplit; s2 += 32) M = fmaxf(M, __ldcg(p.ws_m + (size_t)s2 * p.H + hq));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.f;
+        for (int s2 = lane; s2 < p.nsplit; s2 += 32) {
+            const float w = expf(__ldcg(p.ws_m + (size_t)s2 * p.H + hq) - M);
+            wts[s2 * G + g] = w;
+            L = fmaf(__ldcg(p.ws_l + (size_t)s2 * p.H + hq), w, L);
         }
-        p.out[(size_t)hq * D + d] = o / L;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (lane == 0) Lg[g] = L;
     }
+    __syncthreads();
+    // warp w adds the splits w, w + NW, ... for every output (lane l: outputs
+    // l, l + 32, ...), all their loads in flight together; then the warps'
+    // sums are added in warp order
+    constexpr int OPL = G * D / 32;
+    float part[OPL];
+#pragma unroll
+    for (int k = 0; k < OPL; ++k) part[k] = 0.f;
+    for (int s2 = warp; s2 < p.nsplit; s2 += NW) {
+        const float *src = p.ws_o + ((size_t)s2 * p.H + hk * G) * D;
+#pragma unroll
+        for (int k = 0; k < OPL; ++k) {
+            const int idx = lane + 32 * k;
+            part[k] = fmaf(__ldcg(src + idx), wts[s2 * G + idx / D], part[k]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < OPL; ++k) red[(size_t)warp * G * D + lane + 32 * k] = part[k];
+    __syncthreads();
+    for (int idx = tid; idx < G * D; idx += NW * 32) {
+        const int g = idx / D;
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) o += red[(size_t)w * G * D + idx];
+        p.out[(size_t)(hk * G) * D + idx] = o / Lg[g];
+    }
+    if (tid == 0) p.ws_count[hk] = 0;  // zero again for the next call
 }
 
 }  // namespace dev
 
-size_t attn_smem_bytes(int D, int G, int Lc) {
-    return 16 + (size_t)2 * Lc * D * 4 + (size_t)G * Lc * 4 + (size_t)dev::kAttnWarps * G * D * 4 + 2 * G * 4;
+size_t attn_smem_bytes(int D, int G) {
+    const int LS = dev::attn_sub(D), NW = dev::kAttnWarps;
+    return 64 + (size_t)dev::kAttnStages * 2 * LS * D * 4 + (size_t)NW * G * D * 4 + (size_t)(2 * NW * G + G) * 4 + 16;
 }
+// splits one fold can weigh: its weights [nsplit][G] reuse the ring
+int attn_max_splits(int D, int G) { return dev::kAttnStages * 2 * dev::attn_sub(D) * D / G; }
+int attn_sub_chunk(int D) { return dev::attn_sub(D); }
+int attn_ctas_per_sm(int D, int G) { return G * D <= 512 ? 2 : 1; }
 
 template <int D, int G>
 static int launch_attn_dg(const AttnParams &p, cudaStream_t stream) {
     auto kern = dev::q4attn_split_kernel<D, G>;
     static size_t smem_set[64] = {0};
-    const size_t smem = attn_smem_bytes(D, G, p.Lc);
+    const size_t smem = attn_smem_bytes(D, G);
     if (!raise_smem(kern, smem, smem_set)) return -1;
     dim3 grid(p.nsplit, p.Hkv);
     kern<<<grid, dev::kAttnWarps * 32, smem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return -1;
-    if (p.nsplit > 1) {
-        dev::q4attn_combine_kernel<<<p.H, D, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return -1;
-    }
-    return 0;
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 int launch_attn(const AttnParams &p, void *stream_) {

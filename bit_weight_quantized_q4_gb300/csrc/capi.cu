@@ -632,7 +632,9 @@ extern "C" q4_status q4_decode_check(const void *workspace, cudaStream_t stream)
 // ---------------------------------------------------------------- attention
 
 namespace {
-constexpr int kAttnMinChunk = 16;  // positions per chunk at least
+constexpr int kAttnMinChunk = 16;  // positions per split at least (bounds the workspace)
+// the per-kv-head split counters at the start of the workspace
+inline size_t attn_count_bytes(int32_t H) { return ((size_t)H * sizeof(int) + 15) / 16 * 16; }
 
 bool attn_geometry_ok(int32_t H, int32_t Hkv, int32_t D) {
     if (Hkv < 1 || H < Hkv || H % Hkv != 0 || H > 4096) return false;
@@ -646,7 +648,7 @@ bool attn_geometry_ok(int32_t H, int32_t Hkv, int32_t D) {
 extern "C" size_t q4_attn_workspace_bytes(int32_t H, int32_t D, int32_t max_seq) {
     if (H < 1 || max_seq < 1 || (D != 64 && D != 128)) return 0;
     const size_t splits = ((size_t)max_seq + kAttnMinChunk - 1) / kAttnMinChunk;
-    return splits * (size_t)H * (size_t)(D + 2) * sizeof(float);
+    return attn_count_bytes(H) + splits * (size_t)H * (size_t)(D + 2) * sizeof(float);
 }
 
 extern "C" q4_status q4_attn_decode(const float *q, const float *k_new, const float *v_new, float *k_cache,
@@ -687,24 +689,28 @@ extern "C" q4_status q4_attn_decode(const float *q, const float *k_new, const fl
     p.scale = scale;
     p.total = position + 1;
     p.lo = (window > 0 && p.total > window) ? p.total - window : 0;
-    // about one CTA per SM over all kv heads, chunks of kAttnMinChunk..Lmax
-    // positions (both the chunk's K and V rows are staged in shared memory)
+    // splits: about one CTA per SM slot over all kv heads, each at least one
+    // pipeline stage of positions
     const int len = p.total - p.lo;
-    const int target = std::max(1, sms / Hkv);
-    const int lmax = D == 64 ? 256 : 128;
-    p.Lc = std::min(lmax, std::max(kAttnMinChunk, (len + target - 1) / target));
+    const int G = H / Hkv;
+    const int LS = q4::attn_sub_chunk(D);
+    const int target = std::max(1, q4::attn_ctas_per_sm(D, G) * sms / Hkv);
+    int ns = std::max(1, std::min(std::min(target, q4::attn_max_splits(D, G)), (len + LS - 1) / LS));
+    p.Lc = (len + ns - 1) / ns;
     p.nsplit = (len + p.Lc - 1) / p.Lc;
     if (p.nsplit > 1) {
-        const size_t need = (size_t)p.nsplit * H * (D + 2) * sizeof(float);
+        const size_t need = attn_count_bytes(H) + (size_t)p.nsplit * H * (D + 2) * sizeof(float);
         if (!workspace || workspace_bytes < need) return Q4_ERR_WORKSPACE;
         if (!aligned16(workspace)) return Q4_ERR_ALIGN;
-        p.ws_o = (float *)workspace;
+        p.ws_count = (int *)workspace;
+        p.ws_o = (float *)((char *)workspace + attn_count_bytes(H));
         p.ws_m = p.ws_o + (size_t)p.nsplit * H * D;
         p.ws_l = p.ws_m + (size_t)p.nsplit * H;
     }
-    if (q4::attn_smem_bytes(D, H / Hkv, p.Lc) > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;
+    if (q4::attn_smem_bytes(D, G) > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;
     Q4_TRY(kernel_err_ptr(&p.err));
     p.wait_cycles = g_wait_cycles;
+    p.extra_tx = g_extra_tx;
     cudaGetLastError();
     if (q4::launch_attn(p, stream) != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
     return Q4_OK;

@@ -326,20 +326,27 @@ inline size_t step_smem_bytes(int fmt, int nb, int TGmax, int Kmax, int SWmax, i
 
 // Launchers, one per kernel instantiation family (defined in the .cu files).
 // Decode attention (attn_kernel.cu): one token against an f32 KV cache.
-// CTA (s, hk) takes kv head hk and chunk s of the attended positions
-// [lo, total) of Lc positions; the nsplit chunks are folded afterwards.
+// CTA (s, hk) takes kv head hk and split s -- Lc positions -- of the attended
+// positions [lo, total); with nsplit > 1 the last split of each kv head to
+// finish folds the splits' shares (ws_count[hk] counts them, and is zero
+// again when the call ends).
 struct AttnParams {
     const float *q, *k_new, *v_new;   // [H][D], [Hkv][D], [Hkv][D]
     float *k_cache, *v_cache;         // [Hkv][max_seq][D]
     const float *rope_cos, *rope_sin; // [max_seq][D/2] or nullptr
     float *out;                       // [H][D]
-    float *ws_o, *ws_m, *ws_l;        // chunk partials [nsplit][H][D], maxima and sums [nsplit][H]
+    float *ws_o, *ws_m, *ws_l;        // split shares [nsplit][H][D], maxima and sums [nsplit][H]
+    int *ws_count;                    // [Hkv] splits finished (zero between calls)
     int *err;                         // set nonzero if a copy wait gave up
-    long long wait_cycles;
+    long long wait_cycles;            // bound of one copy wait (SM clock cycles)
+    int extra_tx;                     // bytes the first K copy expects beyond its rows (0; testing only)
     int max_seq, position, H, Hkv, D, lo, total, Lc, nsplit;
     float scale;
 };
-size_t attn_smem_bytes(int D, int G, int Lc);
+size_t attn_smem_bytes(int D, int G);
+int attn_sub_chunk(int D);         // positions per pipeline stage
+int attn_ctas_per_sm(int D, int G);
+int attn_max_splits(int D, int G);
 int launch_attn(const AttnParams &p, void *stream);
 
 int launch_gemv_q4_0(const GemvParams &p, const Plan &plan, void *stream);

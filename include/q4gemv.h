@@ -347,9 +347,12 @@ q4_status q4_argmax_noalloc(const q4_weight *W, const float *x, const float *gam
  * in {1, 2, 4, 8}, else Q4_ERR_UNSUPPORTED; 0 <= position < max_seq <= 2^24
  * and window >= 0, else Q4_ERR_SHAPE.
  * Workspace: a device buffer of q4_attn_workspace_bytes(H, D, max_seq)
- * bytes (16-byte aligned) holds the sequence chunks' partial results when
- * the attended positions are split over several chunks; it may be NULL when
- * they are not (Q4_ERR_WORKSPACE if it is needed and missing or short).
+ * bytes (16-byte aligned), zero-filled by the caller before its first use:
+ * it holds per-kv-head counters (every call leaves them zero) and the
+ * partial results of the splits of the attended positions.  It may be NULL
+ * when the call needs one split only (Q4_ERR_WORKSPACE if it is needed and
+ * missing or short).  Calls that share a workspace must not run at the same
+ * time.
  * The caller owns every buffer; out must not overlap the inputs.  Results
  * do not depend on run-to-run scheduling (chunks are folded in order). */
 size_t q4_attn_workspace_bytes(int32_t H, int32_t D, int32_t max_seq);

@@ -306,7 +306,7 @@ def test_rope_table_host():
 
 def test_attn_workspace_bytes():
     L = q4.lib()
-    assert L.q4_attn_workspace_bytes(32, 64, 4096) == 256 * 32 * 66 * 4
+    assert L.q4_attn_workspace_bytes(32, 64, 4096) == 128 + 256 * 32 * 66 * 4
     assert L.q4_attn_workspace_bytes(32, 96, 4096) == 0 and L.q4_attn_workspace_bytes(0, 64, 16) == 0
 
 

@@ -4,8 +4,8 @@ Every wait in the library's kernels is bounded.  Here each kind is made to
 run out on purpose through the library's testing hook
 (q4_debug_wait_limits): a grid barrier of the persistent decode step that
 expects one arrival more than there are CTAs, and a weight-copy stage of a
-per-call GEMV that expects 16 bytes more than its copies bring.  Neither
-faults or hangs: the kernel records the failure, waits (bounded) for its
+per-call GEMV (and of the decode attention) that expects 16 bytes more than
+its copies bring.  None faults or hangs: the kernel records the failure, waits (bounded) for its
 copies in flight and returns.  The check call then reports Q4_ERR_CUDA, and
 the next normal call gives the same bits as before."""
 import numpy as np
@@ -66,3 +66,25 @@ def test_copy_wait_gives_up_and_the_next_call_is_unchanged(q4):
     y1 = q4.q4_gemv(W, x)
     q4.q4_device_check()
     assert torch.equal(y1, y0)
+
+
+def test_attention_copy_wait_gives_up_and_the_next_call_is_unchanged(q4):
+    rng = np.random.default_rng(23)
+    H, Hkv, D, ms, pos = 32, 8, 64, 2048, 2047
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    q, kn, vn = T(rng.standard_normal((H, D))), T(rng.standard_normal((Hkv, D))), T(rng.standard_normal((Hkv, D)))
+    kc, vc = T(rng.standard_normal((Hkv, ms, D))), T(rng.standard_normal((Hkv, ms, D)))
+    ws = torch.zeros(int(q4.lib().q4_attn_workspace_bytes(H, D, ms)), dtype=torch.uint8, device="cuda")
+    o0 = q4.q4_attn_decode(q, kn, vn, kc, vc, pos, workspace=ws)
+    q4.q4_device_check()
+    q4.q4_debug_wait_limits(copy_wait_cycles=200000, copy_extra_bytes=16)
+    try:
+        q4.q4_attn_decode(q, kn, vn, kc, vc, pos, workspace=ws)
+        with pytest.raises(q4.Q4Error) as e:
+            q4.q4_device_check()
+        assert e.value.status == 6
+    finally:
+        q4.q4_debug_wait_limits()
+    # the split counters are zero again and the result is the same
+    assert torch.equal(q4.q4_attn_decode(q, kn, vn, kc, vc, pos, workspace=ws), o0)
+    q4.q4_device_check()
