@@ -51,7 +51,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-kernels", action="store_true", help="skip the per-shape kernel table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--gemv", metavar="FMT:N:K:NB", default=None,
-                    help="time one q4_gemv shape only (fmt q4_0 or affine; for profiling), then exit")
+                    help="time one q4_gemv shape only (fmt q4_0, affine, q8_0, q4_k or q1; for profiling), then exit")
+    ap.add_argument("--attn", metavar="H:HKV:D:CTX", default=None,
+                    help="time one q4_attn_decode shape only (the token at position CTX-1, RoPE on; for "
+                         "profiling), then exit")
     return ap.parse_args(argv)
 
 
@@ -173,11 +176,16 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: a profile summary taken on other sources is stale."""
+# the sources that define the persistent decode-step kernel and its launch
+STEP_SOURCES = ("capi.cu", "gemv_kernel.cuh", "gemv_launch.cuh", "gemv_q4_0.cu", "q4_internal.h")
+
+
+def kernel_source_hash(names=STEP_SOURCES) -> str:
+    """Hash of the CUDA sources of a kernel (by default the decode step's): a
+    profile summary taken on other sources is stale."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_weight_quantized_q4_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(names):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -549,12 +557,12 @@ def run_one_gemv(args) -> dict:
     q4.build()
     dev = torch.device("cuda:0")
     rng = np.random.default_rng(3)
-    if fmt == "q4_0":
-        H = wl.draw_q4_0(rng, n, k)
-        W = q4.Q4Weight.from_q4_0(H.blocks, n, k, dev)
-    else:
-        H = wl.draw_affine(rng, n, k)
-        W = q4.Q4Weight.from_affine(H.nib, H.s, H.m, n, k, dev)
+    H = wl._draw_fmt(fmt)(rng, n, k)
+    W = (q4.Q4Weight.from_affine(H.nib, H.s, H.m, n, k, dev) if fmt == "affine"
+         else q4.Q4Weight.from_q8_0(H.blocks8, n, k, dev) if fmt == "q8_0"
+         else q4.Q4Weight.from_q4_k(H.blocks_k, n, k, dev) if fmt == "q4_k"
+         else q4.Q4Weight.from_q1(H.blocks1, n, k, dev) if fmt == "q1"
+         else q4.Q4Weight.from_q4_0(H.blocks, n, k, dev))
     x = torch.from_numpy(wl.draw_x(rng, nb, k)).to(dev)
     y = torch.empty((nb, n), dtype=torch.float32, device=dev)
     for _ in range(args.warmup):
@@ -569,6 +577,41 @@ def run_one_gemv(args) -> dict:
     q4.q4_device_check()
     return {"gemv": args.gemv, "calls": args.steps, "us_per_call_warm_l2": round(e0.elapsed_time(e1) * 1e3 / args.steps, 3),
             "note": "one weight reused: warm L2 for matrices under 129 MB; the kernel table times cold weights"}
+
+
+def run_one_attn(args) -> dict:
+    """One decode-attention shape, `warmup` untimed then `steps` timed calls
+    on one pair of caches; for ncu captures."""
+    import torch
+
+    import bit_weight_quantized_q4_gb300 as q4
+    H, Hkv, D, ctx = (int(v) for v in args.attn.split(":"))
+    q4.build()
+    dev = torch.device("cuda:0")
+    g = torch.Generator(device=dev).manual_seed(5)
+    kc = torch.randn(Hkv, ctx, D, device=dev, generator=g)
+    vc = torch.randn(Hkv, ctx, D, device=dev, generator=g)
+    q = torch.randn(H, D, device=dev, generator=g)
+    kn, vn = torch.randn(Hkv, D, device=dev, generator=g), torch.randn(Hkv, D, device=dev, generator=g)
+    c, sn = q4.rope_table(ctx, D, 10000.0)
+    tables = (torch.from_numpy(c).to(dev), torch.from_numpy(sn).to(dev))
+    out = torch.empty(H, D, device=dev)
+    ws = torch.zeros(int(q4.lib().q4_attn_workspace_bytes(H, D, ctx)), dtype=torch.uint8, device=dev)
+    call = lambda: q4.q4_attn_decode(q, kn, vn, kc, vc, ctx - 1, 0, None, rope=tables, out=out, workspace=ws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    q4.q4_device_check()
+    kv_bytes = 2 * Hkv * ctx * D * 4
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    return {"attn": args.attn, "calls": args.steps, "us_per_call_warm_l2": round(us, 3), "kv_bytes": kv_bytes,
+            "note": "one pair of caches reused: warm L2 when they fit in 129 MB; the kernel table times cold caches"}
 
 
 def workload_config(args, wbytes: int, l2: int, world: int) -> dict:
@@ -794,6 +837,8 @@ def main(argv=None):
     rank, world, local = dist_env()
     if args.gemv:
         line = run_one_gemv(args) if rank == 0 else None
+    elif args.attn:
+        line = run_one_attn(args) if rank == 0 else None
     elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:

@@ -48,6 +48,28 @@ __device__ __forceinline__ void load_row(float (&x)[DL], const float *src) {
     }
 }
 
+// N consecutive floats of shared memory (N a power of two), in 16-byte loads
+// where they fit.
+template <int N>
+__device__ __forceinline__ void load_vec(float (&x)[N], const float *src) {
+    if constexpr (N >= 4) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(src + i);
+            x[i] = v.x;
+            x[i + 1] = v.y;
+            x[i + 2] = v.z;
+            x[i + 3] = v.w;
+        }
+    } else if constexpr (N == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(src);
+        x[0] = v.x;
+        x[1] = v.y;
+    } else {
+        x[0] = src[0];
+    }
+}
+
 // 32 partial sums per lane -> lane l holds the warp-wide sum of value l
 // (recursive halving: each round a lane keeps the half of its values whose
 // index bit matches its lane bit and adds its partner's share of it).
@@ -96,7 +118,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, (G * D <= 512 ? 2 : 1))
     float *ring = reinterpret_cast<float *>(smem + 64);
     float *red = ring + (size_t)S * 2 * LS * D;
     float *wm = red + NW * G * D, *wl = wm + NW * G, *Lg = wl + NW * G;
-    int *flag = reinterpret_cast<int *>(Lg + G);
+    float *eb = Lg + G, *ab = eb + NW * 32;  // per warp: this step's exp(s - max) and rescale factors
+    int *flag = reinterpret_cast<int *>(ab + NW * G);
     const size_t row0 = ((size_t)hk * p.max_seq + t0) * D;
     const uint64_t pol = evict_first_policy();
 
@@ -209,27 +232,34 @@ __global__ void __launch_bounds__(kAttnWarps * 32, (G * D <= 512 ? 2 : 1))
             lh = fmaf(lh, alpha, sum);
             mh = mnew;
             // output: rescale each head (lane g holds head g's factor), then
-            // add these positions' rows of V weighted by their exp(s - max)
+            // add these positions' rows of V weighted by their exp(s - max);
+            // both reach every lane through the warp's own shared-memory slots
+            float *ew = eb + warp * 32, *aw = ab + warp * G;
+            ew[lane] = e;
+            if (lane < G) aw[lane] = alpha;
+            __syncwarp();
+            {
+                float a[G];
+                load_vec<G>(a, aw);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float a = __shfl_sync(0xffffffffu, alpha, g);
+                for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int q2 = 0; q2 < DL; ++q2) acc[g][q2] *= a;
+                    for (int q2 = 0; q2 < DL; ++q2) acc[g][q2] *= a[g];
             }
 #pragma unroll
             for (int pp = 0; pp < P; ++pp) {
                 const int r = i * P + pp;
                 if (r < rows) {  // warp-uniform
-                    float vr[DL];
+                    float vr[DL], w[G];
                     load_row<DL>(vr, Vs + (size_t)r * D + lane * DL);
+                    load_vec<G>(w, ew + pp * G);
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float w = __shfl_sync(0xffffffffu, e, pp * G + g);
+                    for (int g = 0; g < G; ++g)
 #pragma unroll
-                        for (int q2 = 0; q2 < DL; ++q2) acc[g][q2] = fmaf(w, vr[q2], acc[g][q2]);
-                    }
+                        for (int q2 = 0; q2 < DL; ++q2) acc[g][q2] = fmaf(w[g], vr[q2], acc[g][q2]);
                 }
             }
+            __syncwarp();  // the slots are read before the next step writes them
         }
         __syncthreads();  // the stage is free again
         if (tid == 0 && j + S < nsub) {
@@ -345,7 +375,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, (G * D <= 512 ? 2 : 1))
 
 size_t attn_smem_bytes(int D, int G) {
     const int LS = dev::attn_sub(D), NW = dev::kAttnWarps;
-    return 64 + (size_t)dev::kAttnStages * 2 * LS * D * 4 + (size_t)NW * G * D * 4 + (size_t)(2 * NW * G + G) * 4 + 16;
+    return 64 + (size_t)dev::kAttnStages * 2 * LS * D * 4 + (size_t)NW * G * D * 4 +
+           (size_t)(2 * NW * G + G + NW * 32 + NW * G) * 4 + 16;
 }
 // splits one fold can weigh: its weights [nsplit][G] reuse the ring
 int attn_max_splits(int D, int G) { return dev::kAttnStages * 2 * dev::attn_sub(D) * D / G; }
