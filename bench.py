@@ -518,6 +518,21 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     out.update(stream_ceiling(Ws, bench_calls, peak, "q4_0_n%d_k%d" % (n4, k)))
     del Ws
     torch.cuda.empty_cache()
+    # the prefill GEMM on the 14336 x 4096 Q4_0 projection at 64, 256 and 512
+    # activation rows (one weight copy reused: its 33 MB stay partly in L2,
+    # which a prefill chunk also sees; the activations are new each call)
+    H = wl.draw_q4_0(rng, n, k)
+    Wg = q4.Q4Weight.from_q4_0(H.blocks, n, k, device)
+    for nbg in (64, 256, 512):
+        xg = torch.from_numpy(wl.draw_x(rng, nbg, k)).to(device)
+        yg = torch.empty((nbg, n), dtype=torch.float32, device=device)
+        wsg = torch.empty(int(q4.lib().q4_gemm_workspace_bytes(nbg, k)), dtype=torch.uint8, device=device)
+        t = bench_calls([Wg], lambda W: q4.q4_gemm(W, xg, out=yg, workspace=wsg))
+        out["gemm_q4_0_n%d_k%d_nb%d" % (n, k, nbg)] = {
+            "us": round(t * 1e6, 3), "tflops": round(2.0 * n * k * nbg / t / 1e12, 1),
+            "what": "staging pass + GEMM (mma.sync f16, fp32 accumulate), weights exact"}
+    del Wg
+    torch.cuda.empty_cache()
     # decode attention of one token (RoPE, KV append, softmax(q K^T) V) at
     # 32 query heads, 8 kv heads, head size 64, over 4096 and 32768 cached
     # positions; the f32 caches rotate over copies totalling > 3x L2

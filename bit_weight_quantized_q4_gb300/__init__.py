@@ -9,7 +9,7 @@ no CPU fallback: if the library is missing the calls raise.
 Entry points (same names as the C ABI in ``include/q4gemv.h``):
 ``q4_gemv``, ``q4_nrm_gemv``, ``q4_dual_gemv``, ``q4_gus_nrm``,
 ``q4_res_gemv``, ``q4_argmax``, ``q4_group_sums``, ``q4_pack_half``,
-``q4_gemv_half``, ``q4_decode_step``, ``q4_attn_decode``; plus ``Q4Weight``
+``q4_gemv_half``, ``q4_gemm``, ``q4_decode_step``, ``q4_attn_decode``; plus ``Q4Weight``
 for repacking host weights into the device layout and ``rope_table``.
 """
 from __future__ import annotations
@@ -103,6 +103,8 @@ def lib() -> ctypes.CDLL:
             "q4_debug_wait_limits": (I32, [ctypes.c_int64, I32, ctypes.c_int64, I32]),
             "q4_plan": (I32, [I32, I32, I32, I32, I32, I32, ctypes.POINTER(ctypes.c_int32)]),
             "q4_attn_workspace_bytes": (SZ, [I32, I32, I32]),
+            "q4_gemm_workspace_bytes": (SZ, [I32, I32]),
+            "q4_gemm": (I32, [W, P, I32, P, I32, P, SZ, P]),
             "q4_attn_decode": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I32, F, P, P, P, P, SZ, P]),
             "q4_rope_table": (I32, [I32, I32, ctypes.c_double, P, P]),
             "q4_status_str": (ctypes.c_char_p, [I32]),
@@ -608,4 +610,30 @@ def q4_attn_decode(q, k_new, v_new, k_cache, v_cache, position: int, window: int
                                 v_cache.data_ptr(), max_seq, int(position), H, Hkv, D, int(window), float(scale),
                                 cp, sp, out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream()),
            "q4_attn_decode")
+    return out
+
+
+# ---------------------------------------------------------------- prefill GEMM
+
+def q4_gemm(W: Q4Weight, x, accumulate: bool = False, out=None, workspace=None):
+    """y = x W^T for any batch width (meant for nb > 16): x ``[nb, k]``
+    float32 CUDA; with ``accumulate`` the product is added to ``out``."""
+    torch = _torch()
+    x = _dev_f32(x, "x")
+    if x.dim() != 2 or x.shape[1] != W.k:
+        raise ValueError("x must be [nb, %d]" % W.k)
+    nb = int(x.shape[0])
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate needs out")
+        out = torch.empty((nb, W.n), dtype=torch.float32, device=x.device)
+    else:
+        _dev_buf(out, "out", torch.float32, (nb, W.n), x.device)
+    wsb = int(lib().q4_gemm_workspace_bytes(nb, W.k))
+    if workspace is None:
+        workspace = torch.empty(max(16, wsb), dtype=torch.uint8, device=x.device)
+    else:
+        _dev_buf(workspace, "workspace", torch.uint8, None, x.device, min_numel=wsb)
+    _check(lib().q4_gemm(W.cref(), x.data_ptr(), nb, out.data_ptr(), int(bool(accumulate)), workspace.data_ptr(),
+                         workspace.numel(), _stream()), "q4_gemm")
     return out

@@ -629,6 +629,41 @@ extern "C" q4_status q4_decode_check(const void *workspace, cudaStream_t stream)
     return err ? Q4_ERR_CUDA : Q4_OK;
 }
 
+// ---------------------------------------------------------------- prefill GEMM
+
+extern "C" size_t q4_gemm_workspace_bytes(int32_t nb, int32_t k) {
+    if (nb < 1 || nb > (1 << 20) || !shape_ok(1, k)) return 0;
+    return q4::gemm_image_bytes(nb, (int)q4::chunks_of(k));
+}
+
+extern "C" q4_status q4_gemm(const q4_weight *W, const float *x, int32_t nb, float *y, int32_t accumulate,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    Q4_TRY(check_weight(W));
+    Q4_TRY(check_act(x));
+    Q4_TRY(check_act(y));
+    if (nb < 1 || nb > (1 << 20)) return Q4_ERR_SHAPE;
+    const size_t need = q4_gemm_workspace_bytes(nb, W->k);
+    if (!workspace || workspace_bytes < need) return Q4_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return Q4_ERR_ALIGN;
+    if (q4::gemm_smem_bytes(W->fmt) > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;
+    q4::GemmParams p{};
+    p.w = (const uint8_t *)W->dev;
+    p.x = x;
+    p.img = (uint8_t *)workspace;
+    p.y = y;
+    p.n = W->n;
+    p.T = (int)q4::tiles_of(W->n);
+    p.C = (int)q4::chunks_of(W->k);
+    p.K = W->k;
+    p.nb = nb;
+    p.accumulate = accumulate != 0;
+    Q4_TRY(kernel_err_ptr(&p.err));
+    p.wait_cycles = g_wait_cycles;
+    cudaGetLastError();
+    if (q4::launch_gemm(p, W->fmt, stream) != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
+    return Q4_OK;
+}
+
 // ---------------------------------------------------------------- attention
 
 namespace {

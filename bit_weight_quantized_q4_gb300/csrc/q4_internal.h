@@ -349,6 +349,22 @@ int attn_ctas_per_sm(int D, int G);
 int attn_max_splits(int D, int G);
 int launch_attn(const AttnParams &p, void *stream);
 
+// Prefill GEMM (gemm_kernel.cu): y[nb][n] (=, or +=) x[nb][K] W^T for any nb;
+// x is first staged into `img` (B fragments, block factors and offsets per 64
+// activation rows and 128-column chunk).
+struct GemmParams {
+    const uint8_t *w;   // packed weights
+    const float *x;     // [nb][K]
+    uint8_t *img;       // staged activations, gemm_image_bytes(nb, C)
+    float *y;           // [nb][n]
+    int n, T, C, K, nb, accumulate;
+    int *err;           // set nonzero if a copy wait gave up
+    long long wait_cycles;
+};
+size_t gemm_image_bytes(int nb, int C);
+size_t gemm_smem_bytes(int fmt);
+int launch_gemm(const GemmParams &p, int fmt, void *stream);
+
 int launch_gemv_q4_0(const GemvParams &p, const Plan &plan, void *stream);
 int launch_gemv_affine(const GemvParams &p, const Plan &plan, void *stream);
 int launch_gemv_q8_0(const GemvParams &p, const Plan &plan, void *stream);

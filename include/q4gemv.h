@@ -326,6 +326,25 @@ q4_status q4_debug_wait_limits(int64_t barrier_polls, int32_t barrier_extra, int
 q4_status q4_argmax_noalloc(const q4_weight *W, const float *x, const float *gamma, float eps,
                             int32_t nb, int32_t *idx, float *val, float *logits, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- prefill GEMM
+ * y = x W^T for a wide activation batch (crate inferencelayer, Functions:
+ * gemm_q4_src, the blocked prefill GEMM whose column tile shares one weight
+ * stream; its dims.z = 1 form accumulates into y).  Any nb >= 1 (meant for
+ * nb > 16, where the GEMV family re-reads the weights per 16 rows); every
+ * weight format.  x: [nb][k] fp32; y: [nb][n] fp32, overwritten, or with
+ * accumulate != 0 y += x W^T (y must then hold the values to add to).
+ * Numerics: every 32-column block of an activation row is scaled by its own
+ * power of two and carried as one f16 per value (as the GEMV calls do above
+ * four rows), weights exact, products accumulated in fp32.
+ * Workspace: q4_gemm_workspace_bytes(nb, k) device bytes (16-byte aligned,
+ * contents need not be initialised) hold the staged activations; the call
+ * launches a staging kernel and the GEMM kernel on `stream`.
+ * Q4_ERR_SHAPE for nb outside 1..2^20, Q4_ERR_WORKSPACE for a missing or short
+ * workspace; the weight and pointer checks are the GEMV family's. */
+size_t q4_gemm_workspace_bytes(int32_t nb, int32_t k);
+q4_status q4_gemm(const q4_weight *W, const float *x, int32_t nb, float *y, int32_t accumulate, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- attention
  * Decode attention of one token (honeycrisp/mod.rs: attn_state, gpu_attention
  * and the fused RoPE + KV-append + SDPA dispatch of

@@ -335,6 +335,21 @@ def test_attn_validation(case, expect):
     assert st == expect
 
 
+def test_gemm_validation():
+    # every case fails before any CUDA call (fake 16-byte aligned addresses)
+    L = q4.lib()
+    W = _cw()
+    ws = q4.lib().q4_gemm_workspace_bytes(40, 64)
+    assert ws == 1 * 1 * (4 * 8 * 32 * 16 + 2 * 4 * 64 * 4)       # one 64-row tile, one chunk
+    assert L.q4_gemm_workspace_bytes(0, 64) == 0 and L.q4_gemm_workspace_bytes(8, 48) == 0
+    assert L.q4_gemm(ctypes.byref(W), None, 40, A, 0, A, ws, None) == 1
+    assert L.q4_gemm(ctypes.byref(W), A + 4, 40, A, 0, A, ws, None) == 3
+    assert L.q4_gemm(ctypes.byref(W), A, 0, A, 0, A, ws, None) == 2
+    assert L.q4_gemm(ctypes.byref(W), A, 40, A, 0, A, ws - 16, None) == 5
+    assert L.q4_gemm(ctypes.byref(W), A, 40, A, 0, None, ws, None) == 5
+    assert L.q4_gemm(ctypes.byref(W), A, 40, A, 0, A + 8, ws, None) == 3
+
+
 def test_repack_validation():
     L = q4.lib()
     buf = np.zeros(4096, np.uint8)
