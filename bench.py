@@ -431,6 +431,16 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
             out["%s_n%d_k%d_nb%d" % (fmt, n, k, nb)] = {"us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1),
                                                       "frac_of_hbm": round(gbs / peak, 4)}
         if fmt == "affine":
+            # the prefill GEMM at verify widths: one weight stream shared by a
+            # 16-row activation tile (staging pass included)
+            for nb in (8, 16):
+                x = torch.from_numpy(wl.draw_x(rng, nb, k)).to(device)
+                y = torch.empty((nb, n), dtype=torch.float32, device=device)
+                wsg = torch.empty(int(q4.lib().q4_gemm_workspace_bytes(nb, k)), dtype=torch.uint8, device=device)
+                t = bench_calls(Ws, lambda W: q4.q4_gemm(W, x, out=y, workspace=wsg))
+                gbs = W0.weight_bytes / t / 1e9
+                out["%s_n%d_k%d_nb%d_gemm" % (fmt, n, k, nb)] = {
+                    "us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
             # the same matvec fed a HalfSet (f16 even/odd streams + group sums,
             # packed once): what a caller verifying several drafts per step runs
             for nb in (8, 16):

@@ -645,7 +645,7 @@ extern "C" q4_status q4_gemm(const q4_weight *W, const float *x, int32_t nb, flo
     const size_t need = q4_gemm_workspace_bytes(nb, W->k);
     if (!workspace || workspace_bytes < need) return Q4_ERR_WORKSPACE;
     if (!aligned16(workspace)) return Q4_ERR_ALIGN;
-    if (q4::gemm_smem_bytes(W->fmt) > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;
+    if (q4::gemm_smem_bytes(W->fmt, nb) > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;
     q4::GemmParams p{};
     p.w = (const uint8_t *)W->dev;
     p.x = x;

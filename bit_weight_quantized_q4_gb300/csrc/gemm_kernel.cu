@@ -4,18 +4,19 @@
 // column tile instead of once per column; gemm_q4_splitk_src for its fold).
 //
 // Two launches.  q4gemm_stage_kernel converts x once into the tensor-core
-// B-fragment image the GEMM reads: per 64 activation rows and 128-column
-// chunk, every 32-column block of a row scaled by its own power of two and
-// carried as one f16 per value (as the engine's batch classes above four
-// rows), the block's factor back, and its offset term (the zero-weight
-// product for Q4_0 and Q8_0, the fp32 block sum for the formats with a min).
-// q4gemm_kernel then gives each CTA 64 weight rows (four 16-row tiles) by 64
-// activation rows: a two-stage ring of TMA bulk copies brings each chunk's four
-// weight records and its image slice into shared memory, and each warp runs
-// one weight tile against four 8-row n-tiles with the engine's record decoding
-// and per-block scale arithmetic.  The activation tile index runs fastest in
-// the grid, so the CTAs that share a weight tile group run together and the
-// weights come from HBM about once.
+// B-fragment image the GEMM reads: per activation tile (64 rows, or 16 for
+// batches of at most 16 rows) and 128-column chunk, every 32-column block of
+// a row scaled by its own power of two and carried as one f16 per value (as
+// the engine's batch classes above four rows), the block's factor back, and
+// its offset term (the zero-weight product for Q4_0 and Q8_0, the fp32 block
+// sum for the formats with a min).  q4gemm_kernel then gives each CTA 64
+// weight rows (four 16-row tiles) by one activation tile: a two-stage ring of
+// TMA bulk copies brings each chunk's four weight records and its image slice
+// into shared memory, and each warp runs one weight tile against its share of
+// the tile's 8-row n-tiles with the engine's record decoding and per-block
+// scale arithmetic.  The activation tile index runs fastest in the grid, so
+// the CTAs that share a weight tile group run together and the weights come
+// from HBM about once.
 #include "gemv_launch.cuh"
 
 namespace q4 {
@@ -23,21 +24,31 @@ namespace dev {
 
 constexpr int kGemmWarps = 8;
 constexpr int kGemmSC = 2;      // chunks per ring stage
-constexpr int kGemmStages = 2;
-constexpr int kGemmImgB = 4 * 8 * 32 * 16;           // B fragments of one chunk: [block][n-tile][lane] x 16 bytes
-constexpr int kGemmImg = kGemmImgB + 2 * 4 * 64 * 4;  // + factors [block][row] and offsets [block][row], fp32
+// ring stages: four for the 16-row activation tile (its stages are small and
+// the kernel streams weights), two for the 64-row tile (tensor-bound)
+Q4_HD constexpr int gemm_stages(int NT) { return NT == 2 ? 4 : 2; }
+// Activation tiles of NT n-tiles (NT * 8 rows): 8 for wide batches, 2 for
+// batches of at most 16 rows.  Per tile and 128-column chunk the image holds
+// the B fragments [block][n-tile][lane] (16 bytes a lane), then the factors
+// and the offsets [block][row] in fp32.
+Q4_HD constexpr int gemm_img_b(int NT) { return 4 * NT * 32 * 16; }
+Q4_HD constexpr int gemm_img(int NT) { return gemm_img_b(NT) + 2 * 4 * NT * 8 * 4; }
 
 // ---------------------------------------------------------------- staging
 
-template <int FMT>
-__global__ void __launch_bounds__(kGemmWarps * 32) q4gemm_stage_kernel(const __grid_constant__ GemmParams p) {
+template <int FMT, int NT>
+__global__ void __launch_bounds__(NT * 32) q4gemm_stage_kernel(const __grid_constant__ GemmParams p) {
+    constexpr int ROWS = NT * 8;
+    // the GEMM (launched as this kernel's dependent) may start now: it
+    // streams weights until it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int c = blockIdx.x, rt = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int nt = warp;                       // n-tile: activation rows rt*64 + nt*8 .. +7
-    const int r = rt * 64 + nt * 8 + g;        // this lane's activation row
-    uint8_t *img = p.img + ((size_t)rt * p.C + c) * kGemmImg;
-    float *F = reinterpret_cast<float *>(img + kGemmImgB), *Gs = F + 4 * 64;
+    const int nt = warp;                       // n-tile: activation rows rt*ROWS + nt*8 .. +7
+    const int r = rt * ROWS + nt * 8 + g;      // this lane's activation row
+    uint8_t *img = p.img + ((size_t)rt * p.C + c) * gemm_img(NT);
+    float *F = reinterpret_cast<float *>(img + gemm_img_b(NT)), *Gs = F + 4 * ROWS;
     // lane (g, t) holds columns 8m + 2t, 8m + 2t + 1 of the chunk, m = 0..15:
     // block m / 4, k16 step (m % 4) / 2, positions 0..7 (m even) or 8..15
     float2 v[16];
@@ -69,8 +80,8 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q4gemm_stage_kernel(const __g
             const __half2 h = __floats2half2_rn(v[4 * j + mm].x * f, v[4 * j + mm].y * f);
             b[mm] = *reinterpret_cast<const uint32_t *>(&h);
         }
-        *reinterpret_cast<uint4 *>(img + ((size_t)(j * 8 + nt) * 32 + lane) * 16) = make_uint4(b[0], b[1], b[2], b[3]);
-        if (t == 0) F[j * 64 + nt * 8 + g] = back;
+        *reinterpret_cast<uint4 *>(img + ((size_t)(j * NT + nt) * 32 + lane) * 16) = make_uint4(b[0], b[1], b[2], b[3]);
+        if (t == 0) F[j * ROWS + nt * 8 + g] = back;
         if constexpr (has_offset(FMT)) {
             // the block's zero-weight product, through the same tensor-core
             // chain as the weights' (so that zero weights give exactly 0):
@@ -80,16 +91,16 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q4gemm_stage_kernel(const __g
             mma16816_c(e, EL, EL, kEightHi, kEightHi, b[0], b[1], z, z, z, z);
             mma16816(e, EL, EL, kEightHi, kEightHi, b[2], b[3]);
             if (g == 0) {
-                Gs[j * 64 + nt * 8 + 2 * t] = e[0];
-                Gs[j * 64 + nt * 8 + 2 * t + 1] = e[1];
+                Gs[j * ROWS + nt * 8 + 2 * t] = e[0];
+                Gs[j * ROWS + nt * 8 + 2 * t + 1] = e[1];
             }
         } else if constexpr (has_min(FMT)) {
             // the block sum of x (its four lanes' shares, added by a butterfly)
             bs += __shfl_xor_sync(0xffffffffu, bs, 1);
             bs += __shfl_xor_sync(0xffffffffu, bs, 2);
-            if (t == 0) Gs[j * 64 + nt * 8 + g] = bs;
+            if (t == 0) Gs[j * ROWS + nt * 8 + g] = bs;
         } else {
-            if (t == 0) Gs[j * 64 + nt * 8 + g] = 0.f;
+            if (t == 0) Gs[j * ROWS + nt * 8 + g] = 0.f;
         }
     }
 }
@@ -131,16 +142,17 @@ struct RecScales {
     }
 };
 
-template <int FMT>
+template <int FMT, int NT>
 __global__ void __launch_bounds__(kGemmWarps * 32, 2) q4gemm_kernel(const __grid_constant__ GemmParams p) {
-    constexpr int REC = rec_bytes(FMT), SC = kGemmSC, S = kGemmStages;
+    constexpr int REC = rec_bytes(FMT), SC = kGemmSC, S = gemm_stages(NT);
+    constexpr int ROWS = NT * 8, NTW = NT / 2, IMG = gemm_img(NT), IMGB = gemm_img_b(NT);
     constexpr int WB = 4 * SC * REC;            // weight bytes of a stage (four tiles)
-    constexpr int STAGE = WB + SC * kGemmImg;   // stage bytes
+    constexpr int STAGE = WB + SC * IMG;        // stage bytes
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     const int rt = blockIdx.x, tg = blockIdx.y;  // activation tile (fastest), weight tile group
-    const int wt = warp & 3, ng = warp >> 2;     // this warp: weight tile, n-tiles 4 ng .. 4 ng + 3
+    const int wt = warp & 3, ng = warp >> 2;     // this warp: weight tile, n-tiles NTW ng .. NTW ng + NTW - 1
     const int tile = 4 * tg + wt;
     const bool tile_ok = tile < p.T;
     const int nst = (p.C + SC - 1) / SC;
@@ -148,27 +160,38 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 2) q4gemm_kernel(const __grid
     uint8_t *ring = smem + 16 * S;
     const uint64_t pol = evict_first_policy();
 
-    auto issue = [&](int k) {  // stage k: chunks k*SC .. (thread 0)
+    // stage k (chunks k*SC ..): the weight records, then the image slice;
+    // both complete on the stage's barrier (thread 0 only)
+    auto issue_w = [&](int k) {
         const int c0 = k * SC, n = min(SC, p.C - c0);
         uint8_t *st = ring + (size_t)(k % S) * STAGE;
         const uint32_t bar = bars + 8 * (k % S);
         const int tiles = min(4, p.T - 4 * tg);
-        mbar_expect_tx(bar, (uint32_t)(tiles * n * REC + n * kGemmImg));
+        mbar_expect_tx(bar, (uint32_t)(tiles * n * REC + n * IMG));
         for (int i = 0; i < tiles; ++i)
             bulk_g2s(smem_u32(st + i * SC * REC), p.w + ((size_t)(4 * tg + i) * p.C + c0) * REC, n * REC, bar, pol);
-        bulk_g2s(smem_u32(st + WB), p.img + ((size_t)rt * p.C + c0) * kGemmImg, n * kGemmImg, bar, pol);
+    };
+    auto issue_img = [&](int k) {
+        const int c0 = k * SC, n = min(SC, p.C - c0);
+        uint8_t *st = ring + (size_t)(k % S) * STAGE;
+        bulk_g2s(smem_u32(st + WB), p.img + ((size_t)rt * p.C + c0) * IMG, n * IMG, bars + 8 * (k % S), pol);
     };
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(bars + 8 * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // weights do not depend on the staging kernel: their first copies go out
+    // before waiting for it, the image slices after
     if (tid == 0)
-        for (int k = 0; k < min(S, nst); ++k) issue(k);
+        for (int k = 0; k < min(S, nst); ++k) issue_w(k);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0)
+        for (int k = 0; k < min(S, nst); ++k) issue_img(k);
 
-    float acc[4][4];
+    float acc[NTW][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < NTW; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
     const float z = 0.f;
@@ -183,8 +206,8 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 2) q4gemm_kernel(const __grid
         if (tile_ok) {  // warp-uniform
             for (int cc = 0; cc < n; ++cc) {
                 const uint32_t ra = smem_u32(st + wt * SC * REC + cc * REC);
-                const uint8_t *img = st + WB + cc * kGemmImg;
-                const float *F = reinterpret_cast<const float *>(img + kGemmImgB), *Gs = F + 4 * 64;
+                const uint8_t *img = st + WB + cc * IMG;
+                const float *F = reinterpret_cast<const float *>(img + IMGB), *Gs = F + 4 * ROWS;
                 RecWords<FMT> rw;
                 rw.load(ra, lane);
                 RecScales<FMT> rs;
@@ -196,14 +219,14 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 2) q4gemm_kernel(const __grid
                     float2 s2, m2;
                     rs.template block<J>(s2, m2);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int ntl = 4 * ng + i;
-                        const uint4 B = *reinterpret_cast<const uint4 *>(img + ((size_t)(J * 8 + ntl) * 32 + lane) * 16);
+                    for (int i = 0; i < NTW; ++i) {
+                        const int ntl = NTW * ng + i;
+                        const uint4 B = *reinterpret_cast<const uint4 *>(img + ((size_t)(J * NT + ntl) * 32 + lane) * 16);
                         float d[4];
                         mma16816_c(d, a[0], a[1], a[2], a[3], B.x, B.y, z, z, z, z);
                         mma16816(d, a[4], a[5], a[6], a[7], B.z, B.w);
-                        const float2 f = *reinterpret_cast<const float2 *>(F + J * 64 + ntl * 8 + 2 * t);
-                        const float2 o = *reinterpret_cast<const float2 *>(Gs + J * 64 + ntl * 8 + 2 * t);
+                        const float2 f = *reinterpret_cast<const float2 *>(F + J * ROWS + ntl * 8 + 2 * t);
+                        const float2 o = *reinterpret_cast<const float2 *>(Gs + J * ROWS + ntl * 8 + 2 * t);
                         // d: (row g, cols 2t, 2t+1), (row g+8, cols 2t, 2t+1)
                         if constexpr (has_offset(FMT)) {
                             acc[i][0] = fmaf(s2.x * f.x, d[0] - o.x, acc[i][0]);
@@ -232,7 +255,8 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 2) q4gemm_kernel(const __grid
         __syncthreads();  // the stage is free again
         if (tid == 0 && k + S < nst) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(k + S);
+            issue_w(k + S);
+            issue_img(k + S);
         }
     }
     if (!ok) {
@@ -247,8 +271,8 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 2) q4gemm_kernel(const __grid
     }
     if (!tile_ok) return;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int col0 = rt * 64 + (4 * ng + i) * 8 + 2 * t;
+    for (int i = 0; i < NTW; ++i) {
+        const int col0 = rt * ROWS + (NTW * ng + i) * 8 + 2 * t;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int row = tile * 16 + g + (e >= 2 ? 8 : 0), col = col0 + (e & 1);
@@ -262,23 +286,45 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 2) q4gemm_kernel(const __grid
 
 }  // namespace dev
 
-size_t gemm_image_bytes(int nb, int C) { return (size_t)((nb + 63) / 64) * C * dev::kGemmImg; }
-size_t gemm_smem_bytes(int fmt) {
-    return 16 * dev::kGemmStages +
-           (size_t)dev::kGemmStages * (4 * dev::kGemmSC * rec_bytes(fmt) + dev::kGemmSC * dev::kGemmImg);
+// activation tile of a batch: 16 rows (2 n-tiles) up to 16 rows, else 64
+static int gemm_nt(int nb) { return nb <= 16 ? 2 : 8; }
+size_t gemm_image_bytes(int nb, int C) {
+    const int NT = gemm_nt(nb);
+    return (size_t)((nb + NT * 8 - 1) / (NT * 8)) * C * dev::gemm_img(NT);
+}
+size_t gemm_smem_bytes(int fmt, int nb) {
+    const int NT = gemm_nt(nb), S = dev::gemm_stages(NT);
+    return 16 * S + (size_t)S * (4 * dev::kGemmSC * rec_bytes(fmt) + dev::kGemmSC * dev::gemm_img(NT));
+}
+
+template <int FMT, int NT>
+static int launch_gemm_nt(const GemmParams &p, cudaStream_t stream) {
+    auto kern = dev::q4gemm_kernel<FMT, NT>;
+    static size_t smem_set[64] = {0};
+    const size_t smem = gemm_smem_bytes(FMT, NT == 2 ? 16 : 64);
+    if (!raise_smem(kern, smem, smem_set)) return -1;
+    const int RT = (p.nb + NT * 8 - 1) / (NT * 8);
+    // staging: an ordinary launch (it overwrites the image a previous call's
+    // GEMM may still be reading)
+    dev::q4gemm_stage_kernel<FMT, NT><<<dim3(p.C, RT), NT * 32, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    // the GEMM as its programmatic dependent
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)RT, (unsigned)((p.T + 3) / 4), 1);
+    cfg.blockDim = dim3(dev::kGemmWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? 0 : -1;
 }
 
 template <int FMT>
 static int launch_gemm_fmt(const GemmParams &p, cudaStream_t stream) {
-    auto kern = dev::q4gemm_kernel<FMT>;
-    static size_t smem_set[64] = {0};
-    const size_t smem = gemm_smem_bytes(FMT);
-    if (!raise_smem(kern, smem, smem_set)) return -1;
-    const int RT = (p.nb + 63) / 64;
-    dev::q4gemm_stage_kernel<FMT><<<dim3(p.C, RT), dev::kGemmWarps * 32, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return -1;
-    kern<<<dim3(RT, (p.T + 3) / 4), dev::kGemmWarps * 32, smem, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    return gemm_nt(p.nb) == 2 ? launch_gemm_nt<FMT, 2>(p, stream) : launch_gemm_nt<FMT, 8>(p, stream);
 }
 
 int launch_gemm(const GemmParams &p, int fmt, void *stream_) {

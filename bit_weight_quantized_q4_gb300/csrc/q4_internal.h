@@ -362,7 +362,7 @@ struct GemmParams {
     long long wait_cycles;
 };
 size_t gemm_image_bytes(int nb, int C);
-size_t gemm_smem_bytes(int fmt);
+size_t gemm_smem_bytes(int fmt, int nb);
 int launch_gemm(const GemmParams &p, int fmt, void *stream);
 
 int launch_gemv_q4_0(const GemvParams &p, const Plan &plan, void *stream);

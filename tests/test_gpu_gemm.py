@@ -1,7 +1,7 @@
 """GPU parity of q4_gemm (the prefill GEMM: y = x W^T for wide activation
 batches; crate inferencelayer, gemm_q4_src) against the f64 oracle, through
-the C ABI: every weight format, batch widths around and far above one
-64-row activation tile, ragged n and k, the accumulate form, exact zeros and
+the C ABI: every weight format, batch widths in the 16-row activation tile
+(1, 9, 16) and around and far above one 64-row tile, ragged n and k, the accumulate form, exact zeros and
 run-to-run determinism."""
 import numpy as np
 import pytest
@@ -26,7 +26,7 @@ def q4():
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("nb", [1, 17, 64, 100, 257])
+@pytest.mark.parametrize("nb", [1, 9, 16, 17, 64, 100, 257])
 @pytest.mark.parametrize("n,k", [(33, 160), (64, 1024), (200, 544), (1000, 2048)])
 def test_gemm_parity(q4, fmt, nb, n, k):
     k = fmt_k(fmt, k)
