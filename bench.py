@@ -52,6 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--gemv", metavar="FMT:N:K:NB", default=None,
                     help="time one q4_gemv shape only (fmt q4_0, affine, q8_0, q4_k or q1; for profiling), then exit")
+    ap.add_argument("--gemm", metavar="FMT:N:K:NB", default=None,
+                    help="time one q4_gemm shape only (for profiling), then exit")
     ap.add_argument("--attn", metavar="H:HKV:D:CTX", default=None,
                     help="time one q4_attn_decode shape only (the token at position CTX-1, RoPE on; for "
                          "profiling), then exit")
@@ -604,6 +606,43 @@ def run_one_gemv(args) -> dict:
             "note": "one weight reused: warm L2 for matrices under 129 MB; the kernel table times cold weights"}
 
 
+def run_one_gemm(args) -> dict:
+    """One prefill-GEMM shape, `warmup` untimed then `steps` timed calls on
+    one weight; for ncu captures."""
+    import numpy as np
+    import torch
+
+    import bit_weight_quantized_q4_gb300 as q4
+    import q4_workloads as wl
+    fmt, n, k, nb = args.gemm.split(":")
+    n, k, nb = int(n), int(k), int(nb)
+    q4.build()
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(3)
+    H = wl._draw_fmt(fmt)(rng, n, k)
+    W = (q4.Q4Weight.from_affine(H.nib, H.s, H.m, n, k, dev) if fmt == "affine"
+         else q4.Q4Weight.from_q8_0(H.blocks8, n, k, dev) if fmt == "q8_0"
+         else q4.Q4Weight.from_q4_k(H.blocks_k, n, k, dev) if fmt == "q4_k"
+         else q4.Q4Weight.from_q1(H.blocks1, n, k, dev) if fmt == "q1"
+         else q4.Q4Weight.from_q4_0(H.blocks, n, k, dev))
+    x = torch.from_numpy(wl.draw_x(rng, nb, k)).to(dev)
+    y = torch.empty((nb, n), dtype=torch.float32, device=dev)
+    ws = torch.empty(int(q4.lib().q4_gemm_workspace_bytes(nb, k)), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        q4.q4_gemm(W, x, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        q4.q4_gemm(W, x, out=y, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    q4.q4_device_check()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    return {"gemm": args.gemm, "calls": args.steps, "us_per_call": round(us, 3),
+            "tflops": round(2.0 * n * k * nb / us / 1e6, 1)}
+
+
 def run_one_attn(args) -> dict:
     """One decode-attention shape, `warmup` untimed then `steps` timed calls
     on one pair of caches; for ncu captures."""
@@ -862,6 +901,8 @@ def main(argv=None):
     rank, world, local = dist_env()
     if args.gemv:
         line = run_one_gemv(args) if rank == 0 else None
+    elif args.gemm:
+        line = run_one_gemm(args) if rank == 0 else None
     elif args.attn:
         line = run_one_attn(args) if rank == 0 else None
     elif args.impl == "reference":
