@@ -392,25 +392,53 @@ def _hw(H) -> HostWeight:
     return HostWeight.affine(H.nib, H.s, H.m, H.n, H.k)
 
 
-def decode_layer(L, src, eps: float) -> dict:
+def layer_attention(q, k, v, kc, vc, spec, cosv=None, sinv=None):
+    """Decode attention of one token inside a layer: q ``[1, heads*head_dim]``,
+    k and v ``[1, kv_heads*head_dim]`` as heads, against the layer's caches
+    ``[kv_heads, max_seq, head_dim]``; scale 1/sqrt(head_dim).  Returns
+    ``(out [1, heads*head_dim], bound, kc', vc')``."""
+    H, Hkv, D = spec.heads, spec.kv_heads, spec.head_dim
+    out, bound, kc2, vc2 = attn_decode(_f64(q).reshape(H, D), _f64(k).reshape(Hkv, D), _f64(v).reshape(Hkv, D),
+                                       kc, vc, spec.position, spec.window, 1.0 / np.sqrt(D), cosv, sinv)
+    return out.reshape(1, H * D), bound.reshape(1, H * D), kc2, vc2
+
+
+def decode_layer(L, src, eps: float, attention=None) -> dict:
     """One layer on f64 activations ``src [nb, hidden]``; returns every
-    intermediate (and its tolerance scale) as f64 arrays."""
+    intermediate (and its tolerance scale) as f64 arrays.  With
+    ``attention = (spec, kc, vc, cosv, sinv)`` (nb = 1) the o projection takes
+    the token's attention output (honeycrisp/mod.rs, gpu_attention between the
+    K+V and the o projection) instead of the layer's stand-in; the result then
+    also holds ``attn`` and the appended caches ``kc``, ``vc``."""
     src = _f64(src)
     q, Sq = q4_nrm_gemv(_hw(L.Wq), src, L.gamma_in, eps)
     k, Sk, v, Sv = q4_dual_gemv(_hw(L.Wk), _hw(L.Wv), src, L.gamma_in, eps)
-    hid_o, So = q4_res_gemv(_hw(L.Wo), L.attn, src)
+    extra = {}
+    o_in = L.attn
+    if attention is not None:
+        spec, kc, vc, cosv, sinv = attention
+        o_in, Sa, kc2, vc2 = layer_attention(q, k, v, kc, vc, spec, cosv, sinv)
+        extra = dict(attn=o_in, Sa=Sa, kc=kc2, vc=vc2)
+    hid_o, So = q4_res_gemv(_hw(L.Wo), o_in, src)
     h, g, Sg, u, Su = q4_gus_nrm(_hw(L.Wg), _hw(L.Wu), hid_o, L.gamma_post, eps)
     hid, Sd = q4_res_gemv(_hw(L.Wd), h, hid_o)
     return dict(q=q, Sq=Sq, k=k, Sk=Sk, v=v, Sv=Sv, hid_o=hid_o, So=So, h=h, g=g, Sg=Sg, u=u, Su=Su,
-                hid=hid, Sd=Sd)
+                hid=hid, Sd=Sd, **extra)
 
 
-def decode_step(cfg, layers=None):
-    """The whole step in f64 from ``cfg.x``; returns (idx, logits, hidden)."""
+def decode_step(cfg, layers=None, attention=None):
+    """The whole step in f64 from ``cfg.x``; returns (idx, logits, hidden).
+    ``attention = (spec, caches)`` runs each layer's real attention against
+    its ``(kc, vc)`` caches (see decode_layer)."""
     hid = _f64(cfg.x)
     Ls = cfg.layers if layers is None else cfg.layers[:layers]
-    for L in Ls:
-        hid = decode_layer(L, hid, cfg.eps)["hid"]
+    tables = None
+    if attention is not None:
+        spec, caches = attention
+        tables = rope_table(spec.max_seq, spec.head_dim, spec.rope_theta)
+    for l, L in enumerate(Ls):
+        att = None if attention is None else (spec, caches[l][0], caches[l][1], tables[0], tables[1])
+        hid = decode_layer(L, hid, cfg.eps, att)["hid"]
     idx, logits, _ = q4_argmax(_hw(cfg.Wlogits), hid, cfg.gamma_final, cfg.eps)
     return idx, logits, hid
 

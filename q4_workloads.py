@@ -401,6 +401,36 @@ def cfg4(seed: int = 4, layers: int = 16, hidden: int = 2048, kv: int = 512,
     return c
 
 
+@dataclass
+class AttnSpec:
+    """Decode attention inside the step (the real step the stand-in replaces):
+    ``heads`` x ``head_dim`` must be the hidden size and ``kv_heads`` x
+    ``head_dim`` the k/v width; the token sits at ``position`` of caches of
+    ``max_seq`` rows."""
+    heads: int = 32
+    kv_heads: int = 8
+    head_dim: int = 64
+    max_seq: int = 4096
+    position: int = 4095
+    window: int = 0
+    rope_theta: float = 10000.0
+
+
+def draw_kv_caches(seed: int, layers: int, spec: AttnSpec):
+    """Per layer the K and V caches ``[kv_heads, max_seq, head_dim]`` fp32:
+    rows before ``position`` (the earlier tokens) ~ N(0, 1), the rest zero."""
+    out = []
+    for l in range(layers):
+        rng = np.random.default_rng(seed * 1000 + 500 + l)
+        shape = (spec.kv_heads, spec.max_seq, spec.head_dim)
+        kc = np.zeros(shape, np.float32)
+        vc = np.zeros(shape, np.float32)
+        kc[:, :spec.position] = rng.standard_normal((spec.kv_heads, spec.position, spec.head_dim))
+        vc[:, :spec.position] = rng.standard_normal((spec.kv_heads, spec.position, spec.head_dim))
+        out.append((kc, vc))
+    return out
+
+
 def q4_0_weight_bytes(n: int, k: int) -> int:
     """Algorithmic Q4_0 bytes: 18 per 32 weights."""
     return n * (k // 32) * 18
