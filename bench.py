@@ -747,6 +747,25 @@ def run_ours(args, rank, world, local):
     gus_us, _ = kernel_timing(step, 3, fused=False, name="gus")
     del calls_graph
 
+    # the real step: each layer's decode attention over 4096 cached positions
+    # (32 / 8 heads of 64) between K+V and the o projection, as library calls
+    # in one graph; it reads the weights and every layer's K and V rows
+    real = None
+    if rank == 0 and world == 1 and not args.no_kernels:
+        spec = wl.AttnSpec(max_seq=4096, position=4095)
+        astep = DecodeStep(cfg, device, attention=(spec, wl.draw_kv_caches(4, args.layers, spec)))
+        ag = astep.capture()
+        for _ in range(max(1, args.warmup)):
+            ag.replay()
+        a_secs = time_replays(ag, args.steps, stream)
+        a_bytes = astep.weight_bytes + astep.kv_bytes
+        real = {"kernels_per_step": astep.n_kernels, "context": spec.position + 1,
+                "us_per_step": round(a_secs * 1e6 / args.steps, 2),
+                "bytes_per_step": a_bytes, "gbs": round(a_bytes * args.steps / a_secs / 1e9, 2),
+                "frac_of_hbm_peak": round(a_bytes * args.steps / a_secs / 1e9 / peak, 4)}
+        del ag, astep
+        torch.cuda.empty_cache()
+
     l2 = int(getattr(props, "L2_cache_size", 0) or 0)
     kernels = None
     if rank == 0 and world == 1 and not args.no_kernels:
@@ -791,6 +810,8 @@ def run_ours(args, rank, world, local):
                            "weight_gbs": round(wbytes * args.steps / calls_secs / 1e9, 2),
                            "gus_launch_us": round(gus_us, 3)},
     }
+    if real is not None:
+        line["step_with_attention"] = real
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if kernels is not None:

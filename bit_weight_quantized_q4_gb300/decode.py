@@ -14,9 +14,14 @@ The step order is the fused decode path of honeycrisp/mod.rs
 (forward_decode_fused_layers: one command buffer per step) with the final
 logits projection and greedy argmax of Module gpu (module sampling).  The
 attention output is replaced by a fixed seeded vector per layer, so the q, k
-and v projections are computed and stored but not consumed.
+and v projections are computed and stored but not consumed -- unless the
+step is built with ``attention`` (a ``q4_workloads.AttnSpec`` and per-layer KV
+caches): then ``run()`` adds each layer's decode attention (``q4_attn_decode``:
+RoPE, append, softmax(q K^T) V over the layer's caches, q/k/v read as heads)
+between the K+V and the o projection, which takes its output: the real step.
 
-Kernels per step: 5 per layer + 2 for the argmax (82 for 16 layers).
+Kernels per step: 5 per layer + 2 for the argmax (82 for 16 layers), one more
+per layer with attention.
 """
 from __future__ import annotations
 
@@ -25,8 +30,8 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import DecodeLayers, Q4Weight, q4_argmax, q4_argmax_workspace_bytes, q4_decode_step, \
-    q4_decode_workspace_bytes, q4_dual_gemv, q4_gus_nrm, q4_nrm_gemv, q4_res_gemv
+from . import DecodeLayers, Q4Weight, lib, q4_argmax, q4_argmax_workspace_bytes, q4_attn_decode, q4_decode_step, \
+    q4_decode_workspace_bytes, q4_dual_gemv, q4_gus_nrm, q4_nrm_gemv, q4_res_gemv, rope_table
 
 
 @dataclass
@@ -54,7 +59,7 @@ class DecodeStep:
     step input; after ``run()`` (or a graph replay) ``idx`` / ``val`` hold
     the argmax and ``hid`` the final hidden state."""
 
-    def __init__(self, cfg, device="cuda"):
+    def __init__(self, cfg, device="cuda", attention=None):
         T = lambda a: torch.from_numpy(a.copy()).to(device)
         W = lambda H: (Q4Weight.from_q8_0(H.blocks8, H.n, H.k, device) if hasattr(H, "blocks8")
                        else Q4Weight.from_q4_k(H.blocks_k, H.n, H.k, device) if hasattr(H, "blocks_k")
@@ -89,10 +94,33 @@ class DecodeStep:
         self.ws = torch.empty(q4_argmax_workspace_bytes(self.Wlogits.n, nb), dtype=torch.uint8, device=device)
         self.step_ws = torch.empty(q4_decode_workspace_bytes(nb), dtype=torch.uint8, device=device)
         self.descs = DecodeLayers(self.layers)
+        # the real step: the attention spec, per-layer device caches, RoPE
+        # tables, the attention output and its workspace
+        self.attention = None
+        if attention is not None:
+            spec, caches = attention
+            if nb != 1 or spec.heads * spec.head_dim != hidden or spec.kv_heads * spec.head_dim != L0.Wk.n:
+                raise ValueError("attention needs nb = 1, heads*head_dim = hidden and kv_heads*head_dim = k width")
+            self.attention = spec
+            self.caches = [(T(kc), T(vc)) for kc, vc in caches]
+            c, sn = rope_table(spec.max_seq, spec.head_dim, spec.rope_theta)
+            self.rope = (T(c), T(sn))
+            self.att = torch.empty((1, hidden), **f32)
+            self.attn_ws = torch.zeros(int(lib().q4_attn_workspace_bytes(spec.heads, spec.head_dim, spec.max_seq)),
+                                       dtype=torch.uint8, device=device)
 
     @property
     def n_kernels(self) -> int:
-        return KERNELS_PER_LAYER * len(self.layers) + KERNELS_FINAL
+        return (KERNELS_PER_LAYER + (self.attention is not None)) * len(self.layers) + KERNELS_FINAL
+
+    @property
+    def kv_bytes(self) -> int:
+        """Cache bytes the step's attention reads (0 without attention)."""
+        a = self.attention
+        if a is None:
+            return 0
+        lo = max(0, a.position + 1 - a.window) if a.window > 0 else 0
+        return len(self.layers) * 2 * a.kv_heads * (a.position + 1 - lo) * a.head_dim * 4
 
     @property
     def weight_bytes(self) -> int:
@@ -113,7 +141,17 @@ class DecodeStep:
             hook and hook("q", l)
             call("kv", l, lambda: q4_dual_gemv(L.Wk, L.Wv, src, L.gamma_in, eps, out_a=self.k, out_b=self.v))
             hook and hook("kv", l)
-            call("o", l, lambda: q4_res_gemv(L.Wo, L.attn, src, out=self.hid))
+            o_in = L.attn
+            a = self.attention
+            if a is not None:
+                kc, vc = self.caches[l]
+                call("attn", l, lambda: q4_attn_decode(
+                    self.q.view(a.heads, a.head_dim), self.k.view(a.kv_heads, a.head_dim),
+                    self.v.view(a.kv_heads, a.head_dim), kc, vc, a.position, a.window, None, rope=self.rope,
+                    out=self.att.view(a.heads, a.head_dim), workspace=self.attn_ws))
+                hook and hook("attn", l)
+                o_in = self.att
+            call("o", l, lambda: q4_res_gemv(L.Wo, o_in, src, out=self.hid))
             hook and hook("o", l)
             call("gus", l, lambda: q4_gus_nrm(L.Wg, L.Wu, self.hid, L.gamma_post, eps, out=self.h))
             hook and hook("gus", l)
@@ -127,7 +165,9 @@ class DecodeStep:
 
     def run_fused(self, n_layers=None):
         """Enqueue the step as one persistent kernel (the first ``n_layers``
-        layers then the logits argmax)."""
+        layers then the logits argmax); the stand-in step only."""
+        if self.attention is not None:
+            raise ValueError("the persistent step runs the stand-in step; run() takes the attention")
         q4_decode_step(self.descs, self.Wlogits, self.gamma_final, self.eps, self.x_in, self.hid, self.q, self.k,
                        self.v, self.h, self.idx, self.val, self.step_ws, n_layers=n_layers)
 

@@ -124,6 +124,71 @@ def test_decode_step_teacher_forced(q4):
     assert torch.equal(step.hid, fin["final"])
 
 
+def test_decode_step_with_attention_teacher_forced(q4):
+    """The real step (decode attention between K+V and the o projection, over
+    each layer's KV cache) at the workload's widths -- 2048 = 32 heads x 64,
+    512 = 8 kv heads x 64 -- with 1000 cached positions, layer by layer
+    against the oracle on the GPU's own inputs."""
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+    spec = wl.AttnSpec(max_seq=1024, position=1000)
+    cfg = wl.cfg4(seed=16, layers=2)
+    caches = wl.draw_kv_caches(16, 2, spec)
+    step = DecodeStep(cfg, attention=(spec, caches))
+    snaps = []
+
+    def hook(name, l):
+        if name == "q":
+            snaps.append({"src": (step.x_in if l == 0 else step.hid).clone(), "q": step.q.clone()})
+        elif name == "kv":
+            snaps[-1].update(k=step.k.clone(), v=step.v.clone())
+        elif name == "attn":
+            snaps[-1]["attn"] = step.att.clone()
+        elif name == "o":
+            snaps[-1]["hid_o"] = step.hid.clone()
+        elif name == "gus":
+            snaps[-1]["h"] = step.h.clone()
+        elif name == "down":
+            snaps[-1]["hid"] = step.hid.clone()
+        elif name == "argmax":
+            snaps.append({"idx": step.idx.clone(), "final": step.hid.clone()})
+
+    step.run(hook=hook)
+    torch.cuda.synchronize()
+    assert step.n_kernels == 6 * 2 + 2
+    cosv, sinv = oracle.rope_table(spec.max_seq, spec.head_dim, spec.rope_theta)
+    for l, L in enumerate(cfg.layers):
+        s = snaps[l]
+        src = s["src"].cpu().numpy()
+        q, Sq = oracle.q4_nrm_gemv(oracle._hw(L.Wq), src, L.gamma_in, cfg.eps)
+        check(to_np(s["q"]), q, Sq, what="attn step layer %d q" % l)
+        ka, Ska, kb, Skb = oracle.q4_dual_gemv(oracle._hw(L.Wk), oracle._hw(L.Wv), src, L.gamma_in, cfg.eps)
+        check(to_np(s["k"]), ka, Ska, what="attn step layer %d k" % l)
+        check(to_np(s["v"]), kb, Skb, what="attn step layer %d v" % l)
+        ar, Sa, kc2, vc2 = oracle.layer_attention(to_np(s["q"]), to_np(s["k"]), to_np(s["v"]), caches[l][0],
+                                                  caches[l][1], spec, cosv, sinv)
+        check(to_np(s["attn"]), ar, Sa, what="attn step layer %d attention" % l)
+        kd, vd = step.caches[l][0].cpu().numpy(), step.caches[l][1].cpu().numpy()
+        assert np.array_equal(vd[:, spec.position], vc2[:, spec.position])
+        assert np.allclose(kd[:, spec.position], kc2[:, spec.position], rtol=1e-5, atol=1e-5)
+        assert np.array_equal(kd[:, :spec.position], caches[l][0][:, :spec.position])
+        ho, So = oracle.q4_res_gemv(oracle._hw(L.Wo), s["attn"].cpu().numpy(), src)
+        check_residual(to_np(s["hid_o"]), ho, So, what="attn step layer %d o" % l)
+        _, g, Sg, u, Su = oracle.q4_gus_nrm(oracle._hw(L.Wg), oracle._hw(L.Wu), s["hid_o"].cpu().numpy(),
+                                            L.gamma_post, cfg.eps)
+        check_swiglu(to_np(s["h"]), g, Sg, u, Su, what="attn step layer %d gus" % l)
+        hd, Sd = oracle.q4_res_gemv(oracle._hw(L.Wd), s["h"].cpu().numpy(), s["hid_o"].cpu().numpy())
+        check_residual(to_np(s["hid"]), hd, Sd, what="attn step layer %d down" % l)
+    fin = snaps[-1]
+    _, lref, _ = oracle.q4_argmax(oracle._hw(cfg.Wlogits), fin["final"].cpu().numpy(), cfg.gamma_final, cfg.eps)
+    check_argmax(fin["idx"].cpu().numpy(), lref, what="attn step argmax")
+    # the captured graph gives the same bits (the appended rows are rewritten
+    # with the same values)
+    g = step.capture()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(step.idx, fin["idx"]) and torch.equal(step.hid, fin["final"])
+
+
 def test_fused_decode_step_teacher_forced(q4):
     """The persistent-kernel step, layer by layer: running it on the first L
     layers gives that prefix's hidden state (the same per-layer arithmetic
