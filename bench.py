@@ -535,14 +535,21 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     # which a prefill chunk also sees; the activations are new each call)
     H = wl.draw_q4_0(rng, n, k)
     Wg = q4.Q4Weight.from_q4_0(H.blocks, n, k, device)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16_peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        bf16_peak = None
     for nbg in (64, 256, 512):
         xg = torch.from_numpy(wl.draw_x(rng, nbg, k)).to(device)
         yg = torch.empty((nbg, n), dtype=torch.float32, device=device)
         wsg = torch.empty(int(q4.lib().q4_gemm_workspace_bytes(nbg, k)), dtype=torch.uint8, device=device)
         t = bench_calls([Wg], lambda W: q4.q4_gemm(W, xg, out=yg, workspace=wsg))
+        tf = 2.0 * n * k * nbg / t / 1e12
         out["gemm_q4_0_n%d_k%d_nb%d" % (n, k, nbg)] = {
-            "us": round(t * 1e6, 3), "tflops": round(2.0 * n * k * nbg / t / 1e12, 1),
-            "what": "staging pass + GEMM (mma.sync f16, fp32 accumulate), weights exact"}
+            "us": round(t * 1e6, 3), "tflops": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / bf16_peak, 4) if bf16_peak else None,
+            "what": "staging pass + GEMM (mma.sync f16, fp32 accumulate), weights exact; peak: measured cuBLAS bf16"}
     del Wg
     torch.cuda.empty_cache()
     # decode attention of one token (RoPE, KV append, softmax(q K^T) V) at
@@ -857,6 +864,50 @@ def _oracle_steps(cfg, threads: int, budget_s: float, max_steps: int):
         oracle.set_threads(old)
 
 
+def cpu_rows(cores: int) -> dict:
+    """The oracle beside the kernel table's other rows, on all host cores:
+    the nb = 1 matvec of the 14336 x 4096 matrix in every format, the prefill
+    GEMM at 64 rows (on a 1024-row slice, scaled to the whole matrix), and
+    decode attention at 4096 cached positions (32 / 8 heads of 64)."""
+    import numpy as np
+
+    import oracle
+    import q4_workloads as wl
+    old = oracle.set_threads(cores)
+    out = {}
+    try:
+        rng = np.random.default_rng(3)
+        n, k = 14336, 4096
+        for fmt in ("q4_0", "affine", "q8_0", "q4_k", "q1"):
+            H = wl._draw_fmt(fmt)(rng, n, k)
+            x = wl.draw_x(rng, 1, k)
+            W = oracle._hw(H)
+            t0 = time.perf_counter()
+            oracle.q4_gemv(W, x)
+            out["%s_n%d_k%d_nb1" % (fmt, n, k)] = {"ms": round((time.perf_counter() - t0) * 1e3, 2),
+                                                   "sample": "one call"}
+        Hs = wl.draw_q4_0(rng, 1024, k)
+        x = wl.draw_x(rng, 64, k)
+        t0 = time.perf_counter()
+        oracle.q4_gemv(oracle._hw(Hs), x)
+        el = time.perf_counter() - t0
+        out["gemm_q4_0_n%d_k%d_nb64" % (n, k)] = {"ms": round(el * 1e3 * n / 1024, 1),
+                                                  "sample": "1024 of the 14336 rows, scaled by 14"}
+        H_, Hkv_, D_, ctx = 32, 8, 64, 4096
+        kc = rng.standard_normal((Hkv_, ctx, D_))
+        vc = rng.standard_normal((Hkv_, ctx, D_))
+        q = rng.standard_normal((H_, D_))
+        kn, vn = rng.standard_normal((Hkv_, D_)), rng.standard_normal((Hkv_, D_))
+        c, sn = oracle.rope_table(ctx, D_, 10000.0)
+        t0 = time.perf_counter()
+        oracle.attn_decode(q, kn, vn, kc, vc, ctx - 1, 0, 0.125, c, sn)
+        out["attn_decode_h%d_kv%d_d%d_ctx%d" % (H_, Hkv_, D_, ctx)] = {
+            "ms": round((time.perf_counter() - t0) * 1e3, 2), "sample": "one call, 1 thread (heads in sequence)"}
+    finally:
+        oracle.set_threads(old)
+    return out
+
+
 def cpu_baseline_sample(cfg, wbytes: int, budget_s: float = 8.0) -> dict:
     """The f64 C oracle on whole decode steps of the same workload: on all
     host cores (the output rows of every GEMV split over threads; rows are
@@ -867,7 +918,9 @@ def cpu_baseline_sample(cfg, wbytes: int, budget_s: float = 8.0) -> dict:
     cores = os.cpu_count() or 1
     n_all, el_all = _oracle_steps(cfg, cores, budget_s, 40)
     n_one, el_one = _oracle_steps(cfg, 1, budget_s, 10)
-    return {"value": round(wbytes * n_all / el_all / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+    rows = cpu_rows(cores)
+    return {"rows": rows,
+            "value": round(wbytes * n_all / el_all / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": "%d full decode step(s) (%d weight bytes each) in the f64 C oracle on %d threads, %.1f s"
                       % (n_all, wbytes, cores, el_all),
             "cpu_model": cpu_model(), "nproc": cores,
