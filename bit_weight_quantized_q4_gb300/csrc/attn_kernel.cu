@@ -96,7 +96,8 @@ Q4_HD constexpr int attn_sub(int D) { return D == 64 ? 64 : 32; }
 // Shared memory of a CTA: 2 mbarriers per stage (64 bytes in all), the ring
 // (per stage LS rows of K, then of V; at the end it holds the fold weights),
 // the warps' outputs [NW][G * D], their running maxima and sums [NW][G], the
-// fold's sums [G] and the last-split flag.
+// fold's sums [G], per warp one step's 32 softmax weights and G rescale
+// factors, and the last-split flag.
 //
 // Each warp keeps its own running softmax over the positions it scores (per
 // head: maximum, sum, and the output, rescaled whenever the maximum grows), so
