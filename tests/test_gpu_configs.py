@@ -189,6 +189,24 @@ def test_decode_step_with_attention_teacher_forced(q4):
     assert torch.equal(step.idx, fin["idx"]) and torch.equal(step.hid, fin["final"])
 
 
+@pytest.mark.parametrize("fmt,window", [("q4_0", 0), ("affine", 40), ("q8_0", 0), ("q4_k", 17), ("q1", 0)])
+def test_decode_step_with_attention_every_format(q4, fmt, window):
+    """The real step at small widths (4 heads / 2 kv heads of 64) in every
+    weight format, with and without a sliding window: its final hidden state
+    and argmax against the oracle's real step (not teacher-forced: two layers
+    stay well inside the tolerance scale)."""
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+    spec = wl.AttnSpec(heads=4, kv_heads=2, head_dim=64, max_seq=128, position=100, window=window)
+    cfg = wl.cfg4(seed=17, layers=2, hidden=256, kv=128, inter=512, vocab=500, nb=1, fmt=fmt)
+    caches = wl.draw_kv_caches(17, 2, spec)
+    step = DecodeStep(cfg, attention=(spec, caches))
+    step.run()
+    torch.cuda.synchronize()
+    idx_ref, lref, hid_ref = oracle.decode_step(cfg, attention=(spec, caches))
+    check_argmax(step.idx.cpu().numpy(), lref, what="real step %s argmax" % fmt)
+    assert np.allclose(to_np(step.hid), hid_ref, rtol=2e-3, atol=2e-3), "real step %s hidden state" % fmt
+
+
 def test_fused_decode_step_teacher_forced(q4):
     """The persistent-kernel step, layer by layer: running it on the first L
     layers gives that prefix's hidden state (the same per-layer arithmetic
