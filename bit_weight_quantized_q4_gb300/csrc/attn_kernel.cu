@@ -12,7 +12,9 @@
 // running softmax per head over its positions (flash decoding); every query
 // head of the group reuses each row.  The last split of a kv head to finish folds the splits' shares in
 // split order: one launch, and a result that does not depend on the order in
-// which the CTAs ran.
+// which the CTAs ran.  The launch is a programmatic dependent of the kernel
+// before it (the projection that writes q, k and v), so CTAs that find an SM
+// free start while it runs and warm L2 with their first cache rows.
 #include "gemv_launch.cuh"
 
 namespace q4 {
@@ -87,6 +89,13 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
     return v[0];
 }
 
+// Start pulling `bytes` (16-byte aligned, a multiple of 16) of global memory
+// into L2 and go on.  A hint only: every later read of those bytes goes
+// through L2, the point of coherence, so it sees every write made since.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 constexpr int kAttnWarps = 8;
 constexpr int kAttnStages = 2;  // ring stages of K and V sub-chunks
 
@@ -135,14 +144,24 @@ __global__ void __launch_bounds__(kAttnWarps * 32, (G * D <= 512 ? 2 : 1))
         mbar_expect_tx(bv, bytes);
         bulk_g2s(smem_u32(kst + LS * D), p.v_cache + row0 + (size_t)j * LS * D, bytes, bv, pol);
     };
+    // Launched as a programmatic dependent of the previous kernel, which may
+    // still be running: until griddepcontrol.wait nothing it (or anything
+    // before it) writes is read -- the first stages' K and V rows only go to
+    // L2, a hint that cannot return old data.  The next kernel may launch now;
+    // it waits for this one to finish before it reads what this one writes.
     if (tid == 0) {
+        const uint32_t pre = (uint32_t)min(n, S * LS) * D * 4;
+        bulk_prefetch_l2(p.k_cache + row0, pre);
+        bulk_prefetch_l2(p.v_cache + row0, pre);
         for (int st = 0; st < S; ++st) {
             mbar_init(bars + 16 * st, 1);
             mbar_init(bars + 16 * st + 8, 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid == 0)
         for (int j = 0; j < min(S, nsub); ++j) issue(j);
 
@@ -390,9 +409,17 @@ static int launch_attn_dg(const AttnParams &p, cudaStream_t stream) {
     static size_t smem_set[64] = {0};
     const size_t smem = attn_smem_bytes(D, G);
     if (!raise_smem(kern, smem, smem_set)) return -1;
-    dim3 grid(p.nsplit, p.Hkv);
-    kern<<<grid, dev::kAttnWarps * 32, smem, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.nsplit, (unsigned)p.Hkv, 1);
+    cfg.blockDim = dim3(dev::kAttnWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? 0 : -1;
 }
 
 int launch_attn(const AttnParams &p, void *stream_) {
