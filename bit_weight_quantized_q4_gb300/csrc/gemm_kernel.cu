@@ -8,8 +8,8 @@
 // batches of at most 16 rows) and 128-column chunk, every 32-column block of
 // a row scaled by its own power of two and carried as one f16 per value (as
 // the engine's batch classes above four rows), the block's factor back, and
-// its offset term (the zero-weight product for Q4_0 and Q8_0, the fp32 block
-// sum for the formats with a min).  q4gemm_kernel then gives each CTA 64
+// its offset term (the zero-weight product times minus the factor back for
+// Q4_0 and Q8_0, the fp32 block sum for the formats with a min).  q4gemm_kernel then gives each CTA 64
 // weight rows (four 16-row tiles) by one activation tile: a two-stage ring of
 // TMA bulk copies brings each chunk's four weight records and its image slice
 // into shared memory, and each warp runs one weight tile against its share of
@@ -85,14 +85,18 @@ __global__ void __launch_bounds__(NT * 32) q4gemm_stage_kernel(const __grid_cons
         if constexpr (has_offset(FMT)) {
             // the block's zero-weight product, through the same tensor-core
             // chain as the weights' (so that zero weights give exactly 0):
-            // lane (g, t) ends with rows 2t and 2t + 1 of the n-tile
+            // lane (g, t) ends with rows 2t and 2t + 1 of the n-tile.  Stored
+            // times minus the rows' factors back (lanes 8t and 8t + 4 hold
+            // them): powers of two, so the product is exact and the GEMM's
+            // fma(f, d, -f o) equals f * (d - o) rounded once.
             constexpr uint32_t EL = zero_lo<FMT>();
             float e[4];
             mma16816_c(e, EL, EL, kEightHi, kEightHi, b[0], b[1], z, z, z, z);
             mma16816(e, EL, EL, kEightHi, kEightHi, b[2], b[3]);
+            const float f0 = __shfl_sync(0xffffffffu, back, 8 * t), f1 = __shfl_sync(0xffffffffu, back, 8 * t + 4);
             if (g == 0) {
-                Gs[j * ROWS + nt * 8 + 2 * t] = e[0];
-                Gs[j * ROWS + nt * 8 + 2 * t + 1] = e[1];
+                Gs[j * ROWS + nt * 8 + 2 * t] = -(f0 * e[0]);
+                Gs[j * ROWS + nt * 8 + 2 * t + 1] = -(f1 * e[1]);
             }
         } else if constexpr (has_min(FMT)) {
             // the block sum of x (its four lanes' shares, added by a butterfly)
@@ -228,11 +232,11 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 2) q4gemm_kernel(const __grid
                         const float2 f = *reinterpret_cast<const float2 *>(F + J * ROWS + ntl * 8 + 2 * t);
                         const float2 o = *reinterpret_cast<const float2 *>(Gs + J * ROWS + ntl * 8 + 2 * t);
                         // d: (row g, cols 2t, 2t+1), (row g+8, cols 2t, 2t+1)
-                        if constexpr (has_offset(FMT)) {
-                            acc[i][0] = fmaf(s2.x * f.x, d[0] - o.x, acc[i][0]);
-                            acc[i][1] = fmaf(s2.x * f.y, d[1] - o.y, acc[i][1]);
-                            acc[i][2] = fmaf(s2.y * f.x, d[2] - o.x, acc[i][2]);
-                            acc[i][3] = fmaf(s2.y * f.y, d[3] - o.y, acc[i][3]);
+                        if constexpr (has_offset(FMT)) {  // o = -f * offset: s * f * (d - offset)
+                            acc[i][0] = fmaf(s2.x, fmaf(f.x, d[0], o.x), acc[i][0]);
+                            acc[i][1] = fmaf(s2.x, fmaf(f.y, d[1], o.y), acc[i][1]);
+                            acc[i][2] = fmaf(s2.y, fmaf(f.x, d[2], o.x), acc[i][2]);
+                            acc[i][3] = fmaf(s2.y, fmaf(f.y, d[3], o.y), acc[i][3]);
                         } else if constexpr (has_min(FMT)) {
                             acc[i][0] = fmaf(m2.x, o.x, fmaf(s2.x * f.x, d[0], acc[i][0]));
                             acc[i][1] = fmaf(m2.x, o.y, fmaf(s2.x * f.y, d[1], acc[i][1]));
