@@ -659,6 +659,7 @@ extern "C" q4_status q4_gemm(const q4_weight *W, const float *x, int32_t nb, flo
     p.accumulate = accumulate != 0;
     Q4_TRY(kernel_err_ptr(&p.err));
     p.wait_cycles = g_wait_cycles;
+    p.extra_tx = g_extra_tx;
     cudaGetLastError();
     if (q4::launch_gemm(p, W->fmt, stream) != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
     return Q4_OK;

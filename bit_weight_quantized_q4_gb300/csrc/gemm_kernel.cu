@@ -171,7 +171,8 @@ __global__ void __launch_bounds__(kGemmWarps * 32, 2) q4gemm_kernel(const __grid
         uint8_t *st = ring + (size_t)(k % S) * STAGE;
         const uint32_t bar = bars + 8 * (k % S);
         const int tiles = min(4, p.T - 4 * tg);
-        mbar_expect_tx(bar, (uint32_t)(tiles * n * REC + n * IMG));
+        // extra_tx: testing the give-up path only
+        mbar_expect_tx(bar, (uint32_t)(tiles * n * REC + n * IMG) + (k == 0 ? (uint32_t)p.extra_tx : 0u));
         for (int i = 0; i < tiles; ++i)
             bulk_g2s(smem_u32(st + i * SC * REC), p.w + ((size_t)(4 * tg + i) * p.C + c0) * REC, n * REC, bar, pol);
     };

@@ -360,6 +360,7 @@ struct GemmParams {
     int n, T, C, K, nb, accumulate;
     int *err;           // set nonzero if a copy wait gave up
     long long wait_cycles;
+    int extra_tx;       // bytes the first stage expects beyond its copies (testing only; 0)
 };
 size_t gemm_image_bytes(int nb, int C);
 size_t gemm_smem_bytes(int fmt, int nb);

@@ -275,8 +275,9 @@ q4_status q4_decode_check(const void *workspace, cudaStream_t stream);
 
 /* Synchronises `stream` and reports whether any GEMV-family kernel of this
  * library on the current device (q4_gemv, q4_nrm_gemv, q4_dual_gemv,
- * q4_gus_nrm, q4_res_gemv, q4_argmax, q4_argmax_noalloc) gave up waiting for
- * its weight copies since the last check (Q4_ERR_CUDA; the flag is then
+ * q4_gus_nrm, q4_res_gemv, q4_argmax, q4_argmax_noalloc, q4_gemm,
+ * q4_attn_decode) gave up waiting for its weight (or K/V) copies since the
+ * last check (Q4_ERR_CUDA; the flag is then
  * cleared) or not (Q4_OK).  Each kernel bounds every such wait (about a
  * second); a kernel that gives up records it in a per-device word of the
  * library, stops streaming, waits (bounded) for its copies in flight and
@@ -292,7 +293,8 @@ q4_status q4_device_check(cudaStream_t stream);
  * barrier expects beyond its CTAs; copy_wait_cycles, the SM clock cycles
  * before a wait for a weight-copy stage gives up (<= 0: the default, 2^31,
  * about a second); copy_extra_bytes (0..4096, a multiple of 16), bytes each
- * weight-copy stage expects beyond its copies.  A non-zero extra makes every
+ * weight-copy stage of the GEMV kernels expects beyond its copies (the first
+ * stage only for q4_gemm and for each CTA of q4_attn_decode).  A non-zero extra makes every
  * such wait run out: the kernel then records the failure (q4_decode_check,
  * q4_device_check), waits for its copies in flight (always bounded by the
  * default second) and returns with its outputs undefined; nothing faults or

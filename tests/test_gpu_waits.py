@@ -4,8 +4,8 @@ Every wait in the library's kernels is bounded.  Here each kind is made to
 run out on purpose through the library's testing hook
 (q4_debug_wait_limits): a grid barrier of the persistent decode step that
 expects one arrival more than there are CTAs, and a weight-copy stage of a
-per-call GEMV (and of the decode attention) that expects 16 bytes more than
-its copies bring.  None faults or hangs: the kernel records the failure, waits (bounded) for its
+per-call GEMV (and of the prefill GEMM and the decode attention) that
+expects 16 bytes more than its copies bring.  None faults or hangs: the kernel records the failure, waits (bounded) for its
 copies in flight and returns.  The check call then reports Q4_ERR_CUDA, and
 the next normal call gives the same bits as before."""
 import numpy as np
@@ -88,3 +88,24 @@ def test_attention_copy_wait_gives_up_and_the_next_call_is_unchanged(q4):
     # the split counters are zero again and the result is the same
     assert torch.equal(q4.q4_attn_decode(q, kn, vn, kc, vc, pos, workspace=ws), o0)
     q4.q4_device_check()
+
+
+@pytest.mark.parametrize("nb", [9, 40])  # the 16-row and the 64-row activation tile
+def test_gemm_copy_wait_gives_up_and_the_next_call_is_unchanged(q4, nb):
+    rng = np.random.default_rng(24 + nb)
+    H = wl.draw_q4_0(rng, 300, 1024)
+    W = dev_weight(H)
+    x = torch.from_numpy(wl.draw_x(rng, nb, 1024)).cuda()
+    y0 = q4.q4_gemm(W, x)
+    q4.q4_device_check()
+    q4.q4_debug_wait_limits(copy_wait_cycles=200000, copy_extra_bytes=16)
+    try:
+        q4.q4_gemm(W, x)
+        with pytest.raises(q4.Q4Error) as e:
+            q4.q4_device_check()
+        assert e.value.status == 6
+    finally:
+        q4.q4_debug_wait_limits()
+    y1 = q4.q4_gemm(W, x)
+    q4.q4_device_check()
+    assert torch.equal(y1, y0)
