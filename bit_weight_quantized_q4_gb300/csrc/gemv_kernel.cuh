@@ -610,11 +610,11 @@ __device__ __forceinline__ uint4 chunk_b(const uint8_t *xchunk, int j, int boff,
     return b;
 }
 
-// The offset products of Q4_0 for nb = 1: per chunk, the product chain above
-// with every nibble equal to 8, once per CTA and job; block j's hi + lo goes
-// to the block-sum slot of block j.  A weight block of all eights then gives
-// exactly the same chain values, so (hi + lo) - offset is exactly zero for it.
-// Runs after the staging barrier; ends with a CTA barrier.
+// The offset products of Q4_0 (and Q8_0) for nb = 1: per chunk, the product
+// chain above with every weight at its zero code (nibble 8, byte 128), once
+// per CTA and job; block j's hi + lo goes to the block-sum slot of block j.
+// A weight block of all zero codes then gives exactly the same chain values,
+// so (hi + lo) - offset is exactly zero for it.
 template <int FMT, int CLS>
 __device__ __forceinline__ void eights_chunk(const Smem &m, int c, int lane) {
     constexpr uint32_t EL = zero_lo<FMT>();
@@ -1144,8 +1144,12 @@ __device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, S
                 const bool two = q.t0 + 2 * pl + 1 < p.T;
                 ChunkX x;
                 load_chunk<0>(x, m, cc, boff, g, t);
+                // both records without a branch, so that their products
+                // interleave; a pair whose second tile is past the end has
+                // no record in that slot (stale bytes of the stage), and
+                // flush drops what it gave
                 record_c0<FMT>(st_a, x, lane, acc[0][0], acc[0][1]);
-                if (two) record_c0<FMT>(st_a + SU * REC, x, lane, acc[1][0], acc[1][1]);
+                record_c0<FMT>(st_a + SU * REC, x, lane, acc[1][0], acc[1][1]);
                 if (++cc == cs) {  // end of this pair's slice: hand the tiles over
                     flush(pl, two);
                     cc = 0;
