@@ -355,6 +355,29 @@ def e2e_timing(step, graph, steps: int, warmup: int):
     return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
+KT_REPLAYS = 15  # timed graph replays per kernel-table row
+
+
+class Timed(float):
+    """A per-call time in seconds: the median over the timed replays (each
+    replay a graph of back-to-back calls), carrying their 10th and 90th
+    percentiles."""
+
+    def __new__(cls, per_call):
+        import numpy as np
+        p10, p50, p90 = (float(v) for v in np.percentile(np.asarray(per_call, dtype=np.float64), [10, 50, 90]))
+        self = super().__new__(cls, p50)
+        self.p10, self.p90 = p10, p90
+        return self
+
+
+def spread(t) -> dict:
+    """The p10 / p90 fields of a kernel-table row (µs), for a Timed value."""
+    if not isinstance(t, Timed):
+        return {}
+    return {"us_p10": round(t.p10 * 1e6, 3), "us_p90": round(t.p90 * 1e6, 3)}
+
+
 def stream_ceiling(Ws, bench_calls, peak: float, tag: str) -> dict:
     """What one launch of a library kernel reaches on the same packed bytes,
     over the same rotation and back-to-back graph as the GEMV rows: a
@@ -370,11 +393,13 @@ def stream_ceiling(Ws, bench_calls, peak: float, tag: str) -> dict:
     t_read = bench_calls(Ws, lambda W: W.tensor.view(torch.int32).sum())
     del dsts
     return {
-        tag + "_copy": {"us": round(t_copy * 1e6, 3), "read_gbs": round(nbytes / t_copy / 1e9, 1),
+        tag + "_copy": {"us": round(t_copy * 1e6, 3), **spread(t_copy),
+                        "read_gbs": round(nbytes / t_copy / 1e9, 1),
                         "read_write_gbs": round(2 * nbytes / t_copy / 1e9, 1),
                         "frac_of_hbm": round(2 * nbytes / t_copy / 1e9 / peak, 4),
                         "what": "device-to-device copy of the packed bytes (reads and writes each byte)"},
-        tag + "_library_read": {"us": round(t_read * 1e6, 3), "read_gbs": round(nbytes / t_read / 1e9, 1),
+        tag + "_library_read": {"us": round(t_read * 1e6, 3), **spread(t_read),
+                                "read_gbs": round(nbytes / t_read / 1e9, 1),
                                 "frac_of_hbm": round(nbytes / t_read / 1e9 / peak, 4),
                                 "what": "torch int32 sum over the packed bytes: a library kernel reading each byte once"},
     }
@@ -382,7 +407,9 @@ def stream_ceiling(Ws, bench_calls, peak: float, tag: str) -> dict:
 
 def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     """Per-shape cold timings of single calls: a graph of `reps` back-to-back
-    calls over rotating weight copies whose total exceeds 3x L2."""
+    calls over rotating weight copies whose total exceeds 3x L2, replayed
+    KT_REPLAYS times; `us` is the median per call, `us_p10` / `us_p90` the
+    spread over the replays."""
     import numpy as np
     import torch
 
@@ -403,11 +430,7 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
                 fn(weights[i % len(weights)])
         g.replay()
         torch.cuda.synchronize()
-        best = None
-        for _ in range(3):
-            t = time_replays(g, 1, torch.cuda.current_stream())
-            best = t if best is None else min(best, t)
-        return best / n_calls
+        return Timed([time_replays(g, 1, torch.cuda.current_stream()) / n_calls for _ in range(KT_REPLAYS)])
 
     for fmt in ("affine", "q4_0", "q8_0", "q4_k", "q1"):
         H = wl._draw_fmt(fmt)(rng, n, k)
@@ -423,15 +446,22 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
             # context: a vendor reduction (torch.amax) reading the same packed bytes, same rotation
             t_ref = bench_calls(Ws, lambda W: torch.amax(W.tensor))
             out["%s_n%d_k%d_vendor_read" % (fmt, n, k)] = {
-                "us": round(t_ref * 1e6, 3), "packed_gbs": round(W0.nbytes / t_ref / 1e9, 1),
+                "us": round(t_ref * 1e6, 3), **spread(t_ref), "packed_gbs": round(W0.nbytes / t_ref / 1e9, 1),
                 "what": "torch.amax over the packed weight bytes: a library kernel reading the same bytes"}
         for nb in ((1, 2, 4, 8, 16) if fmt == "affine" else (1,)):
             x = torch.from_numpy(wl.draw_x(rng, nb, k)).to(device)
             y = torch.empty((nb, n), dtype=torch.float32, device=device)
             t = bench_calls(Ws, lambda W: q4.q4_gemv(W, x, out=y))
             gbs = W0.weight_bytes / t / 1e9
-            out["%s_n%d_k%d_nb%d" % (fmt, n, k, nb)] = {"us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1),
-                                                      "frac_of_hbm": round(gbs / peak, 4)}
+            out["%s_n%d_k%d_nb%d" % (fmt, n, k, nb)] = {"us": round(t * 1e6, 3), **spread(t),
+                                                      "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
+            if fmt == "q4_0":
+                # warm: one copy reused, its bytes resident in L2 between calls
+                t = bench_calls([W0], lambda W: q4.q4_gemv(W, x, out=y))
+                gbs = W0.weight_bytes / t / 1e9
+                out["%s_n%d_k%d_nb%d_warm" % (fmt, n, k, nb)] = {
+                    "us": round(t * 1e6, 3), **spread(t), "weight_gbs": round(gbs, 1),
+                    "what": "one weight copy reused: warm, its bytes in L2 (not an HBM figure)"}
         if fmt == "affine":
             # the prefill GEMM at verify widths: one weight stream shared by a
             # 16-row activation tile (staging pass included)
@@ -442,7 +472,8 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
                 t = bench_calls(Ws, lambda W: q4.q4_gemm(W, x, out=y, workspace=wsg))
                 gbs = W0.weight_bytes / t / 1e9
                 out["%s_n%d_k%d_nb%d_gemm" % (fmt, n, k, nb)] = {
-                    "us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
+                    "us": round(t * 1e6, 3), **spread(t), "weight_gbs": round(gbs, 1),
+                    "frac_of_hbm": round(gbs / peak, 4)}
             # the same matvec fed a HalfSet (f16 even/odd streams + group sums,
             # packed once): what a caller verifying several drafts per step runs
             for nb in (8, 16):
@@ -452,7 +483,8 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
                 t = bench_calls(Ws, lambda W: q4.q4_gemv_half(W, xe, xo, gsum=gs, out=y))
                 gbs = W0.weight_bytes / t / 1e9
                 out["%s_n%d_k%d_nb%d_halfset" % (fmt, n, k, nb)] = {
-                    "us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
+                    "us": round(t * 1e6, 3), **spread(t), "weight_gbs": round(gbs, 1),
+                    "frac_of_hbm": round(gbs / peak, 4)}
         if fmt == "q4_0":
             out.update(stream_ceiling(Ws, bench_calls, peak, "%s_n%d_k%d" % (fmt, n, k)))
         del Ws
@@ -476,7 +508,8 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     Ws = copies_of(c0.W, count_for(c0.W))
     x0, y0 = T(c0.x), torch.empty((1, c0.W.n), dtype=torch.float32, device=device)
     t = bench_calls(Ws, lambda W: q4.q4_gemv(W, x0, out=y0))
-    out["cfg0_q4_gemv_1024x1024"] = {"us": round(t * 1e6, 3), "weight_gbs": round(Ws[0].weight_bytes / t / 1e9, 1)}
+    out["cfg0_q4_gemv_1024x1024"] = {"us": round(t * 1e6, 3), **spread(t),
+                                     "weight_gbs": round(Ws[0].weight_bytes / t / 1e9, 1)}
     del Ws
     c1 = wl.cfg1()
     cnt = count_for(c1.Wq, c1.Wk, c1.Wv)
@@ -486,9 +519,10 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     yk = torch.empty((1, c1.Wk.n), dtype=torch.float32, device=device)
     yv = torch.empty((1, c1.Wv.n), dtype=torch.float32, device=device)
     t = bench_calls(list(range(cnt)), lambda i: q4.q4_nrm_gemv(Wq[i], x1, g1, c1.eps, out=yq))
-    out["cfg1_q4_nrm_gemv_2048x2048"] = {"us": round(t * 1e6, 3), "weight_gbs": round(Wq[0].weight_bytes / t / 1e9, 1)}
+    out["cfg1_q4_nrm_gemv_2048x2048"] = {"us": round(t * 1e6, 3), **spread(t),
+                                         "weight_gbs": round(Wq[0].weight_bytes / t / 1e9, 1)}
     t = bench_calls(list(range(cnt)), lambda i: q4.q4_dual_gemv(Wk[i], Wv[i], x1, g1, c1.eps, out_a=yk, out_b=yv))
-    out["cfg1_q4_dual_gemv_2x512x2048"] = {"us": round(t * 1e6, 3),
+    out["cfg1_q4_dual_gemv_2x512x2048"] = {"us": round(t * 1e6, 3), **spread(t),
                                            "weight_gbs": round(2 * Wk[0].weight_bytes / t / 1e9, 1)}
     del Wq, Wk, Wv
     c2 = wl.cfg2()
@@ -497,7 +531,7 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     x2, g2 = T(c2.x), T(c2.gamma)
     h2 = torch.empty((1, c2.Wg.n), dtype=torch.float32, device=device)
     t = bench_calls(list(range(cnt)), lambda i: q4.q4_gus_nrm(Wg[i], Wu[i], x2, g2, c2.eps, out=h2))
-    out["cfg2_q4_gus_nrm_2x8192x2048"] = {"us": round(t * 1e6, 3),
+    out["cfg2_q4_gus_nrm_2x8192x2048"] = {"us": round(t * 1e6, 3), **spread(t),
                                           "weight_gbs": round(2 * Wg[0].weight_bytes / t / 1e9, 1),
                                           "frac_of_hbm": round(2 * Wg[0].weight_bytes / t / 1e9 / peak, 4)}
     del Wg, Wu
@@ -506,7 +540,7 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     r2 = T(c2.r)
     yd = torch.empty((1, c2.Wd.n), dtype=torch.float32, device=device)
     t = bench_calls(list(range(cnt)), lambda i: q4.q4_res_gemv(Wd[i], h2, r2, out=yd))
-    out["cfg2_q4_res_gemv_2048x8192"] = {"us": round(t * 1e6, 3),
+    out["cfg2_q4_res_gemv_2048x8192"] = {"us": round(t * 1e6, 3), **spread(t),
                                          "weight_gbs": round(Wd[0].weight_bytes / t / 1e9, 1),
                                          "frac_of_hbm": round(Wd[0].weight_bytes / t / 1e9 / peak, 4)}
     del Wd
@@ -524,7 +558,7 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
     y = torch.empty((1, n4), dtype=torch.float32, device=device)
     t = bench_calls(Ws, lambda W: q4.q4_gemv(W, x, out=y))
     gbs = W0.weight_bytes / t / 1e9
-    out["q4_0_n%d_k%d_nb1" % (n4, k)] = {"us": round(t * 1e6, 3), "weight_gbs": round(gbs, 1),
+    out["q4_0_n%d_k%d_nb1" % (n4, k)] = {"us": round(t * 1e6, 3), **spread(t), "weight_gbs": round(gbs, 1),
                                          "frac_of_hbm": round(gbs / peak, 4),
                                          "what": "4x the rows of the 14336 x 4096 case: launch overhead amortised"}
     out.update(stream_ceiling(Ws, bench_calls, peak, "q4_0_n%d_k%d" % (n4, k)))
@@ -547,7 +581,7 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
         t = bench_calls([Wg], lambda W: q4.q4_gemm(W, xg, out=yg, workspace=wsg))
         tf = 2.0 * n * k * nbg / t / 1e12
         out["gemm_q4_0_n%d_k%d_nb%d" % (n, k, nbg)] = {
-            "us": round(t * 1e6, 3), "tflops": round(tf, 1),
+            "us": round(t * 1e6, 3), **spread(t), "tflops": round(tf, 1),
             "frac_of_bf16_peak": round(tf / bf16_peak, 4) if bf16_peak else None,
             "what": "staging pass + GEMM (mma.sync f16, fp32 accumulate), weights exact; peak: measured cuBLAS bf16"}
     del Wg
@@ -571,7 +605,7 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
                                                             rope=tables, out=oa, workspace=ws))
         gbs = kv_bytes / t / 1e9
         out["attn_decode_h%d_kv%d_d%d_ctx%d" % (H_, Hkv_, D_, ctx)] = {
-            "us": round(t * 1e6, 3), "kv_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
+            "us": round(t * 1e6, 3), **spread(t), "kv_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
             "what": "f32 K and V rows of every kv head read once per call"}
         del caches
         torch.cuda.empty_cache()
