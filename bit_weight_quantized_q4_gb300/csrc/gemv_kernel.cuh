@@ -63,6 +63,15 @@ __device__ __forceinline__ uint4 lds128_at(uint32_t a) {
                  : "memory");
     return v;
 }
+// A 16-byte shared load into v where p is non-zero; elsewhere v keeps its
+// value (a predicated load, no select).
+template <int OFF>
+__device__ __forceinline__ void lds128_if(uint4 &v, uint32_t a, uint32_t p) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t@q ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+%6];\n\t}"
+                 : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+                 : "r"(a), "r"(p), "n"(OFF)
+                 : "memory");
+}
 // mbarrier and bulk-copy (TMA engine) primitives for the weight ring.
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -995,6 +1004,26 @@ __device__ __forceinline__ void load_chunk(ChunkX &x, const Smem &m, int cc, int
     x.F = m.fs[gi];
 }
 
+// load_chunk into registers kept over a warp's units: only the lane's own
+// block (g >> 1) is loaded; its other three B registers were zeroed once
+// (zero_chunk) and stay zero, so no select is needed per chunk.
+template <int CLS>
+__device__ __forceinline__ void refresh_chunk(ChunkX &x, const Smem &m, int cc, int boff, int g, int t) {
+    const uint32_t a = smem_u32(m.xs + cc * kBlocksPerChunk * 128 + boff);
+    const uint32_t jj = (uint32_t)(g >> 1);
+    lds128_if<0>(x.B[0], a, jj == 0u);
+    lds128_if<128>(x.B[1], a, jj == 1u);
+    lds128_if<256>(x.B[2], a, jj == 2u);
+    lds128_if<384>(x.B[3], a, jj == 3u);
+    const int gi = gs_idx(cc * kBlocksPerChunk + t, 0, Cls<CLS>::GSW);
+    x.G = m.gs[gi];
+    x.F = m.fs[gi];
+}
+__device__ __forceinline__ void zero_chunk(ChunkX &x) {
+#pragma unroll
+    for (int j = 0; j < kBlocksPerChunk; ++j) x.B[j] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // A lane's weight words of one record: the nibble formats' two 16-byte words
 // (rows g and g+8, word j for block j), or Q8_0's four (rows g and g+8,
 // blocks 0-1 and 2-3).  regs<J>() gives the eight tensor-core A registers of
@@ -1091,7 +1120,10 @@ __device__ __forceinline__ void record_c0(uint32_t ra, const ChunkX &x, int lane
     }
 }
 
-template <int FMT, class RING>
+// OWNB: the chunk registers persist over the warp's units (refresh_chunk);
+// the per-call kernel takes it, the persistent step keeps load_chunk (there
+// the longer-lived registers measured slower).
+template <int FMT, bool OWNB, class RING>
 __device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, StreamOf<FMT, 0> &ws,
                              RING &ring, int warp, int lane, bool cross) {
     using C = Cls<0>;
@@ -1111,6 +1143,11 @@ __device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, S
         if (warp == C::NW - 1) m.wtab[C::NW] = q.ue;
     }
     float *my_slots = m.slots + (size_t)warp * p.SW * kTileRows;
+    ChunkX k0, k1;  // OWNB: the persistent chunk registers
+    if constexpr (OWNB) {
+        zero_chunk(k0);
+        zero_chunk(k1);
+    }
 
     // a tile's slice is done: add the four lanes of each row (a fixed
     // butterfly) and hand the sums to the fold
@@ -1143,7 +1180,12 @@ __device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, S
                 const uint32_t st_a = st_base + su * REC;
                 const bool two = q.t0 + 2 * pl + 1 < p.T;
                 ChunkX x;
-                load_chunk<0>(x, m, cc, boff, g, t);
+                if constexpr (OWNB) {
+                    refresh_chunk<0>(k0, m, cc, boff, g, t);
+                    x = k0;
+                } else {
+                    load_chunk<0>(x, m, cc, boff, g, t);
+                }
                 // both records without a branch, so that their products
                 // interleave; a pair whose second tile is past the end has
                 // no record in that slot (stale bytes of the stage), and
@@ -1162,8 +1204,15 @@ __device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, S
             int su = 0;
             for (; su + 1 < n_st; su += 2) {
                 ChunkX x0, x1;
-                load_chunk<0>(x0, m, cc, boff, g, t);
-                load_chunk<0>(x1, m, cc + 1, boff, g, t);
+                if constexpr (OWNB) {
+                    refresh_chunk<0>(k0, m, cc, boff, g, t);
+                    refresh_chunk<0>(k1, m, cc + 1, boff, g, t);
+                    x0 = k0;
+                    x1 = k1;
+                } else {
+                    load_chunk<0>(x0, m, cc, boff, g, t);
+                    load_chunk<0>(x1, m, cc + 1, boff, g, t);
+                }
                 float b0 = 0.f, b1 = 0.f;
                 record_c0<FMT>(st_base + su * REC, x0, lane, acc[0][0], acc[0][1]);
                 record_c0<FMT>(st_base + (su + 1) * REC, x1, lane, b0, b1);
@@ -1178,7 +1227,12 @@ __device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, S
             }
             if (su < n_st) {
                 ChunkX x0;
-                load_chunk<0>(x0, m, cc, boff, g, t);
+                if constexpr (OWNB) {
+                    refresh_chunk<0>(k0, m, cc, boff, g, t);
+                    x0 = k0;
+                } else {
+                    load_chunk<0>(x0, m, cc, boff, g, t);
+                }
                 record_c0<FMT>(st_base + su * REC, x0, lane, acc[0][0], acc[0][1]);
                 if (++cc == cs) {
                     flush(pl, false);
@@ -1195,12 +1249,13 @@ __device__ void run_units_c0(const GemvParams &p, const Geo &q, const Smem &m, S
 }
 
 // cross: whether a refill may move the stream to its next job (false in the
-// persistent kernel, which refills across jobs at the grid barrier).
-template <int FMT, int CLS, class RING>
+// persistent kernel, which refills across jobs at the grid barrier).  OWNB:
+// see run_units_c0.
+template <int FMT, int CLS, bool OWNB, class RING>
 __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, StreamOf<FMT, CLS> &ws,
                           RING &ring, int warp, int lane, bool cross) {
     if constexpr (CLS == 0) {
-        run_units_c0<FMT>(p, q, m, ws, ring, warp, lane, cross);
+        run_units_c0<FMT, OWNB>(p, q, m, ws, ring, warp, lane, cross);
         return;
     }
     using C = Cls<CLS>;
@@ -1729,7 +1784,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_engine_kernel(con
     const float res0 = S == 1 ? residual_prefetch<CLS>(p, q, tid) : 0.f;
 
     stage_x<FMT, CLS, CLS == 3 ? 8 : 4, CLS != 0>(p, q, m, S, tid, warp, lane);
-    run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane, true);
+    run_units<FMT, CLS, true>(p, q, m, ws, ring, warp, lane, true);
     ring.drain();
     __syncthreads();
     if (S == 1 && p.epi != EPI_ARGMAX) {
@@ -1833,7 +1888,7 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_step_kernel(const
         if (q.tiles_here == 0) continue;  // no work in this job (CTA-uniform)
         const float res0 = residual_prefetch<CLS>(p, q, tid);
         stage_x<FMT, CLS, 4, false>(p, q, m, 1, tid, warp, lane);
-        run_units<FMT, CLS>(p, q, m, ws, ring, warp, lane, false);
+        run_units<FMT, CLS, false>(p, q, m, ws, ring, warp, lane, false);
         csync<NW>();
         if (p.epi != EPI_ARGMAX) {
             fold_store<CLS>(p, q, m, group, tid, res0);
