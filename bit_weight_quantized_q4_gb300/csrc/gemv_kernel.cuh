@@ -1364,8 +1364,13 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
         for (int rc = 0; rc < 2; ++rc) {
             sw[rc] = mw[rc] = make_uint4(0u, 0u, 0u, 0u);
             dd[rc] = dm[rc] = make_float2(0.f, 0.f);
-            if (rc == 0 || two) {
-                const uint32_t ra = st_a + rc * SU * REC;
+            {
+                // both records without a branch (as for nb = 1); what a second
+                // record that is not there gives is dropped at the flush.  A
+                // pair's second slot (stale bytes if its tile is past the end)
+                // lies inside the stage; single-tile units (upt 1) have no
+                // second slot, so theirs reads the first record again.
+                const uint32_t ra = st_a + (upt == 2 ? rc * SU * REC : 0);
                 rw[rc].load(ra, lane);
                 if constexpr (FMT == 4) {  // Q1: one scale word per row pair, for every block
                     uint32_t w1;
@@ -1412,7 +1417,6 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
             }
 #pragma unroll
             for (int rc = 0; rc < 2; ++rc) {
-                if (rc == 1 && !two) continue;
                 uint32_t a[8];
                 rw[rc].template regs<blk>(a);  // rows g (even) and g + 8 (odd)
                 float2 s2, m2 = make_float2(0.f, 0.f);
