@@ -1400,7 +1400,9 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                 // the block's offset product: the same tensor-core chain as the
                 // weights' below, with every weight zero (every nibble 8 for
                 // Q4_0, every biased byte 128 for Q8_0): exactly what such a
-                // block gives, so it cancels to zero
+                // block gives, so it cancels to zero.  Kept times minus the
+                // activation row's block factor F (a power of two: exact), for
+                // both records: fma(F, T, -F G) is F (T - G) rounded once
                 constexpr uint32_t EL = zero_lo<FMT>();
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -1408,10 +1410,10 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                     mma16816_c(e, EL, EL, kEightHi, kEightHi, B[nt].x, B[nt].y, z, z, z, z);
                     mma16816(e, EL, EL, kEightHi, kEightHi, B[nt].z, B[nt].w);
                     if (C::HLN) {
-                        G[0][blk] = e[0] + e[1];
+                        G[0][blk] = -(F[0][blk] * (e[0] + e[1]));
                     } else {
-                        G[2 * nt][blk] = e[0];
-                        G[2 * nt + 1][blk] = e[1];
+                        G[2 * nt][blk] = -(F[2 * nt][blk] * e[0]);
+                        G[2 * nt + 1][blk] = -(F[2 * nt + 1][blk] * e[1]);
                     }
                 }
             }
@@ -1436,8 +1438,8 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                         const float T0 = d[0] + d[1], T2 = d[2] + d[3];
                         const float fb = F[0][blk];
                         if (has_offset(FMT)) {
-                            acc[rc][0] = fmaf(s2.x * fb, T0 - G[0][blk], acc[rc][0]);
-                            acc[rc][1] = fmaf(s2.y * fb, T2 - G[0][blk], acc[rc][1]);
+                            acc[rc][0] = fmaf(s2.x, fmaf(fb, T0, G[0][blk]), acc[rc][0]);
+                            acc[rc][1] = fmaf(s2.y, fmaf(fb, T2, G[0][blk]), acc[rc][1]);
                         } else if (!has_min(FMT)) {
                             acc[rc][0] = fmaf(s2.x * fb, T0, acc[rc][0]);
                             acc[rc][1] = fmaf(s2.y * fb, T2, acc[rc][1]);
@@ -1455,7 +1457,7 @@ __device__ void run_units(const GemvParams &p, const Geo &q, const Smem &m, Stre
                             const float gj = G[2 * nt + (j & 1)][blk];
                             float &ac = acc[rc][4 * nt + j];
                             if (has_offset(FMT)) {
-                                ac = fmaf(sj, d[j] - gj, ac);
+                                ac = fmaf(j < 2 ? s2.x : s2.y, fmaf(F[2 * nt + (j & 1)][blk], d[j], gj), ac);
                             } else if (!has_min(FMT)) {
                                 ac = fmaf(sj, d[j], ac);
                             } else {
