@@ -1781,15 +1781,20 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_engine_kernel(con
     // the next kernel may launch now; it waits for this one before it reads
     // what this one writes
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // weights do not depend on the previous kernel: start their copies first
+    // weights do not depend on the previous kernel: each warp starts its
+    // first stage's copies before waiting for it, and the rest of its ring
+    // once the activations are staged (with the whole ring in flight the
+    // staging's activation loads wait behind the copies: 9.6 against 8.9 us
+    // for the 14336 x 4096 matvec)
     const Geo q = make_geo<NW>(p, group, rank, warp);
     StreamOf<FMT, CLS> ws;
     ws.init_one(&p, q);
-    for (int s = 0; s < C::DU; ++s) ring.push(ws, lane);
+    ring.push(ws, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const float res0 = S == 1 ? residual_prefetch<CLS>(p, q, tid) : 0.f;
 
     stage_x<FMT, CLS, CLS == 3 ? 8 : 4, CLS != 0>(p, q, m, S, tid, warp, lane);
+    for (int s = 1; s < C::DU; ++s) ring.push(ws, lane);
     run_units<FMT, CLS, true>(p, q, m, ws, ring, warp, lane, true);
     ring.drain();
     __syncthreads();
