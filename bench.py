@@ -179,7 +179,8 @@ def measured_peaks() -> tuple[float, str]:
 
 
 # the sources that define the persistent decode-step kernel and its launch
-STEP_SOURCES = ("capi.cu", "gemv_kernel.cuh", "gemv_launch.cuh", "gemv_q4_0.cu", "q4_internal.h")
+STEP_SOURCES = ("attn_common.cuh", "capi.cu", "gemv_kernel.cuh", "gemv_launch.cuh", "gemv_q4_0.cu", "q4_internal.h",
+                "step_attn.cuh")
 
 
 def kernel_source_hash(names=STEP_SOURCES) -> str:
@@ -804,7 +805,17 @@ def run_ours(args, rank, world, local):
                 "us_per_step": round(a_secs * 1e6 / args.steps, 2),
                 "bytes_per_step": a_bytes, "gbs": round(a_bytes * args.steps / a_secs / 1e9, 2),
                 "frac_of_hbm_peak": round(a_bytes * args.steps / a_secs / 1e9 / peak, 4)}
-        del ag, astep
+        del ag
+        # the same real step as one persistent kernel (q4_decode_step_attn)
+        fg = astep.capture(fused=True)
+        for _ in range(max(1, args.warmup)):
+            fg.replay()
+        f_secs = time_replays(fg, args.steps, stream)
+        q4.q4_decode_check(astep.check_ws)
+        real["persistent"] = {"kernels_per_step": 1, "us_per_step": round(f_secs * 1e6 / args.steps, 2),
+                              "gbs": round(a_bytes * args.steps / f_secs / 1e9, 2),
+                              "frac_of_hbm_peak": round(a_bytes * args.steps / f_secs / 1e9 / peak, 4)}
+        del fg, astep
         torch.cuda.empty_cache()
 
     l2 = int(getattr(props, "L2_cache_size", 0) or 0)

@@ -53,6 +53,13 @@ class _CDecodeLayer(ctypes.Structure):
                 ("gamma_post", ctypes.c_void_p), ("attn", ctypes.c_void_p)]
 
 
+class _CStepAttention(ctypes.Structure):
+    _fields_ = [("k_caches", ctypes.c_void_p), ("v_caches", ctypes.c_void_p), ("rope_cos", ctypes.c_void_p),
+                ("rope_sin", ctypes.c_void_p), ("out", ctypes.c_void_p), ("max_seq", ctypes.c_int32),
+                ("position", ctypes.c_int32), ("window", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
 _lib = None
 
 
@@ -98,6 +105,8 @@ def lib() -> ctypes.CDLL:
             "q4_argmax_noalloc": (I32, [W, P, P, F, I32, P, P, P, P]),
             "q4_decode_workspace_bytes": (SZ, [I32]),
             "q4_decode_step": (I32, [P, I32, W, P, F, I32, P, P, P, P, P, P, P, P, P, SZ, P]),
+            "q4_decode_attn_workspace_bytes": (SZ, [I32, I32, I32]),
+            "q4_decode_step_attn": (I32, [P, I32, P, W, P, F, P, P, P, P, P, P, P, P, P, SZ, P]),
             "q4_decode_check": (I32, [P, P]),
             "q4_device_check": (I32, [P]),
             "q4_debug_wait_limits": (I32, [ctypes.c_int64, I32, ctypes.c_int64, I32]),
@@ -512,6 +521,79 @@ class DecodeLayers:
 
     def __len__(self):
         return len(self.layers)
+
+
+def q4_decode_attn_workspace_bytes(heads: int, kv_heads: int, head_dim: int) -> int:
+    return int(lib().q4_decode_attn_workspace_bytes(heads, kv_heads, head_dim))
+
+
+class StepAttention:
+    """The decode attention of ``q4_decode_step_attn``: per-layer caches
+    (``[kv_heads][max_seq][head_dim]`` float32 CUDA tensors), optional RoPE
+    tables, the attention output buffer ``out`` (``[1, heads*head_dim]``)
+    and the geometry.  Keeps the tensors and the host pointer arrays alive."""
+
+    def __init__(self, caches, out, position: int, window: int = 0, rope=None, scale: float | None = None):
+        torch = _torch()
+        self.caches = [(_dev_f32(kc, "k_cache"), _dev_f32(vc, "v_cache")) for kc, vc in caches]
+        if not self.caches:
+            raise ValueError("no caches")
+        kv_heads, max_seq, head_dim = self.caches[0][0].shape
+        for kc, vc in self.caches:
+            if tuple(kc.shape) != (kv_heads, max_seq, head_dim) or tuple(vc.shape) != (kv_heads, max_seq, head_dim):
+                raise ValueError("every cache must be [kv_heads, max_seq, head_dim] like the first")
+        self.out = _dev_f32(out, "out")
+        heads = self.out.numel() // head_dim
+        if heads * head_dim != self.out.numel():
+            raise ValueError("out must hold heads * head_dim values")
+        self.rope = None
+        if rope is not None:
+            c, sn = (_dev_f32(t, "rope table") for t in rope)
+            if tuple(c.shape) != (max_seq, head_dim // 2) or tuple(sn.shape) != (max_seq, head_dim // 2):
+                raise ValueError("rope tables must be [max_seq, head_dim/2]")
+            self.rope = (c, sn)
+        self._k = (ctypes.c_void_p * len(self.caches))(*[kc.data_ptr() for kc, _ in self.caches])
+        self._v = (ctypes.c_void_p * len(self.caches))(*[vc.data_ptr() for _, vc in self.caches])
+        self.c = _CStepAttention(ctypes.cast(self._k, ctypes.c_void_p), ctypes.cast(self._v, ctypes.c_void_p),
+                                 None if self.rope is None else self.rope[0].data_ptr(),
+                                 None if self.rope is None else self.rope[1].data_ptr(), self.out.data_ptr(),
+                                 max_seq, int(position), int(window), heads, kv_heads, head_dim,
+                                 0.0 if scale is None else float(scale))
+        self.heads, self.kv_heads, self.head_dim = heads, kv_heads, head_dim
+
+    def __len__(self):
+        return len(self.caches)
+
+
+def q4_decode_step_attn(layers: DecodeLayers, att: StepAttention, Wlogits: Q4Weight, gamma_final, eps: float, x_in,
+                        hid, q, k, v, h, idx, val, workspace, n_layers: int | None = None):
+    """The real decode step (each layer's decode attention between its q/k/v
+    and o projections) as a single persistent kernel (``q4_decode_step_attn``
+    in the C header); nb = 1.  All buffers are caller-owned CUDA tensors."""
+    torch = _torch()
+    n = len(layers) if n_layers is None else int(n_layers)
+    if n > len(att):
+        raise ValueError("fewer caches than layers")
+    x_in = _dev_f32(x_in, "x_in")
+    if x_in.shape[0] != 1:
+        raise ValueError("the attention step takes one activation row")
+    idx = _dev_buf(idx, "idx", torch.int32, (1,), x_in.device)
+    if val is not None:
+        val = _dev_buf(val, "val", torch.float32, (1,), x_in.device)
+    workspace = _dev_buf(workspace, "workspace", torch.uint8, None, x_in.device,
+                         min_numel=max(1, q4_decode_attn_workspace_bytes(att.heads, att.kv_heads, att.head_dim)))
+    L0 = layers.layers[0]
+    hidden = L0.Wo.n
+    for t, name, width in ((x_in, "x_in", hidden), (hid, "hid", hidden), (q, "q", L0.Wq.n), (k, "k", L0.Wk.n),
+                           (v, "v", L0.Wv.n), (h, "h", L0.Wg.n)):
+        _dev_buf(t, name, torch.float32, (1, width), x_in.device)
+    _check(lib().q4_decode_step_attn(ctypes.cast(layers.arr, ctypes.c_void_p), n, ctypes.byref(att.c),
+                                     Wlogits.cref(), _dev_f32(gamma_final, "gamma_final").data_ptr(), float(eps),
+                                     x_in.data_ptr(), _dev_f32(hid, "hid").data_ptr(), _dev_f32(q, "q").data_ptr(),
+                                     _dev_f32(k, "k").data_ptr(), _dev_f32(v, "v").data_ptr(),
+                                     _dev_f32(h, "h").data_ptr(), idx.data_ptr(),
+                                     None if val is None else val.data_ptr(), workspace.data_ptr(),
+                                     workspace.numel(), _stream()), "q4_decode_step_attn")
 
 
 def q4_decode_step(layers: DecodeLayers, Wlogits: Q4Weight, gamma_final, eps: float, x_in, hid, q, k, v, h,

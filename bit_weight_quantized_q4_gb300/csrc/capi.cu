@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "../../include/q4gemv.h"
@@ -433,7 +434,7 @@ namespace {
 
 constexpr int kStepMaxGroups = 1024;  // bound on the CTAs of a step (argmax pairs)
 
-q4_status check_layer_shapes(const q4_decode_layer &L, int fmt, int hidden, int inter) {
+q4_status check_layer_shapes(const q4_decode_layer &L, int fmt, int hidden, int inter, bool need_attn) {
     const q4_weight *ws[7] = {&L.Wq, &L.Wk, &L.Wv, &L.Wo, &L.Wg, &L.Wu, &L.Wd};
     for (const q4_weight *w : ws) {
         Q4_TRY(check_weight(w));
@@ -443,8 +444,8 @@ q4_status check_layer_shapes(const q4_decode_layer &L, int fmt, int hidden, int 
         return Q4_ERR_SHAPE;
     if (L.Wo.n != hidden || L.Wd.n != hidden || L.Wg.n != inter || L.Wu.n != inter || L.Wd.k != inter)
         return Q4_ERR_SHAPE;
-    if (!L.gamma_in || !L.gamma_post || !L.attn) return Q4_ERR_NULL;
-    if (!aligned16(L.gamma_in) || !aligned16(L.gamma_post) || !aligned16(L.attn)) return Q4_ERR_ALIGN;
+    if (!L.gamma_in || !L.gamma_post || (need_attn && !L.attn)) return Q4_ERR_NULL;
+    if (!aligned16(L.gamma_in) || !aligned16(L.gamma_post) || (need_attn && !aligned16(L.attn))) return Q4_ERR_ALIGN;
     return Q4_OK;
 }
 
@@ -486,6 +487,17 @@ void finish_job(q4::GemvParams &p, int &TGmax, int &Kmax, int &SWmax) {
     if (p.K > Kmax) Kmax = p.K;
 }
 
+// The attention form's workspace: the 16-byte header, the kv heads' split
+// tickets (64 bytes: up to 16 kv heads), the argmax pairs, then the splits'
+// partial outputs, maxima and sums for up to kStepMaxGroups / kv_heads splits.
+constexpr size_t kAttnTicketOff = 16, kAttnPairsOff = 80;
+constexpr int kStepAttnMaxKvHeads = 16;
+bool step_attn_geometry_ok(int heads, int kv_heads, int head_dim) {
+    return head_dim == q4::kStepAttnD && kv_heads >= 1 && kv_heads <= kStepAttnMaxKvHeads &&
+           heads == q4::kStepAttnG * kv_heads;
+}
+size_t step_attn_partials_off() { return kAttnPairsOff + (size_t)8 * kStepMaxGroups; }
+
 }  // namespace
 
 extern "C" size_t q4_decode_workspace_bytes(int32_t nb) {
@@ -493,18 +505,54 @@ extern "C" size_t q4_decode_workspace_bytes(int32_t nb) {
     return 16 + (size_t)8 * nb * kStepMaxGroups;
 }
 
+extern "C" size_t q4_decode_attn_workspace_bytes(int32_t heads, int32_t kv_heads, int32_t head_dim) {
+    if (!step_attn_geometry_ok(heads, kv_heads, head_dim)) return 0;
+    const size_t splits = (size_t)kStepMaxGroups / kv_heads;
+    return step_attn_partials_off() + splits * heads * (head_dim + 2) * sizeof(float);
+}
+
+namespace {
+q4_status run_step(const q4_decode_layer *layers, int32_t n_layers, const q4_step_attention *att,
+                   const q4_weight *Wlogits, const float *gamma_final, float eps, int32_t nb, const float *x_in,
+                   float *hid, float *q, float *k, float *v, float *h, int32_t *idx, float *val, void *workspace,
+                   size_t ws_bytes, cudaStream_t stream);
+}  // namespace
+
+extern "C" q4_status q4_decode_step_attn(const q4_decode_layer *layers, int32_t n_layers,
+                                         const q4_step_attention *att, const q4_weight *Wlogits,
+                                         const float *gamma_final, float eps, const float *x_in, float *hid,
+                                         float *q, float *k, float *v, float *h, int32_t *idx, float *val,
+                                         void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (!att) return Q4_ERR_NULL;
+    return run_step(layers, n_layers, att, Wlogits, gamma_final, eps, 1, x_in, hid, q, k, v, h, idx, val, workspace,
+                    ws_bytes, stream);
+}
+
 extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_layers, const q4_weight *Wlogits,
                                     const float *gamma_final, float eps, int32_t nb, const float *x_in,
                                     float *hid, float *q, float *k, float *v, float *h, int32_t *idx,
                                     float *val, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    return run_step(layers, n_layers, nullptr, Wlogits, gamma_final, eps, nb, x_in, hid, q, k, v, h, idx, val,
+                    workspace, ws_bytes, stream);
+}
+
+namespace {
+// The step's jobs and launch; with `att` each layer also runs its decode
+// attention as a job between the q/k/v and the o job (nb = 1).
+q4_status run_step(const q4_decode_layer *layers, int32_t n_layers, const q4_step_attention *att,
+                   const q4_weight *Wlogits, const float *gamma_final, float eps, int32_t nb, const float *x_in,
+                   float *hid, float *q, float *k, float *v, float *h, int32_t *idx, float *val, void *workspace,
+                   size_t ws_bytes, cudaStream_t stream) {
     if (!layers || !Wlogits) return Q4_ERR_NULL;
-    if (n_layers < 1 || 4 * n_layers + 1 > q4::kMaxStepJobs) return Q4_ERR_UNSUPPORTED;
+    const int jobs_per_layer = att ? 5 : 4;
+    if (n_layers < 1 || n_layers > q4::kMaxStepLayers || jobs_per_layer * n_layers + 1 > q4::kMaxStepJobs)
+        return Q4_ERR_UNSUPPORTED;
     if (!nb_ok(nb)) return Q4_ERR_UNSUPPORTED;
     Q4_TRY(check_weight(Wlogits));
     const int fmt = Wlogits->fmt;
     const int hidden = layers[0].Wo.n, inter = layers[0].Wg.n;
     for (int l = 0; l < n_layers; ++l) {
-        Q4_TRY(check_layer_shapes(layers[l], fmt, hidden, inter));
+        Q4_TRY(check_layer_shapes(layers[l], fmt, hidden, inter, att == nullptr));
         if (layers[l].Wq.n != layers[0].Wq.n || layers[l].Wk.n != layers[0].Wk.n ||
             layers[l].Wv.n != layers[0].Wv.n || layers[l].Wo.k != layers[0].Wo.k)
             return Q4_ERR_SHAPE;
@@ -520,13 +568,43 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     Q4_TRY(check_act(h));
     if (!idx) return Q4_ERR_NULL;
     if (!aligned16(idx) || (val && !aligned16(val))) return Q4_ERR_ALIGN;
+    if (att) {  // the attention form: its own arguments and geometry
+        if (!step_attn_geometry_ok(att->heads, att->kv_heads, att->head_dim)) return Q4_ERR_UNSUPPORTED;
+        const int D = att->head_dim;
+        if (att->heads * D != hidden || att->heads * D != layers[0].Wq.n || att->kv_heads * D != layers[0].Wk.n ||
+            att->kv_heads * D != layers[0].Wv.n)
+            return Q4_ERR_SHAPE;
+        if (att->max_seq < 1 || att->max_seq > (1 << 24) || att->position < 0 || att->position >= att->max_seq ||
+            att->window < 0)
+            return Q4_ERR_SHAPE;
+        if (!att->k_caches || !att->v_caches) return Q4_ERR_NULL;
+        for (int l = 0; l < n_layers; ++l) {
+            Q4_TRY(check_act(att->k_caches[l]));
+            Q4_TRY(check_act(att->v_caches[l]));
+        }
+        if ((att->rope_cos == nullptr) != (att->rope_sin == nullptr)) return Q4_ERR_NULL;
+        if (att->rope_cos) {
+            Q4_TRY(check_act(att->rope_cos));
+            Q4_TRY(check_act(att->rope_sin));
+        }
+        Q4_TRY(check_act(att->out));
+    }
     if (!workspace) return Q4_ERR_WORKSPACE;
     if (!aligned16(workspace)) return Q4_ERR_ALIGN;
-    if (ws_bytes < q4_decode_workspace_bytes(nb)) return Q4_ERR_WORKSPACE;
+    if (ws_bytes < (att ? q4_decode_attn_workspace_bytes(att->heads, att->kv_heads, att->head_dim)
+                        : q4_decode_workspace_bytes(nb)))
+        return Q4_ERR_WORKSPACE;
 
     const int sms = num_sms();
     if (sms <= 0) return Q4_ERR_CUDA;
     const int G = sms < kStepMaxGroups ? sms : kStepMaxGroups;  // one CTA per SM
+    // the attention jobs' split of the positions: cps CTAs per kv head, each
+    // Lc positions of [lo, total), nsplit of them in use
+    int cps = 0;
+    if (att) {
+        cps = G / att->kv_heads;
+        if (cps < 1) return Q4_ERR_UNSUPPORTED;
+    }
 
     // the step's jobs; the StepParams block travels as the kernel argument
     static thread_local q4::StepParams sp;
@@ -540,6 +618,36 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     sp.nb = nb;
     sp.barrier_polls = g_barrier_polls;
     sp.barrier_extra = g_barrier_extra;
+    if (att) {
+        q4::StepAttn &A = sp.att;
+        sp.attn = 1;
+        A.q = q;
+        A.k_new = k;
+        A.v_new = v;
+        A.rope_cos = att->rope_cos;
+        A.rope_sin = att->rope_sin;
+        A.out = att->out;
+        const size_t splits = (size_t)kStepMaxGroups / att->kv_heads;
+        A.ws_count = (int *)(wsb + kAttnTicketOff);
+        A.ws_o = (float *)(wsb + step_attn_partials_off());
+        A.ws_m = A.ws_o + splits * att->heads * att->head_dim;
+        A.ws_l = A.ws_m + splits * att->heads;
+        for (int l = 0; l < n_layers; ++l) {
+            A.k_cache[l] = att->k_caches[l];
+            A.v_cache[l] = att->v_caches[l];
+        }
+        A.max_seq = att->max_seq;
+        A.position = att->position;
+        A.H = att->heads;
+        A.Hkv = att->kv_heads;
+        A.total = att->position + 1;
+        A.lo = (att->window > 0 && A.total > att->window) ? A.total - att->window : 0;
+        const int len = A.total - A.lo;
+        A.cps = cps;
+        A.Lc = (len + cps - 1) / cps;
+        A.nsplit = (len + A.Lc - 1) / A.Lc;
+        A.scale = att->scale > 0.f ? att->scale : 1.0f / sqrtf((float)att->head_dim);
+    }
     int TGmax = 1, Kmax = 0, SWmax = 2;
     int nj = 0;
     for (int l = 0; l < n_layers; ++l) {
@@ -556,10 +664,20 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
         a.epi = q4::EPI_STORE;
         finish_job(a, TGmax, Kmax, SWmax);
         sp.jobs[nj++] = a;
+        if (att) {  // the layer's decode attention: no weights, no tiles
+            q4::GemvParams at = step_job(G, nb, sp.err);
+            at.epi = q4::EPI_ATTN;
+            at.layer = l;
+            at.groups = 0;
+            at.upt = 2;
+            at.K = (int)q4::kChunkK;
+            at.C = at.Cs = 1;
+            sp.jobs[nj++] = at;
+        }
         q4::GemvParams o = step_job(G, nb, sp.err);  // o projection of the attention output + residual
         o.mode = q4::MODE_SINGLE;
         add_mat(o, L.Wo, hid);
-        o.x = L.attn;
+        o.x = att ? att->out : L.attn;
         o.res = src;
         o.epi = q4::EPI_RESIDUAL;
         finish_job(o, TGmax, Kmax, SWmax);
@@ -590,11 +708,19 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     lg.gamma = gamma_final;
     lg.eps = eps;
     lg.epi = q4::EPI_ARGMAX;
-    lg.am_val = (float *)(wsb + 16);
-    lg.am_idx = (int *)(wsb + 16 + (size_t)4 * nb * kStepMaxGroups);
+    const size_t pairs = att ? kAttnPairsOff : 16;
+    lg.am_val = (float *)(wsb + pairs);
+    lg.am_idx = (int *)(wsb + pairs + (size_t)4 * nb * kStepMaxGroups);
     finish_job(lg, TGmax, Kmax, SWmax);
     sp.jobs[nj++] = lg;
     sp.njobs = nj;
+    if (att) {
+        // the attention job's scratch overlays the activation slice (nb = 1:
+        // 512 bytes a 128-column chunk), so that slice is at least that large
+        const size_t scratch = q4::step_attn_scratch_bytes(q4::cls_warps(0));
+        const int chunks = (int)((scratch + 511) / 512);
+        if (Kmax < chunks * (int)q4::kChunkK) Kmax = chunks * (int)q4::kChunkK;
+    }
     sp.Kmax = Kmax;
     sp.TGmax = TGmax;
     sp.SWmax = SWmax;
@@ -603,14 +729,16 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
 
     const size_t smem = q4::step_smem_bytes(fmt, nb, TGmax, Kmax, SWmax, nj);
     if (smem > q4::kSmemMax) return Q4_ERR_UNSUPPORTED;
-    const int occ = fmt == Q4_FMT_Q4_0     ? q4::step_occupancy_q4_0(nb, smem)
-                    : fmt == Q4_FMT_AFFINE ? q4::step_occupancy_affine(nb, smem)
-                    : fmt == Q4_FMT_Q8_0   ? q4::step_occupancy_q8_0(nb, smem)
-                    : fmt == Q4_FMT_Q4_K   ? q4::step_occupancy_q4_k(nb, smem)
-                                           : q4::step_occupancy_q1(nb, smem);
+    const bool an = att != nullptr;
+    const int occ = fmt == Q4_FMT_Q4_0     ? q4::step_occupancy_q4_0(nb, smem, an)
+                    : fmt == Q4_FMT_AFFINE ? q4::step_occupancy_affine(nb, smem, an)
+                    : fmt == Q4_FMT_Q8_0   ? q4::step_occupancy_q8_0(nb, smem, an)
+                    : fmt == Q4_FMT_Q4_K   ? q4::step_occupancy_q4_k(nb, smem, an)
+                                           : q4::step_occupancy_q1(nb, smem, an);
     if (occ < 1) return Q4_ERR_UNSUPPORTED;
     cudaGetLastError();
-    if (cudaMemsetAsync(workspace, 0, 16, stream) != cudaSuccess) return Q4_ERR_CUDA;
+    // the barrier counter and error word (and the attention tickets)
+    if (cudaMemsetAsync(workspace, 0, att ? kAttnPairsOff : 16, stream) != cudaSuccess) return Q4_ERR_CUDA;
     const int rc = fmt == Q4_FMT_Q4_0     ? q4::launch_step_q4_0(sp, G, smem, stream)
                    : fmt == Q4_FMT_AFFINE ? q4::launch_step_affine(sp, G, smem, stream)
                    : fmt == Q4_FMT_Q8_0   ? q4::launch_step_q8_0(sp, G, smem, stream)
@@ -619,6 +747,7 @@ extern "C" q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_lay
     if (rc != 0 || cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
     return Q4_OK;
 }
+}  // namespace
 
 extern "C" q4_status q4_decode_check(const void *workspace, cudaStream_t stream) {
     if (!workspace) return Q4_ERR_NULL;

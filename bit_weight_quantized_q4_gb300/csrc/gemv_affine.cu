@@ -8,5 +8,5 @@ int launch_gemv_affine(const GemvParams &p, const Plan &plan, void *stream) {
 int launch_step_affine(const StepParams &p, int ctas, size_t smem, void *stream) {
     return launch_step_fmt<1>(p, ctas, smem, (cudaStream_t)stream);
 }
-int step_occupancy_affine(int nb, size_t smem) { return step_occupancy_fmt<1>(nb, smem); }
+int step_occupancy_affine(int nb, size_t smem, bool attn) { return step_occupancy_fmt<1>(nb, smem, attn); }
 }  // namespace q4

@@ -1809,6 +1809,12 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_engine_kernel(con
     argmax_epilogue<CLS>(p, q, m, group, tid, warp, lane);
 }
 
+}  // namespace dev
+}  // namespace q4
+#include "step_attn.cuh"
+namespace q4 {
+namespace dev {
+
 // ---------------------------------------------------------------------------
 // Persistent decode-step kernel: one CTA per SM runs the step's jobs in
 // order, separated by grid-wide barriers; the weight stream of every warp
@@ -1853,7 +1859,10 @@ __device__ __forceinline__ bool grid_barrier(unsigned *counter, int *err, unsign
     return fail == 0;
 }
 
-template <int FMT, int CLS>
+// ATT: the jobs include the layers' decode attention (EPI_ATTN jobs,
+// q4_decode_step_attn; nb = 1), each run by step_attn_job.  Without it the
+// kernel is the stand-in step's, unchanged.
+template <int FMT, int CLS, bool ATT>
 __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_step_kernel(const __grid_constant__ StepParams sp) {
     using C = Cls<CLS>;
     constexpr int REC = rec_bytes(FMT);
@@ -1894,6 +1903,12 @@ __global__ void __launch_bounds__(Cls<CLS>::NW * 32, 1) q4gemv_step_kernel(const
             !grid_barrier<NW>(sp.counter, sp.err, (unsigned)j, sp.barrier_polls, (unsigned)sp.barrier_extra, refill)) {
             ring.drain();
             return;
+        }
+        if constexpr (ATT) {
+            if (p.epi == EPI_ATTN) {  // CTA-uniform
+                step_attn_job<NW>(sp.att, p.layer, m.xs, group, tid, warp, lane);
+                continue;
+            }
         }
         const Geo q = geo_of<NW>(p, spans[j], 0, warp);
         if (q.tiles_here == 0) continue;  // no work in this job (CTA-uniform)

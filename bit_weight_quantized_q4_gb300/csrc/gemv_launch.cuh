@@ -60,9 +60,9 @@ static int launch_gemv_fmt(const GemvParams &p, const Plan &plan, cudaStream_t s
     }
 }
 
-template <int FMT, int CLS>
+template <int FMT, int CLS, bool ATT>
 static int launch_step_cls(const StepParams &p, int ctas, size_t smem, cudaStream_t stream) {
-    auto kern = dev::q4gemv_step_kernel<FMT, CLS>;
+    auto kern = dev::q4gemv_step_kernel<FMT, CLS, ATT>;
     static size_t smem_set[64] = {0};
     if (!raise_smem(kern, smem, smem_set)) return -1;
     cudaLaunchConfig_t cfg = {};
@@ -82,17 +82,18 @@ static int launch_step_cls(const StepParams &p, int ctas, size_t smem, cudaStrea
 
 template <int FMT>
 static int launch_step_fmt(const StepParams &p, int ctas, size_t smem, cudaStream_t stream) {
+    if (p.attn) return launch_step_cls<FMT, 0, true>(p, ctas, smem, stream);  // nb = 1 (the host checks)
     switch (cls_of(p.nb)) {
-        case 0: return launch_step_cls<FMT, 0>(p, ctas, smem, stream);
-        case 1: return launch_step_cls<FMT, 1>(p, ctas, smem, stream);
-        case 2: return launch_step_cls<FMT, 2>(p, ctas, smem, stream);
-        default: return launch_step_cls<FMT, 3>(p, ctas, smem, stream);
+        case 0: return launch_step_cls<FMT, 0, false>(p, ctas, smem, stream);
+        case 1: return launch_step_cls<FMT, 1, false>(p, ctas, smem, stream);
+        case 2: return launch_step_cls<FMT, 2, false>(p, ctas, smem, stream);
+        default: return launch_step_cls<FMT, 3, false>(p, ctas, smem, stream);
     }
 }
 
-template <int FMT, int CLS>
+template <int FMT, int CLS, bool ATT>
 static int step_occupancy_cls(size_t smem) {
-    auto kern = dev::q4gemv_step_kernel<FMT, CLS>;
+    auto kern = dev::q4gemv_step_kernel<FMT, CLS, ATT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return 0;
     int blocks = 0;
@@ -102,12 +103,13 @@ static int step_occupancy_cls(size_t smem) {
 }
 
 template <int FMT>
-static int step_occupancy_fmt(int nb, size_t smem) {
+static int step_occupancy_fmt(int nb, size_t smem, bool attn) {
+    if (attn) return step_occupancy_cls<FMT, 0, true>(smem);
     switch (cls_of(nb)) {
-        case 0: return step_occupancy_cls<FMT, 0>(smem);
-        case 1: return step_occupancy_cls<FMT, 1>(smem);
-        case 2: return step_occupancy_cls<FMT, 2>(smem);
-        default: return step_occupancy_cls<FMT, 3>(smem);
+        case 0: return step_occupancy_cls<FMT, 0, false>(smem);
+        case 1: return step_occupancy_cls<FMT, 1, false>(smem);
+        case 2: return step_occupancy_cls<FMT, 2, false>(smem);
+        default: return step_occupancy_cls<FMT, 3, false>(smem);
     }
 }
 

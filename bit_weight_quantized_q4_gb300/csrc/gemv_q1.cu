@@ -8,5 +8,5 @@ int launch_gemv_q1(const GemvParams &p, const Plan &plan, void *stream) {
 int launch_step_q1(const StepParams &p, int ctas, size_t smem, void *stream) {
     return launch_step_fmt<4>(p, ctas, smem, (cudaStream_t)stream);
 }
-int step_occupancy_q1(int nb, size_t smem) { return step_occupancy_fmt<4>(nb, smem); }
+int step_occupancy_q1(int nb, size_t smem, bool attn) { return step_occupancy_fmt<4>(nb, smem, attn); }
 }  // namespace q4

@@ -8,5 +8,5 @@ int launch_gemv_q8_0(const GemvParams &p, const Plan &plan, void *stream) {
 int launch_step_q8_0(const StepParams &p, int ctas, size_t smem, void *stream) {
     return launch_step_fmt<2>(p, ctas, smem, (cudaStream_t)stream);
 }
-int step_occupancy_q8_0(int nb, size_t smem) { return step_occupancy_fmt<2>(nb, smem); }
+int step_occupancy_q8_0(int nb, size_t smem, bool attn) { return step_occupancy_fmt<2>(nb, smem, attn); }
 }  // namespace q4

@@ -95,7 +95,7 @@ inline int64_t chunks_of(int64_t k) { return (k + kChunkK - 1) / kChunkK; }
 
 // ---------------------------------------------------------------- kernel
 enum Mode { MODE_SINGLE = 0, MODE_CONCAT = 1, MODE_PAIRS = 2 };
-enum Epi { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
+enum Epi { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3, EPI_ATTN = 4 };
 
 
 constexpr int kMaxNb = 16;
@@ -157,7 +157,7 @@ struct GemvParams {
     int *err;                    // set nonzero if a kernel wait gave up
     long long wait_cycles;       // bound of one weight-copy wait (SM clock cycles)
     int extra_tx;                // bytes a copy stage expects beyond its copies (0; testing the give-up path only)
-    int pad_;
+    int layer;                   // EPI_ATTN (persistent step only): the layer, an index into StepAttn's caches
 };
 
 // One CTA group's share of a job: its first tile, tile pairs (units of upt
@@ -169,6 +169,26 @@ struct JobSpan {
 
 // The persistent decode-step kernel runs these jobs in order, one CTA per SM.
 constexpr int kMaxStepJobs = 4 * 32 + 1;      // four jobs per layer, up to 32 layers, + logits
+constexpr int kMaxStepLayers = 32;
+
+// The persistent step's decode attention (q4_decode_step_attn): one job per
+// layer between the q/k/v job and the o job.  Geometry fixed at head size
+// 64 and four query heads per kv head.  CTA c takes kv head c / cps and
+// split c % cps of the attended positions [lo, total) -- Lc positions each,
+// nsplit of them in use -- and the last split of a kv head to finish folds
+// the splits' shares (ws_count[hk], zero again when it has).
+constexpr int kStepAttnD = 64, kStepAttnG = 4;
+struct StepAttn {
+    const float *q, *k_new, *v_new;            // the q/k/v job's outputs: [H][D], [Hkv][D], [Hkv][D]
+    const float *rope_cos, *rope_sin;          // [max_seq][D/2], or nullptr (no RoPE)
+    float *out;                                // [H][D]: the o job's input
+    float *ws_o, *ws_m, *ws_l;                 // [nsplit][H][D], [nsplit][H], [nsplit][H]
+    int *ws_count;                             // [Hkv]
+    float *k_cache[kMaxStepLayers];            // per layer [Hkv][max_seq][D]
+    float *v_cache[kMaxStepLayers];
+    int max_seq, position, H, Hkv, lo, total, Lc, nsplit, cps;
+    float scale;
+};
 constexpr long long kBarrierSpins = 1ll << 22;  // polls before a grid barrier gives up
 constexpr long long kWaitCycles = 1ll << 31;    // about a second: bound of one mbarrier wait
 
@@ -185,8 +205,9 @@ struct StepParams {
     float *val;                  // [nb] or nullptr
     long long barrier_polls;     // polls before a grid barrier gives up
     int barrier_extra;           // arrivals a barrier expects beyond the CTAs (0; testing the give-up path only)
-    int pad_;
+    int attn;                    // the jobs include EPI_ATTN jobs (q4_decode_step_attn)
     GemvParams jobs[kMaxStepJobs];
+    StepAttn att;                // their parameters (attn only)
 };
 
 #if defined(__CUDACC__)
@@ -317,6 +338,14 @@ inline Plan make_plan(int fmt, int T, int C, int nb, bool pairs, int num_sms) {
     return best;
 }
 
+// Shared-memory scratch of the persistent step's attention job (step_attn.cuh,
+// NW warps): the warps' output shares, maxima and sums, per-warp softmax
+// slots, a flag.
+inline size_t step_attn_scratch_bytes(int NW) {
+    const size_t G = kStepAttnG, D = kStepAttnD;
+    return ((size_t)NW * G * D + 2 * (size_t)NW * G + (size_t)NW * 32 + (size_t)NW * G) * 4 + 16;
+}
+
 // Dynamic shared memory of one decode-step CTA: the engine's regions plus a
 // copy of every job's parameter block and the CTA's span of every job.
 inline size_t step_smem_bytes(int fmt, int nb, int TGmax, int Kmax, int SWmax, int njobs) {
@@ -378,10 +407,10 @@ int launch_step_q8_0(const StepParams &p, int ctas, size_t smem, void *stream);
 int launch_step_q4_k(const StepParams &p, int ctas, size_t smem, void *stream);
 int launch_step_q1(const StepParams &p, int ctas, size_t smem, void *stream);
 // Decode-step CTAs that can be resident on one SM (0 on error).
-int step_occupancy_q4_0(int nb, size_t smem);
-int step_occupancy_affine(int nb, size_t smem);
-int step_occupancy_q8_0(int nb, size_t smem);
-int step_occupancy_q4_k(int nb, size_t smem);
-int step_occupancy_q1(int nb, size_t smem);
+int step_occupancy_q4_0(int nb, size_t smem, bool attn);
+int step_occupancy_affine(int nb, size_t smem, bool attn);
+int step_occupancy_q8_0(int nb, size_t smem, bool attn);
+int step_occupancy_q4_k(int nb, size_t smem, bool attn);
+int step_occupancy_q1(int nb, size_t smem, bool attn);
 
 }  // namespace q4

@@ -6,7 +6,8 @@ the greedy argmax.
 Two ways to run it, same arithmetic per call:
 * ``run_fused()``: one ``q4_decode_step`` call -- a single persistent kernel
   whose jobs are separated by grid-wide barriers while the weight stream runs
-  ahead across them (the benchmark's step);
+  ahead across them (the benchmark's step); with ``attention``, one
+  ``q4_decode_step_attn`` call, the layers' attention as jobs of the kernel;
 * ``run()``: the individual library calls (82 kernels for 16 layers) on one
   stream, e.g. captured as a CUDA graph.
 
@@ -30,8 +31,9 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import DecodeLayers, Q4Weight, lib, q4_argmax, q4_argmax_workspace_bytes, q4_attn_decode, q4_decode_step, \
-    q4_decode_workspace_bytes, q4_dual_gemv, q4_gus_nrm, q4_nrm_gemv, q4_res_gemv, rope_table
+from . import DecodeLayers, Q4Weight, StepAttention, lib, q4_argmax, q4_argmax_workspace_bytes, q4_attn_decode, \
+    q4_decode_attn_workspace_bytes, q4_decode_step, q4_decode_step_attn, q4_decode_workspace_bytes, q4_dual_gemv, \
+    q4_gus_nrm, q4_nrm_gemv, q4_res_gemv, rope_table
 
 
 @dataclass
@@ -108,6 +110,13 @@ class DecodeStep:
             self.att = torch.empty((1, hidden), **f32)
             self.attn_ws = torch.zeros(int(lib().q4_attn_workspace_bytes(spec.heads, spec.head_dim, spec.max_seq)),
                                        dtype=torch.uint8, device=device)
+            # the persistent form (run_fused): its attention descriptor and
+            # workspace, where its geometry is one the kernel takes
+            self.step_att = None
+            nbytes = q4_decode_attn_workspace_bytes(spec.heads, spec.kv_heads, spec.head_dim)
+            if nbytes:
+                self.step_att = StepAttention(self.caches, self.att, spec.position, spec.window, rope=self.rope)
+                self.step_att_ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
 
     @property
     def n_kernels(self) -> int:
@@ -165,11 +174,23 @@ class DecodeStep:
 
     def run_fused(self, n_layers=None):
         """Enqueue the step as one persistent kernel (the first ``n_layers``
-        layers then the logits argmax); the stand-in step only."""
+        layers then the logits argmax): with attention, its layers' attention
+        as jobs of the kernel (``q4_decode_step_attn``)."""
         if self.attention is not None:
-            raise ValueError("the persistent step runs the stand-in step; run() takes the attention")
+            if self.step_att is None:
+                raise ValueError("the persistent step's attention takes head size 64 and four query heads per kv "
+                                 "head; run() takes the others")
+            q4_decode_step_attn(self.descs, self.step_att, self.Wlogits, self.gamma_final, self.eps, self.x_in,
+                                self.hid, self.q, self.k, self.v, self.h, self.idx, self.val, self.step_att_ws,
+                                n_layers=n_layers)
+            return
         q4_decode_step(self.descs, self.Wlogits, self.gamma_final, self.eps, self.x_in, self.hid, self.q, self.k,
                        self.v, self.h, self.idx, self.val, self.step_ws, n_layers=n_layers)
+
+    @property
+    def check_ws(self):
+        """The workspace q4_decode_check reads after run_fused()."""
+        return self.step_att_ws if self.attention is not None else self.step_ws
 
     @property
     def n_kernels_fused(self) -> int:

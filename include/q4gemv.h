@@ -268,9 +268,59 @@ q4_status q4_decode_step(const q4_decode_layer *layers, int32_t n_layers, const 
                          float *q, float *k, float *v, float *h, int32_t *idx, float *val, void *workspace,
                          size_t ws_bytes, cudaStream_t stream);
 
-/* Synchronises `stream` and reports whether the last q4_decode_step on this
- * workspace completed all its grid barriers and weight copies (Q4_OK) or
- * gave up on one (Q4_ERR_CUDA). */
+/* The decode attention of q4_decode_step_attn (honeycrisp/mod.rs,
+ * gpu_attention and the fused RoPE + KV-append + SDPA dispatch of
+ * forward_decode_fused_layers), for one token at `position`: per layer, q,
+ * the new k and v (the layer's q/k/v projections, read as heads of
+ * head_dim), RoPE of q and k from the tables, k and v appended to the layer's
+ * caches at `position`, then out = softmax(scale q K^T) V over the cached
+ * positions [lo, position] (lo = position + 1 - window when window > 0 and
+ * the context is longer, else 0), query head h reading kv head h / (heads /
+ * kv_heads).
+ * k_caches, v_caches: HOST arrays of n_layers device pointers, each cache
+ * [kv_heads][max_seq][head_dim] fp32 (16-byte aligned), read during the call.
+ * rope_cos, rope_sin: device [max_seq][head_dim/2] tables (q4_rope_table), or
+ * both NULL for no RoPE.  out: device [heads * head_dim], the attention
+ * output the o projections consume (scratch between layers).  scale <= 0
+ * means 1/sqrt(head_dim).  Library-specific geometry limits: head_dim 64 and
+ * four query heads per kv head (Q4_ERR_UNSUPPORTED otherwise; q4_attn_decode
+ * covers the others call by call). */
+typedef struct {
+    float *const *k_caches;
+    float *const *v_caches;
+    const float *rope_cos;
+    const float *rope_sin;
+    float *out;
+    int32_t max_seq, position, window, heads, kv_heads, head_dim;
+    float scale;
+} q4_step_attention;
+
+/* Workspace bytes q4_decode_step_attn needs (nb = 1); 0 for a geometry it
+ * does not take. */
+size_t q4_decode_attn_workspace_bytes(int32_t heads, int32_t kv_heads, int32_t head_dim);
+
+/* The real decode step as a single persistent kernel: q4_decode_step with
+ * each layer's decode attention (q4_step_attention) between its q/k/v and o
+ * projections, in place of the `attn` stand-in (layers[l].attn is not read):
+ *   q, k, v = (Wq, Wk, Wv) * rmsnorm(src, gamma_in)
+ *   out     = attention(q, k, v, caches of layer l)     (appends k, v)
+ *   hid     = src + Wo * out,  then gate/up/SwiGLU and down as in q4_decode_step
+ * then the logits argmax.  nb = 1 (x_in, hid [1][hidden]); heads * head_dim
+ * must equal hidden (Wq.n, Wo.k) and kv_heads * head_dim Wk.n and Wv.n;
+ * n_layers 1..25.  workspace: q4_decode_attn_workspace_bytes bytes; the call
+ * zeroes its first 80 bytes on `stream` before the launch.  Each attention
+ * is a job of the kernel: CTA c takes kv head c / (CTAs / kv_heads) and a
+ * split of the positions, and the last split of a kv head to finish folds
+ * the splits (no wait; the same result whatever the CTA order).  Failure
+ * reporting as for q4_decode_step (q4_decode_check). */
+q4_status q4_decode_step_attn(const q4_decode_layer *layers, int32_t n_layers, const q4_step_attention *att,
+                              const q4_weight *Wlogits, const float *gamma_final, float eps, const float *x_in,
+                              float *hid, float *q, float *k, float *v, float *h, int32_t *idx, float *val,
+                              void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronises `stream` and reports whether the last q4_decode_step (or
+ * q4_decode_step_attn) on this workspace completed all its grid barriers and
+ * weight copies (Q4_OK) or gave up on one (Q4_ERR_CUDA). */
 q4_status q4_decode_check(const void *workspace, cudaStream_t stream);
 
 /* Synchronises `stream` and reports whether any GEMV-family kernel of this

@@ -335,6 +335,62 @@ def test_attn_validation(case, expect):
     assert st == expect
 
 
+def test_step_attn_workspace_bytes():
+    L = q4.lib()
+    assert L.q4_decode_attn_workspace_bytes(32, 8, 64) == 80 + 8 * 1024 + (1024 // 8) * 32 * 66 * 4
+    assert L.q4_decode_attn_workspace_bytes(8, 2, 64) == 80 + 8 * 1024 + 512 * 8 * 66 * 4
+    assert L.q4_decode_attn_workspace_bytes(4, 2, 64) == 0      # two query heads per kv head
+    assert L.q4_decode_attn_workspace_bytes(16, 4, 128) == 0    # head size 128
+    assert L.q4_decode_attn_workspace_bytes(68, 17, 64) == 0    # more than 16 kv heads
+
+
+@pytest.mark.parametrize("case,expect", [("null_att", 1), ("g2", 4), ("d128", 4), ("width", 2), ("pos_past", 2),
+                                         ("neg_window", 2), ("null_caches", 1), ("misaligned_cache", 3),
+                                         ("one_table", 1), ("misaligned_out", 3), ("ws_small", 5),
+                                         ("too_many_layers", 4)])
+def test_step_attn_validation(case, expect):
+    # every case fails before any CUDA call (fake 16-byte aligned addresses)
+    L = q4.lib()
+    hidden, kv, inter, nl = 512, 128, 256, 2
+    heads, kv_heads, D, ms, pos, win = 8, 2, 64, 128, 100, 0
+    caches = [A, A]
+    cos, sin, out = A, A, A
+
+    def layer():
+        return q4._CDecodeLayer(_cw(0, hidden, hidden), _cw(0, kv, hidden), _cw(0, kv, hidden),
+                                _cw(0, hidden, hidden), _cw(0, inter, hidden), _cw(0, inter, hidden),
+                                _cw(0, hidden, inter), A, A, None)
+    if case == "g2":
+        heads, kv_heads = 4, 2
+    elif case == "d128":
+        D = 128
+    elif case == "width":
+        heads, kv_heads = 16, 4
+    elif case == "pos_past":
+        pos = ms
+    elif case == "neg_window":
+        win = -1
+    elif case == "misaligned_cache":
+        caches = [A, A + 4]
+    elif case == "one_table":
+        sin = None
+    elif case == "misaligned_out":
+        out = A + 8
+    elif case == "too_many_layers":
+        nl = 26
+    layers = (q4._CDecodeLayer * nl)(*[layer() for _ in range(nl)])
+    kc = (ctypes.c_void_p * nl)(*(caches + [A] * (nl - len(caches))))
+    att = q4._CStepAttention(ctypes.cast(kc, ctypes.c_void_p), ctypes.cast(kc, ctypes.c_void_p), cos, sin, out, ms,
+                             pos, win, heads, kv_heads, D, 0.0)
+    if case == "null_caches":
+        att.k_caches = None
+    ws = L.q4_decode_attn_workspace_bytes(8, 2, 64) - (1 if case == "ws_small" else 0)
+    Wl = _cw(0, 500, hidden)
+    st = L.q4_decode_step_attn(ctypes.cast(layers, ctypes.c_void_p), nl, None if case == "null_att" else
+                               ctypes.byref(att), ctypes.byref(Wl), A, 1e-6, A, A, A, A, A, A, A, A, A, ws, None)
+    assert st == expect
+
+
 def test_gemm_validation():
     # every case fails before any CUDA call (fake 16-byte aligned addresses)
     L = q4.lib()

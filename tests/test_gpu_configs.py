@@ -207,6 +207,94 @@ def test_decode_step_with_attention_every_format(q4, fmt, window):
     assert np.allclose(to_np(step.hid), hid_ref, rtol=2e-3, atol=2e-3), "real step %s hidden state" % fmt
 
 
+def test_fused_decode_step_with_attention_teacher_forced(q4):
+    """The real step as one persistent kernel (q4_decode_step_attn: each
+    layer's attention a job of the kernel) at the workload's widths -- 32 / 8
+    heads of 64 -- over 1000 cached positions, layer by layer: running it on
+    the first L layers leaves layer L-1's q, k, v, attention output and h, so
+    each is checked against the oracle on the GPU's own inputs of that layer.
+    Then the argmax, a graph replay (same bits) and the call-by-call real
+    step."""
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+    spec = wl.AttnSpec(max_seq=1024, position=1000)
+    cfg = wl.cfg4(seed=18, layers=2)
+    caches = wl.draw_kv_caches(18, 2, spec)
+    step = DecodeStep(cfg, attention=(spec, caches))
+    assert step.step_att is not None
+    cosv, sinv = oracle.rope_table(spec.max_seq, spec.head_dim, spec.rope_theta)
+    prev = cfg.x.astype(np.float64)
+    for L in range(1, len(cfg.layers) + 1):
+        step.run_fused(n_layers=L)
+        q4.q4_decode_check(step.check_ws)
+        lay = cfg.layers[L - 1]
+        tag = "fused real step layer %d" % (L - 1)
+        q, Sq = oracle.q4_nrm_gemv(oracle._hw(lay.Wq), prev, lay.gamma_in, cfg.eps)
+        check(to_np(step.q), q, Sq, what=tag + " q")
+        ka, Ska, kb, Skb = oracle.q4_dual_gemv(oracle._hw(lay.Wk), oracle._hw(lay.Wv), prev, lay.gamma_in, cfg.eps)
+        check(to_np(step.k), ka, Ska, what=tag + " k")
+        check(to_np(step.v), kb, Skb, what=tag + " v")
+        ar, Sa, kc2, vc2 = oracle.layer_attention(to_np(step.q), to_np(step.k), to_np(step.v), caches[L - 1][0],
+                                                  caches[L - 1][1], spec, cosv, sinv)
+        check(to_np(step.att), ar, Sa, what=tag + " attention")
+        kd, vd = step.caches[L - 1][0].cpu().numpy(), step.caches[L - 1][1].cpu().numpy()
+        assert np.array_equal(vd[:, spec.position], vc2[:, spec.position])
+        assert np.allclose(kd[:, spec.position], kc2[:, spec.position], rtol=1e-5, atol=1e-5)
+        assert np.array_equal(kd[:, :spec.position], caches[L - 1][0][:, :spec.position])
+        hid_o, So = oracle.q4_res_gemv(oracle._hw(lay.Wo), to_np(step.att), prev)
+        _, g, Sg, u, Su = oracle.q4_gus_nrm(oracle._hw(lay.Wg), oracle._hw(lay.Wu), hid_o, lay.gamma_post, cfg.eps)
+        check_swiglu(to_np(step.h), g, Sg, u, Su, what=tag + " gus")
+        hid_ref, Sd = oracle.q4_res_gemv(oracle._hw(lay.Wd), to_np(step.h), hid_o)
+        bound_extra = 1e-3 * So + 2.0 ** -22 * np.abs(hid_ref)
+        check(to_np(step.hid), hid_ref, Sd, extra=bound_extra, what=tag + " hid")
+        prev = to_np(step.hid)
+    _, lref, Sl = oracle.q4_argmax(oracle._hw(cfg.Wlogits), prev, cfg.gamma_final, cfg.eps)
+    check_argmax(step.idx.cpu().numpy(), lref, what="fused real step argmax")
+    assert abs(float(step.val[0]) - lref[0].max()) <= 1e-3 * Sl[0].max() + 1e-6
+    fused_idx, fused_hid = step.idx.clone(), step.hid.clone()
+    g = step.capture(fused=True)
+    g.replay()
+    torch.cuda.synchronize()
+    q4.q4_decode_check(step.check_ws)
+    assert torch.equal(step.idx, fused_idx) and torch.equal(step.hid, fused_hid)
+    step.run()
+    torch.cuda.synchronize()
+    assert float((step.hid - fused_hid).abs().max()) <= 1e-4 * float(fused_hid.abs().max())
+
+
+@pytest.mark.parametrize("fmt,window", [("q4_0", 0), ("affine", 40), ("q8_0", 0), ("q4_k", 17), ("q1", 0),
+                                        ("q4_0", 1)])
+def test_fused_decode_step_with_attention_every_format(q4, fmt, window):
+    """The persistent real step at small widths (8 query / 2 kv heads of 64)
+    in every weight format, with and without a sliding window: the final
+    hidden state and argmax against the oracle's real step, and against the
+    call-by-call real step."""
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+    spec = wl.AttnSpec(heads=8, kv_heads=2, head_dim=64, max_seq=128, position=100, window=window)
+    cfg = wl.cfg4(seed=19, layers=2, hidden=512, kv=128, inter=512, vocab=500, nb=1, fmt=fmt)
+    caches = wl.draw_kv_caches(19, 2, spec)
+    step = DecodeStep(cfg, attention=(spec, caches))
+    step.run_fused()
+    q4.q4_decode_check(step.check_ws)
+    idx_ref, lref, hid_ref = oracle.decode_step(cfg, attention=(spec, caches))
+    check_argmax(step.idx.cpu().numpy(), lref, what="fused real step %s argmax" % fmt)
+    assert np.allclose(to_np(step.hid), hid_ref, rtol=2e-3, atol=2e-3), "fused real step %s hidden state" % fmt
+    fused_hid = step.hid.clone()
+    step.run()
+    torch.cuda.synchronize()
+    assert float((step.hid - fused_hid).abs().max()) <= 1e-4 * float(fused_hid.abs().max())
+
+
+def test_fused_decode_step_with_attention_rejects(q4):
+    """Geometries the persistent form does not take fall back to run()."""
+    from bit_weight_quantized_q4_gb300.decode import DecodeStep
+    spec = wl.AttnSpec(heads=4, kv_heads=2, head_dim=64, max_seq=128, position=100)
+    cfg = wl.cfg4(seed=20, layers=1, hidden=256, kv=128, inter=512, vocab=100, nb=1)
+    step = DecodeStep(cfg, attention=(spec, wl.draw_kv_caches(20, 1, spec)))
+    assert step.step_att is None
+    with pytest.raises(ValueError):
+        step.run_fused()
+
+
 def test_fused_decode_step_teacher_forced(q4):
     """The persistent-kernel step, layer by layer: running it on the first L
     layers gives that prefix's hidden state (the same per-layer arithmetic
