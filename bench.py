@@ -584,7 +584,9 @@ def kernel_table(device, l2_bytes: int, peak: float, reps: int = 48) -> dict:
         out["gemm_q4_0_n%d_k%d_nb%d" % (n, k, nbg)] = {
             "us": round(t * 1e6, 3), **spread(t), "tflops": round(tf, 1),
             "frac_of_bf16_peak": round(tf / bf16_peak, 4) if bf16_peak else None,
-            "what": "staging pass + GEMM (mma.sync f16, fp32 accumulate), weights exact; peak: measured cuBLAS bf16"}
+            "what": ("staging pass + GEMM (tcgen05 f16 MMAs into tensor memory; weights exact as f16 hi + lo "
+                     "pairs, so the tensor work is twice the algorithmic flops counted here; fp32 accumulate); "
+                     "peak: measured cuBLAS bf16")}
     del Wg
     torch.cuda.empty_cache()
     # decode attention of one token (RoPE, KV append, softmax(q K^T) V) at

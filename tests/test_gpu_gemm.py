@@ -1,8 +1,9 @@
 """GPU parity of q4_gemm (the prefill GEMM: y = x W^T for wide activation
 batches; crate inferencelayer, gemm_q4_src) against the f64 oracle, through
 the C ABI: every weight format, batch widths in the 16-row activation tile
-(1, 9, 16) and around and far above one 64-row tile, ragged n and k, the accumulate form, exact zeros and
-run-to-run determinism."""
+(1, 9, 16) and around and far above one 64-row (Q4_0: 128-row tensor-memory)
+tile, ragged n and k, the accumulate form, scales over many binades, exact
+zeros and run-to-run determinism."""
 import numpy as np
 import pytest
 
@@ -65,6 +66,25 @@ def test_gemm_workload_shape_and_determinism(q4):
     sub = wl.Q4_0Host(40, 4096, H.blocks[rows])
     ref, S = oracle.q4_gemv(host_weight(sub), x)
     check(to_np(y)[:, rows], ref, S, what="gemm 14336x4096 nb=256 (sampled rows)")
+
+
+@pytest.mark.parametrize("nb", [17, 130])
+def test_gemm_scale_range(q4, nb):
+    # Q4_0 from 17 rows runs on the tensor-memory form, whose operands carry a
+    # power of two per weight row and per activation row: weight rows whose
+    # block scales span 2^-14 .. 2^15 (a few rows all zero), activation rows
+    # from 1e-12 to 1e12, against the oracle at the plain tolerance
+    rng = np.random.default_rng(80 + nb)
+    n, k = 200, 1024
+    q = rng.integers(0, 16, (n, k), dtype=np.uint8)
+    e = rng.integers(-13, 14, (n, 1)) + rng.integers(-6, 1, (n, k // 32))
+    d = (rng.uniform(1.0, 2.0, (n, k // 32)) * 2.0 ** e).astype(np.float16)
+    d[rng.choice(n, 4, replace=False)] = 0
+    H = wl.Q4_0Host(n, k, wl.pack_q4_0(q, d.view(np.uint16)))
+    x = wl.draw_x(rng, nb, k) * (10.0 ** rng.integers(-12, 13, (nb, 1))).astype(np.float32)
+    y = q4.q4_gemm(dev_weight(H), torch.from_numpy(x).cuda())
+    ref, S = oracle.q4_gemv(host_weight(H), x)
+    check(to_np(y), ref, S, what="gemm scale range nb=%d" % nb)
 
 
 def test_gemm_zero_weights_exact(q4):

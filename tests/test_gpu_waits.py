@@ -90,10 +90,12 @@ def test_attention_copy_wait_gives_up_and_the_next_call_is_unchanged(q4):
     q4.q4_device_check()
 
 
-@pytest.mark.parametrize("nb", [9, 40])  # the 16-row and the 64-row activation tile
-def test_gemm_copy_wait_gives_up_and_the_next_call_is_unchanged(q4, nb):
+# the 16-row activation tile, the tensor-memory form (Q4_0 from 17 rows) and
+# the 64-row activation tile of the other formats
+@pytest.mark.parametrize("fmt,nb", [("q4_0", 9), ("q4_0", 40), ("affine", 40)])
+def test_gemm_copy_wait_gives_up_and_the_next_call_is_unchanged(q4, fmt, nb):
     rng = np.random.default_rng(24 + nb)
-    H = wl.draw_q4_0(rng, 300, 1024)
+    H = wl._draw_fmt(fmt)(rng, 300, 1024)
     W = dev_weight(H)
     x = torch.from_numpy(wl.draw_x(rng, nb, 1024)).cuda()
     y0 = q4.q4_gemm(W, x)
