@@ -68,6 +68,9 @@ struct TcCfg {
     static constexpr int Smem = OffRaw + kTcSR * kTcRawSlot;
     static_assert(Smem <= (int)kSmemMax, "tcgen05 GEMM shared memory");
     static_assert(8 * (2 * kTcSR + 2 * SB + kTcSA) <= kTcOffFlags, "barrier area");
+    // the stage completions live in SB slots; a dequant warp waits on stage
+    // s - SA's, which must still be the slot's latest or the one before
+    static_assert(SB >= kTcSA, "completion ring at least as deep as the operand ring");
 };
 // the column tile of a batch: 256 rows above 128, else 128
 Q4_HD constexpr int tc_bn(int nb) { return nb > 128 ? 256 : 128; }
