@@ -68,9 +68,9 @@ def test_gemm_workload_shape_and_determinism(q4):
     check(to_np(y)[:, rows], ref, S, what="gemm 14336x4096 nb=256 (sampled rows)")
 
 
-@pytest.mark.parametrize("nb", [17, 130])
+@pytest.mark.parametrize("nb", [65, 130, 257])
 def test_gemm_scale_range(q4, nb):
-    # Q4_0 from 17 rows runs on the tensor-memory form, whose operands carry a
+    # Q4_0 from 65 rows runs on the tensor-memory form, whose operands carry a
     # power of two per weight row and per activation row: weight rows whose
     # block scales span 2^-14 .. 2^15 (a few rows all zero), activation rows
     # from 1e-12 to 1e12, against the oracle at the plain tolerance

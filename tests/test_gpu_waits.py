@@ -90,9 +90,9 @@ def test_attention_copy_wait_gives_up_and_the_next_call_is_unchanged(q4):
     q4.q4_device_check()
 
 
-# the 16-row activation tile, the tensor-memory form (Q4_0 from 17 rows) and
-# the 64-row activation tile of the other formats
-@pytest.mark.parametrize("fmt,nb", [("q4_0", 9), ("q4_0", 40), ("affine", 40)])
+# the 16-row and the 64-row activation tiles and the tensor-memory form
+# (Q4_0 from 65 rows)
+@pytest.mark.parametrize("fmt,nb", [("q4_0", 9), ("q4_0", 40), ("q4_0", 80)])
 def test_gemm_copy_wait_gives_up_and_the_next_call_is_unchanged(q4, fmt, nb):
     rng = np.random.default_rng(24 + nb)
     H = wl._draw_fmt(fmt)(rng, 300, 1024)
