@@ -17,21 +17,23 @@
 // powers of two back.
 //
 // Two launches.  q4gemm_tc_stage_kernel writes the activation image: per
-// BN-row column tile (BN = 256 for batches over 128 rows, else 128) and
+// BN-row column tile (BN = 512 over 256 rows, 256 over 128, else 128) and
 // 64-column stage, four K = 16 slabs in the K-major, unswizzled operand
 // layout (tc_common.cuh), with the columns of each 32-column block in the
 // order of the weight records' lanes (tc_col), plus each row's factor back.
 // q4gemm_tc_kernel gives each CTA 128 weight rows (eight 16-row record
 // tiles) by BN activation rows, one 128 x BN fp32 accumulator in tensor
-// memory, and three warp roles (q4gemm_tc_kernel):
+// memory (a 512-wide tile fills all 512 columns, two N = 256 MMAs per step),
+// and three warp roles (q4gemm_tc_kernel):
 //   * a copy warp brings the eight tiles' 128-column records (a ring of three
 //     chunk slots, each chunk feeding two stages) and each stage's image
-//     slice (a ring of six or three slots) in by bulk copies (TMA engine);
+//     slice (a ring of six, three or two slots) in by bulk copies (TMA engine);
 //   * sixteen dequant warps turn each stage's records into hi / lo operand
-//     slabs (a ring of three slots), one 16-byte store per lane and slab;
-//   * an MMA warp issues each stage's eight MMAs (four K = 16 steps, hi and
-//     lo, M = 128, N = BN) and commits them to the stage's mbarrier, which
-//     frees the operand and activation slots;
+//     slabs (a ring of three slots, two at BN = 512), one 16-byte store per
+//     lane and slab;
+//   * an MMA warp issues each stage's MMAs (four K = 16 steps, hi and lo,
+//     M = 128, N = min(BN, 256)) and commits them to the stage's mbarrier,
+//     which frees the operand and activation slots;
 //   * at the end the dequant warps read the accumulator out of tensor memory
 //     (warp w: lanes 32 (w % 4) .., columns (BN / 4) (w / 4) ..), scale and
 //     store.
@@ -45,7 +47,6 @@ namespace dev {
 
 constexpr int kTcBM = 128;           // weight rows per CTA (eight record tiles)
 constexpr int kTcBK = 64;            // columns per stage (half a record chunk)
-constexpr int kTcSA = 3;             // hi / lo operand slots
 constexpr int kTcSR = 3;             // raw chunk slots
 constexpr int kTcDW = 16;                    // dequant warps (two per record tile)
 constexpr int kTcThreads = 32 * (kTcDW + 2);  // and a copy warp, an MMA warp
@@ -56,24 +57,31 @@ constexpr int kTcRawSlot = 8 * kRecQ4_0;             // eight records of one chu
 constexpr int kTcOffFlags = 192;                     // tensor-memory address, abort flag
 constexpr int kTcOffRowP = 256;                      // [128] fp32 row factors P, then [128] their inverses
 constexpr int kTcOffA = 2048;
-// Per column-tile width BN (activation rows per CTA, the MMA's N: 128 or
-// 256): the activation slots and the shared-memory map.
+// Per column-tile width BN (activation rows per CTA: 128, 256 or 512; the
+// MMA's N is BN up to 256, and a 512-wide tile takes two N = 256 MMAs per
+// step into the two halves of the tensor memory): the operand and
+// activation slots and the shared-memory map.
 template <int BN>
 struct TcCfg {
-    static_assert(BN == 128 || BN == 256, "column tile");
-    static constexpr int SB = BN == 128 ? 6 : 3;  // activation slots
-    static constexpr int BSlot = BN * kTcBK * 2;  // activations of one stage (16 / 32 KB)
-    static constexpr int OffB = kTcOffA + kTcSA * kTcASlot;
+    static_assert(BN == 128 || BN == 256 || BN == 512, "column tile");
+    static constexpr int NN = BN > 256 ? 256 : BN;             // the MMA's N
+    static constexpr int NH = BN / NN;                          // MMAs per step and operand
+    static constexpr int SA = BN == 512 ? 2 : 3;                // hi / lo operand slots
+    static constexpr int SB = BN == 128 ? 6 : BN == 256 ? 3 : 2;  // activation slots
+    static constexpr int BSlot = BN * kTcBK * 2;  // activations of one stage (16 / 32 / 64 KB)
+    static constexpr int OffB = kTcOffA + SA * kTcASlot;
     static constexpr int OffRaw = OffB + SB * BSlot;
     static constexpr int Smem = OffRaw + kTcSR * kTcRawSlot;
     static_assert(Smem <= (int)kSmemMax, "tcgen05 GEMM shared memory");
-    static_assert(8 * (2 * kTcSR + 2 * SB + kTcSA) <= kTcOffFlags, "barrier area");
+    static_assert(8 * (2 * kTcSR + 2 * SB + SA) <= kTcOffFlags, "barrier area");
     // the stage completions live in SB slots; a dequant warp waits on stage
     // s - SA's, which must still be the slot's latest or the one before
-    static_assert(SB >= kTcSA, "completion ring at least as deep as the operand ring");
+    static_assert(SB >= SA, "completion ring at least as deep as the operand ring");
 };
-// the column tile of a batch: 256 rows above 128, else 128
-Q4_HD constexpr int tc_bn(int nb) { return nb > 128 ? 256 : 128; }
+// the column tile of a batch: 512 rows above 256, 256 above 128, else 128
+// (one wave of 112 CTAs at 512 rows on a 14336-row matrix, and twice the
+// tensor work per hand-off: 116 -> 105 us there)
+Q4_HD constexpr int tc_bn(int nb) { return nb > 256 ? 512 : nb > 128 ? 256 : 128; }
 
 // Bytes of the activation image (the row factors follow it): rows padded to
 // whole column tiles, columns to whole chunks.
@@ -285,7 +293,7 @@ __device__ __forceinline__ void tc_dequant(const uint4 &wv, const uint4 &sv, flo
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_constant__ GemmParams p) {
     using Cf = TcCfg<BN>;
-    constexpr int SA = kTcSA, SB = Cf::SB, SR = kTcSR;
+    constexpr int SA = Cf::SA, SB = Cf::SB, SR = kTcSR;
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nt = blockIdx.x, mt = blockIdx.y;  // activation (column) tile fastest, weight row tile
@@ -380,7 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
     } else if (warp == kTcDW + 1) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
-            const uint32_t idesc = tc::idesc_f16(kTcBM, BN);
+            const uint32_t idesc = tc::idesc_f16(kTcBM, Cf::NN);
             const uint64_t a0 = tc::smem_desc(a_base, 128, 256), b0 = tc::smem_desc(b_base, 128, 256);
             for (int s = 0; s < NS; ++s) {
                 if (*abort_flag) break;
@@ -395,9 +403,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
                 const uint64_t bd = b0 + (uint64_t)(((s % SB) * Cf::BSlot) >> 4);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t bk = bd + (uint64_t)((ks * (BN * 32)) >> 4);
-                    tc::mma_f16(taddr, ad + (uint64_t)((ks * kTcSlab) >> 4), bk, idesc, (s | ks) != 0);
-                    tc::mma_f16(taddr, ad + (uint64_t)((kTcAHalf + ks * kTcSlab) >> 4), bk, idesc, 1u);
+#pragma unroll
+                    for (int nh = 0; nh < Cf::NH; ++nh) {  // activation rows NN nh .. into columns NN nh ..
+                        const uint64_t bk = bd + (uint64_t)((ks * (BN * 32) + nh * (Cf::NN * 32)) >> 4);
+                        const uint32_t d = taddr + (uint32_t)(nh * Cf::NN);
+                        tc::mma_f16(d, ad + (uint64_t)((ks * kTcSlab) >> 4), bk, idesc, (s | ks) != 0);
+                        tc::mma_f16(d, ad + (uint64_t)((kTcAHalf + ks * kTcSlab) >> 4), bk, idesc, 1u);
+                    }
                 }
                 tc::commit(mma_done + 8 * (s % SB));
                 mma_issued = s + 1;
@@ -542,7 +554,11 @@ static int launch_gemm_tc_bn(const GemmParams &p, cudaStream_t stream) {
 
 int launch_gemm_tc(const GemmParams &p, void *stream_) {
     cudaStream_t stream = (cudaStream_t)stream_;
-    return dev::tc_bn(p.nb) == 256 ? launch_gemm_tc_bn<256>(p, stream) : launch_gemm_tc_bn<128>(p, stream);
+    switch (dev::tc_bn(p.nb)) {
+        case 512: return launch_gemm_tc_bn<512>(p, stream);
+        case 256: return launch_gemm_tc_bn<256>(p, stream);
+        default: return launch_gemm_tc_bn<128>(p, stream);
+    }
 }
 
 }  // namespace q4

@@ -402,8 +402,9 @@ def test_gemm_validation():
     # (36864 bytes), or the tensor-memory form's 128 rows x 128 f16 columns
     # plus 128 row factors (33280 bytes)
     assert L.q4_gemm_workspace_bytes(80, 64) == max(2 * 18432, 128 * 128 * 2 + 128 * 4)
-    # 256-row column tiles above 128 rows
+    # 256-row column tiles above 128 rows, 512-row above 256
     assert L.q4_gemm_workspace_bytes(200, 128) == max(4 * 18432, 256 * 128 * 2 + 256 * 4)
+    assert L.q4_gemm_workspace_bytes(300, 128) == max(5 * 18432, 512 * 128 * 2 + 512 * 4)
     assert L.q4_gemm_workspace_bytes(0, 64) == 0 and L.q4_gemm_workspace_bytes(8, 48) == 0
     assert L.q4_gemm(ctypes.byref(W), None, 40, A, 0, A, ws, None) == 1
     assert L.q4_gemm(ctypes.byref(W), A + 4, 40, A, 0, A, ws, None) == 3
