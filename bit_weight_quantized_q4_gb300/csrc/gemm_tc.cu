@@ -18,7 +18,7 @@
 //
 // Two launches.  q4gemm_tc_stage_kernel writes the activation image: per
 // BN-row column tile (BN = 512 over 256 rows, 256 over 128, else 128) and
-// 64-column stage, four K = 16 slabs in the K-major, unswizzled operand
+// stage of BK columns (32 at BN = 512, else 64), K = 16 slabs in the K-major, unswizzled operand
 // layout (tc_common.cuh), with the columns of each 32-column block in the
 // order of the weight records' lanes (tc_col), plus each row's factor back.
 // q4gemm_tc_kernel gives each CTA 128 weight rows (eight 16-row record
@@ -26,7 +26,7 @@
 // memory (a 512-wide tile fills all 512 columns, two N = 256 MMAs per step),
 // and three warp roles (q4gemm_tc_kernel):
 //   * a copy warp brings the eight tiles' 128-column records (a ring of three
-//     chunk slots, each chunk feeding two stages) and each stage's image
+//     chunk slots, each chunk feeding 128 / BK stages) and each stage's image
 //     slice (a ring of six, three or two slots) in by bulk copies (TMA engine);
 //   * sixteen dequant warps turn each stage's records into hi / lo operand
 //     slabs (a ring of three slots, two at BN = 512), one 16-byte store per
@@ -46,16 +46,13 @@ namespace q4 {
 namespace dev {
 
 constexpr int kTcBM = 128;           // weight rows per CTA (eight record tiles)
-constexpr int kTcBK = 64;            // columns per stage (half a record chunk)
 constexpr int kTcSR = 3;             // raw chunk slots
 constexpr int kTcDW = 16;                    // dequant warps (two per record tile)
 constexpr int kTcThreads = 32 * (kTcDW + 2);  // and a copy warp, an MMA warp
 constexpr int kTcSlab = kTcBM * 16 * 2;              // one K = 16 slab of 128 rows (4 KB)
-constexpr int kTcAHalf = 4 * kTcSlab;                // hi (or lo) of one stage (16 KB)
-constexpr int kTcASlot = 2 * kTcAHalf;               // hi + lo (32 KB)
 constexpr int kTcRawSlot = 8 * kRecQ4_0;             // eight records of one chunk (9 KB)
-constexpr int kTcOffFlags = 192;                     // tensor-memory address, abort flag
-constexpr int kTcOffRowP = 256;                      // [128] fp32 row factors P, then [128] their inverses
+constexpr int kTcOffFlags = 512;                     // tensor-memory address, abort flag
+constexpr int kTcOffRowP = 1024;                     // [128] fp32 row factors P, then [128] their inverses
 constexpr int kTcOffA = 2048;
 // Per column-tile width BN (activation rows per CTA: 128, 256 or 512; the
 // MMA's N is BN up to 256, and a 512-wide tile takes two N = 256 MMAs per
@@ -66,10 +63,19 @@ struct TcCfg {
     static_assert(BN == 128 || BN == 256 || BN == 512, "column tile");
     static constexpr int NN = BN > 256 ? 256 : BN;             // the MMA's N
     static constexpr int NH = BN / NN;                          // MMAs per step and operand
-    static constexpr int SA = BN == 512 ? 2 : 3;                // hi / lo operand slots
-    static constexpr int SB = BN == 128 ? 6 : BN == 256 ? 3 : 2;  // activation slots
-    static constexpr int BSlot = BN * kTcBK * 2;  // activations of one stage (16 / 32 / 64 KB)
-    static constexpr int OffB = kTcOffA + SA * kTcASlot;
+    // columns per stage: 32 for the 512-wide tile (four operand slots in
+    // flight instead of two: 105 -> 96 us at nb = 512), else 64 (fewer
+    // hand-offs: 32-column stages measured 52 -> 67 us at nb = 128)
+    static constexpr int BK = BN == 512 ? 32 : 64;
+    static constexpr int BPS = BK / 32;               // blocks per stage
+    static constexpr int SPC = 4 / BPS;               // stages per 128-column record chunk
+    static constexpr int AHalf = (BK / 16) * kTcSlab;  // hi (or lo) of one stage
+    static constexpr int ASlot = 2 * AHalf;           // hi + lo
+    // hi / lo operand slots and activation slots: 192 KB between them
+    static constexpr int SA = BN == 512 ? 4 : 3;
+    static constexpr int SB = BN == 128 ? 6 : BN == 256 ? 3 : 4;
+    static constexpr int BSlot = BN * BK * 2;  // activations of one stage
+    static constexpr int OffB = kTcOffA + SA * ASlot;
     static constexpr int OffRaw = OffB + SB * BSlot;
     static constexpr int Smem = OffRaw + kTcSR * kTcRawSlot;
     static_assert(Smem <= (int)kSmemMax, "tcgen05 GEMM shared memory");
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(256) q4gemm_tc_stage_kernel(const __grid_const
     __shared__ float red[8];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = blockIdx.x;  // activation row
-    const int NS = 2 * p.C, KT = p.C * kChunkK, KG = KT / 8, KGv = p.K / 8;
+    const int NS = Cf::SPC * p.C, KT = p.C * kChunkK, KG = KT / 8, KGv = p.K / 8;
     const bool live = r < p.nb;
     const float *xr = p.x + (size_t)r * p.K;
     float2 v[kTcStageG][4];
@@ -167,7 +173,7 @@ __global__ void __launch_bounds__(256) q4gemm_tc_stage_kernel(const __grid_const
             const __half2 h2 = __floats2half2_rn(u[q].x * sc, u[q].y * sc);
             hw[q] = *reinterpret_cast<const uint32_t *>(&h2);
         }
-        const int k = 8 * gi, s = k / kTcBK, sl = (k % kTcBK) / 16;
+        const int k = 8 * gi, s = k / Cf::BK, sl = (k % Cf::BK) / 16;
         *reinterpret_cast<uint4 *>(base + (size_t)s * Cf::BSlot + sl * (BN * 32) + tc::slab_off(rr, k % 16)) =
             make_uint4(hw[0], hw[1], hw[2], hw[3]);
     };
@@ -240,21 +246,24 @@ __device__ __forceinline__ void tc_row_factors(const GemmParams &p, int tile, bo
     }
 }
 
-// One stage's share of a dequant warp: rows 16 tile + 8 h + g
-// of the record tile, blocks 2 jh and 2 jh + 1 of the chunk.  wv holds the
-// lane's nibble words of the row's four blocks, sv the four blocks' scale
-// words (rows g | g + 8).  Lane-position tp holds the block's
-// elements 8 m + 2 tp and 8 m + 2 tp + 1 (nibbles m and m + 4), m = 0..3; in
-// the operands' column order (tc_col) they are the eight consecutive
-// columns 8 tp .. 8 tp + 7 of the block, so each of hi and lo is one 16-byte
-// store at `rowoff` (+ the block's two slabs).
-__device__ __forceinline__ void tc_dequant(const uint4 &wv, const uint4 &sv, float P, int h, int jh, uint32_t a_hi,
+// One stage's share of a dequant warp: rows 16 tile + 8 h + g of the record
+// tile, blocks BPS part .. BPS part + BPS - 1 of the chunk.  wv holds the lane's nibble words
+// of the row's four blocks, sv the four blocks' scale words (rows g | g + 8).
+// Lane-position tp holds the block's elements 8 m + 2 tp and 8 m + 2 tp + 1
+// (nibbles m and m + 4), m = 0..3; in the operands' column order (tc_col)
+// they are the eight consecutive columns 8 tp .. 8 tp + 7 of the block, so
+// each of hi and lo is one 16-byte store at `rowoff` (+ the block's slabs).
+__device__ __forceinline__ uint32_t word_at(const uint4 &v, int j) {
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+template <int BPS>
+__device__ __forceinline__ void tc_dequant(const uint4 &wv, const uint4 &sv, float P, int h, int part, uint32_t a_hi,
                                            uint32_t a_lo, uint32_t rowoff) {
     const __half2 k1032 = __float2half2_rn(1032.f);
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-        const uint32_t word = jh ? (jj ? wv.w : wv.z) : (jj ? wv.y : wv.x);
-        const uint32_t sw = jh ? (jj ? sv.w : sv.z) : (jj ? sv.y : sv.x);
+    for (int jj = 0; jj < BPS; ++jj) {
+        const int j = BPS * part + jj;
+        const uint32_t word = word_at(wv, j), sw = word_at(sv, j);
         const __half dh = __ushort_as_half((unsigned short)(h ? sw >> 16 : sw & 0xFFFFu));
         const __half2 d2 = __float2half2_rn(__half2float(dh) * P);  // d P: exact
         uint32_t hv[4], lv[4];
@@ -298,7 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nt = blockIdx.x, mt = blockIdx.y;  // activation (column) tile fastest, weight row tile
     const int t0 = 8 * mt, tiles = min(8, p.T - t0);
-    const int C = p.C, NS = 2 * C;
+    const int C = p.C, NS = Cf::SPC * C;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t raw_full = sbase, raw_empty = raw_full + 8 * SR, b_full = raw_empty + 8 * SR;
     const uint32_t a_full = b_full + 8 * SB, mma_done = a_full + 8 * SA;
@@ -363,8 +372,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
             while (raw_issued < C || b_issued < NS) {
                 if (*abort_flag) break;
                 // the next copy due: the image slice of stage b_issued, or
-                // chunk raw_issued's records (needed by stage 2 raw_issued)
-                const bool take_b = b_issued < NS && (raw_issued >= C || b_issued <= 2 * raw_issued);
+                // chunk raw_issued's records (needed by stage SPC raw_issued)
+                const bool take_b = b_issued < NS && (raw_issued >= C || b_issued <= Cf::SPC * raw_issued);
                 if (take_b) {
                     const int s = b_issued;
                     if (!mbar_wait(mma_done + 8 * ((s - SB) % SB), (uint32_t)((s - SB) / SB) & 1u, lim)) {
@@ -399,16 +408,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
                 }
                 tc::fence_after_sync();
                 // descriptors advance by (byte offset >> 4) in their start field
-                const uint64_t ad = a0 + (uint64_t)(((s % SA) * kTcASlot) >> 4);
+                const uint64_t ad = a0 + (uint64_t)(((s % SA) * Cf::ASlot) >> 4);
                 const uint64_t bd = b0 + (uint64_t)(((s % SB) * Cf::BSlot) >> 4);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
+                for (int ks = 0; ks < Cf::BK / 16; ++ks) {
 #pragma unroll
                     for (int nh = 0; nh < Cf::NH; ++nh) {  // activation rows NN nh .. into columns NN nh ..
                         const uint64_t bk = bd + (uint64_t)((ks * (BN * 32) + nh * (Cf::NN * 32)) >> 4);
                         const uint32_t d = taddr + (uint32_t)(nh * Cf::NN);
                         tc::mma_f16(d, ad + (uint64_t)((ks * kTcSlab) >> 4), bk, idesc, (s | ks) != 0);
-                        tc::mma_f16(d, ad + (uint64_t)((kTcAHalf + ks * kTcSlab) >> 4), bk, idesc, 1u);
+                        tc::mma_f16(d, ad + (uint64_t)((Cf::AHalf + ks * kTcSlab) >> 4), bk, idesc, 1u);
                     }
                 }
                 tc::commit(mma_done + 8 * (s % SB));
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
         const uint32_t rowoff = (uint32_t)((tp >> 1) * kTcSlab + (2 * tile + h) * 256 + (tp & 1) * 128 + g * 16);
         uint4 wv = make_uint4(0u, 0u, 0u, 0u), sv = wv;
         for (int s = 0; s < NS; ++s) {
-            const int c = s >> 1, jh = s & 1;
+            const int c = s / Cf::SPC, jh = s % Cf::SPC;  // chunk, part
             if (*abort_flag) break;
             bool ok = true;
             // the operand slot is free once the MMAs of stage s - SA are done
@@ -446,8 +455,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
                 wv = *reinterpret_cast<const uint4 *>(rec + h * 512 + (4 * g + tp) * 16);
                 sv = *reinterpret_cast<const uint4 *>(rec + 1024 + g * 16);
             }
-            const uint32_t a_hi = a_base + (s % SA) * kTcASlot;
-            if (live) tc_dequant(wv, sv, P, h, jh, a_hi, a_hi + kTcAHalf, rowoff);
+            const uint32_t a_hi = a_base + (s % SA) * Cf::ASlot;
+            if (live) tc_dequant<Cf::BPS>(wv, sv, P, h, jh, a_hi, a_hi + Cf::AHalf, rowoff);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the slabs, for the tensor core
             __syncwarp();
             if (lane == 0) {
