@@ -18,21 +18,23 @@
 //
 // Two launches.  q4gemm_tc_stage_kernel writes the activation image: per
 // BN-row column tile (BN = 512 over 256 rows, 256 over 128, else 128) and
-// stage of BK columns (32 at BN = 512, else 64), K = 16 slabs in the K-major, unswizzled operand
-// layout (tc_common.cuh), with the columns of each 32-column block in the
-// order of the weight records' lanes (tc_col), plus each row's factor back.
+// stage of BK columns (32 at BN = 512, else 64), K = 16 slabs in the
+// K-major, unswizzled operand layout (tc_common.cuh), with the columns of
+// each 32-column block in the order of the weight records' lanes (tc_col),
+// plus each row's factor back.
 // q4gemm_tc_kernel gives each CTA 128 weight rows (eight 16-row record
 // tiles) by BN activation rows, one 128 x BN fp32 accumulator in tensor
 // memory (a 512-wide tile fills all 512 columns, two N = 256 MMAs per step),
 // and three warp roles (q4gemm_tc_kernel):
 //   * a copy warp brings the eight tiles' 128-column records (a ring of three
 //     chunk slots, each chunk feeding 128 / BK stages) and each stage's image
-//     slice (a ring of six, three or two slots) in by bulk copies (TMA engine);
+//     slice (a ring of six, three or four slots) in by bulk copies (TMA
+//     engine);
 //   * sixteen dequant warps turn each stage's records into hi / lo operand
-//     slabs (a ring of three slots, two at BN = 512), one 16-byte store per
+//     slabs (a ring of three slots, four at BN = 512), one 16-byte store per
 //     lane and slab;
-//   * an MMA warp issues each stage's MMAs (four K = 16 steps, hi and lo,
-//     M = 128, N = min(BN, 256)) and commits them to the stage's mbarrier,
+//   * an MMA warp issues each stage's MMAs (BK / 16 steps of K = 16, hi and
+//     lo, M = 128, N = min(BN, 256)) and commits them to the stage's mbarrier,
 //     which frees the operand and activation slots;
 //   * at the end the dequant warps read the accumulator out of tensor memory
 //     (warp w: lanes 32 (w % 4) .., columns (BN / 4) (w / 4) ..), scale and
