@@ -385,9 +385,13 @@ q4_status q4_argmax_noalloc(const q4_weight *W, const float *x, const float *gam
  * nb > 16, where the GEMV family re-reads the weights per 16 rows); every
  * weight format.  x: [nb][k] fp32; y: [nb][n] fp32, overwritten, or with
  * accumulate != 0 y += x W^T (y must then hold the values to add to).
- * Numerics: every 32-column block of an activation row is scaled by its own
- * power of two and carried as one f16 per value (as the GEMV calls do above
- * four rows), weights exact, products accumulated in fp32.
+ * Numerics: weights exact, products accumulated in fp32, each activation
+ * carried as one f16 (relative rounding at most 2^-11) after a power-of-two
+ * scale: per 32-column block of a row (as the GEMV calls do above four rows)
+ * in the mma.sync form that serves every format, and Q4_0 up to 64 rows; per
+ * activation row in the tcgen05 form that serves Q4_0 from 65 rows (there the
+ * weights enter the tensor core as f16 hi + lo pairs with an exact sum, and
+ * the fp32 accumulator lives in tensor memory).
  * Workspace: q4_gemm_workspace_bytes(nb, k) device bytes (16-byte aligned,
  * contents need not be initialised) hold the staged activations; the call
  * launches a staging kernel and the GEMM kernel on `stream`.
