@@ -26,13 +26,12 @@
 // tiles) by BN activation rows, one 128 x BN fp32 accumulator in tensor
 // memory (a 512-wide tile fills all 512 columns, two N = 256 MMAs per step),
 // and three warp roles (q4gemm_tc_kernel):
-//   * a copy warp brings the eight tiles' 128-column records (a ring of three
-//     chunk slots, each chunk feeding 128 / BK stages) and each stage's image
-//     slice (a ring of six, three or four slots) in by bulk copies (TMA
-//     engine);
-//   * sixteen dequant warps turn each stage's records into hi / lo operand
-//     slabs (a ring of three slots, four at BN = 512), one 16-byte store per
-//     lane and slab;
+//   * a copy warp brings each stage's image slice in by bulk copies (TMA
+//     engine; a ring of six, three or four slots);
+//   * sixteen dequant warps read their lanes' record words straight from
+//     global memory, three 128-column chunks ahead, and turn each stage's
+//     records into hi / lo operand slabs (a ring of four slots, six at
+//     BN = 512), one 16-byte store per lane and slab;
 //   * an MMA warp issues each stage's MMAs (BK / 16 steps of K = 16, hi and
 //     lo, M = 128, N = min(BN, 256)) and commits them to the stage's mbarrier,
 //     which frees the operand and activation slots;
@@ -48,11 +47,9 @@ namespace q4 {
 namespace dev {
 
 constexpr int kTcBM = 128;           // weight rows per CTA (eight record tiles)
-constexpr int kTcSR = 3;             // raw chunk slots
 constexpr int kTcDW = 16;                    // dequant warps (two per record tile)
 constexpr int kTcThreads = 32 * (kTcDW + 2);  // and a copy warp, an MMA warp
 constexpr int kTcSlab = kTcBM * 16 * 2;              // one K = 16 slab of 128 rows (4 KB)
-constexpr int kTcRawSlot = 8 * kRecQ4_0;             // eight records of one chunk (9 KB)
 constexpr int kTcOffFlags = 512;                     // tensor-memory address, abort flag
 constexpr int kTcOffRowP = 1024;                     // [128] fp32 row factors P, then [128] their inverses
 constexpr int kTcOffA = 2048;
@@ -73,18 +70,17 @@ struct TcCfg {
     static constexpr int SPC = 4 / BPS;               // stages per 128-column record chunk
     static constexpr int AHalf = (BK / 16) * kTcSlab;  // hi (or lo) of one stage
     static constexpr int ASlot = 2 * AHalf;           // hi + lo
-    // hi / lo operand slots and activation slots: 192 KB between them
-    static constexpr int SA = BN == 512 ? 4 : 3;
+    // hi / lo operand slots and activation slots: 224 KB between them
+    static constexpr int SA = BN == 512 ? 6 : 4;
     static constexpr int SB = BN == 128 ? 6 : BN == 256 ? 3 : 4;
+    // stage completions: a waiter for stage k's must find it the slot's
+    // latest or the one before, so the ring is as deep as both rings
+    static constexpr int MD = SA > SB ? SA : SB;
     static constexpr int BSlot = BN * BK * 2;  // activations of one stage
     static constexpr int OffB = kTcOffA + SA * ASlot;
-    static constexpr int OffRaw = OffB + SB * BSlot;
-    static constexpr int Smem = OffRaw + kTcSR * kTcRawSlot;
+    static constexpr int Smem = OffB + SB * BSlot;
     static_assert(Smem <= (int)kSmemMax, "tcgen05 GEMM shared memory");
-    static_assert(8 * (2 * kTcSR + 2 * SB + SA) <= kTcOffFlags, "barrier area");
-    // the stage completions live in SB slots; a dequant warp waits on stage
-    // s - SA's, which must still be the slot's latest or the one before
-    static_assert(SB >= SA, "completion ring at least as deep as the operand ring");
+    static_assert(8 * (SB + SA + MD) <= kTcOffFlags, "barrier area");
 };
 // the column tile of a batch: 512 rows above 256, 256 above 128, else 128
 // (one wave of 112 CTAs at 512 rows on a 14336-row matrix, and twice the
@@ -292,32 +288,31 @@ __device__ __forceinline__ void tc_dequant(const uint4 &wv, const uint4 &sv, flo
 // w / 2) and run the epilogue, warp 16 lane 0 issues the bulk copies, warp 17
 // lane 0 issues the MMAs (warp 17 also owns the tensor memory).  They hand
 // slots over through mbarriers only:
-//   raw_full[c % SR]  chunk c's records landed          (copies; producer arms)
-//   raw_empty[c % SR] the sixteen dequant warps read it  (16 arrivals)
 //   b_full[s % SB]    stage s's image slice landed       (copy; producer arms)
 //   a_full[s % SA]    stage s's hi / lo slabs written    (16 arrivals)
-//   mma_done[s % SB]  stage s's MMAs completed           (tcgen05.commit)
+//   mma_done[s % MD]  stage s's MMAs completed           (tcgen05.commit)
 // A dequant warp writes stage s's operand slot after mma_done of stage
 // s - SA; the producer loads stage s's image slice after mma_done of stage
-// s - SB and chunk c's records after raw_empty of chunk c - SR.  Each such
-// ordering keeps every barrier within one phase of its waiters.
+// s - SB.  With MD >= SA, SB each such ordering keeps every barrier within
+// one phase of its waiters.  (The records went through a shared-memory ring
+// of bulk copies before: reading them into registers freed 27 KB for a
+// fourth (sixth) operand slot, 97 -> 89 us at nb = 512 and 52 -> 44 us at
+// nb = 128.)
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_constant__ GemmParams p) {
     using Cf = TcCfg<BN>;
-    constexpr int SA = Cf::SA, SB = Cf::SB, SR = kTcSR;
+    constexpr int SA = Cf::SA, SB = Cf::SB, MD = Cf::MD;
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nt = blockIdx.x, mt = blockIdx.y;  // activation (column) tile fastest, weight row tile
     const int t0 = 8 * mt, tiles = min(8, p.T - t0);
     const int C = p.C, NS = Cf::SPC * C;
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t raw_full = sbase, raw_empty = raw_full + 8 * SR, b_full = raw_empty + 8 * SR;
-    const uint32_t a_full = b_full + 8 * SB, mma_done = a_full + 8 * SA;
+    const uint32_t b_full = sbase, a_full = b_full + 8 * SB, mma_done = a_full + 8 * SA;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kTcOffFlags);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kTcOffFlags + 4);
     float *rowP = reinterpret_cast<float *>(smem + kTcOffRowP);
     const uint32_t a_base = sbase + kTcOffA, b_base = sbase + Cf::OffB;
-    uint8_t *raw = smem + Cf::OffRaw;
     const uint8_t *img = p.img + (size_t)nt * NS * Cf::BSlot;
     const long long lim = p.wait_cycles;
     auto fail = [&]() {
@@ -326,14 +321,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
     };
 
     if (tid == 0) {
-        for (int i = 0; i < SR; ++i) {
-            mbar_init(raw_full + 8 * i, 1);
-            mbar_init(raw_empty + 8 * i, kTcDW);
-        }
-        for (int i = 0; i < SB; ++i) {
-            mbar_init(b_full + 8 * i, 1);
-            mbar_init(mma_done + 8 * i, 1);
-        }
+        for (int i = 0; i < SB; ++i) mbar_init(b_full + 8 * i, 1);
+        for (int i = 0; i < MD; ++i) mbar_init(mma_done + 8 * i, 1);
         for (int i = 0; i < SA; ++i) mbar_init(a_full + 8 * i, kTcDW);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -348,52 +337,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
     tc::fence_after_sync();
     const uint32_t taddr = *tslot;
 
-    int raw_issued = 0, b_issued = 0, mma_issued = 0;  // the issuing lanes' counts
+    int b_issued = 0, mma_issued = 0;  // the issuing lanes' counts
     if (warp == kTcDW) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
-            auto issue_raw = [&](int c) {
-                const uint32_t bar = raw_full + 8 * (c % SR);
-                // extra_tx: testing the give-up path only
-                mbar_expect_tx(bar, (uint32_t)(tiles * kRecQ4_0) + (c == 0 ? (uint32_t)p.extra_tx : 0u));
-                for (int i = 0; i < tiles; ++i)
-                    bulk_g2s_keep(smem_u32(raw + (c % SR) * kTcRawSlot + i * kRecQ4_0),
-                                  p.w + ((size_t)(t0 + i) * C + c) * kRecQ4_0, kRecQ4_0, bar);
-            };
             auto issue_b = [&](int s) {
                 const uint32_t bar = b_full + 8 * (s % SB);
-                mbar_expect_tx(bar, Cf::BSlot);
+                // extra_tx: testing the give-up path only
+                mbar_expect_tx(bar, Cf::BSlot + (s == 0 ? (uint32_t)p.extra_tx : 0u));
                 bulk_g2s_keep(b_base + (s % SB) * Cf::BSlot, img + (size_t)s * Cf::BSlot, Cf::BSlot, bar);
             };
-            // the weights do not depend on the staging kernel: their first
-            // chunks go out before waiting for it, the image slices after
-            for (; raw_issued < min(SR, C); ++raw_issued) issue_raw(raw_issued);
             asm volatile("griddepcontrol.wait;" ::: "memory");
             for (; b_issued < min(SB, NS); ++b_issued) issue_b(b_issued);
-            // then, in stage order, each slot as soon as it is free
-            while (raw_issued < C || b_issued < NS) {
+            // then, in stage order, each slot as soon as its MMAs are done
+            for (; b_issued < NS; ++b_issued) {
                 if (*abort_flag) break;
-                // the next copy due: the image slice of stage b_issued, or
-                // chunk raw_issued's records (needed by stage SPC raw_issued)
-                const bool take_b = b_issued < NS && (raw_issued >= C || b_issued <= Cf::SPC * raw_issued);
-                if (take_b) {
-                    const int s = b_issued;
-                    if (!mbar_wait(mma_done + 8 * ((s - SB) % SB), (uint32_t)((s - SB) / SB) & 1u, lim)) {
-                        fail();
-                        break;
-                    }
-                    issue_b(s);
-                    ++b_issued;
-                } else {
-                    const int c = raw_issued;
-                    if (!mbar_wait(raw_empty + 8 * ((c - SR) % SR), (uint32_t)((c - SR) / SR) & 1u, lim)) {
-                        fail();
-                        break;
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    issue_raw(c);
-                    ++raw_issued;
+                const int s = b_issued;
+                if (!mbar_wait(mma_done + 8 * ((s - SB) % MD), (uint32_t)((s - SB) / MD) & 1u, lim)) {
+                    fail();
+                    break;
                 }
+                issue_b(s);
             }
         }
     } else if (warp == kTcDW + 1) {
@@ -422,15 +386,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
                         tc::mma_f16(d, ad + (uint64_t)((Cf::AHalf + ks * kTcSlab) >> 4), bk, idesc, 1u);
                     }
                 }
-                tc::commit(mma_done + 8 * (s % SB));
+                tc::commit(mma_done + 8 * (s % MD));
                 mma_issued = s + 1;
             }
         }
     } else {
         // ---------------------------------------------------------- dequant
-        // warp w: record tile w / 2, rows 8 (w % 2) + g; the lane's words of
-        // a chunk are loaded once, at its first stage, and the raw slot is
-        // handed back after that stage
+        // warp w: record tile w / 2, rows 8 (w % 2) + g.  Each lane reads its
+        // 16-byte nibble word and the 16-byte scale word of a chunk straight
+        // from global memory, three chunks ahead of their use.
         // lanes 8 tp .. 8 tp + 7 take lane-position tp of rows g = 0..7, so
         // that each quarter-warp's 16-byte stores fill 128 contiguous bytes
         const int tile = warp >> 1, h = warp & 1, g = lane & 7, tp = lane >> 3;
@@ -439,32 +403,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
         // columns 8 tp .. 8 tp + 7 of a block: slab tp / 2 of its two, core
         // matrix half tp % 2
         const uint32_t rowoff = (uint32_t)((tp >> 1) * kTcSlab + (2 * tile + h) * 256 + (tp & 1) * 128 + g * 16);
-        uint4 wv = make_uint4(0u, 0u, 0u, 0u), sv = wv;
+        const uint8_t *wrec = p.w + (size_t)(t0 + tile) * C * kRecQ4_0;
+        auto load = [&](int c, uint4 &w, uint4 &sc) {
+            if (live && c < C) {
+                w = __ldg(reinterpret_cast<const uint4 *>(wrec + (size_t)c * kRecQ4_0 + h * 512 + (4 * g + tp) * 16));
+                sc = __ldg(reinterpret_cast<const uint4 *>(wrec + (size_t)c * kRecQ4_0 + 1024 + g * 16));
+            }
+        };
+        uint4 w0 = make_uint4(0u, 0u, 0u, 0u), s0 = w0, w1 = w0, s1 = w0, w2 = w0, s2 = w0;
+        load(0, w0, s0);
+        load(1, w1, s1);
+        load(2, w2, s2);
         for (int s = 0; s < NS; ++s) {
             const int c = s / Cf::SPC, jh = s % Cf::SPC;  // chunk, part
             if (*abort_flag) break;
-            bool ok = true;
+            if (jh == 0 && c > 0) {  // the next chunk's words; chunk c + 2's load goes out
+                w0 = w1;
+                s0 = s1;
+                w1 = w2;
+                s1 = s2;
+                load(c + 2, w2, s2);
+            }
             // the operand slot is free once the MMAs of stage s - SA are done
-            if (s >= SA) ok = mbar_wait(mma_done + 8 * ((s - SA) % SB), (uint32_t)((s - SA) / SB) & 1u, lim);
-            if (ok && jh == 0) ok = mbar_wait(raw_full + 8 * (c % SR), (uint32_t)(c / SR) & 1u, lim);
+            const bool ok = s < SA || mbar_wait(mma_done + 8 * ((s - SA) % MD), (uint32_t)((s - SA) / MD) & 1u, lim);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) fail();
                 break;
             }
             tc::fence_after_sync();
-            if (jh == 0 && live) {
-                const uint8_t *rec = raw + (c % SR) * kTcRawSlot + tile * kRecQ4_0;
-                wv = *reinterpret_cast<const uint4 *>(rec + h * 512 + (4 * g + tp) * 16);
-                sv = *reinterpret_cast<const uint4 *>(rec + 1024 + g * 16);
-            }
             const uint32_t a_hi = a_base + (s % SA) * Cf::ASlot;
-            if (live) tc_dequant<Cf::BPS>(wv, sv, P, h, jh, a_hi, a_hi + Cf::AHalf, rowoff);
+            if (live) tc_dequant<Cf::BPS>(w0, s0, P, h, jh, a_hi, a_hi + Cf::AHalf, rowoff);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the slabs, for the tensor core
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(a_full + 8 * (s % SA));
-                if (jh == 0) mbar_arrive(raw_empty + 8 * (c % SR));  // its words are in registers
-            }
+            if (lane == 0) mbar_arrive(a_full + 8 * (s % SA));
         }
     }
 
@@ -475,7 +446,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
     asm volatile("griddepcontrol.wait;" ::: "memory");
     bool ok = !*abort_flag;
     if (ok && warp < kTcDW) {
-        const bool done = mbar_wait(mma_done + 8 * ((NS - 1) % SB), (uint32_t)((NS - 1) / SB) & 1u, lim);
+        const bool done = mbar_wait(mma_done + 8 * ((NS - 1) % MD), (uint32_t)((NS - 1) / MD) & 1u, lim);
         if (!__all_sync(0xffffffffu, done) && lane == 0) fail();
     }
     __syncthreads();
@@ -484,13 +455,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
         // let the copies and products in flight land, free the tensor
         // memory, store nothing
         if (warp == kTcDW && lane == 0) {
-            for (int c = max(0, raw_issued - SR); c < raw_issued; ++c)
-                mbar_wait(raw_full + 8 * (c % SR), (uint32_t)(c / SR) & 1u, kWaitCycles);
             for (int s = max(0, b_issued - SB); s < b_issued; ++s)
                 mbar_wait(b_full + 8 * (s % SB), (uint32_t)(s / SB) & 1u, kWaitCycles);
         }
         if (warp == kTcDW + 1 && lane == 0 && mma_issued > 0)
-            mbar_wait(mma_done + 8 * ((mma_issued - 1) % SB), (uint32_t)((mma_issued - 1) / SB) & 1u, kWaitCycles);
+            mbar_wait(mma_done + 8 * ((mma_issued - 1) % MD), (uint32_t)((mma_issued - 1) / MD) & 1u, kWaitCycles);
         tc::fence_before_sync();
         __syncthreads();
         if (warp == kTcDW + 1) {
