@@ -429,3 +429,30 @@ def test_debug_wait_limits_validation():
     assert L.q4_debug_wait_limits(0, 0, 0, 8) == 2          # bytes in multiples of 16
     assert L.q4_debug_wait_limits(0, 0, 0, 8192) == 2
     assert L.q4_debug_wait_limits(0, 0, 0, 0) == 0          # the defaults
+
+
+def test_record_lane_words_hold_the_tensor_memory_gemm_column_pairs():
+    # The tcgen05 GEMM's dequant reads, for row r and block j of a chunk, the
+    # 32-bit word of lane-position t (offset (r // 8) * 512 + (4 (r % 8) + t)
+    # * 16 + 4 j) and takes nibble m as element 8 m + 2 t and nibble m + 4 as
+    # element 8 m + 2 t + 1 of the block, m = 0..3.  Pin that against the
+    # library's own repack: every element gets a distinct nibble pattern.
+    # The scale word of (row pair g, g + 8; block j) sits at 1024 + 16 g + 4 j:
+    # row g's fp16 d in its low half, row g + 8's in its high half.
+    n, k = 16, 128
+    rng = np.random.default_rng(21)
+    q = rng.integers(0, 16, (n, k), dtype=np.uint8)
+    d = (0x3C00 + np.arange(n * (k // 32), dtype=np.uint16)).reshape(n, k // 32)
+    P = q4.repack_q4_0(wl.pack_q4_0(q, d), n, k)
+    for g in range(8):
+        for j in range(4):
+            sw = int(P[1024 + 16 * g + 4 * j:1024 + 16 * g + 4 * j + 4].view(np.uint32)[0])
+            assert sw & 0xFFFF == d[g, j] and sw >> 16 == d[g + 8, j]
+    for r in range(n):
+        for j in range(4):
+            for t in range(4):
+                off = (r // 8) * 512 + (4 * (r % 8) + t) * 16 + 4 * j
+                word = int(P[off:off + 4].view(np.uint32)[0])
+                for m in range(4):
+                    assert (word >> (4 * m)) & 15 == q[r, 32 * j + 8 * m + 2 * t]
+                    assert (word >> (4 * m + 16)) & 15 == q[r, 32 * j + 8 * m + 2 * t + 1]
