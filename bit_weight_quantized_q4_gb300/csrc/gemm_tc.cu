@@ -200,19 +200,33 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Record geometry of the formats this GEMM takes: Q4_0 (the nibble words of
+// rows 0..7 and 8..15 at 0 and 512, the scale words at 1024) and Q8_0 (the
+// biased bytes at 0 and 1024, blocks 2-3 512 bytes after blocks 0-1, the
+// scale words at 2048), and the largest |q| of each (|q - 8| <= 8, |q| <= 128).
+template <int FMT>
+struct TcFmt {
+    static_assert(FMT == 0 || FMT == 2, "Q4_0 or Q8_0");
+    static constexpr int REC = rec_bytes(FMT);
+    static constexpr int SOFF = FMT == 2 ? 2048 : 1024;
+    static constexpr float QMAX = FMT == 2 ? 128.f : 8.f;
+};
+
 // The row factors P (and 1 / P) of this lane's rows 16 w + g and 16 w + g + 8
 // from the largest |d| of each row over all chunks: lane (g, cp) reads the
 // scale words of chunks cp, cp + 4, ...; a butterfly over the four lanes of
 // g gives the row maxima.
+template <int FMT>
 __device__ __forceinline__ void tc_row_factors(const GemmParams &p, int tile, bool live, float *rowP, int w,
                                                int lane) {
+    using Fm = TcFmt<FMT>;
     const int g = lane >> 2, cp = lane & 3;
     float m0 = 0.f, m1 = 0.f;
     if (live) {
-        const uint8_t *base = p.w + (size_t)tile * p.C * kRecQ4_0 + 1024 + g * 16;
+        const uint8_t *base = p.w + (size_t)tile * p.C * Fm::REC + Fm::SOFF + g * 16;
 #pragma unroll 4
         for (int c = cp; c < p.C; c += 4) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(base + (size_t)c * kRecQ4_0));
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(base + (size_t)c * Fm::REC));
             const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -230,7 +244,7 @@ __device__ __forceinline__ void tc_row_factors(const GemmParams &p, int tile, bo
     if (cp == 0) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const float m = 8.f * (h ? m1 : m0);
+            const float m = Fm::QMAX * (h ? m1 : m0);
             float P = 1.f, Pi = 1.f;
             if (m > 0.f) {  // m = f 2^e, f in [0.5, 1): m P in [2^14, 2^15)
                 int e;
@@ -244,31 +258,74 @@ __device__ __forceinline__ void tc_row_factors(const GemmParams &p, int tile, bo
     }
 }
 
-// One stage's share of a dequant warp: rows 16 tile + 8 h + g of the record
-// tile, blocks BPS part .. BPS part + BPS - 1 of the chunk.  wv holds the lane's nibble words
-// of the row's four blocks, sv the four blocks' scale words (rows g | g + 8).
-// Lane-position tp holds the block's elements 8 m + 2 tp and 8 m + 2 tp + 1
-// (nibbles m and m + 4), m = 0..3; in the operands' column order (tc_col)
-// they are the eight consecutive columns 8 tp .. 8 tp + 7 of the block, so
-// each of hi and lo is one 16-byte store at `rowoff` (+ the block's slabs).
+// A dequant lane's words of one chunk, read straight from global memory:
+// rows 16 tile + 8 h + g (g = lane % 8), lane-position tp = lane / 8.  Q4_0:
+// the 16-byte nibble word (blocks 0..3); Q8_0: the 8 bytes of each block
+// (blocks 0-1, then 2-3); both: the four blocks' scale words (rows g | g + 8).
+template <int FMT>
+struct TcWords {
+    uint4 w[FMT == 2 ? 2 : 1];
+    uint4 sc;
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < (FMT == 2 ? 2 : 1); ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
+        sc = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __device__ __forceinline__ void load(const uint8_t *rec, int h, int g, int tp) {
+        using Fm = TcFmt<FMT>;
+        if constexpr (FMT == 2) {
+            w[0] = __ldg(reinterpret_cast<const uint4 *>(rec + h * 1024 + (4 * g + tp) * 16));
+            w[1] = __ldg(reinterpret_cast<const uint4 *>(rec + h * 1024 + 512 + (4 * g + tp) * 16));
+        } else {
+            w[0] = __ldg(reinterpret_cast<const uint4 *>(rec + h * 512 + (4 * g + tp) * 16));
+        }
+        sc = __ldg(reinterpret_cast<const uint4 *>(rec + Fm::SOFF + g * 16));
+    }
+};
+
 __device__ __forceinline__ uint32_t word_at(const uint4 &v, int j) {
     return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
-template <int BPS>
-__device__ __forceinline__ void tc_dequant(const uint4 &wv, const uint4 &sv, float P, int h, int part, uint32_t a_hi,
+// Element pair m (the block's elements at operand columns 8 tp + 2 m, + 1)
+// as f16x2 (q, q') exactly: Q4_0 from nibbles m and m + 4 of the block's
+// word (q - 8), Q8_0 from bytes 2 m and 2 m + 1 of its 8 (u - 128); a value
+// v <= 255 in the low byte of a half with exponent bits 0x64 is 1024 + v.
+template <int FMT>
+__device__ __forceinline__ __half2 tc_pair(const TcWords<FMT> &x, int j, int m) {
+    uint32_t b;
+    __half2 bias;
+    if constexpr (FMT == 2) {
+        const uint4 v = (j >> 1) ? x.w[FMT == 2 ? 1 : 0] : x.w[0];  // a select, not a dynamic index
+        const uint32_t word = (j & 1) ? ((m >> 1) ? v.w : v.z) : ((m >> 1) ? v.y : v.x);
+        if (m & 1)
+            asm("prmt.b32 %0, %1, 0x64, 0x4342;" : "=r"(b) : "r"(word));
+        else
+            asm("prmt.b32 %0, %1, 0x64, 0x4140;" : "=r"(b) : "r"(word));
+        bias = __float2half2_rn(1152.f);
+    } else {
+        b = ((word_at(x.w[0], j) >> (4 * m)) & 0x000F000Fu) | 0x64006400u;
+        bias = __float2half2_rn(1032.f);
+    }
+    return __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+}
+
+// One stage's share of a dequant warp: blocks BPS part .. BPS part + BPS - 1
+// of the chunk for its row.  Lane-position tp holds the block's elements at
+// operand columns 8 tp .. 8 tp + 7 (tc_col), so each of hi and lo is one
+// 16-byte store at `rowoff` (+ the block's slabs).
+template <int FMT, int BPS>
+__device__ __forceinline__ void tc_dequant(const TcWords<FMT> &x, float P, int h, int part, uint32_t a_hi,
                                            uint32_t a_lo, uint32_t rowoff) {
-    const __half2 k1032 = __float2half2_rn(1032.f);
 #pragma unroll
     for (int jj = 0; jj < BPS; ++jj) {
         const int j = BPS * part + jj;
-        const uint32_t word = word_at(wv, j), sw = word_at(sv, j);
+        const uint32_t sw = word_at(x.sc, j);
         const __half dh = __ushort_as_half((unsigned short)(h ? sw >> 16 : sw & 0xFFFFu));
         const __half2 d2 = __float2half2_rn(__half2float(dh) * P);  // d P: exact
         uint32_t hv[4], lv[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const uint32_t qb = ((word >> (4 * m)) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
-            const __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&qb), k1032);
+            const __half2 q2 = tc_pair<FMT>(x, j, m);
             const __half2 hi = __hmul2(q2, d2);
             const __half2 lo = __hfma2(q2, d2, __hneg2(hi));
             hv[m] = *reinterpret_cast<const uint32_t *>(&hi);
@@ -298,9 +355,10 @@ __device__ __forceinline__ void tc_dequant(const uint4 &wv, const uint4 &sv, flo
 // of bulk copies before: reading them into registers freed 27 KB for a
 // fourth (sixth) operand slot, 97 -> 89 us at nb = 512 and 52 -> 44 us at
 // nb = 128.)
-template <int BN>
+template <int FMT, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_constant__ GemmParams p) {
     using Cf = TcCfg<BN>;
+    using Fm = TcFmt<FMT>;
     constexpr int SA = Cf::SA, SB = Cf::SB, MD = Cf::MD;
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -331,7 +389,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
         tc::tmem_alloc(smem_u32(tslot), BN);
         tc::tmem_relinquish();
     }
-    if (warp < 8) tc_row_factors(p, t0 + warp, warp < tiles, rowP, warp, lane);  // warp w: tile w
+    if (warp < 8) tc_row_factors<FMT>(p, t0 + warp, warp < tiles, rowP, warp, lane);  // warp w: tile w
     tc::fence_before_sync();
     __syncthreads();  // barriers, tensor memory, row factors
     tc::fence_after_sync();
@@ -403,26 +461,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
         // columns 8 tp .. 8 tp + 7 of a block: slab tp / 2 of its two, core
         // matrix half tp % 2
         const uint32_t rowoff = (uint32_t)((tp >> 1) * kTcSlab + (2 * tile + h) * 256 + (tp & 1) * 128 + g * 16);
-        const uint8_t *wrec = p.w + (size_t)(t0 + tile) * C * kRecQ4_0;
-        auto load = [&](int c, uint4 &w, uint4 &sc) {
-            if (live && c < C) {
-                w = __ldg(reinterpret_cast<const uint4 *>(wrec + (size_t)c * kRecQ4_0 + h * 512 + (4 * g + tp) * 16));
-                sc = __ldg(reinterpret_cast<const uint4 *>(wrec + (size_t)c * kRecQ4_0 + 1024 + g * 16));
-            }
+        const uint8_t *wrec = p.w + (size_t)(t0 + tile) * C * Fm::REC;
+        auto load = [&](int c, TcWords<FMT> &x) {
+            if (live && c < C) x.load(wrec + (size_t)c * Fm::REC, h, g, tp);
         };
-        uint4 w0 = make_uint4(0u, 0u, 0u, 0u), s0 = w0, w1 = w0, s1 = w0, w2 = w0, s2 = w0;
-        load(0, w0, s0);
-        load(1, w1, s1);
-        load(2, w2, s2);
+        TcWords<FMT> x0, x1, x2;
+        x0.zero();
+        x1.zero();
+        x2.zero();
+        load(0, x0);
+        load(1, x1);
+        load(2, x2);
         for (int s = 0; s < NS; ++s) {
             const int c = s / Cf::SPC, jh = s % Cf::SPC;  // chunk, part
             if (*abort_flag) break;
             if (jh == 0 && c > 0) {  // the next chunk's words; chunk c + 2's load goes out
-                w0 = w1;
-                s0 = s1;
-                w1 = w2;
-                s1 = s2;
-                load(c + 2, w2, s2);
+                x0 = x1;
+                x1 = x2;
+                load(c + 2, x2);
             }
             // the operand slot is free once the MMAs of stage s - SA are done
             const bool ok = s < SA || mbar_wait(mma_done + 8 * ((s - SA) % MD), (uint32_t)((s - SA) / MD) & 1u, lim);
@@ -432,7 +488,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4gemm_tc_kernel(const __grid_c
             }
             tc::fence_after_sync();
             const uint32_t a_hi = a_base + (s % SA) * Cf::ASlot;
-            if (live) tc_dequant<Cf::BPS>(w0, s0, P, h, jh, a_hi, a_hi + Cf::AHalf, rowoff);
+            if (live) tc_dequant<FMT, Cf::BPS>(x0, P, h, jh, a_hi, a_hi + Cf::AHalf, rowoff);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the slabs, for the tensor core
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full + 8 * (s % SA));
@@ -511,11 +567,11 @@ size_t gemm_tc_image_bytes(int nb, int C) {
 
 // Q4_0 batches wider than 64 rows: the staging kernel, then the GEMM as its
 // programmatic dependent.
-template <int BN>
+template <int FMT, int BN>
 static int launch_gemm_tc_bn(const GemmParams &p, cudaStream_t stream) {
     using Cf = dev::TcCfg<BN>;
     static size_t smem_set[64] = {0};
-    if (!raise_smem(dev::q4gemm_tc_kernel<BN>, (size_t)Cf::Smem, smem_set)) return -1;
+    if (!raise_smem(dev::q4gemm_tc_kernel<FMT, BN>, (size_t)Cf::Smem, smem_set)) return -1;
     const int NT = (p.nb + BN - 1) / BN;
     dev::q4gemm_tc_stage_kernel<BN><<<NT * BN, 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return -1;
@@ -529,16 +585,23 @@ static int launch_gemm_tc_bn(const GemmParams &p, cudaStream_t stream) {
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dev::q4gemm_tc_kernel<BN>, p) == cudaSuccess ? 0 : -1;
+    return cudaLaunchKernelEx(&cfg, dev::q4gemm_tc_kernel<FMT, BN>, p) == cudaSuccess ? 0 : -1;
 }
 
-int launch_gemm_tc(const GemmParams &p, void *stream_) {
-    cudaStream_t stream = (cudaStream_t)stream_;
+template <int FMT>
+static int launch_gemm_tc_fmt(const GemmParams &p, cudaStream_t stream) {
     switch (dev::tc_bn(p.nb)) {
-        case 512: return launch_gemm_tc_bn<512>(p, stream);
-        case 256: return launch_gemm_tc_bn<256>(p, stream);
-        default: return launch_gemm_tc_bn<128>(p, stream);
+        case 512: return launch_gemm_tc_bn<FMT, 512>(p, stream);
+        case 256: return launch_gemm_tc_bn<FMT, 256>(p, stream);
+        default: return launch_gemm_tc_bn<FMT, 128>(p, stream);
     }
+}
+
+int launch_gemm_tc(const GemmParams &p, int fmt, void *stream_) {
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (fmt == 2) return launch_gemm_tc_fmt<2>(p, stream);
+    if (fmt == 0) return launch_gemm_tc_fmt<0>(p, stream);
+    return -1;
 }
 
 }  // namespace q4

@@ -68,23 +68,28 @@ def test_gemm_workload_shape_and_determinism(q4):
     check(to_np(y)[:, rows], ref, S, what="gemm 14336x4096 nb=256 (sampled rows)")
 
 
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
 @pytest.mark.parametrize("nb", [65, 130, 257])
-def test_gemm_scale_range(q4, nb):
-    # Q4_0 from 65 rows runs on the tensor-memory form, whose operands carry a
-    # power of two per weight row and per activation row: weight rows whose
-    # block scales span 2^-14 .. 2^15 (a few rows all zero), activation rows
-    # from 1e-12 to 1e12, against the oracle at the plain tolerance
+def test_gemm_scale_range(q4, fmt, nb):
+    # Q4_0 and Q8_0 from 65 rows run on the tensor-memory form, whose operands
+    # carry a power of two per weight row and per activation row: weight rows
+    # whose block scales span 2^-14 .. 2^15 (2^-14 .. 2^11 for Q8_0, whose
+    # weights reach 128 d; a few rows all zero), activation rows from 1e-12 to
+    # 1e12, against the oracle at the plain tolerance
     rng = np.random.default_rng(80 + nb)
     n, k = 200, 1024
-    q = rng.integers(0, 16, (n, k), dtype=np.uint8)
-    e = rng.integers(-13, 14, (n, 1)) + rng.integers(-6, 1, (n, k // 32))
+    top = 14 if fmt == "q4_0" else 10
+    e = rng.integers(-13, top, (n, 1)) + rng.integers(-6, 1, (n, k // 32))
     d = (rng.uniform(1.0, 2.0, (n, k // 32)) * 2.0 ** e).astype(np.float16)
     d[rng.choice(n, 4, replace=False)] = 0
-    H = wl.Q4_0Host(n, k, wl.pack_q4_0(q, d.view(np.uint16)))
+    if fmt == "q4_0":
+        H = wl.Q4_0Host(n, k, wl.pack_q4_0(rng.integers(0, 16, (n, k), dtype=np.uint8), d.view(np.uint16)))
+    else:
+        H = wl.Q8_0Host(n, k, wl.pack_q8_0(rng.integers(-128, 128, (n, k), dtype=np.int16), d.view(np.uint16)))
     x = wl.draw_x(rng, nb, k) * (10.0 ** rng.integers(-12, 13, (nb, 1))).astype(np.float32)
     y = q4.q4_gemm(dev_weight(H), torch.from_numpy(x).cuda())
     ref, S = oracle.q4_gemv(host_weight(H), x)
-    check(to_np(y), ref, S, what="gemm scale range nb=%d" % nb)
+    check(to_np(y), ref, S, what="gemm scale range %s nb=%d" % (fmt, nb))
 
 
 def test_gemm_zero_weights_exact(q4):
