@@ -1,15 +1,16 @@
 // gemm_tc.cu -- prefill GEMM on the fifth-generation tensor cores (tcgen05,
-// accumulators in tensor memory) for Q4_0 weights and batches wider than 64
-// rows: y[nb][n] = x[nb][k] W^T (crate inferencelayer, Functions:
+// accumulators in tensor memory) for Q4_0 and Q8_0 weights and batches wider
+// than 64 rows: y[nb][n] = x[nb][k] W^T (crate inferencelayer, Functions:
 // gemm_q4_src -- a blocked GEMM whose column tile shares one weight stream).
 //
 // The per-block scales stay exact without per-block partial sums: every
 // weight enters the tensor core as two f16 values hi + lo whose sum is
-// exactly d * (q - 8) * P, where P is a power of two per weight row chosen
-// so that the row's largest |8 d| * P lies in [2^14, 2^15) (no f16
-// overflow, no subnormal scales).  hi = f16(d' (q - 8)) with d' = d P, and
-// lo = f16(d' (q - 8) - hi) is exact: d' (q - 8) has at most 14 significant
-// bits and lies on the grid of ulp(d').  The activations enter as one f16
+// exactly d * q * P (Q4_0: q - 8 for its nibble q; Q8_0: its signed byte),
+// where P is a power of two per weight row chosen so that the row's largest
+// |q|max |d| P lies in [2^14, 2^15) (|q|max = 8 or 128: no f16 overflow, no
+// subnormal scales).  hi = f16(d' q) with d' = d P, and lo = f16(d' q - hi)
+// is exact: d' q has at most 14 (Q8_0: 18) significant bits and lies on the
+// grid of ulp(d').  The activations enter as one f16
 // per value after a power-of-two scale per row of x that puts the row's
 // largest magnitude in [2^14, 2^15), so the only rounding before the fp32
 // accumulation is the activation's (relative 2^-11).  The K sum then runs
@@ -565,7 +566,7 @@ size_t gemm_tc_image_bytes(int nb, int C) {
     return dev::tc_image_bytes(nb, C) + (size_t)((nb + BN - 1) / BN) * BN * sizeof(float);
 }
 
-// Q4_0 batches wider than 64 rows: the staging kernel, then the GEMM as its
+// Q4_0 and Q8_0 batches wider than 64 rows: the staging kernel, then the GEMM as its
 // programmatic dependent.
 template <int FMT, int BN>
 static int launch_gemm_tc_bn(const GemmParams &p, cudaStream_t stream) {
