@@ -762,7 +762,7 @@ extern "C" q4_status q4_decode_check(const void *workspace, cudaStream_t stream)
 
 extern "C" size_t q4_gemm_workspace_bytes(int32_t nb, int32_t k) {
     if (nb < 1 || nb > (1 << 20) || !shape_ok(1, k)) return 0;
-    // enough for either form (the tensor-memory one takes Q4_0 and Q8_0 from 65 rows)
+    // enough for either form (the tensor-memory one takes Q4_0 and Q8_0 from 17 rows)
     const int C = (int)q4::chunks_of(k);
     const size_t a = q4::gemm_image_bytes(nb, C), b = nb >= q4::kGemmTcMinNb ? q4::gemm_tc_image_bytes(nb, C) : 0;
     return a > b ? a : b;

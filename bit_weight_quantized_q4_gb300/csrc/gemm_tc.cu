@@ -1,6 +1,6 @@
 // gemm_tc.cu -- prefill GEMM on the fifth-generation tensor cores (tcgen05,
 // accumulators in tensor memory) for Q4_0 and Q8_0 weights and batches wider
-// than 64 rows: y[nb][n] = x[nb][k] W^T (crate inferencelayer, Functions:
+// than 16 rows: y[nb][n] = x[nb][k] W^T (crate inferencelayer, Functions:
 // gemm_q4_src -- a blocked GEMM whose column tile shares one weight stream).
 //
 // The per-block scales stay exact without per-block partial sums: every
@@ -583,7 +583,7 @@ size_t gemm_tc_image_bytes(int nb, int C) {
     return dev::tc_image_bytes(nb, C) + (size_t)((nb + BN - 1) / BN) * BN * sizeof(float);
 }
 
-// Q4_0 and Q8_0 batches wider than 64 rows: the staging kernel, then the GEMM as its
+// Q4_0 and Q8_0 batches wider than 16 rows: the staging kernel, then the GEMM as its
 // programmatic dependent.
 template <int FMT, int BN>
 static int launch_gemm_tc_bn(const GemmParams &p, cudaStream_t stream) {

@@ -394,11 +394,11 @@ struct GemmParams {
 size_t gemm_image_bytes(int nb, int C);
 size_t gemm_smem_bytes(int fmt, int nb);
 int launch_gemm(const GemmParams &p, int fmt, void *stream);
-// The tensor-memory GEMM (Q4_0 and Q8_0, nb > 64): its activation image and
+// The tensor-memory GEMM (Q4_0 and Q8_0, nb > 16): its activation image and
 // row factors, and its two launches.
 size_t gemm_tc_image_bytes(int nb, int C);
 int launch_gemm_tc(const GemmParams &p, int fmt, void *stream);
-constexpr int kGemmTcMinNb = 65;  // below it the 64-row mma.sync tile is faster
+constexpr int kGemmTcMinNb = 17;  // up to 16 rows the 16-row mma.sync tile is faster
 
 int launch_gemv_q4_0(const GemvParams &p, const Plan &plan, void *stream);
 int launch_gemv_affine(const GemvParams &p, const Plan &plan, void *stream);

@@ -388,8 +388,8 @@ q4_status q4_argmax_noalloc(const q4_weight *W, const float *x, const float *gam
  * Numerics: weights exact, products accumulated in fp32, each activation
  * carried as one f16 (relative rounding at most 2^-11) after a power-of-two
  * scale: per 32-column block of a row (as the GEMV calls do above four rows)
- * in the mma.sync form that serves every format (Q4_0 and Q8_0 up to 64 rows);
- * per activation row in the tcgen05 form that serves Q4_0 and Q8_0 from 65 rows (there the
+ * in the mma.sync form that serves every format (Q4_0 and Q8_0 up to 16 rows);
+ * per activation row in the tcgen05 form that serves Q4_0 and Q8_0 from 17 rows (there the
  * weights enter the tensor core as f16 hi + lo pairs with an exact sum, and
  * the fp32 accumulator lives in tensor memory).
  * Workspace: q4_gemm_workspace_bytes(nb, k) device bytes (16-byte aligned,

@@ -396,11 +396,11 @@ def test_gemm_validation():
     L = q4.lib()
     W = _cw()
     ws = q4.lib().q4_gemm_workspace_bytes(40, 64)
-    assert ws == 1 * 1 * (4 * 8 * 32 * 16 + 2 * 4 * 64 * 4)       # one 64-row tile, one chunk
+    # from 17 rows, the larger of the two forms' images: one 64-row tile of
+    # one chunk (18432 bytes), or the tensor-memory form's 128 rows x 128 f16
+    # columns plus 128 row factors (33280 bytes)
+    assert ws == max(1 * 1 * (4 * 8 * 32 * 16 + 2 * 4 * 64 * 4), 128 * 128 * 2 + 128 * 4)
     assert L.q4_gemm_workspace_bytes(16, 64) == 4 * 2 * 32 * 16 + 2 * 4 * 16 * 4  # one 16-row tile
-    # from 65 rows, the larger of the two forms' images: two 64-row tiles
-    # (36864 bytes), or the tensor-memory form's 128 rows x 128 f16 columns
-    # plus 128 row factors (33280 bytes)
     assert L.q4_gemm_workspace_bytes(80, 64) == max(2 * 18432, 128 * 128 * 2 + 128 * 4)
     # 256-row column tiles above 128 rows, 512-row above 256
     assert L.q4_gemm_workspace_bytes(200, 128) == max(4 * 18432, 256 * 128 * 2 + 256 * 4)

@@ -90,9 +90,10 @@ def test_attention_copy_wait_gives_up_and_the_next_call_is_unchanged(q4):
     q4.q4_device_check()
 
 
-# the 16-row and the 64-row activation tiles and the tensor-memory form
-# (Q4_0 from 65 rows) at its three column-tile widths (128, 256, 512)
-@pytest.mark.parametrize("fmt,nb", [("q4_0", 9), ("q4_0", 40), ("q4_0", 80), ("q4_0", 200), ("q4_0", 300),
+# the 16-row and the 64-row activation tiles of the mma.sync form, and the
+# tensor-memory form (Q4_0 and Q8_0 from 17 rows) at its three column-tile
+# widths (128, 256, 512)
+@pytest.mark.parametrize("fmt,nb", [("q4_0", 9), ("affine", 40), ("q4_0", 40), ("q4_0", 200), ("q4_0", 300),
                                     ("q8_0", 80)])
 def test_gemm_copy_wait_gives_up_and_the_next_call_is_unchanged(q4, fmt, nb):
     rng = np.random.default_rng(24 + nb)
